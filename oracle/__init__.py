@@ -1,0 +1,125 @@
+"""CPU oracle for the Q4_K x M-row matmul -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg may
+import this package.  The product path (``bit_weight_streaming_q4_gb300``) never does,
+and shares no code with it.  The arithmetic lives in ``q4k_oracle.c`` (plain C, fp32
+dequantisation, double accumulation, OpenMP over output channels); this module only
+compiles it and marshals numpy arrays.
+
+Pins (tests/test_oracle_pins.py) check it against closed forms, hand-packed blocks,
+brute force in exact rational arithmetic, and invariants.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "q4k_oracle.c")
+_LIB = os.path.join(_HERE, "_oracle.so")
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with the host C compiler.  -ffp-contract=off keeps each
+    operation rounded as written."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fPIC",
+                               "-shared", "-std=c11", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        lib.oracle_f16_to_double.restype = ctypes.c_double
+        lib.oracle_f16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_scale_min.restype = None
+        lib.oracle_scale_min.argtypes = [ctypes.c_void_p, ctypes.c_int,
+                                         ctypes.POINTER(ctypes.c_int),
+                                         ctypes.POINTER(ctypes.c_int)]
+        lib.oracle_quant.restype = ctypes.c_int
+        lib.oracle_quant.argtypes = [ctypes.c_void_p, ctypes.c_int]
+        lib.oracle_dequant_block.restype = None
+        lib.oracle_dequant_block.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+        lib.oracle_qmm.restype = ctypes.c_int
+        lib.oracle_qmm.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                   ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                   ctypes.c_void_p, ctypes.c_int]
+        lib.oracle_max_threads.restype = ctypes.c_int
+        lib.oracle_max_threads.argtypes = []
+        _lib = lib
+    return _lib
+
+
+def f16_to_double(bits: int) -> float:
+    return float(_load().oracle_f16_to_double(bits))
+
+
+def scale_min(scales12: bytes | np.ndarray, j: int) -> tuple[int, int]:
+    s = np.ascontiguousarray(np.frombuffer(bytes(scales12), dtype=np.uint8))
+    assert s.size == 12
+    sc, mn = ctypes.c_int(), ctypes.c_int()
+    _load().oracle_scale_min(s.ctypes.data, j, ctypes.byref(sc), ctypes.byref(mn))
+    return sc.value, mn.value
+
+
+def quant(qs128: np.ndarray, i: int) -> int:
+    q = np.ascontiguousarray(qs128, dtype=np.uint8)
+    assert q.size == 128
+    return int(_load().oracle_quant(q.ctypes.data, i))
+
+
+def dequant_block(block: np.ndarray) -> np.ndarray:
+    """One 144-byte super-block -> 256 fp32 weights."""
+    b = np.ascontiguousarray(block, dtype=np.uint8).reshape(144)
+    w = np.empty(256, dtype=np.float32)
+    _load().oracle_dequant_block(b.ctypes.data, w.ctypes.data)
+    return w
+
+
+def dequant_matrix(blocks: np.ndarray) -> np.ndarray:
+    """[N, K/256, 144] blocks -> fp32 W[N, K]."""
+    n, kb, _ = blocks.shape
+    out = np.empty((n, kb * 256), dtype=np.float32)
+    for r in range(n):
+        for b in range(kb):
+            out[r, 256 * b:256 * (b + 1)] = dequant_block(blocks[r, b])
+    return out
+
+
+def qmm(blocks: np.ndarray, x: np.ndarray, nthreads: int = 0) -> tuple[np.ndarray, np.ndarray]:
+    """y[M, N] = x W^T in double and S[M, N] = sum_k |w x|.
+
+    blocks: uint8 [N, K/256, 144] (GGUF order); x: float16 [M, K]."""
+    blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+    assert blocks.ndim == 3 and blocks.shape[2] == 144
+    n, kb = blocks.shape[0], blocks.shape[1]
+    k = kb * 256
+    x = np.ascontiguousarray(x, dtype=np.float16)
+    assert x.ndim == 2 and x.shape[1] == k
+    m = x.shape[0]
+    y = np.empty((m, n), dtype=np.float64)
+    s = np.empty((m, n), dtype=np.float64)
+    rc = _load().oracle_qmm(blocks.ctypes.data, n, k, x.view(np.uint16).ctypes.data, m,
+                            y.ctypes.data, s.ctypes.data, nthreads)
+    if rc != 0:
+        raise RuntimeError("oracle_qmm failed")
+    return y, s
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def tolerance(s_abs: np.ndarray) -> np.ndarray:
+    """Per-element bound for the GPU result: 2e-3 * sum_k |w x| + 1e-6."""
+    return 2e-3 * s_abs + 1e-6

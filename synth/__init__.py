@@ -1,0 +1,158 @@
+"""Seeded synthetic inputs for the Q4_K x M-row weight-streaming matmul.
+
+This package feeds both the CPU oracle and the CUDA path.  It draws random bytes and
+rounds random reals to fp16; it holds none of the method's arithmetic.  The generator
+(a counter-based SplitMix64, see ``synth.c``) makes every block and every activation a
+pure function of ``(seed, tensor_id, index)``, so a test can regenerate any rows of a
+12.7 GB weight stack without holding it in host memory.
+
+Workload shapes follow the decode step described on the page "Running 4 coding agents
+on one RTX 3090: a custom CUDA engine for Qwen3.8-27B" (section "How parallel decoding
+works": every active agent's next token plus two drafts, stacked into 12 rows, multiplied
+against the whole weight set in one pass).  The 27B-shaped matrix list is in ``STACK``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "synth.c")
+_LIB = os.path.join(_HERE, "_synth.so")
+
+BLOCK_BYTES = 144      # one Q4_K super-block
+BLOCK_WEIGHTS = 256    # weights per super-block
+D_SCALE = 1e-3         # d, dmin = fp16(|N(0,1)| * 1e-3)
+
+
+def build(force: bool = False) -> str:
+    """Compile the generator with the host C compiler (OpenMP over blocks)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+                               _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        lib.synth_key.restype = ctypes.c_uint64
+        lib.synth_key.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+        lib.synth_f16_from_double.restype = ctypes.c_uint16
+        lib.synth_f16_from_double.argtypes = [ctypes.c_double]
+        lib.synth_q4k_blocks.restype = None
+        lib.synth_q4k_blocks.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64,
+                                         ctypes.c_uint64, ctypes.c_int64, ctypes.c_double]
+        lib.synth_x_f16.restype = None
+        lib.synth_x_f16.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64,
+                                    ctypes.c_uint64, ctypes.c_int64, ctypes.c_double,
+                                    ctypes.c_double]
+        lib.synth_raw.restype = None
+        lib.synth_raw.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64,
+                                  ctypes.c_uint64]
+        _lib = lib
+    return _lib
+
+
+def f16_bits(v: float) -> int:
+    """fp16 bit pattern of a double, round-to-nearest-even (the generator's rounding)."""
+    return int(_load().synth_f16_from_double(float(v)))
+
+
+def raw(key: int, first: int, n: int) -> np.ndarray:
+    out = np.empty(n, dtype=np.uint64)
+    _load().synth_raw(out.ctypes.data, n, key, first)
+    return out
+
+
+def key(seed: int, tensor_id: int) -> int:
+    return int(_load().synth_key(seed, tensor_id))
+
+
+def q4k_blocks(nblocks: int, seed: int, tensor_id: int, first_block: int = 0,
+               scale_mul: float = D_SCALE, out: np.ndarray | None = None) -> np.ndarray:
+    """Blocks first_block .. first_block+nblocks-1 of a tensor, as uint8 [nblocks, 144]."""
+    if out is None:
+        out = np.empty((nblocks, BLOCK_BYTES), dtype=np.uint8)
+    assert out.dtype == np.uint8 and out.flags.c_contiguous and out.size == nblocks * BLOCK_BYTES
+    _load().synth_q4k_blocks(out.ctypes.data, nblocks, seed, tensor_id, first_block, scale_mul)
+    return out
+
+
+def q4k_matrix(n: int, k: int, seed: int, tensor_id: int, rows: np.ndarray | None = None,
+               scale_mul: float = D_SCALE) -> np.ndarray:
+    """Weight matrix W[n, k] as GGUF-ordered super-blocks, uint8 [n, k/256, 144].
+
+    Row r of the matrix is blocks r*(k/256) .. (r+1)*(k/256)-1 of the tensor.  With
+    ``rows`` given, only those rows are generated (in that order)."""
+    assert k % BLOCK_WEIGHTS == 0
+    kb = k // BLOCK_WEIGHTS
+    if rows is None:
+        out = np.empty((n, kb, BLOCK_BYTES), dtype=np.uint8)
+        q4k_blocks(n * kb, seed, tensor_id, 0, scale_mul, out.reshape(n * kb, BLOCK_BYTES))
+        return out
+    rows = np.asarray(rows, dtype=np.int64)
+    out = np.empty((len(rows), kb, BLOCK_BYTES), dtype=np.uint8)
+    for i, r in enumerate(rows):
+        assert 0 <= r < n
+        q4k_blocks(kb, seed, tensor_id, int(r) * kb, scale_mul, out[i].reshape(kb, BLOCK_BYTES))
+    return out
+
+
+def x_f16(m: int, k: int, seed: int, tensor_id: int, outlier_p: float = 0.0,
+          outlier_mul: float = 20.0) -> np.ndarray:
+    """Activations x[m, k] as fp16 (numpy float16), element index = row * k + col."""
+    out = np.empty((m, k), dtype=np.uint16)
+    _load().synth_x_f16(out.ctypes.data, m * k, seed, tensor_id, 0, outlier_p, outlier_mul)
+    return out.view(np.float16)
+
+
+# ----------------------------------------------------------------------------------------
+# Workload shapes.  A matrix maps K inputs to N outputs; W is stored N rows of K/256 blocks.
+# ----------------------------------------------------------------------------------------
+@dataclass(frozen=True)
+class Matrix:
+    name: str
+    n: int          # outputs
+    k: int          # inputs
+    tensor_id: int  # generator stream of the weights; activations use X_ID_OFFSET + tensor_id
+
+    @property
+    def weight_bytes(self) -> int:
+        return self.n * self.k // BLOCK_WEIGHTS * BLOCK_BYTES
+
+
+X_ID_OFFSET = 1000
+LAYERS = 64
+HIDDEN = 5120
+LAYER_SHAPES = (("qkv", 8192, 5120), ("o", 5120, 6144), ("gate_up", 34816, 5120),
+                ("down", 5120, 17408))
+LM_HEAD = Matrix("lm_head", 151936, 5120, 256)
+
+
+def layer_matrices(layer: int) -> list[Matrix]:
+    return [Matrix(f"L{layer}.{nm}", n, k, layer * 4 + i)
+            for i, (nm, n, k) in enumerate(LAYER_SHAPES)]
+
+
+def stack(layers: int = LAYERS, lm_head: bool = True) -> list[Matrix]:
+    """The 27B-shaped decode stack: per layer qkv, o, gate_up, down; then lm_head."""
+    mats = [m for layer in range(layers) for m in layer_matrices(layer)]
+    if lm_head:
+        mats.append(LM_HEAD)
+    return mats
+
+
+SINGLE_PROJECTION = Matrix("proj4096", 4096, 4096, 0)
+SWEEP_MATRICES = (layer_matrices(0)[2], layer_matrices(0)[3])   # gate_up, down
+SWEEP_M = (1, 2, 4, 8, 12, 16, 32, 64)
