@@ -1,0 +1,323 @@
+// C-ABI layer: argument checking, handle lifetime, device memory, launch, and the
+// graph-recorded decode step.  See include/qmm.h for the contract.
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <new>
+#include <unordered_set>
+#include <vector>
+
+#include "qmm.h"
+#include "qmm_internal.h"
+
+namespace {
+
+constexpr uint64_t kMagic = 0x514D4D5F48414E44ull;  // "QMM_HAND"
+
+std::mutex g_mu;
+std::unordered_set<const void*> g_handles;
+std::unordered_set<const void*> g_steps;
+
+bool live_handle(const qmm_handle h) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    return h && g_handles.count(h) && h->magic == kMagic;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+qmm_status check_device(int* dev_out, int* sms_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QMM_ERR_NO_DEVICE;
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return QMM_ERR_NO_DEVICE;
+    if (major != 10 || minor != 3) return QMM_ERR_NO_DEVICE;  // built for sm_103a only
+    *dev_out = dev;
+    *sms_out = sms;
+    return QMM_OK;
+}
+
+void free_handle(qmm_handle h) {
+    if (!h) return;
+    cudaFree(h->wq);
+    cudaFree(h->ws);
+    cudaFree(h->tickets);
+    if (h->err_host) cudaFreeHost(h->err_host);
+    cudaFree(h->x_stage);
+    cudaFree(h->y_stage);
+    h->magic = 0;
+    delete h;
+}
+
+qmm_status launch_run(qmm_handle h, const void* x, int64_t m, float* y, cudaStream_t s, bool pdl) {
+    const int64_t K = h->d.k, N = h->d.n;
+    for (int64_t r0 = 0; r0 < m; r0 += qmm::b1::kMaxM) {
+        const int64_t mc = (m - r0 < qmm::b1::kMaxM) ? m - r0 : qmm::b1::kMaxM;
+        qmm::B1Params p;
+        p.wq = h->wq;
+        p.x = reinterpret_cast<const __half*>(x) + r0 * K;
+        p.y = y + r0 * N;
+        p.ws = h->ws;
+        p.tickets = h->tickets;
+        p.err = h->err_dev;
+        p.units = h->d.units;
+        p.n = N;
+        p.kb = static_cast<int32_t>(h->d.kb);
+        p.m = static_cast<int32_t>(mc);
+        p.grid = h->d.grid;
+        p.ws_cols = h->ws_cols;
+        if (qmm::b1::launch(p, s, pdl) != cudaSuccess) return QMM_ERR_CUDA;
+    }
+    return QMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void qmm_default_options(qmm_options* opt) {
+    if (!opt) return;
+    opt->m_max = 16;
+    opt->backend = QMM_BACKEND_AUTO;
+    opt->ctas_per_sm = 0;
+    opt->host_io = 0;
+}
+
+const char* qmm_status_str(qmm_status s) {
+    switch (s) {
+        case QMM_OK: return "ok";
+        case QMM_ERR_INVALID_ARG: return "invalid argument";
+        case QMM_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case QMM_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case QMM_ERR_OOM: return "device allocation failed";
+        case QMM_ERR_CUDA: return "CUDA error";
+        case QMM_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+        case QMM_ERR_BAD_HANDLE: return "bad handle";
+        case QMM_ERR_NO_DEVICE: return "no sm_103 device";
+    }
+    return "unknown status";
+}
+
+qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
+                      int32_t blocks_on_device, const qmm_options* opt_in, void* stream) {
+    if (!out || !blocks) return QMM_ERR_INVALID_ARG;
+    *out = nullptr;
+    qmm_options opt;
+    qmm_default_options(&opt);
+    if (opt_in) opt = *opt_in;
+    if (opt.m_max < 1 || opt.ctas_per_sm < 0 || opt.ctas_per_sm > 4 || opt.backend < 0 ||
+        opt.backend > QMM_BACKEND_TCGEN05)
+        return QMM_ERR_INVALID_ARG;
+    if (n <= 0 || k <= 0 || k % 256 != 0) return QMM_ERR_UNSUPPORTED_SHAPE;
+    if (blocks_on_device && !aligned16(blocks)) return QMM_ERR_MISALIGNED;
+    if (opt.backend == QMM_BACKEND_TCGEN05) return QMM_ERR_INVALID_ARG;  // not built yet
+
+    int dev = 0, sms = 0;
+    qmm_status st = check_device(&dev, &sms);
+    if (st != QMM_OK) return st;
+    static std::once_flag cfg_once;
+    static cudaError_t cfg_err = cudaSuccess;
+    std::call_once(cfg_once, [] { cfg_err = qmm::b1::configure(); });
+    if (cfg_err != cudaSuccess) return QMM_ERR_CUDA;
+
+    qmm_handle h = new (std::nothrow) qmm_handle_s();
+    if (!h) return QMM_ERR_OOM;
+    h->magic = kMagic;
+    h->device = dev;
+    h->backend = QMM_BACKEND_MMA_SYNC;
+    h->m_max = opt.m_max;
+    qmm::Decomp& d = h->d;
+    d.n = n;
+    d.k = k;
+    d.kb = k / 256;
+    d.rows = qmm::b1::kRows;
+    d.unit_bytes = qmm::b1::kUnitBytes;
+    d.tiles = (n + d.rows - 1) / d.rows;
+    d.units = d.tiles * d.kb;
+    const int cps = opt.ctas_per_sm ? opt.ctas_per_sm : 1;
+    d.grid = static_cast<int32_t>(d.units < static_cast<int64_t>(sms) * cps ? d.units
+                                                                           : static_cast<int64_t>(sms) * cps);
+    h->ws_cols = static_cast<int32_t>(opt.m_max < qmm::b1::kMaxM ? opt.m_max : qmm::b1::kMaxM);
+    h->wq_bytes = d.units * d.unit_bytes;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* staging = nullptr;
+    auto fail = [&](qmm_status code) {
+        cudaFree(staging);
+        free_handle(h);
+        return code;
+    };
+    if (cudaMalloc(&h->wq, h->wq_bytes) != cudaSuccess) return fail(QMM_ERR_OOM);
+    const size_t ws_bytes = static_cast<size_t>(d.grid) * 2 * d.rows * h->ws_cols * sizeof(float);
+    if (cudaMalloc(&h->ws, ws_bytes) != cudaSuccess) return fail(QMM_ERR_OOM);
+    if (cudaMalloc(&h->tickets, d.tiles * sizeof(int)) != cudaSuccess) return fail(QMM_ERR_OOM);
+    if (cudaMemsetAsync(h->tickets, 0, d.tiles * sizeof(int), s) != cudaSuccess) return fail(QMM_ERR_CUDA);
+    if (cudaHostAlloc(&h->err_host, sizeof(int), cudaHostAllocMapped) != cudaSuccess) return fail(QMM_ERR_OOM);
+    *h->err_host = 0;
+    if (cudaHostGetDevicePointer(&h->err_dev, h->err_host, 0) != cudaSuccess) return fail(QMM_ERR_CUDA);
+    if (opt.host_io) {
+        if (cudaMalloc(&h->x_stage, static_cast<size_t>(opt.m_max) * k * 2) != cudaSuccess) return fail(QMM_ERR_OOM);
+        if (cudaMalloc(&h->y_stage, static_cast<size_t>(opt.m_max) * n * 4) != cudaSuccess) return fail(QMM_ERR_OOM);
+    }
+
+    const size_t src_bytes = static_cast<size_t>(n) * d.kb * 144;
+    const uint8_t* src = static_cast<const uint8_t*>(blocks);
+    if (!blocks_on_device) {
+        if (cudaMalloc(&staging, src_bytes) != cudaSuccess) return fail(QMM_ERR_OOM);
+        if (cudaMemcpyAsync(staging, blocks, src_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return fail(QMM_ERR_CUDA);
+        src = staging;
+    }
+    if (qmm::b1::repack(src, h->wq, d, s) != cudaSuccess) return fail(QMM_ERR_CUDA);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return fail(QMM_ERR_CUDA);
+    cudaFree(staging);
+    staging = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_handles.insert(h);
+    }
+    *out = h;
+    return QMM_OK;
+}
+
+qmm_status qmm_run(qmm_handle h, const void* x, int64_t m, float* y, void* stream) {
+    if (!live_handle(h)) return QMM_ERR_BAD_HANDLE;
+    if (*reinterpret_cast<volatile int*>(h->err_host)) return QMM_ERR_DEVICE_TIMEOUT;
+    if (m < 0) return QMM_ERR_INVALID_ARG;
+    if (m == 0) return QMM_OK;
+    if (m > h->m_max) return QMM_ERR_UNSUPPORTED_SHAPE;
+    if (!x || !y) return QMM_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y)) return QMM_ERR_MISALIGNED;
+    return launch_run(h, x, m, y, reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+qmm_status qmm_run_host(qmm_handle h, const void* x_host, int64_t m, float* y_host, void* stream) {
+    if (!live_handle(h)) return QMM_ERR_BAD_HANDLE;
+    if (!h->x_stage) return QMM_ERR_INVALID_ARG;
+    if (m < 0) return QMM_ERR_INVALID_ARG;
+    if (m == 0) return QMM_OK;
+    if (m > h->m_max) return QMM_ERR_UNSUPPORTED_SHAPE;
+    if (!x_host || !y_host) return QMM_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(h->x_stage, x_host, static_cast<size_t>(m) * h->d.k * 2,
+                        cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return QMM_ERR_CUDA;
+    qmm_status st = qmm_run(h, h->x_stage, m, h->y_stage, stream);
+    if (st != QMM_OK) return st;
+    if (cudaMemcpyAsync(y_host, h->y_stage, static_cast<size_t>(m) * h->d.n * 4,
+                        cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return QMM_ERR_CUDA;
+    return QMM_OK;
+}
+
+qmm_status qmm_get_error(qmm_handle h) {
+    if (!live_handle(h)) return QMM_ERR_BAD_HANDLE;
+    if (cudaDeviceSynchronize() != cudaSuccess) return QMM_ERR_CUDA;
+    return *reinterpret_cast<volatile int*>(h->err_host) ? QMM_ERR_DEVICE_TIMEOUT : QMM_OK;
+}
+
+qmm_status qmm_get_info(qmm_handle h, qmm_info* info) {
+    if (!live_handle(h)) return QMM_ERR_BAD_HANDLE;
+    if (!info) return QMM_ERR_INVALID_ARG;
+    info->n = h->d.n;
+    info->k = h->d.k;
+    info->m_max = h->m_max;
+    info->backend = h->backend;
+    info->grid = h->d.grid;
+    info->units = h->d.units;
+    info->rows_per_unit = h->d.rows;
+    info->weight_bytes = h->d.n * h->d.kb * 144;
+    info->packed_bytes = h->wq_bytes;
+    info->workspace_bytes = static_cast<int64_t>(h->d.grid) * 2 * h->d.rows * h->ws_cols * 4 +
+                            h->d.tiles * 4;
+    return QMM_OK;
+}
+
+qmm_status qmm_destroy(qmm_handle h) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!h || !g_handles.count(h)) return QMM_ERR_BAD_HANDLE;
+        g_handles.erase(h);
+    }
+    cudaDeviceSynchronize();
+    free_handle(h);
+    return QMM_OK;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------------- decode step
+struct qmm_step_s {
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+};
+
+extern "C" {
+
+qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handles,
+                           const void* const* xs, float* const* ys, int64_t m, void* stream) {
+    if (!out || count <= 0 || !handles || !xs || !ys || m < 1) return QMM_ERR_INVALID_ARG;
+    *out = nullptr;
+    for (int32_t i = 0; i < count; ++i) {
+        if (!live_handle(handles[i])) return QMM_ERR_BAD_HANDLE;
+        if (!xs[i] || !ys[i]) return QMM_ERR_INVALID_ARG;
+        if (!aligned16(xs[i]) || !aligned16(ys[i])) return QMM_ERR_MISALIGNED;
+        if (m > handles[i]->m_max) return QMM_ERR_UNSUPPORTED_SHAPE;
+    }
+    cudaStream_t cap = nullptr;
+    if (cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking) != cudaSuccess) return QMM_ERR_CUDA;
+    qmm_step st = new (std::nothrow) qmm_step_s();
+    if (!st) {
+        cudaStreamDestroy(cap);
+        return QMM_ERR_OOM;
+    }
+    qmm_status rc = QMM_OK;
+    if (cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) rc = QMM_ERR_CUDA;
+    for (int32_t i = 0; rc == QMM_OK && i < count; ++i)
+        rc = launch_run(handles[i], xs[i], m, ys[i], cap, /*pdl=*/i > 0);
+    cudaGraph_t g = nullptr;
+    cudaError_t ec = cudaStreamEndCapture(cap, &g);
+    if (rc == QMM_OK && ec != cudaSuccess) rc = QMM_ERR_CUDA;
+    if (rc == QMM_OK && cudaGraphInstantiate(&st->exec, g, 0) != cudaSuccess) rc = QMM_ERR_CUDA;
+    st->graph = g;
+    cudaStreamDestroy(cap);
+    if (rc != QMM_OK) {
+        if (st->exec) cudaGraphExecDestroy(st->exec);
+        if (st->graph) cudaGraphDestroy(st->graph);
+        delete st;
+        return rc;
+    }
+    (void)stream;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_steps.insert(st);
+    }
+    *out = st;
+    return QMM_OK;
+}
+
+qmm_status qmm_step_launch(qmm_step s, void* stream) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!s || !g_steps.count(s)) return QMM_ERR_BAD_HANDLE;
+    }
+    return cudaGraphLaunch(s->exec, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? QMM_OK
+                                                                                         : QMM_ERR_CUDA;
+}
+
+qmm_status qmm_step_destroy(qmm_step s) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!s || !g_steps.count(s)) return QMM_ERR_BAD_HANDLE;
+        g_steps.erase(s);
+    }
+    cudaDeviceSynchronize();
+    cudaGraphExecDestroy(s->exec);
+    cudaGraphDestroy(s->graph);
+    delete s;
+    return QMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,74 @@
+// Internal declarations shared by the C-ABI layer and the kernel translation units.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qmm.h"
+
+namespace qmm {
+
+// Work decomposition shared by the backends: the weight matrix is cut into units of
+// (rows_per_unit output rows) x (one 256-wide super-block column).  Units are numbered
+// row-tile-major, u = tile * KB + kb, and stored contiguously in that order, so a run of
+// consecutive units is one contiguous byte range.  Each persistent CTA c takes the units
+// [c*U/P, (c+1)*U/P): a fixed piece that depends only on (N, K, P), never on M.
+struct Decomp {
+    int64_t n = 0, k = 0, kb = 0;  // kb = K / 256
+    int64_t tiles = 0;             // ceil(N / rows_per_unit)
+    int64_t units = 0;             // tiles * kb
+    int32_t rows = 0;              // rows per unit
+    int32_t unit_bytes = 0;        // rows * 144
+    int32_t grid = 0;              // P, persistent CTAs (<= units)
+};
+
+// Piece containing unit u (host mirror of the device formula).
+inline int64_t piece_of(int64_t u, int64_t units, int64_t grid) {
+    return ((u + 1) * grid + units - 1) / units - 1;
+}
+
+struct B1Params {
+    const uint8_t* wq;   // repacked units
+    const __half* x;     // [m, k] fp16
+    float* y;            // [m, n] fp32
+    float* ws;           // split-K partial slots [grid][2][rows][ws_cols]
+    int* tickets;        // [tiles]
+    int* err;            // sticky error word (mapped host memory)
+    int64_t units;
+    int64_t n;
+    int32_t kb;
+    int32_t m;           // rows of this launch, 1..16
+    int32_t grid;
+    int32_t ws_cols;
+};
+
+// Backend 1: warp-level mma.sync streaming kernel.
+namespace b1 {
+constexpr int kRows = 32;
+constexpr int kUnitBytes = kRows * 144;
+constexpr int kMaxM = 16;  // rows per launch
+int smem_bytes();
+cudaError_t repack(const uint8_t* src_dev, uint8_t* dst_dev, const Decomp& d, cudaStream_t s);
+cudaError_t launch(const B1Params& p, cudaStream_t s, bool pdl);
+cudaError_t configure();  // one-time function attributes
+}  // namespace b1
+
+}  // namespace qmm
+
+struct qmm_handle_s {
+    uint64_t magic;
+    int device;
+    int32_t backend;
+    int64_t m_max;
+    qmm::Decomp d;
+    uint8_t* wq = nullptr;        // repacked weights
+    int64_t wq_bytes = 0;
+    float* ws = nullptr;          // split-K partials
+    int32_t ws_cols = 0;
+    int* tickets = nullptr;
+    int* err_host = nullptr;      // mapped pinned word: host view
+    int* err_dev = nullptr;       // device view of the same word
+    void* x_stage = nullptr;      // host_io staging
+    float* y_stage = nullptr;
+};

@@ -1,0 +1,147 @@
+/*
+ * qmm -- Q4_K x M-row weight-streaming matmul for one GB300 (sm_103a).
+ *
+ * What it computes.  y[m, n] = sum_k w[n, k] * x[m, k] for M stacked activation rows
+ * x[M, K] (fp16) against an N x K weight matrix stored as Q4_K super-blocks, with fp32
+ * output y[M, N].  Each super-block covers 256 consecutive weights of one output row:
+ *   bytes 0-1 d (fp16), 2-3 dmin (fp16), 4-15 six-bit (scale, min) pairs of its 8
+ *   sub-blocks of 32 (GGUF Q4_K packing), 16-143 four-bit quants q,
+ *   w = d * sc_j * q - dmin * m_j.
+ * Source: page "Running 4 coding agents on one RTX 3090: a custom CUDA engine for
+ * Qwen3.8-27B", section "How parallel decoding works" -- every active stream's next
+ * token and its draft tokens are stacked into one row batch (4 agents x 3 = 12 rows),
+ * the weights are streamed from memory once per step, and every weight is multiplied
+ * against all rows while it is on chip.  The model file it runs is "Q4_K_M" (first
+ * paragraph), i.e. GGUF Q4_K super-blocks.
+ *
+ * Guarantees.
+ *  - Every weight byte is read from HBM once per qmm_run, whatever M is.
+ *  - Batch invariance: for one handle, row m of y is bit-identical whether x holds that
+ *    row alone or together with other rows, at any position (same page, section on
+ *    keeping agents fast: a prompt chunked in with other agents' rows gives bit-identical
+ *    results to running it alone).  The reduction order depends on (N, K) and the
+ *    handle's launch shape only, never on M or on the other rows.
+ *  - Accuracy: |y - y_exact| <= 2e-3 * sum_k |w x| + 1e-6 per element for weights whose
+ *    dequantised values fit fp16 (|d * 63 * 15| < 65504).  Outputs are not byte-equal to
+ *    other implementations (same page, section "Accuracy": arithmetic order differs).
+ *
+ * Conventions.  All functions return a qmm_status and never abort the process.  Device
+ * pointers are plain CUDA device addresses (e.g. torch tensors' data_ptr()); `stream` is a
+ * cudaStream_t passed as void* (NULL = legacy default stream).  Every call is ordered on
+ * `stream`; qmm_run and qmm_step_launch perform no allocation and no host synchronisation.
+ * One handle must not have two runs in flight at once (they share the handle's split-K
+ * workspace); runs on one stream are serialised automatically.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct qmm_handle_s* qmm_handle;
+
+typedef enum {
+    QMM_OK = 0,
+    QMM_ERR_INVALID_ARG = 1,        /* null pointer, negative size, bad option value */
+    QMM_ERR_UNSUPPORTED_SHAPE = 2,  /* K % 256 != 0, N or K <= 0, M > m_max */
+    QMM_ERR_MISALIGNED = 3,         /* x, y or the weights not 16-byte aligned */
+    QMM_ERR_OOM = 4,                /* a device allocation in qmm_create/qmm_step_create failed */
+    QMM_ERR_CUDA = 5,               /* a CUDA runtime call or a launch failed */
+    QMM_ERR_DEVICE_TIMEOUT = 6,     /* a kernel's bounded wait gave up (sticky, see qmm_get_error) */
+    QMM_ERR_BAD_HANDLE = 7,         /* NULL, destroyed or never-created handle */
+    QMM_ERR_NO_DEVICE = 8           /* the current device is not an sm_103 GPU */
+} qmm_status;
+
+enum {
+    QMM_BACKEND_AUTO = 0,     /* chosen from m_max only (never from a run's M) */
+    QMM_BACKEND_MMA_SYNC = 1, /* warp-level mma.sync m16n8k16, M <= 16 per pass */
+    QMM_BACKEND_TCGEN05 = 2   /* tcgen05.mma with TMEM accumulators */
+};
+
+typedef struct {
+    int32_t m_max;        /* largest M any run will pass; >= 1 */
+    int32_t backend;      /* QMM_BACKEND_*; fixed for the handle's lifetime */
+    int32_t ctas_per_sm;  /* 0 = default; persistent CTAs per SM (part of the reduction order) */
+    int32_t host_io;      /* nonzero: also allocate staging buffers for qmm_run_host */
+} qmm_options;
+
+typedef struct {
+    int64_t n, k, m_max;
+    int32_t backend;          /* the backend actually used */
+    int32_t grid;             /* persistent CTAs per run */
+    int64_t units;            /* work units (row tile x super-block column) */
+    int64_t rows_per_unit;
+    int64_t weight_bytes;     /* N*K/256*144: bytes streamed from HBM per run */
+    int64_t packed_bytes;     /* bytes of the repacked on-device copy (N padded to a tile) */
+    int64_t workspace_bytes;  /* split-K partials + tile tickets */
+} qmm_info;
+
+/* Fill `opt` with defaults: m_max 16, backend auto, ctas_per_sm 0, host_io 0. */
+void qmm_default_options(qmm_options* opt);
+
+/*
+ * Create a handle for an N x K Q4_K weight matrix.
+ *  blocks: N rows of K/256 super-blocks, 144 bytes each, row-major (GGUF order); on the
+ *          device if blocks_on_device != 0 (16-byte aligned), else in host memory.  The
+ *          handle copies and repacks them into its own device memory; the caller may free
+ *          `blocks` once the call returns.
+ *  opt:    NULL for defaults.
+ *  stream: the repack is ordered on it; qmm_create synchronises it before returning.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, OOM, CUDA, NO_DEVICE.
+ */
+qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
+                      int32_t blocks_on_device, const qmm_options* opt, void* stream);
+
+/*
+ * y[M, N] (fp32, device, row-major, 16-byte aligned) = x[M, K] (fp16, device, row-major,
+ * 16-byte aligned) times W^T.  M = 0 is a no-op returning QMM_OK.  1 <= M <= m_max.
+ * Asynchronous: errors found on the device (a bounded wait timing out) are reported by a
+ * later qmm_run or by qmm_get_error.
+ * Errors: BAD_HANDLE, INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA, DEVICE_TIMEOUT.
+ */
+qmm_status qmm_run(qmm_handle h, const void* x, int64_t m, float* y, void* stream);
+
+/*
+ * Same as qmm_run with x and y in host memory (pinned memory gives asynchronous
+ * copies): copies x to the handle's staging buffer, runs, copies y back, all on `stream`.
+ * The caller must synchronise `stream` before reading y.  Needs opt.host_io at create.
+ */
+qmm_status qmm_run_host(qmm_handle h, const void* x_host, int64_t m, float* y_host,
+                        void* stream);
+
+/* Sticky device error word of the handle (synchronises the device to read it). */
+qmm_status qmm_get_error(qmm_handle h);
+
+/* Shape and sizing facts of a handle. */
+qmm_status qmm_get_info(qmm_handle h, qmm_info* info);
+
+/* Free the handle and its device memory (synchronises the device first).  Destroying a
+ * handle twice, or using it afterwards, returns BAD_HANDLE. */
+qmm_status qmm_destroy(qmm_handle h);
+
+/* Static text for a status code. */
+const char* qmm_status_str(qmm_status s);
+
+/*
+ * A decode step: `count` runs (handle i: x_i -> y_i, all with the same M) recorded once
+ * into a CUDA graph, consecutive runs linked by programmatic dependent launch so that each
+ * kernel starts streaming its weights while the previous one drains.  Each run waits for
+ * the previous one to finish before it reads its x, as a layer waits for the one before.
+ *  qmm_step_create: records and instantiates the graph on `stream` (synchronous).
+ *  qmm_step_launch: replays it on `stream` (asynchronous, no allocation).
+ * The x_i/y_i pointers are baked into the graph; the handles must outlive the step.
+ */
+typedef struct qmm_step_s* qmm_step;
+qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handles,
+                           const void* const* xs, float* const* ys, int64_t m, void* stream);
+qmm_status qmm_step_launch(qmm_step s, void* stream);
+qmm_status qmm_step_destroy(qmm_step s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMM_H */

@@ -1,0 +1,50 @@
+"""Helpers for the GPU tests: device buffers through torch, runs through the C ABI,
+and the element-wise tolerance check against the oracle."""
+from __future__ import annotations
+
+import numpy as np
+
+TOL_REL = 2e-3
+TOL_ABS = 1e-6
+
+
+def torch_cuda():
+    import torch
+    assert torch.cuda.is_available(), "GPU test run without a GPU"
+    return torch
+
+
+def to_device_blocks(blocks: np.ndarray):
+    torch = torch_cuda()
+    return torch.from_numpy(np.ascontiguousarray(blocks).reshape(-1)).cuda()
+
+
+def make(blocks: np.ndarray, m_max: int = 16, device_blocks: bool = True, **kw):
+    from bit_weight_streaming_q4_gb300 import Qmm
+    n, kb, _ = blocks.shape
+    src = to_device_blocks(blocks) if device_blocks else np.ascontiguousarray(blocks)
+    return Qmm(src, n, kb * 256, m_max=m_max, **kw)
+
+
+def run(q, x: np.ndarray, m: int | None = None) -> np.ndarray:
+    torch = torch_cuda()
+    m = x.shape[0] if m is None else m
+    xd = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).cuda().view(torch.float16)
+    yd = torch.full((max(m, 1), q.n), float("nan"), dtype=torch.float32, device="cuda")
+    q.run(xd, yd, m)
+    torch.cuda.synchronize()
+    return yd.cpu().numpy()[:m]
+
+
+def assert_parity(y: np.ndarray, y_ref: np.ndarray, s_ref: np.ndarray, what: str = ""):
+    """|y - y_ref| <= 2e-3 * sum_k |w x| + 1e-6 for every element."""
+    assert y.shape == y_ref.shape, (y.shape, y_ref.shape)
+    assert np.all(np.isfinite(y)), f"{what}: non-finite output"
+    err = np.abs(y.astype(np.float64) - y_ref)
+    bound = TOL_REL * s_ref + TOL_ABS
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err / bound), err.shape)
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} elements out of tolerance; "
+                             f"worst at {i}: got {y[i]!r}, want {y_ref[i]!r}, bound {bound[i]!r}")
+    return float((err / bound).max()) if err.size else 0.0

@@ -1,0 +1,106 @@
+"""The C ABI without a GPU: the library loads, exports every function the header
+declares, and rejects bad arguments before touching the device.  Also the host-side
+work decomposition (pieces of units per CTA)."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+from bit_weight_streaming_q4_gb300 import build as qbuild
+from bit_weight_streaming_q4_gb300 import qmm as Q
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qbuild.build()
+    return Q.load()
+
+
+def test_header_declares_expected_api():
+    names = Q.header_functions()
+    assert names == sorted(["qmm_default_options", "qmm_create", "qmm_run", "qmm_run_host",
+                            "qmm_get_error", "qmm_get_info", "qmm_destroy", "qmm_status_str",
+                            "qmm_step_create", "qmm_step_launch", "qmm_step_destroy"])
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", Q.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in Q.header_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        s = lib.qmm_status_str(code)
+        assert s and s != b"unknown status"
+    assert lib.qmm_status_str(99) == b"unknown status"
+
+
+def test_default_options(lib):
+    o = Q.Options()
+    lib.qmm_default_options(ctypes.byref(o))
+    assert (o.m_max, o.backend, o.ctas_per_sm, o.host_io) == (16, 0, 0, 0)
+
+
+def test_argument_errors_need_no_device(lib):
+    h = ctypes.c_void_p()
+    buf = (ctypes.c_uint8 * 144)()
+    o = Q.default_options()
+    assert lib.qmm_create(None, buf, 1, 256, 0, ctypes.byref(o), None) == 1
+    assert lib.qmm_create(ctypes.byref(h), None, 1, 256, 0, ctypes.byref(o), None) == 1
+    assert lib.qmm_create(ctypes.byref(h), buf, 1, 300, 0, ctypes.byref(o), None) == 2
+    assert lib.qmm_create(ctypes.byref(h), buf, 0, 256, 0, ctypes.byref(o), None) == 2
+    assert lib.qmm_create(ctypes.byref(h), buf, 1, -256, 0, ctypes.byref(o), None) == 2
+    bad = Q.default_options(m_max=0)
+    assert lib.qmm_create(ctypes.byref(h), buf, 1, 256, 0, ctypes.byref(bad), None) == 1
+    misaligned = ctypes.addressof(buf) | 1
+    assert lib.qmm_create(ctypes.byref(h), misaligned, 1, 256, 1, ctypes.byref(o), None) == 3
+    # no handle exists: every handle call reports BAD_HANDLE
+    assert lib.qmm_run(None, buf, 1, buf, None) == 7
+    assert lib.qmm_run(ctypes.c_void_p(0x1000), buf, 1, buf, None) == 7
+    assert lib.qmm_destroy(ctypes.c_void_p(0x1000)) == 7
+    assert lib.qmm_get_error(None) == 7
+    assert lib.qmm_step_launch(None, None) == 7
+    assert lib.qmm_step_destroy(None) == 7
+
+
+def test_no_device_is_reported(lib):
+    """Without an sm_103 GPU qmm_create reports NO_DEVICE instead of crashing."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p()
+    buf = (ctypes.c_uint8 * 144)()
+    o = Q.default_options()
+    assert lib.qmm_create(ctypes.byref(h), buf, 1, 256, 0, ctypes.byref(o), None) == 8
+
+
+def _piece_of(u, units, grid):
+    return ((u + 1) * grid + units - 1) // units - 1
+
+
+@pytest.mark.parametrize("units,grid", [(10, 3), (2048, 152), (1920, 152), (189920, 152),
+                                        (7, 7), (152, 152), (3, 1), (1000003, 304)])
+def test_pieces_partition_units(units, grid):
+    bounds = [c * units // grid for c in range(grid + 1)]
+    assert bounds[0] == 0 and bounds[-1] == units
+    sizes = [b - a for a, b in zip(bounds, bounds[1:])]
+    assert min(sizes) >= 1 and max(sizes) - min(sizes) <= 1
+    probe = sorted({0, units - 1, units // 2, *bounds[1:-1], *(b - 1 for b in bounds[1:-1])})
+    for u in probe:
+        c = _piece_of(u, units, grid)
+        assert bounds[c] <= u < bounds[c + 1], (u, c)
+
+
+def test_library_not_built_raises(tmp_path):
+    saved = Q._lib
+    try:
+        Q._lib = None
+        with pytest.raises(RuntimeError, match="not built"):
+            Q.load(str(tmp_path / "missing.so"))
+    finally:
+        Q._lib = saved

@@ -1,0 +1,50 @@
+"""Batch invariance: a row's result is bit-identical alone or batched with other rows, at
+any position in the batch (page "Running 4 coding agents on one RTX 3090", section on
+keeping real agents fast: a prompt chunked in with other agents' rows gives bit-identical
+results to running it alone).  Also run-to-run determinism."""
+import numpy as np
+import pytest
+
+import synth
+from gpu_util import make, run
+
+pytestmark = pytest.mark.gpu
+
+
+def bits(a):
+    return np.ascontiguousarray(a).view(np.uint32)
+
+
+@pytest.mark.parametrize("mat", list(synth.SWEEP_MATRICES) + [synth.Matrix("small", 200, 1280, 77)],
+                         ids=lambda m: m.name)
+def test_sub_batches_bitwise(mat):
+    blocks = synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id)
+    x = synth.x_f16(64, mat.k, seed=0, tensor_id=synth.X_ID_OFFSET + mat.tensor_id)
+    q = make(blocks, m_max=64)
+    full = bits(run(q, x))
+    # every M of the sweep equals the prefix of the 64-row batch
+    for m in synth.SWEEP_M:
+        assert np.array_equal(bits(run(q, x[:m])), full[:m]), m
+    # 12 = 4 + 8, 12 x 1, and 64 = 8 x 8 sub-batches
+    for parts in ([4, 8], [1] * 12, [8] * 8, [3, 5, 7, 1, 16, 32]):
+        r0 = 0
+        for p in parts:
+            assert np.array_equal(bits(run(q, x[r0:r0 + p])), full[r0:r0 + p]), (parts, r0)
+            r0 += p
+    # rows at other positions in the batch
+    perm = np.random.default_rng(0).permutation(64)
+    assert np.array_equal(bits(run(q, x[perm])), full[perm])
+    # the same row surrounded by different neighbours
+    x2 = synth.x_f16(16, mat.k, seed=9, tensor_id=9)
+    x2[5] = x[0]
+    assert np.array_equal(bits(run(q, x2))[5], full[0])
+
+
+def test_repeat_determinism():
+    mat = synth.SWEEP_MATRICES[1]
+    blocks = synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id)
+    x = synth.x_f16(12, mat.k, seed=0, tensor_id=1003)
+    q = make(blocks, m_max=12)
+    ref = bits(run(q, x))
+    for _ in range(100):
+        assert np.array_equal(bits(run(q, x)), ref)
