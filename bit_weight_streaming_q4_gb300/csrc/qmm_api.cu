@@ -51,24 +51,49 @@ void free_handle(qmm_handle h) {
     delete h;
 }
 
+int32_t per_launch(const qmm_handle h) {
+    return h->backend == QMM_BACKEND_TCGEN05 ? qmm::b2::kMaxM : qmm::b1::kMaxM;
+}
+
 qmm_status launch_run(qmm_handle h, const void* x, int64_t m, float* y, cudaStream_t s, bool pdl) {
     const int64_t K = h->d.k, N = h->d.n;
-    for (int64_t r0 = 0; r0 < m; r0 += qmm::b1::kMaxM) {
-        const int64_t mc = (m - r0 < qmm::b1::kMaxM) ? m - r0 : qmm::b1::kMaxM;
-        qmm::B1Params p;
-        p.wq = h->wq;
-        p.x = reinterpret_cast<const __half*>(x) + r0 * K;
-        p.y = y + r0 * N;
-        p.ws = h->ws;
-        p.tickets = h->tickets;
-        p.err = h->err_dev;
-        p.units = h->d.units;
-        p.n = N;
-        p.kb = static_cast<int32_t>(h->d.kb);
-        p.m = static_cast<int32_t>(mc);
-        p.grid = h->d.grid;
-        p.ws_cols = h->ws_cols;
-        if (qmm::b1::launch(p, s, pdl) != cudaSuccess) return QMM_ERR_CUDA;
+    const int64_t step = per_launch(h);
+    for (int64_t r0 = 0; r0 < m; r0 += step) {
+        const int64_t mc = (m - r0 < step) ? m - r0 : step;
+        const __half* xc = reinterpret_cast<const __half*>(x) + r0 * K;
+        float* yc = y + r0 * N;
+        cudaError_t e;
+        if (h->backend == QMM_BACKEND_TCGEN05) {
+            qmm::B2Params p;
+            p.wq = h->wq;
+            p.y = yc;
+            p.ws = h->ws;
+            p.tickets = h->tickets;
+            p.err = h->err_dev;
+            p.units = h->d.units;
+            p.n = N;
+            p.kb = static_cast<int32_t>(h->d.kb);
+            p.m = static_cast<int32_t>(mc);
+            p.grid = h->d.grid;
+            p.ws_cols = h->ws_cols;
+            e = qmm::b2::launch(xc, K, p, s, pdl);
+        } else {
+            qmm::B1Params p;
+            p.wq = h->wq;
+            p.x = xc;
+            p.y = yc;
+            p.ws = h->ws;
+            p.tickets = h->tickets;
+            p.err = h->err_dev;
+            p.units = h->d.units;
+            p.n = N;
+            p.kb = static_cast<int32_t>(h->d.kb);
+            p.m = static_cast<int32_t>(mc);
+            p.grid = h->d.grid;
+            p.ws_cols = h->ws_cols;
+            e = qmm::b1::launch(p, s, pdl);
+        }
+        if (e != cudaSuccess) return QMM_ERR_CUDA;
     }
     return QMM_OK;
 }
@@ -112,34 +137,38 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
         return QMM_ERR_INVALID_ARG;
     if (n <= 0 || k <= 0 || k % 256 != 0) return QMM_ERR_UNSUPPORTED_SHAPE;
     if (blocks_on_device && !aligned16(blocks)) return QMM_ERR_MISALIGNED;
-    if (opt.backend == QMM_BACKEND_TCGEN05) return QMM_ERR_INVALID_ARG;  // not built yet
 
     int dev = 0, sms = 0;
     qmm_status st = check_device(&dev, &sms);
     if (st != QMM_OK) return st;
     static std::once_flag cfg_once;
     static cudaError_t cfg_err = cudaSuccess;
-    std::call_once(cfg_once, [] { cfg_err = qmm::b1::configure(); });
+    std::call_once(cfg_once, [] {
+        cfg_err = qmm::b1::configure();
+        if (cfg_err == cudaSuccess) cfg_err = qmm::b2::configure();
+    });
     if (cfg_err != cudaSuccess) return QMM_ERR_CUDA;
 
     qmm_handle h = new (std::nothrow) qmm_handle_s();
     if (!h) return QMM_ERR_OOM;
     h->magic = kMagic;
     h->device = dev;
-    h->backend = QMM_BACKEND_MMA_SYNC;
+    h->backend = opt.backend == QMM_BACKEND_MMA_SYNC ? QMM_BACKEND_MMA_SYNC : QMM_BACKEND_TCGEN05;
+    const bool tc = h->backend == QMM_BACKEND_TCGEN05;
     h->m_max = opt.m_max;
     qmm::Decomp& d = h->d;
     d.n = n;
     d.k = k;
     d.kb = k / 256;
-    d.rows = qmm::b1::kRows;
-    d.unit_bytes = qmm::b1::kUnitBytes;
+    d.rows = tc ? qmm::b2::kRows : qmm::b1::kRows;
+    d.unit_bytes = tc ? qmm::b2::kUnitBytes : qmm::b1::kUnitBytes;
     d.tiles = (n + d.rows - 1) / d.rows;
     d.units = d.tiles * d.kb;
     const int cps = opt.ctas_per_sm ? opt.ctas_per_sm : 1;
     d.grid = static_cast<int32_t>(d.units < static_cast<int64_t>(sms) * cps ? d.units
                                                                            : static_cast<int64_t>(sms) * cps);
-    h->ws_cols = static_cast<int32_t>(opt.m_max < qmm::b1::kMaxM ? opt.m_max : qmm::b1::kMaxM);
+    const int32_t cols_cap = tc ? qmm::b2::kMaxM : qmm::b1::kMaxM;
+    h->ws_cols = opt.m_max < cols_cap ? opt.m_max : cols_cap;
     h->wq_bytes = d.units * d.unit_bytes;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -170,7 +199,8 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
             return fail(QMM_ERR_CUDA);
         src = staging;
     }
-    if (qmm::b1::repack(src, h->wq, d, s) != cudaSuccess) return fail(QMM_ERR_CUDA);
+    const cudaError_t re = tc ? qmm::b2::repack(src, h->wq, d, s) : qmm::b1::repack(src, h->wq, d, s);
+    if (re != cudaSuccess) return fail(QMM_ERR_CUDA);
     if (cudaStreamSynchronize(s) != cudaSuccess) return fail(QMM_ERR_CUDA);
     cudaFree(staging);
     staging = nullptr;
@@ -232,6 +262,8 @@ qmm_status qmm_get_info(qmm_handle h, qmm_info* info) {
     info->packed_bytes = h->wq_bytes;
     info->workspace_bytes = static_cast<int64_t>(h->d.grid) * 2 * h->d.rows * h->ws_cols * 4 +
                             h->d.tiles * 4;
+    info->m_per_launch = per_launch(h);
+    info->reserved = 0;
     return QMM_OK;
 }
 

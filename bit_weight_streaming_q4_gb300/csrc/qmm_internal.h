@@ -43,6 +43,30 @@ struct B1Params {
     int32_t ws_cols;
 };
 
+struct B2Params {
+    const uint8_t* wq;   // repacked units (128 rows x 256 weights each)
+    float* y;            // [m, n] fp32
+    float* ws;           // split-K partial slots [grid][2][ws_cols][128]
+    int* tickets;        // [tiles]
+    int* err;            // sticky error word (mapped host memory)
+    int64_t units;
+    int64_t n;
+    int32_t kb;
+    int32_t m;           // rows of this launch, 1..128
+    int32_t grid;
+    int32_t ws_cols;
+};
+
+// Backend 2: tcgen05 streaming kernel (weights in tensor memory, x by TMA).
+namespace b2 {
+constexpr int kRows = 128;
+constexpr int kUnitBytes = kRows * 144;
+constexpr int kMaxM = 64;   // rows per launch
+cudaError_t repack(const uint8_t* src_dev, uint8_t* dst_dev, const Decomp& d, cudaStream_t s);
+cudaError_t launch(const void* x, int64_t k, const B2Params& p, cudaStream_t s, bool pdl);
+cudaError_t configure();
+}  // namespace b2
+
 // Backend 1: warp-level mma.sync streaming kernel.
 namespace b1 {
 constexpr int kRows = 32;

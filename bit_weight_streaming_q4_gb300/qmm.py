@@ -38,7 +38,8 @@ class Info(ctypes.Structure):
                 ("backend", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("units", ctypes.c_int64), ("rows_per_unit", ctypes.c_int64),
                 ("weight_bytes", ctypes.c_int64), ("packed_bytes", ctypes.c_int64),
-                ("workspace_bytes", ctypes.c_int64)]
+                ("workspace_bytes", ctypes.c_int64), ("m_per_launch", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 _lib = None

@@ -77,6 +77,9 @@ typedef struct {
     int64_t weight_bytes;     /* N*K/256*144: bytes streamed from HBM per run */
     int64_t packed_bytes;     /* bytes of the repacked on-device copy (N padded to a tile) */
     int64_t workspace_bytes;  /* split-K partials + tile tickets */
+    int32_t m_per_launch;     /* rows one kernel launch handles; a run of M rows makes
+                                 ceil(M / m_per_launch) launches */
+    int32_t reserved;
 } qmm_info;
 
 /* Fill `opt` with defaults: m_max 16, backend auto, ctas_per_sm 0, host_io 0. */

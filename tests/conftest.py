@@ -22,3 +22,9 @@ def _build_host_libs():
     import synth
     synth.build()
     oracle.build()
+
+
+@pytest.fixture(params=[1, 2], ids=["mma_sync", "tcgen05"])
+def backend(request):
+    """Both kernel backends run every GPU parity and invariance test."""
+    return request.param

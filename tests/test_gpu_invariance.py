@@ -17,10 +17,10 @@ def bits(a):
 
 @pytest.mark.parametrize("mat", list(synth.SWEEP_MATRICES) + [synth.Matrix("small", 200, 1280, 77)],
                          ids=lambda m: m.name)
-def test_sub_batches_bitwise(mat):
+def test_sub_batches_bitwise(mat, backend):
     blocks = synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id)
     x = synth.x_f16(64, mat.k, seed=0, tensor_id=synth.X_ID_OFFSET + mat.tensor_id)
-    q = make(blocks, m_max=64)
+    q = make(blocks, m_max=64, backend=backend)
     full = bits(run(q, x))
     # every M of the sweep equals the prefix of the 64-row batch
     for m in synth.SWEEP_M:
@@ -40,11 +40,11 @@ def test_sub_batches_bitwise(mat):
     assert np.array_equal(bits(run(q, x2))[5], full[0])
 
 
-def test_repeat_determinism():
+def test_repeat_determinism(backend):
     mat = synth.SWEEP_MATRICES[1]
     blocks = synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id)
     x = synth.x_f16(12, mat.k, seed=0, tensor_id=1003)
-    q = make(blocks, m_max=12)
+    q = make(blocks, m_max=12, backend=backend)
     ref = bits(run(q, x))
     for _ in range(100):
         assert np.array_equal(bits(run(q, x)), ref)

@@ -13,24 +13,24 @@ from gpu_util import assert_parity, make, run, torch_cuda
 pytestmark = pytest.mark.gpu
 
 
-def test_single_projection_m1():
+def test_single_projection_m1(backend):
     """4096 x 4096, M = 1, seed 0: every output checked."""
     mat = synth.SINGLE_PROJECTION
     blocks = synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id)
     x = synth.x_f16(1, mat.k, seed=0, tensor_id=synth.X_ID_OFFSET + mat.tensor_id)
     y_ref, s_ref = oracle.qmm(blocks, x)
-    q = make(blocks, m_max=1)
+    q = make(blocks, m_max=1, backend=backend)
     assert_parity(run(q, x), y_ref, s_ref, "proj4096 M=1")
 
 
 @pytest.mark.parametrize("mat", synth.SWEEP_MATRICES, ids=lambda m: m.name)
-def test_m_sweep_full_matrices(mat):
+def test_m_sweep_full_matrices(mat, backend):
     """gate_up [5120->34816] and down [17408->5120] at every M of the sweep; the oracle
     runs once on 64 rows (rows are independent, so the first M rows serve every M)."""
     blocks = synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id)
     x = synth.x_f16(64, mat.k, seed=0, tensor_id=synth.X_ID_OFFSET + mat.tensor_id)
     y_ref, s_ref = oracle.qmm(blocks, x)
-    q = make(blocks, m_max=64)
+    q = make(blocks, m_max=64, backend=backend)
     for m in synth.SWEEP_M:
         assert_parity(run(q, x[:m]), y_ref[:m], s_ref[:m], f"{mat.name} M={m}")
 
@@ -39,22 +39,22 @@ def test_m_sweep_full_matrices(mat):
     (1, 256, 1), (33, 256, 3), (40, 512, 5), (100, 768, 9), (257, 1024, 16), (31, 2560, 12),
     (5, 256, 17), (64, 4096, 8), (96, 256, 2), (500, 1280, 13), (1000, 512, 16), (77, 7680, 7),
 ])
-def test_ragged_shapes(n, k, m):
+def test_ragged_shapes(n, k, m, backend):
     """Several tiles, ragged row tails, tiles split between CTAs, M chunked past 16."""
     blocks = synth.q4k_matrix(n, k, seed=1, tensor_id=n * 7 + k)
     x = synth.x_f16(m, k, seed=1, tensor_id=n + k + m)
     y_ref, s_ref = oracle.qmm(blocks, x)
-    q = make(blocks, m_max=max(m, 1))
+    q = make(blocks, m_max=max(m, 1), backend=backend)
     assert_parity(run(q, x), y_ref, s_ref, f"N={n} K={k} M={m}")
 
 
-def test_outlier_activations():
+def test_outlier_activations(backend):
     """1% of activations x20 (the chunked-prefill workload's distribution)."""
     n, k, m = 512, 5120, 16
     blocks = synth.q4k_matrix(n, k, seed=0, tensor_id=2)
     x = synth.x_f16(m, k, seed=0, tensor_id=1002, outlier_p=0.01, outlier_mul=20.0)
     y_ref, s_ref = oracle.qmm(blocks, x)
-    assert_parity(run(make(blocks), x), y_ref, s_ref, "outliers")
+    assert_parity(run(make(blocks, backend=backend), x), y_ref, s_ref, "outliers")
 
 
 def _golden_matrix():
@@ -66,21 +66,21 @@ def _golden_matrix():
     return np.stack(rows)  # [40, 4, 144]: K = 1024
 
 
-def test_hand_packed_blocks():
+def test_hand_packed_blocks(backend):
     """Closed-form blocks (subnormal scales, zeroed pairs, top-bit crossings) in a matrix."""
     blocks = _golden_matrix()
     k = blocks.shape[1] * 256
     x = synth.x_f16(12, k, seed=4, tensor_id=4)
     y_ref, s_ref = oracle.qmm(blocks, x)
-    assert_parity(run(make(blocks), x), y_ref, s_ref, "golden blocks")
+    assert_parity(run(make(blocks, backend=backend), x), y_ref, s_ref, "golden blocks")
     # a row made only of zero blocks gives exactly zero
     zb = np.repeat(blocks[:1, :1] * 0, 4, axis=1)
     zb = np.concatenate([zb, blocks[1:2]], axis=0)
-    y = run(make(zb), x)
+    y = run(make(zb, backend=backend), x)
     assert np.all(y[:, 0] == 0)
 
 
-def test_unit_vectors_pick_columns():
+def test_unit_vectors_pick_columns(backend):
     """x = e_k returns column k of W to within fp16 rounding of the dequantised weight."""
     n, k = 64, 512
     blocks = synth.q4k_matrix(n, k, seed=2, tensor_id=9)
@@ -89,27 +89,27 @@ def test_unit_vectors_pick_columns():
     x = np.zeros((len(cols), k), dtype=np.float16)
     for i, c in enumerate(cols):
         x[i, c] = 1.0
-    y = run(make(blocks), x)
+    y = run(make(blocks, backend=backend), x)
     for i, c in enumerate(cols):
         ref = w[:, c].astype(np.float64)
         assert np.all(np.abs(y[i] - ref) <= 2e-3 * np.abs(ref) + 1e-6), c
 
 
-def test_host_and_device_blocks_agree():
+def test_host_and_device_blocks_agree(backend):
     n, k, m = 70, 1024, 6
     blocks = synth.q4k_matrix(n, k, seed=3, tensor_id=3)
     x = synth.x_f16(m, k, seed=3, tensor_id=30)
-    a = run(make(blocks, device_blocks=True), x)
-    b = run(make(blocks, device_blocks=False), x)
+    a = run(make(blocks, device_blocks=True, backend=backend), x)
+    b = run(make(blocks, device_blocks=False, backend=backend), x)
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
 
 
-def test_run_host_matches_device_run():
+def test_run_host_matches_device_run(backend):
     torch = torch_cuda()
     n, k, m = 300, 2048, 12
     blocks = synth.q4k_matrix(n, k, seed=5, tensor_id=5)
     x = synth.x_f16(m, k, seed=5, tensor_id=50)
-    q = make(blocks, host_io=True)
+    q = make(blocks, host_io=True, backend=backend)
     y_dev = run(q, x)
     xh = torch.from_numpy(x.view(np.int16).copy()).pin_memory()
     yh = torch.empty((m, n), dtype=torch.float32).pin_memory()
@@ -118,12 +118,12 @@ def test_run_host_matches_device_run():
     assert np.array_equal(yh.numpy().view(np.uint32), y_dev.view(np.uint32))
 
 
-def test_argument_errors_with_device():
+def test_argument_errors_with_device(backend):
     from bit_weight_streaming_q4_gb300 import QmmError
     torch = torch_cuda()
     n, k = 64, 512
     blocks = synth.q4k_matrix(n, k, seed=6, tensor_id=6)
-    q = make(blocks, m_max=4)
+    q = make(blocks, m_max=4, backend=backend)
     x = torch.zeros((8, k), dtype=torch.float16, device="cuda")
     y = torch.zeros((8, n), dtype=torch.float32, device="cuda")
     q.run(x, y, 0)                                   # M = 0 is a no-op

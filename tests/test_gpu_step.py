@@ -10,7 +10,7 @@ from gpu_util import assert_parity, make, torch_cuda
 pytestmark = pytest.mark.gpu
 
 
-def test_step_matches_individual_runs():
+def test_step_matches_individual_runs(backend):
     from bit_weight_streaming_q4_gb300 import Step
     torch = torch_cuda()
     mats = [synth.Matrix("a", 512, 1280, 1), synth.Matrix("b", 1280, 768, 2),
@@ -21,7 +21,7 @@ def test_step_matches_individual_runs():
         blocks = synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id)
         x = synth.x_f16(m, mat.k, seed=0, tensor_id=1000 + mat.tensor_id)
         refs.append(oracle.qmm(blocks, x))
-        qs.append(make(blocks, m_max=m))
+        qs.append(make(blocks, m_max=m, backend=backend))
         xs.append(torch.from_numpy(x.view(np.int16)).cuda().view(torch.float16))
         ys.append(torch.zeros((m, mat.n), dtype=torch.float32, device="cuda"))
     single = []
