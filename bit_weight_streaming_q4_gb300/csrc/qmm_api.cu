@@ -153,7 +153,13 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
     if (!h) return QMM_ERR_OOM;
     h->magic = kMagic;
     h->device = dev;
-    h->backend = opt.backend == QMM_BACKEND_MMA_SYNC ? QMM_BACKEND_MMA_SYNC : QMM_BACKEND_TCGEN05;
+    // Auto: the register-fed mma.sync stream for handles that never see more than 16 rows,
+    // tcgen05 otherwise.  Fixed per handle (never per run), so that a row's result does not
+    // depend on how many rows it is batched with.
+    if (opt.backend == QMM_BACKEND_AUTO)
+        h->backend = opt.m_max <= qmm::b1::kMaxM ? QMM_BACKEND_MMA_SYNC : QMM_BACKEND_TCGEN05;
+    else
+        h->backend = opt.backend;
     const bool tc = h->backend == QMM_BACKEND_TCGEN05;
     h->m_max = opt.m_max;
     qmm::Decomp& d = h->d;

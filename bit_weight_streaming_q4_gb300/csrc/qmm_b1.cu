@@ -1,34 +1,49 @@
-// Backend 1: Q4_K weight-streaming matmul on warp-level tensor cores (mma.sync m16n8k16).
+// Backend 1: Q4_K weight-streaming matmul on warp-level tensor cores (mma.sync m16n8k16),
+// for up to 16 stacked rows per launch.
 //
 // The method (page "Running 4 coding agents on one RTX 3090: a custom CUDA engine for
 // Qwen3.8-27B", section "How parallel decoding works"): the M stacked token rows of a
 // decode step are multiplied against every weight while that weight is on chip, so the
-// weights are read from memory once per step however many rows there are.
+// weights are read from memory once per step however many rows there are.  The weight
+// operand comes straight from registers, so nothing but the packed 4-bit stream crosses
+// shared memory.
 //
-// Layout of one unit (32 output rows x one super-block column of 256 weights, 4608 B),
-// written once by repack():
-//   bytes [0, 4096)    quants, in the order the consumer lanes read them:
-//                      [m16 tile r: 2][load i: 4][lane: 32][16 B]
-//                      load i = 2*h + bh gives lane (g = lane/4, t = lane%4) bytes
-//                      qs[32t + 16bh .. +15] of row 16r + 8h + g.
-//   bytes [4096, 4608) the 16-byte block headers (d, dmin, 12 scale bytes) of the 32 rows.
-// Lane t of a quad therefore holds qs[32t .. 32t+31] of its two rows: the low nibbles are
-// weights 64t + 0..31 (sub-block 2t) and the high nibbles weights 64t + 32..63 (sub-block
-// 2t+1).  Each lane needs the (scale, min) pairs of just those two sub-blocks.
+// Arithmetic.  Per super-block and row, w_k = d * sc_j * q_k - dmin * m_j (j = sub-block of
+// k), so y = sum over super-blocks of  d * sum_k (sc_j q_k) x_k  -  dmin * sum_j m_j X_j,
+// with X_j the sum of the activations of sub-block j.  P_k = sc_j * q_k (an integer <= 945)
+// is formed exactly in fp16 from one FMA on the code 1024 + q (or 1024 + 16 q); the tensor
+// cores accumulate P x over the super-block in fp32 (exact products).  The min term is one
+// more m16n8k16 step per super-block: A = m_j (exact small integers), B = X_j split into an
+// fp16 high and low part (fp32 sum of the activations), so it is exact to ~2^-22.  The two
+// partial sums are scaled by d and dmin and added to the fp32 accumulator.
 //
-// MMA k-order.  For step s = 0..15 (i = s % 8, high = s >= 8) lane t supplies the four
-// MMA k slots {2t, 2t+1, 2t+8, 2t+9} with weight offsets 64t + 32*high + 4i + {0, 2, 1, 3}
-// inside the super-block; the activation fragment is loaded with the same permutation, so
-// the MMA sums exactly the products w[n,k] x[m,k].  The order is fixed per handle.
+// Unit = 256 output rows x one super-block column (36864 bytes), written once by repack():
+//   bytes [0, 32768)     quants of eight 32-row slices, slice w read by consumer warp w:
+//                        [w: 8][m16 tile r: 2][row half h: 2][i4: 2][lane: 32][16 B]; the 16
+//                        bytes are the lane's words i = 4 i4 .. 4 i4 + 3; lane (g = lane/4,
+//                        t = lane%4) word i of row 32w + 16r + 8h + g is bytes qs[32t + 4i' .. +3]
+//                        with i' = (i + 2t) % 8.
+//   bytes [32768, 36864) the 16-byte block headers (d, dmin, scales) of the 256 rows.
+// Lane t of a quad reads qs[32t .. 32t+31] of its rows: the low nibbles are weights 64t..64t+31
+// (sub-block 2t), the high nibbles weights 64t+32..64t+63 (sub-block 2t+1).  Its eight words
+// are visited rotated by 2t, so that at any step the four lanes of a quad use four different
+// 16-byte chunks of the swizzled activation tile (no shared-memory bank conflicts).
 //
-// Work split.  CTA c owns the contiguous units [c*U/P, (c+1)*U/P) (U units, P CTAs).  One
-// producer warp streams them into a shared-memory ring with 1-D bulk copies (TMA) and
-// mbarriers; four consumer warps take the units of each row tile round-robin, dequantise
-// in registers to fp16 fragments and accumulate in fp32 on the tensor cores.  At the end of
-// a row tile the four warp partials are summed in warp order through shared memory; a tile
-// split between CTAs is finished by the last CTA to arrive (atomic ticket), which sums the
-// CTA partials in CTA order.  Nothing in this order depends on M or on the other rows, so
-// every row's result is bit-identical however the rows are batched.
+// MMA k-order.  For step s = 0..15 (i = s % 8, i' = (i + 2t) % 8, high = s >= 8) lane t fills
+// the MMA k slots {2t, 2t+1, 2t+8, 2t+9} with weight offsets 64t + 32*high + 4i' + {0, 2, 1, 3}; the
+// activation fragment is read with the same permutation.  The min-term step uses slots
+// (2t, 2t+1) for (hi, lo) of sub-block 2t and (2t+8, 2t+9) for sub-block 2t+1.
+//
+// Warp roles (one persistent CTA per SM per kernel, two CTAs may share an SM so that the
+// next kernel's weights stream in while this one finishes):
+//   warps 0-7  consumers, 32 rows each; warp 8 producer (1-D bulk copies of units, 2-D TMA
+//   of the activation tile x[0..MP-1][kb*256 .. +256] with 128-byte swizzle); warp 9 the
+//   activation sums X_j of each unit, written in fragment order for the min-term step.
+// CTA c owns the units [c*U/P, (c+1)*U/P); a row tile split between CTAs is finished by the
+// last CTA to arrive (atomic ticket), which sums the partials in CTA order.  Nothing in the
+// order of any output's arithmetic depends on M, so rows are bit-identical across batchings.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
 #include "qmm_internal.h"
@@ -37,78 +52,89 @@
 namespace qmm {
 namespace b1 {
 
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kRing = 16;
-constexpr int kQBytes = kRows * 128;
-constexpr int kRedCols = 16;
-constexpr int kRedFloats = kConsumerWarps * kRows * kRedCols;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-// Unit j - kRing of a row tile belongs to the same warp as unit j, so a warp that waits for
-// unit j has already seen the previous fill of that slot complete: the parity it waits on
-// is never a stale one.
-static_assert(kRing % kConsumerWarps == 0, "ring depth must be a multiple of the consumer warps");
+constexpr int kWarps = 8;                       // consumer warps, 32 rows each
+constexpr int kProducerWarp = kWarps;
+constexpr int kConsumerThreads = kWarps * 32;
+constexpr int kQBytes = kRows * 128;            // 32768
+constexpr int kWRing = 4;                       // weight slots
+constexpr int kXRing = 4;                       // activation tiles (TMA)
+constexpr int kFRing = 4;                       // activation fragments
+constexpr int kMinBlocks = 1;                   // one CTA per SM, up to 200 registers per thread
 
-int smem_bytes() {
-    return kRing * kUnitBytes + kRedFloats * 4 + 2 * kRing * 8 + 16;
-}
+template <int NT>
+struct Cfg {
+    static constexpr int kThreads = (kWarps + 1 + NT) * 32;  // consumers, producer, NT fragment warps
+    static constexpr int kMP = 8 * NT;                  // token rows per launch tile
+    static constexpr int kXBox = kMP * 128;             // one 64-wide k box
+    static constexpr int kXSlot = 4 * kXBox;            // x tile of one unit
+    static constexpr int kFragBytes = NT * 8 * 32 * 16; // [nt][word i][lane][16 B]
+    static constexpr int kFSlot = kFragBytes + NT * 32 * 8;  // + min-term fragments [nt][lane][8 B]
+    static constexpr int kXOff = kWRing * kUnitBytes;   // 1024-aligned (36864 = 36 * 1024)
+    static constexpr int kFOff = kXOff + kXRing * kXSlot;
+    static constexpr int kBarOff = kFOff + kFRing * kFSlot;
+    static constexpr int kSmem = kBarOff + (2 * kWRing + 2 * kXRing + 2 * kFRing) * 8 + 16 + 1024;
+};
+
+int smem_bytes(int nt) { return nt == 1 ? Cfg<1>::kSmem : Cfg<2>::kSmem; }
 
 __device__ __forceinline__ int64_t dev_piece_of(int64_t u, int64_t units, int64_t grid) {
     return ((u + 1) * grid + units - 1) / units - 1;
 }
 
-__device__ __forceinline__ void raise_error(int* err, volatile int* abort_flag, int code) {
-    *abort_flag = 1;
-    atomicOr(err, code);
+__device__ __forceinline__ void fail(int* err, volatile int* flags) {
+    if (!flags[0]) {
+        flags[0] = 1;
+        atomicOr(err, 1);
+    }
 }
 
-// Per-row constants for the lane's two sub-blocks j0 = 2t (low nibbles, quant encoded as
-// 1024 + q) and j1 = 2t + 1 (high nibbles, encoded as 1024 + 16q).  Lane .x of each fp16x2
-// belongs to j0, lane .y to j1.
-struct RowScales {
-    uint32_t scx;   // {sc0, sc1 / 16}
-    uint32_t nscx;  // {-1024 sc0, -64 sc1}: scx * code + nscx = sc * q exactly
-    uint32_t d2;    // {d, d}
-    uint32_t nbh;   // {-B_h0, -B_h1},  B_h = fp16(dmin * m)
-    uint32_t nbl;   // {-B_l0, -B_l1},  B_l = dmin * m - B_h exactly (error-free product)
+// Per row: constants of the lane's two sub-blocks j0 = 2t (fp16x2 lane .x) and j1 = 2t+1 (.y).
+struct RowK {
+    uint32_t s;    // {sc0, sc1/16}:  code * s + n = sc * q exactly
+    uint32_t n;    // {-1024 sc0, -64 sc1}
+    uint32_t m;    // {m0, m1}
+    uint32_t dd;   // {d, dmin} as fp16
 };
 
-__device__ __forceinline__ RowScales row_scales(uint4 hd, int t) {
-    const uint32_t s0 = hd.y, s1 = hd.z, s2 = hd.w;
+__device__ __forceinline__ RowK row_consts(uint4 hd, int t) {
     uint32_t SC, MN;
     if (t >= 2) {  // sub-blocks 4..7: low 4 bits from s[8..11], top 2 bits from s[0..7]
-        SC = (s2 & 0x0F0F0F0Fu) | ((s0 >> 2) & 0x30303030u);
-        MN = ((s2 >> 4) & 0x0F0F0F0Fu) | ((s1 >> 2) & 0x30303030u);
+        SC = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
+        MN = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
     } else {       // sub-blocks 0..3: low 6 bits of s[0..3] and s[4..7]
-        SC = s0 & 0x3F3F3F3Fu;
-        MN = s1 & 0x3F3F3F3Fu;
+        SC = hd.y & 0x3F3F3F3Fu;
+        MN = hd.z & 0x3F3F3F3Fu;
     }
     const uint32_t b0 = 2u * (t & 1);
-    // bytes b0, b0+1 -> 16-bit lanes {1024 + v0, 1024 + v1} -> {v0, v1} exactly
-    const uint32_t sel = b0 | ((b0 + 1) << 8);
+    const uint32_t sel = b0 | ((b0 + 1) << 8);  // bytes b0, b0+1 -> 16-bit lanes
     const __half2 k1024 = as_h2(0x64006400u);
     const __half2 sc = __hsub2(as_h2(and_or(prmt(SC, 0, sel), 0x00FF00FFu, 0x64006400u)), k1024);
     const __half2 mn = __hsub2(as_h2(and_or(prmt(MN, 0, sel), 0x00FF00FFu, 0x64006400u)), k1024);
-    RowScales r;
-    r.scx = as_u32(__hmul2(sc, as_h2(0x2C003C00u)));    // * {1, 1/16}
-    r.nscx = as_u32(__hmul2(sc, as_h2(0xD400E400u)));   // * {-1024, -64}
-    const __half2 d = as_h2(prmt(hd.x, 0, 0x1010u));    // {d, d}
-    const __half2 dm = as_h2(prmt(hd.x, 0, 0x3232u));   // {dmin, dmin}
-    const __half2 bh = __hmul2(dm, mn);
-    r.d2 = as_u32(d);
-    r.nbh = as_u32(__hneg2(bh));
-    r.nbl = as_u32(__hfma2(__hneg2(dm), mn, bh));       // -(dmin*m - B_h), exact
+    RowK r;
+    r.s = as_u32(__hmul2(sc, as_h2(0x2C003C00u)));  // * {1, 1/16}
+    r.n = as_u32(__hmul2(sc, as_h2(0xD400E400u)));  // * {-1024, -64}
+    r.m = as_u32(mn);
+    r.dd = hd.x;
     return r;
 }
 
 template <int NT>
-__global__ void __launch_bounds__(kThreads, 2) stream_kernel(const B1Params p) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint8_t* ring = smem;
-    float* red = reinterpret_cast<float*>(smem + kRing * kUnitBytes);
-    uint64_t* full = reinterpret_cast<uint64_t*>(red + kRedFloats);
-    uint64_t* empty = full + kRing;
-    volatile int* flags = reinterpret_cast<volatile int*>(empty + kRing);  // [0] abort [1] last
+__global__ void __launch_bounds__(Cfg<NT>::kThreads, kMinBlocks)
+    stream_kernel(const __grid_constant__ CUtensorMap xmap, const B1Params p) {
+    using C = Cfg<NT>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* wring = smem;
+    uint8_t* xring = smem + C::kXOff;
+    uint8_t* fring = smem + C::kFOff;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+    uint64_t* wfull = bars;
+    uint64_t* wempty = wfull + kWRing;
+    uint64_t* xfull = wempty + kWRing;
+    uint64_t* xempty = xfull + kXRing;
+    uint64_t* ffull = xempty + kXRing;
+    uint64_t* fempty = ffull + kFRing;
+    volatile int* flags = reinterpret_cast<volatile int*>(fempty + kFRing);  // [0] abort [1] last
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -118,66 +144,152 @@ __global__ void __launch_bounds__(kThreads, 2) stream_kernel(const B1Params p) {
     const int64_t u0 = c * U / p.grid;
     const int64_t u1 = (c + 1) * U / p.grid;
     const int nunits = static_cast<int>(u1 - u0);
+    const int KB = p.kb;
 
     if (tid == 0) {
-        for (int i = 0; i < kRing; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+        for (int i = 0; i < kWRing; ++i) {
+            mbar_init(&wfull[i], 1);
+            mbar_init(&wempty[i], kWarps);
+        }
+        for (int i = 0; i < kXRing; ++i) {
+            mbar_init(&xfull[i], 1);
+            mbar_init(&xempty[i], NT);
+        }
+        for (int i = 0; i < kFRing; ++i) {
+            mbar_init(&ffull[i], NT);
+            mbar_init(&fempty[i], kWarps);
         }
         flags[0] = 0;
         flags[1] = 0;
         fence_mbar_init();
     }
     __syncthreads();
-    // Let the next kernel in the stream start its weight prefetch while this one runs.
     griddep_launch_dependents();
 
-    if (warp == kConsumerWarps) {
-        // ---------------- producer: weights do not depend on the previous kernel, so the
-        // stream starts before griddepcontrol.wait.
+    // ------------------------------------------------------------------ producer
+    if (warp == kProducerWarp) {
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
             const uint8_t* src = p.wq + u0 * kUnitBytes;
-            int issued = 0;
-            for (int j = 0; j < nunits; ++j) {
-                const int slot = j % kRing;
-                if (j >= kRing && !mbar_wait_bounded(&empty[slot], ((j / kRing) - 1) & 1, flags)) {
-                    raise_error(p.err, flags, 1);
-                    break;
-                }
-                mbar_arrive_expect_tx(&full[slot], kUnitBytes);
-                bulk_g2s(ring + slot * kUnitBytes, src + static_cast<int64_t>(j) * kUnitBytes,
-                         kUnitBytes, &full[slot], pol);
-                issued = j + 1;
+            const int pre = nunits < kWRing ? nunits : kWRing;
+            for (int j = 0; j < pre; ++j) {
+                mbar_arrive_expect_tx(&wfull[j], kUnitBytes);
+                bulk_g2s(wring + j * kUnitBytes, src + static_cast<int64_t>(j) * kUnitBytes, kUnitBytes, &wfull[j], pol);
             }
+            int w_issued = pre, x_issued = 0;
+            griddep_wait();  // activations may be written by the previous kernel
+            prefetch_tmap(&xmap);
+            // Keep both rings as full as their consumers allow, polling without blocking on
+            // either, so that activation tiles run ahead of the weights they pair with.
+            bool ok = true;
+            uint64_t t0 = globaltimer_ns();
+            while (ok && (w_issued < nunits || x_issued < nunits) && !flags[0]) {
+                bool progress = false;
+                if (x_issued < nunits) {
+                    const int jx = x_issued;
+                    const int xs = jx % kXRing;
+                    if (jx < kXRing || mbar_try_wait(&xempty[xs], ((jx / kXRing) - 1) & 1)) {
+                        mbar_arrive_expect_tx(&xfull[xs], C::kXSlot);
+                        const int kb = static_cast<int>((u0 + jx) % KB);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            tma_load_2d(xring + xs * C::kXSlot + i * C::kXBox, &xmap, kb * 256 + 64 * i, 0, &xfull[xs]);
+                        x_issued = jx + 1;
+                        progress = true;
+                    }
+                }
+                if (w_issued < nunits) {
+                    const int jj = w_issued;
+                    const int s = jj % kWRing;
+                    if (mbar_try_wait(&wempty[s], ((jj / kWRing) - 1) & 1)) {
+                        mbar_arrive_expect_tx(&wfull[s], kUnitBytes);
+                        bulk_g2s(wring + s * kUnitBytes, src + static_cast<int64_t>(jj) * kUnitBytes, kUnitBytes, &wfull[s],
+                                 pol);
+                        w_issued = jj + 1;
+                        progress = true;
+                    }
+                }
+                if (progress) {
+                    t0 = globaltimer_ns();
+                } else if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                    ok = false;
+                }
+            }
+            if (!ok) fail(p.err, flags);
             if (flags[0]) {
-                // Failure path: do not leave bulk copies writing into a CTA that has exited.
+                // failure path: let every copy already issued land before the CTA can exit
                 volatile int no_abort = 0;
-                for (int j = issued > kRing ? issued - kRing : 0; j < issued; ++j)
-                    mbar_wait_bounded(&full[j % kRing], (j / kRing) & 1, &no_abort);
+                for (int j = w_issued > kWRing ? w_issued - kWRing : 0; j < w_issued; ++j)
+                    mbar_wait_bounded(&wfull[j % kWRing], (j / kWRing) & 1, &no_abort);
+                for (int j = x_issued > kXRing ? x_issued - kXRing : 0; j < x_issued; ++j)
+                    mbar_wait_bounded(&xfull[j % kXRing], (j / kXRing) & 1, &no_abort);
             }
         }
         return;
     }
 
-    // ---------------- consumers
-    griddep_wait();  // x may be written by the previous kernel
-
-    const int g = lane >> 2;
-    const int t = lane & 3;
-    const int KB = p.kb;
-    const int64_t K = static_cast<int64_t>(KB) * 256;
-    const int64_t t_first = u0 / KB;
-    const int64_t t_last = (u1 - 1) / KB;
-
-    // this lane's activation row pointer per 8-token group (nullptr for padding rows)
-    const __half* xrow[NT];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int m = nt * 8 + g;
-        xrow[nt] = (m < p.m) ? p.x + m * K + 64 * t : nullptr;
+    // ------------------------------------------------------------------ activation fragments
+    // Fragment warp nt turns the activation tile of each unit into the consumers' MMA B
+    // fragments for tokens 8nt..8nt+7 (lane (g, t) of word step i: the 4+4 activations at
+    // k = 64t + 4i' and 64t + 32 + 4i', i' = (i + 2t) % 8, in slot order) and into the
+    // min-term fragments (fp32 sums of sub-blocks 2t and 2t+1, split into fp16 hi + lo).
+    if (warp > kProducerWarp) {
+        const int g = lane >> 2, t = lane & 3;
+        const int nt = warp - kProducerWarp - 1;  // this warp's 8-token group
+        for (int j = 0; j < nunits; ++j) {
+            const int xs = j % kXRing;
+            const int fs = j % kFRing;
+            bool ok = true;
+            if (j >= kFRing) ok = mbar_wait_bounded(&fempty[fs], ((j / kFRing) - 1) & 1, flags);
+            ok = ok && mbar_wait_bounded(&xfull[xs], (j / kXRing) & 1, flags);
+            if (!ok) fail(p.err, flags);
+            uint8_t* fst = fring + fs * C::kFSlot;
+            {
+                const int tok = nt * 8 + g;
+                const uint8_t* xrow = xring + xs * C::kXSlot + t * C::kXBox + tok * 128;  // box t, token row
+                float x_lo = 0.f, x_hi = 0.f;
+#pragma unroll 4
+                for (int i = 0; i < 8; ++i) {
+                    const int ir = (i + 2 * t) & 7;
+                    const uint2 vl = *reinterpret_cast<const uint2*>(xrow + (((ir >> 1) ^ (tok & 7)) * 16) + (ir & 1) * 8);
+                    const uint2 vh = *reinterpret_cast<const uint2*>(xrow + (((4 + (ir >> 1)) ^ (tok & 7)) * 16) + (ir & 1) * 8);
+                    uint4 f;
+                    f.x = prmt(vl.x, vl.y, 0x5410u);  // {x[4i'], x[4i'+2]}
+                    f.y = prmt(vl.x, vl.y, 0x7632u);  // {x[4i'+1], x[4i'+3]}
+                    f.z = prmt(vh.x, vh.y, 0x5410u);
+                    f.w = prmt(vh.x, vh.y, 0x7632u);
+                    *reinterpret_cast<uint4*>(fst + ((nt * 8 + i) * 32 + lane) * 16) = f;
+                    const float2 a0 = __half22float2(as_h2(vl.x)), a1 = __half22float2(as_h2(vl.y));
+                    const float2 b0 = __half22float2(as_h2(vh.x)), b1 = __half22float2(as_h2(vh.y));
+                    x_lo += (a0.x + a0.y) + (a1.x + a1.y);
+                    x_hi += (b0.x + b0.y) + (b1.x + b1.y);
+                }
+                // X = hi + lo, hi = fp16(X) saturated to the finite range, lo = fp16(X - hi)
+                const float lim = 65504.f;
+                const float cl = fminf(fmaxf(x_lo, -lim), lim), ch = fminf(fmaxf(x_hi, -lim), lim);
+                const __half l_hi = __float2half_rn(cl), h_hi = __float2half_rn(ch);
+                uint2 mt;
+                mt.x = as_u32(__halves2half2(l_hi, __float2half_rn(cl - __half2float(l_hi))));  // slots 2t, 2t+1
+                mt.y = as_u32(__halves2half2(h_hi, __float2half_rn(ch - __half2float(h_hi))));  // slots 2t+8, 2t+9
+                *reinterpret_cast<uint2*>(fst + C::kFragBytes + (nt * 32 + lane) * 8) = mt;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&xempty[xs]);
+                mbar_arrive(&ffull[fs]);
+            }
+        }
+        return;
     }
 
+    // ------------------------------------------------------------------ consumers
+    const int g = lane >> 2;
+    const int t = lane & 3;
+    const int64_t t_first = u0 / KB;
+    const int64_t t_last = (u1 - 1) / KB;
+    griddep_wait();  // y and the workspace may still be in use by the previous kernel
+
+    int j = 0;  // piece-relative unit index
     for (int64_t tile = t_first; tile <= t_last; ++tile) {
         const int64_t ja = (tile * KB > u0 ? tile * KB : u0) - u0;
         const int64_t jb = ((tile + 1) * KB < u1 ? (tile + 1) * KB : u1) - u0;
@@ -190,135 +302,123 @@ __global__ void __launch_bounds__(kThreads, 2) stream_kernel(const B1Params p) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc[r][nt][e] = 0.f;
 
-        for (int64_t j = ja + warp; j < jb; j += kConsumerWarps) {
-            const int slot = static_cast<int>(j % kRing);
-            const uint32_t ph = static_cast<uint32_t>((j / kRing) & 1);
-            const int64_t kb = u0 + j - tile * KB;
-
-            // activations for this super-block column: 64 halves per lane per token group
-            uint4 xv[NT][8];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                if (xrow[nt]) {
-                    const uint4* src = reinterpret_cast<const uint4*>(xrow[nt] + kb * 256);
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) xv[nt][v] = src[v];
-                } else {
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) xv[nt][v] = make_uint4(0, 0, 0, 0);
-                }
-            }
-            // warm L1 with this warp's next column
-            if (j + kConsumerWarps < jb) {
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    if (xrow[nt])
-                        asm volatile("prefetch.global.L1 [%0];" ::"l"(xrow[nt] + (kb + kConsumerWarps) * 256));
-            }
-
-            if (!mbar_wait_bounded(&full[slot], ph, flags)) {
-                if (!flags[0]) raise_error(p.err, flags, 1);
-                continue;  // keep the control flow (and barrier counts) of the other warps
-            }
-            const uint8_t* us = ring + slot * kUnitBytes;
-            uint4 qv[2][4];
+        for (; j < jb; ++j) {
+            const int s = j % kWRing;
+            const int fs = j % kFRing;
+            if (!mbar_wait_bounded(&wfull[s], (j / kWRing) & 1, flags)) fail(p.err, flags);
+            // this warp's words: [r][h][i4][lane][16 B], word i = 4 i4 + component
+            const uint8_t* myq = wring + s * kUnitBytes + warp * 4096;
+            uint4 qv[2][2][2];
             uint4 hd[2][2];
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    qv[r][i] = *reinterpret_cast<const uint4*>(us + ((r * 4 + i) * 32 + lane) * 16);
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-                    hd[r][h] = *reinterpret_cast<const uint4*>(us + kQBytes + (16 * r + 8 * h + g) * 16);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
-
-            RowScales rs[2][2];
 #pragma unroll
             for (int r = 0; r < 2; ++r)
 #pragma unroll
-                for (int h = 0; h < 2; ++h) rs[r][h] = row_scales(hd[r][h], t);
+                for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                    for (int i4 = 0; i4 < 2; ++i4)
+                        qv[r][h][i4] = *reinterpret_cast<const uint4*>(myq + (((r * 2 + h) * 2 + i4) * 32 + lane) * 16);
+                    hd[r][h] = *reinterpret_cast<const uint4*>(wring + s * kUnitBytes + kQBytes +
+                                                               (32 * warp + 16 * r + 8 * h + g) * 16);
+                }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&wempty[s]);
+
+            RowK rk[2][2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) rk[r][h] = row_consts(hd[r][h], t);
+
+            if (!mbar_wait_bounded(&ffull[fs], (j / kFRing) & 1, flags)) fail(p.err, flags);
+            const uint8_t* fst = fring + fs * C::kFSlot;
+
+            float dp[2][NT][4];
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) dp[r][nt][e] = 0.f;
 
 #pragma unroll
-            for (int s = 0; s < 16; ++s) {
-                const int i = s & 7;
-                const int hi = s >> 3;
-                uint32_t b01[NT], b23[NT];
+            for (int i = 0; i < 8; ++i) {  // word i: step (i, low nibbles) then (i, high nibbles)
+                uint4 f[NT];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const uint4 xq = xv[nt][hi * 4 + (i >> 1)];
-                    const uint32_t x01 = (i & 1) ? xq.z : xq.x;  // halves 4i, 4i+1
-                    const uint32_t x23 = (i & 1) ? xq.w : xq.y;  // halves 4i+2, 4i+3
-                    b01[nt] = prmt(x01, x23, 0x5410u);           // {x[4i], x[4i+2]}
-                    b23[nt] = prmt(x01, x23, 0x7632u);           // {x[4i+1], x[4i+3]}
-                }
+                for (int nt = 0; nt < NT; ++nt) f[nt] = *reinterpret_cast<const uint4*>(fst + ((nt * 8 + i) * 32 + lane) * 16);
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    uint32_t a[4];
+                    uint32_t alo[4], ahi[4];
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const uint4 qq = qv[r][2 * h + (i >> 2)];
+                        const uint4 qq = qv[r][h][i >> 2];
                         const uint32_t w = (i & 3) == 0 ? qq.x : (i & 3) == 1 ? qq.y : (i & 3) == 2 ? qq.z : qq.w;
-                        // code = 1024 + q (low nibbles) or 1024 + 16q (high nibbles)
-                        const uint32_t mask = hi ? 0x00F000F0u : 0x000F000Fu;
-                        const __half2 c02 = as_h2(and_or(w, mask, 0x64006400u));
-                        const __half2 c13 = as_h2(and_or(w >> 8, mask, 0x64006400u));
-                        const RowScales& z = rs[r][h];
-                        const __half2 scx = hi ? __high2half2(as_h2(z.scx)) : __low2half2(as_h2(z.scx));
-                        const __half2 nsc = hi ? __high2half2(as_h2(z.nscx)) : __low2half2(as_h2(z.nscx));
-                        const __half2 nbh = hi ? __high2half2(as_h2(z.nbh)) : __low2half2(as_h2(z.nbh));
-                        const __half2 nbl = hi ? __high2half2(as_h2(z.nbl)) : __low2half2(as_h2(z.nbl));
-                        const __half2 d2 = as_h2(z.d2);
-                        // P = sc*q exactly; w = fp16(d*P - B_h) - B_l  (within ~1 ulp of w)
-                        const __half2 p02 = __hfma2(c02, scx, nsc);
-                        const __half2 p13 = __hfma2(c13, scx, nsc);
-                        a[h] = as_u32(__hadd2(__hfma2(p02, d2, nbh), nbl));       // k slots 2t, 2t+1
-                        a[2 + h] = as_u32(__hadd2(__hfma2(p13, d2, nbh), nbl));   // k slots 2t+8, 2t+9
+                        const uint32_t w8 = w >> 8;
+                        const __half2 s_lo = __low2half2(as_h2(rk[r][h].s)), n_lo = __low2half2(as_h2(rk[r][h].n));
+                        const __half2 s_hi = __high2half2(as_h2(rk[r][h].s)), n_hi = __high2half2(as_h2(rk[r][h].n));
+                        // P = sc*q, exact: code * s + n
+                        alo[h] = as_u32(__hfma2(as_h2(and_or(w, 0x000F000Fu, 0x64006400u)), s_lo, n_lo));
+                        alo[2 + h] = as_u32(__hfma2(as_h2(and_or(w8, 0x000F000Fu, 0x64006400u)), s_lo, n_lo));
+                        ahi[h] = as_u32(__hfma2(as_h2(and_or(w, 0x00F000F0u, 0x64006400u)), s_hi, n_hi));
+                        ahi[2 + h] = as_u32(__hfma2(as_h2(and_or(w8, 0x00F000F0u, 0x64006400u)), s_hi, n_hi));
                     }
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-                        mma_m16n8k16(acc[r][nt], a[0], a[1], a[2], a[3], b01[nt], b23[nt]);
+                    for (int nt = 0; nt < NT; ++nt) {
+                        mma_m16n8k16(dp[r][nt], alo[0], alo[1], alo[2], alo[3], f[nt].x, f[nt].y);
+                        mma_m16n8k16(dp[r][nt], ahi[0], ahi[1], ahi[2], ahi[3], f[nt].z, f[nt].w);
+                    }
+                }
+            }
+
+            // min term: sum_j m_j X_j with X split into fp16 hi + lo
+            uint2 xb[NT];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) xb[nt] = *reinterpret_cast<const uint2*>(fst + C::kFragBytes + (nt * 32 + lane) * 8);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&fempty[fs]);
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const __half2 m0 = as_h2(rk[r][0].m), m1 = as_h2(rk[r][1].m);
+                const uint32_t a0 = as_u32(__low2half2(m0)), a2 = as_u32(__high2half2(m0));   // row g
+                const uint32_t a1 = as_u32(__low2half2(m1)), a3 = as_u32(__high2half2(m1));   // row g+8
+                const float2 dd0 = __half22float2(as_h2(rk[r][0].dd)), dd1 = __half22float2(as_h2(rk[r][1].dd));
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    float dm[4] = {0.f, 0.f, 0.f, 0.f};
+                    mma_m16n8k16(dm, a0, a1, a2, a3, xb[nt].x, xb[nt].y);
+                    acc[r][nt][0] = fmaf(dd0.x, dp[r][nt][0], acc[r][nt][0]);
+                    acc[r][nt][1] = fmaf(dd0.x, dp[r][nt][1], acc[r][nt][1]);
+                    acc[r][nt][2] = fmaf(dd1.x, dp[r][nt][2], acc[r][nt][2]);
+                    acc[r][nt][3] = fmaf(dd1.x, dp[r][nt][3], acc[r][nt][3]);
+                    acc[r][nt][0] = fmaf(-dd0.y, dm[0], acc[r][nt][0]);
+                    acc[r][nt][1] = fmaf(-dd0.y, dm[1], acc[r][nt][1]);
+                    acc[r][nt][2] = fmaf(-dd1.y, dm[2], acc[r][nt][2]);
+                    acc[r][nt][3] = fmaf(-dd1.y, dm[3], acc[r][nt][3]);
                 }
             }
         }
 
-        // ---------------- fixed-order reduction of the warp partials of this row tile
-        float* rw = red + warp * kRows * kRedCols;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const int col = nt * 8 + 2 * t;
-                rw[(16 * r + g) * kRedCols + col] = acc[r][nt][0];
-                rw[(16 * r + g) * kRedCols + col + 1] = acc[r][nt][1];
-                rw[(16 * r + g + 8) * kRedCols + col] = acc[r][nt][2];
-                rw[(16 * r + g + 8) * kRedCols + col + 1] = acc[r][nt][3];
-            }
-        }
-        named_bar_sync(1, kConsumerThreads);
-
-        const int nw = static_cast<int>(jb - ja < kConsumerWarps ? jb - ja : kConsumerWarps);
+        // ---------------- write the row tile (or its split-K partial)
         const bool whole = (ja + u0 == tile * KB) && (jb + u0 == (tile + 1) * KB);
-        const int nel = kRows * p.m;
-        if (whole) {
-            for (int e = tid; e < nel; e += kConsumerThreads) {
-                const int row = e & (kRows - 1), m = e / kRows;
-                float v = red[row * kRedCols + m];
-                for (int w = 1; w < nw; ++w) v += red[(w * kRows + row) * kRedCols + m];
-                const int64_t n = tile * kRows + row;
-                if (n < p.n) p.y[m * p.n + n] = v;
-            }
-        } else {
-            const int side = (tile == t_first) ? 0 : 1;
-            float* part = p.ws + (c * 2 + side) * kRows * p.ws_cols;
-            for (int e = tid; e < nel; e += kConsumerThreads) {
-                const int row = e & (kRows - 1), m = e / kRows;
-                float v = red[row * kRedCols + m];
-                for (int w = 1; w < nw; ++w) v += red[(w * kRows + row) * kRedCols + m];
-                part[m * kRows + row] = v;
-            }
+        const int side = (tile == t_first) ? 0 : 1;
+        float* part = p.ws + (c * 2 + side) * static_cast<int64_t>(kRows) * p.ws_cols;
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int row = 32 * warp + 16 * r + g + 8 * (e >> 1);
+                    const int m = nt * 8 + 2 * t + (e & 1);
+                    if (m < p.m) {
+                        if (whole) {
+                            const int64_t n = tile * kRows + row;
+                            if (n < p.n) p.y[static_cast<int64_t>(m) * p.n + n] = acc[r][nt][e];
+                        } else {
+                            part[m * kRows + row] = acc[r][nt][e];
+                        }
+                    }
+                }
+        if (!whole) {
             __threadfence();
             named_bar_sync(1, kConsumerThreads);
             const int64_t pa = dev_piece_of(tile * KB, U, p.grid);
@@ -330,79 +430,133 @@ __global__ void __launch_bounds__(kThreads, 2) stream_kernel(const B1Params p) {
             named_bar_sync(1, kConsumerThreads);
             if (flags[1]) {
                 __threadfence();
-                for (int e = tid; e < nel; e += kConsumerThreads) {
-                    const int row = e & (kRows - 1), m = e / kRows;
-                    float v = 0.f;
-                    for (int64_t pc = pa; pc <= pb; ++pc) {
-                        const int64_t pc_first_tile = (pc * U / p.grid) / KB;
-                        const int sd = (tile == pc_first_tile) ? 0 : 1;
-                        const float pv = __ldcg(p.ws + (pc * 2 + sd) * kRows * p.ws_cols + m * kRows + row);
-                        v = (pc == pa) ? pv : v + pv;
-                    }
-                    const int64_t n = tile * kRows + row;
-                    if (n < p.n) p.y[m * p.n + n] = v;
+                float sum[2][NT][4];
+#pragma unroll 1
+                for (int64_t pc = pa; pc <= pb; ++pc) {
+                    const int64_t pc_first_tile = (pc * U / p.grid) / KB;
+                    const int sd = (tile == pc_first_tile) ? 0 : 1;
+                    const float* src = p.ws + (pc * 2 + sd) * static_cast<int64_t>(kRows) * p.ws_cols;
+#pragma unroll
+                    for (int r = 0; r < 2; ++r)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int row = 32 * warp + 16 * r + g + 8 * (e >> 1);
+                                const int m = nt * 8 + 2 * t + (e & 1);
+                                const float v = (m < p.m) ? __ldcg(src + m * kRows + row) : 0.f;
+                                sum[r][nt][e] = (pc == pa) ? v : sum[r][nt][e] + v;
+                            }
                 }
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int row = 32 * warp + 16 * r + g + 8 * (e >> 1);
+                            const int m = nt * 8 + 2 * t + (e & 1);
+                            const int64_t n = tile * kRows + row;
+                            if (m < p.m && n < p.n) p.y[static_cast<int64_t>(m) * p.n + n] = sum[r][nt][e];
+                        }
                 if (tid == 0) p.tickets[tile] = 0;  // ready for the next run
             }
+            named_bar_sync(1, kConsumerThreads);  // flags[1] is reused by the next tile
         }
-        named_bar_sync(1, kConsumerThreads);  // red and flags are reused by the next tile
     }
 }
 
 // One thread per 16-byte piece of the packed layout.
-__global__ void repack_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
-                              int64_t n, int32_t kb, int64_t units) {
+__global__ void repack_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int64_t n, int32_t kb,
+                              int64_t units) {
+    constexpr int kSegs = kUnitBytes / 16;  // 2304
     const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    constexpr int kSegs = kUnitBytes / 16;  // 288
     if (idx >= units * kSegs) return;
     const int64_t u = idx / kSegs;
     const int seg = static_cast<int>(idx % kSegs);
     const int64_t tile = u / kb;
     const int b = static_cast<int>(u % kb);
-    int row, off;
-    if (seg < 256) {
-        const int r = seg >> 7, i = (seg >> 5) & 3, L = seg & 31;
-        const int g = L >> 2, t = L & 3, h = i >> 1, bh = i & 1;
-        row = 16 * r + 8 * h + g;
-        off = 16 + 32 * t + 16 * bh;
-    } else {
-        row = seg - 256;
-        off = 0;
-    }
-    const int64_t nrow = tile * kRows + row;
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (nrow < n) v = *reinterpret_cast<const uint4*>(src + (nrow * kb + b) * 144 + off);
-    *reinterpret_cast<uint4*>(dst + u * kUnitBytes + seg * 16) = v;
+    if (seg < kQBytes / 16) {
+        // 16 output bytes = words 4 i4 .. 4 i4 + 3 of one lane of one (w, r, h) row group
+        const int w = seg >> 8, r = (seg >> 7) & 1, h = (seg >> 6) & 1, i4 = (seg >> 5) & 1, lane = seg & 31;
+        const int g = lane >> 2, t = lane & 3;
+        const int row = 32 * w + 16 * r + 8 * h + g;
+        const int64_t nrow = tile * kRows + row;
+        if (nrow < n) {
+            const uint32_t* qs = reinterpret_cast<const uint32_t*>(src + (nrow * kb + b) * 144 + 16 + 32 * t);
+            uint32_t wv[4];
+            for (int e = 0; e < 4; ++e) wv[e] = qs[(4 * i4 + e + 2 * t) & 7];
+            v = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+    } else {
+        const int row = seg - kQBytes / 16;
+        const int64_t nrow = tile * kRows + row;
+        if (nrow < n) v = *reinterpret_cast<const uint4*>(src + (nrow * kb + b) * 144);
+    }
+    *reinterpret_cast<uint4*>(dst + u * kUnitBytes + static_cast<int64_t>(seg) * 16) = v;
 }
 
 cudaError_t repack(const uint8_t* src_dev, uint8_t* dst_dev, const Decomp& d, cudaStream_t s) {
     const int64_t total = d.units * (kUnitBytes / 16);
     const int threads = 256;
     const int64_t blocks = (total + threads - 1) / threads;
-    repack_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(src_dev, dst_dev, d.n,
-                                                                   static_cast<int32_t>(d.kb), d.units);
+    repack_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(src_dev, dst_dev, d.n, static_cast<int32_t>(d.kb),
+                                                                   d.units);
     return cudaGetLastError();
 }
 
 cudaError_t configure() {
-    cudaError_t e = cudaFuncSetAttribute(stream_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes());
+    cudaError_t e = cudaFuncSetAttribute(stream_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<1>::kSmem);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(stream_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes());
+    return cudaFuncSetAttribute(stream_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<2>::kSmem);
 }
 
-cudaError_t launch(const B1Params& p, cudaStream_t s, bool pdl) {
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+template <int NT>
+static cudaError_t launch_nt(const CUtensorMap& tmap, const B1Params& p, cudaStream_t s, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem_bytes();
+    cfg.blockDim = dim3(Cfg<NT>::kThreads);
+    cfg.dynamicSmemBytes = Cfg<NT>::kSmem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (p.m <= 8) return cudaLaunchKernelEx(&cfg, stream_kernel<1>, p);
-    return cudaLaunchKernelEx(&cfg, stream_kernel<2>, p);
+    return cudaLaunchKernelEx(&cfg, stream_kernel<NT>, tmap, p);
+}
+
+cudaError_t launch(const B1Params& p, cudaStream_t s, bool pdl) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const int nt = p.m <= 8 ? 1 : 2;
+    const int64_t k = static_cast<int64_t>(p.kb) * 256;
+    CUtensorMap tmap;
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(p.m)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(k) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(8 * nt)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(p.x), gdim, gstride, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    return nt == 1 ? launch_nt<1>(tmap, p, s, pdl) : launch_nt<2>(tmap, p, s, pdl);
 }
 
 }  // namespace b1

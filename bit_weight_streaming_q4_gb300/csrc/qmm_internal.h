@@ -69,10 +69,10 @@ cudaError_t configure();
 
 // Backend 1: warp-level mma.sync streaming kernel.
 namespace b1 {
-constexpr int kRows = 32;
+constexpr int kRows = 256;
 constexpr int kUnitBytes = kRows * 144;
 constexpr int kMaxM = 16;  // rows per launch
-int smem_bytes();
+int smem_bytes(int nt);
 cudaError_t repack(const uint8_t* src_dev, uint8_t* dst_dev, const Decomp& d, cudaStream_t s);
 cudaError_t launch(const B1Params& p, cudaStream_t s, bool pdl);
 cudaError_t configure();  // one-time function attributes
