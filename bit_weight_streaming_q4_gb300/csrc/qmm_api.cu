@@ -2,6 +2,8 @@
 // graph-recorded decode step.  See include/qmm.h for the contract.
 #include <cuda_runtime.h>
 
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 #include <new>
 #include <unordered_set>
@@ -78,20 +80,20 @@ qmm_status launch_run(qmm_handle h, const void* x, int64_t m, float* y, cudaStre
             p.ws_cols = h->ws_cols;
             e = qmm::b2::launch(xc, K, p, s, pdl);
         } else {
-            qmm::B1Params p;
-            p.wq = h->wq;
-            p.x = xc;
-            p.y = yc;
-            p.ws = h->ws;
-            p.tickets = h->tickets;
-            p.err = h->err_dev;
-            p.units = h->d.units;
-            p.n = N;
-            p.kb = static_cast<int32_t>(h->d.kb);
-            p.m = static_cast<int32_t>(mc);
-            p.grid = h->d.grid;
-            p.ws_cols = h->ws_cols;
-            e = qmm::b1::launch(p, s, pdl);
+            qmm::B1Mat mat;
+            e = qmm::b1::make_mat(&mat, h->wq, xc, yc, h->tickets, h->d.units, N, static_cast<int32_t>(h->d.kb),
+                                  h->d.grid, static_cast<int32_t>(mc));
+            if (e == cudaSuccess) {
+                qmm::B1Params p = {};
+                p.mats = nullptr;
+                p.ws = h->ws;
+                p.err = h->err_dev;
+                p.done = nullptr;
+                p.count = 1;
+                p.m = static_cast<int32_t>(mc);
+                p.ws_cols = h->ws_cols;
+                e = qmm::b1::launch(mat, p, h->d.grid, s, pdl, false);
+            }
         }
         if (e != cudaSuccess) return QMM_ERR_CUDA;
     }
@@ -288,9 +290,28 @@ qmm_status qmm_destroy(qmm_handle h) {
 
 // ------------------------------------------------------------------------- decode step
 struct qmm_step_s {
-    cudaGraph_t graph = nullptr;
+    cudaGraph_t graph = nullptr;  // launch-per-run path (tcgen05 handles, or more than 16 rows)
     cudaGraphExec_t exec = nullptr;
+    // persistent path: every matrix in one cooperative launch of the mma.sync kernel
+    qmm::B1Mat* mats = nullptr;   // device
+    float* ws = nullptr;
+    int* done = nullptr;
+    int* err_host = nullptr;
+    int* err_dev = nullptr;
+    qmm::B1Params params = {};
+    int grid = 0;
 };
+
+static void free_step(qmm_step st) {
+    if (!st) return;
+    if (st->exec) cudaGraphExecDestroy(st->exec);
+    if (st->graph) cudaGraphDestroy(st->graph);
+    cudaFree(st->mats);
+    cudaFree(st->ws);
+    cudaFree(st->done);
+    if (st->err_host) cudaFreeHost(st->err_host);
+    delete st;
+}
 
 extern "C" {
 
@@ -304,27 +325,67 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
         if (!aligned16(xs[i]) || !aligned16(ys[i])) return QMM_ERR_MISALIGNED;
         if (m > handles[i]->m_max) return QMM_ERR_UNSUPPORTED_SHAPE;
     }
-    cudaStream_t cap = nullptr;
-    if (cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking) != cudaSuccess) return QMM_ERR_CUDA;
     qmm_step st = new (std::nothrow) qmm_step_s();
-    if (!st) {
-        cudaStreamDestroy(cap);
-        return QMM_ERR_OOM;
-    }
+    if (!st) return QMM_ERR_OOM;
+    // QMM_STEP_MODE=persistent selects one persistent kernel for the whole step (mma.sync
+    // handles, up to 16 rows); the default records one launch per run into a CUDA graph.
+    const char* mode = getenv("QMM_STEP_MODE");
+    bool persistent = m <= qmm::b1::kMaxM && mode && strcmp(mode, "persistent") == 0;
+    for (int32_t i = 0; i < count; ++i) persistent = persistent && handles[i]->backend == QMM_BACKEND_MMA_SYNC;
     qmm_status rc = QMM_OK;
-    if (cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess) rc = QMM_ERR_CUDA;
-    for (int32_t i = 0; rc == QMM_OK && i < count; ++i)
-        rc = launch_run(handles[i], xs[i], m, ys[i], cap, /*pdl=*/i > 0);
-    cudaGraph_t g = nullptr;
-    cudaError_t ec = cudaStreamEndCapture(cap, &g);
-    if (rc == QMM_OK && ec != cudaSuccess) rc = QMM_ERR_CUDA;
-    if (rc == QMM_OK && cudaGraphInstantiate(&st->exec, g, 0) != cudaSuccess) rc = QMM_ERR_CUDA;
-    st->graph = g;
-    cudaStreamDestroy(cap);
+    if (persistent) {
+        // one persistent kernel walks all matrices; matrix i+1's activations are read only
+        // after every CTA has finished matrix i
+        std::vector<qmm::B1Mat> host(count);
+        int grid = 0;
+        for (int32_t i = 0; i < count && rc == QMM_OK; ++i) {
+            const qmm_handle h = handles[i];
+            if (qmm::b1::make_mat(&host[i], h->wq, xs[i], ys[i], h->tickets, h->d.units, h->d.n,
+                                  static_cast<int32_t>(h->d.kb), h->d.grid, static_cast<int32_t>(m)) != cudaSuccess)
+                rc = QMM_ERR_CUDA;
+            grid = h->d.grid > grid ? h->d.grid : grid;
+        }
+        const size_t ws_bytes = static_cast<size_t>(grid) * 2 * qmm::b1::kRows * m * sizeof(float);
+        if (rc == QMM_OK && cudaMalloc(&st->mats, sizeof(qmm::B1Mat) * count) != cudaSuccess) rc = QMM_ERR_OOM;
+        if (rc == QMM_OK && cudaMalloc(&st->ws, ws_bytes) != cudaSuccess) rc = QMM_ERR_OOM;
+        if (rc == QMM_OK && cudaMalloc(&st->done, sizeof(int) * (count + 1)) != cudaSuccess) rc = QMM_ERR_OOM;
+        if (rc == QMM_OK && cudaHostAlloc(&st->err_host, sizeof(int), cudaHostAllocMapped) != cudaSuccess)
+            rc = QMM_ERR_OOM;
+        if (rc == QMM_OK) {
+            *st->err_host = 0;
+            if (cudaHostGetDevicePointer(&st->err_dev, st->err_host, 0) != cudaSuccess ||
+                cudaMemcpy(st->mats, host.data(), sizeof(qmm::B1Mat) * count, cudaMemcpyHostToDevice) != cudaSuccess ||
+                cudaMemset(st->done, 0, sizeof(int) * (count + 1)) != cudaSuccess)
+                rc = QMM_ERR_CUDA;
+        }
+        if (rc == QMM_OK) {
+            st->grid = grid;
+            st->params.mats = st->mats;
+            st->params.ws = st->ws;
+            st->params.err = st->err_dev;
+            st->params.done = st->done;
+            st->params.count = count;
+            st->params.m = static_cast<int32_t>(m);
+            st->params.ws_cols = static_cast<int32_t>(m);
+        }
+    } else {
+        cudaStream_t cap = nullptr;
+        if (cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking) != cudaSuccess) rc = QMM_ERR_CUDA;
+        if (rc == QMM_OK && cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+            rc = QMM_ERR_CUDA;
+        for (int32_t i = 0; rc == QMM_OK && i < count; ++i)
+            rc = launch_run(handles[i], xs[i], m, ys[i], cap, /*pdl=*/i > 0);
+        if (cap) {
+            cudaGraph_t g = nullptr;
+            cudaError_t ec = cudaStreamEndCapture(cap, &g);
+            if (rc == QMM_OK && ec != cudaSuccess) rc = QMM_ERR_CUDA;
+            if (rc == QMM_OK && cudaGraphInstantiate(&st->exec, g, 0) != cudaSuccess) rc = QMM_ERR_CUDA;
+            st->graph = g;
+            cudaStreamDestroy(cap);
+        }
+    }
     if (rc != QMM_OK) {
-        if (st->exec) cudaGraphExecDestroy(st->exec);
-        if (st->graph) cudaGraphDestroy(st->graph);
-        delete st;
+        free_step(st);
         return rc;
     }
     (void)stream;
@@ -341,8 +402,13 @@ qmm_status qmm_step_launch(qmm_step s, void* stream) {
         std::lock_guard<std::mutex> lk(g_mu);
         if (!s || !g_steps.count(s)) return QMM_ERR_BAD_HANDLE;
     }
-    return cudaGraphLaunch(s->exec, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? QMM_OK
-                                                                                         : QMM_ERR_CUDA;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    if (s->mats) {
+        if (*reinterpret_cast<volatile int*>(s->err_host)) return QMM_ERR_DEVICE_TIMEOUT;
+        const qmm::B1Mat unused = {};
+        return qmm::b1::launch(unused, s->params, s->grid, cs, true, true) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+    }
+    return cudaGraphLaunch(s->exec, cs) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
 }
 
 qmm_status qmm_step_destroy(qmm_step s) {
@@ -352,9 +418,7 @@ qmm_status qmm_step_destroy(qmm_step s) {
         g_steps.erase(s);
     }
     cudaDeviceSynchronize();
-    cudaGraphExecDestroy(s->exec);
-    cudaGraphDestroy(s->graph);
-    delete s;
+    free_step(s);
     return QMM_OK;
 }
 

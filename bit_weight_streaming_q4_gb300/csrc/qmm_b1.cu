@@ -118,9 +118,30 @@ __device__ __forceinline__ RowK row_consts(uint4 hd, int t) {
     return r;
 }
 
+__device__ __forceinline__ void piece_of_cta(const B1Mat& M, int64_t c, int64_t& u0, int64_t& u1) {
+    if (c < M.grid) {
+        u0 = c * M.units / M.grid;
+        u1 = (c + 1) * M.units / M.grid;
+    } else {
+        u0 = u1 = 0;
+    }
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Cursor over the CTA's units of a list of matrices, in order: matrix i, unit j of its piece.
+struct Cursor {
+    int i;
+    int64_t j, u0, u1;
+};
+
 template <int NT>
 __global__ void __launch_bounds__(Cfg<NT>::kThreads, kMinBlocks)
-    stream_kernel(const __grid_constant__ CUtensorMap xmap, const B1Params p) {
+    stream_kernel(const __grid_constant__ B1Mat single, const B1Params p) {
     using C = Cfg<NT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -140,11 +161,24 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, kMinBlocks)
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int64_t c = blockIdx.x;
-    const int64_t U = p.units;
-    const int64_t u0 = c * U / p.grid;
-    const int64_t u1 = (c + 1) * U / p.grid;
-    const int nunits = static_cast<int>(u1 - u0);
-    const int KB = p.kb;
+    const int count = p.count;
+    const int ncta = static_cast<int>(gridDim.x);
+    // matrix i of the run (a single run passes its matrix by value)
+    auto mat = [&](int i) -> const B1Mat& { return count == 1 ? single : p.mats[i]; };
+    auto next = [&](Cursor& k) {
+        ++k.j;
+        while (k.i < count && k.j >= k.u1 - k.u0) {
+            ++k.i;
+            k.j = 0;
+            if (k.i < count) piece_of_cta(mat(k.i), c, k.u0, k.u1);
+        }
+    };
+    auto first = [&](Cursor& k) {
+        k.i = 0;
+        k.j = -1;
+        piece_of_cta(mat(0), c, k.u0, k.u1);
+        next(k);
+    };
 
     if (tid == 0) {
         for (int i = 0; i < kWRing; ++i) {
@@ -170,42 +204,53 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, kMinBlocks)
     if (warp == kProducerWarp) {
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
-            const uint8_t* src = p.wq + u0 * kUnitBytes;
-            const int pre = nunits < kWRing ? nunits : kWRing;
-            for (int j = 0; j < pre; ++j) {
-                mbar_arrive_expect_tx(&wfull[j], kUnitBytes);
-                bulk_g2s(wring + j * kUnitBytes, src + static_cast<int64_t>(j) * kUnitBytes, kUnitBytes, &wfull[j], pol);
-            }
-            int w_issued = pre, x_issued = 0;
+            Cursor w, x;
+            first(w);
+            first(x);
+            int64_t wseq = 0, xseq = 0;
+            auto issue_w = [&]() {
+                const B1Mat& M = mat(w.i);
+                const int s = static_cast<int>(wseq % kWRing);
+                mbar_arrive_expect_tx(&wfull[s], kUnitBytes);
+                bulk_g2s(wring + s * kUnitBytes, M.wq + (w.u0 + w.j) * kUnitBytes, kUnitBytes, &wfull[s], pol);
+                ++wseq;
+                next(w);
+            };
+            // weights do not depend on the previous kernel: start streaming them right away
+            while (w.i < count && wseq < kWRing) issue_w();
             griddep_wait();  // activations may be written by the previous kernel
-            prefetch_tmap(&xmap);
             // Keep both rings as full as their consumers allow, polling without blocking on
-            // either, so that activation tiles run ahead of the weights they pair with.
+            // either.  The activation tile of a matrix is loaded only once every CTA has
+            // finished the matrix before it (its input depends on that matrix's output).
             bool ok = true;
+            int dep_ready = 0;  // matrices whose predecessor is known to be complete
             uint64_t t0 = globaltimer_ns();
-            while (ok && (w_issued < nunits || x_issued < nunits) && !flags[0]) {
+            while (ok && (w.i < count || x.i < count) && !flags[0]) {
                 bool progress = false;
-                if (x_issued < nunits) {
-                    const int jx = x_issued;
-                    const int xs = jx % kXRing;
-                    if (jx < kXRing || mbar_try_wait(&xempty[xs], ((jx / kXRing) - 1) & 1)) {
+                if (x.i < count) {
+                    bool dep = x.i <= dep_ready;
+                    if (!dep && ld_acquire(p.done + (x.i - 1)) >= ncta) {
+                        dep_ready = x.i;
+                        dep = true;
+                    }
+                    const int xs = static_cast<int>(xseq % kXRing);
+                    if (dep && (xseq < kXRing || mbar_try_wait(&xempty[xs], ((xseq / kXRing) - 1) & 1))) {
+                        const B1Mat& M = mat(x.i);
+                        if (x.j == 0) prefetch_tmap(&M.xmap);
                         mbar_arrive_expect_tx(&xfull[xs], C::kXSlot);
-                        const int kb = static_cast<int>((u0 + jx) % KB);
+                        const int kb = static_cast<int>((x.u0 + x.j) % M.kb);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            tma_load_2d(xring + xs * C::kXSlot + i * C::kXBox, &xmap, kb * 256 + 64 * i, 0, &xfull[xs]);
-                        x_issued = jx + 1;
+                        for (int b = 0; b < 4; ++b)
+                            tma_load_2d(xring + xs * C::kXSlot + b * C::kXBox, &M.xmap, kb * 256 + 64 * b, 0, &xfull[xs]);
+                        ++xseq;
+                        next(x);
                         progress = true;
                     }
                 }
-                if (w_issued < nunits) {
-                    const int jj = w_issued;
-                    const int s = jj % kWRing;
-                    if (mbar_try_wait(&wempty[s], ((jj / kWRing) - 1) & 1)) {
-                        mbar_arrive_expect_tx(&wfull[s], kUnitBytes);
-                        bulk_g2s(wring + s * kUnitBytes, src + static_cast<int64_t>(jj) * kUnitBytes, kUnitBytes, &wfull[s],
-                                 pol);
-                        w_issued = jj + 1;
+                if (w.i < count) {
+                    const int s = static_cast<int>(wseq % kWRing);
+                    if (mbar_try_wait(&wempty[s], ((wseq / kWRing) - 1) & 1)) {
+                        issue_w();
                         progress = true;
                     }
                 }
@@ -219,9 +264,9 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, kMinBlocks)
             if (flags[0]) {
                 // failure path: let every copy already issued land before the CTA can exit
                 volatile int no_abort = 0;
-                for (int j = w_issued > kWRing ? w_issued - kWRing : 0; j < w_issued; ++j)
+                for (int64_t j = wseq > kWRing ? wseq - kWRing : 0; j < wseq; ++j)
                     mbar_wait_bounded(&wfull[j % kWRing], (j / kWRing) & 1, &no_abort);
-                for (int j = x_issued > kXRing ? x_issued - kXRing : 0; j < x_issued; ++j)
+                for (int64_t j = xseq > kXRing ? xseq - kXRing : 0; j < xseq; ++j)
                     mbar_wait_bounded(&xfull[j % kXRing], (j / kXRing) & 1, &no_abort);
             }
         }
@@ -236,43 +281,47 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, kMinBlocks)
     if (warp > kProducerWarp) {
         const int g = lane >> 2, t = lane & 3;
         const int nt = warp - kProducerWarp - 1;  // this warp's 8-token group
-        for (int j = 0; j < nunits; ++j) {
-            const int xs = j % kXRing;
-            const int fs = j % kFRing;
+        int64_t total = 0;
+        for (int i = 0; i < count; ++i) {
+            int64_t u0, u1;
+            piece_of_cta(mat(i), c, u0, u1);
+            total += u1 - u0;
+        }
+        for (int64_t j = 0; j < total; ++j) {
+            const int xs = static_cast<int>(j % kXRing);
+            const int fs = static_cast<int>(j % kFRing);
             bool ok = true;
             if (j >= kFRing) ok = mbar_wait_bounded(&fempty[fs], ((j / kFRing) - 1) & 1, flags);
             ok = ok && mbar_wait_bounded(&xfull[xs], (j / kXRing) & 1, flags);
             if (!ok) fail(p.err, flags);
             uint8_t* fst = fring + fs * C::kFSlot;
-            {
-                const int tok = nt * 8 + g;
-                const uint8_t* xrow = xring + xs * C::kXSlot + t * C::kXBox + tok * 128;  // box t, token row
-                float x_lo = 0.f, x_hi = 0.f;
+            const int tok = nt * 8 + g;
+            const uint8_t* xrow = xring + xs * C::kXSlot + t * C::kXBox + tok * 128;  // box t, token row
+            float x_lo = 0.f, x_hi = 0.f;
 #pragma unroll 4
-                for (int i = 0; i < 8; ++i) {
-                    const int ir = (i + 2 * t) & 7;
-                    const uint2 vl = *reinterpret_cast<const uint2*>(xrow + (((ir >> 1) ^ (tok & 7)) * 16) + (ir & 1) * 8);
-                    const uint2 vh = *reinterpret_cast<const uint2*>(xrow + (((4 + (ir >> 1)) ^ (tok & 7)) * 16) + (ir & 1) * 8);
-                    uint4 f;
-                    f.x = prmt(vl.x, vl.y, 0x5410u);  // {x[4i'], x[4i'+2]}
-                    f.y = prmt(vl.x, vl.y, 0x7632u);  // {x[4i'+1], x[4i'+3]}
-                    f.z = prmt(vh.x, vh.y, 0x5410u);
-                    f.w = prmt(vh.x, vh.y, 0x7632u);
-                    *reinterpret_cast<uint4*>(fst + ((nt * 8 + i) * 32 + lane) * 16) = f;
-                    const float2 a0 = __half22float2(as_h2(vl.x)), a1 = __half22float2(as_h2(vl.y));
-                    const float2 b0 = __half22float2(as_h2(vh.x)), b1 = __half22float2(as_h2(vh.y));
-                    x_lo += (a0.x + a0.y) + (a1.x + a1.y);
-                    x_hi += (b0.x + b0.y) + (b1.x + b1.y);
-                }
-                // X = hi + lo, hi = fp16(X) saturated to the finite range, lo = fp16(X - hi)
-                const float lim = 65504.f;
-                const float cl = fminf(fmaxf(x_lo, -lim), lim), ch = fminf(fmaxf(x_hi, -lim), lim);
-                const __half l_hi = __float2half_rn(cl), h_hi = __float2half_rn(ch);
-                uint2 mt;
-                mt.x = as_u32(__halves2half2(l_hi, __float2half_rn(cl - __half2float(l_hi))));  // slots 2t, 2t+1
-                mt.y = as_u32(__halves2half2(h_hi, __float2half_rn(ch - __half2float(h_hi))));  // slots 2t+8, 2t+9
-                *reinterpret_cast<uint2*>(fst + C::kFragBytes + (nt * 32 + lane) * 8) = mt;
+            for (int i = 0; i < 8; ++i) {
+                const int ir = (i + 2 * t) & 7;
+                const uint2 vl = *reinterpret_cast<const uint2*>(xrow + (((ir >> 1) ^ (tok & 7)) * 16) + (ir & 1) * 8);
+                const uint2 vh = *reinterpret_cast<const uint2*>(xrow + (((4 + (ir >> 1)) ^ (tok & 7)) * 16) + (ir & 1) * 8);
+                uint4 f;
+                f.x = prmt(vl.x, vl.y, 0x5410u);  // {x[4i'], x[4i'+2]}
+                f.y = prmt(vl.x, vl.y, 0x7632u);  // {x[4i'+1], x[4i'+3]}
+                f.z = prmt(vh.x, vh.y, 0x5410u);
+                f.w = prmt(vh.x, vh.y, 0x7632u);
+                *reinterpret_cast<uint4*>(fst + ((nt * 8 + i) * 32 + lane) * 16) = f;
+                const float2 a0 = __half22float2(as_h2(vl.x)), a1 = __half22float2(as_h2(vl.y));
+                const float2 b0 = __half22float2(as_h2(vh.x)), b1 = __half22float2(as_h2(vh.y));
+                x_lo += (a0.x + a0.y) + (a1.x + a1.y);
+                x_hi += (b0.x + b0.y) + (b1.x + b1.y);
             }
+            // X = hi + lo, hi = fp16(X) saturated to the finite range, lo = fp16(X - hi)
+            const float lim = 65504.f;
+            const float cl = fminf(fmaxf(x_lo, -lim), lim), ch = fminf(fmaxf(x_hi, -lim), lim);
+            const __half l_hi = __float2half_rn(cl), h_hi = __float2half_rn(ch);
+            uint2 mt;
+            mt.x = as_u32(__halves2half2(l_hi, __float2half_rn(cl - __half2float(l_hi))));  // slots 2t, 2t+1
+            mt.y = as_u32(__halves2half2(h_hi, __float2half_rn(ch - __half2float(h_hi))));  // slots 2t+8, 2t+9
+            *reinterpret_cast<uint2*>(fst + C::kFragBytes + (nt * 32 + lane) * 8) = mt;
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&xempty[xs]);
@@ -285,157 +334,177 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, kMinBlocks)
     // ------------------------------------------------------------------ consumers
     const int g = lane >> 2;
     const int t = lane & 3;
-    const int64_t t_first = u0 / KB;
-    const int64_t t_last = (u1 - 1) / KB;
     griddep_wait();  // y and the workspace may still be in use by the previous kernel
+    int64_t gseq = 0;  // position in the CTA's unit sequence (ring slots and phases)
+    for (int mi = 0; mi < count; ++mi) {
+        const B1Mat& M = mat(mi);
+        int64_t u0, u1;
+        piece_of_cta(M, c, u0, u1);
+        const int KB = M.kb;
+        const int64_t U = M.units;
+        const int64_t P = M.grid;
+        const int64_t t_first = u0 < u1 ? u0 / KB : 0;
+        const int64_t t_last = u0 < u1 ? (u1 - 1) / KB : -1;
+        int64_t j = 0;  // piece-relative unit index
+        for (int64_t tile = t_first; tile <= t_last; ++tile) {
+            const int64_t ja = (tile * KB > u0 ? tile * KB : u0) - u0;
+            const int64_t jb = ((tile + 1) * KB < u1 ? (tile + 1) * KB : u1) - u0;
 
-    int j = 0;  // piece-relative unit index
-    for (int64_t tile = t_first; tile <= t_last; ++tile) {
-        const int64_t ja = (tile * KB > u0 ? tile * KB : u0) - u0;
-        const int64_t jb = ((tile + 1) * KB < u1 ? (tile + 1) * KB : u1) - u0;
-
-        float acc[2][NT][4];
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[r][nt][e] = 0.f;
-
-        for (; j < jb; ++j) {
-            const int s = j % kWRing;
-            const int fs = j % kFRing;
-            if (!mbar_wait_bounded(&wfull[s], (j / kWRing) & 1, flags)) fail(p.err, flags);
-            // this warp's words: [r][h][i4][lane][16 B], word i = 4 i4 + component
-            const uint8_t* myq = wring + s * kUnitBytes + warp * 4096;
-            uint4 qv[2][2][2];
-            uint4 hd[2][2];
-#pragma unroll
-            for (int r = 0; r < 2; ++r)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                    for (int i4 = 0; i4 < 2; ++i4)
-                        qv[r][h][i4] = *reinterpret_cast<const uint4*>(myq + (((r * 2 + h) * 2 + i4) * 32 + lane) * 16);
-                    hd[r][h] = *reinterpret_cast<const uint4*>(wring + s * kUnitBytes + kQBytes +
-                                                               (32 * warp + 16 * r + 8 * h + g) * 16);
-                }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&wempty[s]);
-
-            RowK rk[2][2];
-#pragma unroll
-            for (int r = 0; r < 2; ++r)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) rk[r][h] = row_consts(hd[r][h], t);
-
-            if (!mbar_wait_bounded(&ffull[fs], (j / kFRing) & 1, flags)) fail(p.err, flags);
-            const uint8_t* fst = fring + fs * C::kFSlot;
-
-            float dp[2][NT][4];
+            float acc[2][NT][4];
 #pragma unroll
             for (int r = 0; r < 2; ++r)
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) dp[r][nt][e] = 0.f;
+                    for (int e = 0; e < 4; ++e) acc[r][nt][e] = 0.f;
 
+            for (; j < jb; ++j, ++gseq) {
+                const int s = static_cast<int>(gseq % kWRing);
+                const int fs = static_cast<int>(gseq % kFRing);
+                if (!mbar_wait_bounded(&wfull[s], (gseq / kWRing) & 1, flags)) fail(p.err, flags);
+                // this warp's words: [r][h][i4][lane][16 B], word i = 4 i4 + component
+                const uint8_t* myq = wring + s * kUnitBytes + warp * 4096;
+                uint4 qv[2][2][2];
+                uint4 hd[2][2];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {  // word i: step (i, low nibbles) then (i, high nibbles)
-                uint4 f[NT];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) f[nt] = *reinterpret_cast<const uint4*>(fst + ((nt * 8 + i) * 32 + lane) * 16);
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    uint32_t alo[4], ahi[4];
+                for (int r = 0; r < 2; ++r)
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const uint4 qq = qv[r][h][i >> 2];
-                        const uint32_t w = (i & 3) == 0 ? qq.x : (i & 3) == 1 ? qq.y : (i & 3) == 2 ? qq.z : qq.w;
-                        const uint32_t w8 = w >> 8;
-                        const __half2 s_lo = __low2half2(as_h2(rk[r][h].s)), n_lo = __low2half2(as_h2(rk[r][h].n));
-                        const __half2 s_hi = __high2half2(as_h2(rk[r][h].s)), n_hi = __high2half2(as_h2(rk[r][h].n));
-                        // P = sc*q, exact: code * s + n
-                        alo[h] = as_u32(__hfma2(as_h2(and_or(w, 0x000F000Fu, 0x64006400u)), s_lo, n_lo));
-                        alo[2 + h] = as_u32(__hfma2(as_h2(and_or(w8, 0x000F000Fu, 0x64006400u)), s_lo, n_lo));
-                        ahi[h] = as_u32(__hfma2(as_h2(and_or(w, 0x00F000F0u, 0x64006400u)), s_hi, n_hi));
-                        ahi[2 + h] = as_u32(__hfma2(as_h2(and_or(w8, 0x00F000F0u, 0x64006400u)), s_hi, n_hi));
+#pragma unroll
+                        for (int i4 = 0; i4 < 2; ++i4)
+                            qv[r][h][i4] = *reinterpret_cast<const uint4*>(myq + (((r * 2 + h) * 2 + i4) * 32 + lane) * 16);
+                        hd[r][h] = *reinterpret_cast<const uint4*>(wring + s * kUnitBytes + kQBytes +
+                                                                   (32 * warp + 16 * r + 8 * h + g) * 16);
                     }
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        mma_m16n8k16(dp[r][nt], alo[0], alo[1], alo[2], alo[3], f[nt].x, f[nt].y);
-                        mma_m16n8k16(dp[r][nt], ahi[0], ahi[1], ahi[2], ahi[3], f[nt].z, f[nt].w);
-                    }
-                }
-            }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&wempty[s]);
 
-            // min term: sum_j m_j X_j with X split into fp16 hi + lo
-            uint2 xb[NT];
+                RowK rk[2][2];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) xb[nt] = *reinterpret_cast<const uint2*>(fst + C::kFragBytes + (nt * 32 + lane) * 8);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&fempty[fs]);
+                for (int r = 0; r < 2; ++r)
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const __half2 m0 = as_h2(rk[r][0].m), m1 = as_h2(rk[r][1].m);
-                const uint32_t a0 = as_u32(__low2half2(m0)), a2 = as_u32(__high2half2(m0));   // row g
-                const uint32_t a1 = as_u32(__low2half2(m1)), a3 = as_u32(__high2half2(m1));   // row g+8
-                const float2 dd0 = __half22float2(as_h2(rk[r][0].dd)), dd1 = __half22float2(as_h2(rk[r][1].dd));
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    float dm[4] = {0.f, 0.f, 0.f, 0.f};
-                    mma_m16n8k16(dm, a0, a1, a2, a3, xb[nt].x, xb[nt].y);
-                    acc[r][nt][0] = fmaf(dd0.x, dp[r][nt][0], acc[r][nt][0]);
-                    acc[r][nt][1] = fmaf(dd0.x, dp[r][nt][1], acc[r][nt][1]);
-                    acc[r][nt][2] = fmaf(dd1.x, dp[r][nt][2], acc[r][nt][2]);
-                    acc[r][nt][3] = fmaf(dd1.x, dp[r][nt][3], acc[r][nt][3]);
-                    acc[r][nt][0] = fmaf(-dd0.y, dm[0], acc[r][nt][0]);
-                    acc[r][nt][1] = fmaf(-dd0.y, dm[1], acc[r][nt][1]);
-                    acc[r][nt][2] = fmaf(-dd1.y, dm[2], acc[r][nt][2]);
-                    acc[r][nt][3] = fmaf(-dd1.y, dm[3], acc[r][nt][3]);
-                }
-            }
-        }
+                    for (int h = 0; h < 2; ++h) rk[r][h] = row_consts(hd[r][h], t);
 
-        // ---------------- write the row tile (or its split-K partial)
-        const bool whole = (ja + u0 == tile * KB) && (jb + u0 == (tile + 1) * KB);
-        const int side = (tile == t_first) ? 0 : 1;
-        float* part = p.ws + (c * 2 + side) * static_cast<int64_t>(kRows) * p.ws_cols;
+                if (!mbar_wait_bounded(&ffull[fs], (gseq / kFRing) & 1, flags)) fail(p.err, flags);
+                const uint8_t* fst = fring + fs * C::kFSlot;
+
+                float dp[2][NT][4];
 #pragma unroll
-        for (int r = 0; r < 2; ++r)
+                for (int r = 0; r < 2; ++r)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+                    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int row = 32 * warp + 16 * r + g + 8 * (e >> 1);
-                    const int m = nt * 8 + 2 * t + (e & 1);
-                    if (m < p.m) {
-                        if (whole) {
-                            const int64_t n = tile * kRows + row;
-                            if (n < p.n) p.y[static_cast<int64_t>(m) * p.n + n] = acc[r][nt][e];
-                        } else {
-                            part[m * kRows + row] = acc[r][nt][e];
+                        for (int e = 0; e < 4; ++e) dp[r][nt][e] = 0.f;
+
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {  // word i: step (i, low nibbles) then (i, high nibbles)
+                    uint4 f[NT];
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) f[nt] = *reinterpret_cast<const uint4*>(fst + ((nt * 8 + i) * 32 + lane) * 16);
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        uint32_t alo[4], ahi[4];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint4 qq = qv[r][h][i >> 2];
+                            const uint32_t w = (i & 3) == 0 ? qq.x : (i & 3) == 1 ? qq.y : (i & 3) == 2 ? qq.z : qq.w;
+                            const uint32_t w8 = w >> 8;
+                            const __half2 s_lo = __low2half2(as_h2(rk[r][h].s)), n_lo = __low2half2(as_h2(rk[r][h].n));
+                            const __half2 s_hi = __high2half2(as_h2(rk[r][h].s)), n_hi = __high2half2(as_h2(rk[r][h].n));
+                            // P = sc*q, exact: code * s + n
+                            alo[h] = as_u32(__hfma2(as_h2(and_or(w, 0x000F000Fu, 0x64006400u)), s_lo, n_lo));
+                            alo[2 + h] = as_u32(__hfma2(as_h2(and_or(w8, 0x000F000Fu, 0x64006400u)), s_lo, n_lo));
+                            ahi[h] = as_u32(__hfma2(as_h2(and_or(w, 0x00F000F0u, 0x64006400u)), s_hi, n_hi));
+                            ahi[2 + h] = as_u32(__hfma2(as_h2(and_or(w8, 0x00F000F0u, 0x64006400u)), s_hi, n_hi));
+                        }
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            mma_m16n8k16(dp[r][nt], alo[0], alo[1], alo[2], alo[3], f[nt].x, f[nt].y);
+                            mma_m16n8k16(dp[r][nt], ahi[0], ahi[1], ahi[2], ahi[3], f[nt].z, f[nt].w);
                         }
                     }
                 }
-        if (!whole) {
-            __threadfence();
-            named_bar_sync(1, kConsumerThreads);
-            const int64_t pa = dev_piece_of(tile * KB, U, p.grid);
-            const int64_t pb = dev_piece_of((tile + 1) * KB - 1, U, p.grid);
-            if (tid == 0) {
-                const int old = atomicAdd(&p.tickets[tile], 1);
-                flags[1] = (old == static_cast<int>(pb - pa)) ? 1 : 0;
+
+                // min term: sum_j m_j X_j with X split into fp16 hi + lo
+                uint2 xb[NT];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) xb[nt] = *reinterpret_cast<const uint2*>(fst + C::kFragBytes + (nt * 32 + lane) * 8);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&fempty[fs]);
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const __half2 m0 = as_h2(rk[r][0].m), m1 = as_h2(rk[r][1].m);
+                    const uint32_t a0 = as_u32(__low2half2(m0)), a2 = as_u32(__high2half2(m0));   // row g
+                    const uint32_t a1 = as_u32(__low2half2(m1)), a3 = as_u32(__high2half2(m1));   // row g+8
+                    const float2 dd0 = __half22float2(as_h2(rk[r][0].dd)), dd1 = __half22float2(as_h2(rk[r][1].dd));
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        float dm[4] = {0.f, 0.f, 0.f, 0.f};
+                        mma_m16n8k16(dm, a0, a1, a2, a3, xb[nt].x, xb[nt].y);
+                        acc[r][nt][0] = fmaf(dd0.x, dp[r][nt][0], acc[r][nt][0]);
+                        acc[r][nt][1] = fmaf(dd0.x, dp[r][nt][1], acc[r][nt][1]);
+                        acc[r][nt][2] = fmaf(dd1.x, dp[r][nt][2], acc[r][nt][2]);
+                        acc[r][nt][3] = fmaf(dd1.x, dp[r][nt][3], acc[r][nt][3]);
+                        acc[r][nt][0] = fmaf(-dd0.y, dm[0], acc[r][nt][0]);
+                        acc[r][nt][1] = fmaf(-dd0.y, dm[1], acc[r][nt][1]);
+                        acc[r][nt][2] = fmaf(-dd1.y, dm[2], acc[r][nt][2]);
+                        acc[r][nt][3] = fmaf(-dd1.y, dm[3], acc[r][nt][3]);
+                    }
+                }
+        
             }
-            named_bar_sync(1, kConsumerThreads);
-            if (flags[1]) {
+
+            // ---------------- write the row tile (or its split-K partial)
+            const bool whole = (ja + u0 == tile * KB) && (jb + u0 == (tile + 1) * KB);
+            const int side = (tile == t_first) ? 0 : 1;
+            float* part = p.ws + (c * 2 + side) * static_cast<int64_t>(kRows) * p.ws_cols;
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int row = 32 * warp + 16 * r + g + 8 * (e >> 1);
+                        const int m = nt * 8 + 2 * t + (e & 1);
+                        if (m < p.m) {
+                            if (whole) {
+                                const int64_t n = tile * kRows + row;
+                                if (n < M.n) M.y[static_cast<int64_t>(m) * M.n + n] = acc[r][nt][e];
+                            } else {
+                                part[m * kRows + row] = acc[r][nt][e];
+                            }
+                        }
+                    }
+            if (!whole) {
                 __threadfence();
-                float sum[2][NT][4];
+                named_bar_sync(1, kConsumerThreads);
+                const int64_t pa = dev_piece_of(tile * KB, U, P);
+                const int64_t pb = dev_piece_of((tile + 1) * KB - 1, U, P);
+                if (tid == 0) {
+                    const int old = atomicAdd(&M.tickets[tile], 1);
+                    flags[1] = (old == static_cast<int>(pb - pa)) ? 1 : 0;
+                }
+                named_bar_sync(1, kConsumerThreads);
+                if (flags[1]) {
+                    __threadfence();
+                    float sum[2][NT][4];
 #pragma unroll 1
-                for (int64_t pc = pa; pc <= pb; ++pc) {
-                    const int64_t pc_first_tile = (pc * U / p.grid) / KB;
-                    const int sd = (tile == pc_first_tile) ? 0 : 1;
-                    const float* src = p.ws + (pc * 2 + sd) * static_cast<int64_t>(kRows) * p.ws_cols;
+                    for (int64_t pc = pa; pc <= pb; ++pc) {
+                        const int64_t pc_first_tile = (pc * U / P) / KB;
+                        const int sd = (tile == pc_first_tile) ? 0 : 1;
+                        const float* src = p.ws + (pc * 2 + sd) * static_cast<int64_t>(kRows) * p.ws_cols;
+#pragma unroll
+                        for (int r = 0; r < 2; ++r)
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int row = 32 * warp + 16 * r + g + 8 * (e >> 1);
+                                    const int m = nt * 8 + 2 * t + (e & 1);
+                                    const float v = (m < p.m) ? __ldcg(src + m * kRows + row) : 0.f;
+                                    sum[r][nt][e] = (pc == pa) ? v : sum[r][nt][e] + v;
+                                }
+                    }
 #pragma unroll
                     for (int r = 0; r < 2; ++r)
 #pragma unroll
@@ -444,24 +513,27 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, kMinBlocks)
                             for (int e = 0; e < 4; ++e) {
                                 const int row = 32 * warp + 16 * r + g + 8 * (e >> 1);
                                 const int m = nt * 8 + 2 * t + (e & 1);
-                                const float v = (m < p.m) ? __ldcg(src + m * kRows + row) : 0.f;
-                                sum[r][nt][e] = (pc == pa) ? v : sum[r][nt][e] + v;
+                                const int64_t n = tile * kRows + row;
+                                if (m < p.m && n < M.n) M.y[static_cast<int64_t>(m) * M.n + n] = sum[r][nt][e];
                             }
+                    if (tid == 0) M.tickets[tile] = 0;  // ready for the next run
                 }
-#pragma unroll
-                for (int r = 0; r < 2; ++r)
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int row = 32 * warp + 16 * r + g + 8 * (e >> 1);
-                            const int m = nt * 8 + 2 * t + (e & 1);
-                            const int64_t n = tile * kRows + row;
-                            if (m < p.m && n < p.n) p.y[static_cast<int64_t>(m) * p.n + n] = sum[r][nt][e];
-                        }
-                if (tid == 0) p.tickets[tile] = 0;  // ready for the next run
+                named_bar_sync(1, kConsumerThreads);  // flags[1] is reused by the next tile
             }
-            named_bar_sync(1, kConsumerThreads);  // flags[1] is reused by the next tile
+
+        }
+        if (count > 1) {
+            // this CTA is done with matrix mi: count it towards the matrix's completion
+            __threadfence();
+            named_bar_sync(1, kConsumerThreads);
+            if (tid == 0) atomicAdd(p.done + mi, 1);
+        }
+    }
+    if (count > 1 && tid == 0) {
+        // the last CTA to finish resets the completion counters for the next launch
+        if (atomicAdd(p.done + count, 1) == ncta - 1) {
+            for (int i = 0; i <= count; ++i) p.done[i] = 0;
+            __threadfence();
         }
     }
 }
@@ -528,35 +600,50 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 template <int NT>
-static cudaError_t launch_nt(const CUtensorMap& tmap, const B1Params& p, cudaStream_t s, bool pdl) {
+static cudaError_t launch_nt(const B1Mat& single, const B1Params& p, int grid, cudaStream_t s, bool pdl,
+                             bool cooperative) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(Cfg<NT>::kThreads);
     cfg.dynamicSmemBytes = Cfg<NT>::kSmem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = cooperative ? 1 : 0;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, stream_kernel<NT>, tmap, p);
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, stream_kernel<NT>, single, p);
 }
 
-cudaError_t launch(const B1Params& p, cudaStream_t s, bool pdl) {
+cudaError_t make_mat(B1Mat* out, const uint8_t* wq, const void* x, float* y, int* tickets, int64_t units,
+                     int64_t n, int32_t kb, int32_t grid, int32_t m) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    const int nt = p.m <= 8 ? 1 : 2;
-    const int64_t k = static_cast<int64_t>(p.kb) * 256;
-    CUtensorMap tmap;
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(p.m)};
+    const int nt = m <= 8 ? 1 : 2;
+    const int64_t k = static_cast<int64_t>(kb) * 256;
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(m)};
     const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(k) * 2};
     const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(8 * nt)};
     const cuuint32_t estr[2] = {1, 1};
-    if (enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half*>(p.x), gdim, gstride, box, estr,
+    if (enc(&out->xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(x), gdim, gstride, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    return nt == 1 ? launch_nt<1>(tmap, p, s, pdl) : launch_nt<2>(tmap, p, s, pdl);
+    out->wq = wq;
+    out->y = y;
+    out->tickets = tickets;
+    out->units = units;
+    out->n = n;
+    out->kb = kb;
+    out->grid = grid;
+    return cudaSuccess;
+}
+
+cudaError_t launch(const B1Mat& single, const B1Params& p, int grid, cudaStream_t s, bool pdl, bool cooperative) {
+    return p.m <= 8 ? launch_nt<1>(single, p, grid, s, pdl, cooperative)
+                    : launch_nt<2>(single, p, grid, s, pdl, cooperative);
 }
 
 }  // namespace b1

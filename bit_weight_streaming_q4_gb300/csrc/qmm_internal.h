@@ -1,6 +1,7 @@
 // Internal declarations shared by the C-ABI layer and the kernel translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -28,19 +29,28 @@ inline int64_t piece_of(int64_t u, int64_t units, int64_t grid) {
     return ((u + 1) * grid + units - 1) / units - 1;
 }
 
-struct B1Params {
-    const uint8_t* wq;   // repacked units
-    const __half* x;     // [m, k] fp16
-    float* y;            // [m, n] fp32
-    float* ws;           // split-K partial slots [grid][2][rows][ws_cols]
-    int* tickets;        // [tiles]
-    int* err;            // sticky error word (mapped host memory)
+// One matrix of a backend-1 launch.  A single run passes it by value; a decode step keeps an
+// array of them in device memory (the tensor map needs 64-byte alignment).
+struct alignas(128) B1Mat {
+    CUtensorMap xmap;      // activations [m, k] fp16: box 64 x (8 * NT), 128-byte swizzle
+    const uint8_t* wq;     // repacked units
+    float* y;              // [m, n] fp32
+    int* tickets;          // [tiles], zero between runs
     int64_t units;
     int64_t n;
     int32_t kb;
-    int32_t m;           // rows of this launch, 1..16
-    int32_t grid;
+    int32_t grid;          // CTAs owning pieces of this matrix (fixed per handle)
+};
+
+struct B1Params {
+    const B1Mat* mats;     // device array of `count` matrices (count > 1 only)
+    float* ws;             // split-K partial slots [grid][2][256][ws_cols]
+    int* err;              // sticky error word (mapped host memory)
+    int* done;             // [count + 1] completion counters, zero between launches (count > 1)
+    int32_t count;         // matrices in this launch
+    int32_t m;             // rows of this launch, 1..16
     int32_t ws_cols;
+    int32_t pad;
 };
 
 struct B2Params {
@@ -74,7 +84,11 @@ constexpr int kUnitBytes = kRows * 144;
 constexpr int kMaxM = 16;  // rows per launch
 int smem_bytes(int nt);
 cudaError_t repack(const uint8_t* src_dev, uint8_t* dst_dev, const Decomp& d, cudaStream_t s);
-cudaError_t launch(const B1Params& p, cudaStream_t s, bool pdl);
+// Fill a matrix descriptor for a run of m rows (1..16) of x against the handle's weights.
+cudaError_t make_mat(B1Mat* out, const uint8_t* wq, const void* x, float* y, int* tickets, int64_t units,
+                     int64_t n, int32_t kb, int32_t grid, int32_t m);
+// Launch over `p.count` matrices (`single` when count == 1) on `grid` persistent CTAs.
+cudaError_t launch(const B1Mat& single, const B1Params& p, int grid, cudaStream_t s, bool pdl, bool cooperative);
 cudaError_t configure();  // one-time function attributes
 }  // namespace b1
 

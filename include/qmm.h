@@ -130,13 +130,20 @@ qmm_status qmm_destroy(qmm_handle h);
 const char* qmm_status_str(qmm_status s);
 
 /*
- * A decode step: `count` runs (handle i: x_i -> y_i, all with the same M) recorded once
- * into a CUDA graph, consecutive runs linked by programmatic dependent launch so that each
- * kernel starts streaming its weights while the previous one drains.  Each run waits for
- * the previous one to finish before it reads its x, as a layer waits for the one before.
- *  qmm_step_create: records and instantiates the graph on `stream` (synchronous).
+ * A decode step: `count` runs (handle i: x_i -> y_i, all with the same M), set up once and
+ * replayed with one call.  Each run reads its x only after the previous run has finished, as a
+ * layer waits for the one before; the weights of a run stream in while the previous one ends.
+ * Two implementations, chosen by the environment variable QMM_STEP_MODE at qmm_step_create:
+ *   default:      the runs are recorded into a CUDA graph, consecutive kernels linked by
+ *                 programmatic dependent launch;
+ *   "persistent": (mma.sync handles, M <= 16) one cooperative persistent kernel walks all
+ *                 matrices, a device-wide completion count per matrix gating the next one's
+ *                 activation loads.
+ * Both give results bit-identical to the same runs issued one by one.
+ *  qmm_step_create: builds the step (synchronous; `stream` is not used).
  *  qmm_step_launch: replays it on `stream` (asynchronous, no allocation).
- * The x_i/y_i pointers are baked into the graph; the handles must outlive the step.
+ * The x_i/y_i pointers are baked in; the handles must outlive the step, and a step must not
+ * run concurrently with another run of the same handles.
  */
 typedef struct qmm_step_s* qmm_step;
 qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handles,

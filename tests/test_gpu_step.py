@@ -1,5 +1,6 @@
-"""The recorded decode step (CUDA graph of runs with programmatic dependent launch)
-gives bit-identical results to the same runs issued one by one."""
+"""The decode step (a CUDA graph of runs linked by programmatic dependent launch, or one
+persistent kernel over all matrices) gives bit-identical results to the same runs issued one
+by one, including matrices too small to give every CTA a piece."""
 import numpy as np
 import pytest
 
@@ -10,7 +11,9 @@ from gpu_util import assert_parity, make, torch_cuda
 pytestmark = pytest.mark.gpu
 
 
-def test_step_matches_individual_runs(backend):
+@pytest.mark.parametrize("mode", ["graph", "persistent"])
+def test_step_matches_individual_runs(backend, mode, monkeypatch):
+    monkeypatch.setenv("QMM_STEP_MODE", mode)
     from bit_weight_streaming_q4_gb300 import Step
     torch = torch_cuda()
     mats = [synth.Matrix("a", 512, 1280, 1), synth.Matrix("b", 1280, 768, 2),
