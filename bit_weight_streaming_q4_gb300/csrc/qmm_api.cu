@@ -123,6 +123,7 @@ const char* qmm_status_str(qmm_status s) {
         case QMM_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
         case QMM_ERR_BAD_HANDLE: return "bad handle";
         case QMM_ERR_NO_DEVICE: return "no sm_103 device";
+        case QMM_ERR_SCRATCH_TOO_SMALL: return "shape exceeds the fixed scratch of qmm_run_noalloc";
     }
     return "unknown status";
 }

@@ -18,7 +18,8 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "qmm.h")
 QMM_OK = 0
 STATUS = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED_SHAPE",
           3: "QMM_ERR_MISALIGNED", 4: "QMM_ERR_OOM", 5: "QMM_ERR_CUDA",
-          6: "QMM_ERR_DEVICE_TIMEOUT", 7: "QMM_ERR_BAD_HANDLE", 8: "QMM_ERR_NO_DEVICE"}
+          6: "QMM_ERR_DEVICE_TIMEOUT", 7: "QMM_ERR_BAD_HANDLE", 8: "QMM_ERR_NO_DEVICE",
+          9: "QMM_ERR_SCRATCH_TOO_SMALL"}
 BACKEND_AUTO, BACKEND_MMA_SYNC, BACKEND_TCGEN05 = 0, 1, 2
 
 
@@ -77,6 +78,7 @@ def load(path: str = LIB_PATH):
                                            ctypes.POINTER(vp), ctypes.POINTER(vp), i64, vp]),
         "qmm_step_launch": (ctypes.c_int, [vp, vp]),
         "qmm_step_destroy": (ctypes.c_int, [vp]),
+        "qmm_run_noalloc": (ctypes.c_int, [vp, i64, i64, vp, i64, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -165,6 +167,15 @@ class Qmm:
             self.close()
         except Exception:
             pass
+
+
+def run_noalloc(blocks, n: int, k: int, x, y, m: int | None = None, stream: int | None = None) -> None:
+    """y[:m] = x[:m] @ W^T from raw Q4_K blocks on the device, without any allocation: the
+    library packs the weights into its fixed scratch array (see qmm_run_noalloc in qmm.h)."""
+    if m is None:
+        m = x.shape[0]
+    st = current_stream() if stream is None else stream
+    _check(load().qmm_run_noalloc(_ptr(blocks), n, k, _ptr(x), m, _ptr(y), st), "qmm_run_noalloc")
 
 
 class Step:

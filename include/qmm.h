@@ -52,7 +52,8 @@ typedef enum {
     QMM_ERR_CUDA = 5,               /* a CUDA runtime call or a launch failed */
     QMM_ERR_DEVICE_TIMEOUT = 6,     /* a kernel's bounded wait gave up (sticky, see qmm_get_error) */
     QMM_ERR_BAD_HANDLE = 7,         /* NULL, destroyed or never-created handle */
-    QMM_ERR_NO_DEVICE = 8           /* the current device is not an sm_103 GPU */
+    QMM_ERR_NO_DEVICE = 8,          /* the current device is not an sm_103 GPU */
+    QMM_ERR_SCRATCH_TOO_SMALL = 9   /* qmm_run_noalloc: the shape does not fit its fixed scratch */
 } qmm_status;
 
 enum {
@@ -150,6 +151,27 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
                            const void* const* xs, float* const* ys, int64_t m, void* stream);
 qmm_status qmm_step_launch(qmm_step s, void* stream);
 qmm_status qmm_step_destroy(qmm_step s);
+
+/*
+ * A run that allocates nothing (no counterpart on the pages: it exists for callers that
+ * cannot call cudaMalloc where they need the matmul -- a framework whose memory pool owns the
+ * device, code that must not synchronise the device, a plugin with a fixed memory budget).
+ *  blocks: the N x K weight matrix as Q4_K super-blocks, row-major (GGUF order), on the
+ *          device, 16-byte aligned; x [M, K] fp16 and y [M, N] fp32 on the device, 16-byte
+ *          aligned.  Computes the same product as qmm_run with the mma.sync kernel.
+ *  Scratch: every call packs the weights, the split-K workspace and the tile tickets into one
+ *          fixed 48 MiB device array of the library (held by every GPU that loads it, until the
+ *          process exits); the packed weights plus the workspace must fit, which allows Q4_K
+ *          matrices up to about 40 MiB -- larger shapes return QMM_ERR_SCRATCH_TOO_SMALL.
+ *          M may be any size (16 rows per launch).
+ *  The first call on each device looks up the scratch array's device address, so it must
+ *  come before any stream capture.  Calls share the array and keep its last contents (each
+ *  call clears what must start at zero): calls that overlap on the GPU race -- serialise them.
+ *  Device-side wait failures of this entry point are not reported.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, NO_DEVICE, SCRATCH_TOO_SMALL, CUDA.
+ */
+qmm_status qmm_run_noalloc(const void* blocks, int64_t n, int64_t k, const void* x, int64_t m, float* y,
+                           void* stream);
 
 #ifdef __cplusplus
 }

@@ -21,7 +21,8 @@ def test_header_declares_expected_api():
     names = Q.header_functions()
     assert names == sorted(["qmm_default_options", "qmm_create", "qmm_run", "qmm_run_host",
                             "qmm_get_error", "qmm_get_info", "qmm_destroy", "qmm_status_str",
-                            "qmm_step_create", "qmm_step_launch", "qmm_step_destroy"])
+                            "qmm_step_create", "qmm_step_launch", "qmm_step_destroy",
+                            "qmm_run_noalloc"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -34,7 +35,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(9):
+    for code in range(10):
         s = lib.qmm_status_str(code)
         assert s and s != b"unknown status"
     assert lib.qmm_status_str(99) == b"unknown status"
