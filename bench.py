@@ -128,36 +128,44 @@ class ClockSampler:
 class Stack:
     """All matrices of the step resident on the GPU, with activations and outputs."""
 
-    def __init__(self, layers: int, m_max: int, torch, seed: int = 0):
+    def __init__(self, layers: int, m_max: int, torch, seed: int = 0, wide_m: int = 0):
+        """Handles for runs of up to m_max rows (qs); with wide_m, a second set of handles for
+        runs of up to wide_m rows (qs_wide), created from the same blocks."""
         from bit_weight_streaming_q4_gb300 import Qmm
         self.torch = torch
         self.mats = synth.stack(layers)
         self.m_max = m_max
-        self.qs = []
+        rows = max(m_max, wide_m)
+        self.qs, self.qs_wide = [], []
         for mat in self.mats:
             blocks = synth.q4k_matrix(mat.n, mat.k, seed=seed, tensor_id=mat.tensor_id)
             dev = torch.from_numpy(blocks.reshape(-1)).cuda()
             self.qs.append(Qmm(dev, mat.n, mat.k, m_max=m_max))
+            if wide_m:
+                self.qs_wide.append(Qmm(dev, mat.n, mat.k, m_max=wide_m))
             del dev
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
         self.weight_bytes = sum(m.weight_bytes for m in self.mats)
-        # activations for every matrix (own stream per matrix), rows 0..m_max-1
+        # activations for every matrix (own stream per matrix), `rows` rows reserved each
         self.x_off, off = [], 0
         for mat in self.mats:
             self.x_off.append(off)
-            off += m_max * mat.k
+            off += rows * mat.k
         xh = np.empty(off, dtype=np.float16)
         for mat, o in zip(self.mats, self.x_off):
-            xh[o:o + m_max * mat.k] = synth.x_f16(m_max, mat.k, seed=seed,
-                                                    tensor_id=synth.X_ID_OFFSET + mat.tensor_id).ravel()
+            xh[o:o + rows * mat.k] = synth.x_f16(rows, mat.k, seed=seed,
+                                                  tensor_id=synth.X_ID_OFFSET + mat.tensor_id).ravel()
         self.x_host = xh
         self.x = torch.from_numpy(xh.view(np.int16)).cuda().view(torch.float16)
         self.y_off, off = [], 0
         for mat in self.mats:
             self.y_off.append(off)
-            off += m_max * mat.n
+            off += rows * mat.n
         self.y = torch.zeros(off, dtype=torch.float32, device="cuda")
+
+    def handles(self, m):
+        return self.qs if m <= self.m_max else self.qs_wide
 
     def x_ptrs(self):
         # rows 0..m-1 of matrix i start at x_off[i] (row stride K); m_max rows reserved
@@ -209,60 +217,118 @@ def sampled_parity(stack, m, rng_seed=0, rows_per_matrix=2, matrices=None):
 
 
 # ------------------------------------------------------------------------------- oracle arm
+class OracleWalk:
+    """The oracle over a walk of the step's weights: five cursors, one per matrix shape (qkv,
+    o, gate_up, down of layer 0, 1, 2, ... and lm_head), take turns running the next chunk of
+    rows of their matrix against that matrix's M activation rows.  A sample runs chunks until
+    it has taken ~target_s seconds of oracle time and continues where the last one stopped, so
+    consecutive samples cover the step's shapes in proportion."""
+
+    CHUNK_WEIGHTS = 8 << 20
+
+    def __init__(self, layers: int = synth.LAYERS, m: int = HEADLINE_M):
+        import oracle
+        oracle.build()
+        self.oracle = oracle
+        self.m = m
+        self.lists = [[synth.layer_matrices(layer)[t] for layer in range(layers)] for t in range(4)]
+        self.lists.append([synth.LM_HEAD])
+        self.cur = [[0, 0] for _ in self.lists]   # (matrix index in its list, next row)
+        self.turn = 0
+        self.seen: dict[str, int] = {}
+        self._x = {}
+        oracle.qmm(synth.q4k_matrix(64, 5120, seed=0, tensor_id=9999),
+                   synth.x_f16(m, 5120, seed=0, tensor_id=9999))  # start the thread pool
+
+    def _x_for(self, mat):
+        if mat.name not in self._x:
+            self._x = {mat.name: synth.x_f16(self.m, mat.k, seed=0,
+                                             tensor_id=synth.X_ID_OFFSET + mat.tensor_id)}
+        return self._x[mat.name]
+
+    def _chunk(self):
+        for _ in range(len(self.lists)):
+            t = self.turn
+            self.turn = (self.turn + 1) % len(self.lists)
+            i, r0 = self.cur[t]
+            if i >= len(self.lists[t]):
+                continue
+            mat = self.lists[t][i]
+            r1 = min(mat.n, r0 + max(16, self.CHUNK_WEIGHTS // mat.k))
+            self.cur[t] = [i + 1, 0] if r1 == mat.n else [i, r1]
+            return mat, r0, r1
+        self.cur = [[0, 0] for _ in self.lists]   # walked the whole step: start again
+        return self._chunk()
+
+    def sample(self, target_s: float):
+        """Returns (weights processed, oracle seconds)."""
+        w, t = 0, 0.0
+        while t < target_s:
+            mat, r0, r1 = self._chunk()
+            blocks = synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id,
+                                      rows=np.arange(r0, r1))
+            x = self._x_for(mat)
+            t0 = time.perf_counter()
+            self.oracle.qmm(blocks, x)
+            t += time.perf_counter() - t0
+            w += (r1 - r0) * mat.k
+            self.seen[mat.name] = self.seen.get(mat.name, 0) + (r1 - r0)
+        return w, t
+
+    def describe(self, w, t):
+        names = list(self.seen)
+        shown = ", ".join(f"{n}[{self.seen[n]} rows]" for n in names[:6])
+        more = f" and {len(names) - 6} more matrices" if len(names) > 6 else ""
+        return (f"M={self.m}: {shown}{more} ({w * 144 // 256 / 1e6:.1f} MB of weights, {t:.1f} s "
+                f"of oracle time); weight GB/s, the full step scaled by weight bytes")
+
+    def cores(self):
+        return self.oracle.max_threads()
+
+
 def cpu_oracle_sample(target_s: float, layers: int = synth.LAYERS, m: int = HEADLINE_M):
-    """Time the oracle on a bounded sample of the step: a contiguous block of rows of each of
-    the five matrix shapes (layer 0 and lm_head), sized so the run takes ~target_s seconds.
-    Returns weight GB/s of the oracle and a description."""
-    import oracle
-    oracle.build()
-    shapes = synth.layer_matrices(0) + [synth.LM_HEAD]
-    # calibrate on a small block
-    mat = shapes[0]
-    rows = 64
-    blocks = synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id, rows=np.arange(rows))
-    x = synth.x_f16(m, mat.k, seed=0, tensor_id=synth.X_ID_OFFSET + mat.tensor_id)
-    t0 = time.perf_counter()
-    oracle.qmm(blocks, x)
-    per_weight = (time.perf_counter() - t0) / (rows * mat.k)
-    weights_target = target_s / max(per_weight, 1e-12)
-    per_shape = weights_target / len(shapes)
-    total_w, total_t = 0, 0.0
-    parts = []
-    for mat in shapes:
-        r = int(max(16, min(mat.n, per_shape // mat.k)))
-        blocks = synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id, rows=np.arange(r))
-        x = synth.x_f16(m, mat.k, seed=0, tensor_id=synth.X_ID_OFFSET + mat.tensor_id)
-        t0 = time.perf_counter()
-        oracle.qmm(blocks, x)
-        total_t += time.perf_counter() - t0
-        total_w += r * mat.k
-        parts.append(f"{mat.name}[:{r}]")
-    gbs = total_w * 144 / 256 / total_t / 1e9
-    return {"gbs": gbs, "seconds": total_t, "cores": oracle.max_threads(),
-            "sample": f"M={m}, rows {', '.join(parts)} ({total_w * 144 // 256 / 1e6:.1f} MB of "
-                      f"weights, {total_t:.1f} s); scaled to the full step by weight bytes"}
+    walk = OracleWalk(layers, m)
+    w, t = walk.sample(target_s)
+    return {"gbs": w * 144 / 256 / t / 1e9, "seconds": t, "cores": walk.cores(),
+            "sample": walk.describe(w, t)}
+
+
+def workload_config(layers: int, m: int, weight_bytes: int) -> dict:
+    return {"workload": f"decode step M={m} (4 streams x (1 token + 2 drafts)): {layers} x "
+                        f"{{qkv 5120->8192, o 6144->5120, gate_up 5120->34816, down 17408->5120}} "
+                        f"+ lm_head 5120->151936, Q4_K 144 B/256 weights",
+            "m": m, "matrices": 4 * layers + 1, "weight_bytes": weight_bytes,
+            "l2": "inputs larger than L2 (12.7 GB of weights streamed per step; no flush)"}
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the oracle, as it stands, on the host cores.  Each step is a bounded
+    sample of the step's weights (a walk over its matrices), so that K steps take about
+    --cpu-seconds of oracle time in total."""
     if rank != 0:
         return
     full_bytes = sum(m.weight_bytes for m in synth.stack(args.layers))
-    per_step_s = max(1.0, args.cpu_seconds / max(args.steps, 1))
-    for _ in range(min(args.warmup, 1)):
-        cpu_oracle_sample(0.5)
-    samples = [cpu_oracle_sample(per_step_s) for _ in range(max(1, min(args.steps, 5)))]
-    gbs = statistics.median(s["gbs"] for s in samples)
+    per_step_s = max(0.02, args.cpu_seconds / max(args.steps, 1))
+    walk = OracleWalk(args.layers, HEADLINE_M)
+    for _ in range(args.warmup):
+        walk.sample(per_step_s)
+    walk.seen.clear()
+    w, t = 0, 0.0
+    for _ in range(args.steps):
+        dw, dt = walk.sample(per_step_s)
+        w += dw
+        t += dt
+    gbs = w * 144 / 256 / t / 1e9
     step_s = full_bytes / (gbs * 1e9)
     line = {
         "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": world,
-        "steps": len(samples), "warmup": min(args.warmup, 1), "ms_per_step": step_s * 1e3,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"decode step M={HEADLINE_M}: {args.layers} x {{qkv, o, gate_up, down}} "
-                               f"+ lm_head, Q4_K", "m": HEADLINE_M, "weight_bytes": full_bytes},
+        "config": workload_config(args.layers, HEADLINE_M, full_bytes),
         "tok_s": HEADLINE_M / step_s,
-        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": samples[0]["cores"],
-                         "kind": "oracle", "sample": samples[0]["sample"]},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": walk.cores(), "kind": "oracle",
+                         "sample": walk.describe(w, t)},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -277,8 +343,9 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-    m_max = max((HEADLINE_M,) + (() if args.no_extra else EXTRA_M))
-    stack = Stack(args.layers, m_max, torch)
+    # decode handles (mma.sync, up to 16 rows) for M = 1 and 12; tcgen05 handles for M = 64
+    wide = 0 if args.no_extra else max(m for m in EXTRA_M)
+    stack = Stack(args.layers, 16, torch, wide_m=wide if wide > 16 else 0)
     stream = torch.cuda.Stream()
     n_mats = len(stack.mats)
 
@@ -289,7 +356,7 @@ def run_ours(args, rank, world, local_rank):
 
     def measure(m, steps, warmup):
         with torch.cuda.stream(stream):
-            step = Step(stack.qs, stack.x_ptrs(), stack.y_ptrs(), m, stream=stream.cuda_stream)
+            step = Step(stack.handles(m), stack.x_ptrs(), stack.y_ptrs(), m, stream=stream.cuda_stream)
         barrier()
         t = time_graph(torch, step, steps, warmup, stream)
         step.close()
@@ -388,7 +455,11 @@ def run_ours(args, rank, world, local_rank):
             sm = tm / steps_m
             wbm, xbm, ybm = stack.bytes_for(m)
             by_m[str(m)] = {"weight_gbs": wbm / sm / 1e9, "tok_s": m / sm, "ms_per_step": sm * 1e3,
-                            "frac_of_hbm_measured": wbm / sm / 1e9 / hbm}
+                            "frac_of_hbm_measured": wbm / sm / 1e9 / hbm,
+                            "backend": int(stack.handles(m)[0].info().backend)}
+            if not args.no_parity:
+                last = len(stack.mats) - 1
+                by_m[str(m)]["parity"] = sampled_parity(stack, m, matrices=[0, 1, 2, 3, last])
 
     cpu = None
     if rank == 0:
@@ -402,11 +473,7 @@ def run_ours(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
-        "config": {"workload": f"decode step M={HEADLINE_M} (4 streams x (1 token + 2 drafts)): "
-                               f"{args.layers} x {{qkv 5120->8192, o 6144->5120, gate_up 5120->34816, "
-                               f"down 17408->5120}} + lm_head 5120->151936, Q4_K 144 B/256 weights",
-                   "m": HEADLINE_M, "matrices": n_mats, "weight_bytes": wb,
-                   "l2": "inputs larger than L2 (12.7 GB of weights streamed per step; no flush)",
+        "config": {**workload_config(args.layers, HEADLINE_M, wb),
                    "backend": int(info.backend), "ctas": int(info.grid),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "tok_s": HEADLINE_M * world / step_s,

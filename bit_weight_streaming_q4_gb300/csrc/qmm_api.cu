@@ -5,6 +5,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <set>
 #include <new>
 #include <unordered_set>
 #include <vector>
@@ -81,17 +82,16 @@ qmm_status launch_run(qmm_handle h, const void* x, int64_t m, float* y, cudaStre
             e = qmm::b2::launch(xc, K, p, s, pdl);
         } else {
             qmm::B1Mat mat;
-            e = qmm::b1::make_mat(&mat, h->wq, xc, yc, h->tickets, h->d.units, N, static_cast<int32_t>(h->d.kb),
-                                  h->d.grid, static_cast<int32_t>(mc));
+            e = qmm::b1::make_mat(&mat, h->wq, xc, yc, h->ws, h->ws_cols, h->tickets, h->d.units, N,
+                                  static_cast<int32_t>(h->d.kb), h->d.grid, static_cast<int32_t>(mc));
             if (e == cudaSuccess) {
                 qmm::B1Params p = {};
                 p.mats = nullptr;
-                p.ws = h->ws;
                 p.err = h->err_dev;
                 p.done = nullptr;
                 p.count = 1;
                 p.m = static_cast<int32_t>(mc);
-                p.ws_cols = h->ws_cols;
+                p.flags = 0;
                 e = qmm::b1::launch(mat, p, h->d.grid, s, pdl, false);
             }
         }
@@ -176,8 +176,12 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
     const int cps = opt.ctas_per_sm ? opt.ctas_per_sm : 1;
     d.grid = static_cast<int32_t>(d.units < static_cast<int64_t>(sms) * cps ? d.units
                                                                            : static_cast<int64_t>(sms) * cps);
-    const int32_t cols_cap = tc ? qmm::b2::kMaxM : qmm::b1::kMaxM;
-    h->ws_cols = opt.m_max < cols_cap ? opt.m_max : cols_cap;
+    // split-K partial slot width: tcgen05, one column per row of x (up to 64); mma.sync, the
+    // accumulator floats of a consumer thread (8 per 8-row group of x, up to 16)
+    if (tc)
+        h->ws_cols = opt.m_max < qmm::b2::kMaxM ? opt.m_max : qmm::b2::kMaxM;
+    else
+        h->ws_cols = qmm::b1::ws_floats(opt.m_max);
     h->wq_bytes = d.units * d.unit_bytes;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -295,7 +299,6 @@ struct qmm_step_s {
     cudaGraphExec_t exec = nullptr;
     // persistent path: every matrix in one cooperative launch of the mma.sync kernel
     qmm::B1Mat* mats = nullptr;   // device
-    float* ws = nullptr;
     int* done = nullptr;
     int* err_host = nullptr;
     int* err_dev = nullptr;
@@ -308,7 +311,6 @@ static void free_step(qmm_step st) {
     if (st->exec) cudaGraphExecDestroy(st->exec);
     if (st->graph) cudaGraphDestroy(st->graph);
     cudaFree(st->mats);
-    cudaFree(st->ws);
     cudaFree(st->done);
     if (st->err_host) cudaFreeHost(st->err_host);
     delete st;
@@ -317,8 +319,11 @@ static void free_step(qmm_step st) {
 extern "C" {
 
 qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handles,
-                           const void* const* xs, float* const* ys, int64_t m, void* stream) {
+                           const void* const* xs, float* const* ys, int64_t m, uint32_t flags, void* stream) {
     if (!out || count <= 0 || !handles || !xs || !ys || m < 1) return QMM_ERR_INVALID_ARG;
+    if (flags & ~static_cast<uint32_t>(QMM_STEP_INDEPENDENT | QMM_STEP_GRAPH | QMM_STEP_PERSISTENT))
+        return QMM_ERR_INVALID_ARG;
+    if ((flags & QMM_STEP_GRAPH) && (flags & QMM_STEP_PERSISTENT)) return QMM_ERR_INVALID_ARG;
     *out = nullptr;
     for (int32_t i = 0; i < count; ++i) {
         if (!live_handle(handles[i])) return QMM_ERR_BAD_HANDLE;
@@ -328,27 +333,36 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
     }
     qmm_step st = new (std::nothrow) qmm_step_s();
     if (!st) return QMM_ERR_OOM;
-    // QMM_STEP_MODE=persistent selects one persistent kernel for the whole step (mma.sync
-    // handles, up to 16 rows); the default records one launch per run into a CUDA graph.
-    const char* mode = getenv("QMM_STEP_MODE");
-    bool persistent = m <= qmm::b1::kMaxM && mode && strcmp(mode, "persistent") == 0;
+    // One persistent kernel for the whole step when the runs are independent (or the caller
+    // asks for it), every handle is an mma.sync handle and M fits one launch; a CUDA graph of
+    // runs otherwise (measured faster for dependent runs: the completion of a kernel is a
+    // cheaper device-wide barrier than counters polled from a persistent kernel).
+    bool persistent = m <= qmm::b1::kMaxM && !(flags & QMM_STEP_GRAPH) &&
+                      (flags & (QMM_STEP_INDEPENDENT | QMM_STEP_PERSISTENT));
     for (int32_t i = 0; i < count; ++i) persistent = persistent && handles[i]->backend == QMM_BACKEND_MMA_SYNC;
+    if (persistent) {
+        // a handle's tickets and partial slots serve one matrix of a launch at a time
+        std::set<qmm_handle> seen(handles, handles + count);
+        if (static_cast<int32_t>(seen.size()) != count) {
+            delete st;
+            return QMM_ERR_INVALID_ARG;
+        }
+    }
     qmm_status rc = QMM_OK;
     if (persistent) {
-        // one persistent kernel walks all matrices; matrix i+1's activations are read only
-        // after every CTA has finished matrix i
+        // One persistent kernel walks all matrices.  Dependent (default): matrix i+1's
+        // activations are read only after every CTA has finished matrix i.  Independent: the
+        // matrices overlap freely.
         std::vector<qmm::B1Mat> host(count);
         int grid = 0;
         for (int32_t i = 0; i < count && rc == QMM_OK; ++i) {
             const qmm_handle h = handles[i];
-            if (qmm::b1::make_mat(&host[i], h->wq, xs[i], ys[i], h->tickets, h->d.units, h->d.n,
+            if (qmm::b1::make_mat(&host[i], h->wq, xs[i], ys[i], h->ws, h->ws_cols, h->tickets, h->d.units, h->d.n,
                                   static_cast<int32_t>(h->d.kb), h->d.grid, static_cast<int32_t>(m)) != cudaSuccess)
                 rc = QMM_ERR_CUDA;
             grid = h->d.grid > grid ? h->d.grid : grid;
         }
-        const size_t ws_bytes = static_cast<size_t>(grid) * 2 * qmm::b1::kRows * m * sizeof(float);
         if (rc == QMM_OK && cudaMalloc(&st->mats, sizeof(qmm::B1Mat) * count) != cudaSuccess) rc = QMM_ERR_OOM;
-        if (rc == QMM_OK && cudaMalloc(&st->ws, ws_bytes) != cudaSuccess) rc = QMM_ERR_OOM;
         if (rc == QMM_OK && cudaMalloc(&st->done, sizeof(int) * (count + 1)) != cudaSuccess) rc = QMM_ERR_OOM;
         if (rc == QMM_OK && cudaHostAlloc(&st->err_host, sizeof(int), cudaHostAllocMapped) != cudaSuccess)
             rc = QMM_ERR_OOM;
@@ -362,12 +376,11 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
         if (rc == QMM_OK) {
             st->grid = grid;
             st->params.mats = st->mats;
-            st->params.ws = st->ws;
             st->params.err = st->err_dev;
             st->params.done = st->done;
             st->params.count = count;
             st->params.m = static_cast<int32_t>(m);
-            st->params.ws_cols = static_cast<int32_t>(m);
+            st->params.flags = (flags & QMM_STEP_INDEPENDENT) ? 0 : qmm::kB1Dependent;
         }
     } else {
         cudaStream_t cap = nullptr;

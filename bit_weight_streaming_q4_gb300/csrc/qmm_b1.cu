@@ -34,14 +34,20 @@
 // activation fragment is read with the same permutation.  The min-term step uses slots
 // (2t, 2t+1) for (hi, lo) of sub-block 2t and (2t+8, 2t+9) for sub-block 2t+1.
 //
-// Warp roles (one persistent CTA per SM per kernel, two CTAs may share an SM so that the
-// next kernel's weights stream in while this one finishes):
-//   warps 0-7  consumers, 32 rows each; warp 8 producer (1-D bulk copies of units, 2-D TMA
-//   of the activation tile x[0..MP-1][kb*256 .. +256] with 128-byte swizzle); warp 9 the
-//   activation sums X_j of each unit, written in fragment order for the min-term step.
-// CTA c owns the units [c*U/P, (c+1)*U/P); a row tile split between CTAs is finished by the
-// last CTA to arrive (atomic ticket), which sums the partials in CTA order.  Nothing in the
-// order of any output's arithmetic depends on M, so rows are bit-identical across batchings.
+// Warp roles (one persistent CTA per SM; 11 or 12 warps, so 168 registers per thread):
+//   warps 0-7   consumers, 32 rows each: dequantise into MMA A fragments, mma.sync, per-unit
+//               scaling, the row tile's result or split-K partial;
+//   warp 8      weight producer: 1-D bulk copies of whole units into a 4-slot ring, streaming
+//               across matrix boundaries without waiting on anything but the ring;
+//   warps 9..   one fragment warp per 8 tokens: 2-D TMA (128-byte swizzle) of its 8 activation
+//               rows of each unit, turned into MMA B fragments and sub-block sums;
+//   last warp   helper: publishes the CTA's split-K partials and (dependent steps) completed
+//               matrices with device-scope release adds, so that no consumer waits on one.
+// CTA c owns the units [c*U/P, (c+1)*U/P).  A row tile cut between CTAs pa..pb is reduced by
+// pa, which holds the tile's first units and reaches them last, at the end of its piece: the
+// others write their partials and move on; pa waits for the ticket to count them and adds them
+// to its own in CTA order.  Nothing in the order of any output's arithmetic depends on M, so
+// rows are bit-identical across batchings.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -53,26 +59,29 @@ namespace qmm {
 namespace b1 {
 
 constexpr int kWarps = 8;                       // consumer warps, 32 rows each
-constexpr int kProducerWarp = kWarps;
+constexpr int kProducerWarp = kWarps;           // weight units
 constexpr int kConsumerThreads = kWarps * 32;
 constexpr int kQBytes = kRows * 128;            // 32768
 constexpr int kWRing = 4;                       // weight slots
-constexpr int kXRing = 4;                       // activation tiles (TMA)
-constexpr int kFRing = 4;                       // activation fragments
-constexpr int kMinBlocks = 1;                   // one CTA per SM, up to 200 registers per thread
+constexpr int kXRing = 5;                       // activation slots per 8-token group
+constexpr int kFRing = 4;                       // fragment slots
+constexpr int kEv = 4;                          // consumer -> helper events in flight
+constexpr int kXBox = 8 * 128;                  // one 64-wide k box of 8 tokens (SW128)
+constexpr int kXSlot = 4 * kXBox;               // 8 tokens x 256 k
 
 template <int NT>
 struct Cfg {
-    static constexpr int kThreads = (kWarps + 1 + NT) * 32;  // consumers, producer, NT fragment warps
-    static constexpr int kMP = 8 * NT;                  // token rows per launch tile
-    static constexpr int kXBox = kMP * 128;             // one 64-wide k box
-    static constexpr int kXSlot = 4 * kXBox;            // x tile of one unit
-    static constexpr int kFragBytes = NT * 8 * 32 * 16; // [nt][word i][lane][16 B]
-    static constexpr int kFSlot = kFragBytes + NT * 32 * 8;  // + min-term fragments [nt][lane][8 B]
-    static constexpr int kXOff = kWRing * kUnitBytes;   // 1024-aligned (36864 = 36 * 1024)
-    static constexpr int kFOff = kXOff + kXRing * kXSlot;
+    static constexpr int kFragWarp0 = kProducerWarp + 1;      // NT fragment warps (one per 8 tokens)
+    static constexpr int kHelperWarp = kFragWarp0 + NT;       // publishes partials and completions
+    static constexpr int kThreads = (kHelperWarp + 1) * 32;   // 11 or 12 warps: 168 registers each
+    static constexpr int kFragBytes = NT * 8 * 32 * 16;       // [nt][word i][lane][16 B]
+    static constexpr int kFSlot = kFragBytes + NT * 32 * 8;   // + min-term fragments [nt][lane][8 B]
+    static constexpr int kXOff = kWRing * kUnitBytes;         // 1024-aligned (36864 = 36 * 1024)
+    static constexpr int kFOff = kXOff + NT * kXRing * kXSlot;
     static constexpr int kBarOff = kFOff + kFRing * kFSlot;
-    static constexpr int kSmem = kBarOff + (2 * kWRing + 2 * kXRing + 2 * kFRing) * 8 + 16 + 1024;
+    static constexpr int kNumBars = 2 * kWRing + NT * kXRing + 2 * kFRing + 2 * kEv;
+    static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
+    static_assert(kSmem <= 232448, "shared memory budget");
 };
 
 int smem_bytes(int nt) { return nt == 1 ? Cfg<1>::kSmem : Cfg<2>::kSmem; }
@@ -81,6 +90,7 @@ __device__ __forceinline__ int64_t dev_piece_of(int64_t u, int64_t units, int64_
     return ((u + 1) * grid + units - 1) / units - 1;
 }
 
+// Record a failure once: the sticky word for the host, the shared abort flag for the CTA.
 __device__ __forceinline__ void fail(int* err, volatile int* flags) {
     if (!flags[0]) {
         flags[0] = 1;
@@ -127,20 +137,30 @@ __device__ __forceinline__ void piece_of_cta(const B1Mat& M, int64_t c, int64_t&
     }
 }
 
-__device__ __forceinline__ int ld_acquire(const int* p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
 // Cursor over the CTA's units of a list of matrices, in order: matrix i, unit j of its piece.
 struct Cursor {
     int i;
     int64_t j, u0, u1;
 };
 
+// Bounded spin until *p >= target (acquire).  False on timeout or when the CTA aborts.
+__device__ __forceinline__ bool wait_count(const int* p, int target, volatile int* flags) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (ld_acquire_gpu(p) >= target) return true;
+        if (flags[0]) return false;
+        if ((it & 63u) == 63u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        __nanosleep(64);
+    }
+}
+
+// mbarrier wait whose outcome the whole warp agrees on (all lanes call it).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* flags) {
+    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, flags));
+}
+
 template <int NT>
-__global__ void __launch_bounds__(Cfg<NT>::kThreads, kMinBlocks)
+__global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     stream_kernel(const __grid_constant__ B1Mat single, const B1Params p) {
     using C = Cfg<NT>;
     extern __shared__ uint8_t smem_raw[];
@@ -151,11 +171,12 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, kMinBlocks)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
     uint64_t* wfull = bars;
     uint64_t* wempty = wfull + kWRing;
-    uint64_t* xfull = wempty + kWRing;
-    uint64_t* xempty = xfull + kXRing;
-    uint64_t* ffull = xempty + kXRing;
+    uint64_t* xfull = wempty + kWRing;      // [nt][kXRing]
+    uint64_t* ffull = xfull + NT * kXRing;
     uint64_t* fempty = ffull + kFRing;
-    volatile int* flags = reinterpret_cast<volatile int*>(fempty + kFRing);  // [0] abort [1] last
+    uint64_t* evfull = fempty + kFRing;
+    uint64_t* evempty = evfull + kEv;
+    volatile int* flags = reinterpret_cast<volatile int*>(evempty + kEv);  // [0] abort
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -163,6 +184,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, kMinBlocks)
     const int64_t c = blockIdx.x;
     const int count = p.count;
     const int ncta = static_cast<int>(gridDim.x);
+    const bool dependent = (p.flags & kB1Dependent) != 0 && count > 1;
     // matrix i of the run (a single run passes its matrix by value)
     auto mat = [&](int i) -> const B1Mat& { return count == 1 ? single : p.mats[i]; };
     auto next = [&](Cursor& k) {
@@ -185,80 +207,42 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, kMinBlocks)
             mbar_init(&wfull[i], 1);
             mbar_init(&wempty[i], kWarps);
         }
-        for (int i = 0; i < kXRing; ++i) {
-            mbar_init(&xfull[i], 1);
-            mbar_init(&xempty[i], NT);
-        }
+        for (int i = 0; i < NT * kXRing; ++i) mbar_init(&xfull[i], 1);
         for (int i = 0; i < kFRing; ++i) {
             mbar_init(&ffull[i], NT);
             mbar_init(&fempty[i], kWarps);
         }
+        for (int i = 0; i < kEv; ++i) {
+            mbar_init(&evfull[i], kWarps);
+            mbar_init(&evempty[i], 1);
+        }
         flags[0] = 0;
-        flags[1] = 0;
         fence_mbar_init();
     }
     __syncthreads();
     griddep_launch_dependents();
 
-    // ------------------------------------------------------------------ producer
+    // ------------------------------------------------------------------ weight producer
     if (warp == kProducerWarp) {
         if (lane == 0) {
+            // Weights never depend on earlier kernels: stream them from the first instruction,
+            // across matrix boundaries, limited only by the ring.
             const uint64_t pol = l2_policy_evict_first();
-            Cursor w, x;
+            Cursor w;
             first(w);
-            first(x);
-            int64_t wseq = 0, xseq = 0;
-            auto issue_w = [&]() {
-                const B1Mat& M = mat(w.i);
+            int64_t wseq = 0;
+            bool ok = true;
+            while (w.i < count) {
                 const int s = static_cast<int>(wseq % kWRing);
+                if (wseq >= kWRing && !mbar_wait_bounded(&wempty[s], ((wseq / kWRing) - 1) & 1, flags)) {
+                    ok = false;
+                    break;
+                }
+                const B1Mat& M = mat(w.i);
                 mbar_arrive_expect_tx(&wfull[s], kUnitBytes);
                 bulk_g2s(wring + s * kUnitBytes, M.wq + (w.u0 + w.j) * kUnitBytes, kUnitBytes, &wfull[s], pol);
                 ++wseq;
                 next(w);
-            };
-            // weights do not depend on the previous kernel: start streaming them right away
-            while (w.i < count && wseq < kWRing) issue_w();
-            griddep_wait();  // activations may be written by the previous kernel
-            // Keep both rings as full as their consumers allow, polling without blocking on
-            // either.  The activation tile of a matrix is loaded only once every CTA has
-            // finished the matrix before it (its input depends on that matrix's output).
-            bool ok = true;
-            int dep_ready = 0;  // matrices whose predecessor is known to be complete
-            uint64_t t0 = globaltimer_ns();
-            while (ok && (w.i < count || x.i < count) && !flags[0]) {
-                bool progress = false;
-                if (x.i < count) {
-                    bool dep = x.i <= dep_ready;
-                    if (!dep && ld_acquire(p.done + (x.i - 1)) >= ncta) {
-                        dep_ready = x.i;
-                        dep = true;
-                    }
-                    const int xs = static_cast<int>(xseq % kXRing);
-                    if (dep && (xseq < kXRing || mbar_try_wait(&xempty[xs], ((xseq / kXRing) - 1) & 1))) {
-                        const B1Mat& M = mat(x.i);
-                        if (x.j == 0) prefetch_tmap(&M.xmap);
-                        mbar_arrive_expect_tx(&xfull[xs], C::kXSlot);
-                        const int kb = static_cast<int>((x.u0 + x.j) % M.kb);
-#pragma unroll
-                        for (int b = 0; b < 4; ++b)
-                            tma_load_2d(xring + xs * C::kXSlot + b * C::kXBox, &M.xmap, kb * 256 + 64 * b, 0, &xfull[xs]);
-                        ++xseq;
-                        next(x);
-                        progress = true;
-                    }
-                }
-                if (w.i < count) {
-                    const int s = static_cast<int>(wseq % kWRing);
-                    if (mbar_try_wait(&wempty[s], ((wseq / kWRing) - 1) & 1)) {
-                        issue_w();
-                        progress = true;
-                    }
-                }
-                if (progress) {
-                    t0 = globaltimer_ns();
-                } else if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                    ok = false;
-                }
             }
             if (!ok) fail(p.err, flags);
             if (flags[0]) {
@@ -266,43 +250,82 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, kMinBlocks)
                 volatile int no_abort = 0;
                 for (int64_t j = wseq > kWRing ? wseq - kWRing : 0; j < wseq; ++j)
                     mbar_wait_bounded(&wfull[j % kWRing], (j / kWRing) & 1, &no_abort);
-                for (int64_t j = xseq > kXRing ? xseq - kXRing : 0; j < xseq; ++j)
-                    mbar_wait_bounded(&xfull[j % kXRing], (j / kXRing) & 1, &no_abort);
             }
         }
         return;
     }
 
     // ------------------------------------------------------------------ activation fragments
-    // Fragment warp nt turns the activation tile of each unit into the consumers' MMA B
-    // fragments for tokens 8nt..8nt+7 (lane (g, t) of word step i: the 4+4 activations at
-    // k = 64t + 4i' and 64t + 32 + 4i', i' = (i + 2t) % 8, in slot order) and into the
-    // min-term fragments (fp32 sums of sub-blocks 2t and 2t+1, split into fp16 hi + lo).
-    if (warp > kProducerWarp) {
+    // Fragment warp nt loads the activations of tokens 8nt..8nt+7 for each unit (2-D TMA,
+    // 128-byte swizzle, rows past M read as zero) and turns them into the consumers' MMA B
+    // fragments (lane (g, t) of word step i: the 4+4 activations at k = 64t + 4i' and
+    // 64t + 32 + 4i', i' = (i + 2t) % 8, in slot order) and into the min-term fragments (fp32
+    // sums of sub-blocks 2t and 2t+1, split into fp16 hi + lo).
+    if (warp >= C::kFragWarp0 && warp < C::kHelperWarp) {
         const int g = lane >> 2, t = lane & 3;
-        const int nt = warp - kProducerWarp - 1;  // this warp's 8-token group
+        const int nt = warp - C::kFragWarp0;
+        uint8_t* myx = xring + nt * kXRing * kXSlot;
+        uint64_t* myfull = xfull + nt * kXRing;
         int64_t total = 0;
         for (int i = 0; i < count; ++i) {
             int64_t u0, u1;
             piece_of_cta(mat(i), c, u0, u1);
             total += u1 - u0;
         }
+        Cursor xc;  // next unit whose activations are to be loaded (lane 0)
+        first(xc);
+        int64_t issued = 0;
+        int ready = 0;  // activations of matrices <= ready may be read (dependent step)
+        bool ok = true;
+        // lane 0: TMA of the next unit's activation slice into its ring slot.  In a dependent
+        // step a matrix's first slice is issued only once the matrix before it is complete;
+        // until then the warp keeps serving the units it already has.
+        auto blocked = [&]() { return dependent && xc.i > ready; };
+        auto issue = [&]() {
+            const B1Mat& M = mat(xc.i);
+            const int xs = static_cast<int>(issued % kXRing);
+            if (issued >= kXRing) fence_proxy_async_smem();  // earlier generic reads of the slot
+            mbar_arrive_expect_tx(&myfull[xs], kXSlot);
+            const int kb = static_cast<int>((xc.u0 + xc.j) % M.kb);
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                tma_load_2d(myx + xs * kXSlot + b * kXBox, &M.xmap, kb * 256 + 64 * b, 8 * nt, &myfull[xs]);
+            ++issued;
+            next(xc);
+        };
+        if (lane == 0) {
+            griddep_wait();  // activations may be written by the previous kernel
+            while (issued < total && issued < kXRing && !blocked()) issue();
+        }
+        __syncwarp();
         for (int64_t j = 0; j < total; ++j) {
             const int xs = static_cast<int>(j % kXRing);
             const int fs = static_cast<int>(j % kFRing);
-            bool ok = true;
-            if (j >= kFRing) ok = mbar_wait_bounded(&fempty[fs], ((j / kFRing) - 1) & 1, flags);
-            ok = ok && mbar_wait_bounded(&xfull[xs], (j / kXRing) & 1, flags);
-            if (!ok) fail(p.err, flags);
+            if (lane == 0 && issued == j) {
+                // unit j opens a matrix whose input was not yet known to be complete: every
+                // unit before it has been served, so waiting here cannot hold up the matrix
+                // being waited for
+                if (wait_count(p.done + (xc.i - 1), ncta, flags)) {
+                    ready = xc.i;
+                    while (issued < total && issued < j + kXRing && !blocked()) issue();
+                } else {
+                    fail(p.err, flags);
+                }
+            }
+            ok = j < kFRing || warp_wait(&fempty[fs], ((j / kFRing) - 1) & 1, flags);
+            ok = ok && warp_wait(&myfull[xs], (j / kXRing) & 1, flags);
+            if (!ok) {
+                if (lane == 0) fail(p.err, flags);
+                break;
+            }
             uint8_t* fst = fring + fs * C::kFSlot;
-            const int tok = nt * 8 + g;
-            const uint8_t* xrow = xring + xs * C::kXSlot + t * C::kXBox + tok * 128;  // box t, token row
+            const uint8_t* xrow = myx + xs * kXSlot + t * kXBox + g * 128;  // box t, token g of the group
             float x_lo = 0.f, x_hi = 0.f;
 #pragma unroll 4
             for (int i = 0; i < 8; ++i) {
                 const int ir = (i + 2 * t) & 7;
-                const uint2 vl = *reinterpret_cast<const uint2*>(xrow + (((ir >> 1) ^ (tok & 7)) * 16) + (ir & 1) * 8);
-                const uint2 vh = *reinterpret_cast<const uint2*>(xrow + (((4 + (ir >> 1)) ^ (tok & 7)) * 16) + (ir & 1) * 8);
+                const uint2 vl = *reinterpret_cast<const uint2*>(xrow + (((ir >> 1) ^ g) * 16) + (ir & 1) * 8);
+                const uint2 vh = *reinterpret_cast<const uint2*>(xrow + (((4 + (ir >> 1)) ^ g) * 16) + (ir & 1) * 8);
                 uint4 f;
                 f.x = prmt(vl.x, vl.y, 0x5410u);  // {x[4i'], x[4i'+2]}
                 f.y = prmt(vl.x, vl.y, 0x7632u);  // {x[4i'+1], x[4i'+3]}
@@ -324,8 +347,70 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, kMinBlocks)
             *reinterpret_cast<uint2*>(fst + C::kFragBytes + (nt * 32 + lane) * 8) = mt;
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&xempty[xs]);
                 mbar_arrive(&ffull[fs]);
+                while (issued < total && issued <= j + kXRing && !blocked()) issue();  // refill
+            }
+            __syncwarp();
+        }
+        if (lane == 0 && flags[0]) {
+            // failure path: let every activation copy already issued land before exiting
+            volatile int no_abort = 0;
+            for (int64_t j = issued > kXRing ? issued - kXRing : 0; j < issued; ++j)
+                mbar_wait_bounded(&myfull[j % kXRing], (j / kXRing) & 1, &no_abort);
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------------ helper
+    // Publishes, in the consumers' order, each split-K partial this CTA wrote (release add on
+    // the tile's ticket) and, in a dependent step, each matrix this CTA finished; the
+    // consumers hand over through the event ring and never wait for the device-wide write.
+    if (warp == C::kHelperWarp) {
+        if (lane == 0) {
+            int64_t ev = 0;
+            bool ok = true;
+            auto take = [&]() -> bool {
+                const int e = static_cast<int>(ev % kEv);
+                if (!mbar_wait_bounded(&evfull[e], (ev / kEv) & 1, flags)) return false;
+                return true;
+            };
+            auto give = [&]() {
+                mbar_arrive(&evempty[ev % kEv]);
+                ++ev;
+            };
+            for (int mi = 0; ok && mi < count; ++mi) {
+                const B1Mat& M = mat(mi);
+                int64_t u0, u1;
+                piece_of_cta(M, c, u0, u1);
+                if (u0 < u1) {
+                    const int64_t KB = M.kb;
+                    const int64_t tf = u0 / KB, tl = (u1 - 1) / KB;
+                    if (u0 > tf * KB) {
+                        // the first tile's first units belong to an earlier CTA: publish the partial
+                        if (!(ok = take())) break;
+                        red_add_release_gpu(M.tickets + tf, 1);
+                        give();
+                    }
+                    if (tl * KB >= u0 && u1 < (tl + 1) * KB) {
+                        // this CTA reduced its last tile: every consumer warp has read the ticket
+                        if (!(ok = take())) break;
+                        M.tickets[tl] = 0;  // ready for the next run
+                        give();
+                    }
+                }
+                if (dependent) {
+                    if (!(ok = take())) break;
+                    red_add_release_gpu(p.done + mi, 1);
+                    give();
+                }
+            }
+            if (!ok) fail(p.err, flags);
+            if (dependent && ok) {
+                // the last CTA to finish resets the completion counters for the next launch
+                if (atom_add_acq_rel_gpu(p.done + count, 1) == ncta - 1) {
+                    for (int i = 0; i <= count; ++i) p.done[i] = 0;
+                    __threadfence();
+                }
             }
         }
         return;
@@ -334,9 +419,22 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, kMinBlocks)
     // ------------------------------------------------------------------ consumers
     const int g = lane >> 2;
     const int t = lane & 3;
-    griddep_wait();  // y and the workspace may still be in use by the previous kernel
+    griddep_wait();  // y, the partial slots and the tickets may still be in use by the previous kernel
     int64_t gseq = 0;  // position in the CTA's unit sequence (ring slots and phases)
-    for (int mi = 0; mi < count; ++mi) {
+    int64_t ev = 0;    // events handed to the helper
+    bool live = true;
+    auto post = [&]() -> bool {  // hand an event to the helper (after this warp's writes)
+        const int e = static_cast<int>(ev % kEv);
+        __syncwarp();
+        if (ev >= kEv && !warp_wait(&evempty[e], ((ev / kEv) - 1) & 1, flags)) {
+            if (lane == 0) fail(p.err, flags);
+            return false;
+        }
+        if (lane == 0) mbar_arrive(&evfull[e]);
+        ++ev;
+        return true;
+    };
+    for (int mi = 0; live && mi < count; ++mi) {
         const B1Mat& M = mat(mi);
         int64_t u0, u1;
         piece_of_cta(M, c, u0, u1);
@@ -346,7 +444,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, kMinBlocks)
         const int64_t t_first = u0 < u1 ? u0 / KB : 0;
         const int64_t t_last = u0 < u1 ? (u1 - 1) / KB : -1;
         int64_t j = 0;  // piece-relative unit index
-        for (int64_t tile = t_first; tile <= t_last; ++tile) {
+        for (int64_t tile = t_first; live && tile <= t_last; ++tile) {
             const int64_t ja = (tile * KB > u0 ? tile * KB : u0) - u0;
             const int64_t jb = ((tile + 1) * KB < u1 ? (tile + 1) * KB : u1) - u0;
 
@@ -361,31 +459,33 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, kMinBlocks)
             for (; j < jb; ++j, ++gseq) {
                 const int s = static_cast<int>(gseq % kWRing);
                 const int fs = static_cast<int>(gseq % kFRing);
-                if (!mbar_wait_bounded(&wfull[s], (gseq / kWRing) & 1, flags)) fail(p.err, flags);
+                if (!warp_wait(&wfull[s], (gseq / kWRing) & 1, flags)) {
+                    if (lane == 0) fail(p.err, flags);
+                    live = false;
+                    break;
+                }
                 // this warp's words: [r][h][i4][lane][16 B], word i = 4 i4 + component
                 const uint8_t* myq = wring + s * kUnitBytes + warp * 4096;
-                uint4 qv[2][2][2];
-                uint4 hd[2][2];
-#pragma unroll
-                for (int r = 0; r < 2; ++r)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                        for (int i4 = 0; i4 < 2; ++i4)
-                            qv[r][h][i4] = *reinterpret_cast<const uint4*>(myq + (((r * 2 + h) * 2 + i4) * 32 + lane) * 16);
-                        hd[r][h] = *reinterpret_cast<const uint4*>(wring + s * kUnitBytes + kQBytes +
-                                                                   (32 * warp + 16 * r + 8 * h + g) * 16);
-                    }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&wempty[s]);
-
                 RowK rk[2][2];
 #pragma unroll
                 for (int r = 0; r < 2; ++r)
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) rk[r][h] = row_consts(hd[r][h], t);
+                    for (int h = 0; h < 2; ++h)
+                        rk[r][h] = row_consts(*reinterpret_cast<const uint4*>(
+                                                  wring + s * kUnitBytes + kQBytes + (32 * warp + 16 * r + 8 * h + g) * 16),
+                                              t);
+                uint4 qv[2][2];  // words of the current half (i4) of the unit
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        qv[r][h] = *reinterpret_cast<const uint4*>(myq + (((r * 2 + h) * 2 + 0) * 32 + lane) * 16);
 
-                if (!mbar_wait_bounded(&ffull[fs], (gseq / kFRing) & 1, flags)) fail(p.err, flags);
+                if (!warp_wait(&ffull[fs], (gseq / kFRing) & 1, flags)) {
+                    if (lane == 0) fail(p.err, flags);
+                    live = false;
+                    break;
+                }
                 const uint8_t* fst = fring + fs * C::kFSlot;
 
                 float dp[2][NT][4];
@@ -398,6 +498,16 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, kMinBlocks)
 
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {  // word i: step (i, low nibbles) then (i, high nibbles)
+                    if (i == 4) {
+                        // second half of the words; then the weight slot is no longer read
+#pragma unroll
+                        for (int r = 0; r < 2; ++r)
+#pragma unroll
+                            for (int h = 0; h < 2; ++h)
+                                qv[r][h] = *reinterpret_cast<const uint4*>(myq + (((r * 2 + h) * 2 + 1) * 32 + lane) * 16);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&wempty[s]);
+                    }
                     uint4 f[NT];
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) f[nt] = *reinterpret_cast<const uint4*>(fst + ((nt * 8 + i) * 32 + lane) * 16);
@@ -406,7 +516,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, kMinBlocks)
                         uint32_t alo[4], ahi[4];
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
-                            const uint4 qq = qv[r][h][i >> 2];
+                            const uint4 qq = qv[r][h];
                             const uint32_t w = (i & 3) == 0 ? qq.x : (i & 3) == 1 ? qq.y : (i & 3) == 2 ? qq.z : qq.w;
                             const uint32_t w8 = w >> 8;
                             const __half2 s_lo = __low2half2(as_h2(rk[r][h].s)), n_lo = __low2half2(as_h2(rk[r][h].n));
@@ -451,13 +561,66 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, kMinBlocks)
                         acc[r][nt][3] = fmaf(-dd1.y, dm[3], acc[r][nt][3]);
                     }
                 }
-        
             }
+            if (!live) break;
 
-            // ---------------- write the row tile (or its split-K partial)
+            // ---------------- the row tile: whole, reduced here, or a partial for its reducer
+            // A tile cut between CTAs pa..pb is reduced by pa, the CTA holding its first units
+            // (it reaches them last, at the end of its piece); pa+1..pb hand in partials.
             const bool whole = (ja + u0 == tile * KB) && (jb + u0 == (tile + 1) * KB);
-            const int side = (tile == t_first) ? 0 : 1;
-            float* part = p.ws + (c * 2 + side) * static_cast<int64_t>(kRows) * p.ws_cols;
+            const int64_t pa = dev_piece_of(tile * KB, U, P);
+            if (!whole && pa != c) {
+                // (only the first tile of a piece can be shared without being owned)
+                float4* part = reinterpret_cast<float4*>(M.ws + c * static_cast<int64_t>(kConsumerThreads) * M.ws_cols);
+#pragma unroll
+                for (int r = 0; r < 2; ++r)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        part[(r * NT + nt) * kConsumerThreads + tid] =
+                            make_float4(acc[r][nt][0], acc[r][nt][1], acc[r][nt][2], acc[r][nt][3]);
+                live = post();
+                continue;
+            }
+            if (!whole) {
+                // wait for the partials of CTAs pa+1..pb, then add them in that order
+                const int64_t pb = dev_piece_of((tile + 1) * KB - 1, U, P);
+                bool got = true;
+                if (lane == 0) got = wait_count(M.tickets + tile, static_cast<int>(pb - pa), flags);
+                if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+                    if (lane == 0) fail(p.err, flags);
+                    live = false;
+                    break;
+                }
+                __syncwarp();  // the other lanes' loads come after lane 0's acquire
+                constexpr int kB = NT == 1 ? 4 : 2;  // partials in flight together
+#pragma unroll 1
+                for (int64_t pc0 = pa + 1; pc0 <= pb; pc0 += kB) {
+                    float4 v[kB][2 * NT];
+#pragma unroll
+                    for (int q = 0; q < kB; ++q) {
+                        if (pc0 + q <= pb) {
+                            const float4* src = reinterpret_cast<const float4*>(
+                                M.ws + (pc0 + q) * static_cast<int64_t>(kConsumerThreads) * M.ws_cols);
+#pragma unroll
+                            for (int f = 0; f < 2 * NT; ++f) v[q][f] = __ldcg(src + f * kConsumerThreads + tid);
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < kB; ++q) {
+                        if (pc0 + q <= pb) {
+#pragma unroll
+                            for (int r = 0; r < 2; ++r)
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt) {
+                                    acc[r][nt][0] += v[q][r * NT + nt].x;
+                                    acc[r][nt][1] += v[q][r * NT + nt].y;
+                                    acc[r][nt][2] += v[q][r * NT + nt].z;
+                                    acc[r][nt][3] += v[q][r * NT + nt].w;
+                                }
+                        }
+                    }
+                }
+            }
 #pragma unroll
             for (int r = 0; r < 2; ++r)
 #pragma unroll
@@ -466,75 +629,12 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, kMinBlocks)
                     for (int e = 0; e < 4; ++e) {
                         const int row = 32 * warp + 16 * r + g + 8 * (e >> 1);
                         const int m = nt * 8 + 2 * t + (e & 1);
-                        if (m < p.m) {
-                            if (whole) {
-                                const int64_t n = tile * kRows + row;
-                                if (n < M.n) M.y[static_cast<int64_t>(m) * M.n + n] = acc[r][nt][e];
-                            } else {
-                                part[m * kRows + row] = acc[r][nt][e];
-                            }
-                        }
+                        const int64_t n = tile * kRows + row;
+                        if (m < p.m && n < M.n) M.y[static_cast<int64_t>(m) * M.n + n] = acc[r][nt][e];
                     }
-            if (!whole) {
-                __threadfence();
-                named_bar_sync(1, kConsumerThreads);
-                const int64_t pa = dev_piece_of(tile * KB, U, P);
-                const int64_t pb = dev_piece_of((tile + 1) * KB - 1, U, P);
-                if (tid == 0) {
-                    const int old = atomicAdd(&M.tickets[tile], 1);
-                    flags[1] = (old == static_cast<int>(pb - pa)) ? 1 : 0;
-                }
-                named_bar_sync(1, kConsumerThreads);
-                if (flags[1]) {
-                    __threadfence();
-                    float sum[2][NT][4];
-#pragma unroll 1
-                    for (int64_t pc = pa; pc <= pb; ++pc) {
-                        const int64_t pc_first_tile = (pc * U / P) / KB;
-                        const int sd = (tile == pc_first_tile) ? 0 : 1;
-                        const float* src = p.ws + (pc * 2 + sd) * static_cast<int64_t>(kRows) * p.ws_cols;
-#pragma unroll
-                        for (int r = 0; r < 2; ++r)
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const int row = 32 * warp + 16 * r + g + 8 * (e >> 1);
-                                    const int m = nt * 8 + 2 * t + (e & 1);
-                                    const float v = (m < p.m) ? __ldcg(src + m * kRows + row) : 0.f;
-                                    sum[r][nt][e] = (pc == pa) ? v : sum[r][nt][e] + v;
-                                }
-                    }
-#pragma unroll
-                    for (int r = 0; r < 2; ++r)
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int row = 32 * warp + 16 * r + g + 8 * (e >> 1);
-                                const int m = nt * 8 + 2 * t + (e & 1);
-                                const int64_t n = tile * kRows + row;
-                                if (m < p.m && n < M.n) M.y[static_cast<int64_t>(m) * M.n + n] = sum[r][nt][e];
-                            }
-                    if (tid == 0) M.tickets[tile] = 0;  // ready for the next run
-                }
-                named_bar_sync(1, kConsumerThreads);  // flags[1] is reused by the next tile
-            }
-
+            if (!whole) live = post();  // the helper may now reset the tile's ticket
         }
-        if (count > 1) {
-            // this CTA is done with matrix mi: count it towards the matrix's completion
-            __threadfence();
-            named_bar_sync(1, kConsumerThreads);
-            if (tid == 0) atomicAdd(p.done + mi, 1);
-        }
-    }
-    if (count > 1 && tid == 0) {
-        // the last CTA to finish resets the completion counters for the next launch
-        if (atomicAdd(p.done + count, 1) == ncta - 1) {
-            for (int i = 0; i <= count; ++i) p.done[i] = 0;
-            __threadfence();
-        }
+        if (live && dependent) live = post();  // this CTA's part of matrix mi is written
     }
 }
 
@@ -617,15 +717,15 @@ static cudaError_t launch_nt(const B1Mat& single, const B1Params& p, int grid, c
     return cudaLaunchKernelEx(&cfg, stream_kernel<NT>, single, p);
 }
 
-cudaError_t make_mat(B1Mat* out, const uint8_t* wq, const void* x, float* y, int* tickets, int64_t units,
-                     int64_t n, int32_t kb, int32_t grid, int32_t m) {
+cudaError_t make_mat(B1Mat* out, const uint8_t* wq, const void* x, float* y, float* ws, int32_t ws_cols,
+                     int* tickets, int64_t units, int64_t n, int32_t kb, int32_t grid, int32_t m) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    const int nt = m <= 8 ? 1 : 2;
+    if (ws_cols < 8 * (m <= 8 ? 1 : 2)) return cudaErrorInvalidValue;
     const int64_t k = static_cast<int64_t>(kb) * 256;
     const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(m)};
     const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(k) * 2};
-    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(8 * nt)};
+    const cuuint32_t box[2] = {64, 8};
     const cuuint32_t estr[2] = {1, 1};
     if (enc(&out->xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(x), gdim, gstride, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -633,6 +733,9 @@ cudaError_t make_mat(B1Mat* out, const uint8_t* wq, const void* x, float* y, int
         return cudaErrorInvalidValue;
     out->wq = wq;
     out->y = y;
+    out->ws = ws;
+    out->ws_cols = ws_cols;
+    out->pad = 0;
     out->tickets = tickets;
     out->units = units;
     out->n = n;

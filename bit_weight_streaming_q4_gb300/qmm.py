@@ -75,7 +75,7 @@ def load(path: str = LIB_PATH):
         "qmm_destroy": (ctypes.c_int, [vp]),
         "qmm_status_str": (ctypes.c_char_p, [ctypes.c_int]),
         "qmm_step_create": (ctypes.c_int, [ctypes.POINTER(vp), i32, ctypes.POINTER(vp),
-                                           ctypes.POINTER(vp), ctypes.POINTER(vp), i64, vp]),
+                                           ctypes.POINTER(vp), ctypes.POINTER(vp), i64, ctypes.c_uint32, vp]),
         "qmm_step_launch": (ctypes.c_int, [vp, vp]),
         "qmm_step_destroy": (ctypes.c_int, [vp]),
         "qmm_run_noalloc": (ctypes.c_int, [vp, i64, i64, vp, i64, vp, vp]),
@@ -178,10 +178,16 @@ def run_noalloc(blocks, n: int, k: int, x, y, m: int | None = None, stream: int 
     _check(load().qmm_run_noalloc(_ptr(blocks), n, k, _ptr(x), m, _ptr(y), st), "qmm_run_noalloc")
 
 
-class Step:
-    """A list of runs recorded once into a CUDA graph and replayed as one launch."""
+STEP_INDEPENDENT = 1   # no x of the step is written by one of its runs: runs may overlap
+STEP_GRAPH = 2         # force the CUDA-graph implementation
+STEP_PERSISTENT = 4    # force the persistent kernel (mma.sync handles, M <= 16)
 
-    def __init__(self, mats: list[Qmm], xs, ys, m: int, stream: int | None = None):
+
+class Step:
+    """A list of runs set up once and replayed as one launch (see qmm_step_create): one
+    persistent kernel for mma.sync handles, else a CUDA graph of runs."""
+
+    def __init__(self, mats: list[Qmm], xs, ys, m: int, stream: int | None = None, flags: int = 0):
         lib = load()
         n = len(mats)
         H = (ctypes.c_void_p * n)(*[q.handle for q in mats])
@@ -189,7 +195,7 @@ class Step:
         Y = (ctypes.c_void_p * n)(*[_ptr(y) for y in ys])
         self._s = ctypes.c_void_p()
         st = current_stream() if stream is None else stream
-        _check(lib.qmm_step_create(ctypes.byref(self._s), n, H, X, Y, m, st), "qmm_step_create")
+        _check(lib.qmm_step_create(ctypes.byref(self._s), n, H, X, Y, m, flags, st), "qmm_step_create")
         self._keep = (mats, xs, ys)
 
     def launch(self, stream: int | None = None) -> None:

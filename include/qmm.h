@@ -131,24 +131,38 @@ qmm_status qmm_destroy(qmm_handle h);
 const char* qmm_status_str(qmm_status s);
 
 /*
- * A decode step: `count` runs (handle i: x_i -> y_i, all with the same M), set up once and
- * replayed with one call.  Each run reads its x only after the previous run has finished, as a
- * layer waits for the one before; the weights of a run stream in while the previous one ends.
- * Two implementations, chosen by the environment variable QMM_STEP_MODE at qmm_step_create:
- *   default:      the runs are recorded into a CUDA graph, consecutive kernels linked by
- *                 programmatic dependent launch;
- *   "persistent": (mma.sync handles, M <= 16) one cooperative persistent kernel walks all
- *                 matrices, a device-wide completion count per matrix gating the next one's
- *                 activation loads.
- * Both give results bit-identical to the same runs issued one by one.
+ * A decode step ("How parallel decoding works" on the RTX 3090 engine page: one persistent
+ * kernel walks every weight matrix of the step): `count` runs (handle i: x_i -> y_i, all with
+ * the same M), set up once and replayed with one call.
+ *  flags = 0:                    dependent runs: run i reads x_i only after run i-1 has
+ *                                finished (as a layer waits for the one before), so x_i may be
+ *                                run i-1's output; the weights of run i stream in meanwhile.
+ *  flags = QMM_STEP_INDEPENDENT: the caller guarantees that no x_i is written by a run of
+ *                                the step; the runs overlap freely.
+ *  QMM_STEP_GRAPH / QMM_STEP_PERSISTENT: choose the implementation instead of the default.
+ * Implementations: (persistent) one cooperative persistent kernel walks all matrices, every
+ * handle an mma.sync handle, M <= 16, each handle at most once; in a dependent step a
+ * device-wide completion count per matrix gates the next one's activation loads.  (graph) the
+ * runs recorded into a CUDA graph, consecutive kernels linked by programmatic dependent launch.
+ * Default: persistent for independent steps where it applies, graph otherwise.  All give
+ * results bit-identical to the same runs issued one by one.
  *  qmm_step_create: builds the step (synchronous; `stream` is not used).
  *  qmm_step_launch: replays it on `stream` (asynchronous, no allocation).
  * The x_i/y_i pointers are baked in; the handles must outlive the step, and a step must not
  * run concurrently with another run of the same handles.
+ * Errors: INVALID_ARG (also a repeated handle in a persistent step, unknown flags),
+ * BAD_HANDLE, MISALIGNED, UNSUPPORTED_SHAPE (M > a handle's m_max), OOM, CUDA; a launch after
+ * a device-side timeout of the persistent kernel returns DEVICE_TIMEOUT.
  */
+enum {
+    QMM_STEP_INDEPENDENT = 1u,
+    QMM_STEP_GRAPH = 2u,
+    QMM_STEP_PERSISTENT = 4u
+};
 typedef struct qmm_step_s* qmm_step;
 qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handles,
-                           const void* const* xs, float* const* ys, int64_t m, void* stream);
+                           const void* const* xs, float* const* ys, int64_t m, uint32_t flags,
+                           void* stream);
 qmm_status qmm_step_launch(qmm_step s, void* stream);
 qmm_status qmm_step_destroy(qmm_step s);
 
