@@ -82,16 +82,18 @@ qmm_status launch_run(qmm_handle h, const void* x, int64_t m, float* y, cudaStre
             e = qmm::b2::launch(xc, K, p, s, pdl);
         } else {
             qmm::B1Mat mat;
-            e = qmm::b1::make_mat(&mat, h->wq, xc, yc, h->ws, h->ws_cols, h->tickets, h->d.units, N,
-                                  static_cast<int32_t>(h->d.kb), h->d.grid, static_cast<int32_t>(mc));
+            e = qmm::b1::make_mat(&mat, h->wq, xc, yc, h->tickets, h->d.units, N, static_cast<int32_t>(h->d.kb),
+                                  static_cast<int32_t>(mc));
             if (e == cudaSuccess) {
                 qmm::B1Params p = {};
                 p.mats = nullptr;
+                p.first_mat = nullptr;
+                p.ws = h->ws;
                 p.err = h->err_dev;
-                p.done = nullptr;
+                p.units = h->d.units;
                 p.count = 1;
                 p.m = static_cast<int32_t>(mc);
-                p.flags = 0;
+                p.ws_cols = h->ws_cols;
                 e = qmm::b1::launch(mat, p, h->d.grid, s, pdl, false);
             }
         }
@@ -192,7 +194,9 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
         return code;
     };
     if (cudaMalloc(&h->wq, h->wq_bytes) != cudaSuccess) return fail(QMM_ERR_OOM);
-    const size_t ws_bytes = static_cast<size_t>(d.grid) * 2 * d.rows * h->ws_cols * sizeof(float);
+    // split-K partial slots: tcgen05, two per CTA of rows x columns; mma.sync, one per CTA
+    const size_t ws_bytes = tc ? static_cast<size_t>(d.grid) * 2 * d.rows * h->ws_cols * sizeof(float)
+                               : static_cast<size_t>(d.grid) * qmm::b1::kConsumerThreads * h->ws_cols * sizeof(float);
     if (cudaMalloc(&h->ws, ws_bytes) != cudaSuccess) return fail(QMM_ERR_OOM);
     if (cudaMalloc(&h->tickets, d.tiles * sizeof(int)) != cudaSuccess) return fail(QMM_ERR_OOM);
     if (cudaMemsetAsync(h->tickets, 0, d.tiles * sizeof(int), s) != cudaSuccess) return fail(QMM_ERR_CUDA);
@@ -273,7 +277,9 @@ qmm_status qmm_get_info(qmm_handle h, qmm_info* info) {
     info->rows_per_unit = h->d.rows;
     info->weight_bytes = h->d.n * h->d.kb * 144;
     info->packed_bytes = h->wq_bytes;
-    info->workspace_bytes = static_cast<int64_t>(h->d.grid) * 2 * h->d.rows * h->ws_cols * 4 +
+    info->workspace_bytes = (h->backend == QMM_BACKEND_TCGEN05
+                                 ? static_cast<int64_t>(h->d.grid) * 2 * h->d.rows * h->ws_cols * 4
+                                 : static_cast<int64_t>(h->d.grid) * qmm::b1::kConsumerThreads * h->ws_cols * 4) +
                             h->d.tiles * 4;
     info->m_per_launch = per_launch(h);
     info->reserved = 0;
@@ -299,7 +305,8 @@ struct qmm_step_s {
     cudaGraphExec_t exec = nullptr;
     // persistent path: every matrix in one cooperative launch of the mma.sync kernel
     qmm::B1Mat* mats = nullptr;   // device
-    int* done = nullptr;
+    int32_t* first_mat = nullptr; // device, [grid]
+    float* ws = nullptr;          // split-K partial slots, one per CTA
     int* err_host = nullptr;
     int* err_dev = nullptr;
     qmm::B1Params params = {};
@@ -311,7 +318,8 @@ static void free_step(qmm_step st) {
     if (st->exec) cudaGraphExecDestroy(st->exec);
     if (st->graph) cudaGraphDestroy(st->graph);
     cudaFree(st->mats);
-    cudaFree(st->done);
+    cudaFree(st->first_mat);
+    cudaFree(st->ws);
     if (st->err_host) cudaFreeHost(st->err_host);
     delete st;
 }
@@ -321,9 +329,7 @@ extern "C" {
 qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handles,
                            const void* const* xs, float* const* ys, int64_t m, uint32_t flags, void* stream) {
     if (!out || count <= 0 || !handles || !xs || !ys || m < 1) return QMM_ERR_INVALID_ARG;
-    if (flags & ~static_cast<uint32_t>(QMM_STEP_INDEPENDENT | QMM_STEP_GRAPH | QMM_STEP_PERSISTENT))
-        return QMM_ERR_INVALID_ARG;
-    if ((flags & QMM_STEP_GRAPH) && (flags & QMM_STEP_PERSISTENT)) return QMM_ERR_INVALID_ARG;
+    if (flags & ~static_cast<uint32_t>(QMM_STEP_INDEPENDENT | QMM_STEP_GRAPH)) return QMM_ERR_INVALID_ARG;
     *out = nullptr;
     for (int32_t i = 0; i < count; ++i) {
         if (!live_handle(handles[i])) return QMM_ERR_BAD_HANDLE;
@@ -333,12 +339,10 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
     }
     qmm_step st = new (std::nothrow) qmm_step_s();
     if (!st) return QMM_ERR_OOM;
-    // One persistent kernel for the whole step when the runs are independent (or the caller
-    // asks for it), every handle is an mma.sync handle and M fits one launch; a CUDA graph of
-    // runs otherwise (measured faster for dependent runs: the completion of a kernel is a
-    // cheaper device-wide barrier than counters polled from a persistent kernel).
-    bool persistent = m <= qmm::b1::kMaxM && !(flags & QMM_STEP_GRAPH) &&
-                      (flags & (QMM_STEP_INDEPENDENT | QMM_STEP_PERSISTENT));
+    // One persistent kernel for the whole step when the runs are independent, every handle is
+    // an mma.sync handle and M fits one launch (unless QMM_STEP_GRAPH asks for the graph); a
+    // CUDA graph of runs otherwise.
+    bool persistent = m <= qmm::b1::kMaxM && !(flags & QMM_STEP_GRAPH) && (flags & QMM_STEP_INDEPENDENT);
     for (int32_t i = 0; i < count; ++i) persistent = persistent && handles[i]->backend == QMM_BACKEND_MMA_SYNC;
     if (persistent) {
         // a handle's tickets and partial slots serve one matrix of a launch at a time
@@ -350,37 +354,54 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
     }
     qmm_status rc = QMM_OK;
     if (persistent) {
-        // One persistent kernel walks all matrices.  Dependent (default): matrix i+1's
-        // activations are read only after every CTA has finished matrix i.  Independent: the
-        // matrices overlap freely.
+        // One persistent kernel: the matrices' unit sequences are concatenated and cut into one
+        // piece per CTA (stream-K over the whole step), so at most one row tile per CTA
+        // boundary is split between two CTAs.
         std::vector<qmm::B1Mat> host(count);
-        int grid = 0;
+        int64_t total = 0;
         for (int32_t i = 0; i < count && rc == QMM_OK; ++i) {
             const qmm_handle h = handles[i];
-            if (qmm::b1::make_mat(&host[i], h->wq, xs[i], ys[i], h->ws, h->ws_cols, h->tickets, h->d.units, h->d.n,
-                                  static_cast<int32_t>(h->d.kb), h->d.grid, static_cast<int32_t>(m)) != cudaSuccess)
+            if (qmm::b1::make_mat(&host[i], h->wq, xs[i], ys[i], h->tickets, h->d.units, h->d.n,
+                                  static_cast<int32_t>(h->d.kb), static_cast<int32_t>(m)) != cudaSuccess)
                 rc = QMM_ERR_CUDA;
-            grid = h->d.grid > grid ? h->d.grid : grid;
+            host[i].base = total;
+            total += h->d.units;
         }
+        int sms = 0;
+        if (rc == QMM_OK && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, handles[0]->device) != cudaSuccess)
+            rc = QMM_ERR_CUDA;
+        const int grid = static_cast<int>(total < sms ? total : sms);
+        std::vector<int32_t> firsts(grid > 0 ? grid : 1);
+        for (int c = 0, i = 0; c < grid; ++c) {
+            const int64_t g0 = c * total / grid;
+            while (host[i].base + host[i].units <= g0) ++i;
+            firsts[c] = i;
+        }
+        const int32_t ws_cols = qmm::b1::ws_floats(m);
+        const size_t ws_bytes = static_cast<size_t>(grid) * qmm::b1::kConsumerThreads * ws_cols * sizeof(float);
         if (rc == QMM_OK && cudaMalloc(&st->mats, sizeof(qmm::B1Mat) * count) != cudaSuccess) rc = QMM_ERR_OOM;
-        if (rc == QMM_OK && cudaMalloc(&st->done, sizeof(int) * (count + 1)) != cudaSuccess) rc = QMM_ERR_OOM;
+        if (rc == QMM_OK && cudaMalloc(&st->first_mat, sizeof(int32_t) * firsts.size()) != cudaSuccess) rc = QMM_ERR_OOM;
+        if (rc == QMM_OK && cudaMalloc(&st->ws, ws_bytes) != cudaSuccess) rc = QMM_ERR_OOM;
         if (rc == QMM_OK && cudaHostAlloc(&st->err_host, sizeof(int), cudaHostAllocMapped) != cudaSuccess)
             rc = QMM_ERR_OOM;
         if (rc == QMM_OK) {
             *st->err_host = 0;
             if (cudaHostGetDevicePointer(&st->err_dev, st->err_host, 0) != cudaSuccess ||
                 cudaMemcpy(st->mats, host.data(), sizeof(qmm::B1Mat) * count, cudaMemcpyHostToDevice) != cudaSuccess ||
-                cudaMemset(st->done, 0, sizeof(int) * (count + 1)) != cudaSuccess)
+                cudaMemcpy(st->first_mat, firsts.data(), sizeof(int32_t) * firsts.size(), cudaMemcpyHostToDevice) !=
+                    cudaSuccess)
                 rc = QMM_ERR_CUDA;
         }
         if (rc == QMM_OK) {
             st->grid = grid;
             st->params.mats = st->mats;
+            st->params.first_mat = st->first_mat;
+            st->params.ws = st->ws;
             st->params.err = st->err_dev;
-            st->params.done = st->done;
+            st->params.units = total;
             st->params.count = count;
             st->params.m = static_cast<int32_t>(m);
-            st->params.flags = (flags & QMM_STEP_INDEPENDENT) ? 0 : qmm::kB1Dependent;
+            st->params.ws_cols = ws_cols;
         }
     } else {
         cudaStream_t cap = nullptr;

@@ -34,20 +34,23 @@
 // activation fragment is read with the same permutation.  The min-term step uses slots
 // (2t, 2t+1) for (hi, lo) of sub-block 2t and (2t+8, 2t+9) for sub-block 2t+1.
 //
-// Warp roles (one persistent CTA per SM; 11 or 12 warps, so 168 registers per thread):
-//   warps 0-7   consumers, 32 rows each: dequantise into MMA A fragments, mma.sync, per-unit
-//               scaling, the row tile's result or split-K partial;
-//   warp 8      weight producer: 1-D bulk copies of whole units into a 4-slot ring, streaming
+// Warp roles (one persistent CTA per SM; 7 or 8 warps, so up to 255 registers per thread):
+//   warps 0-3   consumers, 64 rows each (4 m16 row tiles): dequantise into MMA A fragments,
+//               mma.sync, per-unit scaling, the row tile's result or split-K partial;
+//   warp 4      weight producer: 1-D bulk copies of whole units into a 4-slot ring, streaming
 //               across matrix boundaries without waiting on anything but the ring;
-//   warps 9..   one fragment warp per 8 tokens: 2-D TMA (128-byte swizzle) of its 8 activation
+//   warps 5..   one fragment warp per 8 tokens: 2-D TMA (128-byte swizzle) of its 8 activation
 //               rows of each unit, turned into MMA B fragments and sub-block sums;
-//   last warp   helper: publishes the CTA's split-K partials and (dependent steps) completed
-//               matrices with device-scope release adds, so that no consumer waits on one.
-// CTA c owns the units [c*U/P, (c+1)*U/P).  A row tile cut between CTAs pa..pb is reduced by
-// pa, which holds the tile's first units and reaches them last, at the end of its piece: the
-// others write their partials and move on; pa waits for the ticket to count them and adds them
-// to its own in CTA order.  Nothing in the order of any output's arithmetic depends on M, so
-// rows are bit-identical across batchings.
+//   last warp   helper: publishes the CTA's split-K partial with a device-scope release add
+//               and resets the ticket of the tile the CTA reduced, so that no consumer waits
+//               on a device-wide write.
+// Decomposition: a launch concatenates the unit sequences of its matrices (one matrix for a
+// run, every matrix of an independent decode step) and CTA c takes the units
+// [c*U/P, (c+1)*U/P).  A row tile cut between CTAs pa..pb is reduced by pa, which holds the
+// tile's first units and reaches them last, at the end of its piece: the others write their
+// partials and move on; pa waits for the ticket to count them and adds them to its own in
+// piece order.  Nothing in the order of any output's arithmetic depends on M, so rows are
+// bit-identical across batchings.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -58,9 +61,10 @@
 namespace qmm {
 namespace b1 {
 
-constexpr int kWarps = 8;                       // consumer warps, 32 rows each
+constexpr int kWarps = 4;                       // consumer warps, 64 rows each
+constexpr int kRT = 4;                          // m16 row tiles per consumer warp
 constexpr int kProducerWarp = kWarps;           // weight units
-constexpr int kConsumerThreads = kWarps * 32;
+static_assert(kConsumerThreads == kWarps * 32 && kWarps * kRT * 16 == kRows, "row split");
 constexpr int kQBytes = kRows * 128;            // 32768
 constexpr int kWRing = 4;                       // weight slots
 constexpr int kXRing = 5;                       // activation slots per 8-token group
@@ -72,8 +76,8 @@ constexpr int kXSlot = 4 * kXBox;               // 8 tokens x 256 k
 template <int NT>
 struct Cfg {
     static constexpr int kFragWarp0 = kProducerWarp + 1;      // NT fragment warps (one per 8 tokens)
-    static constexpr int kHelperWarp = kFragWarp0 + NT;       // publishes partials and completions
-    static constexpr int kThreads = (kHelperWarp + 1) * 32;   // 11 or 12 warps: 168 registers each
+    static constexpr int kHelperWarp = kFragWarp0 + NT;       // publishes partials, resets tickets
+    static constexpr int kThreads = (kHelperWarp + 1) * 32;   // 7 or 8 warps: up to 255 registers
     static constexpr int kFragBytes = NT * 8 * 32 * 16;       // [nt][word i][lane][16 B]
     static constexpr int kFSlot = kFragBytes + NT * 32 * 8;   // + min-term fragments [nt][lane][8 B]
     static constexpr int kXOff = kWRing * kUnitBytes;         // 1024-aligned (36864 = 36 * 1024)
@@ -86,6 +90,7 @@ struct Cfg {
 
 int smem_bytes(int nt) { return nt == 1 ? Cfg<1>::kSmem : Cfg<2>::kSmem; }
 
+// Piece (CTA) holding unit u of the launch's unit sequence.
 __device__ __forceinline__ int64_t dev_piece_of(int64_t u, int64_t units, int64_t grid) {
     return ((u + 1) * grid + units - 1) / units - 1;
 }
@@ -128,19 +133,10 @@ __device__ __forceinline__ RowK row_consts(uint4 hd, int t) {
     return r;
 }
 
-__device__ __forceinline__ void piece_of_cta(const B1Mat& M, int64_t c, int64_t& u0, int64_t& u1) {
-    if (c < M.grid) {
-        u0 = c * M.units / M.grid;
-        u1 = (c + 1) * M.units / M.grid;
-    } else {
-        u0 = u1 = 0;
-    }
-}
-
-// Cursor over the CTA's units of a list of matrices, in order: matrix i, unit j of its piece.
+// Position in a CTA's piece: unit j of matrix i, whose part of the piece ends at unit e.
 struct Cursor {
     int i;
-    int64_t j, u0, u1;
+    int64_t j, e;
 };
 
 // Bounded spin until *p >= target (acquire).  False on timeout or when the CTA aborts.
@@ -183,23 +179,31 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     const int lane = tid & 31;
     const int64_t c = blockIdx.x;
     const int count = p.count;
-    const int ncta = static_cast<int>(gridDim.x);
-    const bool dependent = (p.flags & kB1Dependent) != 0 && count > 1;
-    // matrix i of the run (a single run passes its matrix by value)
+    const int64_t U = p.units;                 // units of the launch, all matrices
+    const int64_t P = gridDim.x;               // pieces
+    const int64_t g0 = c * U / P, g1 = (c + 1) * U / P;  // this CTA's piece of the unit sequence
+    // matrix i of the launch (a single run passes its matrix by value)
     auto mat = [&](int i) -> const B1Mat& { return count == 1 ? single : p.mats[i]; };
-    auto next = [&](Cursor& k) {
-        ++k.j;
-        while (k.i < count && k.j >= k.u1 - k.u0) {
-            ++k.i;
-            k.j = 0;
-            if (k.i < count) piece_of_cta(mat(k.i), c, k.u0, k.u1);
+    // move k to the first matrix >= i that has units in the piece
+    auto enter = [&](Cursor& k, int i) {
+        for (; i < count; ++i) {
+            const B1Mat& M = mat(i);
+            if (M.base >= g1) break;
+            const int64_t lo = g0 > M.base ? g0 - M.base : 0;
+            const int64_t hi = g1 - M.base < M.units ? g1 - M.base : M.units;
+            if (lo < hi) {
+                k.i = i;
+                k.j = lo;
+                k.e = hi;
+                return;
+            }
         }
+        k.i = count;
+        k.j = k.e = 0;
     };
-    auto first = [&](Cursor& k) {
-        k.i = 0;
-        k.j = -1;
-        piece_of_cta(mat(0), c, k.u0, k.u1);
-        next(k);
+    auto first = [&](Cursor& k) { enter(k, count == 1 ? 0 : p.first_mat[c]); };
+    auto next = [&](Cursor& k) {
+        if (++k.j >= k.e) enter(k, k.i + 1);
     };
 
     if (tid == 0) {
@@ -232,15 +236,21 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             first(w);
             int64_t wseq = 0;
             bool ok = true;
+            int cur = -1;
+            const uint8_t* src = nullptr;  // the current matrix's next unit
             while (w.i < count) {
                 const int s = static_cast<int>(wseq % kWRing);
                 if (wseq >= kWRing && !mbar_wait_bounded(&wempty[s], ((wseq / kWRing) - 1) & 1, flags)) {
                     ok = false;
                     break;
                 }
-                const B1Mat& M = mat(w.i);
+                if (w.i != cur) {  // read the matrix's descriptor once
+                    cur = w.i;
+                    src = mat(w.i).wq + w.j * kUnitBytes;
+                }
                 mbar_arrive_expect_tx(&wfull[s], kUnitBytes);
-                bulk_g2s(wring + s * kUnitBytes, M.wq + (w.u0 + w.j) * kUnitBytes, kUnitBytes, &wfull[s], pol);
+                bulk_g2s(wring + s * kUnitBytes, src, kUnitBytes, &wfull[s], pol);
+                src += kUnitBytes;
                 ++wseq;
                 next(w);
             }
@@ -266,53 +276,41 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         const int nt = warp - C::kFragWarp0;
         uint8_t* myx = xring + nt * kXRing * kXSlot;
         uint64_t* myfull = xfull + nt * kXRing;
-        int64_t total = 0;
-        for (int i = 0; i < count; ++i) {
-            int64_t u0, u1;
-            piece_of_cta(mat(i), c, u0, u1);
-            total += u1 - u0;
-        }
         Cursor xc;  // next unit whose activations are to be loaded (lane 0)
         first(xc);
+        Cursor cc;  // next unit to turn into fragments
+        first(cc);
         int64_t issued = 0;
-        int ready = 0;  // activations of matrices <= ready may be read (dependent step)
-        bool ok = true;
-        // lane 0: TMA of the next unit's activation slice into its ring slot.  In a dependent
-        // step a matrix's first slice is issued only once the matrix before it is complete;
-        // until then the warp keeps serving the units it already has.
-        auto blocked = [&]() { return dependent && xc.i > ready; };
+        int cur = -1;   // matrix whose descriptor fields are cached (lane 0)
+        const void* xmap = nullptr;
+        int kbn = 1, kb = 0;
+        // lane 0: TMA of the next unit's activation slice into its ring slot
         auto issue = [&]() {
-            const B1Mat& M = mat(xc.i);
+            if (xc.i != cur) {  // read the matrix's descriptor once
+                const B1Mat& M = mat(xc.i);
+                cur = xc.i;
+                xmap = &M.xmap;
+                kbn = M.kb;
+                kb = static_cast<int>(xc.j % kbn);
+            }
             const int xs = static_cast<int>(issued % kXRing);
             if (issued >= kXRing) fence_proxy_async_smem();  // earlier generic reads of the slot
             mbar_arrive_expect_tx(&myfull[xs], kXSlot);
-            const int kb = static_cast<int>((xc.u0 + xc.j) % M.kb);
 #pragma unroll
-            for (int b = 0; b < 4; ++b)
-                tma_load_2d(myx + xs * kXSlot + b * kXBox, &M.xmap, kb * 256 + 64 * b, 8 * nt, &myfull[xs]);
+            for (int b = 0; b < 4; ++b) tma_load_2d(myx + xs * kXSlot + b * kXBox, xmap, kb * 256 + 64 * b, 8 * nt, &myfull[xs]);
+            kb = (kb + 1 == kbn) ? 0 : kb + 1;
             ++issued;
             next(xc);
         };
         if (lane == 0) {
             griddep_wait();  // activations may be written by the previous kernel
-            while (issued < total && issued < kXRing && !blocked()) issue();
+            while (xc.i < count && issued < kXRing) issue();
         }
         __syncwarp();
-        for (int64_t j = 0; j < total; ++j) {
+        for (int64_t j = 0; cc.i < count; ++j, next(cc)) {
             const int xs = static_cast<int>(j % kXRing);
             const int fs = static_cast<int>(j % kFRing);
-            if (lane == 0 && issued == j) {
-                // unit j opens a matrix whose input was not yet known to be complete: every
-                // unit before it has been served, so waiting here cannot hold up the matrix
-                // being waited for
-                if (wait_count(p.done + (xc.i - 1), ncta, flags)) {
-                    ready = xc.i;
-                    while (issued < total && issued < j + kXRing && !blocked()) issue();
-                } else {
-                    fail(p.err, flags);
-                }
-            }
-            ok = j < kFRing || warp_wait(&fempty[fs], ((j / kFRing) - 1) & 1, flags);
+            bool ok = j < kFRing || warp_wait(&fempty[fs], ((j / kFRing) - 1) & 1, flags);
             ok = ok && warp_wait(&myfull[xs], (j / kXRing) & 1, flags);
             if (!ok) {
                 if (lane == 0) fail(p.err, flags);
@@ -320,12 +318,12 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             }
             uint8_t* fst = fring + fs * C::kFSlot;
             const uint8_t* xrow = myx + xs * kXSlot + t * kXBox + g * 128;  // box t, token g of the group
-            float x_lo = 0.f, x_hi = 0.f;
-#pragma unroll 4
+            float sl[8], sh[8];
+#pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int ir = (i + 2 * t) & 7;
-                const uint2 vl = *reinterpret_cast<const uint2*>(xrow + (((ir >> 1) ^ g) * 16) + (ir & 1) * 8);
-                const uint2 vh = *reinterpret_cast<const uint2*>(xrow + (((4 + (ir >> 1)) ^ g) * 16) + (ir & 1) * 8);
+                const uint2 vl = lds64(xrow + (((ir >> 1) ^ g) * 16) + (ir & 1) * 8);
+                const uint2 vh = lds64(xrow + (((4 + (ir >> 1)) ^ g) * 16) + (ir & 1) * 8);
                 uint4 f;
                 f.x = prmt(vl.x, vl.y, 0x5410u);  // {x[4i'], x[4i'+2]}
                 f.y = prmt(vl.x, vl.y, 0x7632u);  // {x[4i'+1], x[4i'+3]}
@@ -334,9 +332,11 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                 *reinterpret_cast<uint4*>(fst + ((nt * 8 + i) * 32 + lane) * 16) = f;
                 const float2 a0 = __half22float2(as_h2(vl.x)), a1 = __half22float2(as_h2(vl.y));
                 const float2 b0 = __half22float2(as_h2(vh.x)), b1 = __half22float2(as_h2(vh.y));
-                x_lo += (a0.x + a0.y) + (a1.x + a1.y);
-                x_hi += (b0.x + b0.y) + (b1.x + b1.y);
+                sl[i] = (a0.x + a0.y) + (a1.x + a1.y);
+                sh[i] = (b0.x + b0.y) + (b1.x + b1.y);
             }
+            const float x_lo = ((sl[0] + sl[1]) + (sl[2] + sl[3])) + ((sl[4] + sl[5]) + (sl[6] + sl[7]));
+            const float x_hi = ((sh[0] + sh[1]) + (sh[2] + sh[3])) + ((sh[4] + sh[5]) + (sh[6] + sh[7]));
             // X = hi + lo, hi = fp16(X) saturated to the finite range, lo = fp16(X - hi)
             const float lim = 65504.f;
             const float cl = fminf(fmaxf(x_lo, -lim), lim), ch = fminf(fmaxf(x_hi, -lim), lim);
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&ffull[fs]);
-                while (issued < total && issued <= j + kXRing && !blocked()) issue();  // refill
+                if (xc.i < count) issue();  // refill this slot (unit j + kXRing)
             }
             __syncwarp();
         }
@@ -362,56 +362,44 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     }
 
     // ------------------------------------------------------------------ helper
-    // Publishes, in the consumers' order, each split-K partial this CTA wrote (release add on
-    // the tile's ticket) and, in a dependent step, each matrix this CTA finished; the
-    // consumers hand over through the event ring and never wait for the device-wide write.
+    // Publishes the CTA's split-K partial (release add on the tile's ticket) and, after the
+    // CTA reduced a tile, resets that tile's ticket; the consumers hand over through the event
+    // ring and never wait for a device-wide write.  A piece can share only its first tile
+    // without owning it (a partial) and own only its last tile without finishing it (a
+    // reduction), so each CTA has at most one of each per launch.
     if (warp == C::kHelperWarp) {
         if (lane == 0) {
             int64_t ev = 0;
             bool ok = true;
-            auto take = [&]() -> bool {
-                const int e = static_cast<int>(ev % kEv);
-                if (!mbar_wait_bounded(&evfull[e], (ev / kEv) & 1, flags)) return false;
-                return true;
-            };
+            auto take = [&]() -> bool { return mbar_wait_bounded(&evfull[ev % kEv], (ev / kEv) & 1, flags); };
             auto give = [&]() {
                 mbar_arrive(&evempty[ev % kEv]);
                 ++ev;
             };
-            for (int mi = 0; ok && mi < count; ++mi) {
-                const B1Mat& M = mat(mi);
-                int64_t u0, u1;
-                piece_of_cta(M, c, u0, u1);
-                if (u0 < u1) {
-                    const int64_t KB = M.kb;
-                    const int64_t tf = u0 / KB, tl = (u1 - 1) / KB;
-                    if (u0 > tf * KB) {
-                        // the first tile's first units belong to an earlier CTA: publish the partial
-                        if (!(ok = take())) break;
-                        red_add_release_gpu(M.tickets + tf, 1);
-                        give();
-                    }
-                    if (tl * KB >= u0 && u1 < (tl + 1) * KB) {
-                        // this CTA reduced its last tile: every consumer warp has read the ticket
-                        if (!(ok = take())) break;
-                        M.tickets[tl] = 0;  // ready for the next run
-                        give();
-                    }
-                }
-                if (dependent) {
+            Cursor k;
+            first(k);
+            bool first_part = true;
+            while (ok && k.i < count) {
+                const B1Mat& M = mat(k.i);
+                const int64_t KB = M.kb;
+                const int64_t lo = k.j, hi = k.e;
+                const int64_t tf = lo / KB, tl = (hi - 1) / KB;
+                if (first_part && lo > tf * KB) {
+                    // the first tile's first units belong to an earlier CTA: publish the partial
                     if (!(ok = take())) break;
-                    red_add_release_gpu(p.done + mi, 1);
+                    red_add_release_gpu(M.tickets + tf, 1);
                     give();
                 }
+                if (tl * KB >= lo && hi < (tl + 1) * KB) {
+                    // this CTA reduced its last tile: every consumer warp has read the ticket
+                    if (!(ok = take())) break;
+                    M.tickets[tl] = 0;  // ready for the next run
+                    give();
+                }
+                first_part = false;
+                enter(k, k.i + 1);
             }
             if (!ok) fail(p.err, flags);
-            if (dependent && ok) {
-                // the last CTA to finish resets the completion counters for the next launch
-                if (atom_add_acq_rel_gpu(p.done + count, 1) == ncta - 1) {
-                    for (int i = 0; i <= count; ++i) p.done[i] = 0;
-                    __threadfence();
-                }
-            }
         }
         return;
     }
@@ -434,29 +422,26 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         ++ev;
         return true;
     };
-    for (int mi = 0; live && mi < count; ++mi) {
-        const B1Mat& M = mat(mi);
-        int64_t u0, u1;
-        piece_of_cta(M, c, u0, u1);
+    Cursor mk;  // walks the matrices of the piece
+    first(mk);
+    while (live && mk.i < count) {
+        const B1Mat& M = mat(mk.i);
+        const int64_t u0 = mk.j, u1 = mk.e;  // this piece's units of matrix mk.i
         const int KB = M.kb;
-        const int64_t U = M.units;
-        const int64_t P = M.grid;
-        const int64_t t_first = u0 < u1 ? u0 / KB : 0;
-        const int64_t t_last = u0 < u1 ? (u1 - 1) / KB : -1;
-        int64_t j = 0;  // piece-relative unit index
-        for (int64_t tile = t_first; live && tile <= t_last; ++tile) {
-            const int64_t ja = (tile * KB > u0 ? tile * KB : u0) - u0;
-            const int64_t jb = ((tile + 1) * KB < u1 ? (tile + 1) * KB : u1) - u0;
+        const int64_t base = M.base;
+        for (int64_t tile = u0 / KB; live && tile <= (u1 - 1) / KB; ++tile) {
+            const int64_t ja = tile * KB > u0 ? tile * KB : u0;
+            const int64_t jb = (tile + 1) * KB < u1 ? (tile + 1) * KB : u1;
 
-            float acc[2][NT][4];
+            float acc[kRT][NT][4];
 #pragma unroll
-            for (int r = 0; r < 2; ++r)
+            for (int r = 0; r < kRT; ++r)
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) acc[r][nt][e] = 0.f;
 
-            for (; j < jb; ++j, ++gseq) {
+            for (int64_t j = ja; j < jb; ++j, ++gseq) {
                 const int s = static_cast<int>(gseq % kWRing);
                 const int fs = static_cast<int>(gseq % kFRing);
                 if (!warp_wait(&wfull[s], (gseq / kWRing) & 1, flags)) {
@@ -464,22 +449,20 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                     live = false;
                     break;
                 }
-                // this warp's words: [r][h][i4][lane][16 B], word i = 4 i4 + component
-                const uint8_t* myq = wring + s * kUnitBytes + warp * 4096;
-                RowK rk[2][2];
+                // this warp's words: [r][h][i4][lane][16 B], word i = 4 i4 + component (rows 64 warp + 16 r + 8 h + g)
+                const uint8_t* myq = wring + s * kUnitBytes + warp * (kRT * 2048);
+                RowK rk[kRT][2];
 #pragma unroll
-                for (int r = 0; r < 2; ++r)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-                        rk[r][h] = row_consts(*reinterpret_cast<const uint4*>(
-                                                  wring + s * kUnitBytes + kQBytes + (32 * warp + 16 * r + 8 * h + g) * 16),
-                                              t);
-                uint4 qv[2][2];  // words of the current half (i4) of the unit
-#pragma unroll
-                for (int r = 0; r < 2; ++r)
+                for (int r = 0; r < kRT; ++r)
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
-                        qv[r][h] = *reinterpret_cast<const uint4*>(myq + (((r * 2 + h) * 2 + 0) * 32 + lane) * 16);
+                        rk[r][h] = row_consts(lds128(wring + s * kUnitBytes + kQBytes + (64 * warp + 16 * r + 8 * h + g) * 16), t);
+                uint4 qv[kRT][2];  // words of the current half (i4) of the unit
+#pragma unroll
+                for (int r = 0; r < kRT; ++r)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        qv[r][h] = lds128(myq + (((r * 2 + h) * 2 + 0) * 32 + lane) * 16);
 
                 if (!warp_wait(&ffull[fs], (gseq / kFRing) & 1, flags)) {
                     if (lane == 0) fail(p.err, flags);
@@ -488,9 +471,9 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                 }
                 const uint8_t* fst = fring + fs * C::kFSlot;
 
-                float dp[2][NT][4];
+                float dp[kRT][NT][4];
 #pragma unroll
-                for (int r = 0; r < 2; ++r)
+                for (int r = 0; r < kRT; ++r)
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -501,18 +484,18 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                     if (i == 4) {
                         // second half of the words; then the weight slot is no longer read
 #pragma unroll
-                        for (int r = 0; r < 2; ++r)
+                        for (int r = 0; r < kRT; ++r)
 #pragma unroll
                             for (int h = 0; h < 2; ++h)
-                                qv[r][h] = *reinterpret_cast<const uint4*>(myq + (((r * 2 + h) * 2 + 1) * 32 + lane) * 16);
+                                qv[r][h] = lds128(myq + (((r * 2 + h) * 2 + 1) * 32 + lane) * 16);
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&wempty[s]);
                     }
                     uint4 f[NT];
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) f[nt] = *reinterpret_cast<const uint4*>(fst + ((nt * 8 + i) * 32 + lane) * 16);
+                    for (int nt = 0; nt < NT; ++nt) f[nt] = lds128(fst + ((nt * 8 + i) * 32 + lane) * 16);
 #pragma unroll
-                    for (int r = 0; r < 2; ++r) {
+                    for (int r = 0; r < kRT; ++r) {
                         uint32_t alo[4], ahi[4];
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
@@ -522,10 +505,10 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                             const __half2 s_lo = __low2half2(as_h2(rk[r][h].s)), n_lo = __low2half2(as_h2(rk[r][h].n));
                             const __half2 s_hi = __high2half2(as_h2(rk[r][h].s)), n_hi = __high2half2(as_h2(rk[r][h].n));
                             // P = sc*q, exact: code * s + n
-                            alo[h] = as_u32(__hfma2(as_h2(and_or(w, 0x000F000Fu, 0x64006400u)), s_lo, n_lo));
-                            alo[2 + h] = as_u32(__hfma2(as_h2(and_or(w8, 0x000F000Fu, 0x64006400u)), s_lo, n_lo));
-                            ahi[h] = as_u32(__hfma2(as_h2(and_or(w, 0x00F000F0u, 0x64006400u)), s_hi, n_hi));
-                            ahi[2 + h] = as_u32(__hfma2(as_h2(and_or(w8, 0x00F000F0u, 0x64006400u)), s_hi, n_hi));
+                            alo[h] = as_u32(__hfma2(as_h2(and_or_pinned(w, 0x000F000Fu, 0x64006400u)), s_lo, n_lo));
+                            alo[2 + h] = as_u32(__hfma2(as_h2(and_or_pinned(w8, 0x000F000Fu, 0x64006400u)), s_lo, n_lo));
+                            ahi[h] = as_u32(__hfma2(as_h2(and_or_pinned(w, 0x00F000F0u, 0x64006400u)), s_hi, n_hi));
+                            ahi[2 + h] = as_u32(__hfma2(as_h2(and_or_pinned(w8, 0x00F000F0u, 0x64006400u)), s_hi, n_hi));
                         }
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
@@ -538,11 +521,11 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                 // min term: sum_j m_j X_j with X split into fp16 hi + lo
                 uint2 xb[NT];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) xb[nt] = *reinterpret_cast<const uint2*>(fst + C::kFragBytes + (nt * 32 + lane) * 8);
+                for (int nt = 0; nt < NT; ++nt) xb[nt] = lds64(fst + C::kFragBytes + (nt * 32 + lane) * 8);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&fempty[fs]);
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
+                for (int r = 0; r < kRT; ++r) {
                     const __half2 m0 = as_h2(rk[r][0].m), m1 = as_h2(rk[r][1].m);
                     const uint32_t a0 = as_u32(__low2half2(m0)), a2 = as_u32(__high2half2(m0));   // row g
                     const uint32_t a1 = as_u32(__low2half2(m1)), a3 = as_u32(__high2half2(m1));   // row g+8
@@ -565,15 +548,16 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             if (!live) break;
 
             // ---------------- the row tile: whole, reduced here, or a partial for its reducer
-            // A tile cut between CTAs pa..pb is reduced by pa, the CTA holding its first units
-            // (it reaches them last, at the end of its piece); pa+1..pb hand in partials.
-            const bool whole = (ja + u0 == tile * KB) && (jb + u0 == (tile + 1) * KB);
-            const int64_t pa = dev_piece_of(tile * KB, U, P);
-            if (!whole && pa != c) {
+            // A tile cut between pieces pa..pb is reduced by pa, the CTA holding its first units
+            // (it reaches them last, at the end of its piece): the others write their partials
+            // and move on; pa waits for the ticket to count them and adds them in piece order.
+            const bool whole = (ja == tile * KB) && (jb == (tile + 1) * KB);
+            const int64_t pa = whole ? c : dev_piece_of(base + tile * KB, U, P);
+            if (pa != c) {
                 // (only the first tile of a piece can be shared without being owned)
-                float4* part = reinterpret_cast<float4*>(M.ws + c * static_cast<int64_t>(kConsumerThreads) * M.ws_cols);
+                float4* part = reinterpret_cast<float4*>(p.ws + c * static_cast<int64_t>(kConsumerThreads) * p.ws_cols);
 #pragma unroll
-                for (int r = 0; r < 2; ++r)
+                for (int r = 0; r < kRT; ++r)
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
                         part[(r * NT + nt) * kConsumerThreads + tid] =
@@ -582,8 +566,8 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                 continue;
             }
             if (!whole) {
-                // wait for the partials of CTAs pa+1..pb, then add them in that order
-                const int64_t pb = dev_piece_of((tile + 1) * KB - 1, U, P);
+                // wait for the partials of pieces pa+1..pb, then add them in that order
+                const int64_t pb = dev_piece_of(base + (tile + 1) * KB - 1, U, P);
                 bool got = true;
                 if (lane == 0) got = wait_count(M.tickets + tile, static_cast<int>(pb - pa), flags);
                 if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
@@ -592,24 +576,23 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                     break;
                 }
                 __syncwarp();  // the other lanes' loads come after lane 0's acquire
-                constexpr int kB = NT == 1 ? 4 : 2;  // partials in flight together
+                constexpr int kB = NT == 1 ? 8 : 4;  // partials whose loads are in flight together
 #pragma unroll 1
                 for (int64_t pc0 = pa + 1; pc0 <= pb; pc0 += kB) {
-                    float4 v[kB][2 * NT];
+                    float4 v[kB][kRT * NT];
 #pragma unroll
                     for (int q = 0; q < kB; ++q) {
-                        if (pc0 + q <= pb) {
-                            const float4* src = reinterpret_cast<const float4*>(
-                                M.ws + (pc0 + q) * static_cast<int64_t>(kConsumerThreads) * M.ws_cols);
+                        const int64_t pq = pc0 + q <= pb ? pc0 + q : pb;  // (loaded, not added)
+                        const float4* src = reinterpret_cast<const float4*>(
+                            p.ws + pq * static_cast<int64_t>(kConsumerThreads) * p.ws_cols);
 #pragma unroll
-                            for (int f = 0; f < 2 * NT; ++f) v[q][f] = __ldcg(src + f * kConsumerThreads + tid);
-                        }
+                        for (int f = 0; f < kRT * NT; ++f) v[q][f] = __ldcg(src + f * kConsumerThreads + tid);
                     }
 #pragma unroll
                     for (int q = 0; q < kB; ++q) {
                         if (pc0 + q <= pb) {
 #pragma unroll
-                            for (int r = 0; r < 2; ++r)
+                            for (int r = 0; r < kRT; ++r)
 #pragma unroll
                                 for (int nt = 0; nt < NT; ++nt) {
                                     acc[r][nt][0] += v[q][r * NT + nt].x;
@@ -622,19 +605,19 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                 }
             }
 #pragma unroll
-            for (int r = 0; r < 2; ++r)
+            for (int r = 0; r < kRT; ++r)
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int row = 32 * warp + 16 * r + g + 8 * (e >> 1);
+                        const int row = 64 * warp + 16 * r + g + 8 * (e >> 1);
                         const int m = nt * 8 + 2 * t + (e & 1);
                         const int64_t n = tile * kRows + row;
                         if (m < p.m && n < M.n) M.y[static_cast<int64_t>(m) * M.n + n] = acc[r][nt][e];
                     }
             if (!whole) live = post();  // the helper may now reset the tile's ticket
         }
-        if (live && dependent) live = post();  // this CTA's part of matrix mi is written
+        enter(mk, mk.i + 1);
     }
 }
 
@@ -717,11 +700,10 @@ static cudaError_t launch_nt(const B1Mat& single, const B1Params& p, int grid, c
     return cudaLaunchKernelEx(&cfg, stream_kernel<NT>, single, p);
 }
 
-cudaError_t make_mat(B1Mat* out, const uint8_t* wq, const void* x, float* y, float* ws, int32_t ws_cols,
-                     int* tickets, int64_t units, int64_t n, int32_t kb, int32_t grid, int32_t m) {
+cudaError_t make_mat(B1Mat* out, const uint8_t* wq, const void* x, float* y, int* tickets, int64_t units,
+                     int64_t n, int32_t kb, int32_t m) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    if (ws_cols < 8 * (m <= 8 ? 1 : 2)) return cudaErrorInvalidValue;
     const int64_t k = static_cast<int64_t>(kb) * 256;
     const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(m)};
     const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(k) * 2};
@@ -733,14 +715,12 @@ cudaError_t make_mat(B1Mat* out, const uint8_t* wq, const void* x, float* y, flo
         return cudaErrorInvalidValue;
     out->wq = wq;
     out->y = y;
-    out->ws = ws;
-    out->ws_cols = ws_cols;
-    out->pad = 0;
     out->tickets = tickets;
+    out->base = 0;
     out->units = units;
     out->n = n;
     out->kb = kb;
-    out->grid = grid;
+    out->pad = 0;
     return cudaSuccess;
 }
 

@@ -29,33 +29,31 @@ inline int64_t piece_of(int64_t u, int64_t units, int64_t grid) {
     return ((u + 1) * grid + units - 1) / units - 1;
 }
 
-// One matrix of a backend-1 launch.  A single run passes it by value; a decode step keeps an
-// array of them in device memory (the tensor map needs 64-byte alignment).
+// One matrix of a backend-1 launch.  A launch works on the concatenation of its matrices' unit
+// sequences (matrix i's units at base_i .. base_i + units_i - 1) and cuts it into one piece per
+// CTA; a single run has one matrix and passes it by value, a decode step keeps an array of
+// them in device memory (the tensor map needs 64-byte alignment).
 struct alignas(128) B1Mat {
     CUtensorMap xmap;      // activations [m, k] fp16: box 64 x 8 (one 8-token group), 128-byte swizzle
     const uint8_t* wq;     // repacked units
     float* y;              // [m, n] fp32
-    float* ws;             // split-K partials, one slot per CTA: [grid][ws_cols / 4][256 threads] float4
     int* tickets;          // [tiles]: partials published for the tile; zero between runs
+    int64_t base;          // first unit of this matrix in the launch's sequence
     int64_t units;
     int64_t n;
     int32_t kb;
-    int32_t grid;          // CTAs owning pieces of this matrix (fixed per handle)
-    int32_t ws_cols;       // floats per consumer thread in a partial slot (8 or 16)
     int32_t pad;
 };
 
-enum : int32_t {
-    kB1Dependent = 1,      // step: matrix i's activations are read only after matrix i-1 is complete
-};
-
 struct B1Params {
-    const B1Mat* mats;     // device array of `count` matrices (count > 1 only)
-    int* err;              // sticky error word (mapped host memory)
-    int* done;             // [count + 1] completion counters, zero between launches (dependent steps)
-    int32_t count;         // matrices in this launch
-    int32_t m;             // rows of this launch, 1..16
-    int32_t flags;         // kB1Dependent
+    const B1Mat* mats;       // device array of `count` matrices (count > 1 only)
+    const int32_t* first_mat;// [grid]: matrix holding each piece's first unit (count > 1 only)
+    float* ws;               // split-K partials, one slot per CTA: [grid][ws_cols / 4][128 threads] float4
+    int* err;                // sticky error word (mapped host memory)
+    int64_t units;           // units of all matrices of the launch
+    int32_t count;           // matrices in this launch
+    int32_t m;               // rows of this launch, 1..16
+    int32_t ws_cols;         // floats per consumer thread in a partial slot
     int32_t pad;
 };
 
@@ -88,14 +86,15 @@ namespace b1 {
 constexpr int kRows = 256;
 constexpr int kUnitBytes = kRows * 144;
 constexpr int kMaxM = 16;  // rows per launch
+constexpr int kConsumerThreads = 128;  // 4 consumer warps, 64 rows each
 // floats of a split-K partial per consumer thread for runs of up to m rows; a handle keeps
-// one such slot per CTA
-constexpr int32_t ws_floats(int64_t m) { return m > 8 ? 16 : 8; }
+// one slot of kConsumerThreads x ws_floats per CTA
+constexpr int32_t ws_floats(int64_t m) { return m > 8 ? 32 : 16; }
 int smem_bytes(int nt);
 cudaError_t repack(const uint8_t* src_dev, uint8_t* dst_dev, const Decomp& d, cudaStream_t s);
 // Fill a matrix descriptor for a run of m rows (1..16) of x against the handle's weights.
-cudaError_t make_mat(B1Mat* out, const uint8_t* wq, const void* x, float* y, float* ws, int32_t ws_cols,
-                     int* tickets, int64_t units, int64_t n, int32_t kb, int32_t grid, int32_t m);
+cudaError_t make_mat(B1Mat* out, const uint8_t* wq, const void* x, float* y, int* tickets, int64_t units,
+                     int64_t n, int32_t kb, int32_t m);
 // Launch over `p.count` matrices (`single` when count == 1) on `grid` persistent CTAs.
 cudaError_t launch(const B1Mat& single, const B1Params& p, int grid, cudaStream_t s, bool pdl, bool cooperative);
 cudaError_t configure();  // one-time function attributes

@@ -56,7 +56,7 @@ extern "C" qmm_status qmm_run_noalloc(const void* blocks, int64_t n, int64_t k, 
     if (major != 10 || minor != 3) return QMM_ERR_NO_DEVICE;
     const int64_t grid = units < sms ? units : sms;
     const int32_t cols = qmm::b1::ws_floats(m);
-    const size_t ws = align256(static_cast<size_t>(grid) * 2 * qmm::b1::kRows * cols * sizeof(float));
+    const size_t ws = align256(static_cast<size_t>(grid) * qmm::b1::kConsumerThreads * cols * sizeof(float));
     const size_t tickets = align256(static_cast<size_t>(tiles) * sizeof(int));
     const size_t need = packed + ws + tickets + 256;
     if (need > kScratchBytes) return QMM_ERR_SCRATCH_TOO_SMALL;
@@ -97,14 +97,16 @@ extern "C" qmm_status qmm_run_noalloc(const void* blocks, int64_t n, int64_t k, 
     for (int64_t r0 = 0; r0 < m; r0 += qmm::b1::kMaxM) {
         const int64_t mc = (m - r0 < qmm::b1::kMaxM) ? m - r0 : qmm::b1::kMaxM;
         qmm::B1Mat mat;
-        if (qmm::b1::make_mat(&mat, wq, static_cast<const __half*>(x) + r0 * k, y + r0 * n, wsp, cols, tk, units, n,
-                              static_cast<int32_t>(kb), static_cast<int32_t>(grid), static_cast<int32_t>(mc)) !=
-            cudaSuccess)
+        if (qmm::b1::make_mat(&mat, wq, static_cast<const __half*>(x) + r0 * k, y + r0 * n, tk, units, n,
+                              static_cast<int32_t>(kb), static_cast<int32_t>(mc)) != cudaSuccess)
             return QMM_ERR_CUDA;
         qmm::B1Params p = {};
+        p.ws = wsp;
         p.err = err;
+        p.units = units;
         p.count = 1;
         p.m = static_cast<int32_t>(mc);
+        p.ws_cols = cols;
         if (qmm::b1::launch(mat, p, static_cast<int>(grid), s, false, false) != cudaSuccess) return QMM_ERR_CUDA;
     }
     return QMM_OK;

@@ -87,6 +87,22 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint3
 }
 
 // ---------------------------------------------------------------- programmatic dependent launch
+// Shared-memory loads that stay where they are written: the scheduler may not hoist them
+// (and stretch their registers' live ranges) across the other pinned loads and mbarrier ops.
+__device__ __forceinline__ uint4 lds128(const void* p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_u32(p)));
+    return v;
+}
+
+__device__ __forceinline__ uint2 lds64(const void* p) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(smem_u32(p)));
+    return v;
+}
+
 // ---------------------------------------------------------------- device-scope counters
 // Release add: every write ordered before it (by this thread, or by others through a CTA
 // barrier or mbarrier it has waited on) is visible before the new count.
@@ -121,6 +137,14 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
 __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
     uint32_t d;
     asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// The same, pinned in program order relative to the other volatile statements (keeps the
+// scheduler from dequantising far ahead of use and running out of registers).
+__device__ __forceinline__ uint32_t and_or_pinned(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm volatile("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
     return d;
 }
 

@@ -131,21 +131,25 @@ qmm_status qmm_destroy(qmm_handle h);
 const char* qmm_status_str(qmm_status s);
 
 /*
- * A decode step ("How parallel decoding works" on the RTX 3090 engine page: one persistent
- * kernel walks every weight matrix of the step): `count` runs (handle i: x_i -> y_i, all with
- * the same M), set up once and replayed with one call.
+ * A decode step ("How parallel decoding works" on the RTX 3090 engine page: every weight
+ * matrix of the step is streamed once, all stacked rows multiplied against it): `count` runs
+ * (handle i: x_i -> y_i, all with the same M), set up once and replayed with one call.
  *  flags = 0:                    dependent runs: run i reads x_i only after run i-1 has
  *                                finished (as a layer waits for the one before), so x_i may be
- *                                run i-1's output; the weights of run i stream in meanwhile.
+ *                                run i-1's output.  The runs are recorded into a CUDA graph,
+ *                                consecutive kernels linked by programmatic dependent launch
+ *                                (the weights of run i stream in while run i-1 ends); results
+ *                                are bit-identical to the same runs issued one by one.
  *  flags = QMM_STEP_INDEPENDENT: the caller guarantees that no x_i is written by a run of
- *                                the step; the runs overlap freely.
- *  QMM_STEP_GRAPH / QMM_STEP_PERSISTENT: choose the implementation instead of the default.
- * Implementations: (persistent) one cooperative persistent kernel walks all matrices, every
- * handle an mma.sync handle, M <= 16, each handle at most once; in a dependent step a
- * device-wide completion count per matrix gates the next one's activation loads.  (graph) the
- * runs recorded into a CUDA graph, consecutive kernels linked by programmatic dependent launch.
- * Default: persistent for independent steps where it applies, graph otherwise.  All give
- * results bit-identical to the same runs issued one by one.
+ *                                the step.  When every handle is an mma.sync handle and
+ *                                M <= 16, one cooperative persistent kernel streams all the
+ *                                matrices: their unit sequences are concatenated and cut into
+ *                                one piece per CTA, so only CTA boundaries split a row tile.
+ *                                Each handle may then appear at most once.  The split-K order
+ *                                differs from that of single runs, so results agree with them
+ *                                within rounding (not bit for bit); a row's result still does
+ *                                not depend on M.
+ *  QMM_STEP_GRAPH:               use the CUDA graph even for an independent step.
  *  qmm_step_create: builds the step (synchronous; `stream` is not used).
  *  qmm_step_launch: replays it on `stream` (asynchronous, no allocation).
  * The x_i/y_i pointers are baked in; the handles must outlive the step, and a step must not
@@ -156,8 +160,7 @@ const char* qmm_status_str(qmm_status s);
  */
 enum {
     QMM_STEP_INDEPENDENT = 1u,
-    QMM_STEP_GRAPH = 2u,
-    QMM_STEP_PERSISTENT = 4u
+    QMM_STEP_GRAPH = 2u
 };
 typedef struct qmm_step_s* qmm_step;
 qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handles,
