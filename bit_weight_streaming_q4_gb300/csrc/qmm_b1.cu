@@ -30,8 +30,9 @@
 // 16-byte chunks of the swizzled activation tile (no shared-memory bank conflicts).
 //
 // MMA k-order.  For step s = 0..15 (i = s % 8, i' = (i + 2t) % 8, high = s >= 8) lane t fills
-// the MMA k slots {2t, 2t+1, 2t+8, 2t+9} with weight offsets 64t + 32*high + 4i' + {0, 2, 1, 3}; the
-// activation fragment is read with the same permutation.  The min-term step uses slots
+// the MMA k slots {2t, 2t+1, 2t+8, 2t+9} with weight offsets 64t + 32*high + 4i' + {0, 1, 2, 3}
+// (repack swaps the middle bytes of each quant word to get this order), so that each pair of
+// slots is a pair of adjacent activations.  The min-term step uses slots
 // (2t, 2t+1) for (hi, lo) of sub-block 2t and (2t+8, 2t+9) for sub-block 2t+1.
 //
 // Warp roles (one persistent CTA per SM; 7 or 8 warps, so up to 255 registers per thread):
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     // Fragment warp nt loads the activations of tokens 8nt..8nt+7 for each unit (2-D TMA,
     // 128-byte swizzle, rows past M read as zero) and turns them into the consumers' MMA B
     // fragments (lane (g, t) of word step i: the 4+4 activations at k = 64t + 4i' and
-    // 64t + 32 + 4i', i' = (i + 2t) % 8, in slot order) and into the min-term fragments (fp32
+    // 64t + 32 + 4i', i' = (i + 2t) % 8, in k order) and into the min-term fragments (fp32
     // sums of sub-blocks 2t and 2t+1, split into fp16 hi + lo).
     if (warp >= C::kFragWarp0 && warp < C::kHelperWarp) {
         const int g = lane >> 2, t = lane & 3;
@@ -324,12 +325,8 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                 const int ir = (i + 2 * t) & 7;
                 const uint2 vl = lds64(xrow + (((ir >> 1) ^ g) * 16) + (ir & 1) * 8);
                 const uint2 vh = lds64(xrow + (((4 + (ir >> 1)) ^ g) * 16) + (ir & 1) * 8);
-                uint4 f;
-                f.x = prmt(vl.x, vl.y, 0x5410u);  // {x[4i'], x[4i'+2]}
-                f.y = prmt(vl.x, vl.y, 0x7632u);  // {x[4i'+1], x[4i'+3]}
-                f.z = prmt(vh.x, vh.y, 0x5410u);
-                f.w = prmt(vh.x, vh.y, 0x7632u);
-                *reinterpret_cast<uint4*>(fst + ((nt * 8 + i) * 32 + lane) * 16) = f;
+                // slots (2t, 2t+1) and (2t+8, 2t+9) hold adjacent activation pairs
+                *reinterpret_cast<uint4*>(fst + ((nt * 8 + i) * 32 + lane) * 16) = make_uint4(vl.x, vl.y, vh.x, vh.y);
                 const float2 a0 = __half22float2(as_h2(vl.x)), a1 = __half22float2(as_h2(vl.y));
                 const float2 b0 = __half22float2(as_h2(vh.x)), b1 = __half22float2(as_h2(vh.y));
                 sl[i] = (a0.x + a0.y) + (a1.x + a1.y);
@@ -641,7 +638,9 @@ __global__ void repack_kernel(const uint8_t* __restrict__ src, uint8_t* __restri
         if (nrow < n) {
             const uint32_t* qs = reinterpret_cast<const uint32_t*>(src + (nrow * kb + b) * 144 + 16 + 32 * t);
             uint32_t wv[4];
-            for (int e = 0; e < 4; ++e) wv[e] = qs[(4 * i4 + e + 2 * t) & 7];
+            // bytes 1 and 2 of each word swapped: the low nibbles at bits 0 and 16 (and, after a
+            // shift by 8, at bits 8 and 24) are then weights k, k+1 (k+2, k+3)
+            for (int e = 0; e < 4; ++e) wv[e] = __byte_perm(qs[(4 * i4 + e + 2 * t) & 7], 0, 0x3120);
             v = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
     } else {
