@@ -65,37 +65,23 @@ qmm_status launch_run(qmm_handle h, const void* x, int64_t m, float* y, cudaStre
         const int64_t mc = (m - r0 < step) ? m - r0 : step;
         const __half* xc = reinterpret_cast<const __half*>(x) + r0 * K;
         float* yc = y + r0 * N;
-        cudaError_t e;
-        if (h->backend == QMM_BACKEND_TCGEN05) {
-            qmm::B2Params p;
-            p.wq = h->wq;
-            p.y = yc;
+        const bool tc = h->backend == QMM_BACKEND_TCGEN05;
+        qmm::MatDesc mat;
+        cudaError_t e = tc ? qmm::b2::make_mat(&mat, h->wq, xc, yc, h->tickets, h->d.units, N,
+                                               static_cast<int32_t>(h->d.kb), static_cast<int32_t>(mc))
+                           : qmm::b1::make_mat(&mat, h->wq, xc, yc, h->tickets, h->d.units, N,
+                                               static_cast<int32_t>(h->d.kb), static_cast<int32_t>(mc));
+        if (e == cudaSuccess) {
+            qmm::LaunchParams p = {};
+            p.mats = nullptr;
+            p.first_mat = nullptr;
             p.ws = h->ws;
-            p.tickets = h->tickets;
             p.err = h->err_dev;
             p.units = h->d.units;
-            p.n = N;
-            p.kb = static_cast<int32_t>(h->d.kb);
+            p.count = 1;
             p.m = static_cast<int32_t>(mc);
-            p.grid = h->d.grid;
-            p.ws_cols = h->ws_cols;
-            e = qmm::b2::launch(xc, K, p, s, pdl);
-        } else {
-            qmm::B1Mat mat;
-            e = qmm::b1::make_mat(&mat, h->wq, xc, yc, h->tickets, h->d.units, N, static_cast<int32_t>(h->d.kb),
-                                  static_cast<int32_t>(mc));
-            if (e == cudaSuccess) {
-                qmm::B1Params p = {};
-                p.mats = nullptr;
-                p.first_mat = nullptr;
-                p.ws = h->ws;
-                p.err = h->err_dev;
-                p.units = h->d.units;
-                p.count = 1;
-                p.m = static_cast<int32_t>(mc);
-                p.ws_cols = h->ws_cols;
-                e = qmm::b1::launch(mat, p, h->d.grid, s, pdl, false);
-            }
+            p.ws_cols = tc ? qmm::b2::mp_for(mc) : h->ws_cols;
+            e = tc ? qmm::b2::launch(mat, p, h->d.grid, s, pdl, false) : qmm::b1::launch(mat, p, h->d.grid, s, pdl, false);
         }
         if (e != cudaSuccess) return QMM_ERR_CUDA;
     }
@@ -181,7 +167,7 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
     // split-K partial slot width: tcgen05, one column per row of x (up to 64); mma.sync, the
     // accumulator floats of a consumer thread (8 per 8-row group of x, up to 16)
     if (tc)
-        h->ws_cols = opt.m_max < qmm::b2::kMaxM ? opt.m_max : qmm::b2::kMaxM;
+        h->ws_cols = qmm::b2::mp_for(opt.m_max < qmm::b2::kMaxM ? opt.m_max : qmm::b2::kMaxM);
     else
         h->ws_cols = qmm::b1::ws_floats(opt.m_max);
     h->wq_bytes = d.units * d.unit_bytes;
@@ -195,8 +181,10 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
     };
     if (cudaMalloc(&h->wq, h->wq_bytes) != cudaSuccess) return fail(QMM_ERR_OOM);
     // split-K partial slots: tcgen05, two per CTA of rows x columns; mma.sync, one per CTA
-    const size_t ws_bytes = tc ? static_cast<size_t>(d.grid) * 2 * d.rows * h->ws_cols * sizeof(float)
-                               : static_cast<size_t>(d.grid) * qmm::b1::kConsumerThreads * h->ws_cols * sizeof(float);
+    // split-K partial slots, one per CTA: 128 rows x up to 64 columns (tcgen05), or the
+    // accumulators of the 128 consumer threads (mma.sync)
+    const size_t ws_bytes = static_cast<size_t>(d.grid) * (tc ? qmm::b2::kRows : qmm::b1::kConsumerThreads) *
+                            h->ws_cols * sizeof(float);
     if (cudaMalloc(&h->ws, ws_bytes) != cudaSuccess) return fail(QMM_ERR_OOM);
     if (cudaMalloc(&h->tickets, d.tiles * sizeof(int)) != cudaSuccess) return fail(QMM_ERR_OOM);
     if (cudaMemsetAsync(h->tickets, 0, d.tiles * sizeof(int), s) != cudaSuccess) return fail(QMM_ERR_CUDA);
@@ -277,9 +265,9 @@ qmm_status qmm_get_info(qmm_handle h, qmm_info* info) {
     info->rows_per_unit = h->d.rows;
     info->weight_bytes = h->d.n * h->d.kb * 144;
     info->packed_bytes = h->wq_bytes;
-    info->workspace_bytes = (h->backend == QMM_BACKEND_TCGEN05
-                                 ? static_cast<int64_t>(h->d.grid) * 2 * h->d.rows * h->ws_cols * 4
-                                 : static_cast<int64_t>(h->d.grid) * qmm::b1::kConsumerThreads * h->ws_cols * 4) +
+    info->workspace_bytes = static_cast<int64_t>(h->d.grid) *
+                                (h->backend == QMM_BACKEND_TCGEN05 ? qmm::b2::kRows : qmm::b1::kConsumerThreads) *
+                                h->ws_cols * 4 +
                             h->d.tiles * 4;
     info->m_per_launch = per_launch(h);
     info->reserved = 0;
@@ -304,12 +292,13 @@ struct qmm_step_s {
     cudaGraph_t graph = nullptr;  // launch-per-run path (tcgen05 handles, or more than 16 rows)
     cudaGraphExec_t exec = nullptr;
     // persistent path: every matrix in one cooperative launch of the mma.sync kernel
-    qmm::B1Mat* mats = nullptr;   // device
+    qmm::MatDesc* mats = nullptr;   // device
     int32_t* first_mat = nullptr; // device, [grid]
     float* ws = nullptr;          // split-K partial slots, one per CTA
+    bool tcgen05 = false;         // the backend of every handle of a persistent step
     int* err_host = nullptr;
     int* err_dev = nullptr;
-    qmm::B1Params params = {};
+    qmm::LaunchParams params = {};
     int grid = 0;
 };
 
@@ -342,8 +331,11 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
     // One persistent kernel for the whole step when the runs are independent, every handle is
     // an mma.sync handle and M fits one launch (unless QMM_STEP_GRAPH asks for the graph); a
     // CUDA graph of runs otherwise.
-    bool persistent = m <= qmm::b1::kMaxM && !(flags & QMM_STEP_GRAPH) && (flags & QMM_STEP_INDEPENDENT);
-    for (int32_t i = 0; i < count; ++i) persistent = persistent && handles[i]->backend == QMM_BACKEND_MMA_SYNC;
+    const int32_t be = handles[0]->backend;
+    const bool tc = be == QMM_BACKEND_TCGEN05;
+    bool persistent = m <= (tc ? qmm::b2::kMaxM : qmm::b1::kMaxM) && !(flags & QMM_STEP_GRAPH) &&
+                      (flags & QMM_STEP_INDEPENDENT);
+    for (int32_t i = 0; i < count; ++i) persistent = persistent && handles[i]->backend == be;
     if (persistent) {
         // a handle's tickets and partial slots serve one matrix of a launch at a time
         std::set<qmm_handle> seen(handles, handles + count);
@@ -357,13 +349,16 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
         // One persistent kernel: the matrices' unit sequences are concatenated and cut into one
         // piece per CTA (stream-K over the whole step), so at most one row tile per CTA
         // boundary is split between two CTAs.
-        std::vector<qmm::B1Mat> host(count);
+        std::vector<qmm::MatDesc> host(count);
         int64_t total = 0;
         for (int32_t i = 0; i < count && rc == QMM_OK; ++i) {
             const qmm_handle h = handles[i];
-            if (qmm::b1::make_mat(&host[i], h->wq, xs[i], ys[i], h->tickets, h->d.units, h->d.n,
-                                  static_cast<int32_t>(h->d.kb), static_cast<int32_t>(m)) != cudaSuccess)
-                rc = QMM_ERR_CUDA;
+            const cudaError_t me =
+                tc ? qmm::b2::make_mat(&host[i], h->wq, xs[i], ys[i], h->tickets, h->d.units, h->d.n,
+                                       static_cast<int32_t>(h->d.kb), static_cast<int32_t>(m))
+                   : qmm::b1::make_mat(&host[i], h->wq, xs[i], ys[i], h->tickets, h->d.units, h->d.n,
+                                       static_cast<int32_t>(h->d.kb), static_cast<int32_t>(m));
+            if (me != cudaSuccess) rc = QMM_ERR_CUDA;
             host[i].base = total;
             total += h->d.units;
         }
@@ -377,9 +372,10 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
             while (host[i].base + host[i].units <= g0) ++i;
             firsts[c] = i;
         }
-        const int32_t ws_cols = qmm::b1::ws_floats(m);
-        const size_t ws_bytes = static_cast<size_t>(grid) * qmm::b1::kConsumerThreads * ws_cols * sizeof(float);
-        if (rc == QMM_OK && cudaMalloc(&st->mats, sizeof(qmm::B1Mat) * count) != cudaSuccess) rc = QMM_ERR_OOM;
+        const int32_t ws_cols = tc ? qmm::b2::mp_for(m) : qmm::b1::ws_floats(m);
+        const size_t ws_bytes = static_cast<size_t>(grid) * (tc ? qmm::b2::kRows : qmm::b1::kConsumerThreads) *
+                                ws_cols * sizeof(float);
+        if (rc == QMM_OK && cudaMalloc(&st->mats, sizeof(qmm::MatDesc) * count) != cudaSuccess) rc = QMM_ERR_OOM;
         if (rc == QMM_OK && cudaMalloc(&st->first_mat, sizeof(int32_t) * firsts.size()) != cudaSuccess) rc = QMM_ERR_OOM;
         if (rc == QMM_OK && cudaMalloc(&st->ws, ws_bytes) != cudaSuccess) rc = QMM_ERR_OOM;
         if (rc == QMM_OK && cudaHostAlloc(&st->err_host, sizeof(int), cudaHostAllocMapped) != cudaSuccess)
@@ -387,12 +383,13 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
         if (rc == QMM_OK) {
             *st->err_host = 0;
             if (cudaHostGetDevicePointer(&st->err_dev, st->err_host, 0) != cudaSuccess ||
-                cudaMemcpy(st->mats, host.data(), sizeof(qmm::B1Mat) * count, cudaMemcpyHostToDevice) != cudaSuccess ||
+                cudaMemcpy(st->mats, host.data(), sizeof(qmm::MatDesc) * count, cudaMemcpyHostToDevice) != cudaSuccess ||
                 cudaMemcpy(st->first_mat, firsts.data(), sizeof(int32_t) * firsts.size(), cudaMemcpyHostToDevice) !=
                     cudaSuccess)
                 rc = QMM_ERR_CUDA;
         }
         if (rc == QMM_OK) {
+            st->tcgen05 = tc;
             st->grid = grid;
             st->params.mats = st->mats;
             st->params.first_mat = st->first_mat;
@@ -440,8 +437,10 @@ qmm_status qmm_step_launch(qmm_step s, void* stream) {
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     if (s->mats) {
         if (*reinterpret_cast<volatile int*>(s->err_host)) return QMM_ERR_DEVICE_TIMEOUT;
-        const qmm::B1Mat unused = {};
-        return qmm::b1::launch(unused, s->params, s->grid, cs, true, true) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+        const qmm::MatDesc unused = {};
+        const cudaError_t e = s->tcgen05 ? qmm::b2::launch(unused, s->params, s->grid, cs, true, true)
+                                         : qmm::b1::launch(unused, s->params, s->grid, cs, true, true);
+        return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
     }
     return cudaGraphLaunch(s->exec, cs) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
 }

@@ -158,7 +158,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 
 template <int NT>
 __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
-    stream_kernel(const __grid_constant__ B1Mat single, const B1Params p) {
+    stream_kernel(const __grid_constant__ MatDesc single, const LaunchParams p) {
     using C = Cfg<NT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -184,11 +184,11 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     const int64_t P = gridDim.x;               // pieces
     const int64_t g0 = c * U / P, g1 = (c + 1) * U / P;  // this CTA's piece of the unit sequence
     // matrix i of the launch (a single run passes its matrix by value)
-    auto mat = [&](int i) -> const B1Mat& { return count == 1 ? single : p.mats[i]; };
+    auto mat = [&](int i) -> const MatDesc& { return count == 1 ? single : p.mats[i]; };
     // move k to the first matrix >= i that has units in the piece
     auto enter = [&](Cursor& k, int i) {
         for (; i < count; ++i) {
-            const B1Mat& M = mat(i);
+            const MatDesc& M = mat(i);
             if (M.base >= g1) break;
             const int64_t lo = g0 > M.base ? g0 - M.base : 0;
             const int64_t hi = g1 - M.base < M.units ? g1 - M.base : M.units;
@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         // lane 0: TMA of the next unit's activation slice into its ring slot
         auto issue = [&]() {
             if (xc.i != cur) {  // read the matrix's descriptor once
-                const B1Mat& M = mat(xc.i);
+                const MatDesc& M = mat(xc.i);
                 cur = xc.i;
                 xmap = &M.xmap;
                 kbn = M.kb;
@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             first(k);
             bool first_part = true;
             while (ok && k.i < count) {
-                const B1Mat& M = mat(k.i);
+                const MatDesc& M = mat(k.i);
                 const int64_t KB = M.kb;
                 const int64_t lo = k.j, hi = k.e;
                 const int64_t tf = lo / KB, tl = (hi - 1) / KB;
@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     Cursor mk;  // walks the matrices of the piece
     first(mk);
     while (live && mk.i < count) {
-        const B1Mat& M = mat(mk.i);
+        const MatDesc& M = mat(mk.i);
         const int64_t u0 = mk.j, u1 = mk.e;  // this piece's units of matrix mk.i
         const int KB = M.kb;
         const int64_t base = M.base;
@@ -682,7 +682,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 template <int NT>
-static cudaError_t launch_nt(const B1Mat& single, const B1Params& p, int grid, cudaStream_t s, bool pdl,
+static cudaError_t launch_nt(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl,
                              bool cooperative) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -699,7 +699,7 @@ static cudaError_t launch_nt(const B1Mat& single, const B1Params& p, int grid, c
     return cudaLaunchKernelEx(&cfg, stream_kernel<NT>, single, p);
 }
 
-cudaError_t make_mat(B1Mat* out, const uint8_t* wq, const void* x, float* y, int* tickets, int64_t units,
+cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, int* tickets, int64_t units,
                      int64_t n, int32_t kb, int32_t m) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
@@ -723,7 +723,7 @@ cudaError_t make_mat(B1Mat* out, const uint8_t* wq, const void* x, float* y, int
     return cudaSuccess;
 }
 
-cudaError_t launch(const B1Mat& single, const B1Params& p, int grid, cudaStream_t s, bool pdl, bool cooperative) {
+cudaError_t launch(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl, bool cooperative) {
     return p.m <= 8 ? launch_nt<1>(single, p, grid, s, pdl, cooperative)
                     : launch_nt<2>(single, p, grid, s, pdl, cooperative);
 }

@@ -2,7 +2,9 @@
 //
 // The method (page "Running 4 coding agents on one RTX 3090: a custom CUDA engine for
 // Qwen3.8-27B", section "How parallel decoding works"): every weight is read from memory
-// once per step and multiplied against all M stacked token rows while it is on chip.
+// once per step and multiplied against all M stacked token rows while it is on chip.  The
+// tensor-core instruction costs the same for any N up to 64, so this backend serves runs of
+// more than 16 rows (up to 64 per launch).
 //
 // One unit = 128 output rows x one super-block column (256 weights per row), 18432 bytes,
 // stored contiguously by repack():
@@ -13,20 +15,26 @@
 //                         shift give fp16x2 codes of consecutive weight pairs.
 //   bytes [16384, 18432): the 16-byte block headers (d, dmin, scales) of the 128 rows.
 //
-// Warp roles of a persistent CTA (one per SM):
+// Warp roles of a persistent CTA (one per SM, 16 warps):
 //   warps 0-7   dequantisation, two groups of four; group g takes the units j = g (mod 2)
 //               of the CTA's piece, one output row per thread (warp w owns tensor-memory
 //               lanes 32(w%4)..+31), and writes fp16 weights into the group's A buffer in
 //               tensor memory;
-//   warp 8      producer: 1-D bulk copies of the units into a shared-memory ring, 2-D TMA
-//               loads (128-byte swizzle) of the activation tiles x[0..MP-1][kb*256..+256];
-//   warp 9      per-sub-block activation sums and the tcgen05.mma issue: A = weights in
-//               tensor memory (M = 128 rows), B = x in shared memory (N = MP tokens), fp32
-//               accumulators in tensor memory, double-buffered per row tile;
-//   warps 10-13 epilogue: accumulators -> y, or a split-K partial that the last CTA to
-//               finish the row tile sums in CTA order.
-// The piece of units of each CTA and every reduction order depend only on (N, K, grid),
-// never on M, so each row's result is bit-identical across batchings.
+//   warp 8      weight producer: 1-D bulk copies of the units into a shared-memory ring,
+//               across matrix boundaries;
+//   warp 9      activations: 2-D TMA (128-byte swizzle) of x[0..MP-1][kb*256..+256] for each
+//               unit (the dequantising group also forms the unit's per-sub-block activation
+//               sums for the correction step);
+//   warp 10     tcgen05.mma issue (one thread): A = weights in tensor memory (M = 128 rows),
+//               B = x in shared memory (N = MP tokens), fp32 accumulators in tensor memory,
+//               double-buffered per row tile;
+//   warps 11-14 epilogue: accumulators -> y, a split-K partial, or the reduction of a split
+//               row tile;
+//   warp 15     helper: publishes the CTA's partial and resets the ticket of the tile it
+//               reduced.
+// Decomposition as in the mma.sync backend: a launch concatenates its matrices' unit
+// sequences, CTA c takes [c*U/P, (c+1)*U/P), and a row tile cut between CTAs pa..pb is
+// reduced by pa in piece order.  Nothing in any output's arithmetic depends on M.
 //
 // Dequantisation, exact to ~1 ulp of fp16 for every input: with code c = 1024 + q (or
 // 1024 + 16q), P = sc*q is exact from one fp16 FMA; B = dmin*m splits error-free into
@@ -47,32 +55,36 @@ constexpr int kQBytes = kRows * 128;
 constexpr int kGroups = 2;                 // dequant warp groups
 constexpr int kDqWarps = 4 * kGroups;
 constexpr int kProducerWarp = kDqWarps;    // 8
-constexpr int kMmaWarp = kDqWarps + 1;     // 9
-constexpr int kEpiWarp0 = kDqWarps + 2;    // 10..13
-constexpr int kThreads = (kEpiWarp0 + 4) * 32;  // 448
+constexpr int kXWarp = kDqWarps + 1;       // 9
+constexpr int kMmaWarp = kDqWarps + 2;     // 10
+constexpr int kEpiWarp0 = kDqWarps + 3;    // 11..14
+constexpr int kHelperWarp = kEpiWarp0 + 4; // 15
+constexpr int kThreads = (kHelperWarp + 1) * 32;  // 512: 128 registers per thread
+constexpr int kEpiThreads = 128;
 constexpr int kTmemCols = 512;
 constexpr int kACols = 136;  // one unit: 128 columns of weights + 8 of the -B_l step
 constexpr int kNA = kGroups; // one A buffer per group
-constexpr int kWRing = 4;
-static_assert(kWRing % kGroups == 0, "a weight slot must always feed the same group");
+constexpr int kEv = 4;
 // named barriers
-constexpr int kBarEpi = 1, kBarTmem = 2, kBarTeardown = 3;
+constexpr int kBarTmem = 1, kBarTeardown = 2;
 constexpr int kTmemUsers = (kDqWarps + 1 + 4) * 32;  // dequant + MMA + epilogue warps
-constexpr int kTeardownThreads = (1 + 4) * 32;       // MMA + epilogue warps
 
 template <int MP>
 struct Cfg {
-    static constexpr int kXRing = MP <= 16 ? 4 : 2;
+    static constexpr int kWRing = MP <= 32 ? 6 : 4;   // weight slots (a multiple of kGroups)
+    static constexpr int kXRing = 4;
     static constexpr int kXBox = MP * 128;    // one 64-wide k box of x
     static constexpr int kXSlot = 4 * kXBox;  // x tile of one unit
     static constexpr int kXsBytes = MP * 32;  // the B tile of the -B_l step: [MP tokens][16 k]
     static constexpr int kAccCol = kNA * kACols;
     static_assert(kAccCol + 2 * MP <= kTmemCols, "tensor memory budget");
+    static_assert(kWRing % kGroups == 0, "a weight slot must always feed the same group");
     static constexpr int kWOff = kXRing * kXSlot;
     static constexpr int kXsOff = kWOff + kWRing * kUnitBytes;
     static constexpr int kBarOff = kXsOff + kXRing * kXsBytes;
-    static constexpr int kNumBars = 2 * kWRing + 2 * kXRing + 2 * kNA + 4;
+    static constexpr int kNumBars = 2 * kWRing + 2 * kXRing + 2 * kNA + 4 + 2 * kEv + 1;
     static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
+    static_assert(kSmem <= 232448, "shared memory budget");
 };
 
 __device__ __forceinline__ int64_t dev_piece_of(int64_t u, int64_t units, int64_t grid) {
@@ -85,6 +97,25 @@ __device__ __forceinline__ void fail(int* err, volatile int* flags) {
         atomicOr(err, 1);
     }
 }
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* flags) {
+    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, flags));
+}
+
+__device__ __forceinline__ bool wait_count(const int* p, int target, volatile int* flags) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (ld_acquire_gpu(p) >= target) return true;
+        if (flags[0]) return false;
+        if ((it & 63u) == 63u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        __nanosleep(64);
+    }
+}
+
+struct Cursor {
+    int i;
+    int64_t j, e;
+};
 
 // Scale constants of a pair of sub-blocks (fp16x2 lane .x / .y).
 struct PairScale {
@@ -134,8 +165,10 @@ __device__ __forceinline__ uint64_t smem_desc_xs(uint32_t saddr) {
 
 template <int MP>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_kernel(const __grid_constant__ CUtensorMap xmap, const B2Params p) {
+    tc_kernel(const __grid_constant__ MatDesc single, const LaunchParams p) {
     using C = Cfg<MP>;
+    constexpr int kWRing = C::kWRing;
+    constexpr int kXRing = C::kXRing;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* xring = smem;
@@ -145,32 +178,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* wfull = bars;
     uint64_t* wempty = wfull + kWRing;
     uint64_t* xfull = wempty + kWRing;
-    uint64_t* xempty = xfull + C::kXRing;
-    uint64_t* tfull = xempty + C::kXRing;
+    uint64_t* xempty = xfull + kXRing;
+    uint64_t* tfull = xempty + kXRing;
     uint64_t* tempty = tfull + kNA;
     uint64_t* accfull = tempty + kNA;
     uint64_t* accempty = accfull + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 2);
-    volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] abort [1] last
+    uint64_t* evfull = accempty + 2;
+    uint64_t* evempty = evfull + kEv;
+    uint64_t* mmadone = evempty + kEv;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mmadone + 1);
+    volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] abort
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int64_t c = blockIdx.x;
+    const int count = p.count;
     const int64_t U = p.units;
-    const int64_t u0 = c * U / p.grid;
-    const int64_t u1 = (c + 1) * U / p.grid;
-    const int nunits = static_cast<int>(u1 - u0);
-    const int KB = p.kb;
-    const int64_t t_first = u0 / KB;
-    const int64_t t_last = (u1 - 1) / KB;
+    const int64_t P = gridDim.x;
+    const int64_t g0 = c * U / P, g1 = (c + 1) * U / P;
+    auto mat = [&](int i) -> const MatDesc& { return count == 1 ? single : p.mats[i]; };
+    auto enter = [&](Cursor& k, int i) {
+        for (; i < count; ++i) {
+            const MatDesc& M = mat(i);
+            if (M.base >= g1) break;
+            const int64_t lo = g0 > M.base ? g0 - M.base : 0;
+            const int64_t hi = g1 - M.base < M.units ? g1 - M.base : M.units;
+            if (lo < hi) {
+                k.i = i;
+                k.j = lo;
+                k.e = hi;
+                return;
+            }
+        }
+        k.i = count;
+        k.j = k.e = 0;
+    };
+    auto first = [&](Cursor& k) { enter(k, count == 1 ? 0 : p.first_mat[c]); };
+    auto next = [&](Cursor& k) {
+        if (++k.j >= k.e) enter(k, k.i + 1);
+    };
 
     if (tid == 0) {
         for (int i = 0; i < kWRing; ++i) {
             mbar_init(&wfull[i], 1);
             mbar_init(&wempty[i], 4);
         }
-        for (int i = 0; i < C::kXRing; ++i) {
+        for (int i = 0; i < kXRing; ++i) {
             mbar_init(&xfull[i], 1);
             mbar_init(&xempty[i], 1);
         }
@@ -182,12 +236,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&accfull[i], 1);
             mbar_init(&accempty[i], 4);
         }
+        for (int i = 0; i < kEv; ++i) {
+            mbar_init(&evfull[i], 4);
+            mbar_init(&evempty[i], 1);
+        }
+        mbar_init(mmadone, 1);
         flags[0] = 0;
-        flags[1] = 0;
         fence_mbar_init();
     }
     // the upper (always zero) k half of every -B_l step's B tile
-    for (int i = tid; i < C::kXRing * MP * 4; i += kThreads) {
+    for (int i = tid; i < kXRing * MP * 4; i += kThreads) {
         const int slot = i / (MP * 4), r = (i / 4) % MP, e = i % 4;
         *reinterpret_cast<uint32_t*>(xsum + slot * C::kXsBytes + (r >> 3) * 256 + 128 + (r & 7) * 16 + e * 4) = 0u;
     }
@@ -195,58 +253,122 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     griddep_launch_dependents();
 
-    // ------------------------------------------------------------------ producer
+    // ------------------------------------------------------------------ weight producer
     if (warp == kProducerWarp) {
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
-            const uint8_t* src = p.wq + u0 * kUnitBytes;
-            const int pre = nunits < kWRing ? nunits : kWRing;
-            for (int j = 0; j < pre; ++j) {
-                mbar_arrive_expect_tx(&wfull[j], kUnitBytes);
-                bulk_g2s(wring + j * kUnitBytes, src + static_cast<int64_t>(j) * kUnitBytes, kUnitBytes,
-                         &wfull[j], pol);
-            }
-            int w_issued = pre, x_issued = 0;
-            griddep_wait();  // activations may be written by the previous kernel
-            prefetch_tmap(&xmap);
-            for (int j = 0; j < nunits && !flags[0]; ++j) {
-                const int xs = j % C::kXRing;
-                if (j >= C::kXRing && !mbar_wait_bounded(&xempty[xs], ((j / C::kXRing) - 1) & 1, flags)) {
-                    fail(p.err, flags);
+            Cursor w;
+            first(w);
+            int64_t wseq = 0;
+            bool ok = true;
+            int cur = -1;
+            const uint8_t* src = nullptr;
+            while (w.i < count) {
+                const int s = static_cast<int>(wseq % kWRing);
+                if (wseq >= kWRing && !mbar_wait_bounded(&wempty[s], ((wseq / kWRing) - 1) & 1, flags)) {
+                    ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(&xfull[xs], C::kXSlot);
-                const int kb = static_cast<int>((u0 + j) % KB);
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    tma_load_2d(xring + xs * C::kXSlot + i * C::kXBox, &xmap, kb * 256 + 64 * i, 0, &xfull[xs]);
-                x_issued = j + 1;
-                const int jj = j + kWRing;
-                if (jj < nunits) {
-                    const int s = jj % kWRing;
-                    if (!mbar_wait_bounded(&wempty[s], ((jj / kWRing) - 1) & 1, flags)) {
-                        fail(p.err, flags);
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&wfull[s], kUnitBytes);
-                    bulk_g2s(wring + s * kUnitBytes, src + static_cast<int64_t>(jj) * kUnitBytes, kUnitBytes,
-                             &wfull[s], pol);
-                    w_issued = jj + 1;
+                if (w.i != cur) {
+                    cur = w.i;
+                    src = mat(w.i).wq + w.j * kUnitBytes;
                 }
+                mbar_arrive_expect_tx(&wfull[s], kUnitBytes);
+                bulk_g2s(wring + s * kUnitBytes, src, kUnitBytes, &wfull[s], pol);
+                src += kUnitBytes;
+                ++wseq;
+                next(w);
             }
+            if (!ok) fail(p.err, flags);
             if (flags[0]) {
-                // failure path: let every copy already issued land before the CTA can exit
                 volatile int no_abort = 0;
-                for (int j = w_issued > kWRing ? w_issued - kWRing : 0; j < w_issued; ++j)
+                for (int64_t j = wseq > kWRing ? wseq - kWRing : 0; j < wseq; ++j)
                     mbar_wait_bounded(&wfull[j % kWRing], (j / kWRing) & 1, &no_abort);
-                for (int j = x_issued > C::kXRing ? x_issued - C::kXRing : 0; j < x_issued; ++j)
-                    mbar_wait_bounded(&xfull[j % C::kXRing], (j / C::kXRing) & 1, &no_abort);
             }
         }
         return;
     }
 
-    // ------------------------------------------------------------------ activation sums + MMA
+    // ------------------------------------------------------------------ activations
+    // TMA of each unit's activation tile, up to kXRing units ahead of the tensor core (a slot
+    // is reused once the MMAs that read it have finished).
+    if (warp == kXWarp) {
+        if (lane == 0) {
+            Cursor xc;
+            first(xc);
+            int64_t issued = 0;
+            int cur = -1, kbn = 1, kb = 0;
+            const void* xmap = nullptr;
+            bool ok = true;
+            griddep_wait();  // activations may be written by the previous kernel
+            while (xc.i < count) {
+                const int xs = static_cast<int>(issued % kXRing);
+                if (issued >= kXRing && !mbar_wait_bounded(&xempty[xs], ((issued / kXRing) - 1) & 1, flags)) {
+                    ok = false;
+                    break;
+                }
+                if (xc.i != cur) {
+                    const MatDesc& M = mat(xc.i);
+                    cur = xc.i;
+                    xmap = &M.xmap;
+                    kbn = M.kb;
+                    kb = static_cast<int>(xc.j % kbn);
+                }
+                mbar_arrive_expect_tx(&xfull[xs], C::kXSlot);
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+                    tma_load_2d(xring + xs * C::kXSlot + b * C::kXBox, xmap, kb * 256 + 64 * b, 0, &xfull[xs]);
+                kb = (kb + 1 == kbn) ? 0 : kb + 1;
+                ++issued;
+                next(xc);
+            }
+            if (!ok) fail(p.err, flags);
+            if (flags[0]) {
+                volatile int no_abort = 0;
+                for (int64_t j = issued > kXRing ? issued - kXRing : 0; j < issued; ++j)
+                    mbar_wait_bounded(&xfull[j % kXRing], (j / kXRing) & 1, &no_abort);
+            }
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------------ helper
+    if (warp == kHelperWarp) {
+        if (lane == 0) {
+            int64_t ev = 0;
+            bool ok = true;
+            auto take = [&]() -> bool { return mbar_wait_bounded(&evfull[ev % kEv], (ev / kEv) & 1, flags); };
+            auto give = [&]() {
+                mbar_arrive(&evempty[ev % kEv]);
+                ++ev;
+            };
+            Cursor k;
+            first(k);
+            bool first_part = true;
+            while (ok && k.i < count) {
+                const MatDesc& M = mat(k.i);
+                const int64_t KB = M.kb;
+                const int64_t lo = k.j, hi = k.e;
+                const int64_t tf = lo / KB, tl = (hi - 1) / KB;
+                if (first_part && lo > tf * KB) {
+                    if (!(ok = take())) break;
+                    red_add_release_gpu(M.tickets + tf, 1);
+                    give();
+                }
+                if (tl * KB >= lo && hi < (tl + 1) * KB) {
+                    if (!(ok = take())) break;
+                    M.tickets[tl] = 0;  // ready for the next run
+                    give();
+                }
+                first_part = false;
+                enter(k, k.i + 1);
+            }
+            if (!ok) fail(p.err, flags);
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------------ MMA issue
     if (warp == kMmaWarp) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
@@ -255,64 +377,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t tbase = *tmem_slot;
         constexpr uint32_t kIdesc = idesc_f16_f32(kRows, MP);
-        int seg = 0;
-        for (int64_t tile = t_first; tile <= t_last; ++tile, ++seg) {
-            const int64_t ja = (tile * KB > u0 ? tile * KB : u0) - u0;
-            const int64_t jb = ((tile + 1) * KB < u1 ? (tile + 1) * KB : u1) - u0;
-            const int b = seg & 1;
-            if (seg >= 2 && !mbar_wait_bounded(&accempty[b], ((seg >> 1) - 1) & 1, flags)) fail(p.err, flags);
-            tc_fence_after();
-            const uint32_t d_tmem = tbase + C::kAccCol + b * MP;
-            for (int64_t j = ja; j < jb; ++j) {
-                const int xs = static_cast<int>(j % C::kXRing);
-                const int a = static_cast<int>(j % kNA);
-                bool ok = mbar_wait_bounded(&xfull[xs], (j / C::kXRing) & 1, flags);
-                // X[t][s] = sum of the 32 activations of token t in sub-block s (fp16, clamped)
-                if (ok) {
-                    const uint8_t* xt = xring + xs * C::kXSlot;
-                    uint8_t* xst = xsum + xs * C::kXsBytes;
-#pragma unroll 1
-                    for (int pi = lane; pi < MP * 8; pi += 32) {
-                        const int t = pi % MP, s = pi / MP;
-                        const uint8_t* rowp = xt + (s >> 1) * C::kXBox + t * 128;
-                        __half2 acc2 = __float2half2_rn(0.f);
-#pragma unroll
-                        for (int cc = 0; cc < 4; ++cc) {
-                            const int chunk = ((s & 1) * 4 + cc) ^ (t & 7);
-                            const uint4 v = *reinterpret_cast<const uint4*>(rowp + chunk * 16);
-                            acc2 = __hadd2(acc2, __hadd2(__hadd2(as_h2(v.x), as_h2(v.y)),
-                                                         __hadd2(as_h2(v.z), as_h2(v.w))));
-                        }
-                        __half sum = __hadd(__low2half(acc2), __high2half(acc2));
-                        sum = __hmin(__hmax(sum, __ushort_as_half(0xFBFFu)), __ushort_as_half(0x7BFFu));
-                        *reinterpret_cast<__half*>(xst + (t >> 3) * 256 + (t & 7) * 16 + s * 2) = sum;
-                    }
-                    fence_proxy_async_smem();
+        int64_t seg = 0, j = 0;
+        bool live = true;
+        Cursor mk;
+        first(mk);
+        while (live && mk.i < count) {
+            const int64_t KB = mat(mk.i).kb;
+            const int64_t u0 = mk.j, u1 = mk.e;
+            for (int64_t tile = u0 / KB; live && tile <= (u1 - 1) / KB; ++tile, ++seg) {
+                const int64_t ja = tile * KB > u0 ? tile * KB : u0;
+                const int64_t jb = (tile + 1) * KB < u1 ? (tile + 1) * KB : u1;
+                const int b = static_cast<int>(seg & 1);
+                if (seg >= 2 && !warp_wait(&accempty[b], ((seg >> 1) - 1) & 1, flags)) {
+                    live = false;
+                    break;
                 }
-                __syncwarp();
-                if (lane == 0) {
-                    ok = ok && mbar_wait_bounded(&tfull[a], (j / kNA) & 1, flags);
-                    if (!ok) fail(p.err, flags);
+                tc_fence_after();
+                const uint32_t d_tmem = tbase + C::kAccCol + b * MP;
+                for (int64_t u = ja; u < jb; ++u, ++j) {
+                    const int xs = static_cast<int>(j % kXRing);
+                    const int a = static_cast<int>(j % kNA);
+                    if (!warp_wait(&tfull[a], (j / kNA) & 1, flags)) {
+                        live = false;
+                        break;
+                    }
                     tc_fence_after();
-                    if (ok) {
+                    if (lane == 0) {
                         const uint32_t xaddr = smem_u32(xring + xs * C::kXSlot);
                         const uint32_t acol = tbase + a * kACols;
 #pragma unroll
                         for (int kk = 0; kk < 16; ++kk) {
                             const uint64_t bdesc = smem_desc_sw128(xaddr + (kk >> 2) * C::kXBox + (kk & 3) * 32);
-                            tc_mma_f16_ts(d_tmem, acol + 8 * kk, bdesc, kIdesc, (j > ja || kk > 0) ? 1u : 0u);
+                            tc_mma_f16_ts(d_tmem, acol + 8 * kk, bdesc, kIdesc, (u > ja || kk > 0) ? 1u : 0u);
                         }
                         tc_mma_f16_ts(d_tmem, acol + 128, smem_desc_xs(smem_u32(xsum + xs * C::kXsBytes)), kIdesc, 1u);
+                        tc_commit(&tempty[a]);
+                        tc_commit(&xempty[xs]);
                     }
-                    tc_commit(&tempty[a]);
-                    tc_commit(&xempty[xs]);
+                    __syncwarp();
                 }
+                if (!live) break;
+                if (lane == 0) tc_commit(&accfull[b]);
                 __syncwarp();
             }
-            if (lane == 0) tc_commit(&accfull[b]);
-            __syncwarp();
+            enter(mk, mk.i + 1);
         }
-        named_bar_sync(kBarTeardown, kTeardownThreads);  // every accumulator has been read
+        if (!live && lane == 0) fail(p.err, flags);
+        // every MMA issued has finished before the tensor memory is released
+        if (lane == 0) {
+            tc_commit(mmadone);
+            volatile int no_abort = 0;
+            mbar_wait_bounded(mmadone, 0, &no_abort);
+        }
+        __syncwarp();
+        tc_fence_before();
+        named_bar_sync(kBarTeardown, kTmemUsers);
         tc_fence_after();
         tmem_dealloc(tbase, kTmemCols);
         return;
@@ -322,143 +441,199 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp >= kEpiWarp0) {
         const int q = warp & 3;  // tensor-memory lane quarter
         const int row = 32 * q + lane;
-        const int etid = tid - kEpiWarp0 * 32;
+        const int etid = tid - kEpiWarp0 * 32;  // 0..127, one per row (in lane-quarter order)
         named_bar_sync(kBarTmem, kTmemUsers);
         tc_fence_after();
         const uint32_t tbase = *tmem_slot;
-        griddep_wait();  // y and the workspace may still be in use by the previous kernel
-        int seg = 0;
-        for (int64_t tile = t_first; tile <= t_last; ++tile, ++seg) {
-            const int64_t ja = (tile * KB > u0 ? tile * KB : u0) - u0;
-            const int64_t jb = ((tile + 1) * KB < u1 ? (tile + 1) * KB : u1) - u0;
-            const int b = seg & 1;
-            if (!mbar_wait_bounded(&accfull[b], (seg >> 1) & 1, flags)) fail(p.err, flags);
-            tc_fence_after();
-            const bool whole = (ja + u0 == tile * KB) && (jb + u0 == (tile + 1) * KB);
-            const int side = (tile == t_first) ? 0 : 1;
-            float* part = p.ws + (c * 2 + side) * static_cast<int64_t>(kRows) * p.ws_cols;
-            const int64_t n = tile * kRows + row;
-#pragma unroll 1
-            for (int c0 = 0; c0 < MP; c0 += 16) {
-                uint32_t v[16];
-                tmem_ld16(tbase + (static_cast<uint32_t>(32 * q) << 16) + C::kAccCol + b * MP + c0, v);
-                tc_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int m = c0 + i;
-                    if (m < p.m) {
-                        const float val = __uint_as_float(v[i]);
-                        if (whole) {
-                            if (n < p.n) p.y[static_cast<int64_t>(m) * p.n + n] = val;
-                        } else {
-                            part[m * kRows + row] = val;
-                        }
-                    }
-                }
-            }
-            tc_fence_before();
+        griddep_wait();  // y, the partial slots and the tickets may still be in use by the previous kernel
+        int64_t seg = 0, ev = 0;
+        bool live = true;
+        auto post = [&]() -> bool {
+            const int e = static_cast<int>(ev % kEv);
             __syncwarp();
-            if (lane == 0) mbar_arrive(&accempty[b]);
-            if (!whole) {
-                __threadfence();
-                named_bar_sync(kBarEpi, 128);
-                const int64_t pa = dev_piece_of(tile * KB, U, p.grid);
-                const int64_t pb = dev_piece_of((tile + 1) * KB - 1, U, p.grid);
-                if (etid == 0) {
-                    const int old = atomicAdd(&p.tickets[tile], 1);
-                    flags[1] = (old == static_cast<int>(pb - pa)) ? 1 : 0;
+            if (ev >= kEv && !warp_wait(&evempty[e], ((ev / kEv) - 1) & 1, flags)) return false;
+            if (lane == 0) mbar_arrive(&evfull[e]);
+            ++ev;
+            return true;
+        };
+        Cursor mk;
+        first(mk);
+        while (live && mk.i < count) {
+            const MatDesc& M = mat(mk.i);
+            const int64_t KB = M.kb;
+            const int64_t u0 = mk.j, u1 = mk.e;
+            const int64_t base = M.base;
+            for (int64_t tile = u0 / KB; live && tile <= (u1 - 1) / KB; ++tile, ++seg) {
+                const int64_t ja = tile * KB > u0 ? tile * KB : u0;
+                const int64_t jb = (tile + 1) * KB < u1 ? (tile + 1) * KB : u1;
+                const int b = static_cast<int>(seg & 1);
+                if (!warp_wait(&accfull[b], (seg >> 1) & 1, flags)) {
+                    live = false;
+                    break;
                 }
-                named_bar_sync(kBarEpi, 128);
-                if (flags[1]) {
-                    __threadfence();
-                    // sum the CTA partials in CTA order; the loads of one part are independent
+                tc_fence_after();
+                const uint32_t tacc = tbase + (static_cast<uint32_t>(32 * q) << 16) + C::kAccCol + b * MP;
+                const bool whole = (ja == tile * KB) && (jb == (tile + 1) * KB);
+                const int64_t pa = whole ? c : dev_piece_of(base + tile * KB, U, P);
+                const int64_t n = tile * kRows + row;
+                if (pa != c) {
+                    // a partial for the tile's reducer: [float4 f][128 rows] in this CTA's slot
+                    float4* part = reinterpret_cast<float4*>(p.ws + c * static_cast<int64_t>(kRows) * p.ws_cols);
 #pragma unroll 1
-                    for (int m0 = 0; m0 < p.m; m0 += 16) {
-                        float acc[16];
-#pragma unroll 1
-                        for (int64_t pc = pa; pc <= pb; ++pc) {
-                            const int64_t pc_first_tile = (pc * U / p.grid) / KB;
-                            const int sd = (tile == pc_first_tile) ? 0 : 1;
-                            const float* src = p.ws + (pc * 2 + sd) * static_cast<int64_t>(kRows) * p.ws_cols + row;
-                            float pv[16];
+                    for (int c0 = 0; c0 < MP; c0 += 16) {
+                        uint32_t v[16];
+                        tmem_ld16(tacc + c0, v);
+                        tc_wait_ld();
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) pv[i] = (m0 + i < p.m) ? __ldcg(src + (m0 + i) * kRows) : 0.f;
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) acc[i] = (pc == pa) ? pv[i] : acc[i] + pv[i];
-                        }
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            if (m0 + i < p.m && n < p.n) p.y[static_cast<int64_t>(m0 + i) * p.n + n] = acc[i];
+                        for (int f = 0; f < 4; ++f)
+                            part[(c0 / 4 + f) * kEpiThreads + etid] =
+                                make_float4(__uint_as_float(v[4 * f]), __uint_as_float(v[4 * f + 1]),
+                                            __uint_as_float(v[4 * f + 2]), __uint_as_float(v[4 * f + 3]));
                     }
-                    if (etid == 0) p.tickets[tile] = 0;  // ready for the next run
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&accempty[b]);
+                    live = post();
+                    continue;
                 }
-                named_bar_sync(kBarEpi, 128);  // flags[1] is reused by the next tile
+                int64_t pb = pa;
+                if (!whole) {
+                    pb = dev_piece_of(base + (tile + 1) * KB - 1, U, P);
+                    bool got = true;
+                    if (lane == 0) got = wait_count(M.tickets + tile, static_cast<int>(pb - pa), flags);
+                    if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+                        live = false;
+                        break;
+                    }
+                    __syncwarp();  // the other lanes' loads come after lane 0's acquire
+                }
+#pragma unroll 1
+                for (int c0 = 0; c0 < MP; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tacc + c0, v);
+                    tc_wait_ld();
+                    float acc[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[i] = __uint_as_float(v[i]);
+#pragma unroll 1
+                    for (int64_t pc = pa + 1; pc <= pb; ++pc) {
+                        const float4* src = reinterpret_cast<const float4*>(p.ws + pc * static_cast<int64_t>(kRows) * p.ws_cols);
+                        float4 pv[4];
+#pragma unroll
+                        for (int f = 0; f < 4; ++f) pv[f] = __ldcg(src + (c0 / 4 + f) * kEpiThreads + etid);
+#pragma unroll
+                        for (int f = 0; f < 4; ++f) {
+                            acc[4 * f] += pv[f].x;
+                            acc[4 * f + 1] += pv[f].y;
+                            acc[4 * f + 2] += pv[f].z;
+                            acc[4 * f + 3] += pv[f].w;
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int m = c0 + i;
+                        if (m < p.m && n < M.n) M.y[static_cast<int64_t>(m) * M.n + n] = acc[i];
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&accempty[b]);
+                if (!whole) live = post();  // the helper may now reset the tile's ticket
             }
+            enter(mk, mk.i + 1);
         }
-        named_bar_sync(kBarTeardown, kTeardownThreads);
+        if (!live && lane == 0) fail(p.err, flags);
+        named_bar_sync(kBarTeardown, kTmemUsers);
         return;
     }
 
     // ------------------------------------------------------------------ dequant warps
-    const int q = warp & 3;   // lane quarter: rows 32q .. 32q+31
-    const int g = warp >> 2;  // group: units j = g (mod kGroups)
-    const int row = 32 * q + lane;
-    named_bar_sync(kBarTmem, kTmemUsers);
-    tc_fence_after();
-    const uint32_t tlane = *tmem_slot + (static_cast<uint32_t>(32 * q) << 16);
-
-    for (int j = g; j < nunits; j += kGroups) {
-        const int s = j % kWRing;
-        const int a = j % kNA;
-        if (!mbar_wait_bounded(&wfull[s], (j / kWRing) & 1, flags)) fail(p.err, flags);
-        const uint8_t* u = wring + s * kUnitBytes;
-        uint4 qv[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) qv[i] = *reinterpret_cast<const uint4*>(u + (i * kRows + row) * 16);
-        const uint4 hd = *reinterpret_cast<const uint4*>(u + kQBytes + row * 16);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&wempty[s]);
-
-        // (scale, min) pairs of sub-blocks (0,1), (2,3) from the low 6 bits of s[0..7] and
-        // (4,5), (6,7) from s[8..11] plus the top 2 bits of s[0..7]
-        const uint32_t SClo = hd.y & 0x3F3F3F3Fu;
-        const uint32_t MNlo = hd.z & 0x3F3F3F3Fu;
-        const uint32_t SChi = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
-        const uint32_t MNhi = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
-        const uint32_t dm = prmt(hd.x, 0, 0x3232u);
-        const __half2 d2 = as_h2(prmt(hd.x, 0, 0x1010u));
-        PairScale ps[4];
-        ps[0] = pair_scale(SClo, MNlo, 0, dm);
-        ps[1] = pair_scale(SClo, MNlo, 2, dm);
-        ps[2] = pair_scale(SChi, MNhi, 0, dm);
-        ps[3] = pair_scale(SChi, MNhi, 2, dm);
-
-        if (j >= kNA && !mbar_wait_bounded(&tempty[a], ((j / kNA) - 1) & 1, flags)) fail(p.err, flags);
+    {
+        const int q = warp & 3;   // lane quarter: rows 32q .. 32q+31
+        const int g = warp >> 2;  // group: units j = g (mod kGroups)
+        const int row = 32 * q + lane;
+        named_bar_sync(kBarTmem, kTmemUsers);
         tc_fence_after();
-        const uint32_t tcol = tlane + a * kACols;
+        const uint32_t tlane = *tmem_slot + (static_cast<uint32_t>(32 * q) << 16);
+        const int64_t nunits = g1 - g0;
+        for (int64_t j = g; j < nunits; j += kGroups) {
+            const int s = static_cast<int>(j % kWRing);
+            const int a = static_cast<int>(j % kNA);
+            if (!warp_wait(&wfull[s], (j / kWRing) & 1, flags)) break;
+            const uint8_t* u = wring + s * kUnitBytes;
+            uint4 qv[8];
 #pragma unroll
-        for (int sb = 0; sb < 8; ++sb) {
-            const PairScale& z = ps[sb >> 1];
-            const bool hiL = sb & 1;
-            const __half2 s1 = hiL ? __high2half2(as_h2(z.s1)) : __low2half2(as_h2(z.s1));
-            const __half2 n1 = hiL ? __high2half2(as_h2(z.n1)) : __low2half2(as_h2(z.n1));
-            const __half2 s16 = hiL ? __high2half2(as_h2(z.s16)) : __low2half2(as_h2(z.s16));
-            const __half2 n16 = hiL ? __high2half2(as_h2(z.n16)) : __low2half2(as_h2(z.n16));
-            const __half2 nbh = hiL ? __high2half2(as_h2(z.nbh)) : __low2half2(as_h2(z.nbh));
-            uint32_t out[16];
-            dq_word(qv[sb].x, s1, n1, s16, n16, d2, nbh, out + 0);
-            dq_word(qv[sb].y, s1, n1, s16, n16, d2, nbh, out + 4);
-            dq_word(qv[sb].z, s1, n1, s16, n16, d2, nbh, out + 8);
-            dq_word(qv[sb].w, s1, n1, s16, n16, d2, nbh, out + 12);
-            tmem_st16(tcol + 16 * sb, out);
+            for (int i = 0; i < 8; ++i) qv[i] = lds128(u + (i * kRows + row) * 16);
+            const uint4 hd = lds128(u + kQBytes + row * 16);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&wempty[s]);
+
+            // (scale, min) pairs of sub-blocks (0,1), (2,3) from the low 6 bits of s[0..7] and
+            // (4,5), (6,7) from s[8..11] plus the top 2 bits of s[0..7]
+            const uint32_t SClo = hd.y & 0x3F3F3F3Fu;
+            const uint32_t MNlo = hd.z & 0x3F3F3F3Fu;
+            const uint32_t SChi = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
+            const uint32_t MNhi = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
+            const uint32_t dm = prmt(hd.x, 0, 0x3232u);
+            const __half2 d2 = as_h2(prmt(hd.x, 0, 0x1010u));
+            PairScale ps[4];
+            ps[0] = pair_scale(SClo, MNlo, 0, dm);
+            ps[1] = pair_scale(SClo, MNlo, 2, dm);
+            ps[2] = pair_scale(SChi, MNhi, 0, dm);
+            ps[3] = pair_scale(SChi, MNhi, 2, dm);
+
+            if (j >= kNA && !warp_wait(&tempty[a], ((j / kNA) - 1) & 1, flags)) break;
+            tc_fence_after();
+            const uint32_t tcol = tlane + a * kACols;
+#pragma unroll
+            for (int sb = 0; sb < 8; ++sb) {
+                const PairScale& z = ps[sb >> 1];
+                const bool hiL = sb & 1;
+                const __half2 s1 = hiL ? __high2half2(as_h2(z.s1)) : __low2half2(as_h2(z.s1));
+                const __half2 n1 = hiL ? __high2half2(as_h2(z.n1)) : __low2half2(as_h2(z.n1));
+                const __half2 s16 = hiL ? __high2half2(as_h2(z.s16)) : __low2half2(as_h2(z.s16));
+                const __half2 n16 = hiL ? __high2half2(as_h2(z.n16)) : __low2half2(as_h2(z.n16));
+                const __half2 nbh = hiL ? __high2half2(as_h2(z.nbh)) : __low2half2(as_h2(z.nbh));
+                uint32_t out[16];
+                dq_word(qv[sb].x, s1, n1, s16, n16, d2, nbh, out + 0);
+                dq_word(qv[sb].y, s1, n1, s16, n16, d2, nbh, out + 4);
+                dq_word(qv[sb].z, s1, n1, s16, n16, d2, nbh, out + 8);
+                dq_word(qv[sb].w, s1, n1, s16, n16, d2, nbh, out + 12);
+                tmem_st16(tcol + 16 * sb, out);
+            }
+            // the -B_l step: k slots 0..7 = sub-blocks 0..7, slots 8..15 zero
+            const uint32_t bl[8] = {ps[0].nbl, ps[1].nbl, ps[2].nbl, ps[3].nbl, 0u, 0u, 0u, 0u};
+            tmem_st8(tcol + 128, bl);
+            // the activation sums of this unit for the -B_l step: X[t][s] = sum of the 32
+            // activations of token t in sub-block s (fp16, clamped); MP * 8 of them, shared
+            // out over the group's 128 threads
+            const int xs = static_cast<int>(j % kXRing);
+            if (!warp_wait(&xfull[xs], (j / kXRing) & 1, flags)) break;
+            const uint8_t* xt = xring + xs * C::kXSlot;
+            uint8_t* xst = xsum + xs * C::kXsBytes;
+#pragma unroll
+            for (int pi = row; pi < MP * 8; pi += kRows) {
+                const int t = pi % MP, sb = pi / MP;
+                const uint8_t* rowp = xt + (sb >> 1) * C::kXBox + t * 128;
+                __half2 acc2 = __float2half2_rn(0.f);
+#pragma unroll
+                for (int cc4 = 0; cc4 < 4; ++cc4) {
+                    const int chunk = ((sb & 1) * 4 + cc4) ^ (t & 7);
+                    const uint4 v = lds128(rowp + chunk * 16);
+                    acc2 = __hadd2(acc2, __hadd2(__hadd2(as_h2(v.x), as_h2(v.y)), __hadd2(as_h2(v.z), as_h2(v.w))));
+                }
+                __half sum = __hadd(__low2half(acc2), __high2half(acc2));
+                sum = __hmin(__hmax(sum, __ushort_as_half(0xFBFFu)), __ushort_as_half(0x7BFFu));
+                *reinterpret_cast<__half*>(xst + (t >> 3) * 256 + (t & 7) * 16 + sb * 2) = sum;
+            }
+            fence_proxy_async_smem();  // the sums are read by the tensor core
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tfull[a]);
         }
-        // the -B_l step: k slots 0..7 = sub-blocks 0..7, slots 8..15 zero
-        const uint32_t bl[8] = {ps[0].nbl, ps[1].nbl, ps[2].nbl, ps[3].nbl, 0u, 0u, 0u, 0u};
-        tmem_st8(tcol + 128, bl);
-        tc_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tfull[a]);
+        if (flags[0] && lane == 0) fail(p.err, flags);
+        named_bar_sync(kBarTeardown, kTmemUsers);
     }
 }
 
@@ -537,40 +712,55 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-int mp_for(int m) { return m <= 16 ? 16 : m <= 32 ? 32 : 64; }
+int mp_for(int64_t m) { return m <= 16 ? 16 : m <= 32 ? 32 : 64; }
 
-template <int MP>
-static cudaError_t launch_mp(const CUtensorMap& tmap, const B2Params& p, cudaStream_t s, bool pdl) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Cfg<MP>::kSmem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_kernel<MP>, tmap, p);
-}
-
-cudaError_t launch(const void* x, int64_t k, const B2Params& p, cudaStream_t s, bool pdl) {
+cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, int* tickets, int64_t units,
+                     int64_t n, int32_t kb, int32_t m) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    const int mp = mp_for(p.m);
-    CUtensorMap tmap;
-    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(p.m)};
+    const int64_t k = static_cast<int64_t>(kb) * 256;
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(m)};
     const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(k) * 2};
-    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(mp)};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(mp_for(m))};
     const cuuint32_t estr[2] = {1, 1};
-    if (enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(x), gdim, gstride, box, estr,
+    if (enc(&out->xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(x), gdim, gstride, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    switch (mp) {
-        case 16: return launch_mp<16>(tmap, p, s, pdl);
-        case 32: return launch_mp<32>(tmap, p, s, pdl);
-        default: return launch_mp<64>(tmap, p, s, pdl);
+    out->wq = wq;
+    out->y = y;
+    out->tickets = tickets;
+    out->base = 0;
+    out->units = units;
+    out->n = n;
+    out->kb = kb;
+    out->pad = 0;
+    return cudaSuccess;
+}
+
+template <int MP>
+static cudaError_t launch_mp(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl,
+                             bool cooperative) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Cfg<MP>::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = cooperative ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, tc_kernel<MP>, single, p);
+}
+
+cudaError_t launch(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl, bool cooperative) {
+    switch (mp_for(p.m)) {
+        case 16: return launch_mp<16>(single, p, grid, s, pdl, cooperative);
+        case 32: return launch_mp<32>(single, p, grid, s, pdl, cooperative);
+        default: return launch_mp<64>(single, p, grid, s, pdl, cooperative);
     }
 }
 

@@ -33,8 +33,8 @@ inline int64_t piece_of(int64_t u, int64_t units, int64_t grid) {
 // sequences (matrix i's units at base_i .. base_i + units_i - 1) and cuts it into one piece per
 // CTA; a single run has one matrix and passes it by value, a decode step keeps an array of
 // them in device memory (the tensor map needs 64-byte alignment).
-struct alignas(128) B1Mat {
-    CUtensorMap xmap;      // activations [m, k] fp16: box 64 x 8 (one 8-token group), 128-byte swizzle
+struct alignas(128) MatDesc {
+    CUtensorMap xmap;      // activations [m, k] fp16, 128-byte swizzle: box 64 x 8 (mma.sync) or 64 x MP (tcgen05)
     const uint8_t* wq;     // repacked units
     float* y;              // [m, n] fp32
     int* tickets;          // [tiles]: partials published for the tile; zero between runs
@@ -45,10 +45,10 @@ struct alignas(128) B1Mat {
     int32_t pad;
 };
 
-struct B1Params {
-    const B1Mat* mats;       // device array of `count` matrices (count > 1 only)
+struct LaunchParams {
+    const MatDesc* mats;       // device array of `count` matrices (count > 1 only)
     const int32_t* first_mat;// [grid]: matrix holding each piece's first unit (count > 1 only)
-    float* ws;               // split-K partials, one slot per CTA: [grid][ws_cols / 4][128 threads] float4
+    float* ws;               // split-K partials, one slot per CTA of 128 threads x ws_cols floats
     int* err;                // sticky error word (mapped host memory)
     int64_t units;           // units of all matrices of the launch
     int32_t count;           // matrices in this launch
@@ -57,27 +57,18 @@ struct B1Params {
     int32_t pad;
 };
 
-struct B2Params {
-    const uint8_t* wq;   // repacked units (128 rows x 256 weights each)
-    float* y;            // [m, n] fp32
-    float* ws;           // split-K partial slots [grid][2][ws_cols][128]
-    int* tickets;        // [tiles]
-    int* err;            // sticky error word (mapped host memory)
-    int64_t units;
-    int64_t n;
-    int32_t kb;
-    int32_t m;           // rows of this launch, 1..128
-    int32_t grid;
-    int32_t ws_cols;
-};
-
-// Backend 2: tcgen05 streaming kernel (weights in tensor memory, x by TMA).
+// Backend 2: tcgen05 streaming kernel (weights dequantised into tensor memory, x by TMA).
 namespace b2 {
 constexpr int kRows = 128;
 constexpr int kUnitBytes = kRows * 144;
 constexpr int kMaxM = 64;   // rows per launch
+int mp_for(int64_t m);      // tokens per launch tile: 16, 32 or 64
 cudaError_t repack(const uint8_t* src_dev, uint8_t* dst_dev, const Decomp& d, cudaStream_t s);
-cudaError_t launch(const void* x, int64_t k, const B2Params& p, cudaStream_t s, bool pdl);
+// Fill a matrix descriptor for a run of m rows (1..64) of x against the handle's weights.
+cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, int* tickets, int64_t units,
+                     int64_t n, int32_t kb, int32_t m);
+// Launch over `p.count` matrices (`single` when count == 1); p.ws_cols = mp_for(p.m).
+cudaError_t launch(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl, bool cooperative);
 cudaError_t configure();
 }  // namespace b2
 
@@ -93,10 +84,10 @@ constexpr int32_t ws_floats(int64_t m) { return m > 8 ? 32 : 16; }
 int smem_bytes(int nt);
 cudaError_t repack(const uint8_t* src_dev, uint8_t* dst_dev, const Decomp& d, cudaStream_t s);
 // Fill a matrix descriptor for a run of m rows (1..16) of x against the handle's weights.
-cudaError_t make_mat(B1Mat* out, const uint8_t* wq, const void* x, float* y, int* tickets, int64_t units,
+cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, int* tickets, int64_t units,
                      int64_t n, int32_t kb, int32_t m);
 // Launch over `p.count` matrices (`single` when count == 1) on `grid` persistent CTAs.
-cudaError_t launch(const B1Mat& single, const B1Params& p, int grid, cudaStream_t s, bool pdl, bool cooperative);
+cudaError_t launch(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl, bool cooperative);
 cudaError_t configure();  // one-time function attributes
 }  // namespace b1
 

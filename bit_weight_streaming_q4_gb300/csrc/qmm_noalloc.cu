@@ -96,11 +96,11 @@ extern "C" qmm_status qmm_run_noalloc(const void* blocks, int64_t n, int64_t k, 
     if (cudaMemsetAsync(tk, 0, tickets + 256, s) != cudaSuccess) return QMM_ERR_CUDA;
     for (int64_t r0 = 0; r0 < m; r0 += qmm::b1::kMaxM) {
         const int64_t mc = (m - r0 < qmm::b1::kMaxM) ? m - r0 : qmm::b1::kMaxM;
-        qmm::B1Mat mat;
+        qmm::MatDesc mat;
         if (qmm::b1::make_mat(&mat, wq, static_cast<const __half*>(x) + r0 * k, y + r0 * n, tk, units, n,
                               static_cast<int32_t>(kb), static_cast<int32_t>(mc)) != cudaSuccess)
             return QMM_ERR_CUDA;
-        qmm::B1Params p = {};
+        qmm::LaunchParams p = {};
         p.ws = wsp;
         p.err = err;
         p.units = units;

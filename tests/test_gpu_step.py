@@ -78,13 +78,15 @@ def test_independent_step_parity_and_repeatability(backend, m):
     step.close()
 
 
-def test_independent_step_rows_do_not_depend_on_m():
-    """The persistent step's rows are bit-identical whether the step has 16, 9 or 3 rows."""
+@pytest.mark.parametrize("backend_ms", [(1, (16, 9, 3)), (2, (64, 40, 17, 5))], ids=["mma_sync", "tcgen05"])
+def test_independent_step_rows_do_not_depend_on_m(backend_ms):
+    """The persistent step's rows are bit-identical whatever the number of rows of the step."""
     from bit_weight_streaming_q4_gb300 import Step
     torch = torch_cuda()
-    qs, xs, ys, _ = _setup(1, 16, MATS)
+    be, ms = backend_ms
+    qs, xs, ys, refs = _setup(be, ms[0], MATS)
     outs = {}
-    for m in (16, 9, 3):
+    for m in ms:
         step = Step(qs, xs, ys, m, flags=1)
         for y in ys:
             y.fill_(float("nan"))
@@ -92,8 +94,10 @@ def test_independent_step_rows_do_not_depend_on_m():
         torch.cuda.synchronize()
         outs[m] = [y.cpu().numpy()[:m].copy() for y in ys]
         step.close()
-    for m in (9, 3):
-        for a, b in zip(outs[16], outs[m]):
+    for (y_ref, s_ref), got, mat in zip(refs, outs[ms[0]], MATS):
+        assert_parity(got, y_ref, s_ref, mat.name)
+    for m in ms[1:]:
+        for a, b in zip(outs[ms[0]], outs[m]):
             assert np.array_equal(a[:m].view(np.uint32), b.view(np.uint32))
 
 
