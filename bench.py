@@ -34,6 +34,11 @@ if ROOT not in sys.path:
 import synth  # noqa: E402
 
 METRIC = "Q4K x M-row decode GEMM: weight GB/s (% of HBM peak) and step tok/s at M=1/12/64"
+# DRAM bytes per 256-row unit measured by ncu for the mma.sync step kernel (profiles/
+# stream_kernel_step_m12.md); valid only for the kernel source it was taken from
+TRAFFIC_PER_UNIT = {"source": "bit_weight_streaming_q4_gb300/csrc/qmm_b1.cu",
+                    "sha256": "43d77ce69d57d591d1ae8852fdc3a0d12692e52edc2c34708f401cbef0162db2",
+                    "bytes": 37194.0}
 HEADLINE_M = 12
 EXTRA_M = (1, 64)
 NOMINAL_HBM_GBS = 8000.0
@@ -180,6 +185,21 @@ class Stack:
         xb = sum(m * mat.k * 2 for mat in self.mats)
         yb = sum(m * mat.n * 4 for mat in self.mats)
         return self.weight_bytes, xb, yb
+
+
+def measured_traffic(stack):
+    """DRAM bytes of one step launch from the ncu capture, scaled by the launch's units; None
+    when the kernel source differs from the one the counters were taken from."""
+    import hashlib
+    path = os.path.join(ROOT, TRAFFIC_PER_UNIT["source"])
+    try:
+        with open(path, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != TRAFFIC_PER_UNIT["sha256"]:
+                return None
+    except OSError:
+        return None
+    units = sum(q.info().units for q in stack.qs)
+    return TRAFFIC_PER_UNIT["bytes"] * units
 
 
 def time_graph(torch, step, steps, warmup, stream):
@@ -463,7 +483,7 @@ def run_ours(args, rank, world, local_rank):
             by_m[str(m)] = {"weight_gbs": wbm / sm / 1e9, "tok_s": m / sm, "ms_per_step": sm * 1e3,
                             "frac_of_hbm_measured": wbm / sm / 1e9 / hbm,
                             "backend": int(stack.handles(m)[0].info().backend),
-                            "runs": "independent" if m <= 16 else "CUDA graph of runs"}
+                            "runs": "independent (one persistent kernel per step)"}
             if not args.no_parity:
                 last = len(stack.mats) - 1
                 by_m[str(m)]["parity"] = sampled_parity(stack, m, matrices=[0, 1, 2, 3, last])
@@ -489,7 +509,7 @@ def run_ours(args, rank, world, local_rank):
         "by_m": by_m,
         "dependent_step": dependent,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": None,
+                     "frac": achieved / hbm, "traffic": measured_traffic(stack),
                      "kernel": "qmm::b1::stream_kernel<2> (one persistent launch per step)",
                      "note": f"algorithmic bytes per launch (weights + x + y of the 257 matrices) "
                              f"/ launch time; peak is the {peak_kind} copy bandwidth"},
