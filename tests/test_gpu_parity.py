@@ -147,3 +147,25 @@ def test_argument_errors_with_device(backend):
     assert lib.qmm_run(raw, x.data_ptr(), 1, y.data_ptr(), None) == 7
     assert lib.qmm_destroy(raw) == 7
     assert lib.qmm_destroy(None) == 7
+
+
+@pytest.mark.parametrize("mat", [synth.layer_matrices(0)[2], synth.layer_matrices(0)[3]], ids=lambda m: m.name)
+def test_chunked_prefill_m524(mat, backend):
+    """The chunked-prefill step: M = 524 rows (512-token prompt chunk + 12 decode rows) with 1%
+    outlier activations x20, on gate_up and down at full size.  Sampled output columns (rows of
+    W) against the oracle, every row; and each of a few rows bit-identical to the same row run
+    alone (the run of 524 rows is cut into launches, which must not change any row's bits)."""
+    torch = torch_cuda()
+    m = 524
+    blocks = synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id)
+    x = synth.x_f16(m, mat.k, seed=0, tensor_id=synth.X_ID_OFFSET + mat.tensor_id,
+                    outlier_p=0.01, outlier_mul=20.0)
+    q = make(blocks, m_max=m, backend=backend)
+    y = run(q, x)
+    rng = np.random.default_rng(11)
+    cols = np.sort(rng.choice(mat.n, size=24, replace=False))
+    y_ref, s_ref = oracle.qmm(synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id, rows=cols), x)
+    assert_parity(y[:, cols], y_ref, s_ref, f"{mat.name} M=524")
+    for r in (0, 77, 511, 523):
+        alone = run(q, x[r:r + 1])
+        assert np.array_equal(alone[0].view(np.uint32), y[r].view(np.uint32)), r
