@@ -18,20 +18,25 @@
 // Warp roles of a persistent CTA (one per SM, 16 warps):
 //   warps 0-7   dequantisation, two groups of four; group g takes the units j = g (mod 2)
 //               of the CTA's piece, one output row per thread (warp w owns tensor-memory
-//               lanes 32(w%4)..+31), and writes fp16 weights into the group's A buffer in
-//               tensor memory;
+//               lanes 32(w%4)..+31), and writes fp16 weights into A buffer j mod 3 in
+//               tensor memory (three buffers, so that a group can dequantise its next unit
+//               while the tensor core still reads the last two);
 //   warp 8      weight producer: 1-D bulk copies of the units into a shared-memory ring,
 //               across matrix boundaries;
 //   warp 9      activations: 2-D TMA (128-byte swizzle) of x[0..MP-1][kb*256..+256] for each
 //               unit (the dequantising group also forms the unit's per-sub-block activation
 //               sums for the correction step);
-//   warp 10     tcgen05.mma issue (one thread): A = weights in tensor memory (M = 128 rows),
+//   warps 10, 15 tcgen05.mma issue (one thread each), warp 10 for the units of group 0 and
+//               warp 15 for those of group 1: A = weights in tensor memory (M = 128 rows),
 //               B = x in shared memory (N = MP tokens), fp32 accumulators in tensor memory,
-//               double-buffered per row tile;
-//   warps 11-14 epilogue: accumulators -> y, a split-K partial, or the reduction of a split
-//               row tile;
-//   warp 15     helper: publishes the CTA's partial and resets the ticket of the tile it
-//               reduced.
+//               one per issuing warp (double-buffered per row tile where tensor memory
+//               has room: MP <= 32).  A single thread
+//               cannot keep the tensor core busy: after a burst of MMAs its next
+//               shared-memory access (the mbarrier wait for the next unit) stalls until the
+//               burst has drained, so two issuers take turns;
+//   warps 11-14 epilogue: the sum of the two accumulators -> y, a split-K partial, or the
+//               reduction of a split row tile; warp 11 also publishes the CTA's partial and
+//               resets the ticket of the tile it reduced.
 // Decomposition as in the mma.sync backend: a launch concatenates its matrices' unit
 // sequences, CTA c takes [c*U/P, (c+1)*U/P), and a row tile cut between CTAs pa..pb is
 // reduced by pa in piece order.  Nothing in any output's arithmetic depends on M.
@@ -39,8 +44,8 @@
 // Dequantisation, exact to ~1 ulp of fp16 for every input: with code c = 1024 + q (or
 // 1024 + 16q), P = sc*q is exact from one fp16 FMA; B = dmin*m splits error-free into
 // B_h + B_l; the weight written is fp16(d*P - B_h), and the -B_l part goes to the tensor
-// core as one extra K=16 step per unit: A = -B_l of the 8 sub-blocks, B = the activation
-// sums of the 8 sub-blocks.
+// core as one extra K=16 step per unit: A = -B_l of the 8 sub-blocks (a small tile in
+// shared memory), B = the activation sums of the 8 sub-blocks.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -56,33 +61,44 @@ constexpr int kGroups = 2;                 // dequant warp groups
 constexpr int kDqWarps = 4 * kGroups;
 constexpr int kProducerWarp = kDqWarps;    // 8
 constexpr int kXWarp = kDqWarps + 1;       // 9
-constexpr int kMmaWarp = kDqWarps + 2;     // 10
-constexpr int kEpiWarp0 = kDqWarps + 3;    // 11..14
-constexpr int kHelperWarp = kEpiWarp0 + 4; // 15
-constexpr int kThreads = (kHelperWarp + 1) * 32;  // 512: 128 registers per thread
+constexpr int kMmaWarp0 = kDqWarps + 2;   // 10: MMAs of group 0's units
+constexpr int kEpiWarp0 = kDqWarps + 3;   // 11..14
+constexpr int kMmaWarp1 = kEpiWarp0 + 4;  // 15: MMAs of group 1's units
+constexpr int kThreads = (kMmaWarp1 + 1) * 32;  // 512: 128 registers per thread
 constexpr int kEpiThreads = 128;
 constexpr int kTmemCols = 512;
-constexpr int kACols = 136;  // one unit: 128 columns of weights + 8 of the -B_l step
-constexpr int kNA = kGroups; // one A buffer per group
-constexpr int kEv = 4;
+constexpr int kACols = 128;  // one unit of fp16 weights: 128 rows x 256 k
+constexpr int kNA = 3;       // A buffers in tensor memory, unit j -> buffer j mod 3
+// The handshakes on the A buffers (tfull: written; tempty: read by the MMAs) use a pair of
+// mbarriers per unit j mod 6, so that each barrier only ever serves one dequant group, one
+// issuer and one buffer, and no waiter can fall two phases behind (a parity wait cannot tell
+// that from a phase already done).
+constexpr int kTB = 6;
+constexpr int kBlBytes = kRows * 32;  // A tile of the -B_l step: [128 rows][16 k] fp16
 // named barriers
 constexpr int kBarTmem = 1, kBarTeardown = 2;
-constexpr int kTmemUsers = (kDqWarps + 1 + 4) * 32;  // dequant + MMA + epilogue warps
+constexpr int kTmemUsers = (kDqWarps + 2 + 4) * 32;  // dequant + MMA + epilogue warps
 
 template <int MP>
 struct Cfg {
-    static constexpr int kWRing = MP <= 32 ? 6 : 4;   // weight slots (a multiple of kGroups)
-    static constexpr int kXRing = 4;
+    // ring depths, as deep as shared memory allows: weight slots and activation slots, each a
+    // multiple of kGroups so that a slot (and its barriers) always serves the same group
+    static constexpr int kWRing = MP == 16 ? 8 : MP == 32 ? 6 : 4;
+    static constexpr int kXRing = MP == 16 ? 8 : MP == 32 ? 6 : 4;
     static constexpr int kXBox = MP * 128;    // one 64-wide k box of x
     static constexpr int kXSlot = 4 * kXBox;  // x tile of one unit
     static constexpr int kXsBytes = MP * 32;  // the B tile of the -B_l step: [MP tokens][16 k]
-    static constexpr int kAccCol = kNA * kACols;
-    static_assert(kAccCol + 2 * MP <= kTmemCols, "tensor memory budget");
-    static_assert(kWRing % kGroups == 0, "a weight slot must always feed the same group");
+    // accumulator buffers per issuer: two (the epilogue of a tile overlaps the next tile's
+    // MMAs) where tensor memory has room, else one
+    static constexpr int kAccBufs = MP == 64 ? 1 : 2;
+    static constexpr int kAccCol = kNA * kACols;  // accumulator (issuer e, buffer b) at + (e * kAccBufs + b) * MP
+    static_assert(kAccCol + 2 * kAccBufs * MP <= kTmemCols, "tensor memory budget");
+    static_assert(kWRing % kGroups == 0 && kXRing % kGroups == 0, "a slot must always feed the same group");
     static constexpr int kWOff = kXRing * kXSlot;
     static constexpr int kXsOff = kWOff + kWRing * kUnitBytes;
-    static constexpr int kBarOff = kXsOff + kXRing * kXsBytes;
-    static constexpr int kNumBars = 2 * kWRing + 2 * kXRing + 2 * kNA + 4 + 2 * kEv + 1;
+    static constexpr int kBlOff = kXsOff + kXRing * kXsBytes;
+    static constexpr int kBarOff = kBlOff + kNA * kBlBytes;
+    static constexpr int kNumBars = 2 * kWRing + 2 * kXRing + 2 * kTB + 4 + 2 + 2;
     static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
     static_assert(kSmem <= 232448, "shared memory budget");
 };
@@ -156,9 +172,10 @@ __device__ __forceinline__ void dq_word(uint32_t w, __half2 s1, __half2 n1, __ha
     out[3] = as_u32(__hfma2(__hfma2(c67, s16, n16), d2, nbh));
 }
 
-// Shared-memory descriptor of the -B_l step's B tile: K-major, no swizzle, core matrices of
-// 8 tokens x 16 bytes; the two k halves 128 bytes apart, token groups 256 bytes apart.
-__device__ __forceinline__ uint64_t smem_desc_xs(uint32_t saddr) {
+// Shared-memory descriptor of the -B_l step's A and B tiles ([rows][16 k] fp16): K-major, no
+// swizzle, core matrices of 8 rows x 16 bytes; the two k halves 128 bytes apart, 8-row groups
+// 256 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_k16(uint32_t saddr) {
     return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(128 >> 4) << 16) |
            (static_cast<uint64_t>(256 >> 4) << 32) | (static_cast<uint64_t>(1) << 46);
 }
@@ -174,19 +191,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* xring = smem;
     uint8_t* wring = smem + C::kWOff;
     uint8_t* xsum = smem + C::kXsOff;
+    uint8_t* blt = smem + C::kBlOff;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
     uint64_t* wfull = bars;
     uint64_t* wempty = wfull + kWRing;
     uint64_t* xfull = wempty + kWRing;
     uint64_t* xempty = xfull + kXRing;
     uint64_t* tfull = xempty + kXRing;
-    uint64_t* tempty = tfull + kNA;
-    uint64_t* accfull = tempty + kNA;
-    uint64_t* accempty = accfull + 2;
-    uint64_t* evfull = accempty + 2;
-    uint64_t* evempty = evfull + kEv;
-    uint64_t* mmadone = evempty + kEv;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mmadone + 1);
+    uint64_t* tempty = tfull + kTB;
+    uint64_t* accfull = tempty + kTB;   // [2]: both issuers' accumulators of buffer b are final
+    uint64_t* accempty = accfull + 2;   // [2]: the epilogue has read buffer b
+    uint64_t* evpart = accempty + 2;    // the four epilogue warps have written the partial
+    uint64_t* evred = evpart + 1;       // ... have read the partials of the tile they reduced
+    uint64_t* mmadone = evred + 1;      // [2]: every MMA of issuer e has finished
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mmadone + 2);
     volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] abort
 
     const int tid = threadIdx.x;
@@ -228,19 +246,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&xfull[i], 1);
             mbar_init(&xempty[i], 1);
         }
-        for (int i = 0; i < kNA; ++i) {
+        for (int i = 0; i < kTB; ++i) {
             mbar_init(&tfull[i], 4);
             mbar_init(&tempty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&accfull[i], 1);
+            mbar_init(&accfull[i], 2);
             mbar_init(&accempty[i], 4);
+            mbar_init(&mmadone[i], 1);
         }
-        for (int i = 0; i < kEv; ++i) {
-            mbar_init(&evfull[i], 4);
-            mbar_init(&evempty[i], 1);
-        }
-        mbar_init(mmadone, 1);
+        mbar_init(evpart, 4);
+        mbar_init(evred, 4);
         flags[0] = 0;
         fence_mbar_init();
     }
@@ -248,6 +264,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = tid; i < kXRing * MP * 4; i += kThreads) {
         const int slot = i / (MP * 4), r = (i / 4) % MP, e = i % 4;
         *reinterpret_cast<uint32_t*>(xsum + slot * C::kXsBytes + (r >> 3) * 256 + 128 + (r & 7) * 16 + e * 4) = 0u;
+    }
+    // ... and of the A tiles of the -B_l step
+    for (int i = tid; i < kNA * kRows * 4; i += kThreads) {
+        const int slot = i / (kRows * 4), r = (i / 4) % kRows, e = i % 4;
+        *reinterpret_cast<uint32_t*>(blt + slot * kBlBytes + (r >> 3) * 256 + 128 + (r & 7) * 16 + e * 4) = 0u;
     }
     fence_proxy_async_smem();
     __syncthreads();
@@ -332,46 +353,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
 
-    // ------------------------------------------------------------------ helper
-    if (warp == kHelperWarp) {
-        if (lane == 0) {
-            int64_t ev = 0;
-            bool ok = true;
-            auto take = [&]() -> bool { return mbar_wait_bounded(&evfull[ev % kEv], (ev / kEv) & 1, flags); };
-            auto give = [&]() {
-                mbar_arrive(&evempty[ev % kEv]);
-                ++ev;
-            };
-            Cursor k;
-            first(k);
-            bool first_part = true;
-            while (ok && k.i < count) {
-                const MatDesc& M = mat(k.i);
-                const int64_t KB = M.kb;
-                const int64_t lo = k.j, hi = k.e;
-                const int64_t tf = lo / KB, tl = (hi - 1) / KB;
-                if (first_part && lo > tf * KB) {
-                    if (!(ok = take())) break;
-                    red_add_release_gpu(M.tickets + tf, 1);
-                    give();
-                }
-                if (tl * KB >= lo && hi < (tl + 1) * KB) {
-                    if (!(ok = take())) break;
-                    M.tickets[tl] = 0;  // ready for the next run
-                    give();
-                }
-                first_part = false;
-                enter(k, k.i + 1);
-            }
-            if (!ok) fail(p.err, flags);
-        }
-        return;
-    }
-
     // ------------------------------------------------------------------ MMA issue
-    if (warp == kMmaWarp) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
+    // Issuer e takes the units j = e (mod 2) of the piece (those of dequant group e) and
+    // accumulates them into its own accumulator of the tile's buffer; it walks every row tile
+    // of the piece, also those holding none of its units, so that both issuers and the
+    // epilogue agree on the buffer of each tile.
+    if (warp == kMmaWarp0 || warp == kMmaWarp1) {
+        const int e = warp == kMmaWarp0 ? 0 : 1;
+        if (e == 0) {
+            tmem_alloc(tmem_slot, kTmemCols);
+            tmem_relinquish();
+        }
         tc_fence_before();
         named_bar_sync(kBarTmem, kTmemUsers);
         tc_fence_after();
@@ -387,34 +379,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int64_t tile = u0 / KB; live && tile <= (u1 - 1) / KB; ++tile, ++seg) {
                 const int64_t ja = tile * KB > u0 ? tile * KB : u0;
                 const int64_t jb = (tile + 1) * KB < u1 ? (tile + 1) * KB : u1;
-                const int b = static_cast<int>(seg & 1);
-                if (seg >= 2 && !warp_wait(&accempty[b], ((seg >> 1) - 1) & 1, flags)) {
+                const int b = static_cast<int>(seg % C::kAccBufs);
+                if (seg >= C::kAccBufs && !warp_wait(&accempty[b], ((seg / C::kAccBufs) - 1) & 1, flags)) {
                     live = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tbase + C::kAccCol + b * MP;
+                const uint32_t d_tmem = tbase + C::kAccCol + (e * C::kAccBufs + b) * MP;
+                bool fresh = true;
                 for (int64_t u = ja; u < jb; ++u, ++j) {
+                    if ((j & 1) != e) continue;
                     const int xs = static_cast<int>(j % kXRing);
                     const int a = static_cast<int>(j % kNA);
-                    if (!warp_wait(&tfull[a], (j / kNA) & 1, flags)) {
+                    const int tb = static_cast<int>(j % kTB);
+                    if (!warp_wait(&tfull[tb], (j / kTB) & 1, flags)) {
                         live = false;
                         break;
                     }
                     tc_fence_after();
                     if (lane == 0) {
                         const uint32_t xaddr = smem_u32(xring + xs * C::kXSlot);
-                        const uint32_t acol = tbase + a * kACols;
 #pragma unroll
                         for (int kk = 0; kk < 16; ++kk) {
                             const uint64_t bdesc = smem_desc_sw128(xaddr + (kk >> 2) * C::kXBox + (kk & 3) * 32);
-                            tc_mma_f16_ts(d_tmem, acol + 8 * kk, bdesc, kIdesc, (u > ja || kk > 0) ? 1u : 0u);
+                            tc_mma_f16_ts(d_tmem, tbase + a * kACols + 8 * kk, bdesc, kIdesc, (!fresh || kk > 0) ? 1u : 0u);
                         }
-                        tc_mma_f16_ts(d_tmem, acol + 128, smem_desc_xs(smem_u32(xsum + xs * C::kXsBytes)), kIdesc, 1u);
-                        tc_commit(&tempty[a]);
+                        tc_mma_f16_ss(d_tmem, smem_desc_k16(smem_u32(blt + a * kBlBytes)),
+                                      smem_desc_k16(smem_u32(xsum + xs * C::kXsBytes)), kIdesc, 1u);
+                        tc_commit(&tempty[tb]);
                         tc_commit(&xempty[xs]);
                     }
                     __syncwarp();
+                    fresh = false;
                 }
                 if (!live) break;
                 if (lane == 0) tc_commit(&accfull[b]);
@@ -425,36 +421,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!live && lane == 0) fail(p.err, flags);
         // every MMA issued has finished before the tensor memory is released
         if (lane == 0) {
-            tc_commit(mmadone);
+            tc_commit(&mmadone[e]);
             volatile int no_abort = 0;
-            mbar_wait_bounded(mmadone, 0, &no_abort);
+            mbar_wait_bounded(&mmadone[e], 0, &no_abort);
         }
         __syncwarp();
         tc_fence_before();
         named_bar_sync(kBarTeardown, kTmemUsers);
         tc_fence_after();
-        tmem_dealloc(tbase, kTmemCols);
+        if (e == 0) tmem_dealloc(tbase, kTmemCols);
         return;
     }
 
     // ------------------------------------------------------------------ epilogue
-    if (warp >= kEpiWarp0) {
+    if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
         const int q = warp & 3;  // tensor-memory lane quarter
         const int row = 32 * q + lane;
         const int etid = tid - kEpiWarp0 * 32;  // 0..127, one per row (in lane-quarter order)
         named_bar_sync(kBarTmem, kTmemUsers);
         tc_fence_after();
-        const uint32_t tbase = *tmem_slot;
+        const uint32_t tq = *tmem_slot + (static_cast<uint32_t>(32 * q) << 16) + C::kAccCol;
         griddep_wait();  // y, the partial slots and the tickets may still be in use by the previous kernel
-        int64_t seg = 0, ev = 0;
+        int64_t seg = 0, jl = 0;  // jl: local index of the tile's first unit in the piece
         bool live = true;
-        auto post = [&]() -> bool {
-            const int e = static_cast<int>(ev % kEv);
+        // All four warps arrive on `ev` (each at most once per launch); lane 0 of warp
+        // kEpiWarp0 then waits for the other three.  False if that wait gave up.
+        auto gather = [&](uint64_t* ev) -> bool {
             __syncwarp();
-            if (ev >= kEv && !warp_wait(&evempty[e], ((ev / kEv) - 1) & 1, flags)) return false;
-            if (lane == 0) mbar_arrive(&evfull[e]);
-            ++ev;
-            return true;
+            if (lane == 0) mbar_arrive(ev);
+            return !(warp == kEpiWarp0 && lane == 0) || mbar_wait_bounded(ev, 0, flags);
         };
         Cursor mk;
         first(mk);
@@ -466,13 +461,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int64_t tile = u0 / KB; live && tile <= (u1 - 1) / KB; ++tile, ++seg) {
                 const int64_t ja = tile * KB > u0 ? tile * KB : u0;
                 const int64_t jb = (tile + 1) * KB < u1 ? (tile + 1) * KB : u1;
-                const int b = static_cast<int>(seg & 1);
-                if (!warp_wait(&accfull[b], (seg >> 1) & 1, flags)) {
+                const int b = static_cast<int>(seg % C::kAccBufs);
+                // which issuers hold units of this tile (issuer e takes local indices = e mod 2)
+                const bool has0 = jb - ja >= 2 || (jl & 1) == 0;
+                const bool has1 = jb - ja >= 2 || (jl & 1) == 1;
+                jl += jb - ja;
+                if (!warp_wait(&accfull[b], (seg / C::kAccBufs) & 1, flags)) {
                     live = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t tacc = tbase + (static_cast<uint32_t>(32 * q) << 16) + C::kAccCol + b * MP;
+                const uint32_t tacc0 = tq + b * MP, tacc1 = tq + (C::kAccBufs + b) * MP;
+                // columns c0 .. c0 + 15 of the tile's result: issuer 0's sum + issuer 1's sum
+                auto load_acc = [&](int c0, float (&acc)[16]) {
+                    uint32_t v[16];
+                    tmem_ld16((has0 ? tacc0 : tacc1) + c0, v);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[i] = __uint_as_float(v[i]);
+                    if (has0 && has1) {
+                        tmem_ld16(tacc1 + c0, v);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[i] += __uint_as_float(v[i]);
+                    }
+                };
                 const bool whole = (ja == tile * KB) && (jb == (tile + 1) * KB);
                 const int64_t pa = whole ? c : dev_piece_of(base + tile * KB, U, P);
                 const int64_t n = tile * kRows + row;
@@ -481,19 +494,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float4* part = reinterpret_cast<float4*>(p.ws + c * static_cast<int64_t>(kRows) * p.ws_cols);
 #pragma unroll 1
                     for (int c0 = 0; c0 < MP; c0 += 16) {
-                        uint32_t v[16];
-                        tmem_ld16(tacc + c0, v);
-                        tc_wait_ld();
+                        float acc[16];
+                        load_acc(c0, acc);
 #pragma unroll
                         for (int f = 0; f < 4; ++f)
                             part[(c0 / 4 + f) * kEpiThreads + etid] =
-                                make_float4(__uint_as_float(v[4 * f]), __uint_as_float(v[4 * f + 1]),
-                                            __uint_as_float(v[4 * f + 2]), __uint_as_float(v[4 * f + 3]));
+                                make_float4(acc[4 * f], acc[4 * f + 1], acc[4 * f + 2], acc[4 * f + 3]);
                     }
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&accempty[b]);
-                    live = post();
+                    // publish: one release increment of the tile's ticket after all four warps' writes
+                    const bool ok = gather(evpart);
+                    if (ok && warp == kEpiWarp0 && lane == 0) red_add_release_gpu(M.tickets + tile, 1);
+                    live = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                     continue;
                 }
                 int64_t pb = pa;
@@ -509,12 +523,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
 #pragma unroll 1
                 for (int c0 = 0; c0 < MP; c0 += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(tacc + c0, v);
-                    tc_wait_ld();
                     float acc[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[i] = __uint_as_float(v[i]);
+                    load_acc(c0, acc);
 #pragma unroll 1
                     for (int64_t pc = pa + 1; pc <= pb; ++pc) {
                         const float4* src = reinterpret_cast<const float4*>(p.ws + pc * static_cast<int64_t>(kRows) * p.ws_cols);
@@ -538,7 +548,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&accempty[b]);
-                if (!whole) live = post();  // the helper may now reset the tile's ticket
+                // the partials are read: the tile's ticket is ready for the next run
+                if (!whole) {
+                    const bool ok = gather(evred);
+                    if (ok && warp == kEpiWarp0 && lane == 0) M.tickets[tile] = 0;
+                    live = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                }
             }
             enter(mk, mk.i + 1);
         }
@@ -582,31 +597,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ps[2] = pair_scale(SChi, MNhi, 0, dm);
             ps[3] = pair_scale(SChi, MNhi, 2, dm);
 
-            if (j >= kNA && !warp_wait(&tempty[a], ((j / kNA) - 1) & 1, flags)) break;
-            tc_fence_after();
-            const uint32_t tcol = tlane + a * kACols;
-#pragma unroll
-            for (int sb = 0; sb < 8; ++sb) {
-                const PairScale& z = ps[sb >> 1];
-                const bool hiL = sb & 1;
-                const __half2 s1 = hiL ? __high2half2(as_h2(z.s1)) : __low2half2(as_h2(z.s1));
-                const __half2 n1 = hiL ? __high2half2(as_h2(z.n1)) : __low2half2(as_h2(z.n1));
-                const __half2 s16 = hiL ? __high2half2(as_h2(z.s16)) : __low2half2(as_h2(z.s16));
-                const __half2 n16 = hiL ? __high2half2(as_h2(z.n16)) : __low2half2(as_h2(z.n16));
-                const __half2 nbh = hiL ? __high2half2(as_h2(z.nbh)) : __low2half2(as_h2(z.nbh));
-                uint32_t out[16];
-                dq_word(qv[sb].x, s1, n1, s16, n16, d2, nbh, out + 0);
-                dq_word(qv[sb].y, s1, n1, s16, n16, d2, nbh, out + 4);
-                dq_word(qv[sb].z, s1, n1, s16, n16, d2, nbh, out + 8);
-                dq_word(qv[sb].w, s1, n1, s16, n16, d2, nbh, out + 12);
-                tmem_st16(tcol + 16 * sb, out);
-            }
-            // the -B_l step: k slots 0..7 = sub-blocks 0..7, slots 8..15 zero
-            const uint32_t bl[8] = {ps[0].nbl, ps[1].nbl, ps[2].nbl, ps[3].nbl, 0u, 0u, 0u, 0u};
-            tmem_st8(tcol + 128, bl);
             // the activation sums of this unit for the -B_l step: X[t][s] = sum of the 32
             // activations of token t in sub-block s (fp16, clamped); MP * 8 of them, shared
-            // out over the group's 128 threads
+            // out over the group's 128 threads.  Formed before the wait for the A buffer: the
+            // sums' slot was last read by the MMAs of unit j - kXRing, which finished before
+            // the slot was refilled.
             const int xs = static_cast<int>(j % kXRing);
             if (!warp_wait(&xfull[xs], (j / kXRing) & 1, flags)) break;
             const uint8_t* xt = xring + xs * C::kXSlot;
@@ -626,11 +621,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sum = __hmin(__hmax(sum, __ushort_as_half(0xFBFFu)), __ushort_as_half(0x7BFFu));
                 *reinterpret_cast<__half*>(xst + (t >> 3) * 256 + (t & 7) * 16 + sb * 2) = sum;
             }
-            fence_proxy_async_smem();  // the sums are read by the tensor core
+
+            // the A buffer was last read by the MMAs of unit j - kNA
+            if (j >= kNA && !warp_wait(&tempty[(j - kNA) % kTB], ((j - kNA) / kTB) & 1, flags)) break;
+            tc_fence_after();
+            const uint32_t tcol = tlane + a * kACols;
+#pragma unroll
+            for (int sb = 0; sb < 8; ++sb) {
+                const PairScale& z = ps[sb >> 1];
+                const bool hiL = sb & 1;
+                const __half2 s1 = hiL ? __high2half2(as_h2(z.s1)) : __low2half2(as_h2(z.s1));
+                const __half2 n1 = hiL ? __high2half2(as_h2(z.n1)) : __low2half2(as_h2(z.n1));
+                const __half2 s16 = hiL ? __high2half2(as_h2(z.s16)) : __low2half2(as_h2(z.s16));
+                const __half2 n16 = hiL ? __high2half2(as_h2(z.n16)) : __low2half2(as_h2(z.n16));
+                const __half2 nbh = hiL ? __high2half2(as_h2(z.nbh)) : __low2half2(as_h2(z.nbh));
+                uint32_t out[16];
+                dq_word(qv[sb].x, s1, n1, s16, n16, d2, nbh, out + 0);
+                dq_word(qv[sb].y, s1, n1, s16, n16, d2, nbh, out + 4);
+                dq_word(qv[sb].z, s1, n1, s16, n16, d2, nbh, out + 8);
+                dq_word(qv[sb].w, s1, n1, s16, n16, d2, nbh, out + 12);
+                tmem_st16(tcol + 16 * sb, out);
+            }
+            // the -B_l step's A row: k slots 0..7 = sub-blocks 0..7 (slots 8..15 stay zero)
+            *reinterpret_cast<uint4*>(blt + a * kBlBytes + (row >> 3) * 256 + (row & 7) * 16) =
+                make_uint4(ps[0].nbl, ps[1].nbl, ps[2].nbl, ps[3].nbl);
+            fence_proxy_async_smem();  // the sums and the -B_l row are read by the tensor core
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&tfull[a]);
+            if (lane == 0) mbar_arrive(&tfull[j % kTB]);
         }
         if (flags[0] && lane == 0) fail(p.err, flags);
         named_bar_sync(kBarTeardown, kTmemUsers);

@@ -101,15 +101,18 @@ def test_independent_step_rows_do_not_depend_on_m(backend_ms):
             assert np.array_equal(a[:m].view(np.uint32), b.view(np.uint32))
 
 
-@pytest.mark.parametrize("m", [1, 8, 16])
-def test_persistent_step_many_small_matrices(m):
-    """Forty matrices, most smaller than one unit per CTA, in one persistent launch."""
+@pytest.mark.parametrize("be_m", [(1, 1), (1, 8), (1, 16), (2, 24), (2, 64)],
+                         ids=["mma_sync-1", "mma_sync-8", "mma_sync-16", "tcgen05-24", "tcgen05-64"])
+def test_persistent_step_many_small_matrices(be_m):
+    """Forty matrices, most smaller than one unit per CTA, in one persistent launch: pieces of
+    one or two units, row tiles that only one of the tensor-core issuers touches."""
     from bit_weight_streaming_q4_gb300 import Step
     torch = torch_cuda()
+    be, m = be_m
     rng = np.random.default_rng(5)
     mats = [synth.Matrix(f"s{i}", int(rng.integers(1, 2000)), 256 * int(rng.integers(1, 12)), 100 + i)
             for i in range(40)]
-    qs, xs, ys, refs = _setup(1, m, mats)
+    qs, xs, ys, refs = _setup(be, m, mats)
     step = Step(qs, xs, ys, m, flags=1)
     for _ in range(2):
         step.launch()
@@ -157,3 +160,40 @@ def test_persistent_step_rejects_repeated_handle():
     with pytest.raises(QmmError):
         Step([q, q], [x, x], [y, y], 4, flags=1)
     Step([q, q], [x, x], [y, y], 4).close()   # the graph runs them one after the other
+
+
+@pytest.mark.parametrize("m", [20, 32, 64])
+def test_tcgen05_step_sustained_launches(m):
+    """Forty back-to-back launches of a decode-sized persistent tcgen05 step (two layers of the
+    27B shapes and the lm_head, 1.4 GB of weights): no wait runs out and every launch gives
+    the first launch's bits.  The buffer handshakes only race under sustained load."""
+    from bit_weight_streaming_q4_gb300 import Step
+    torch = torch_cuda()
+    mats = synth.stack(2)
+    qs, xs, xs_host, ys = [], [], [], []
+    for mat in mats:
+        blocks = synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id)
+        qs.append(make(blocks, m_max=m, backend=2))
+        del blocks
+        x = synth.x_f16(m, mat.k, seed=0, tensor_id=synth.X_ID_OFFSET + mat.tensor_id)
+        xs_host.append(x)
+        xs.append(torch.from_numpy(x.view(np.int16)).cuda().view(torch.float16))
+        ys.append(torch.zeros((m, mat.n), dtype=torch.float32, device="cuda"))
+    step = Step(qs, xs, ys, m, flags=1)
+    step.launch()
+    torch.cuda.synchronize()
+    first = [y.cpu().numpy().copy() for y in ys]
+    for rep in range(4):
+        for _ in range(10):
+            step.launch()
+        torch.cuda.synchronize()
+        for a, y, mat in zip(first, ys, mats):
+            assert np.array_equal(a.view(np.uint32), y.cpu().numpy().view(np.uint32)), (rep, mat.name)
+    assert all(q.error() == 0 for q in qs)
+    step.close()
+    # three sampled output rows of each matrix checked against the oracle
+    for mat, a, x in zip(mats, first, xs_host):
+        rows = np.array([0, mat.n // 2, mat.n - 1])
+        blocks = synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id, rows=rows)
+        y_ref, s_ref = oracle.qmm(blocks, x)
+        assert_parity(a[:, rows], y_ref, s_ref, mat.name)
