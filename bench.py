@@ -34,11 +34,18 @@ if ROOT not in sys.path:
 import synth  # noqa: E402
 
 METRIC = "Q4K x M-row decode GEMM: weight GB/s (% of HBM peak) and step tok/s at M=1/12/64"
-# DRAM bytes per 256-row unit measured by ncu for the mma.sync step kernel (profiles/
-# stream_kernel_step_m12.md); valid only for the kernel source it was taken from
-TRAFFIC_PER_UNIT = {"source": "bit_weight_streaming_q4_gb300/csrc/qmm_b1.cu",
-                    "sha256": "43d77ce69d57d591d1ae8852fdc3a0d12692e52edc2c34708f401cbef0162db2",
-                    "bytes": 37194.0}
+# DRAM bytes per work unit of each backend's persistent step launch, measured by ncu
+# (profiles/stream_kernel_step_m12.md, profiles/tc_kernel_step_m12.md); each is valid only for
+# the kernel source it was taken from
+TRAFFIC_PER_UNIT = {
+    1: {"source": "bit_weight_streaming_q4_gb300/csrc/qmm_b1.cu",
+        "sha256": "43d77ce69d57d591d1ae8852fdc3a0d12692e52edc2c34708f401cbef0162db2",
+        "bytes": 37194.0},
+    2: {"source": "bit_weight_streaming_q4_gb300/csrc/qmm_b2.cu",
+        "sha256": "29081b5a4e56c527a88b7a622500e1894233e87e1b720563f78d1026a98da6a2",
+        "bytes": 18590.5},
+}
+KERNEL_NAME = {1: "qmm::b1::stream_kernel<2>", 2: "qmm::b2::tc_kernel<16>"}
 HEADLINE_M = 12
 EXTRA_M = (1, 64)
 NOMINAL_HBM_GBS = 8000.0
@@ -135,21 +142,27 @@ class ClockSampler:
 class Stack:
     """All matrices of the step resident on the GPU, with activations and outputs."""
 
-    def __init__(self, layers: int, m_max: int, torch, seed: int = 0, wide_m: int = 0):
+    def __init__(self, layers: int, m_max: int, torch, seed: int = 0, wide_m: int = 0,
+                 narrow_m: int = 0):
         """Handles for runs of up to m_max rows (qs); with wide_m, a second set of handles for
-        runs of up to wide_m rows (qs_wide), created from the same blocks."""
+        runs of up to wide_m rows (qs_wide), and with narrow_m a third for runs of up to
+        narrow_m rows (qs_narrow), all created from the same blocks (the automatic backend
+        follows each set's m_max)."""
         from bit_weight_streaming_q4_gb300 import Qmm
         self.torch = torch
         self.mats = synth.stack(layers)
         self.m_max = m_max
         rows = max(m_max, wide_m)
-        self.qs, self.qs_wide = [], []
+        self.narrow_m = narrow_m
+        self.qs, self.qs_wide, self.qs_narrow = [], [], []
         for mat in self.mats:
             blocks = synth.q4k_matrix(mat.n, mat.k, seed=seed, tensor_id=mat.tensor_id)
             dev = torch.from_numpy(blocks.reshape(-1)).cuda()
             self.qs.append(Qmm(dev, mat.n, mat.k, m_max=m_max))
             if wide_m:
                 self.qs_wide.append(Qmm(dev, mat.n, mat.k, m_max=wide_m))
+            if narrow_m:
+                self.qs_narrow.append(Qmm(dev, mat.n, mat.k, m_max=narrow_m))
             del dev
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
@@ -172,6 +185,8 @@ class Stack:
         self.y = torch.zeros(off, dtype=torch.float32, device="cuda")
 
     def handles(self, m):
+        if self.narrow_m and m <= self.narrow_m:
+            return self.qs_narrow
         return self.qs if m <= self.m_max else self.qs_wide
 
     def x_ptrs(self):
@@ -187,19 +202,23 @@ class Stack:
         return self.weight_bytes, xb, yb
 
 
-def measured_traffic(stack):
-    """DRAM bytes of one step launch from the ncu capture, scaled by the launch's units; None
-    when the kernel source differs from the one the counters were taken from."""
+def measured_traffic(handles):
+    """DRAM bytes of one step launch over `handles` from the ncu capture of their backend,
+    scaled by the launch's units; None when there is no capture or the kernel source differs
+    from the one the counters were taken from."""
     import hashlib
-    path = os.path.join(ROOT, TRAFFIC_PER_UNIT["source"])
+    ref = TRAFFIC_PER_UNIT.get(int(handles[0].info().backend))
+    if ref is None:
+        return None
+    path = os.path.join(ROOT, ref["source"])
     try:
         with open(path, "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != TRAFFIC_PER_UNIT["sha256"]:
+            if hashlib.sha256(f.read()).hexdigest() != ref["sha256"]:
                 return None
     except OSError:
         return None
-    units = sum(q.info().units for q in stack.qs)
-    return TRAFFIC_PER_UNIT["bytes"] * units
+    units = sum(q.info().units for q in handles)
+    return ref["bytes"] * units
 
 
 def time_graph(torch, step, steps, warmup, stream):
@@ -366,9 +385,11 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-    # decode handles (mma.sync, up to 16 rows) for M = 1 and 12; tcgen05 handles for M = 64
+    # decode handles: up to 16 rows (tcgen05) for M = 12, up to 8 rows (mma.sync) for M = 1,
+    # up to 64 rows (tcgen05) for M = 64
     wide = 0 if args.no_extra else max(m for m in EXTRA_M)
-    stack = Stack(args.layers, 16, torch, wide_m=wide if wide > 16 else 0)
+    narrow = 0 if args.no_extra or min(EXTRA_M) > 8 else 8
+    stack = Stack(args.layers, 16, torch, wide_m=wide if wide > 16 else 0, narrow_m=narrow)
     stream = torch.cuda.Stream()
     n_mats = len(stack.mats)
 
@@ -466,8 +487,9 @@ def run_ours(args, rank, world, local_rank):
                                 ydev[b:b + HEADLINE_M * mat.n].view(np.uint32))
                  for mat, a, b in zip(stack.mats, yo, stack.y_off))
 
+    head_backend = int(stack.handles(HEADLINE_M)[0].info().backend)
     by_m = {str(HEADLINE_M): {"weight_gbs": value / world, "tok_s": HEADLINE_M / step_s,
-                              "ms_per_step": step_s * 1e3, "runs": "independent", "backend": 1}}
+                              "ms_per_step": step_s * 1e3, "runs": "independent", "backend": head_backend}}
     # the same step as a chain of dependent runs (each matrix may read the previous one's
     # output): a CUDA graph of runs linked by programmatic dependent launch
     steps_dep = max(20, args.steps // 2)
@@ -494,7 +516,7 @@ def run_ours(args, rank, world, local_rank):
         cpu = {"value": c["gbs"], "unit": "GB/s", "cores": c["cores"], "kind": "oracle",
                "sample": c["sample"]}
 
-    info = stack.qs[0].info()
+    info = stack.handles(HEADLINE_M)[0].info()
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
@@ -509,8 +531,8 @@ def run_ours(args, rank, world, local_rank):
         "by_m": by_m,
         "dependent_step": dependent,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": measured_traffic(stack),
-                     "kernel": "qmm::b1::stream_kernel<2> (one persistent launch per step)",
+                     "frac": achieved / hbm, "traffic": measured_traffic(stack.handles(HEADLINE_M)),
+                     "kernel": f"{KERNEL_NAME[head_backend]} (one persistent launch per step)",
                      "note": f"algorithmic bytes per launch (weights + x + y of the 257 matrices) "
                              f"/ launch time; peak is the {peak_kind} copy bandwidth"},
         "cpu_baseline": cpu,

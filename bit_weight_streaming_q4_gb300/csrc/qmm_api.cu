@@ -58,6 +58,9 @@ int32_t per_launch(const qmm_handle h) {
     return h->backend == QMM_BACKEND_TCGEN05 ? qmm::b2::kMaxM : qmm::b1::kMaxM;
 }
 
+// Largest m_max for which QMM_BACKEND_AUTO picks the mma.sync backend.
+constexpr int64_t kAutoMmaSyncMaxM = 8;
+
 qmm_status launch_run(qmm_handle h, const void* x, int64_t m, float* y, cudaStream_t s, bool pdl) {
     const int64_t K = h->d.k, N = h->d.n;
     const int64_t step = per_launch(h);
@@ -144,11 +147,12 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
     if (!h) return QMM_ERR_OOM;
     h->magic = kMagic;
     h->device = dev;
-    // Auto: the register-fed mma.sync stream for handles that never see more than 16 rows,
-    // tcgen05 otherwise.  Fixed per handle (never per run), so that a row's result does not
+    // Auto: the register-fed mma.sync stream for handles that never see more than 8 rows (one
+    // n8 fragment per MMA), tcgen05 otherwise (from 9 rows on it streams faster than two
+    // mma.sync fragments).  Fixed per handle (never per run), so that a row's result does not
     // depend on how many rows it is batched with.
     if (opt.backend == QMM_BACKEND_AUTO)
-        h->backend = opt.m_max <= qmm::b1::kMaxM ? QMM_BACKEND_MMA_SYNC : QMM_BACKEND_TCGEN05;
+        h->backend = opt.m_max <= kAutoMmaSyncMaxM ? QMM_BACKEND_MMA_SYNC : QMM_BACKEND_TCGEN05;
     else
         h->backend = opt.backend;
     const bool tc = h->backend == QMM_BACKEND_TCGEN05;

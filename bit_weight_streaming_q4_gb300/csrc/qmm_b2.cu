@@ -18,9 +18,9 @@
 // Warp roles of a persistent CTA (one per SM, 16 warps):
 //   warps 0-7   dequantisation, two groups of four; group g takes the units j = g (mod 2)
 //               of the CTA's piece, one output row per thread (warp w owns tensor-memory
-//               lanes 32(w%4)..+31), and writes fp16 weights into A buffer j mod 3 in
-//               tensor memory (three buffers, so that a group can dequantise its next unit
-//               while the tensor core still reads the last two);
+//               lanes 32(w%4)..+31), and writes fp16 weights into A buffer j mod kNA in
+//               tensor memory (kNA = 3 where there is room, so that a group can dequantise
+//               its next unit while the tensor core still reads the last two);
 //   warp 8      weight producer: 1-D bulk copies of the units into a shared-memory ring,
 //               across matrix boundaries;
 //   warp 9      activations: 2-D TMA (128-byte swizzle) of x[0..MP-1][kb*256..+256] for each
@@ -29,8 +29,7 @@
 //   warps 10, 15 tcgen05.mma issue (one thread each), warp 10 for the units of group 0 and
 //               warp 15 for those of group 1: A = weights in tensor memory (M = 128 rows),
 //               B = x in shared memory (N = MP tokens), fp32 accumulators in tensor memory,
-//               one per issuing warp (double-buffered per row tile where tensor memory
-//               has room: MP <= 32).  A single thread
+//               one per issuing warp, double-buffered per row tile.  A single thread
 //               cannot keep the tensor core busy: after a burst of MMAs its next
 //               shared-memory access (the mbarrier wait for the next unit) stalls until the
 //               burst has drained, so two issuers take turns;
@@ -68,11 +67,10 @@ constexpr int kThreads = (kMmaWarp1 + 1) * 32;  // 512: 128 registers per thread
 constexpr int kEpiThreads = 128;
 constexpr int kTmemCols = 512;
 constexpr int kACols = 128;  // one unit of fp16 weights: 128 rows x 256 k
-constexpr int kNA = 3;       // A buffers in tensor memory, unit j -> buffer j mod 3
 // The handshakes on the A buffers (tfull: written; tempty: read by the MMAs) use a pair of
 // mbarriers per unit j mod 6, so that each barrier only ever serves one dequant group, one
-// issuer and one buffer, and no waiter can fall two phases behind (a parity wait cannot tell
-// that from a phase already done).
+// issuer and one buffer (unit j -> buffer j mod kNA, kNA = 2 or 3), and no waiter can fall
+// two phases behind (a parity wait cannot tell that from a phase already done).
 constexpr int kTB = 6;
 constexpr int kBlBytes = kRows * 32;  // A tile of the -B_l step: [128 rows][16 k] fp16
 // named barriers
@@ -88,11 +86,15 @@ struct Cfg {
     static constexpr int kXBox = MP * 128;    // one 64-wide k box of x
     static constexpr int kXSlot = 4 * kXBox;  // x tile of one unit
     static constexpr int kXsBytes = MP * 32;  // the B tile of the -B_l step: [MP tokens][16 k]
-    // accumulator buffers per issuer: two (the epilogue of a tile overlaps the next tile's
-    // MMAs) where tensor memory has room, else one
-    static constexpr int kAccBufs = MP == 64 ? 1 : 2;
+    // A buffers in tensor memory (unit j -> buffer j mod kNA): three where tensor memory has
+    // room, so that a group can dequantise its next unit while the tensor core still reads
+    // the last two; two at MP = 64, where the accumulators take the room.  Accumulators:
+    // two buffers per issuer, so that the epilogue of a tile overlaps the next tile's MMAs.
+    static constexpr int kNA = MP == 64 ? 2 : 3;
+    static constexpr int kAccBufs = 2;
     static constexpr int kAccCol = kNA * kACols;  // accumulator (issuer e, buffer b) at + (e * kAccBufs + b) * MP
     static_assert(kAccCol + 2 * kAccBufs * MP <= kTmemCols, "tensor memory budget");
+    static_assert(kTB % kNA == 0 && kTB % 2 == 0, "one barrier pair per unit mod kTB");
     static_assert(kWRing % kGroups == 0 && kXRing % kGroups == 0, "a slot must always feed the same group");
     static constexpr int kWOff = kXRing * kXSlot;
     static constexpr int kXsOff = kWOff + kWRing * kUnitBytes;
@@ -266,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint32_t*>(xsum + slot * C::kXsBytes + (r >> 3) * 256 + 128 + (r & 7) * 16 + e * 4) = 0u;
     }
     // ... and of the A tiles of the -B_l step
-    for (int i = tid; i < kNA * kRows * 4; i += kThreads) {
+    for (int i = tid; i < C::kNA * kRows * 4; i += kThreads) {
         const int slot = i / (kRows * 4), r = (i / 4) % kRows, e = i % 4;
         *reinterpret_cast<uint32_t*>(blt + slot * kBlBytes + (r >> 3) * 256 + 128 + (r & 7) * 16 + e * 4) = 0u;
     }
@@ -390,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int64_t u = ja; u < jb; ++u, ++j) {
                     if ((j & 1) != e) continue;
                     const int xs = static_cast<int>(j % kXRing);
-                    const int a = static_cast<int>(j % kNA);
+                    const int a = static_cast<int>(j % C::kNA);
                     const int tb = static_cast<int>(j % kTB);
                     if (!warp_wait(&tfull[tb], (j / kTB) & 1, flags)) {
                         live = false;
@@ -573,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t nunits = g1 - g0;
         for (int64_t j = g; j < nunits; j += kGroups) {
             const int s = static_cast<int>(j % kWRing);
-            const int a = static_cast<int>(j % kNA);
+            const int a = static_cast<int>(j % C::kNA);
             if (!warp_wait(&wfull[s], (j / kWRing) & 1, flags)) break;
             const uint8_t* u = wring + s * kUnitBytes;
             uint4 qv[8];
@@ -623,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 
             // the A buffer was last read by the MMAs of unit j - kNA
-            if (j >= kNA && !warp_wait(&tempty[(j - kNA) % kTB], ((j - kNA) / kTB) & 1, flags)) break;
+            if (j >= C::kNA && !warp_wait(&tempty[(j - C::kNA) % kTB], ((j - C::kNA) / kTB) & 1, flags)) break;
             tc_fence_after();
             const uint32_t tcol = tlane + a * kACols;
 #pragma unroll
