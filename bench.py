@@ -221,6 +221,46 @@ def measured_traffic(handles):
     return ref["bytes"] * units
 
 
+def lm_head_verify(stack, m, stream, reps=50):
+    """Per-launch time of the lm_head run that writes y[m, 151936] and of the fused argmax
+    (qmm_run_argmax) on the same handle and activations; the argmax is checked against the
+    plain run's y (exact: same arithmetic)."""
+    torch = stack.torch
+    i = len(stack.mats) - 1
+    q = stack.handles(m)[i]
+    mat = stack.mats[i]
+    x = stack.x[stack.x_off[i]:].data_ptr()
+    y = stack.y[stack.y_off[i]:]
+    idx = torch.empty(m, dtype=torch.int32, device="cuda")
+    val = torch.empty(m, dtype=torch.float32, device="cuda")
+    s = stream.cuda_stream
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    us_y = timed(lambda: q.run(x, y.data_ptr(), m, s))
+    yh = y[:m * mat.n].view(m, mat.n).cpu().numpy()
+    us_a = timed(lambda: q.run_argmax(x, idx, val, m, s))
+    ih, vh = idx.cpu().numpy(), val.cpu().numpy()
+    ref = np.argmax(yh, axis=1)
+    ok = bool(np.array_equal(ih, ref) and
+              np.array_equal(vh.view(np.uint32), yh[np.arange(m), ref].view(np.uint32)))
+    wb = mat.weight_bytes
+    return {"backend": int(q.info().backend), "us_write_y": us_y, "us_argmax": us_a,
+            "weight_gbs_write_y": wb / us_y / 1e3, "weight_gbs_argmax": wb / us_a / 1e3,
+            "y_bytes_not_written": 4 * m * mat.n, "argmax_matches_y": ok}
+
+
 def time_graph(torch, step, steps, warmup, stream):
     for _ in range(warmup):
         step.launch(stream.cuda_stream)
@@ -510,6 +550,12 @@ def run_ours(args, rank, world, local_rank):
                 last = len(stack.mats) - 1
                 by_m[str(m)]["parity"] = sampled_parity(stack, m, matrices=[0, 1, 2, 3, last])
 
+    # Greedy verification of the lm_head fused into its matmul (qmm_run_argmax) against the
+    # plain run that writes y, per launch, on the step's lm_head handles and activations
+    verify = None
+    if not args.no_extra:
+        verify = {str(m): lm_head_verify(stack, m, stream) for m in sorted({*EXTRA_M, HEADLINE_M})}
+
     cpu = None
     if rank == 0:
         c = cpu_oracle_sample(args.cpu_seconds)
@@ -530,6 +576,7 @@ def run_ours(args, rank, world, local_rank):
         "frac_of_hbm": {"measured": value / world / hbm, "nominal_8TBs": value / world / NOMINAL_HBM_GBS},
         "by_m": by_m,
         "dependent_step": dependent,
+        "lm_head_verify": verify,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": measured_traffic(stack.handles(HEADLINE_M)),
                      "kernel": f"{KERNEL_NAME[head_backend]} (one persistent launch per step)",

@@ -50,6 +50,7 @@ void free_handle(qmm_handle h) {
     if (h->err_host) cudaFreeHost(h->err_host);
     cudaFree(h->x_stage);
     cudaFree(h->y_stage);
+    cudaFree(h->amax_keys);
     h->magic = 0;
     delete h;
 }
@@ -61,13 +62,16 @@ int32_t per_launch(const qmm_handle h) {
 // Largest m_max for which QMM_BACKEND_AUTO picks the mma.sync backend.
 constexpr int64_t kAutoMmaSyncMaxM = 8;
 
-qmm_status launch_run(qmm_handle h, const void* x, int64_t m, float* y, cudaStream_t s, bool pdl) {
+// One run in launches of at most per_launch(h) rows.  With idx and val given, each launch
+// writes its rows' argmax column and value there instead of y (y is not touched).
+qmm_status launch_run(qmm_handle h, const void* x, int64_t m, float* y, cudaStream_t s, bool pdl,
+                      int32_t* idx = nullptr, float* val = nullptr) {
     const int64_t K = h->d.k, N = h->d.n;
     const int64_t step = per_launch(h);
     for (int64_t r0 = 0; r0 < m; r0 += step) {
         const int64_t mc = (m - r0 < step) ? m - r0 : step;
         const __half* xc = reinterpret_cast<const __half*>(x) + r0 * K;
-        float* yc = y + r0 * N;
+        float* yc = idx ? nullptr : y + r0 * N;
         const bool tc = h->backend == QMM_BACKEND_TCGEN05;
         qmm::MatDesc mat;
         cudaError_t e = tc ? qmm::b2::make_mat(&mat, h->wq, xc, yc, h->tickets, h->d.units, N,
@@ -84,6 +88,12 @@ qmm_status launch_run(qmm_handle h, const void* x, int64_t m, float* y, cudaStre
             p.count = 1;
             p.m = static_cast<int32_t>(mc);
             p.ws_cols = tc ? qmm::b2::mp_for(mc) : h->ws_cols;
+            if (idx) {
+                p.amax_keys = h->amax_keys;
+                p.amax_count = h->amax_count;
+                p.amax_idx = idx + r0;
+                p.amax_val = val + r0;
+            }
             e = tc ? qmm::b2::launch(mat, p, h->d.grid, s, pdl, false) : qmm::b1::launch(mat, p, h->d.grid, s, pdl, false);
         }
         if (e != cudaSuccess) return QMM_ERR_CUDA;
@@ -192,6 +202,11 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
     if (cudaMalloc(&h->ws, ws_bytes) != cudaSuccess) return fail(QMM_ERR_OOM);
     if (cudaMalloc(&h->tickets, d.tiles * sizeof(int)) != cudaSuccess) return fail(QMM_ERR_OOM);
     if (cudaMemsetAsync(h->tickets, 0, d.tiles * sizeof(int), s) != cudaSuccess) return fail(QMM_ERR_CUDA);
+    // argmax keys (one per row of a launch, at most 64) and their launch counter
+    constexpr size_t kAmaxBytes = 64 * sizeof(unsigned long long) + sizeof(unsigned long long);
+    if (cudaMalloc(&h->amax_keys, kAmaxBytes) != cudaSuccess) return fail(QMM_ERR_OOM);
+    h->amax_count = reinterpret_cast<int*>(h->amax_keys + 64);
+    if (cudaMemsetAsync(h->amax_keys, 0, kAmaxBytes, s) != cudaSuccess) return fail(QMM_ERR_CUDA);
     if (cudaHostAlloc(&h->err_host, sizeof(int), cudaHostAllocMapped) != cudaSuccess) return fail(QMM_ERR_OOM);
     *h->err_host = 0;
     if (cudaHostGetDevicePointer(&h->err_dev, h->err_host, 0) != cudaSuccess) return fail(QMM_ERR_CUDA);
@@ -230,6 +245,18 @@ qmm_status qmm_run(qmm_handle h, const void* x, int64_t m, float* y, void* strea
     if (!x || !y) return QMM_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(y)) return QMM_ERR_MISALIGNED;
     return launch_run(h, x, m, y, reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+qmm_status qmm_run_argmax(qmm_handle h, const void* x, int64_t m, int32_t* idx, float* val, void* stream) {
+    if (!live_handle(h)) return QMM_ERR_BAD_HANDLE;
+    if (*reinterpret_cast<volatile int*>(h->err_host)) return QMM_ERR_DEVICE_TIMEOUT;
+    if (m < 0) return QMM_ERR_INVALID_ARG;
+    if (m == 0) return QMM_OK;
+    if (m > h->m_max) return QMM_ERR_UNSUPPORTED_SHAPE;
+    if (!x || !idx || !val) return QMM_ERR_INVALID_ARG;
+    if (!aligned16(x) || (reinterpret_cast<uintptr_t>(idx) & 3) || (reinterpret_cast<uintptr_t>(val) & 3))
+        return QMM_ERR_MISALIGNED;
+    return launch_run(h, x, m, nullptr, reinterpret_cast<cudaStream_t>(stream), true, idx, val);
 }
 
 qmm_status qmm_run_host(qmm_handle h, const void* x_host, int64_t m, float* y_host, void* stream) {

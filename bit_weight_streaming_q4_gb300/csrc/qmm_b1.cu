@@ -85,7 +85,9 @@ struct Cfg {
     static constexpr int kFOff = kXOff + NT * kXRing * kXSlot;
     static constexpr int kBarOff = kFOff + kFRing * kFSlot;
     static constexpr int kNumBars = 2 * kWRing + NT * kXRing + 2 * kFRing + 2 * kEv;
-    static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;
+    // argmax launches: each consumer warp's best key per token, [warp 4][token 16]
+    static constexpr int kBestOff = kBarOff + kNumBars * 8 + 16;
+    static constexpr int kSmem = kBestOff + 4 * 16 * 8 + 1024;
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -404,6 +406,12 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     // ------------------------------------------------------------------ consumers
     const int g = lane >> 2;
     const int t = lane & 3;
+    // argmax launches: the best key of each token over this warp's final rows (one lane
+    // owns each entry)
+    const bool amax = p.amax_keys != nullptr;
+    unsigned long long* best = reinterpret_cast<unsigned long long*>(smem + C::kBestOff) + 16 * warp;
+    if (lane < 16) best[lane] = 0ull;
+    __syncwarp();
     griddep_wait();  // y, the partial slots and the tickets may still be in use by the previous kernel
     int64_t gseq = 0;  // position in the CTA's unit sequence (ring slots and phases)
     int64_t ev = 0;    // events handed to the helper
@@ -601,20 +609,53 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                     }
                 }
             }
-#pragma unroll
-            for (int r = 0; r < kRT; ++r)
+            if (amax) {
+                // token m = 8 nt + 2 t + par: the best of this thread's 8 rows, then of the
+                // 8 lanes sharing t (g = 0..7); lane t keeps the warp's best
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int row = 64 * warp + 16 * r + g + 8 * (e >> 1);
-                        const int m = nt * 8 + 2 * t + (e & 1);
-                        const int64_t n = tile * kRows + row;
-                        if (m < p.m && n < M.n) M.y[static_cast<int64_t>(m) * M.n + n] = acc[r][nt][e];
+                    for (int par = 0; par < 2; ++par) {
+                        unsigned long long key = 0ull;
+#pragma unroll
+                        for (int r = 0; r < kRT; ++r)
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const int64_t n = tile * kRows + 64 * warp + 16 * r + g + 8 * h;
+                                if (n < M.n) {
+                                    const unsigned long long k = amax_key(acc[r][nt][2 * h + par], n);
+                                    key = k > key ? k : key;
+                                }
+                            }
+#pragma unroll
+                        for (int sh = 4; sh < 32; sh <<= 1) {
+                            const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, sh);
+                            key = o > key ? o : key;
+                        }
+                        const int m = nt * 8 + 2 * t + par;
+                        if (g == 0 && m < p.m && key > best[m]) best[m] = key;
                     }
+            } else {
+#pragma unroll
+                for (int r = 0; r < kRT; ++r)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int row = 64 * warp + 16 * r + g + 8 * (e >> 1);
+                            const int m = nt * 8 + 2 * t + (e & 1);
+                            const int64_t n = tile * kRows + row;
+                            if (m < p.m && n < M.n) M.y[static_cast<int64_t>(m) * M.n + n] = acc[r][nt][e];
+                        }
+            }
             if (!whole) live = post();  // the helper may now reset the tile's ticket
         }
         enter(mk, mk.i + 1);
+    }
+    if (amax && live) {
+        __syncwarp();
+        if (lane < p.m) atomicMax(p.amax_keys + lane, best[lane]);
+        amax_finish_warp(p, 4 * static_cast<int>(gridDim.x), lane);
     }
 }
 

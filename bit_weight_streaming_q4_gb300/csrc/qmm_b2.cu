@@ -100,8 +100,10 @@ struct Cfg {
     static constexpr int kXsOff = kWOff + kWRing * kUnitBytes;
     static constexpr int kBlOff = kXsOff + kXRing * kXsBytes;
     static constexpr int kBarOff = kBlOff + kNA * kBlBytes;
-    static constexpr int kNumBars = 2 * kWRing + 2 * kXRing + 2 * kTB + 4 + 2 + 2;
-    static constexpr int kSmem = kBarOff + kNumBars * 8 + 16 + 1024;  // + alignment slack
+    static constexpr int kNumBars = 2 * kWRing + 2 * kXRing + 2 * kTB + 4 + 2 + 2 + 1;
+    // argmax launches: the epilogue warps' best keys, [warp 4][token MP]
+    static constexpr int kAmaxOff = kBarOff + kNumBars * 8 + 16;
+    static constexpr int kSmem = kAmaxOff + 4 * MP * 8 + 1024;  // + alignment slack
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -206,7 +208,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* evpart = accempty + 2;    // the four epilogue warps have written the partial
     uint64_t* evred = evpart + 1;       // ... have read the partials of the tile they reduced
     uint64_t* mmadone = evred + 1;      // [2]: every MMA of issuer e has finished
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mmadone + 2);
+    uint64_t* evamax = mmadone + 2;     // argmax launches: the four epilogue warps' keys are in
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(evamax + 1);
+    unsigned long long* amax_sm = reinterpret_cast<unsigned long long*>(smem + C::kAmaxOff);
     volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] abort
 
     const int tid = threadIdx.x;
@@ -259,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(evpart, 4);
         mbar_init(evred, 4);
+        mbar_init(evamax, 4);
         flags[0] = 0;
         fence_mbar_init();
     }
@@ -446,6 +451,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         griddep_wait();  // y, the partial slots and the tickets may still be in use by the previous kernel
         int64_t seg = 0, jl = 0;  // jl: local index of the tile's first unit in the piece
         bool live = true;
+        // argmax launches: this warp's best key of token m in lane m % 32 (best0: m < 32, best1:
+        // m >= 32), over the final values of the rows it owns
+        const bool amax = p.amax_keys != nullptr;
+        unsigned long long best0 = 0ull, best1 = 0ull;
         // All four warps arrive on `ev` (each at most once per launch); lane 0 of warp
         // kEpiWarp0 then waits for the other three.  False if that wait gave up.
         auto gather = [&](uint64_t* ev) -> bool {
@@ -541,10 +550,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                             acc[4 * f + 3] += pv[f].w;
                         }
                     }
+                    if (amax) {
+                        // per token: the warp's largest value (one redux over order-mapped
+                        // bits, 0 for rows past N; -0 counts as +0) and its lowest row
+                        // (ballot), folded into the owning lane's best key
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int m = c0 + i;
-                        if (m < p.m && n < M.n) M.y[static_cast<int64_t>(m) * M.n + n] = acc[i];
+                        for (int i = 0; i < 16; ++i) {
+                            const int m = c0 + i;
+                            if (m >= p.m) break;
+                            const uint32_t u = __float_as_uint(acc[i] + 0.0f);  // -0 -> +0
+                            const uint32_t o = n < M.n ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
+                            const uint32_t mx = __reduce_max_sync(0xffffffffu, o);
+                            const int first = __ffs(__ballot_sync(0xffffffffu, o == mx)) - 1;
+                            if ((m & 31) == lane && mx != 0u) {
+                                const uint32_t nf = static_cast<uint32_t>(n - lane + first);
+                                const unsigned long long key =
+                                    (static_cast<unsigned long long>(mx) << 32) | (0xFFFFFFFFu - nf);
+                                if (m < 32) best0 = key > best0 ? key : best0;
+                                else best1 = key > best1 ? key : best1;
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int m = c0 + i;
+                            if (m < p.m && n < M.n) M.y[static_cast<int64_t>(m) * M.n + n] = acc[i];
+                        }
                     }
                 }
                 tc_fence_before();
@@ -558,6 +589,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             enter(mk, mk.i + 1);
+        }
+        if (amax && live) {
+            // the CTA's best key per token (over the four warps) goes out as one atomic
+            if (lane < MP) amax_sm[q * MP + lane] = best0;
+            if (MP > 32 && lane + 32 < MP) amax_sm[q * MP + lane + 32] = best1;
+            const bool ok = gather(evamax);
+            if (warp == kEpiWarp0) {
+                if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+                    __syncwarp();  // the other lanes read after lane 0's wait
+                    for (int m = lane; m < p.m; m += 32) {
+                        unsigned long long k = amax_sm[m];
+#pragma unroll
+                        for (int w = 1; w < 4; ++w) k = amax_sm[w * MP + m] > k ? amax_sm[w * MP + m] : k;
+                        atomicMax(p.amax_keys + m, k);
+                    }
+                    amax_finish_warp(p, static_cast<int>(gridDim.x), lane);
+                } else {
+                    live = false;
+                }
+            }
         }
         if (!live && lane == 0) fail(p.err, flags);
         named_bar_sync(kBarTeardown, kTmemUsers);

@@ -52,10 +52,47 @@ struct LaunchParams {
     int* err;                // sticky error word (mapped host memory)
     int64_t units;           // units of all matrices of the launch
     int32_t count;           // matrices in this launch
-    int32_t m;               // rows of this launch, 1..16
+    int32_t m;               // rows of this launch (1..16 mma.sync, 1..64 tcgen05)
     int32_t ws_cols;         // floats per consumer thread in a partial slot
     int32_t pad;
+    // Row-wise argmax instead of y (single-matrix launches only; null otherwise): the
+    // launch folds (value, column) keys into amax_keys[m] (zero before and after a launch),
+    // and the last of its writer warps, counted in amax_count (zero before and after),
+    // decodes them into amax_idx[m] / amax_val[m].
+    unsigned long long* amax_keys;
+    int* amax_count;
+    int32_t* amax_idx;
+    float* amax_val;
 };
+
+// Argmax keys: the value's bits mapped to an unsigned order (larger value, larger key; -0
+// counts as +0) in the high half, the complement of the column in the low half, so that the
+// largest key is the largest value at its lowest column.  Key 0 is below every value.
+__device__ __forceinline__ unsigned long long amax_key(float v, int64_t n) {
+    const uint32_t u = __float_as_uint(v + 0.0f);
+    const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return (static_cast<unsigned long long>(o) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(n));
+}
+
+// Warp-collective, after the warp has folded its keys into p.amax_keys: the last of the
+// launch's `writers` warps to arrive decodes every row's key into amax_idx / amax_val (column
+// -1 if a row saw no column) and zeroes the keys and the counter for the next launch.
+__device__ __forceinline__ void amax_finish_warp(const LaunchParams& p, int writers, int lane) {
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) last = atomicAdd(p.amax_count, 1) == writers - 1;
+    if (!__shfl_sync(0xffffffffu, last, 0)) return;
+    __threadfence();
+    for (int m = lane; m < p.m; m += 32) {
+        const unsigned long long k = atomicExch(p.amax_keys + m, 0ull);
+        const uint32_t o = static_cast<uint32_t>(k >> 32);
+        p.amax_idx[m] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(k));
+        p.amax_val[m] = __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
+    }
+    __syncwarp();
+    if (lane == 0) atomicExch(p.amax_count, 0);
+}
 
 // Backend 2: tcgen05 streaming kernel (weights dequantised into tensor memory, x by TMA).
 namespace b2 {
@@ -108,4 +145,6 @@ struct qmm_handle_s {
     int* err_dev = nullptr;       // device view of the same word
     void* x_stage = nullptr;      // host_io staging
     float* y_stage = nullptr;
+    unsigned long long* amax_keys = nullptr;  // qmm_run_argmax: [64] keys, then the counter
+    int* amax_count = nullptr;
 };

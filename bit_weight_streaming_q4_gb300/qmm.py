@@ -70,6 +70,7 @@ def load(path: str = LIB_PATH):
                                       ctypes.POINTER(Options), vp]),
         "qmm_run": (ctypes.c_int, [vp, vp, i64, vp, vp]),
         "qmm_run_host": (ctypes.c_int, [vp, vp, i64, vp, vp]),
+        "qmm_run_argmax": (ctypes.c_int, [vp, vp, i64, vp, vp, vp]),
         "qmm_get_error": (ctypes.c_int, [vp]),
         "qmm_get_info": (ctypes.c_int, [vp, ctypes.POINTER(Info)]),
         "qmm_destroy": (ctypes.c_int, [vp]),
@@ -149,6 +150,14 @@ class Qmm:
             m = x.shape[0]
         st = current_stream() if stream is None else stream
         _check(load().qmm_run(self._h, _ptr(x), m, _ptr(y), st), "qmm_run")
+
+    def run_argmax(self, x, idx, val, m: int | None = None, stream: int | None = None) -> None:
+        """idx[:m], val[:m] = the column and value of each row's largest entry of x[:m] @ W^T
+        (lowest column on ties), without forming the product (idx int32, val fp32, device)."""
+        if m is None:
+            m = x.shape[0]
+        st = current_stream() if stream is None else stream
+        _check(load().qmm_run_argmax(self._h, _ptr(x), m, _ptr(idx), _ptr(val), st), "qmm_run_argmax")
 
     def run_host(self, x_host, y_host, m: int, stream: int | None = None) -> None:
         st = current_stream() if stream is None else stream

@@ -111,6 +111,23 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
 qmm_status qmm_run(qmm_handle h, const void* x, int64_t m, float* y, void* stream);
 
 /*
+ * Greedy verification head (page "Running 4 coding agents on one RTX 3090", sections "How
+ * parallel decoding works" and the greedy acceptance of draft tokens): for every row r < M
+ * of x, idx[r] = the column n of the largest y[r][n] and val[r] = that y[r][n], where y is
+ * what qmm_run would compute (same arithmetic, same bits); among equal largest values the
+ * lowest column wins.  y itself is never formed in memory: each launch folds the rows'
+ * maxima into the handle's key buffer and its last finishing warp writes idx and val.
+ *  x:    fp16 [M, K], device, row-major, 16-byte aligned.
+ *  idx:  int32 [M], device, 4-byte aligned; val: fp32 [M], device, 4-byte aligned.
+ * Calls on one handle must be ordered (same stream, or synchronised): they share its key
+ * buffer.  Results are undefined if some y[r][n] is NaN.  After a DEVICE_TIMEOUT the handle
+ * must be destroyed (its key buffer may hold a partial launch).
+ * Errors: BAD_HANDLE, INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA, DEVICE_TIMEOUT.
+ */
+qmm_status qmm_run_argmax(qmm_handle h, const void* x, int64_t m, int32_t* idx, float* val,
+                          void* stream);
+
+/*
  * Same as qmm_run with x and y in host memory (pinned memory gives asynchronous
  * copies): copies x to the handle's staging buffer, runs, copies y back, all on `stream`.
  * The caller must synchronise `stream` before reading y.  Needs opt.host_io at create.

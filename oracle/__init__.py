@@ -123,3 +123,15 @@ def max_threads() -> int:
 def tolerance(s_abs: np.ndarray) -> np.ndarray:
     """Per-element bound for the GPU result: 2e-3 * sum_k |w x| + 1e-6."""
     return 2e-3 * s_abs + 1e-6
+
+
+def argmax_rows(y: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """Greedy verification of each row (page "Running 4 coding agents on one RTX 3090",
+    section "How parallel decoding works": a drafted token is kept when it is the most likely
+    next token, i.e. the largest logit of its row): idx[r] = the column holding the row's
+    largest value, val[r] = that value.  The pages do not order equal maxima; the reading
+    taken here is the lowest column (numpy's argmax returns the first one)."""
+    y = np.asarray(y)
+    assert y.ndim == 2 and y.shape[1] > 0
+    idx = np.argmax(y, axis=1)
+    return idx, y[np.arange(y.shape[0]), idx]

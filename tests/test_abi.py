@@ -22,7 +22,7 @@ def test_header_declares_expected_api():
     assert names == sorted(["qmm_default_options", "qmm_create", "qmm_run", "qmm_run_host",
                             "qmm_get_error", "qmm_get_info", "qmm_destroy", "qmm_status_str",
                             "qmm_step_create", "qmm_step_launch", "qmm_step_destroy",
-                            "qmm_run_noalloc"])
+                            "qmm_run_noalloc", "qmm_run_argmax"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -66,6 +66,8 @@ def test_argument_errors_need_no_device(lib):
     assert lib.qmm_destroy(ctypes.c_void_p(0x1000)) == 7
     assert lib.qmm_get_error(None) == 7
     assert lib.qmm_step_launch(None, None) == 7
+    assert lib.qmm_run_argmax(None, buf, 1, buf, buf, None) == 7
+    assert lib.qmm_run_argmax(ctypes.c_void_p(0x1000), buf, 1, buf, buf, None) == 7
     assert lib.qmm_step_destroy(None) == 7
 
 

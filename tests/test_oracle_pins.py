@@ -254,3 +254,48 @@ def test_empty_shapes():
     assert y.shape == (0, 3)
     y, s = oracle.qmm(np.zeros((0, 1, 144), dtype=np.uint8), np.ones((2, 256), dtype=np.float16))
     assert y.shape == (2, 0)
+
+
+# --------------------------------------------------------------------- greedy verification
+def _brute_argmax(y):
+    """Plain loop: the first column holding the row's largest value."""
+    out = []
+    for row in y:
+        best = 0
+        for j in range(1, len(row)):
+            if row[j] > row[best]:
+                best = j
+        out.append(best)
+    return out
+
+
+def test_argmax_rows_brute_force_and_ties():
+    rng = np.random.default_rng(4)
+    # integer-valued rows with many repeated maxima, so ties are common
+    y = rng.integers(-3, 4, (40, 17)).astype(np.float64)
+    idx, val = oracle.argmax_rows(y)
+    assert list(idx) == _brute_argmax(y)
+    assert np.array_equal(val, y.max(axis=1))
+    # a tie between columns 5 and 11 (both hold the maximum): the lower column
+    t = np.zeros((1, 16))
+    t[0, 5] = t[0, 11] = 2.0
+    assert oracle.argmax_rows(t)[0][0] == 5
+    # negative rows and one column
+    assert oracle.argmax_rows(np.array([[-5.0, -1.0, -3.0]]))[0][0] == 1
+    assert oracle.argmax_rows(np.array([[-7.0]]))[0][0] == 0
+
+
+def test_argmax_of_identical_weight_rows_is_the_lower_row():
+    """Two output rows with the same blocks have equal logits; with both ahead of every other
+    row (closed form: all quants 15, every scale 63, min 0, so each weight is d*63*15, and
+    x = 1), greedy verification must name the lower row."""
+    n, k = 6, 256
+    blocks = np.zeros((n, 1, 144), dtype=np.uint8)
+    for r in range(n):
+        d = 0x3C00 if r in (2, 4) else 0x3800  # 1.0 for rows 2 and 4, 0.5 elsewhere
+        blocks[r, 0] = pack_block(d, 0, [63] * 8, [0] * 8, [15] * 256)
+    x = np.ones((1, k), dtype=np.float16)
+    y, _ = oracle.qmm(blocks, x)
+    assert y[0, 2] == y[0, 4] == 256 * 63 * 15 and y[0, 0] == 256 * 63 * 15 / 2
+    idx, val = oracle.argmax_rows(y)
+    assert idx[0] == 2 and val[0] == 256 * 63 * 15
