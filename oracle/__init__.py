@@ -56,6 +56,14 @@ def _load():
                                    ctypes.c_void_p, ctypes.c_int]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
+        lib.oracle_qmm_fmt.restype = ctypes.c_int
+        lib.oracle_qmm_fmt.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                       ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                       ctypes.c_void_p, ctypes.c_int]
+        lib.oracle_dequant_fmt.restype = ctypes.c_int
+        lib.oracle_dequant_fmt.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+        lib.oracle_q6k_quant.restype = ctypes.c_int
+        lib.oracle_q6k_quant.argtypes = [ctypes.c_void_p, ctypes.c_int]
         _lib = lib
     return _lib
 
@@ -87,8 +95,15 @@ def dequant_block(block: np.ndarray) -> np.ndarray:
 
 
 def dequant_matrix(blocks: np.ndarray) -> np.ndarray:
-    """[N, K/256, 144] blocks -> fp32 W[N, K]."""
-    n, kb, _ = blocks.shape
+    """[N, K/256, 144] blocks -> fp32 W[N, K] (other formats: double, by block size)."""
+    n, kb, nbytes = blocks.shape
+    if nbytes != 144:
+        per = FORMATS[nbytes][1]
+        out = np.empty((n, kb * per), dtype=np.float64)
+        for r in range(n):
+            for b in range(kb):
+                out[r, per * b:per * (b + 1)] = dequant_block_fmt(blocks[r, b])
+        return out
     out = np.empty((n, kb * 256), dtype=np.float32)
     for r in range(n):
         for b in range(kb):
@@ -96,24 +111,47 @@ def dequant_matrix(blocks: np.ndarray) -> np.ndarray:
     return out
 
 
+# block bytes -> (format id of the C oracle, weights per block)
+FORMATS = {144: (0, 256), 210: (1, 256), 34: (2, 32)}
+FORMAT_NAMES = {144: "Q4_K", 210: "Q6_K", 34: "Q8_0"}
+
+
 def qmm(blocks: np.ndarray, x: np.ndarray, nthreads: int = 0) -> tuple[np.ndarray, np.ndarray]:
     """y[M, N] = x W^T in double and S[M, N] = sum_k |w x|.
 
-    blocks: uint8 [N, K/256, 144] (GGUF order); x: float16 [M, K]."""
+    blocks: uint8 [N, blocks per row, block bytes] (GGUF order; 144 B Q4_K, 210 B Q6_K,
+    34 B Q8_0 blocks); x: float16 [M, K]."""
     blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
-    assert blocks.ndim == 3 and blocks.shape[2] == 144
+    assert blocks.ndim == 3 and blocks.shape[2] in FORMATS
+    fmt, per = FORMATS[blocks.shape[2]]
     n, kb = blocks.shape[0], blocks.shape[1]
-    k = kb * 256
+    k = kb * per
     x = np.ascontiguousarray(x, dtype=np.float16)
     assert x.ndim == 2 and x.shape[1] == k
     m = x.shape[0]
     y = np.empty((m, n), dtype=np.float64)
     s = np.empty((m, n), dtype=np.float64)
-    rc = _load().oracle_qmm(blocks.ctypes.data, n, k, x.view(np.uint16).ctypes.data, m,
-                            y.ctypes.data, s.ctypes.data, nthreads)
+    rc = _load().oracle_qmm_fmt(fmt, blocks.ctypes.data, n, k, x.view(np.uint16).ctypes.data, m,
+                                y.ctypes.data, s.ctypes.data, nthreads)
     if rc != 0:
         raise RuntimeError("oracle_qmm failed")
     return y, s
+
+
+def dequant_block_fmt(block: np.ndarray) -> np.ndarray:
+    """One block of any format (by its size) -> its weights in double."""
+    b = np.ascontiguousarray(block, dtype=np.uint8).ravel()
+    fmt, per = FORMATS[b.size]
+    w = np.empty(per, dtype=np.float64)
+    assert _load().oracle_dequant_fmt(fmt, b.ctypes.data, w.ctypes.data) == per
+    return w
+
+
+def q6k_quant(block: np.ndarray, i: int) -> int:
+    """The 6-bit quant of weight i of a 210-byte Q6_K block."""
+    b = np.ascontiguousarray(block, dtype=np.uint8).ravel()
+    assert b.size == 210
+    return int(_load().oracle_q6k_quant(b.ctypes.data, i))
 
 
 def max_threads() -> int:

@@ -134,6 +134,116 @@ int oracle_qmm(const uint8_t* blocks, int64_t N, int64_t K, const uint16_t* x, i
     return failed ? -1 : 0;
 }
 
+/*
+ * Other block formats of a mixed-quant model file (page "Running 4 coding agents on one RTX
+ * 3090", the note on mixed-quant builds; page "Breaking the limits of Qwen3.8-27B again",
+ * the int8 weights of its lm_head).  Their byte layouts are the GGUF conventions (readings,
+ * listed with the design notes); each weight is computed exactly in double:
+ *
+ * Q8_0: 34-byte blocks of 32 weights: bytes 0-1 d (fp16), 2-33 q[0..31] (int8);
+ *       weight i = d * q[i].
+ * Q6_K: 210-byte super-blocks of 256 weights: bytes 0-127 ql, 128-191 qh, 192-207 sc[0..15]
+ *       (int8), 208-209 d (fp16).  Weight i: h = i / 128, c = (i % 128) / 32, l = i % 32;
+ *       low 4 bits = (ql[64h + l + 32 (c & 1)] >> (4 (c >> 1))) & 15, high 2 bits =
+ *       (qh[32h + l] >> (2c)) & 3, q = low | high << 4 (0..63), sub-block j = i / 16;
+ *       weight i = d * sc[j] * (q - 32).
+ */
+enum { ORACLE_Q4_K = 0, ORACLE_Q6_K = 1, ORACLE_Q8_0 = 2 };
+
+static void dequant_q8_0(const uint8_t* blk, double* w) {
+    double d = oracle_f16_to_double((uint16_t)(blk[0] | (blk[1] << 8)));
+    for (int i = 0; i < 32; ++i) w[i] = d * (double)(int8_t)blk[2 + i];
+}
+
+/* The 6-bit quant of weight i (0..255) of a Q6_K block. */
+int oracle_q6k_quant(const uint8_t* blk, int i) {
+    const uint8_t* ql = blk;
+    const uint8_t* qh = blk + 128;
+    int h = i / 128, c = (i % 128) / 32, l = i % 32;
+    int lo = (ql[64 * h + l + 32 * (c & 1)] >> (4 * (c >> 1))) & 15;
+    int hi = (qh[32 * h + l] >> (2 * c)) & 3;
+    return lo | (hi << 4);
+}
+
+static void dequant_q6_k(const uint8_t* blk, double* w) {
+    double d = oracle_f16_to_double((uint16_t)(blk[208] | (blk[209] << 8)));
+    const int8_t* sc = (const int8_t*)(blk + 192);
+    for (int i = 0; i < 256; ++i) w[i] = d * (double)sc[i / 16] * (double)(oracle_q6k_quant(blk, i) - 32);
+}
+
+/*
+ * oracle_qmm for any of the three formats.  blocks: N rows of K / (weights per block)
+ * blocks in GGUF order (Q4_K 144 B / 256 weights, Q6_K 210 B / 256, Q8_0 34 B / 32).
+ * Q4_K goes through oracle_qmm above; the others dequantise a row in double and
+ * accumulate in double in increasing k.
+ */
+int oracle_qmm_fmt(int fmt, const uint8_t* blocks, int64_t N, int64_t K, const uint16_t* x, int64_t M,
+                   double* y, double* s_abs, int nthreads) {
+    if (fmt == ORACLE_Q4_K) return oracle_qmm(blocks, N, K, x, M, y, s_abs, nthreads);
+    int per = fmt == ORACLE_Q6_K ? 256 : fmt == ORACLE_Q8_0 ? 32 : 0;
+    int bytes = fmt == ORACLE_Q6_K ? 210 : 34;
+    if (!per || N < 0 || M < 0 || K < 0 || K % per != 0) return -1;
+    int64_t nb = K / per;
+    double* xd = (double*)malloc(sizeof(double) * (size_t)(M * K > 0 ? M * K : 1));
+    if (!xd) return -1;
+    for (int64_t i = 0; i < M * K; ++i) xd[i] = oracle_f16_to_double(x[i]);
+    int failed = 0;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads) reduction(| : failed)
+#endif
+    {
+        double* w = (double*)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+        if (!w) {
+            failed = 1;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(static)
+#endif
+            for (int64_t n = 0; n < N; ++n) {
+                for (int64_t b = 0; b < nb; ++b) {
+                    const uint8_t* blk = blocks + (n * nb + b) * bytes;
+                    if (fmt == ORACLE_Q6_K) dequant_q6_k(blk, w + b * per);
+                    else dequant_q8_0(blk, w + b * per);
+                }
+                for (int64_t m = 0; m < M; ++m) {
+                    const double* xrow = xd + m * K;
+                    double sum = 0.0, sum_abs = 0.0;
+                    for (int64_t kk = 0; kk < K; ++kk) {
+                        double prod = w[kk] * xrow[kk];
+                        sum += prod;
+                        sum_abs += fabs(prod);
+                    }
+                    y[m * N + n] = sum;
+                    if (s_abs) s_abs[m * N + n] = sum_abs;
+                }
+            }
+            free(w);
+        }
+    }
+    free(xd);
+    return failed ? -1 : 0;
+}
+
+/* Dequantise one block of format fmt (256 weights for Q4_K / Q6_K, 32 for Q8_0) to double. */
+int oracle_dequant_fmt(int fmt, const uint8_t* blk, double* w) {
+    if (fmt == ORACLE_Q4_K) {
+        float wf[256];
+        oracle_dequant_block(blk, wf);
+        for (int i = 0; i < 256; ++i) w[i] = wf[i];
+        return 256;
+    }
+    if (fmt == ORACLE_Q6_K) {
+        dequant_q6_k(blk, w);
+        return 256;
+    }
+    if (fmt == ORACLE_Q8_0) {
+        dequant_q8_0(blk, w);
+        return 32;
+    }
+    return -1;
+}
+
 /* Number of threads the OpenMP runtime would use (1 without OpenMP). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP

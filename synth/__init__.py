@@ -57,6 +57,9 @@ def _load():
         lib.synth_x_f16.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64,
                                     ctypes.c_uint64, ctypes.c_int64, ctypes.c_double,
                                     ctypes.c_double]
+        lib.synth_blocks.restype = None
+        lib.synth_blocks.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_uint64,
+                                     ctypes.c_uint64, ctypes.c_int64, ctypes.c_double]
         lib.synth_raw.restype = None
         lib.synth_raw.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64,
                                   ctypes.c_uint64]
@@ -106,6 +109,31 @@ def q4k_matrix(n: int, k: int, seed: int, tensor_id: int, rows: np.ndarray | Non
     for i, r in enumerate(rows):
         assert 0 <= r < n
         q4k_blocks(kb, seed, tensor_id, int(r) * kb, scale_mul, out[i].reshape(kb, BLOCK_BYTES))
+    return out
+
+
+# other block types of a mixed-quant model file: (block bytes, weights per block, d scale);
+# the scales keep |w| below about 1, like the Q4_K workloads
+Q6_K = (210, 256, 2e-4)
+Q8_0 = (34, 32, 1e-2)
+
+
+def fmt_matrix(fmt: tuple, n: int, k: int, seed: int, tensor_id: int,
+               rows: np.ndarray | None = None) -> np.ndarray:
+    """Weight matrix W[n, k] in block type fmt (Q6_K or Q8_0) as GGUF-ordered blocks,
+    uint8 [n, k / weights per block, block bytes]; with ``rows``, only those rows."""
+    nbytes, per, scale = fmt
+    assert k % per == 0
+    kb = k // per
+    rows_ = range(n) if rows is None else np.asarray(rows, dtype=np.int64)
+    if rows is None:
+        out = np.empty((n, kb, nbytes), dtype=np.uint8)
+        _load().synth_blocks(out.ctypes.data, n * kb, nbytes, seed, tensor_id, 0, scale)
+        return out
+    out = np.empty((len(rows_), kb, nbytes), dtype=np.uint8)
+    for i, r in enumerate(rows_):
+        assert 0 <= r < n
+        _load().synth_blocks(out[i].ctypes.data, kb, nbytes, seed, tensor_id, int(r) * kb, scale)
     return out
 
 

@@ -107,6 +107,34 @@ void synth_q4k_blocks(uint8_t* out, int64_t nblocks, uint64_t seed, uint64_t ten
 }
 
 /*
+ * Fill `nblocks` blocks of another GGUF block type, blocks first_block ..
+ * first_block+nblocks-1 of tensor (seed, tensor_id): every byte random from the counter
+ * stream, then the fp16 scale field(s) overwritten with fp16(|N(0,1)| * scale_mul).
+ *   bytes = 34  (Q8_0): d at bytes 0-1, 32 int8 quants.
+ *   bytes = 210 (Q6_K): d at bytes 208-209; ql, qh and the 16 int8 scales random.
+ * Each block draws from its own range of 32 counter values.
+ */
+void synth_blocks(uint8_t* out, int64_t nblocks, int64_t bytes, uint64_t seed, uint64_t tensor_id,
+                  int64_t first_block, double scale_mul) {
+    uint64_t key = synth_key(seed, tensor_id);
+    const int d_off = bytes == 34 ? 0 : (int)bytes - 2;
+#pragma omp parallel for schedule(static)
+    for (int64_t b = 0; b < nblocks; ++b) {
+        uint64_t base = (uint64_t)(first_block + b) * 32;
+        uint8_t* blk = out + bytes * b;
+        for (int64_t i = 0; i < bytes; i += 8) {
+            uint64_t r = ctr_rand(key, base + (uint64_t)(i / 8));
+            for (int64_t j = 0; j < 8 && i + j < bytes; ++j) blk[i + j] = (uint8_t)(r >> (8 * j));
+        }
+        double z0, z1;
+        box_muller(ctr_rand(key, base + 30), ctr_rand(key, base + 31), &z0, &z1);
+        uint16_t d = synth_f16_from_double(fabs(z0) * scale_mul);
+        blk[d_off] = (uint8_t)(d & 0xFF);
+        blk[d_off + 1] = (uint8_t)(d >> 8);
+    }
+}
+
+/*
  * Fill n fp16 activations, elements first .. first+n-1 of tensor (seed, tensor_id),
  * as N(0,1); with probability outlier_p an element is multiplied by outlier_mul before
  * rounding.  Element i uses normal number i of the pair stream (pairs from Box-Muller)

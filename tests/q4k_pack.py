@@ -43,3 +43,35 @@ def pack_block(d_bits: int, dmin_bits: int, sc, mn, q) -> np.ndarray:
            + pack_scales(sc, mn) + pack_quants(q))
     assert len(raw) == 144
     return np.frombuffer(raw, dtype=np.uint8).copy()
+
+
+def pack_q8_0(d_bits: int, q) -> np.ndarray:
+    """Q8_0 block (GGUF): bytes 0-1 d (fp16 LE), then the 32 quants as int8."""
+    q = [int(v) for v in q]
+    assert len(q) == 32 and all(-128 <= v < 128 for v in q)
+    raw = int(d_bits).to_bytes(2, "little") + bytes((v + 256) % 256 for v in q)
+    return np.frombuffer(raw, dtype=np.uint8).copy()
+
+
+def pack_q6_k(d_bits: int, sc, q) -> np.ndarray:
+    """Q6_K super-block (GGUF) from 16 int8 scales and 256 6-bit quants.
+
+    Written by walking the 256 weights and scattering each one's bits: weight i sits in
+    half h = i // 128 at position r = i % 128; its quarter c = r // 32 picks the ql byte
+    (first or second 32 of the half's 64) and its nibble (low for c < 2), and the 2-bit
+    field (2c .. 2c+1) of qh byte 32h + i % 32.  Bytes: ql 0-127, qh 128-191, scales
+    192-207, d 208-209."""
+    q = [int(v) for v in q]
+    sc = [int(v) for v in sc]
+    assert len(q) == 256 and all(0 <= v < 64 for v in q)
+    assert len(sc) == 16 and all(-128 <= v < 128 for v in sc)
+    ql, qh = [0] * 128, [0] * 64
+    for i, v in enumerate(q):
+        h, r = divmod(i, 128)
+        c, l = divmod(r, 32)
+        ql_index = 64 * h + l + 32 * (c % 2)
+        ql[ql_index] |= (v & 15) << (4 * (c // 2))
+        qh[32 * h + l] |= (v >> 4) << (2 * c)
+    raw = bytes(ql) + bytes(qh) + bytes((v + 256) % 256 for v in sc) + int(d_bits).to_bytes(2, "little")
+    assert len(raw) == 210
+    return np.frombuffer(raw, dtype=np.uint8).copy()

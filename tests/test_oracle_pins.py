@@ -299,3 +299,70 @@ def test_argmax_of_identical_weight_rows_is_the_lower_row():
     assert y[0, 2] == y[0, 4] == 256 * 63 * 15 and y[0, 0] == 256 * 63 * 15 / 2
     idx, val = oracle.argmax_rows(y)
     assert idx[0] == 2 and val[0] == 256 * 63 * 15
+
+
+# --------------------------------------------------------------------- other block formats
+def test_q8_0_closed_form_and_round_trip():
+    from q4k_pack import pack_q8_0
+    q = [-128, -1, 0, 1, 127] + [(7 * i) % 256 - 128 for i in range(27)]
+    blk = pack_q8_0(0x3800, q)  # d = 0.5
+    w = oracle.dequant_block_fmt(blk)
+    assert list(w) == [0.5 * v for v in q]
+    # x = e_k picks weight k of every row
+    blocks = np.stack([pack_q8_0(0x3C00, q)[None], pack_q8_0(0x4000, q[::-1])[None]])
+    for col in (0, 4, 31):
+        x = np.zeros((1, 32), dtype=np.float16)
+        x[0, col] = 1.0
+        y, s = oracle.qmm(blocks, x)
+        assert y[0, 0] == q[col] and y[0, 1] == 2.0 * q[::-1][col]
+
+
+def test_q6_k_closed_form_and_round_trip():
+    from q4k_pack import pack_q6_k
+    rng = np.random.default_rng(12)
+    q = rng.integers(0, 64, 256)
+    sc = rng.integers(-128, 128, 16)
+    blk = pack_q6_k(0x3400, sc, q)  # d = 0.25
+    for i in range(256):
+        assert oracle.q6k_quant(blk, i) == q[i]
+    w = oracle.dequant_block_fmt(blk)
+    assert np.array_equal(w, 0.25 * sc[np.arange(256) // 16] * (q - 32.0))
+    # a scale of zero zeroes its sub-block of 16 weights; q = 32 is a zero weight
+    sc2 = sc.copy()
+    sc2[5] = 0
+    q2 = q.copy()
+    q2[200] = 32
+    w2 = oracle.dequant_block_fmt(pack_q6_k(0x3400, sc2, q2))
+    assert np.all(w2[80:96] == 0) and w2[200] == 0
+
+
+@pytest.mark.parametrize("fmt,n,k,m", [("q8", 3, 64, 2), ("q8", 2, 256, 1), ("q6", 2, 256, 2), ("q6", 1, 512, 1)])
+def test_brute_force_tiny_formats(fmt, n, k, m):
+    """Exact rational sums for Q8_0 and Q6_K matrices against the oracle's double sums."""
+    f = synth.Q8_0 if fmt == "q8" else synth.Q6_K
+    blocks = synth.fmt_matrix(f, n, k, seed=13, tensor_id=n * 10 + m)
+    x = synth.x_f16(m, k, seed=13, tensor_id=70 + m)
+    y, s = oracle.qmm(blocks, x)
+    per = f[1]
+    for r in range(n):
+        # weights from the bytes, written out here without the oracle
+        wr = []
+        for b in range(k // per):
+            blk = blocks[r, b]
+            if fmt == "q8":
+                d = Fraction(float(np.frombuffer(blk[:2].tobytes(), dtype=np.float16)[0]))
+                wr += [d * int(np.int8(v)) for v in blk[2:34].view(np.int8)]
+            else:
+                d = Fraction(float(np.frombuffer(blk[208:210].tobytes(), dtype=np.float16)[0]))
+                scs = blk[192:208].view(np.int8)
+                for i in range(256):
+                    h, rr = divmod(i, 128)
+                    c, l = divmod(rr, 32)
+                    lo = (int(blk[64 * h + l + 32 * (c % 2)]) >> (4 * (c // 2))) & 15
+                    hi = (int(blk[128 + 32 * h + l]) >> (2 * c)) & 3
+                    wr.append(d * int(scs[i // 16]) * ((lo | hi << 4) - 32))
+        for t in range(m):
+            ye = sum(wk * Fraction(float(xv)) for wk, xv in zip(wr, x[t]))
+            se = sum(abs(wk * Fraction(float(xv))) for wk, xv in zip(wr, x[t]))
+            assert abs(Fraction(y[t, r]) - ye) <= Fraction(1, 10**9) * se + Fraction(1, 10**30)
+            assert abs(Fraction(s[t, r]) - se) <= Fraction(1, 10**9) * se + Fraction(1, 10**30)
