@@ -261,6 +261,46 @@ def lm_head_verify(stack, m, stream, reps=50):
             "y_bytes_not_written": 4 * m * mat.n, "argmax_matches_y": ok}
 
 
+def format_line(torch, fmt, code, m, stream, parity, reps=50):
+    """Per-launch time of one lm_head-shaped matrix (151936 x 5120) in another block format
+    at M rows, its weight GB/s, and a sampled oracle check of three rows."""
+    from bit_weight_streaming_q4_gb300 import Qmm
+    mat = synth.LM_HEAD
+    blocks = synth.fmt_matrix(fmt, mat.n, mat.k, seed=0, tensor_id=mat.tensor_id)
+    dev = torch.from_numpy(blocks.reshape(-1)).cuda()
+    q = Qmm(dev, mat.n, mat.k, m_max=16, format=code)
+    del dev
+    x = synth.x_f16(m, mat.k, seed=0, tensor_id=synth.X_ID_OFFSET + mat.tensor_id)
+    xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.float16)
+    yd = torch.empty((m, mat.n), dtype=torch.float32, device="cuda")
+    s = stream.cuda_stream
+    for _ in range(3):
+        q.run(xd, yd, m, s)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        q.run(xd, yd, m, s)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    info = q.info()
+    line = {"matrix": f"lm_head {mat.n} x {mat.k}", "m": m, "backend": int(info.backend),
+            "weight_bytes": int(info.weight_bytes), "us_per_launch": us,
+            "weight_gbs": info.weight_bytes / us / 1e3}
+    if parity:
+        import oracle
+        rows = np.array([0, mat.n // 2, mat.n - 1])
+        y_ref, s_ref = oracle.qmm(blocks[rows], x)
+        got = yd.cpu().numpy()[:, rows]
+        ratio = np.abs(got - y_ref) / (2e-3 * s_ref + 1e-6)
+        line["parity"] = {"checked_outputs": int(ratio.size), "max_err_over_bound": float(ratio.max()),
+                          "pass": bool(ratio.max() <= 1.0)}
+    q.close()
+    return line
+
+
 def time_graph(torch, step, steps, warmup, stream):
     for _ in range(warmup):
         step.launch(stream.cuda_stream)
@@ -553,8 +593,12 @@ def run_ours(args, rank, world, local_rank):
     # Greedy verification of the lm_head fused into its matmul (qmm_run_argmax) against the
     # plain run that writes y, per launch, on the step's lm_head handles and activations
     verify = None
+    formats = None
     if not args.no_extra:
         verify = {str(m): lm_head_verify(stack, m, stream) for m in sorted({*EXTRA_M, HEADLINE_M})}
+        # the other block formats of a mixed-quant file, on the lm_head shape at M = 12
+        formats = {name: format_line(torch, f, code, HEADLINE_M, stream, not args.no_parity)
+                   for name, f, code in (("Q6_K", synth.Q6_K, 1), ("Q8_0", synth.Q8_0, 2))}
 
     cpu = None
     if rank == 0:
@@ -577,6 +621,7 @@ def run_ours(args, rank, world, local_rank):
         "by_m": by_m,
         "dependent_step": dependent,
         "lm_head_verify": verify,
+        "formats": formats,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": measured_traffic(stack.handles(HEADLINE_M)),
                      "kernel": f"{KERNEL_NAME[head_backend]} (one persistent launch per step)",

@@ -94,7 +94,8 @@ qmm_status launch_run(qmm_handle h, const void* x, int64_t m, float* y, cudaStre
                 p.amax_idx = idx + r0;
                 p.amax_val = val + r0;
             }
-            e = tc ? qmm::b2::launch(mat, p, h->d.grid, s, pdl, false) : qmm::b1::launch(mat, p, h->d.grid, s, pdl, false);
+            e = tc ? qmm::b2::launch(mat, p, h->d.grid, s, pdl, false, h->format)
+                   : qmm::b1::launch(mat, p, h->d.grid, s, pdl, false);
         }
         if (e != cudaSuccess) return QMM_ERR_CUDA;
     }
@@ -111,6 +112,7 @@ void qmm_default_options(qmm_options* opt) {
     opt->backend = QMM_BACKEND_AUTO;
     opt->ctas_per_sm = 0;
     opt->host_io = 0;
+    opt->format = QMM_FORMAT_Q4_K;
 }
 
 const char* qmm_status_str(qmm_status s) {
@@ -137,8 +139,10 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
     qmm_default_options(&opt);
     if (opt_in) opt = *opt_in;
     if (opt.m_max < 1 || opt.ctas_per_sm < 0 || opt.ctas_per_sm > 4 || opt.backend < 0 ||
-        opt.backend > QMM_BACKEND_TCGEN05)
+        opt.backend > QMM_BACKEND_TCGEN05 || opt.format < QMM_FORMAT_Q4_K || opt.format > QMM_FORMAT_Q8_0)
         return QMM_ERR_INVALID_ARG;
+    // the mma.sync backend streams Q4_K only
+    if (opt.format != QMM_FORMAT_Q4_K && opt.backend == QMM_BACKEND_MMA_SYNC) return QMM_ERR_INVALID_ARG;
     if (n <= 0 || k <= 0 || k % 256 != 0) return QMM_ERR_UNSUPPORTED_SHAPE;
     if (blocks_on_device && !aligned16(blocks)) return QMM_ERR_MISALIGNED;
 
@@ -162,7 +166,8 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
     // mma.sync fragments).  Fixed per handle (never per run), so that a row's result does not
     // depend on how many rows it is batched with.
     if (opt.backend == QMM_BACKEND_AUTO)
-        h->backend = opt.m_max <= kAutoMmaSyncMaxM ? QMM_BACKEND_MMA_SYNC : QMM_BACKEND_TCGEN05;
+        h->backend = opt.m_max <= kAutoMmaSyncMaxM && opt.format == QMM_FORMAT_Q4_K ? QMM_BACKEND_MMA_SYNC
+                                                                                    : QMM_BACKEND_TCGEN05;
     else
         h->backend = opt.backend;
     const bool tc = h->backend == QMM_BACKEND_TCGEN05;
@@ -172,7 +177,8 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
     d.k = k;
     d.kb = k / 256;
     d.rows = tc ? qmm::b2::kRows : qmm::b1::kRows;
-    d.unit_bytes = tc ? qmm::b2::kUnitBytes : qmm::b1::kUnitBytes;
+    h->format = opt.format;
+    d.unit_bytes = tc ? qmm::b2::unit_bytes(opt.format) : qmm::b1::kUnitBytes;
     d.tiles = (n + d.rows - 1) / d.rows;
     d.units = d.tiles * d.kb;
     const int cps = opt.ctas_per_sm ? opt.ctas_per_sm : 1;
@@ -215,7 +221,7 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
         if (cudaMalloc(&h->y_stage, static_cast<size_t>(opt.m_max) * n * 4) != cudaSuccess) return fail(QMM_ERR_OOM);
     }
 
-    const size_t src_bytes = static_cast<size_t>(n) * d.kb * 144;
+    const size_t src_bytes = static_cast<size_t>(n) * (k / qmm::block_weights(opt.format)) * qmm::block_bytes(opt.format);
     const uint8_t* src = static_cast<const uint8_t*>(blocks);
     if (!blocks_on_device) {
         if (cudaMalloc(&staging, src_bytes) != cudaSuccess) return fail(QMM_ERR_OOM);
@@ -223,7 +229,7 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
             return fail(QMM_ERR_CUDA);
         src = staging;
     }
-    const cudaError_t re = tc ? qmm::b2::repack(src, h->wq, d, s) : qmm::b1::repack(src, h->wq, d, s);
+    const cudaError_t re = tc ? qmm::b2::repack(src, h->wq, d, opt.format, s) : qmm::b1::repack(src, h->wq, d, s);
     if (re != cudaSuccess) return fail(QMM_ERR_CUDA);
     if (cudaStreamSynchronize(s) != cudaSuccess) return fail(QMM_ERR_CUDA);
     cudaFree(staging);
@@ -294,14 +300,14 @@ qmm_status qmm_get_info(qmm_handle h, qmm_info* info) {
     info->grid = h->d.grid;
     info->units = h->d.units;
     info->rows_per_unit = h->d.rows;
-    info->weight_bytes = h->d.n * h->d.kb * 144;
+    info->weight_bytes = h->d.n * (h->d.k / qmm::block_weights(h->format)) * qmm::block_bytes(h->format);
     info->packed_bytes = h->wq_bytes;
     info->workspace_bytes = static_cast<int64_t>(h->d.grid) *
                                 (h->backend == QMM_BACKEND_TCGEN05 ? qmm::b2::kRows : qmm::b1::kConsumerThreads) *
                                 h->ws_cols * 4 +
                             h->d.tiles * 4;
     info->m_per_launch = per_launch(h);
-    info->reserved = 0;
+    info->format = h->format;
     return QMM_OK;
 }
 
@@ -327,6 +333,7 @@ struct qmm_step_s {
     int32_t* first_mat = nullptr; // device, [grid]
     float* ws = nullptr;          // split-K partial slots, one per CTA
     bool tcgen05 = false;         // the backend of every handle of a persistent step
+    int32_t format = QMM_FORMAT_Q4_K;  // ... and their block format
     int* err_host = nullptr;
     int* err_dev = nullptr;
     qmm::LaunchParams params = {};
@@ -366,7 +373,9 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
     const bool tc = be == QMM_BACKEND_TCGEN05;
     bool persistent = m <= (tc ? qmm::b2::kMaxM : qmm::b1::kMaxM) && !(flags & QMM_STEP_GRAPH) &&
                       (flags & QMM_STEP_INDEPENDENT);
-    for (int32_t i = 0; i < count; ++i) persistent = persistent && handles[i]->backend == be;
+    // one persistent launch runs one kernel: one backend and one block format
+    for (int32_t i = 0; i < count; ++i)
+        persistent = persistent && handles[i]->backend == be && handles[i]->format == handles[0]->format;
     if (persistent) {
         // a handle's tickets and partial slots serve one matrix of a launch at a time
         std::set<qmm_handle> seen(handles, handles + count);
@@ -421,6 +430,7 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
         }
         if (rc == QMM_OK) {
             st->tcgen05 = tc;
+            st->format = handles[0]->format;
             st->grid = grid;
             st->params.mats = st->mats;
             st->params.first_mat = st->first_mat;
@@ -469,7 +479,7 @@ qmm_status qmm_step_launch(qmm_step s, void* stream) {
     if (s->mats) {
         if (*reinterpret_cast<volatile int*>(s->err_host)) return QMM_ERR_DEVICE_TIMEOUT;
         const qmm::MatDesc unused = {};
-        const cudaError_t e = s->tcgen05 ? qmm::b2::launch(unused, s->params, s->grid, cs, true, true)
+        const cudaError_t e = s->tcgen05 ? qmm::b2::launch(unused, s->params, s->grid, cs, true, true, s->format)
                                          : qmm::b1::launch(unused, s->params, s->grid, cs, true, true);
         return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
     }

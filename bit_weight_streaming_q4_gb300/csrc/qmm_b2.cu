@@ -45,6 +45,7 @@
 // B_h + B_l; the weight written is fp16(d*P - B_h), and the -B_l part goes to the tensor
 // core as one extra K=16 step per unit: A = -B_l of the 8 sub-blocks (a small tile in
 // shared memory), B = the activation sums of the 8 sub-blocks.
+#include <cstring>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -77,15 +78,25 @@ constexpr int kBlBytes = kRows * 32;  // A tile of the -B_l step: [128 rows][16 
 constexpr int kBarTmem = 1, kBarTeardown = 2;
 constexpr int kTmemUsers = (kDqWarps + 2 + 4) * 32;  // dequant + MMA + epilogue warps
 
-template <int MP>
+// Ring depths (weight slots, activation slots) per block format and tile width, as deep as
+// shared memory allows; each a multiple of kGroups so that a slot always serves one group.
+constexpr int w_ring(int f, int mp) {
+    return f == QMM_FORMAT_Q4_K ? (mp == 16 ? 8 : mp == 32 ? 6 : 4) : f == QMM_FORMAT_Q6_K ? (mp == 64 ? 4 : 6) : 4;
+}
+constexpr int x_ring(int f, int mp) {
+    return f == QMM_FORMAT_Q4_K ? (mp == 16 ? 8 : mp == 32 ? 6 : 4) : mp == 16 ? (f == QMM_FORMAT_Q6_K ? 6 : 8)
+                                                                   : mp == 32 ? 4 : 2;
+}
+
+template <int MP, int F>
 struct Cfg {
-    // ring depths, as deep as shared memory allows: weight slots and activation slots, each a
-    // multiple of kGroups so that a slot (and its barriers) always serves the same group
-    static constexpr int kWRing = MP == 16 ? 8 : MP == 32 ? 6 : 4;
-    static constexpr int kXRing = MP == 16 ? 8 : MP == 32 ? 6 : 4;
+    static constexpr int kUnitBytes = unit_bytes(F);
+    static constexpr bool kMin = F == QMM_FORMAT_Q4_K;  // the format has a min term (the -B_l step)
+    static constexpr int kWRing = w_ring(F, MP);
+    static constexpr int kXRing = x_ring(F, MP);
     static constexpr int kXBox = MP * 128;    // one 64-wide k box of x
     static constexpr int kXSlot = 4 * kXBox;  // x tile of one unit
-    static constexpr int kXsBytes = MP * 32;  // the B tile of the -B_l step: [MP tokens][16 k]
+    static constexpr int kXsBytes = kMin ? MP * 32 : 0;  // the B tile of the -B_l step: [MP tokens][16 k]
     // A buffers in tensor memory (unit j -> buffer j mod kNA): three where tensor memory has
     // room, so that a group can dequantise its next unit while the tensor core still reads
     // the last two; two at MP = 64, where the accumulators take the room.  Accumulators:
@@ -99,7 +110,7 @@ struct Cfg {
     static constexpr int kWOff = kXRing * kXSlot;
     static constexpr int kXsOff = kWOff + kWRing * kUnitBytes;
     static constexpr int kBlOff = kXsOff + kXRing * kXsBytes;
-    static constexpr int kBarOff = kBlOff + kNA * kBlBytes;
+    static constexpr int kBarOff = kBlOff + (kMin ? kNA * kBlBytes : 0);
     static constexpr int kNumBars = 2 * kWRing + 2 * kXRing + 2 * kTB + 4 + 2 + 2 + 1;
     // argmax launches: the epilogue warps' best keys, [warp 4][token MP]
     static constexpr int kAmaxOff = kBarOff + kNumBars * 8 + 16;
@@ -176,6 +187,91 @@ __device__ __forceinline__ void dq_word(uint32_t w, __half2 s1, __half2 n1, __ha
     out[3] = as_u32(__hfma2(__hfma2(c67, s16, n16), d2, nbh));
 }
 
+// ---------------------------------------------------------------- Q8_0 and Q6_K units
+// Q8_0 unit (34,816 B, by repack()): quants [block 8][row 128][32 B] (the 32 int8 of the
+// row's block, in order), then the blocks' d [row 128][8 x fp16].  A byte b of quant q maps
+// to the fp16 code 1024 + (q + 128) (byte ^ 0x80 OR-ed into the mantissa of 1024), so
+// q = code - 1152 exactly and the weight is fp16(q * d), one rounding.
+__device__ __forceinline__ void q80_word(uint32_t w, __half2 d2, uint32_t* out) {
+    const uint32_t xw = w ^ 0x80808080u;
+    const __half2 nb = as_h2(0xE480E480u);  // -1152
+    out[0] = as_u32(__hmul2(__hadd2(as_h2(prmt(xw, 0x64646464u, 0x4140u)), nb), d2));
+    out[1] = as_u32(__hmul2(__hadd2(as_h2(prmt(xw, 0x64646464u, 0x4342u)), nb), d2));
+}
+
+__device__ __forceinline__ void dq_unit_q80(const uint8_t* u, int row, uint32_t tcol) {
+    const uint4 dv = lds128(u + kRows * 256 + row * 16);
+    const uint32_t dw[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        const uint4 qa = lds128(u + (b * kRows + row) * 32);
+        const uint4 qb = lds128(u + (b * kRows + row) * 32 + 16);
+        const __half2 d2 = (b & 1) ? __high2half2(as_h2(dw[b >> 1])) : __low2half2(as_h2(dw[b >> 1]));
+        uint32_t out[16];
+        q80_word(qa.x, d2, out + 0);
+        q80_word(qa.y, d2, out + 2);
+        q80_word(qa.z, d2, out + 4);
+        q80_word(qa.w, d2, out + 6);
+        q80_word(qb.x, d2, out + 8);
+        q80_word(qb.y, d2, out + 10);
+        q80_word(qb.z, d2, out + 12);
+        q80_word(qb.w, d2, out + 14);
+        tmem_st16(tcol + 16 * b, out);
+    }
+}
+
+// Q6_K unit (26,880 B, by repack()): low nibbles [chunk 8][row 128][16 B] (chunk c = weights
+// 32c .. 32c+31, words as in the Q4_K layout: nibble e of word i at bit 0,16,4,20,8,24,12,28),
+// high bit pairs [chunk 8][row 128][8 B] (a 16-bit field per word: e0,e4,e2,e6 in the low
+// byte, e1,e5,e3,e7 in the high byte, 2 bits each), scales [row 128][16 x int8], d [row 128]
+// [fp16].  The field, spread to bits 4-11 and 20-27 of a word, supplies the high bits of
+// codes 1024 + q (bits 4-5) and 1024 + 16q (bits 8-9) with one mask each, and those of the
+// shifted codes after >> 2.  q - 32 is then exact in fp16, and the weight is
+// fp16((q - 32) * (ds_h + ds_l)) with d * sc = ds_h + ds_l split exactly in fp32.
+__device__ __forceinline__ void q6_word(uint32_t w, uint32_t h, __half2 dsh, __half2 dsl, uint32_t* out) {
+    const uint32_t w8 = w >> 8, h2 = h >> 2;
+    const uint32_t c01 = and_or(h, 0x00300030u, and_or(w, 0x000F000Fu, 0x64006400u));
+    const uint32_t c23 = and_or(h, 0x03000300u, and_or(w, 0x00F000F0u, 0x64006400u));
+    const uint32_t c45 = and_or(h2, 0x00300030u, and_or(w8, 0x000F000Fu, 0x64006400u));
+    const uint32_t c67 = and_or(h2, 0x03000300u, and_or(w8, 0x00F000F0u, 0x64006400u));
+    const __half2 n1056 = as_h2(0xE420E420u), s16 = as_h2(0x2C002C00u), n96 = as_h2(0xD600D600u);
+    const __half2 p01 = __hadd2(as_h2(c01), n1056);          // q - 32
+    const __half2 p23 = __hfma2(as_h2(c23), s16, n96);        // (1024 + 16q) / 16 - 96 = q - 32
+    const __half2 p45 = __hadd2(as_h2(c45), n1056);
+    const __half2 p67 = __hfma2(as_h2(c67), s16, n96);
+    out[0] = as_u32(__hfma2(p01, dsh, __hmul2(p01, dsl)));
+    out[1] = as_u32(__hfma2(p23, dsh, __hmul2(p23, dsl)));
+    out[2] = as_u32(__hfma2(p45, dsh, __hmul2(p45, dsl)));
+    out[3] = as_u32(__hfma2(p67, dsh, __hmul2(p67, dsl)));
+}
+
+__device__ __forceinline__ void dq_unit_q6k(const uint8_t* u, int row, uint32_t tcol) {
+    constexpr int kQh = kRows * 128, kSc = kQh + kRows * 64, kD = kSc + kRows * 16;
+    const uint4 scv = lds128(u + kSc + row * 16);
+    const uint32_t scw[4] = {scv.x, scv.y, scv.z, scv.w};
+    const float d = __half2float(*reinterpret_cast<const __half*>(u + kD + row * 2));
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint4 ql = lds128(u + (c * kRows + row) * 16);
+        const uint2 qh = lds64(u + kQh + (c * kRows + row) * 8);
+        __half2 dsh[2], dsl[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {  // sub-blocks 2c and 2c + 1 (16 weights each)
+            const int sb = 2 * c + t;
+            const float dsc = d * static_cast<float>(static_cast<int8_t>(scw[sb >> 2] >> (8 * (sb & 3))));
+            const __half hh = __float2half_rn(dsc);
+            dsh[t] = __half2half2(hh);
+            dsl[t] = __half2half2(__float2half_rn(dsc - __half2float(hh)));
+        }
+        uint32_t out[16];
+        q6_word(ql.x, prmt(qh.x, 0u, 0x4140u) << 4, dsh[0], dsl[0], out + 0);
+        q6_word(ql.y, prmt(qh.x, 0u, 0x4342u) << 4, dsh[0], dsl[0], out + 4);
+        q6_word(ql.z, prmt(qh.y, 0u, 0x4140u) << 4, dsh[1], dsl[1], out + 8);
+        q6_word(ql.w, prmt(qh.y, 0u, 0x4342u) << 4, dsh[1], dsl[1], out + 12);
+        tmem_st16(tcol + 16 * c, out);
+    }
+}
+
 // Shared-memory descriptor of the -B_l step's A and B tiles ([rows][16 k] fp16): K-major, no
 // swizzle, core matrices of 8 rows x 16 bytes; the two k halves 128 bytes apart, 8-row groups
 // 256 bytes apart.
@@ -184,10 +280,11 @@ __device__ __forceinline__ uint64_t smem_desc_k16(uint32_t saddr) {
            (static_cast<uint64_t>(256 >> 4) << 32) | (static_cast<uint64_t>(1) << 46);
 }
 
-template <int MP>
+template <int MP, int F>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_kernel(const __grid_constant__ MatDesc single, const LaunchParams p) {
-    using C = Cfg<MP>;
+    using C = Cfg<MP, F>;
+    constexpr int kUnitBytes = C::kUnitBytes;
     constexpr int kWRing = C::kWRing;
     constexpr int kXRing = C::kXRing;
     extern __shared__ uint8_t smem_raw[];
@@ -267,15 +364,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         flags[0] = 0;
         fence_mbar_init();
     }
-    // the upper (always zero) k half of every -B_l step's B tile
-    for (int i = tid; i < kXRing * MP * 4; i += kThreads) {
-        const int slot = i / (MP * 4), r = (i / 4) % MP, e = i % 4;
-        *reinterpret_cast<uint32_t*>(xsum + slot * C::kXsBytes + (r >> 3) * 256 + 128 + (r & 7) * 16 + e * 4) = 0u;
-    }
-    // ... and of the A tiles of the -B_l step
-    for (int i = tid; i < C::kNA * kRows * 4; i += kThreads) {
-        const int slot = i / (kRows * 4), r = (i / 4) % kRows, e = i % 4;
-        *reinterpret_cast<uint32_t*>(blt + slot * kBlBytes + (r >> 3) * 256 + 128 + (r & 7) * 16 + e * 4) = 0u;
+    if constexpr (C::kMin) {
+        // the upper (always zero) k half of every -B_l step's B tile
+        for (int i = tid; i < kXRing * MP * 4; i += kThreads) {
+            const int slot = i / (MP * 4), r = (i / 4) % MP, e = i % 4;
+            *reinterpret_cast<uint32_t*>(xsum + slot * C::kXsBytes + (r >> 3) * 256 + 128 + (r & 7) * 16 + e * 4) = 0u;
+        }
+        // ... and of the A tiles of the -B_l step
+        for (int i = tid; i < C::kNA * kRows * 4; i += kThreads) {
+            const int slot = i / (kRows * 4), r = (i / 4) % kRows, e = i % 4;
+            *reinterpret_cast<uint32_t*>(blt + slot * kBlBytes + (r >> 3) * 256 + 128 + (r & 7) * 16 + e * 4) = 0u;
+        }
     }
     fence_proxy_async_smem();
     __syncthreads();
@@ -411,8 +510,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint64_t bdesc = smem_desc_sw128(xaddr + (kk >> 2) * C::kXBox + (kk & 3) * 32);
                             tc_mma_f16_ts(d_tmem, tbase + a * kACols + 8 * kk, bdesc, kIdesc, (!fresh || kk > 0) ? 1u : 0u);
                         }
-                        tc_mma_f16_ss(d_tmem, smem_desc_k16(smem_u32(blt + a * kBlBytes)),
-                                      smem_desc_k16(smem_u32(xsum + xs * C::kXsBytes)), kIdesc, 1u);
+                        if constexpr (C::kMin)
+                            tc_mma_f16_ss(d_tmem, smem_desc_k16(smem_u32(blt + a * kBlBytes)),
+                                          smem_desc_k16(smem_u32(xsum + xs * C::kXsBytes)), kIdesc, 1u);
                         tc_commit(&tempty[tb]);
                         tc_commit(&xempty[xs]);
                     }
@@ -629,75 +729,91 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int a = static_cast<int>(j % C::kNA);
             if (!warp_wait(&wfull[s], (j / kWRing) & 1, flags)) break;
             const uint8_t* u = wring + s * kUnitBytes;
-            uint4 qv[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) qv[i] = lds128(u + (i * kRows + row) * 16);
-            const uint4 hd = lds128(u + kQBytes + row * 16);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&wempty[s]);
+            if constexpr (F == QMM_FORMAT_Q4_K) {
+                uint4 qv[8];
+    #pragma unroll
+                for (int i = 0; i < 8; ++i) qv[i] = lds128(u + (i * kRows + row) * 16);
+                const uint4 hd = lds128(u + kQBytes + row * 16);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&wempty[s]);
 
-            // (scale, min) pairs of sub-blocks (0,1), (2,3) from the low 6 bits of s[0..7] and
-            // (4,5), (6,7) from s[8..11] plus the top 2 bits of s[0..7]
-            const uint32_t SClo = hd.y & 0x3F3F3F3Fu;
-            const uint32_t MNlo = hd.z & 0x3F3F3F3Fu;
-            const uint32_t SChi = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
-            const uint32_t MNhi = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
-            const uint32_t dm = prmt(hd.x, 0, 0x3232u);
-            const __half2 d2 = as_h2(prmt(hd.x, 0, 0x1010u));
-            PairScale ps[4];
-            ps[0] = pair_scale(SClo, MNlo, 0, dm);
-            ps[1] = pair_scale(SClo, MNlo, 2, dm);
-            ps[2] = pair_scale(SChi, MNhi, 0, dm);
-            ps[3] = pair_scale(SChi, MNhi, 2, dm);
+                // (scale, min) pairs of sub-blocks (0,1), (2,3) from the low 6 bits of s[0..7] and
+                // (4,5), (6,7) from s[8..11] plus the top 2 bits of s[0..7]
+                const uint32_t SClo = hd.y & 0x3F3F3F3Fu;
+                const uint32_t MNlo = hd.z & 0x3F3F3F3Fu;
+                const uint32_t SChi = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
+                const uint32_t MNhi = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
+                const uint32_t dm = prmt(hd.x, 0, 0x3232u);
+                const __half2 d2 = as_h2(prmt(hd.x, 0, 0x1010u));
+                PairScale ps[4];
+                ps[0] = pair_scale(SClo, MNlo, 0, dm);
+                ps[1] = pair_scale(SClo, MNlo, 2, dm);
+                ps[2] = pair_scale(SChi, MNhi, 0, dm);
+                ps[3] = pair_scale(SChi, MNhi, 2, dm);
 
-            // the activation sums of this unit for the -B_l step: X[t][s] = sum of the 32
-            // activations of token t in sub-block s (fp16, clamped); MP * 8 of them, shared
-            // out over the group's 128 threads.  Formed before the wait for the A buffer: the
-            // sums' slot was last read by the MMAs of unit j - kXRing, which finished before
-            // the slot was refilled.
-            const int xs = static_cast<int>(j % kXRing);
-            if (!warp_wait(&xfull[xs], (j / kXRing) & 1, flags)) break;
-            const uint8_t* xt = xring + xs * C::kXSlot;
-            uint8_t* xst = xsum + xs * C::kXsBytes;
-#pragma unroll
-            for (int pi = row; pi < MP * 8; pi += kRows) {
-                const int t = pi % MP, sb = pi / MP;
-                const uint8_t* rowp = xt + (sb >> 1) * C::kXBox + t * 128;
-                __half2 acc2 = __float2half2_rn(0.f);
-#pragma unroll
-                for (int cc4 = 0; cc4 < 4; ++cc4) {
-                    const int chunk = ((sb & 1) * 4 + cc4) ^ (t & 7);
-                    const uint4 v = lds128(rowp + chunk * 16);
-                    acc2 = __hadd2(acc2, __hadd2(__hadd2(as_h2(v.x), as_h2(v.y)), __hadd2(as_h2(v.z), as_h2(v.w))));
+                // the activation sums of this unit for the -B_l step: X[t][s] = sum of the 32
+                // activations of token t in sub-block s (fp16, clamped); MP * 8 of them, shared
+                // out over the group's 128 threads.  Formed before the wait for the A buffer: the
+                // sums' slot was last read by the MMAs of unit j - kXRing, which finished before
+                // the slot was refilled.
+                const int xs = static_cast<int>(j % kXRing);
+                if (!warp_wait(&xfull[xs], (j / kXRing) & 1, flags)) break;
+                const uint8_t* xt = xring + xs * C::kXSlot;
+                uint8_t* xst = xsum + xs * C::kXsBytes;
+    #pragma unroll
+                for (int pi = row; pi < MP * 8; pi += kRows) {
+                    const int t = pi % MP, sb = pi / MP;
+                    const uint8_t* rowp = xt + (sb >> 1) * C::kXBox + t * 128;
+                    __half2 acc2 = __float2half2_rn(0.f);
+    #pragma unroll
+                    for (int cc4 = 0; cc4 < 4; ++cc4) {
+                        const int chunk = ((sb & 1) * 4 + cc4) ^ (t & 7);
+                        const uint4 v = lds128(rowp + chunk * 16);
+                        acc2 = __hadd2(acc2, __hadd2(__hadd2(as_h2(v.x), as_h2(v.y)), __hadd2(as_h2(v.z), as_h2(v.w))));
+                    }
+                    __half sum = __hadd(__low2half(acc2), __high2half(acc2));
+                    sum = __hmin(__hmax(sum, __ushort_as_half(0xFBFFu)), __ushort_as_half(0x7BFFu));
+                    *reinterpret_cast<__half*>(xst + (t >> 3) * 256 + (t & 7) * 16 + sb * 2) = sum;
                 }
-                __half sum = __hadd(__low2half(acc2), __high2half(acc2));
-                sum = __hmin(__hmax(sum, __ushort_as_half(0xFBFFu)), __ushort_as_half(0x7BFFu));
-                *reinterpret_cast<__half*>(xst + (t >> 3) * 256 + (t & 7) * 16 + sb * 2) = sum;
-            }
 
-            // the A buffer was last read by the MMAs of unit j - kNA
-            if (j >= C::kNA && !warp_wait(&tempty[(j - C::kNA) % kTB], ((j - C::kNA) / kTB) & 1, flags)) break;
-            tc_fence_after();
-            const uint32_t tcol = tlane + a * kACols;
-#pragma unroll
-            for (int sb = 0; sb < 8; ++sb) {
-                const PairScale& z = ps[sb >> 1];
-                const bool hiL = sb & 1;
-                const __half2 s1 = hiL ? __high2half2(as_h2(z.s1)) : __low2half2(as_h2(z.s1));
-                const __half2 n1 = hiL ? __high2half2(as_h2(z.n1)) : __low2half2(as_h2(z.n1));
-                const __half2 s16 = hiL ? __high2half2(as_h2(z.s16)) : __low2half2(as_h2(z.s16));
-                const __half2 n16 = hiL ? __high2half2(as_h2(z.n16)) : __low2half2(as_h2(z.n16));
-                const __half2 nbh = hiL ? __high2half2(as_h2(z.nbh)) : __low2half2(as_h2(z.nbh));
-                uint32_t out[16];
-                dq_word(qv[sb].x, s1, n1, s16, n16, d2, nbh, out + 0);
-                dq_word(qv[sb].y, s1, n1, s16, n16, d2, nbh, out + 4);
-                dq_word(qv[sb].z, s1, n1, s16, n16, d2, nbh, out + 8);
-                dq_word(qv[sb].w, s1, n1, s16, n16, d2, nbh, out + 12);
-                tmem_st16(tcol + 16 * sb, out);
+                // the A buffer was last read by the MMAs of unit j - kNA
+                if (j >= C::kNA && !warp_wait(&tempty[(j - C::kNA) % kTB], ((j - C::kNA) / kTB) & 1, flags)) break;
+                tc_fence_after();
+                const uint32_t tcol = tlane + a * kACols;
+    #pragma unroll
+                for (int sb = 0; sb < 8; ++sb) {
+                    const PairScale& z = ps[sb >> 1];
+                    const bool hiL = sb & 1;
+                    const __half2 s1 = hiL ? __high2half2(as_h2(z.s1)) : __low2half2(as_h2(z.s1));
+                    const __half2 n1 = hiL ? __high2half2(as_h2(z.n1)) : __low2half2(as_h2(z.n1));
+                    const __half2 s16 = hiL ? __high2half2(as_h2(z.s16)) : __low2half2(as_h2(z.s16));
+                    const __half2 n16 = hiL ? __high2half2(as_h2(z.n16)) : __low2half2(as_h2(z.n16));
+                    const __half2 nbh = hiL ? __high2half2(as_h2(z.nbh)) : __low2half2(as_h2(z.nbh));
+                    uint32_t out[16];
+                    dq_word(qv[sb].x, s1, n1, s16, n16, d2, nbh, out + 0);
+                    dq_word(qv[sb].y, s1, n1, s16, n16, d2, nbh, out + 4);
+                    dq_word(qv[sb].z, s1, n1, s16, n16, d2, nbh, out + 8);
+                    dq_word(qv[sb].w, s1, n1, s16, n16, d2, nbh, out + 12);
+                    tmem_st16(tcol + 16 * sb, out);
+                }
+                // the -B_l step's A row: k slots 0..7 = sub-blocks 0..7 (slots 8..15 stay zero)
+                *reinterpret_cast<uint4*>(blt + a * kBlBytes + (row >> 3) * 256 + (row & 7) * 16) =
+                    make_uint4(ps[0].nbl, ps[1].nbl, ps[2].nbl, ps[3].nbl);
+            } else {
+                // no sums to form: the wait on the activation tile keeps the MMAs of this unit
+                // after its arrival, as the Q4_K path's sums do
+                const int xs = static_cast<int>(j % kXRing);
+                if (!warp_wait(&xfull[xs], (j / kXRing) & 1, flags)) break;
+                if (j >= C::kNA && !warp_wait(&tempty[(j - C::kNA) % kTB], ((j - C::kNA) / kTB) & 1, flags)) break;
+                tc_fence_after();
+                const uint32_t tcol = tlane + a * kACols;
+                if constexpr (F == QMM_FORMAT_Q8_0)
+                    dq_unit_q80(u, row, tcol);
+                else
+                    dq_unit_q6k(u, row, tcol);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&wempty[s]);
             }
-            // the -B_l step's A row: k slots 0..7 = sub-blocks 0..7 (slots 8..15 stay zero)
-            *reinterpret_cast<uint4*>(blt + a * kBlBytes + (row >> 3) * 256 + (row & 7) * 16) =
-                make_uint4(ps[0].nbl, ps[1].nbl, ps[2].nbl, ps[3].nbl);
             fence_proxy_async_smem();  // the sums and the -B_l row are read by the tensor core
             tc_wait_st();
             tc_fence_before();
@@ -748,25 +864,140 @@ __global__ void repack_kernel(const uint8_t* __restrict__ src, uint8_t* __restri
     *reinterpret_cast<uint4*>(dst + u * kUnitBytes + static_cast<int64_t>(seg) * 16) = out;
 }
 
-cudaError_t repack(const uint8_t* src_dev, uint8_t* dst_dev, const Decomp& d, cudaStream_t s) {
-    const int64_t total = d.units * (kUnitBytes / 16);
+// Q8_0: one thread per 16-byte piece of a unit (34,816 B): pieces 0..2047 are the quant
+// halves [block 8][row 128][2 x 16 B], pieces 2048..2175 the d's of a row's 8 blocks.
+// Source row n holds K/32 blocks of 34 bytes; rows past N are zero.
+__global__ void repack_q80_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int64_t n,
+                                  int32_t kb, int64_t units) {
+    constexpr int kUnit = unit_bytes(QMM_FORMAT_Q8_0), kSegs = kUnit / 16;
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= units * kSegs) return;
+    const int64_t u = idx / kSegs;
+    const int seg = static_cast<int>(idx % kSegs);
+    const int64_t tile = u / kb;
+    const int b = static_cast<int>(u % kb);  // super-block column: Q8_0 blocks 8b .. 8b + 7
+    uint8_t out[16] = {};
+    if (seg < 2048) {
+        const int blk = seg >> 8, row = (seg >> 1) & 127, half = seg & 1;
+        const int64_t nrow = tile * kRows + row;
+        if (nrow < n) {
+            const uint8_t* q = src + (nrow * kb * 8 + 8 * b + blk) * 34 + 2 + 16 * half;
+            for (int i = 0; i < 16; ++i) out[i] = q[i];
+        }
+    } else {
+        const int row = seg - 2048;
+        const int64_t nrow = tile * kRows + row;
+        if (nrow < n)
+            for (int blk = 0; blk < 8; ++blk) {
+                const uint8_t* q = src + (nrow * kb * 8 + 8 * b + blk) * 34;
+                out[2 * blk] = q[0];
+                out[2 * blk + 1] = q[1];
+            }
+    }
+    uint4 v;
+    memcpy(&v, out, 16);
+    *reinterpret_cast<uint4*>(dst + u * kUnit + static_cast<int64_t>(seg) * 16) = v;
+}
+
+// Q6_K: one thread per 16-byte piece of a unit (26,880 B): pieces 0..1023 the low nibbles
+// [chunk 8][row 128][16 B], 1024..1535 the high bit fields [chunk 8][row 128][8 B] (two rows
+// per piece), 1536..1663 the scales [row 128][16 B], 1664..1679 the d's [row 128][2 B] (eight
+// rows per piece).  Rows past N are zero.
+__global__ void repack_q6k_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int64_t n,
+                                  int32_t kb, int64_t units) {
+    constexpr int kUnit = unit_bytes(QMM_FORMAT_Q6_K), kSegs = kUnit / 16;
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= units * kSegs) return;
+    const int64_t u = idx / kSegs;
+    const int seg = static_cast<int>(idx % kSegs);
+    const int64_t tile = u / kb;
+    const int b = static_cast<int>(u % kb);
+    // the 6-bit quant of weight i of a source block (GGUF Q6_K order)
+    auto quant = [](const uint8_t* blk, int i) -> int {
+        const int h = i / 128, c = (i % 128) / 32, l = i % 32;
+        const int lo = (blk[64 * h + l + 32 * (c & 1)] >> (4 * (c >> 1))) & 15;
+        const int hi = (blk[128 + 32 * h + l] >> (2 * c)) & 3;
+        return lo | (hi << 4);
+    };
+    auto block_of = [&](int row) -> const uint8_t* {
+        const int64_t nrow = tile * kRows + row;
+        return nrow < n ? src + (nrow * kb + b) * 210 : nullptr;
+    };
+    uint8_t out[16] = {};
+    if (seg < 1024) {  // low nibbles of chunk c, row: 4 words, nibble e of word i at pos[e]
+        const int c = seg >> 7, row = seg & 127;
+        const uint8_t* blk = block_of(row);
+        const int pos[8] = {0, 16, 4, 20, 8, 24, 12, 28};
+        if (blk)
+            for (int i = 0; i < 4; ++i) {
+                uint32_t w = 0;
+                for (int e = 0; e < 8; ++e) w |= static_cast<uint32_t>(quant(blk, 32 * c + 8 * i + e) & 15) << pos[e];
+                memcpy(out + 4 * i, &w, 4);
+            }
+    } else if (seg < 1536) {  // high bit fields of chunk c, rows 2r and 2r + 1
+        const int c = (seg - 1024) >> 6, r2 = ((seg - 1024) & 63) * 2;
+        const int fpos[8] = {0, 8, 4, 12, 2, 10, 6, 14};
+        for (int t = 0; t < 2; ++t) {
+            const uint8_t* blk = block_of(r2 + t);
+            if (!blk) continue;
+            for (int i = 0; i < 4; ++i) {
+                uint32_t f = 0;
+                for (int e = 0; e < 8; ++e) f |= static_cast<uint32_t>(quant(blk, 32 * c + 8 * i + e) >> 4) << fpos[e];
+                out[8 * t + 2 * i] = static_cast<uint8_t>(f);
+                out[8 * t + 2 * i + 1] = static_cast<uint8_t>(f >> 8);
+            }
+        }
+    } else if (seg < 1664) {  // scales of a row
+        const uint8_t* blk = block_of(seg - 1536);
+        if (blk)
+            for (int i = 0; i < 16; ++i) out[i] = blk[192 + i];
+    } else {  // d of rows 8p .. 8p + 7
+        const int r0 = (seg - 1664) * 8;
+        for (int t = 0; t < 8; ++t) {
+            const uint8_t* blk = block_of(r0 + t);
+            if (blk) {
+                out[2 * t] = blk[208];
+                out[2 * t + 1] = blk[209];
+            }
+        }
+    }
+    uint4 v;
+    memcpy(&v, out, 16);
+    *reinterpret_cast<uint4*>(dst + u * kUnit + static_cast<int64_t>(seg) * 16) = v;
+}
+
+cudaError_t repack(const uint8_t* src_dev, uint8_t* dst_dev, const Decomp& d, int format, cudaStream_t s) {
+    const int64_t total = d.units * (unit_bytes(format) / 16);
     const int threads = 256;
-    const int64_t blocks = (total + threads - 1) / threads;
-    repack_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(src_dev, dst_dev, d.n, static_cast<int32_t>(d.kb),
-                                                                   d.units);
+    const unsigned blocks = static_cast<unsigned>((total + threads - 1) / threads);
+    const int32_t kb = static_cast<int32_t>(d.kb);
+    if (format == QMM_FORMAT_Q8_0)
+        repack_q80_kernel<<<blocks, threads, 0, s>>>(src_dev, dst_dev, d.n, kb, d.units);
+    else if (format == QMM_FORMAT_Q6_K)
+        repack_q6k_kernel<<<blocks, threads, 0, s>>>(src_dev, dst_dev, d.n, kb, d.units);
+    else
+        repack_kernel<<<blocks, threads, 0, s>>>(src_dev, dst_dev, d.n, kb, d.units);
     return cudaGetLastError();
 }
 
-template <int MP>
+template <int MP, int F>
 static cudaError_t set_attr() {
-    return cudaFuncSetAttribute(tc_kernel<MP>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<MP>::kSmem);
+    return cudaFuncSetAttribute(tc_kernel<MP, F>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<MP, F>::kSmem);
+}
+
+template <int F>
+static cudaError_t set_attr_all() {
+    cudaError_t e;
+    if ((e = set_attr<16, F>()) != cudaSuccess) return e;
+    if ((e = set_attr<32, F>()) != cudaSuccess) return e;
+    return set_attr<64, F>();
 }
 
 cudaError_t configure() {
     cudaError_t e;
-    if ((e = set_attr<16>()) != cudaSuccess) return e;
-    if ((e = set_attr<32>()) != cudaSuccess) return e;
-    return set_attr<64>();
+    if ((e = set_attr_all<QMM_FORMAT_Q4_K>()) != cudaSuccess) return e;
+    if ((e = set_attr_all<QMM_FORMAT_Q6_K>()) != cudaSuccess) return e;
+    return set_attr_all<QMM_FORMAT_Q8_0>();
 }
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -810,13 +1041,13 @@ cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, i
     return cudaSuccess;
 }
 
-template <int MP>
+template <int MP, int F>
 static cudaError_t launch_mp(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl,
                              bool cooperative) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Cfg<MP>::kSmem;
+    cfg.dynamicSmemBytes = Cfg<MP, F>::kSmem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -825,14 +1056,25 @@ static cudaError_t launch_mp(const MatDesc& single, const LaunchParams& p, int g
     attr[1].val.cooperative = cooperative ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, tc_kernel<MP>, single, p);
+    return cudaLaunchKernelEx(&cfg, tc_kernel<MP, F>, single, p);
 }
 
-cudaError_t launch(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl, bool cooperative) {
+template <int F>
+static cudaError_t launch_f(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl,
+                            bool cooperative) {
     switch (mp_for(p.m)) {
-        case 16: return launch_mp<16>(single, p, grid, s, pdl, cooperative);
-        case 32: return launch_mp<32>(single, p, grid, s, pdl, cooperative);
-        default: return launch_mp<64>(single, p, grid, s, pdl, cooperative);
+        case 16: return launch_mp<16, F>(single, p, grid, s, pdl, cooperative);
+        case 32: return launch_mp<32, F>(single, p, grid, s, pdl, cooperative);
+        default: return launch_mp<64, F>(single, p, grid, s, pdl, cooperative);
+    }
+}
+
+cudaError_t launch(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl, bool cooperative,
+                   int format) {
+    switch (format) {
+        case QMM_FORMAT_Q6_K: return launch_f<QMM_FORMAT_Q6_K>(single, p, grid, s, pdl, cooperative);
+        case QMM_FORMAT_Q8_0: return launch_f<QMM_FORMAT_Q8_0>(single, p, grid, s, pdl, cooperative);
+        default: return launch_f<QMM_FORMAT_Q4_K>(single, p, grid, s, pdl, cooperative);
     }
 }
 

@@ -94,18 +94,25 @@ __device__ __forceinline__ void amax_finish_warp(const LaunchParams& p, int writ
     if (lane == 0) atomicExch(p.amax_count, 0);
 }
 
+// Block formats: bytes per block and weights per block, by QMM_FORMAT_*.
+__host__ __device__ constexpr int block_bytes(int format) { return format == QMM_FORMAT_Q6_K ? 210 : format == QMM_FORMAT_Q8_0 ? 34 : 144; }
+__host__ __device__ constexpr int block_weights(int format) { return format == QMM_FORMAT_Q8_0 ? 32 : 256; }
+
 // Backend 2: tcgen05 streaming kernel (weights dequantised into tensor memory, x by TMA).
 namespace b2 {
 constexpr int kRows = 128;
-constexpr int kUnitBytes = kRows * 144;
+constexpr int kUnitBytes = kRows * 144;  // Q4_K
+// bytes of one unit (128 rows x 256 weights) of a format
+__host__ __device__ constexpr int unit_bytes(int format) { return kRows * block_bytes(format) * (256 / block_weights(format)); }
 constexpr int kMaxM = 64;   // rows per launch
 int mp_for(int64_t m);      // tokens per launch tile: 16, 32 or 64
-cudaError_t repack(const uint8_t* src_dev, uint8_t* dst_dev, const Decomp& d, cudaStream_t s);
+cudaError_t repack(const uint8_t* src_dev, uint8_t* dst_dev, const Decomp& d, int format, cudaStream_t s);
 // Fill a matrix descriptor for a run of m rows (1..64) of x against the handle's weights.
 cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, int* tickets, int64_t units,
                      int64_t n, int32_t kb, int32_t m);
-// Launch over `p.count` matrices (`single` when count == 1); p.ws_cols = mp_for(p.m).
-cudaError_t launch(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl, bool cooperative);
+// Launch over `p.count` matrices of one format (`single` when count == 1); p.ws_cols = mp_for(p.m).
+cudaError_t launch(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl, bool cooperative,
+                   int format);
 cudaError_t configure();
 }  // namespace b2
 
@@ -134,6 +141,7 @@ struct qmm_handle_s {
     uint64_t magic;
     int device;
     int32_t backend;
+    int32_t format = QMM_FORMAT_Q4_K;
     int64_t m_max;
     qmm::Decomp d;
     uint8_t* wq = nullptr;        // repacked weights

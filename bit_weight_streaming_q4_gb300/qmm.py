@@ -21,6 +21,7 @@ STATUS = {0: "QMM_OK", 1: "QMM_ERR_INVALID_ARG", 2: "QMM_ERR_UNSUPPORTED_SHAPE",
           6: "QMM_ERR_DEVICE_TIMEOUT", 7: "QMM_ERR_BAD_HANDLE", 8: "QMM_ERR_NO_DEVICE",
           9: "QMM_ERR_SCRATCH_TOO_SMALL"}
 BACKEND_AUTO, BACKEND_MMA_SYNC, BACKEND_TCGEN05 = 0, 1, 2
+FORMAT_Q4_K, FORMAT_Q6_K, FORMAT_Q8_0 = 0, 1, 2
 
 
 class QmmError(RuntimeError):
@@ -31,7 +32,8 @@ class QmmError(RuntimeError):
 
 class Options(ctypes.Structure):
     _fields_ = [("m_max", ctypes.c_int32), ("backend", ctypes.c_int32),
-                ("ctas_per_sm", ctypes.c_int32), ("host_io", ctypes.c_int32)]
+                ("ctas_per_sm", ctypes.c_int32), ("host_io", ctypes.c_int32),
+                ("format", ctypes.c_int32)]
 
 
 class Info(ctypes.Structure):
@@ -40,7 +42,7 @@ class Info(ctypes.Structure):
                 ("units", ctypes.c_int64), ("rows_per_unit", ctypes.c_int64),
                 ("weight_bytes", ctypes.c_int64), ("packed_bytes", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_int64), ("m_per_launch", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("format", ctypes.c_int32)]
 
 
 _lib = None
@@ -111,25 +113,28 @@ def current_stream() -> int:
 
 
 def default_options(m_max: int = 16, backend: int = BACKEND_AUTO, ctas_per_sm: int = 0,
-                    host_io: bool = False) -> Options:
+                    host_io: bool = False, format: int = FORMAT_Q4_K) -> Options:
     o = Options()
     load().qmm_default_options(ctypes.byref(o))
     o.m_max, o.backend, o.ctas_per_sm, o.host_io = m_max, backend, ctas_per_sm, int(host_io)
+    o.format = format
     return o
 
 
 class Qmm:
-    """One N x K Q4_K weight matrix resident on the GPU.
+    """One N x K weight matrix resident on the GPU.
 
-    blocks: uint8 [N, K/256, 144] GGUF-ordered super-blocks, as a torch CUDA tensor
-    (device) or a numpy array / CPU tensor (host)."""
+    blocks: GGUF-ordered blocks of `format` as uint8 ([N, K/256, 144] Q4_K, [N, K/256, 210]
+    Q6_K, [N, K/32, 34] Q8_0), a torch CUDA tensor (device) or a numpy array / CPU tensor
+    (host)."""
 
     def __init__(self, blocks, n: int, k: int, m_max: int = 16, backend: int = BACKEND_AUTO,
-                 ctas_per_sm: int = 0, host_io: bool = False, stream: int | None = None):
+                 ctas_per_sm: int = 0, host_io: bool = False, stream: int | None = None,
+                 format: int = FORMAT_Q4_K):
         lib = load()
         on_dev = bool(getattr(blocks, "is_cuda", False))
         self._h = ctypes.c_void_p()
-        opt = default_options(m_max, backend, ctas_per_sm, host_io)
+        opt = default_options(m_max, backend, ctas_per_sm, host_io, format)
         st = current_stream() if stream is None else stream
         _check(lib.qmm_create(ctypes.byref(self._h), _ptr(blocks), n, k, int(on_dev),
                               ctypes.byref(opt), st), "qmm_create")

@@ -64,11 +64,29 @@ enum {
     QMM_BACKEND_TCGEN05 = 2   /* tcgen05.mma with TMEM accumulators, 64 rows per launch */
 };
 
+/*
+ * Block formats of the weight matrix.  Q4_K is the format of the method; Q6_K and Q8_0 are
+ * the other block types of a mixed-quant model file (page "Running 4 coding agents on one
+ * RTX 3090", the note on mixed-quant builds) and int8 weights (page "Breaking the limits of
+ * Qwen3.8-27B again", its int8 lm_head).  Byte layouts are the GGUF ones:
+ *   Q4_K 144 B per 256 weights: d, dmin (fp16), 12 B of 6-bit scales/mins, 128 B of nibbles;
+ *   Q6_K 210 B per 256 weights: ql[128], qh[64], 16 int8 scales, d (fp16);
+ *        w = d * scale[i/16] * (q - 32) with q the 6-bit quant;
+ *   Q8_0 34 B per 32 weights: d (fp16), 32 int8 quants; w = d * q.
+ * Q6_K and Q8_0 run on the TCGEN05 backend only.
+ */
+enum {
+    QMM_FORMAT_Q4_K = 0,
+    QMM_FORMAT_Q6_K = 1,
+    QMM_FORMAT_Q8_0 = 2
+};
+
 typedef struct {
     int32_t m_max;        /* largest M any run will pass; >= 1 */
     int32_t backend;      /* QMM_BACKEND_*; fixed for the handle's lifetime */
     int32_t ctas_per_sm;  /* 0 = default; persistent CTAs per SM (part of the reduction order) */
     int32_t host_io;      /* nonzero: also allocate staging buffers for qmm_run_host */
+    int32_t format;       /* QMM_FORMAT_* of the blocks passed to qmm_create */
 } qmm_options;
 
 typedef struct {
@@ -77,23 +95,26 @@ typedef struct {
     int32_t grid;             /* persistent CTAs per run */
     int64_t units;            /* work units (row tile x super-block column) */
     int64_t rows_per_unit;
-    int64_t weight_bytes;     /* N*K/256*144: bytes streamed from HBM per run */
+    int64_t weight_bytes;     /* bytes of the blocks (Q4_K N*K/256*144): streamed from HBM per run */
     int64_t packed_bytes;     /* bytes of the repacked on-device copy (N padded to a tile) */
     int64_t workspace_bytes;  /* split-K partials + tile tickets */
     int32_t m_per_launch;     /* rows one kernel launch handles; a run of M rows makes
                                  ceil(M / m_per_launch) launches */
-    int32_t reserved;
+    int32_t format;           /* QMM_FORMAT_* of the handle */
 } qmm_info;
 
-/* Fill `opt` with defaults: m_max 16, backend auto, ctas_per_sm 0, host_io 0. */
+/* Fill `opt` with defaults: m_max 16, backend auto, ctas_per_sm 0, host_io 0, format Q4_K. */
 void qmm_default_options(qmm_options* opt);
 
 /*
- * Create a handle for an N x K Q4_K weight matrix.
- *  blocks: N rows of K/256 super-blocks, 144 bytes each, row-major (GGUF order); on the
- *          device if blocks_on_device != 0 (16-byte aligned), else in host memory.  The
- *          handle copies and repacks them into its own device memory; the caller may free
- *          `blocks` once the call returns.
+ * Create a handle for an N x K weight matrix in block format opt->format (K a multiple of
+ * 256 for every format).
+ *  blocks: N rows of blocks, row-major (GGUF order): K/256 Q4_K blocks of 144 bytes, K/256
+ *          Q6_K blocks of 210 bytes or K/32 Q8_0 blocks of 34 bytes per row; on the device
+ *          if blocks_on_device != 0 (16-byte aligned), else in host memory.  The handle
+ *          copies and repacks them into its own device memory; the caller may free
+ *          `blocks` once the call returns.  A Q6_K or Q8_0 handle with the MMA_SYNC backend
+ *          is an INVALID_ARG.
  *  opt:    NULL for defaults.
  *  stream: the repack is ordered on it; qmm_create synchronises it before returning.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, OOM, CUDA, NO_DEVICE.

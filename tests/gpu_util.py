@@ -20,10 +20,13 @@ def to_device_blocks(blocks: np.ndarray):
 
 
 def make(blocks: np.ndarray, m_max: int = 16, device_blocks: bool = True, **kw):
+    """A handle for [N, blocks per row, block bytes] blocks (144: Q4_K, 210: Q6_K, 34: Q8_0;
+    pass format= for the latter two)."""
     from bit_weight_streaming_q4_gb300 import Qmm
-    n, kb, _ = blocks.shape
+    n, kb, nbytes = blocks.shape
+    per = 32 if nbytes == 34 else 256
     src = to_device_blocks(blocks) if device_blocks else np.ascontiguousarray(blocks)
-    return Qmm(src, n, kb * 256, m_max=m_max, **kw)
+    return Qmm(src, n, kb * per, m_max=m_max, **kw)
 
 
 def run(q, x: np.ndarray, m: int | None = None) -> np.ndarray:

@@ -44,7 +44,7 @@ def test_status_strings(lib):
 def test_default_options(lib):
     o = Q.Options()
     lib.qmm_default_options(ctypes.byref(o))
-    assert (o.m_max, o.backend, o.ctas_per_sm, o.host_io) == (16, 0, 0, 0)
+    assert (o.m_max, o.backend, o.ctas_per_sm, o.host_io, o.format) == (16, 0, 0, 0, 0)
 
 
 def test_argument_errors_need_no_device(lib):
@@ -58,6 +58,10 @@ def test_argument_errors_need_no_device(lib):
     assert lib.qmm_create(ctypes.byref(h), buf, 1, -256, 0, ctypes.byref(o), None) == 2
     bad = Q.default_options(m_max=0)
     assert lib.qmm_create(ctypes.byref(h), buf, 1, 256, 0, ctypes.byref(bad), None) == 1
+    # an unknown block format, and a Q6_K / Q8_0 handle on the mma.sync backend
+    for fmt, be in ((3, 0), (-1, 0), (1, 1), (2, 1)):
+        o2 = Q.default_options(backend=be, format=fmt)
+        assert lib.qmm_create(ctypes.byref(h), buf, 1, 256, 0, ctypes.byref(o2), None) == 1
     misaligned = ctypes.addressof(buf) | 1
     assert lib.qmm_create(ctypes.byref(h), misaligned, 1, 256, 1, ctypes.byref(o), None) == 3
     # no handle exists: every handle call reports BAD_HANDLE
