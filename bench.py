@@ -42,8 +42,8 @@ TRAFFIC_PER_UNIT = {
         "sha256": "43d77ce69d57d591d1ae8852fdc3a0d12692e52edc2c34708f401cbef0162db2",
         "bytes": 37194.0},
     2: {"source": "bit_weight_streaming_q4_gb300/csrc/qmm_b2.cu",
-        "sha256": "29081b5a4e56c527a88b7a622500e1894233e87e1b720563f78d1026a98da6a2",
-        "bytes": 18590.5},
+        "sha256": "b03b6dc9ff5c28d4eb7fe303b5e4d0bff713329c59632724d179b3be4cda2729",
+        "bytes": 18581.6},
 }
 KERNEL_NAME = {1: "qmm::b1::stream_kernel<2>", 2: "qmm::b2::tc_kernel<16>"}
 HEADLINE_M = 12
