@@ -19,16 +19,18 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "q4k_oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "attn_oracle.c")]
 _LIB = os.path.join(_HERE, "_oracle.so")
 
 
 def build(force: bool = False) -> str:
     """Compile the oracle with the host C compiler.  -ffp-contract=off keeps each
     operation rounded as written."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    newest = max(os.path.getmtime(p) for p in _SRCS)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fPIC",
-                               "-shared", "-std=c11", _SRC, "-o", tmp, "-lm"])
+                               "-shared", "-std=c11", *_SRCS, "-o", tmp, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -62,6 +64,12 @@ def _load():
                                        ctypes.c_void_p, ctypes.c_int]
         lib.oracle_dequant_fmt.restype = ctypes.c_int
         lib.oracle_dequant_fmt.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+        lib.oracle_attn.restype = ctypes.c_int
+        lib.oracle_attn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        lib.oracle_kv.restype = ctypes.c_double
+        lib.oracle_kv.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int]
         lib.oracle_q6k_quant.restype = ctypes.c_int
         lib.oracle_q6k_quant.argtypes = [ctypes.c_void_p, ctypes.c_int]
         _lib = lib
@@ -173,3 +181,43 @@ def argmax_rows(y: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     assert y.ndim == 2 and y.shape[1] > 0
     idx = np.argmax(y, axis=1)
     return idx, y[np.arange(y.shape[0]), idx]
+
+
+# --------------------------------------------------------------------- decode attention
+ATTN_D, ATTN_PAGE_TOKENS, ATTN_RECORD_BYTES = 128, 64, 17408
+
+
+def attn(pool: np.ndarray, page_table: np.ndarray, q: np.ndarray, row_agent, row_len, kv_heads: int,
+         nthreads: int = 0) -> tuple[np.ndarray, np.ndarray]:
+    """Stacked-row decode attention over a paged q8_0 KV pool (see attn_oracle.c for the
+    definition and the pool layout): out[r, h] = softmax(q[r, h] . K^T / sqrt(128)) V over the
+    first row_len[r] tokens of agent row_agent[r], K and V of KV head h // (H / kv_heads).
+    Returns out and S = sum_t p_t |v_t| in double, both [rows, H, 128].
+
+    pool: uint8, records of 17,408 bytes, (page P, head g) at (P * kv_heads + g) * 17408;
+    page_table: int32 [agents, max_pages]; q: float16 [rows, H, 128]."""
+    pool = np.ascontiguousarray(pool, dtype=np.uint8)
+    pt = np.ascontiguousarray(page_table, dtype=np.int32)
+    assert pt.ndim == 2
+    q = np.ascontiguousarray(q, dtype=np.float16)
+    assert q.ndim == 3 and q.shape[2] == ATTN_D
+    rows, heads = q.shape[0], q.shape[1]
+    ra = np.ascontiguousarray(row_agent, dtype=np.int32)
+    rl = np.ascontiguousarray(row_len, dtype=np.int32)
+    assert ra.shape == (rows,) and rl.shape == (rows,)
+    assert np.all(pt >= 0) and (pt.max(initial=0) + 1) * kv_heads * ATTN_RECORD_BYTES <= pool.size
+    out = np.empty((rows, heads, ATTN_D))
+    s = np.empty((rows, heads, ATTN_D))
+    rc = _load().oracle_attn(pool.ctypes.data, pt.ctypes.data, pt.shape[1], q.view(np.uint16).ctypes.data,
+                             ra.ctypes.data, rl.ctypes.data, rows, heads, kv_heads, out.ctypes.data,
+                             s.ctypes.data, nthreads)
+    if rc != 0:
+        raise RuntimeError("oracle_attn failed")
+    return out, s
+
+
+def kv_value(record: np.ndarray, which: int, slot: int, d: int) -> float:
+    """Element d of K (which 0) or V (which 1) of token `slot` of one 17,408-byte record."""
+    r = np.ascontiguousarray(record, dtype=np.uint8).ravel()
+    assert r.size == ATTN_RECORD_BYTES
+    return float(_load().oracle_kv(r.ctypes.data, which, slot, d))

@@ -60,6 +60,9 @@ def _load():
         lib.synth_blocks.restype = None
         lib.synth_blocks.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_uint64,
                                      ctypes.c_uint64, ctypes.c_int64, ctypes.c_double]
+        lib.synth_kv_records.restype = None
+        lib.synth_kv_records.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint64,
+                                         ctypes.c_int64, ctypes.c_double]
         lib.synth_raw.restype = None
         lib.synth_raw.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64,
                                   ctypes.c_uint64]
@@ -184,3 +187,62 @@ def stack(layers: int = LAYERS, lm_head: bool = True) -> list[Matrix]:
 SINGLE_PROJECTION = Matrix("proj4096", 4096, 4096, 0)
 SWEEP_MATRICES = (layer_matrices(0)[2], layer_matrices(0)[3])   # gate_up, down
 SWEEP_M = (1, 2, 4, 8, 12, 16, 32, 64)
+
+
+# ----------------------------------------------------------------- decode attention inputs
+# Attention shapes of the 27B-shaped stack: qkv 5120 -> 8192 = 48 query heads + 2 x 8 KV heads
+# of 128, o 6144 -> 5120 (48 x 128 in).  KV pages of 64 tokens, one 17,408-byte record per
+# (page, KV head); the pool layout is documented with the attention oracle.
+ATTN_HEADS, ATTN_KV_HEADS, ATTN_DIM, ATTN_PAGE = 48, 8, 128, 64
+KV_RECORD_BYTES = 17408
+KV_SCALE = 1.0 / 64  # K, V = fp16(|N(0,1)| / 64) * int8: values of order one
+
+
+def kv_pool(pages: int, kv_heads: int, seed: int, tensor_id: int, first_page: int = 0) -> np.ndarray:
+    """Pages first_page .. first_page+pages-1 of a synthetic q8_0 KV pool, as uint8
+    [pages * kv_heads * 17408] (record (page, head) at (page * kv_heads + head) * 17408)."""
+    out = np.empty(pages * kv_heads * KV_RECORD_BYTES, dtype=np.uint8)
+    _load().synth_kv_records(out.ctypes.data, pages * kv_heads, seed, tensor_id, first_page * kv_heads,
+                             KV_SCALE)
+    return out
+
+
+@dataclass(frozen=True)
+class AttnWorkload:
+    """Agents with cache lengths, R stacked rows per agent (row j of agent a attends to the
+    agent's first cache[a] + j + 1 tokens), and a shared pool whose pages are handed out in a
+    seeded random order."""
+    cache: tuple            # tokens already cached per agent
+    rows_per_agent: int
+    heads: int = ATTN_HEADS
+    kv_heads: int = ATTN_KV_HEADS
+
+    def lengths(self):
+        return [c + self.rows_per_agent for c in self.cache]
+
+    def pages_of(self):
+        return [(n + ATTN_PAGE - 1) // ATTN_PAGE for n in self.lengths()]
+
+    def build(self, seed: int = 0):
+        """(page_table int32 [agents, max_pages], pool pages, row_agent, row_len)."""
+        pages = self.pages_of()
+        total = sum(pages)
+        perm = np.random.default_rng(seed).permutation(total).astype(np.int32)
+        max_pages = max(pages)
+        table = np.zeros((len(pages), max_pages), dtype=np.int32)
+        off = 0
+        for a, n in enumerate(pages):
+            table[a, :n] = perm[off:off + n]
+            off += n
+        row_agent = np.repeat(np.arange(len(pages), dtype=np.int32), self.rows_per_agent)
+        row_len = np.array([c + j + 1 for c in self.cache for j in range(self.rows_per_agent)], dtype=np.int32)
+        return table, total, row_agent, row_len
+
+
+# The decode step of the pages: 4 agents with 23K-token contexts, 1 token + 2 drafts each.
+ATTN_DECODE = AttnWorkload(cache=(23000, 23000, 23000, 23000), rows_per_agent=3)
+
+
+def attn_q(rows: int, heads: int, seed: int, tensor_id: int) -> np.ndarray:
+    """Queries q[rows, heads, 128] fp16, N(0,1)."""
+    return x_f16(rows, heads * ATTN_DIM, seed, tensor_id).reshape(rows, heads, ATTN_DIM)

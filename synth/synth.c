@@ -135,6 +135,41 @@ void synth_blocks(uint8_t* out, int64_t nblocks, int64_t bytes, uint64_t seed, u
 }
 
 /*
+ * Fill `nrecords` KV records of 17,408 bytes (records first .. first+nrecords-1 of tensor
+ * (seed, tensor_id)): K quants (8192 random bytes), 256 K scales, V quants (8192 random
+ * bytes), 256 V scales; each scale fp16(|N(0,1)| * scale_mul).  Record r draws from its own
+ * range of 4096 counter values.
+ */
+void synth_kv_records(uint8_t* out, int64_t nrecords, uint64_t seed, uint64_t tensor_id, int64_t first,
+                      double scale_mul) {
+    uint64_t key = synth_key(seed, tensor_id);
+#pragma omp parallel for schedule(static)
+    for (int64_t rr = 0; rr < nrecords; ++rr) {
+        uint64_t base = (uint64_t)(first + rr) * 4096;
+        uint8_t* rec = out + 17408 * rr;
+        for (int part = 0; part < 2; ++part) {
+            uint8_t* qs = rec + part * 8704;
+            for (int i = 0; i < 8192; i += 8) {
+                uint64_t r = ctr_rand(key, base + (uint64_t)(part * 2048 + i / 8));
+                for (int j = 0; j < 8; ++j) qs[i + j] = (uint8_t)(r >> (8 * j));
+            }
+            uint8_t* sc = qs + 8192;
+            for (int i = 0; i < 256; i += 2) {
+                double z0, z1;
+                uint64_t c = base + 1024 + (uint64_t)(part * 256 + i);
+                box_muller(ctr_rand(key, c), ctr_rand(key, c + 1), &z0, &z1);
+                uint16_t h0 = synth_f16_from_double(fabs(z0) * scale_mul);
+                uint16_t h1 = synth_f16_from_double(fabs(z1) * scale_mul);
+                sc[2 * i] = (uint8_t)(h0 & 0xFF);
+                sc[2 * i + 1] = (uint8_t)(h0 >> 8);
+                sc[2 * i + 2] = (uint8_t)(h1 & 0xFF);
+                sc[2 * i + 3] = (uint8_t)(h1 >> 8);
+            }
+        }
+    }
+}
+
+/*
  * Fill n fp16 activations, elements first .. first+n-1 of tensor (seed, tensor_id),
  * as N(0,1); with probability outlier_p an element is multiplied by outlier_mul before
  * rounding.  Element i uses normal number i of the pair stream (pairs from Box-Muller)
