@@ -65,7 +65,8 @@ def parse():
                     help="target CPU time of the oracle sample")
     ap.add_argument("--single", default=None,
                     help="profiling mode: run one matrix of the stack (proj4096, qkv, o, gate_up, "
-                         "down, lm_head) --steps times at --m rows and print its timing")
+                         "down, lm_head) --steps times at --m rows, or the decode attention "
+                         "(attention) --steps times, and print its timing")
     ap.add_argument("--m", type=int, default=HEADLINE_M)
     ap.add_argument("--backend", type=int, default=0, help="0 auto, 1 mma.sync, 2 tcgen05")
     return ap.parse_args()
@@ -298,6 +299,55 @@ def format_line(torch, fmt, code, m, stream, parity, reps=50):
         line["parity"] = {"checked_outputs": int(ratio.size), "max_err_over_bound": float(ratio.max()),
                           "pass": bool(ratio.max() <= 1.0)}
     q.close()
+    return line
+
+
+def attention_line(torch, stream, hbm, parity, reps=50):
+    """Stacked-row decode attention of one layer at the pages' decode step (4 agents with
+    23,000 cached tokens, 1 token + 2 drafts each, 48 query heads over 8 KV heads, q8_0 KV in
+    a shared paged pool): time per call, KV GB/s (every page read once per call) and a
+    sampled oracle check of two rows."""
+    from bit_weight_streaming_q4_gb300.qmm import AttnDims, attn_decode, attn_workspace_bytes
+    w = synth.ATTN_DECODE
+    table, total, ra, rl = w.build(seed=0)
+    pool = synth.kv_pool(total, w.kv_heads, seed=0, tensor_id=60)
+    q = synth.attn_q(len(ra), w.heads, seed=0, tensor_id=61)
+    agent_rows = np.concatenate([[0], np.cumsum(np.bincount(ra, minlength=table.shape[0]))]).astype(np.int32)
+    pool_d = torch.from_numpy(pool).cuda()
+    table_d = torch.from_numpy(table).cuda()
+    ar_d = torch.from_numpy(agent_rows).cuda()
+    rl_d = torch.from_numpy(rl).cuda()
+    q_d = torch.from_numpy(q.view(np.int16)).cuda().view(torch.float16)
+    out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    s = stream.cuda_stream
+    dims = AttnDims(w.heads, w.kv_heads, table.shape[0], table.shape[1], total)
+    ws = torch.empty(attn_workspace_bytes(dims), dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        attn_decode(pool_d, table_d, ar_d, rl_d, q_d, out, w.kv_heads, s, ws, err)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        attn_decode(pool_d, table_d, ar_d, rl_d, q_d, out, w.kv_heads, s, ws, err)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    kv_bytes = sum(w.pages_of()) * w.kv_heads * synth.KV_RECORD_BYTES
+    line = {"workload": "4 agents x 23,000 cached tokens, 3 rows each (1 token + 2 drafts), 48 query heads "
+                        "over 8 KV heads of 128, q8_0 KV pool in 64-token pages; one layer",
+            "kv_bytes": kv_bytes, "us_per_call": us, "kv_gbs": kv_bytes / us / 1e3,
+            "frac_of_hbm_measured": kv_bytes / us / 1e3 / hbm, "error_word": int(err.item()),
+            "kernels_per_call": 2}
+    if parity:
+        import oracle
+        rows = np.array([0, len(ra) - 1])
+        ref, sabs = oracle.attn(pool, table, q[rows], ra[rows], rl[rows], w.kv_heads)
+        got = out.cpu().numpy()[rows]
+        ratio = np.abs(got - ref) / (2e-3 * sabs + 1e-6)
+        line["parity"] = {"checked_outputs": int(ratio.size), "max_err_over_bound": float(ratio.max()),
+                          "pass": bool(ratio.max() <= 1.0)}
     return line
 
 
@@ -594,11 +644,13 @@ def run_ours(args, rank, world, local_rank):
     # plain run that writes y, per launch, on the step's lm_head handles and activations
     verify = None
     formats = None
+    attention = None
     if not args.no_extra:
         verify = {str(m): lm_head_verify(stack, m, stream) for m in sorted({*EXTRA_M, HEADLINE_M})}
         # the other block formats of a mixed-quant file, on the lm_head shape at M = 12
         formats = {name: format_line(torch, f, code, HEADLINE_M, stream, not args.no_parity)
                    for name, f, code in (("Q6_K", synth.Q6_K, 1), ("Q8_0", synth.Q8_0, 2))}
+        attention = attention_line(torch, stream, hbm, not args.no_parity)
 
     cpu = None
     if rank == 0:
@@ -622,6 +674,7 @@ def run_ours(args, rank, world, local_rank):
         "dependent_step": dependent,
         "lm_head_verify": verify,
         "formats": formats,
+        "attention": attention,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": measured_traffic(stack.handles(HEADLINE_M)),
                      "kernel": f"{KERNEL_NAME[head_backend]} (one persistent launch per step)",
@@ -645,6 +698,13 @@ def run_single(args):
     import torch
     from bit_weight_streaming_q4_gb300 import Qmm
     torch.cuda.set_device(0)
+    if args.single == "attention":
+        peaks, _ = measured_peaks()
+        stream = torch.cuda.Stream()
+        line = attention_line(torch, stream, float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS)), not args.no_parity,
+                              reps=max(args.steps, 1))
+        print(json.dumps({"single": "attention", **line}), flush=True)
+        return
     shapes = {"proj4096": synth.SINGLE_PROJECTION, "lm_head": synth.LM_HEAD}
     shapes.update({m.name.split(".")[1]: m for m in synth.layer_matrices(0)})
     mat = shapes[args.single]

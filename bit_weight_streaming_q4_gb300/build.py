@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libqmm.so")
-SOURCES = ["qmm_api.cu", "qmm_b1.cu", "qmm_b2.cu", "qmm_noalloc.cu"]
+SOURCES = ["qmm_api.cu", "qmm_b1.cu", "qmm_b2.cu", "qmm_noalloc.cu", "qmm_attn.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

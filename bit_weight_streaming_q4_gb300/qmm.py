@@ -45,6 +45,11 @@ class Info(ctypes.Structure):
                 ("format", ctypes.c_int32)]
 
 
+class AttnDims(ctypes.Structure):
+    _fields_ = [("heads", ctypes.c_int32), ("kv_heads", ctypes.c_int32), ("agents", ctypes.c_int32),
+                ("max_pages", ctypes.c_int32), ("pool_pages", ctypes.c_int64)]
+
+
 _lib = None
 
 
@@ -82,6 +87,9 @@ def load(path: str = LIB_PATH):
         "qmm_step_launch": (ctypes.c_int, [vp, vp]),
         "qmm_step_destroy": (ctypes.c_int, [vp]),
         "qmm_run_noalloc": (ctypes.c_int, [vp, i64, i64, vp, i64, vp, vp]),
+        "qmm_attn_workspace_bytes": (ctypes.c_int, [ctypes.POINTER(AttnDims), ctypes.POINTER(i64)]),
+        "qmm_attn_decode": (ctypes.c_int, [ctypes.POINTER(AttnDims), vp, vp, vp, vp, vp, i64, vp, vp, i64,
+                                           vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -225,3 +233,37 @@ class Step:
             self.close()
         except Exception:
             pass
+
+
+ATTN_RECORD_BYTES = 17408
+
+
+def attn_workspace_bytes(dims: AttnDims) -> int:
+    n = ctypes.c_int64()
+    _check(load().qmm_attn_workspace_bytes(ctypes.byref(dims), ctypes.byref(n)), "qmm_attn_workspace_bytes")
+    return n.value
+
+
+def attn_decode(pool, page_table, agent_rows, row_len, q, out, kv_heads: int, stream: int | None = None,
+                workspace=None, err=None):
+    """Stacked-row decode attention over a paged q8_0 KV pool (qmm_attn_decode in qmm.h).
+
+    pool: uint8 CUDA tensor of 17,408-byte records; page_table: int32 CUDA tensor [agents,
+    max_pages]; agent_rows: int32 CUDA tensor [agents + 1]; row_len: int32 CUDA tensor [rows];
+    q: fp16 CUDA tensor [rows, heads, 128]; out: fp32 CUDA tensor [rows, heads, 128].  The
+    workspace and the error word are allocated unless given; returns the error word (a CUDA
+    int32 tensor of one element, nonzero after the launch if the device reported a failure)."""
+    import torch
+    lib = load()
+    dims = AttnDims(int(q.shape[1]), int(kv_heads), int(page_table.shape[0]), int(page_table.shape[1]),
+                    int(pool.numel() // (kv_heads * ATTN_RECORD_BYTES)))
+    nbytes = attn_workspace_bytes(dims)
+    if workspace is None or workspace.numel() < nbytes:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=q.device)
+    st = current_stream() if stream is None else stream
+    _check(lib.qmm_attn_decode(ctypes.byref(dims), _ptr(pool), _ptr(page_table), _ptr(agent_rows), _ptr(row_len),
+                               _ptr(q), int(q.shape[0]), _ptr(out), _ptr(workspace), workspace.numel(), _ptr(err), st),
+           "qmm_attn_decode")
+    return err

@@ -149,6 +149,54 @@ qmm_status qmm_run_argmax(qmm_handle h, const void* x, int64_t m, int32_t* idx, 
                           void* stream);
 
 /*
+ * Stacked-row decode attention over a paged q8_0 KV pool (page "Running 4 coding agents on
+ * one RTX 3090", section "How parallel decoding works": the step's rows are every agent's
+ * next token and drafts, and each agent's rows attend to that agent's own cache in a shared
+ * paged pool of q8_0 entries).  For row r of agent a and query head h, with
+ * g = h / (heads / kv_heads):
+ *     out[r][h] = softmax over t < row_len[r] of (q[r][h] . k_t / sqrt(128)), times v_t,
+ * k_t and v_t being token t of agent a, KV head g.  Head dimension 128, pages of 64 tokens.
+ * Every pointer is device memory; nothing is copied from the host, so the call can be
+ * captured in a CUDA graph.
+ *  pool:       16-byte aligned; record (page P, KV head g) of 17,408 bytes at
+ *              (P * kv_heads + g) * 17408:
+ *                bytes     0 ..  8191  K quants int8, dim d of token t at
+ *                                      t * 128 + 16 * ((d / 16) ^ (2 (t % 4) + (t / 4) % 2)) + d % 16
+ *                bytes  8192 ..  8703  K scales fp16 [token 64][dim block 4]
+ *                bytes  8704 .. 16895  V quants int8 [dim 128][token 64]
+ *                bytes 16896 .. 17407  V scales fp16 [dim block 4][token 64]
+ *              element = scale of its 32-dim block * quant.
+ *  page_table: int32 [agents][max_pages]: token t of agent a is in page page_table[a][t / 64],
+ *              slot t % 64.  An entry outside [0, pool_pages) sets *err_word |= 2 and the
+ *              run of pages holding it is skipped.
+ *  agent_rows: int32 [agents + 1], non-decreasing: agent a's rows are agent_rows[a] ..
+ *              agent_rows[a + 1] - 1 (an agent may have none).
+ *  row_len:    int32 [rows]: 1 <= row_len[r] <= max_pages * 64.
+ *  q:          fp16 [rows][heads][128], 16-byte aligned; out: fp32 [rows][heads][128].
+ *  An agent with more than 32 queries per KV head (its rows x heads / kv_heads), or a row
+ *  length out of range, sets *err_word |= 4 and its rows' outputs are zero.
+ *  workspace:  16-byte aligned, at least qmm_attn_workspace_bytes(dims) bytes (fixed by dims);
+ *              used by this call until its kernels finish.
+ *  err_word:   device-visible int, or-ed with 1 if a device-side wait ran out, 2 or 4 as
+ *              above; the caller zeroes it and reads it after synchronising.
+ * Errors: INVALID_ARG, MISALIGNED, SCRATCH_TOO_SMALL, CUDA.
+ */
+typedef struct {
+    int32_t heads;       /* query heads, a multiple of kv_heads */
+    int32_t kv_heads;
+    int32_t agents;      /* rows of page_table */
+    int32_t max_pages;   /* columns of page_table */
+    int64_t pool_pages;  /* pages in the pool */
+} qmm_attn_dims;
+
+qmm_status qmm_attn_workspace_bytes(const qmm_attn_dims* dims, int64_t* bytes);
+
+qmm_status qmm_attn_decode(const qmm_attn_dims* dims, const void* pool, const int32_t* page_table,
+                           const int32_t* agent_rows, const int32_t* row_len, const void* q, int64_t rows,
+                           float* out, void* workspace, int64_t workspace_bytes, int* err_word,
+                           void* stream);
+
+/*
  * Same as qmm_run with x and y in host memory (pinned memory gives asynchronous
  * copies): copies x to the handle's staging buffer, runs, copies y back, all on `stream`.
  * The caller must synchronise `stream` before reading y.  Needs opt.host_io at create.

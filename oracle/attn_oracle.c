@@ -20,10 +20,14 @@
  *
  * Pool layout (a reading; the pages give none): a page holds 64 consecutive tokens of one
  * agent for every KV head; (page P, head g) is the 17,408-byte record at (P * Hkv + g) * 17408:
- *   bytes     0 ..  8191  K quants, int8 [token 64][dim 128]
+ *   bytes     0 ..  8191  K quants, int8: token t's 128 dims in a 128-byte row, dim d at
+ *                         t * 128 + 16 * ((d / 16) XOR key(t)) + d % 16, key(t) =
+ *                         2 * (t % 4) + (t / 4) % 2 (16-byte pieces of a row permuted by the
+ *                         token, so that the pieces that four consecutive tokens read together,
+ *                         two neighbouring pieces each, lie in different shared-memory banks)
  *   bytes  8192 ..  8703  K scales, fp16 [token 64][dim block 4]
  *   bytes  8704 .. 16895  V quants, int8 [dim 128][token 64]   (dim-major)
- *   bytes 16896 .. 17407  V scales, fp16 [token 64][dim block 4]
+ *   bytes 16896 .. 17407  V scales, fp16 [dim block 4][token 64]
  * A K or V element is scale * quant, with the scale of its 32-dim block (q8_0).  Token t of
  * agent a is slot t % 64 of page page_table[a * max_pages + t / 64].
  */
@@ -43,8 +47,15 @@ double oracle_f16_to_double(uint16_t h);
 /* Element d of K (which = 0) or V (which = 1) of token `slot` in the record `rec`. */
 double oracle_kv(const uint8_t* rec, int which, int slot, int d) {
     const uint8_t* base = rec + which * 8704;
-    int8_t q = which == 0 ? (int8_t)base[slot * ATTN_D + d] : (int8_t)base[d * ATTN_PT + slot];
-    const uint8_t* sc = base + 8192 + 2 * (slot * 4 + d / 32);
+    int8_t q;
+    const uint8_t* sc;
+    if (which == 0) {
+        q = (int8_t)base[slot * ATTN_D + 16 * ((d / 16) ^ (2 * (slot % 4) + (slot / 4) % 2)) + d % 16];
+        sc = base + 8192 + 2 * (slot * 4 + d / 32);
+    } else {
+        q = (int8_t)base[d * ATTN_PT + slot];
+        sc = base + 8192 + 2 * ((d / 32) * ATTN_PT + slot);
+    }
     return oracle_f16_to_double((uint16_t)(sc[0] | (sc[1] << 8))) * (double)q;
 }
 

@@ -22,7 +22,8 @@ def test_header_declares_expected_api():
     assert names == sorted(["qmm_default_options", "qmm_create", "qmm_run", "qmm_run_host",
                             "qmm_get_error", "qmm_get_info", "qmm_destroy", "qmm_status_str",
                             "qmm_step_create", "qmm_step_launch", "qmm_step_destroy",
-                            "qmm_run_noalloc", "qmm_run_argmax"])
+                            "qmm_run_noalloc", "qmm_run_argmax", "qmm_attn_workspace_bytes",
+                            "qmm_attn_decode"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -111,3 +112,19 @@ def test_library_not_built_raises(tmp_path):
             Q.load(str(tmp_path / "missing.so"))
     finally:
         Q._lib = saved
+
+
+def test_attention_arguments_without_device(lib):
+    """The attention entry's workspace size (fixed by the dimensions) and the argument errors
+    it reports before any launch."""
+    dims = Q.AttnDims(48, 8, 4, 400, 1600)
+    nbytes = ctypes.c_int64()
+    assert lib.qmm_attn_workspace_bytes(ctypes.byref(dims), ctypes.byref(nbytes)) == 0
+    assert nbytes.value == 4 * 8 * 13 * 32 * 130 * 4  # agents x KV heads x 32-page runs x queries
+    for bad in (Q.AttnDims(48, 7, 4, 400, 1600), Q.AttnDims(0, 8, 4, 400, 1600), Q.AttnDims(48, 8, 0, 400, 1600),
+                Q.AttnDims(48, 8, 4, 0, 1600), Q.AttnDims(48, 8, 4, 400, 0)):
+        assert lib.qmm_attn_workspace_bytes(ctypes.byref(bad), ctypes.byref(nbytes)) == 1
+    buf = (ctypes.c_uint8 * 64)()
+    assert lib.qmm_attn_decode(ctypes.byref(dims), None, buf, buf, buf, buf, 1, buf, buf, 10**9, buf, None) == 1
+    assert lib.qmm_attn_decode(ctypes.byref(dims), buf, buf, buf, buf, buf, 0, buf, buf, 10**9, buf, None) == 1
+    assert lib.qmm_attn_decode(ctypes.byref(dims), buf, buf, buf, buf, buf, 1, buf, buf, 16, buf, None) in (3, 9)

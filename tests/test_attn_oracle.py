@@ -29,15 +29,20 @@ PT = oracle.ATTN_PAGE_TOKENS
 
 def decode_records(pool, kv_heads):
     """K [page, head, token, dim] and V [page, head, token, dim] in double, from the layout:
-    K quants int8 [token][dim], K scales fp16 [token][4], V quants int8 [dim][token], V scales
-    fp16 [token][4]."""
+    K quants int8 in 128-byte token rows whose 16-byte pieces are permuted (piece p of token t
+    stored at position p ^ (2 (t % 4) + (t / 4) % 2)), K scales fp16 [token][4], V quants int8 [dim][token], V
+    scales fp16 [4][token]."""
     recs = pool.reshape(-1, kv_heads, REC)
-    kq = recs[:, :, :8192].view(np.int8).reshape(-1, kv_heads, PT, D).astype(np.float64)
+    kq_stored = recs[:, :, :8192].view(np.int8).reshape(-1, kv_heads, PT, 8, 16)
+    t = np.arange(PT)[:, None]
+    pieces = np.arange(8)[None, :] ^ (2 * (t % 4) + (t // 4) % 2)   # [token][logical piece] -> stored
+    kq = np.take_along_axis(kq_stored, pieces[None, None, :, :, None], axis=3).reshape(-1, kv_heads, PT, D)
+    kq = kq.astype(np.float64)
     ks = recs[:, :, 8192:8704].copy().view(np.float16).reshape(-1, kv_heads, PT, 4).astype(np.float64)
     vq = recs[:, :, 8704:16896].view(np.int8).reshape(-1, kv_heads, D, PT).astype(np.float64)
-    vs = recs[:, :, 16896:].copy().view(np.float16).reshape(-1, kv_heads, PT, 4).astype(np.float64)
+    vs = recs[:, :, 16896:].copy().view(np.float16).reshape(-1, kv_heads, 4, PT).astype(np.float64)
     k = kq * np.repeat(ks, 32, axis=3)
-    v = np.swapaxes(vq, 2, 3) * np.repeat(vs, 32, axis=3)
+    v = np.swapaxes(vq, 2, 3) * np.repeat(np.swapaxes(vs, 2, 3), 32, axis=3)
     return k, v
 
 
@@ -96,7 +101,7 @@ def _zero_k_holds(attn, pool, table, q, kvh):
             for t in range(70):
                 rec = recs[table[0, t // PT], g]
                 qv = int(rec[8704 + d * PT + t % PT].astype(np.int8))
-                sc = Fraction(float(rec[16896 + 2 * ((t % PT) * 4 + d // 32):][:2].copy().view(np.float16)[0]))
+                sc = Fraction(float(rec[16896 + 2 * ((d // 32) * PT + t % PT):][:2].copy().view(np.float16)[0]))
                 total += sc * qv
             if abs(Fraction(out[0, h, d]) - total / 70) > Fraction(1, 10**12) * (1 + abs(total)):
                 return False
@@ -125,7 +130,7 @@ def _causal_holds(attn, pool, table, q, ra, rl, kvh):
     recs = pool2.reshape(-1, kvh, REC)
     # token 71 of agent 0 (row 0 attends to 71 tokens: 0..70): scramble its K and V quants
     p, slot = table[0, 71 // PT], 71 % PT
-    recs[p, :, slot * D:(slot + 1) * D] ^= 0x55
+    recs[p, :, slot * D:(slot + 1) * D] ^= 0x55  # the token's whole (permuted) K row
     recs[p, :, 8704 + slot:8704 + 8192:PT] ^= 0x55
     out2, _ = attn(pool2, table, q, ra, rl, kvh)
     return np.array_equal(out[0], out2[0]) and not np.array_equal(out[1], out2[1])
@@ -190,11 +195,14 @@ MUTANTS = {
     "no_score_scale": ("s[t] = dot / sqrt((double)ATTN_D);", "s[t] = dot;"),
     "v_not_transposed": ("(int8_t)base[d * ATTN_PT + slot]", "(int8_t)base[slot * ATTN_D + d]"),
     "scale_block_16": ("2 * (slot * 4 + d / 32)", "2 * (slot * 4 + (d / 16) % 4)"),
+    "k_pieces_unpermuted": ("16 * ((d / 16) ^ (2 * (slot % 4) + (slot / 4) % 2)) + d % 16", "d"),
+    "k_piece_key_plain": ("(2 * (slot % 4) + (slot / 4) % 2)", "(slot % 8)"),
+    "v_scales_token_major": ("2 * ((d / 32) * ATTN_PT + slot)", "2 * (slot * 4 + d / 32)"),
     "one_token_short": ("for (int t = 0; t < len; ++t) {\n                const uint8_t* rec = pool + ((size_t)page_table[a * max_pages + t / ATTN_PT] * Hkv + g) * ATTN_REC;\n                const double p",
                         "for (int t = 0; t < len - 1; ++t) {\n                const uint8_t* rec = pool + ((size_t)page_table[a * max_pages + t / ATTN_PT] * Hkv + g) * ATTN_REC;\n                const double p"),
     "gqa_modulo": ("const int g = h / group,", "const int g = h % Hkv,"),
     "page_slot_shift": ("oracle_kv(rec, 0, t % ATTN_PT, d)", "oracle_kv(rec, 0, (t + 1) % ATTN_PT, d)"),
-    "v_scale_from_k": ("const uint8_t* sc = base + 8192", "const uint8_t* sc = rec + 8192"),
+    "v_scale_from_k": ("sc = base + 8192 + 2 * ((d / 32) * ATTN_PT + slot);", "sc = rec + 8192 + 2 * ((d / 32) * ATTN_PT + slot);"),
 }
 
 
