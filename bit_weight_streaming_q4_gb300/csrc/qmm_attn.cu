@@ -44,12 +44,12 @@ namespace attn {
 
 constexpr int kD = 128, kPT = 64, kRec = 17408;
 constexpr int kMaxQ = 32;   // queries per item: rows of the agent x heads of the group
-constexpr int kChunk = 32;  // pages per work item (one wave of CTAs at the pages' decode step)
+constexpr int kSlotCap = 1024;  // upper bound on the resident CTAs a launch is planned for
 constexpr int kStages = 4;  // pages in flight per CTA
 constexpr int kThreads = 128;
 constexpr int kPart = kD + 2;  // floats per query of an item's partial: o[128], m, l
 constexpr float kNegBig = -1e30f;
-constexpr int kPS = kPT + 8;  // halves per row of the probability tile (16-byte padding: no bank conflicts)
+constexpr int kPS = kPT + 4;  // halves per row of the probability tile (136 bytes: conflict-free 8-byte reads)
 
 struct Item {
     int32_t agent, g;      // agent, KV head
@@ -66,14 +66,15 @@ struct Params {
     const int32_t* row_len;     // [rows]
     const int32_t* agent_rows;  // [agents + 1]: agent a's rows are agent_rows[a] .. agent_rows[a+1] - 1
     int32_t heads, kv_heads, group;
-    int32_t agents, max_chunks;
+    int32_t agents;
+    int32_t runs, chunk;        // runs of pages per (agent, KV head), pages per run
     float* ws;                  // [agent][kv head][run][kMaxQ][kPart]
     int* err;                   // sticky error word
     float* out;                 // [rows][heads][128]
     int64_t rows;
 };
 
-// Agent a's rows (r0, nr) and its number of 32-page runs, or -1 runs (and the error word)
+// Agent a's rows (r0, nr) and its number of runs of p.chunk pages, or -1 runs (and the error word)
 // if its rows or lengths are outside what the kernels handle.
 __device__ __forceinline__ int agent_runs(const Params& p, int a, int& r0, int& nr) {
     r0 = p.agent_rows[a];
@@ -87,7 +88,7 @@ __device__ __forceinline__ int agent_runs(const Params& p, int a, int& r0, int& 
         maxlen = len > maxlen ? len : maxlen;
     }
     const int pages = (maxlen + kPT - 1) / kPT;
-    return (pages + kChunk - 1) / kChunk;
+    return (pages + p.chunk - 1) / p.chunk;
 }
 
 // Bytes 0, 1 (sel 0x4140) or 2, 3 (sel 0x4342) of four int8 already XORed with 0x80, as
@@ -96,22 +97,40 @@ __device__ __forceinline__ uint32_t i8pair_to_h2(uint32_t biased, uint32_t sel) 
     return as_u32(__hadd2(as_h2(prmt(biased, 0x64646464u, sel)), as_h2(0xE480E480u)));
 }
 
-__global__ void __launch_bounds__(kThreads) attn_partial(const Params p) {
+// 2^x (the ex2 instruction, flush to zero).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// d = A.B with a zero accumulator.
+__device__ __forceinline__ void mma_m16n8k16_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+__global__ void __launch_bounds__(kThreads, 3) attn_partial(const Params p) {
     extern __shared__ __align__(128) uint8_t sm[];
     // ring slot i % kStages holds page i
-    __half* P = reinterpret_cast<__half*>(sm + kStages * kRec);       // [kMaxQ][kPS]
-    float* red_max = reinterpret_cast<float*>(P + kMaxQ * kPS);       // [4][kMaxQ]
-    float* red_sum = red_max + 4 * kMaxQ;                              // [4][kMaxQ]
+    __half* P = reinterpret_cast<__half*>(sm + kStages * kRec);       // [kMaxQ][kPS] probabilities
+    float* red_max = reinterpret_cast<float*>(P + kMaxQ * kPS);       // [kMaxQ][4 warps]
+    float* red_sum = red_max + 4 * kMaxQ;                              // [kMaxQ][4 warps]
     uint64_t* bar = reinterpret_cast<uint64_t*>(red_sum + 4 * kMaxQ);  // [kStages]
     volatile int* flags = reinterpret_cast<volatile int*>(bar + kStages);  // [0] abort
+    int* qlen_sm = const_cast<int*>(reinterpret_cast<volatile int*>(flags + 4));  // [kMaxQ] tokens per query
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g8 = lane >> 2, t4 = lane & 3;
     // this CTA's work item
     Item it;
-    it.agent = blockIdx.x / (p.kv_heads * p.max_chunks);
-    it.g = (blockIdx.x / p.max_chunks) % p.kv_heads;
-    const int run = blockIdx.x % p.max_chunks;
+    it.agent = blockIdx.x / (p.kv_heads * p.runs);
+    it.g = (blockIdx.x / p.runs) % p.kv_heads;
+    const int run = blockIdx.x % p.runs;
+    int minlen = 0;  // the shortest row of the item: pages below it need no mask
     {
         const int runs = agent_runs(p, it.agent, it.r0, it.nr);
         if (runs < 0) {
@@ -120,13 +139,17 @@ __global__ void __launch_bounds__(kThreads) attn_partial(const Params p) {
         }
         if (run >= runs) return;
         int maxlen = 0;
-        for (int r = it.r0; r < it.r0 + it.nr; ++r) maxlen = p.row_len[r] > maxlen ? p.row_len[r] : maxlen;
+        minlen = p.row_len[it.r0];
+        for (int r = it.r0; r < it.r0 + it.nr; ++r) {
+            maxlen = p.row_len[r] > maxlen ? p.row_len[r] : maxlen;
+            minlen = p.row_len[r] < minlen ? p.row_len[r] : minlen;
+        }
         const int pages = (maxlen + kPT - 1) / kPT;
-        it.page0 = run * kChunk;
-        it.npages = pages - it.page0 < kChunk ? pages - it.page0 : kChunk;
+        it.page0 = run * p.chunk;
+        it.npages = pages - it.page0 < p.chunk ? pages - it.page0 : p.chunk;
     }
     const int nq = it.nr * p.group;
-    const int nmt = (nq + 15) >> 4;  // m16 tiles of queries (1 or 2)
+    const int nnt = (nq + 7) >> 3;  // n8 tiles of queries (1 .. 4)
     const float c2 = 1.4426950408889634f * 0.08838834764831845f;  // log2(e) / sqrt(128)
 
     if (tid == 0) {
@@ -134,6 +157,7 @@ __global__ void __launch_bounds__(kThreads) attn_partial(const Params p) {
         flags[0] = 0;
         fence_mbar_init();
     }
+    if (tid < kMaxQ) qlen_sm[tid] = tid < nq ? p.row_len[it.r0 + tid / p.group] : 0;
     __syncthreads();
 
     // the record of logical page i of the item, or null (and the error word) if the page
@@ -160,211 +184,215 @@ __global__ void __launch_bounds__(kThreads) attn_partial(const Params p) {
     if (tid == 0)
         for (int i = 0; i < kStages - 1 && i < it.npages; ++i) issue(i);
 
-    // Query fragments (A of QK^T).  The dims of k-step ks = 2 blk + k2 are assigned so that
-    // each thread's eight dims of a 32-dim block are contiguous: slots (2t, 2t+1) are dims
-    // 32 blk + 8t + 4 k2 + {0, 1} and slots (2t+8, 2t+9) dims 32 blk + 8t + 4 k2 + {2, 3};
-    // K's B fragments use the same assignment.  Query qi = 16 mt + row is head
-    // g * group + qi % group of row r0 + qi / group; queries past nq are zero.
-    uint32_t qa[2][8][4];
-    int qlen[2][2];  // tokens attended by this thread's two query rows of each m-tile
+    // Both products run with tokens or dims as the MMA's M and the item's queries as N (n8
+    // tiles nt: queries 8 nt .. 8 nt + 7; query qi is head g * group + qi % group of row
+    // r0 + qi / group, and queries past nq are zero).
+    //
+    // S^T = K . Q^T: warp w takes tokens 16w .. 16w + 15 of the page.  The dims of k-step
+    // ks = 2 blk + k2 are assigned so that every thread's eight dims of a 32-dim block are
+    // contiguous: k-slots (2t, 2t+1) are dims 32 blk + 8t + 4 k2 + {0, 1}, slots (2t+8, 2t+9)
+    // dims 32 blk + 8t + 4 k2 + {2, 3}.  qb holds Q^T's B fragments for all k-steps.
+    uint32_t qb[4][8][2];
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+    for (int nt = 0; nt < 4; ++nt) {
+        const int qi = 8 * nt + g8;
+        const __half* qrow = nullptr;
+        if (qi < nq)
+            qrow = p.q + (static_cast<int64_t>(it.r0 + qi / p.group) * p.heads + it.g * p.group + qi % p.group) * kD;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int qi = 16 * mt + g8 + 8 * hh;
-            qlen[mt][hh] = 0;
-            const __half* qrow = nullptr;
-            if (qi < nq) {
-                const int r = it.r0 + qi / p.group;
-                const int h = it.g * p.group + qi % p.group;
-                qrow = p.q + (static_cast<int64_t>(r) * p.heads + h) * kD;
-                qlen[mt][hh] = p.row_len[r];
-            }
+        for (int blk = 0; blk < 4; ++blk) {
+            const uint4 v = qrow ? *reinterpret_cast<const uint4*>(qrow + 32 * blk + 8 * t4) : make_uint4(0u, 0u, 0u, 0u);
+            qb[nt][2 * blk][0] = v.x;
+            qb[nt][2 * blk][1] = v.y;
+            qb[nt][2 * blk + 1][0] = v.z;
+            qb[nt][2 * blk + 1][1] = v.w;
+        }
+    }
+
+    // Running state per accumulator column: the maximum score, the thread's share of the
+    // sum of probabilities, and O^T (dims 32w + 16 mt + {g8, g8 + 8}).  Probabilities carry a
+    // factor 2^8 (kept in the sum too) so that P times a V scale stays clear of the fp16
+    // subnormal range.
+    float m_run[4][2], l_part[4][2];
+    float o[2][4][4];  // [m16 tile of dims][n8 tile of queries][accumulator]
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint2 v = qrow ? *reinterpret_cast<const uint2*>(qrow + 32 * (ks >> 1) + 8 * t4 + 4 * (ks & 1))
-                                     : make_uint2(0u, 0u);
-                qa[mt][ks][hh] = v.x;      // a0 (row g8) / a1 (row g8 + 8)
-                qa[mt][ks][2 + hh] = v.y;  // a2 / a3
+    for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            m_run[nt][e] = kNegBig;
+            l_part[nt][e] = 0.f;
+        }
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) o[mt][nt][c] = 0.f;
+    }
+
+    const int t0 = 16 * warp + g8;                           // the thread's tokens t0, t0 + 8
+    const int kkey = 2 * (g8 & 3) + ((g8 >> 2) & 1);          // K piece key of both (t0 % 8 == g8)
+    bool live = true;
+    int consumed = 0;
+    for (int i = 0; i < it.npages; ++i) {
+        const bool ok = mbar_wait_bounded(&bar[i % kStages], (i / kStages) & 1, flags);
+        const uint8_t* rec = sm + (i % kStages) * kRec;
+        const int tbase = (it.page0 + i) * kPT;  // logical index of the page's first token
+
+        // ---- scores s[nt][c]: c0 (token t0, query 8nt + 2t4), c1 (t0, +1), c2 (t0 + 8, ..), c3
+        float s[4][4];
+        {
+            const uint2 sca = *reinterpret_cast<const uint2*>(rec + 8192 + t0 * 8);
+            const uint2 scb = *reinterpret_cast<const uint2*>(rec + 8192 + (t0 + 8) * 8);
+#pragma unroll
+            for (int blk = 0; blk < 4; ++blk) {
+                const uint8_t* kr = rec + t0 * kD + 16 * ((2 * blk + (t4 >> 1)) ^ kkey) + 8 * (t4 & 1);
+                const uint2 ka = *reinterpret_cast<const uint2*>(kr);
+                const uint2 kb = *reinterpret_cast<const uint2*>(kr + 8 * kD);
+                const uint32_t xa = ka.x ^ 0x80808080u, ya = ka.y ^ 0x80808080u;
+                const uint32_t xb = kb.x ^ 0x80808080u, yb = kb.y ^ 0x80808080u;
+                // A fragments of k-steps 2 blk (from .x) and 2 blk + 1 (from .y)
+                const uint32_t a00 = i8pair_to_h2(xa, 0x4140u), a01 = i8pair_to_h2(xb, 0x4140u);
+                const uint32_t a02 = i8pair_to_h2(xa, 0x4342u), a03 = i8pair_to_h2(xb, 0x4342u);
+                const uint32_t a10 = i8pair_to_h2(ya, 0x4140u), a11 = i8pair_to_h2(yb, 0x4140u);
+                const uint32_t a12 = i8pair_to_h2(ya, 0x4342u), a13 = i8pair_to_h2(yb, 0x4342u);
+                const uint32_t wa = (blk >> 1) ? sca.y : sca.x, wb = (blk >> 1) ? scb.y : scb.x;
+                const float sa = __half2float((blk & 1) ? __high2half(as_h2(wa)) : __low2half(as_h2(wa)));
+                const float sb = __half2float((blk & 1) ? __high2half(as_h2(wb)) : __low2half(as_h2(wb)));
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    if (nt < nnt) {
+                        float tmp[4];
+                        mma_m16n8k16_z(tmp, a00, a01, a02, a03, qb[nt][2 * blk][0], qb[nt][2 * blk][1]);
+                        mma_m16n8k16(tmp, a10, a11, a12, a13, qb[nt][2 * blk + 1][0], qb[nt][2 * blk + 1][1]);
+                        if (blk == 0) {
+                            s[nt][0] = tmp[0] * sa;
+                            s[nt][1] = tmp[1] * sa;
+                            s[nt][2] = tmp[2] * sb;
+                            s[nt][3] = tmp[3] * sb;
+                        } else {
+                            s[nt][0] = fmaf(tmp[0], sa, s[nt][0]);
+                            s[nt][1] = fmaf(tmp[1], sa, s[nt][1]);
+                            s[nt][2] = fmaf(tmp[2], sb, s[nt][2]);
+                            s[nt][3] = fmaf(tmp[3], sb, s[nt][3]);
+                        }
+                    }
+                }
             }
         }
-
-    float m_run[2][2], l_run[2][2];
-    float o[2][4][4];  // [m-tile][n8 tile of dims 32w + 8nt][accumulator]
+        // ---- masks (only on pages reaching past the shortest row) and the warp's maxima
+        if (tbase + kPT > minlen) {
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
+            for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            m_run[mt][hh] = kNegBig;
-            l_run[mt][hh] = 0.f;
+                for (int e = 0; e < 2; ++e) {
+                    if (nt < nnt) {
+                        const int len = qlen_sm[8 * nt + 2 * t4 + e];
+                        if (tbase + t0 >= len) s[nt][e] = kNegBig;
+                        if (tbase + t0 + 8 >= len) s[nt][2 + e] = kNegBig;
+                    }
+                }
         }
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
-    }
-
-    bool live = true;
-    int consumed = 0;
-    for (int i = 0; i < it.npages; ++i) {
-        // slot (i + kStages - 1) % kStages held page i - 1, released at the end of the last iteration
-        if (tid == 0 && i + kStages - 1 < it.npages) issue(i + kStages - 1);
-        const bool ok = mbar_wait_bounded(&bar[i % kStages], (i / kStages) & 1, flags);
-        // one decision for the whole CTA (every thread reaches this barrier)
+            for (int e = 0; e < 2; ++e) {
+                if (nt < nnt) {
+                    float mx = fmaxf(s[nt][e], s[nt][2 + e]);
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                    if (g8 == 0) red_max[(8 * nt + 2 * t4 + e) * 4 + warp] = mx;
+                }
+            }
+        // one decision for the whole CTA (every thread reaches this barrier); the scores of a
+        // page whose wait failed are never used
         if (__syncthreads_or(!ok || flags[0])) {
             live = false;
             break;
         }
         consumed = i + 1;
-        const uint8_t* rec = sm + (i % kStages) * kRec;
-        const int tbase = (it.page0 + i) * kPT;  // logical index of the page's first token
+        // every warp is past page i - 1: its slot takes page i + kStages - 1
+        if (tid == 0 && i + kStages - 1 < it.npages) issue(i + kStages - 1);
 
-        // ---- scores of tokens 16w .. 16w + 15: s[mt][nt][e], raw dot products
-        float s[2][2][4];
+        // ---- new maxima, rescaling, probabilities (x 2^8, fp16) to shared memory
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
+        for (int nt = 0; nt < 4; ++nt) {
+            if (nt < nnt) {
+                float pr[4];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+                for (int e = 0; e < 2; ++e) {
+                    const float4 rm = *reinterpret_cast<const float4*>(red_max + (8 * nt + 2 * t4 + e) * 4);
+                    const float mn = fmaxf(fmaxf(m_run[nt][e], fmaxf(rm.x, rm.y)), fmaxf(rm.z, rm.w));
+                    const float alpha = ex2((m_run[nt][e] - mn) * c2);
+                    const float mc2 = mn == kNegBig ? __int_as_float(0x7f800000) : fmaf(mn, c2, -8.f);
+                    pr[e] = ex2(fmaf(s[nt][e], c2, -mc2));
+                    pr[2 + e] = ex2(fmaf(s[nt][2 + e], c2, -mc2));
+                    l_part[nt][e] = fmaf(l_part[nt][e], alpha, pr[e] + pr[2 + e]);
+                    m_run[nt][e] = mn;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) s[mt][nt][e] = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int tokb = 16 * warp + 8 * nt + g8;      // this thread's B column (token)
-            const int tokc = 16 * warp + 8 * nt + 2 * t4;  // its accumulator columns (tokens)
-            // the four block scales of the two accumulator tokens
-            const uint2 sc0v = *reinterpret_cast<const uint2*>(rec + 8192 + tokc * 8);
-            const uint2 sc1v = *reinterpret_cast<const uint2*>(rec + 8192 + (tokc + 1) * 8);
-            const uint32_t sc0w[2] = {sc0v.x, sc0v.y}, sc1w[2] = {sc1v.x, sc1v.y};
-#pragma unroll
-            for (int blk = 0; blk < 4; ++blk) {
-                // eight contiguous dims 32 blk + 8 t4 .. + 7 of token tokb (16-byte piece p of
-                // the row is stored at p ^ key, key = 2 (token % 4) + (token / 4) % 2: the 16
-                // threads of a half-warp read 16 different 8-byte bank pairs)
-                const int piece = (2 * blk + (t4 >> 1)) ^ (2 * (tokb & 3) + ((tokb >> 2) & 1));
-                const uint2 kw = *reinterpret_cast<const uint2*>(rec + tokb * kD + 16 * piece + 8 * (t4 & 1));
-                const float sc0 = __half2float((blk & 1) ? __high2half(as_h2(sc0w[blk >> 1])) : __low2half(as_h2(sc0w[blk >> 1])));
-                const float sc1 = __half2float((blk & 1) ? __high2half(as_h2(sc1w[blk >> 1])) : __low2half(as_h2(sc1w[blk >> 1])));
-                const uint32_t kx = kw.x ^ 0x80808080u, ky = kw.y ^ 0x80808080u;
-                const uint32_t b00 = i8pair_to_h2(kx, 0x4140u), b01 = i8pair_to_h2(kx, 0x4342u);
-                const uint32_t b10 = i8pair_to_h2(ky, 0x4140u), b11 = i8pair_to_h2(ky, 0x4342u);
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    if (mt >= nmt) break;
-                    float tmp[4] = {0.f, 0.f, 0.f, 0.f};
-                    const int ks = 2 * blk;
-                    mma_m16n8k16(tmp, qa[mt][ks][0], qa[mt][ks][1], qa[mt][ks][2], qa[mt][ks][3], b00, b01);
-                    mma_m16n8k16(tmp, qa[mt][ks + 1][0], qa[mt][ks + 1][1], qa[mt][ks + 1][2], qa[mt][ks + 1][3], b10, b11);
-                    s[mt][nt][0] += tmp[0] * sc0;
-                    s[mt][nt][1] += tmp[1] * sc1;
-                    s[mt][nt][2] += tmp[2] * sc0;
-                    s[mt][nt][3] += tmp[3] * sc1;
+                    for (int mt = 0; mt < 2; ++mt) {
+                        o[mt][nt][e] *= alpha;
+                        o[mt][nt][2 + e] *= alpha;
+                    }
                 }
+                // P[query][token]: lanes g8 and g8 ^ 1 swap values so that each stores two
+                // consecutive tokens of one query (even g8: query 2t4, odd: query 2t4 + 1)
+                const bool odd = g8 & 1;
+                const uint32_t mine_lo = as_u32(__floats2half2_rn(pr[0], pr[1]));  // (t0, q), (t0, q+1)
+                const uint32_t mine_hi = as_u32(__floats2half2_rn(pr[2], pr[3]));  // (t0+8, q), (t0+8, q+1)
+                // even sends its q+1 values, odd its q values: (token t0, token t0 + 8)
+                const uint32_t send = odd ? prmt(mine_lo, mine_hi, 0x5410u) : prmt(mine_lo, mine_hi, 0x7632u);
+                const uint32_t got = __shfl_xor_sync(0xffffffffu, send, 4);
+                // even: (own q of t0, partner's q of t0 + 1), and the same for t0 + 8
+                // odd:  (partner's q+1 of t0 - 1, own q+1 of t0), and the same for t0 + 7
+                const uint32_t lo = odd ? prmt(got, mine_lo, 0x7610u) : prmt(mine_lo, got, 0x5410u);
+                const uint32_t hi = odd ? prmt(got, mine_hi, 0x7632u) : prmt(mine_hi, got, 0x7610u);
+                const int qrow = 8 * nt + 2 * t4 + (odd ? 1 : 0);
+                const int tcol = odd ? t0 - 1 : t0;
+                *reinterpret_cast<uint32_t*>(P + qrow * kPS + tcol) = lo;
+                *reinterpret_cast<uint32_t*>(P + qrow * kPS + tcol + 8) = hi;
             }
         }
-        // ---- masking and this warp's row maxima over its 16 tokens
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float mx = kNegBig;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int e2 = 0; e2 < 2; ++e2) {
-                        const int t = tbase + 16 * warp + 8 * nt + 2 * t4 + e2;
-                        float& v = s[mt][nt][2 * hh + e2];
-                        if (t >= qlen[mt][hh]) v = kNegBig;
-                        mx = fmaxf(mx, v);
-                    }
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                if (t4 == 0) red_max[warp * kMaxQ + 16 * mt + g8 + 8 * hh] = mx;
-            }
-        __syncthreads();
-        // ---- the page's maxima, new running maxima, probabilities (fp16) to shared memory
-        float m_new[2][2];
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int qi = 16 * mt + g8 + 8 * hh;
-                float mx = m_run[mt][hh];
-#pragma unroll
-                for (int w = 0; w < 4; ++w) mx = fmaxf(mx, red_max[w * kMaxQ + qi]);
-                m_new[mt][hh] = mx;
-                float sum = 0.f;
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    float pr[2];
-#pragma unroll
-                    for (int e2 = 0; e2 < 2; ++e2) {
-                        const float v = s[mt][nt][2 * hh + e2];
-                        pr[e2] = v == kNegBig ? 0.f : exp2f((v - mx) * c2);
-                        sum += pr[e2];
-                    }
-                    *reinterpret_cast<__half2*>(P + qi * kPS + 16 * warp + 8 * nt + 2 * t4) = __floats2half2_rn(pr[0], pr[1]);
-                }
-                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-                if (t4 == 0) red_sum[warp * kMaxQ + qi] = sum;
-            }
-        __syncthreads();
-        // ---- running sums and rescaling of the output
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int qi = 16 * mt + g8 + 8 * hh;
-                const float alpha = m_run[mt][hh] == m_new[mt][hh] ? 1.f : exp2f((m_run[mt][hh] - m_new[mt][hh]) * c2);
-                float add = 0.f;
-#pragma unroll
-                for (int w = 0; w < 4; ++w) add += red_sum[w * kMaxQ + qi];
-                l_run[mt][hh] = l_run[mt][hh] * alpha + add;
-                m_run[mt][hh] = m_new[mt][hh];
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt) {
-                    o[mt][nt][2 * hh] *= alpha;
-                    o[mt][nt][2 * hh + 1] *= alpha;
-                }
-            }
-        // ---- P . V for dims 32w .. 32w + 31 (one V scale block).  Tokens of k-step ks are
-        // assigned so that each thread's sixteen tokens 16 t4 .. 16 t4 + 15 are contiguous:
-        // slots (2t, 2t+1) are tokens 16t + 4 ks + {0, 1}, slots (2t+8, 2t+9) 16t + 4 ks + {2, 3}.
+        __syncthreads();  // P complete
+
+        // ---- O^T += V^T . (P x V scale)^T for dims 32w .. 32w + 31 (one V scale block).
+        // Tokens of k-step ks are assigned so that every thread's sixteen tokens are
+        // contiguous: k-slots (2t, 2t+1) are tokens 16t + 4 ks + {0, 1}, slots (2t+8, 2t+9)
+        // tokens 16t + 4 ks + {2, 3}.
         {
-            const uint4 dva = *reinterpret_cast<const uint4*>(rec + 16896 + (warp * kPT + 16 * t4) * 2);
-            const uint4 dvb = *reinterpret_cast<const uint4*>(rec + 16896 + (warp * kPT + 16 * t4 + 8) * 2);
-            const uint32_t dv[8] = {dva.x, dva.y, dva.z, dva.w, dvb.x, dvb.y, dvb.z, dvb.w};
-            // A fragments: P times the tokens' V scales, [m-tile][row g8 / g8 + 8][token pair]
-            uint32_t pa[2][2][8];
+            uint32_t wv[2][2][4];  // raw V: [m16 tile][row g8 / g8 + 8][word ks], biased
 #pragma unroll
             for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const __half* prow = P + (16 * mt + g8 + 8 * hh) * kPS + 16 * t4;
-                    const uint4 x = *reinterpret_cast<const uint4*>(prow);
-                    const uint4 y = *reinterpret_cast<const uint4*>(prow + 8);
-                    const uint32_t pw[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) pa[mt][hh][j] = as_u32(__hmul2(as_h2(pw[j]), as_h2(dv[j])));
+                for (int h = 0; h < 2; ++h) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(rec + 8704 + (32 * warp + 16 * mt + 8 * h + g8) * kPT + 16 * t4);
+                    wv[mt][h][0] = v.x ^ 0x80808080u;
+                    wv[mt][h][1] = v.y ^ 0x80808080u;
+                    wv[mt][h][2] = v.z ^ 0x80808080u;
+                    wv[mt][h][3] = v.w ^ 0x80808080u;
                 }
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                const int dim = 32 * warp + 8 * nt + g8;
-                const uint4 vq = *reinterpret_cast<const uint4*>(rec + 8704 + dim * kPT + 16 * t4);
-                const uint32_t vw[4] = {vq.x ^ 0x80808080u, vq.y ^ 0x80808080u, vq.z ^ 0x80808080u, vq.w ^ 0x80808080u};
+            for (int ks = 0; ks < 4; ++ks) {
+                // V scales of tokens 16 t4 + 4 ks .. + 3 (this warp's block)
+                const uint2 dv = *reinterpret_cast<const uint2*>(rec + 16896 + (warp * kPT + 16 * t4 + 4 * ks) * 2);
+                uint32_t pb[4][2];  // B fragments: (P x V scale) of query 8 nt + g8, the k-step's tokens
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint32_t b0 = i8pair_to_h2(vw[ks], 0x4140u), b1 = i8pair_to_h2(vw[ks], 0x4342u);
-#pragma unroll
-                    for (int mt = 0; mt < 2; ++mt) {
-                        if (mt >= nmt) break;
-                        mma_m16n8k16(o[mt][nt], pa[mt][0][2 * ks], pa[mt][1][2 * ks], pa[mt][0][2 * ks + 1],
-                                     pa[mt][1][2 * ks + 1], b0, b1);
+                for (int nt = 0; nt < 4; ++nt) {
+                    if (nt < nnt) {
+                        const uint2 pw = *reinterpret_cast<const uint2*>(P + (8 * nt + g8) * kPS + 16 * t4 + 4 * ks);
+                        pb[nt][0] = as_u32(__hmul2(as_h2(pw.x), as_h2(dv.x)));
+                        pb[nt][1] = as_u32(__hmul2(as_h2(pw.y), as_h2(dv.y)));
                     }
+                }
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    const uint32_t a0 = i8pair_to_h2(wv[mt][0][ks], 0x4140u), a2 = i8pair_to_h2(wv[mt][0][ks], 0x4342u);
+                    const uint32_t a1 = i8pair_to_h2(wv[mt][1][ks], 0x4140u), a3 = i8pair_to_h2(wv[mt][1][ks], 0x4342u);
+#pragma unroll
+                    for (int nt = 0; nt < 4; ++nt)
+                        if (nt < nnt) mma_m16n8k16(o[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
                 }
             }
         }
-        __syncthreads();  // P and this page's buffer are free again
     }
     if (!live) {
         if (tid == 0) {
@@ -376,24 +404,38 @@ __global__ void __launch_bounds__(kThreads) attn_partial(const Params p) {
         return;
     }
 
-    // ---- the item's partial: o (this warp's dims), m and l per query
+    // ---- the item's partial: o, m and l per query
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            if (nt < nnt) {
+                float l = l_part[nt][e];
+                l += __shfl_xor_sync(0xffffffffu, l, 4);
+                l += __shfl_xor_sync(0xffffffffu, l, 8);
+                l += __shfl_xor_sync(0xffffffffu, l, 16);
+                if (g8 == 0) red_sum[(8 * nt + 2 * t4 + e) * 4 + warp] = l;
+            }
+        }
+    __syncthreads();
     float* part = p.ws + static_cast<int64_t>(blockIdx.x) * kMaxQ * kPart;  // slot (agent, g, run)
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int qi = 16 * mt + g8 + 8 * hh;
-            if (qi >= nq) continue;
+        for (int e = 0; e < 2; ++e) {
+            const int qi = 8 * nt + 2 * t4 + e;
+            if (nt >= nnt || qi >= nq) continue;
             float* pq = part + qi * kPart;
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                const int dim = 32 * warp + 8 * nt + 2 * t4;
-                pq[dim] = o[mt][nt][2 * hh];
-                pq[dim + 1] = o[mt][nt][2 * hh + 1];
+            for (int mt = 0; mt < 2; ++mt) {
+                const int dim = 32 * warp + 16 * mt + g8;
+                pq[dim] = o[mt][nt][e];
+                pq[dim + 8] = o[mt][nt][2 + e];
             }
-            if (warp == 0 && t4 == 0) {
-                pq[kD] = m_run[mt][hh];
-                pq[kD + 1] = l_run[mt][hh];
+            if (warp == 0 && g8 == 0) {
+                const float4 ls = *reinterpret_cast<const float4*>(red_sum + qi * 4);
+                pq[kD] = m_run[nt][e];
+                pq[kD + 1] = (ls.x + ls.y) + (ls.z + ls.w);
             }
         }
 }
@@ -422,7 +464,7 @@ __global__ void attn_combine(const Params p) {
     }
     const int g = h / p.group;
     const int qi = static_cast<int>(r - r0) * p.group + h % p.group;
-    const int64_t first = (static_cast<int64_t>(a) * p.kv_heads + g) * p.max_chunks;
+    const int64_t first = (static_cast<int64_t>(a) * p.kv_heads + g) * p.runs;
     const float c2 = 1.4426950408889634f * 0.08838834764831845f;
     float m = kNegBig;
     for (int c = 0; c < n; ++c) m = fmaxf(m, p.ws[((first + c) * kMaxQ + qi) * kPart + kD]);
@@ -438,7 +480,27 @@ __global__ void attn_combine(const Params p) {
     p.out[idx] = o / l;
 }
 
-constexpr int kSmem = kStages * kRec + kMaxQ * kPS * 2 + 2 * 4 * kMaxQ * 4 + kStages * 8 + 16;
+constexpr int kSmem = kStages * kRec + kMaxQ * kPS * 2 + 2 * 4 * kMaxQ * 4 + kStages * 8 + 16 + kMaxQ * 4;
+
+// Runs per (agent, KV head) and pages per run for a launch on `slots` resident CTAs: the
+// runs of a full-width page table fill one wave.  The cut depends only on the dims and the
+// device, never on the rows, so a row's result does not depend on the rest of the batch.
+void plan_runs(const qmm_attn_dims* dims, int64_t slots, int32_t* runs, int32_t* chunk) {
+    const int64_t items = static_cast<int64_t>(dims->agents) * dims->kv_heads;
+    const int64_t cap = slots < kSlotCap ? slots : kSlotCap;
+    int64_t r = cap / items;
+    if (r < 1) r = 1;
+    const int64_t c = (dims->max_pages + r - 1) / r;
+    *chunk = static_cast<int32_t>(c);
+    *runs = static_cast<int32_t>((dims->max_pages + c - 1) / c);
+}
+
+// Largest number of runs any device can be planned for (kSlotCap resident CTAs).
+int64_t max_runs(const qmm_attn_dims* dims) {
+    int32_t runs = 0, chunk = 0;
+    plan_runs(dims, kSlotCap, &runs, &chunk);
+    return runs;
+}
 
 }  // namespace attn
 }  // namespace qmm
@@ -450,8 +512,8 @@ qmm_status qmm_attn_workspace_bytes(const qmm_attn_dims* dims, int64_t* bytes) {
     if (dims->heads < 1 || dims->kv_heads < 1 || dims->heads % dims->kv_heads != 0 || dims->agents < 1 ||
         dims->max_pages < 1 || dims->pool_pages < 1)
         return QMM_ERR_INVALID_ARG;
-    const int64_t runs = (dims->max_pages + qmm::attn::kChunk - 1) / qmm::attn::kChunk;
-    *bytes = static_cast<int64_t>(dims->agents) * dims->kv_heads * runs * qmm::attn::kMaxQ * qmm::attn::kPart * 4;
+    *bytes = static_cast<int64_t>(dims->agents) * dims->kv_heads * qmm::attn::max_runs(dims) * qmm::attn::kMaxQ *
+             qmm::attn::kPart * 4;
     return QMM_OK;
 }
 
@@ -467,12 +529,22 @@ qmm_status qmm_attn_decode(const qmm_attn_dims* dims, const void* pool, const in
         (reinterpret_cast<uintptr_t>(workspace) & 15))
         return QMM_ERR_MISALIGNED;
     if (workspace_bytes < need) return QMM_ERR_SCRATCH_TOO_SMALL;
-    static bool configured = false;
-    if (!configured) {
+    // resident CTAs of the partial kernel on the current device (queried once per device)
+    static int cached_device = -1;
+    static int64_t slots = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return QMM_ERR_CUDA;
+    if (dev != cached_device) {
+        int sms = 0, per_sm = 0;
         if (cudaFuncSetAttribute(qmm::attn::attn_partial, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 qmm::attn::kSmem) != cudaSuccess)
+                                 qmm::attn::kSmem) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, qmm::attn::attn_partial, qmm::attn::kThreads,
+                                                          qmm::attn::kSmem) != cudaSuccess ||
+            per_sm < 1)
             return QMM_ERR_CUDA;
-        configured = true;
+        slots = static_cast<int64_t>(sms) * per_sm;
+        cached_device = dev;
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     qmm::attn::Params p = {};
@@ -487,12 +559,12 @@ qmm_status qmm_attn_decode(const qmm_attn_dims* dims, const void* pool, const in
     p.kv_heads = dims->kv_heads;
     p.group = dims->heads / dims->kv_heads;
     p.agents = dims->agents;
-    p.max_chunks = (dims->max_pages + qmm::attn::kChunk - 1) / qmm::attn::kChunk;
+    qmm::attn::plan_runs(dims, slots, &p.runs, &p.chunk);
     p.ws = static_cast<float*>(workspace);
     p.err = err_word;
     p.out = out;
     p.rows = rows;
-    const int64_t grid = static_cast<int64_t>(p.agents) * p.kv_heads * p.max_chunks;
+    const int64_t grid = static_cast<int64_t>(p.agents) * p.kv_heads * p.runs;
     qmm::attn::attn_partial<<<static_cast<unsigned>(grid), qmm::attn::kThreads, qmm::attn::kSmem, s>>>(p);
     if (cudaGetLastError() != cudaSuccess) return QMM_ERR_CUDA;
     const int64_t n = rows * dims->heads * qmm::attn::kD;

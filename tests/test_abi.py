@@ -120,7 +120,16 @@ def test_attention_arguments_without_device(lib):
     dims = Q.AttnDims(48, 8, 4, 400, 1600)
     nbytes = ctypes.c_int64()
     assert lib.qmm_attn_workspace_bytes(ctypes.byref(dims), ctypes.byref(nbytes)) == 0
-    assert nbytes.value == 4 * 8 * 13 * 32 * 130 * 4  # agents x KV heads x 32-page runs x queries
+    # agents x KV heads x runs x queries x (128 + 2) floats; runs are planned for at most 1024
+    # resident CTAs: at most 1024 // 32 = 32 runs, so runs of ceil(400 / 32) = 13 pages, of
+    # which 400 pages make 31
+    assert nbytes.value == 4 * 8 * 31 * 32 * 130 * 4
+    wide = Q.AttnDims(48, 8, 128, 20, 1600)  # 1024 (agent, KV head) pairs: one run each
+    assert lib.qmm_attn_workspace_bytes(ctypes.byref(wide), ctypes.byref(nbytes)) == 0
+    assert nbytes.value == 128 * 8 * 1 * 32 * 130 * 4
+    short = Q.AttnDims(48, 8, 1, 5, 1600)  # at most one run per page
+    assert lib.qmm_attn_workspace_bytes(ctypes.byref(short), ctypes.byref(nbytes)) == 0
+    assert nbytes.value == 1 * 8 * 5 * 32 * 130 * 4
     for bad in (Q.AttnDims(48, 7, 4, 400, 1600), Q.AttnDims(0, 8, 4, 400, 1600), Q.AttnDims(48, 8, 0, 400, 1600),
                 Q.AttnDims(48, 8, 4, 0, 1600), Q.AttnDims(48, 8, 4, 400, 0)):
         assert lib.qmm_attn_workspace_bytes(ctypes.byref(bad), ctypes.byref(nbytes)) == 1
