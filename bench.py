@@ -42,8 +42,8 @@ TRAFFIC_PER_UNIT = {
         "sha256": "43d77ce69d57d591d1ae8852fdc3a0d12692e52edc2c34708f401cbef0162db2",
         "bytes": 37194.0},
     2: {"source": "bit_weight_streaming_q4_gb300/csrc/qmm_b2.cu",
-        "sha256": "b03b6dc9ff5c28d4eb7fe303b5e4d0bff713329c59632724d179b3be4cda2729",
-        "bytes": 18581.6},
+        "sha256": "d2ecdf10f7db0088debcec47e1977b63443fd07e80b46c92245eb3ad23d1b5e7",
+        "bytes": 18582.0},
 }
 KERNEL_NAME = {1: "qmm::b1::stream_kernel<2>", 2: "qmm::b2::tc_kernel<16>"}
 HEADLINE_M = 12
@@ -351,6 +351,192 @@ def attention_line(torch, stream, hbm, parity, reps=50):
     return line
 
 
+def timed_calls(torch, stream, fn, calls, warmup=3):
+    """Seconds for `calls` calls of fn(i) on `stream` after `warmup` untimed ones."""
+    for i in range(warmup):
+        fn(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(calls):
+        fn(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3
+
+
+def graph_of(torch, stream, fn):
+    """fn() captured once into a CUDA graph on `stream` (calls short enough that the host's
+    launch cost would otherwise set the pace); returns a function that replays it on
+    `stream`."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+
+    def replay():
+        with torch.cuda.stream(stream):
+            g.replay()
+
+    replay.graph = g
+    return replay
+
+
+def copies_for(weight_bytes, floor=4):
+    """Handles of one matrix to rotate through so that every call reads weights from HBM:
+    at least `floor`, and at least 4 x L2 (129 MB) of weights in total."""
+    return max(floor, -(-4 * 129_000_000 // weight_bytes))
+
+
+def single_projection_line(torch, stream, hbm, parity, calls=400):
+    """The single projection 4096 x 4096 at M = 1 (9.4 MB, L2-sized): cold weight GB/s over
+    rotating copies (55 handles, 4 x L2) replayed from a CUDA graph, and the latency of one
+    isolated call (the median of 20 calls, each timed alone on an idle GPU)."""
+    from bit_weight_streaming_q4_gb300 import Qmm
+    mat = synth.SINGLE_PROJECTION
+    blocks = synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id)
+    dev = torch.from_numpy(blocks.reshape(-1)).cuda()
+    n = copies_for(mat.weight_bytes)
+    qs = [Qmm(dev, mat.n, mat.k, m_max=1) for _ in range(n)]
+    del dev
+    x = synth.x_f16(1, mat.k, seed=0, tensor_id=synth.X_ID_OFFSET + mat.tensor_id)
+    xd = torch.from_numpy(x.view(np.int16)).cuda().view(torch.float16)
+    yd = torch.empty((1, mat.n), dtype=torch.float32, device="cuda")
+    s = stream.cuda_stream
+
+    def sweep():
+        for q in qs:
+            q.run(xd, yd, 1, s)
+
+    replay = graph_of(torch, stream, sweep)
+    reps = max(1, calls // n)
+    t = timed_calls(torch, stream, lambda i: replay(), reps)
+    calls = reps * n
+    lat = []
+    for i in range(20):
+        lat.append(timed_calls(torch, stream, lambda j: qs[(i + j) % n].run(xd, yd, 1, s), 1, warmup=0) * 1e6)
+    us = t * 1e6 / calls
+    line = {"matrix": f"{mat.n} x {mat.k}", "m": 1, "backend": int(qs[0].info().backend), "copies": n,
+            "us_per_call": us, "weight_gbs": mat.weight_bytes / us / 1e3,
+            "frac_of_hbm_measured": mat.weight_bytes / us / 1e3 / hbm,
+            "single_call_us_median": statistics.median(lat)}
+    if parity:
+        import oracle
+        y_ref, s_ref = oracle.qmm(blocks, x)
+        ratio = np.abs(yd.cpu().numpy() - y_ref) / (2e-3 * s_ref + 1e-6)
+        line["parity"] = {"checked_outputs": int(ratio.size), "max_err_over_bound": float(ratio.max()),
+                          "pass": bool(ratio.max() <= 1.0)}
+    for q in qs:
+        q.close()
+    return line
+
+
+SWEEP_M = (1, 2, 4, 8, 12, 16, 32, 64)
+
+
+def m_sweep_line(torch, stream, hbm, calls=40):
+    """gate_up (5120 -> 34816) and down (17408 -> 5120) of layer 0 at every M of the sweep:
+    weight GB/s of the pair, run back to back on rotating copies (4 per handle set; the pair
+    is 150.4 MB), replayed from a CUDA graph.  Handles per set: m_max 8 (mma.sync) for M <= 8,
+    and 16, 32, 64 (tcgen05)."""
+    from bit_weight_streaming_q4_gb300 import Qmm
+    mats = [m for m in synth.layer_matrices(0) if m.name.endswith(("gate_up", "down"))]
+    pair_bytes = sum(m.weight_bytes for m in mats)
+    sets = {}
+    devs = [torch.from_numpy(synth.q4k_matrix(m.n, m.k, seed=0, tensor_id=m.tensor_id).reshape(-1)).cuda()
+            for m in mats]
+    for mm in (8, 16, 32, 64):
+        sets[mm] = [[Qmm(d, m.n, m.k, m_max=mm) for d, m in zip(devs, mats)] for _ in range(4)]
+    del devs
+    xs = [torch.from_numpy(synth.x_f16(64, m.k, seed=0, tensor_id=synth.X_ID_OFFSET + m.tensor_id)
+                           .view(np.int16)).cuda().view(torch.float16) for m in mats]
+    ys = [torch.empty((64, m.n), dtype=torch.float32, device="cuda") for m in mats]
+    s = stream.cuda_stream
+    out = {}
+    for m in SWEEP_M:
+        mm = 8 if m <= 8 else (16 if m <= 16 else (32 if m <= 32 else 64))
+        hs = sets[mm]
+
+        def four_pairs():
+            for pair in hs:
+                for q, x, y in zip(pair, xs, ys):
+                    q.run(x, y, m, s)
+
+        replay = graph_of(torch, stream, four_pairs)
+        reps = max(1, calls // 4)
+        t = timed_calls(torch, stream, lambda i: replay(), reps)
+        per = t / (4 * reps)
+        out[str(m)] = {"backend": int(hs[0][0].info().backend), "m_max": mm, "us_per_pair": per * 1e6,
+                       "weight_gbs": pair_bytes / per / 1e9, "frac_of_hbm_measured": pair_bytes / per / 1e9 / hbm,
+                       "tok_s": m / per}
+    for hs in sets.values():
+        for pair in hs:
+            for q in pair:
+                q.close()
+    return {"matrices": "layer 0 gate_up 5120->34816 + down 17408->5120 (150.4 MB), independent runs",
+            "by_m": out}
+
+
+PREFILL_M = 524
+
+
+def prefill_line(torch, stream, peaks, parity, steps=3, layers=synth.LAYERS):
+    """Chunked prefill: M = 524 rows (512 prompt + 12 decode) through the 64-layer set without
+    lm_head, activations N(0,1) with 1 % outliers x 20, handles with m_max = 524 (tcgen05, 128
+    rows per launch: every matrix streams its weights 5 times).  Tensor-bound: reported
+    against the measured bf16 tensor peak (fp16 runs at the same rate)."""
+    from bit_weight_streaming_q4_gb300 import Qmm
+    mats = synth.stack(layers, lm_head=False)
+    m = PREFILL_M
+    qs, xs, ys, flops, wb = [], [], [], 0, 0
+    for mat in mats:
+        dev = torch.from_numpy(synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id).reshape(-1)).cuda()
+        qs.append(Qmm(dev, mat.n, mat.k, m_max=m))
+        del dev
+        x = synth.x_f16(m, mat.k, seed=0, tensor_id=synth.X_ID_OFFSET + mat.tensor_id, outlier_p=0.01)
+        xs.append(torch.from_numpy(x.view(np.int16)).cuda().view(torch.float16))
+        ys.append(torch.empty((m, mat.n), dtype=torch.float32, device="cuda"))
+        flops += 2 * m * mat.n * mat.k
+        wb += mat.weight_bytes
+    s = stream.cuda_stream
+
+    def step(_):
+        for q, x, y in zip(qs, xs, ys):
+            q.run(x, y, m, s)
+
+    t = timed_calls(torch, stream, step, steps, warmup=1) / steps
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0)))
+    tflops = flops / t / 1e12
+    line = {"workload": f"chunked prefill M={m} (512 prompt + 12 decode rows): {layers} x {{qkv, o, gate_up, down}}, "
+                        f"no lm_head, x with 1% outliers x20",
+            "m": m, "backend": int(qs[0].info().backend), "launches_per_run": -(-m // 128),
+            "ms_per_step": t * 1e3, "tok_s": m / t, "weight_gbs": wb / t / 1e9, "tflops": tflops,
+            "tensor_peak_tflops": peak, "frac_of_tensor_peak": tflops / peak,
+            "note": "peak = measured bf16 sustained (fp16 has the same dense rate)"}
+    if parity:
+        import oracle
+        worst, checked = 0.0, 0
+        for i in (0, 1, 2, 3, len(mats) - 1):
+            mat = mats[i]
+            rows = np.array([0, mat.n // 2, mat.n - 1])
+            blocks = synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id, rows=rows)
+            x = xs[i].view(torch.int16).cpu().numpy().view(np.float16)
+            y_ref, s_ref = oracle.qmm(blocks, x)
+            got = ys[i].cpu().numpy()[:, rows]
+            ratio = np.abs(got - y_ref) / (2e-3 * s_ref + 1e-6)
+            worst = max(worst, float(ratio.max()))
+            checked += ratio.size
+        line["parity"] = {"checked_outputs": checked, "max_err_over_bound": worst, "pass": worst <= 1.0}
+    for q in qs:
+        q.close()
+    del xs, ys
+    torch.cuda.empty_cache()
+    return line
+
+
 def time_graph(torch, step, steps, warmup, stream):
     for _ in range(warmup):
         step.launch(stream.cuda_stream)
@@ -645,12 +831,16 @@ def run_ours(args, rank, world, local_rank):
     verify = None
     formats = None
     attention = None
+    single = sweep = prefill = None
     if not args.no_extra:
         verify = {str(m): lm_head_verify(stack, m, stream) for m in sorted({*EXTRA_M, HEADLINE_M})}
         # the other block formats of a mixed-quant file, on the lm_head shape at M = 12
         formats = {name: format_line(torch, f, code, HEADLINE_M, stream, not args.no_parity)
                    for name, f, code in (("Q6_K", synth.Q6_K, 1), ("Q8_0", synth.Q8_0, 2))}
         attention = attention_line(torch, stream, hbm, not args.no_parity)
+        single = single_projection_line(torch, stream, hbm, not args.no_parity)
+        sweep = m_sweep_line(torch, stream, hbm)
+        prefill = prefill_line(torch, stream, peaks, not args.no_parity, layers=args.layers)
 
     cpu = None
     if rank == 0:
@@ -675,6 +865,9 @@ def run_ours(args, rank, world, local_rank):
         "lm_head_verify": verify,
         "formats": formats,
         "attention": attention,
+        "single_projection": single,
+        "m_sweep": sweep,
+        "chunked_prefill": prefill,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": measured_traffic(stack.handles(HEADLINE_M)),
                      "kernel": f"{KERNEL_NAME[head_backend]} (one persistent launch per step)",

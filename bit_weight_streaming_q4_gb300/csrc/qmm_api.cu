@@ -184,7 +184,7 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
     const int cps = opt.ctas_per_sm ? opt.ctas_per_sm : 1;
     d.grid = static_cast<int32_t>(d.units < static_cast<int64_t>(sms) * cps ? d.units
                                                                            : static_cast<int64_t>(sms) * cps);
-    // split-K partial slot width: tcgen05, one column per row of x (up to 64); mma.sync, the
+    // split-K partial slot width: tcgen05, one column per row of x (up to 128); mma.sync, the
     // accumulator floats of a consumer thread (8 per 8-row group of x, up to 16)
     if (tc)
         h->ws_cols = qmm::b2::mp_for(opt.m_max < qmm::b2::kMaxM ? opt.m_max : qmm::b2::kMaxM);
@@ -200,18 +200,18 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
         return code;
     };
     if (cudaMalloc(&h->wq, h->wq_bytes) != cudaSuccess) return fail(QMM_ERR_OOM);
-    // split-K partial slots: tcgen05, two per CTA of rows x columns; mma.sync, one per CTA
-    // split-K partial slots, one per CTA: 128 rows x up to 64 columns (tcgen05), or the
+    // split-K partial slots, one per CTA: 128 rows x up to 128 columns (tcgen05), or the
     // accumulators of the 128 consumer threads (mma.sync)
     const size_t ws_bytes = static_cast<size_t>(d.grid) * (tc ? qmm::b2::kRows : qmm::b1::kConsumerThreads) *
                             h->ws_cols * sizeof(float);
     if (cudaMalloc(&h->ws, ws_bytes) != cudaSuccess) return fail(QMM_ERR_OOM);
     if (cudaMalloc(&h->tickets, d.tiles * sizeof(int)) != cudaSuccess) return fail(QMM_ERR_OOM);
     if (cudaMemsetAsync(h->tickets, 0, d.tiles * sizeof(int), s) != cudaSuccess) return fail(QMM_ERR_CUDA);
-    // argmax keys (one per row of a launch, at most 64) and their launch counter
-    constexpr size_t kAmaxBytes = 64 * sizeof(unsigned long long) + sizeof(unsigned long long);
+    // argmax keys (one per row of a launch, at most 128) and their launch counter
+    constexpr int kKeys = qmm::b2::kMaxM > qmm::b1::kMaxM ? qmm::b2::kMaxM : qmm::b1::kMaxM;
+    constexpr size_t kAmaxBytes = kKeys * sizeof(unsigned long long) + sizeof(unsigned long long);
     if (cudaMalloc(&h->amax_keys, kAmaxBytes) != cudaSuccess) return fail(QMM_ERR_OOM);
-    h->amax_count = reinterpret_cast<int*>(h->amax_keys + 64);
+    h->amax_count = reinterpret_cast<int*>(h->amax_keys + kKeys);
     if (cudaMemsetAsync(h->amax_keys, 0, kAmaxBytes, s) != cudaSuccess) return fail(QMM_ERR_CUDA);
     if (cudaHostAlloc(&h->err_host, sizeof(int), cudaHostAllocMapped) != cudaSuccess) return fail(QMM_ERR_OOM);
     *h->err_host = 0;

@@ -4,7 +4,8 @@
 // Qwen3.8-27B", section "How parallel decoding works"): every weight is read from memory
 // once per step and multiplied against all M stacked token rows while it is on chip.  The
 // tensor-core instruction costs the same for any N up to 64, so this backend serves runs of
-// more than 16 rows (up to 64 per launch).
+// more than 8 rows: up to 64 per launch for decode, and 128 per launch (twice the tensor-core
+// time per unit, half the weight passes) for longer runs such as a chunked prefill.
 //
 // One unit = 128 output rows x one super-block column (256 weights per row), 18432 bytes,
 // stored contiguously by repack():
@@ -81,11 +82,13 @@ constexpr int kTmemUsers = (kDqWarps + 2 + 4) * 32;  // dequant + MMA + epilogue
 // Ring depths (weight slots, activation slots) per block format and tile width, as deep as
 // shared memory allows; each a multiple of kGroups so that a slot always serves one group.
 constexpr int w_ring(int f, int mp) {
-    return f == QMM_FORMAT_Q4_K ? (mp == 16 ? 8 : mp == 32 ? 6 : 4) : f == QMM_FORMAT_Q6_K ? (mp == 64 ? 4 : 6) : 4;
+    return mp == 128 ? (f == QMM_FORMAT_Q4_K ? 4 : 2)
+                     : f == QMM_FORMAT_Q4_K ? (mp == 16 ? 8 : mp == 32 ? 6 : 4) : f == QMM_FORMAT_Q6_K ? (mp == 64 ? 4 : 6) : 4;
 }
 constexpr int x_ring(int f, int mp) {
-    return f == QMM_FORMAT_Q4_K ? (mp == 16 ? 8 : mp == 32 ? 6 : 4) : mp == 16 ? (f == QMM_FORMAT_Q6_K ? 6 : 8)
-                                                                   : mp == 32 ? 4 : 2;
+    return mp == 128 ? 2
+                     : f == QMM_FORMAT_Q4_K ? (mp == 16 ? 8 : mp == 32 ? 6 : 4) : mp == 16 ? (f == QMM_FORMAT_Q6_K ? 6 : 8)
+                                                                                    : mp == 32 ? 4 : 2;
 }
 
 template <int MP, int F>
@@ -96,13 +99,14 @@ struct Cfg {
     static constexpr int kXRing = x_ring(F, MP);
     static constexpr int kXBox = MP * 128;    // one 64-wide k box of x
     static constexpr int kXSlot = 4 * kXBox;  // x tile of one unit
-    static constexpr int kXsBytes = kMin ? MP * 32 : 0;  // the B tile of the -B_l step: [MP tokens][16 k]
+    static constexpr int kXsBytes = kMin ? MP * 32 : 0;  // the B tile of the -B_l step: [k half 2][MP tokens][8 fp16]
     // A buffers in tensor memory (unit j -> buffer j mod kNA): three where tensor memory has
     // room, so that a group can dequantise its next unit while the tensor core still reads
-    // the last two; two at MP = 64, where the accumulators take the room.  Accumulators:
-    // two buffers per issuer, so that the epilogue of a tile overlaps the next tile's MMAs.
-    static constexpr int kNA = MP == 64 ? 2 : 3;
-    static constexpr int kAccBufs = 2;
+    // the last two; two from MP = 64 on, where the accumulators take the room.  Accumulators:
+    // two buffers per issuer, so that the epilogue of a tile overlaps the next tile's MMAs,
+    // except at MP = 128 (one: a tile's MMAs wait for the epilogue of the tile before).
+    static constexpr int kNA = MP >= 64 ? 2 : 3;
+    static constexpr int kAccBufs = MP == 128 ? 1 : 2;
     static constexpr int kAccCol = kNA * kACols;  // accumulator (issuer e, buffer b) at + (e * kAccBufs + b) * MP
     static_assert(kAccCol + 2 * kAccBufs * MP <= kTmemCols, "tensor memory budget");
     static_assert(kTB % kNA == 0 && kTB % 2 == 0, "one barrier pair per unit mod kTB");
@@ -272,12 +276,14 @@ __device__ __forceinline__ void dq_unit_q6k(const uint8_t* u, int row, uint32_t 
     }
 }
 
-// Shared-memory descriptor of the -B_l step's A and B tiles ([rows][16 k] fp16): K-major, no
-// swizzle, core matrices of 8 rows x 16 bytes; the two k halves 128 bytes apart, 8-row groups
-// 256 bytes apart.
-__device__ __forceinline__ uint64_t smem_desc_k16(uint32_t saddr) {
-    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(128 >> 4) << 16) |
-           (static_cast<uint64_t>(256 >> 4) << 32) | (static_cast<uint64_t>(1) << 46);
+// Shared-memory descriptor of a -B_l step operand ([rows][16 k] fp16): K-major, no swizzle,
+// core matrices of 8 rows x 16 bytes, the two k halves `kstride` bytes apart and 8-row groups
+// `gstride` bytes apart.  The A tile is [group][k half][8 rows][16 B] (128, 256); the B tile
+// of MP tokens is [k half][token][16 B] (MP * 16, 128): the eight sub-block sums of a token
+// are one 16-byte row, written by the dequantisation warps.
+__device__ __forceinline__ uint64_t smem_desc_k16(uint32_t saddr, uint32_t kstride, uint32_t gstride) {
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(kstride >> 4) << 16) |
+           (static_cast<uint64_t>(gstride >> 4) << 32) | (static_cast<uint64_t>(1) << 46);
 }
 
 template <int MP, int F>
@@ -368,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the upper (always zero) k half of every -B_l step's B tile
         for (int i = tid; i < kXRing * MP * 4; i += kThreads) {
             const int slot = i / (MP * 4), r = (i / 4) % MP, e = i % 4;
-            *reinterpret_cast<uint32_t*>(xsum + slot * C::kXsBytes + (r >> 3) * 256 + 128 + (r & 7) * 16 + e * 4) = 0u;
+            *reinterpret_cast<uint32_t*>(xsum + slot * C::kXsBytes + MP * 16 + r * 16 + e * 4) = 0u;
         }
         // ... and of the A tiles of the -B_l step
         for (int i = tid; i < C::kNA * kRows * 4; i += kThreads) {
@@ -511,8 +517,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tc_mma_f16_ts(d_tmem, tbase + a * kACols + 8 * kk, bdesc, kIdesc, (!fresh || kk > 0) ? 1u : 0u);
                         }
                         if constexpr (C::kMin)
-                            tc_mma_f16_ss(d_tmem, smem_desc_k16(smem_u32(blt + a * kBlBytes)),
-                                          smem_desc_k16(smem_u32(xsum + xs * C::kXsBytes)), kIdesc, 1u);
+                            tc_mma_f16_ss(d_tmem, smem_desc_k16(smem_u32(blt + a * kBlBytes), 128, 256),
+                                          smem_desc_k16(smem_u32(xsum + xs * C::kXsBytes), MP * 16, 128), kIdesc, 1u);
                         tc_commit(&tempty[tb]);
                         tc_commit(&xempty[xs]);
                     }
@@ -551,10 +557,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         griddep_wait();  // y, the partial slots and the tickets may still be in use by the previous kernel
         int64_t seg = 0, jl = 0;  // jl: local index of the tile's first unit in the piece
         bool live = true;
-        // argmax launches: this warp's best key of token m in lane m % 32 (best0: m < 32, best1:
+        // argmax launches: this warp's best key of token m in lane m % 32 (best[m / 32]
         // m >= 32), over the final values of the rows it owns
         const bool amax = p.amax_keys != nullptr;
-        unsigned long long best0 = 0ull, best1 = 0ull;
+        unsigned long long best[(MP + 31) / 32];
+#pragma unroll
+        for (int i = 0; i < (MP + 31) / 32; ++i) best[i] = 0ull;
         // All four warps arrive on `ev` (each at most once per launch); lane 0 of warp
         // kEpiWarp0 then waits for the other three.  False if that wait gave up.
         auto gather = [&](uint64_t* ev) -> bool {
@@ -666,8 +674,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const uint32_t nf = static_cast<uint32_t>(n - lane + first);
                                 const unsigned long long key =
                                     (static_cast<unsigned long long>(mx) << 32) | (0xFFFFFFFFu - nf);
-                                if (m < 32) best0 = key > best0 ? key : best0;
-                                else best1 = key > best1 ? key : best1;
+#pragma unroll
+                                for (int bi = 0; bi < (MP + 31) / 32; ++bi)
+                                    if (bi == (m >> 5)) best[bi] = key > best[bi] ? key : best[bi];
                             }
                         }
                     } else {
@@ -692,8 +701,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (amax && live) {
             // the CTA's best key per token (over the four warps) goes out as one atomic
-            if (lane < MP) amax_sm[q * MP + lane] = best0;
-            if (MP > 32 && lane + 32 < MP) amax_sm[q * MP + lane + 32] = best1;
+#pragma unroll
+            for (int bi = 0; bi < (MP + 31) / 32; ++bi)
+                if (32 * bi + lane < MP) amax_sm[q * MP + 32 * bi + lane] = best[bi];
             const bool ok = gather(evamax);
             if (warp == kEpiWarp0) {
                 if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
@@ -773,7 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     __half sum = __hadd(__low2half(acc2), __high2half(acc2));
                     sum = __hmin(__hmax(sum, __ushort_as_half(0xFBFFu)), __ushort_as_half(0x7BFFu));
-                    *reinterpret_cast<__half*>(xst + (t >> 3) * 256 + (t & 7) * 16 + sb * 2) = sum;
+                    *reinterpret_cast<__half*>(xst + t * 16 + sb * 2) = sum;
                 }
 
                 // the A buffer was last read by the MMAs of unit j - kNA
@@ -990,7 +1000,8 @@ static cudaError_t set_attr_all() {
     cudaError_t e;
     if ((e = set_attr<16, F>()) != cudaSuccess) return e;
     if ((e = set_attr<32, F>()) != cudaSuccess) return e;
-    return set_attr<64, F>();
+    if ((e = set_attr<64, F>()) != cudaSuccess) return e;
+    return set_attr<128, F>();
 }
 
 cudaError_t configure() {
@@ -1015,7 +1026,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-int mp_for(int64_t m) { return m <= 16 ? 16 : m <= 32 ? 32 : 64; }
+int mp_for(int64_t m) { return m <= 16 ? 16 : m <= 32 ? 32 : m <= 64 ? 64 : 128; }
 
 cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, int* tickets, int64_t units,
                      int64_t n, int32_t kb, int32_t m) {
@@ -1065,7 +1076,8 @@ static cudaError_t launch_f(const MatDesc& single, const LaunchParams& p, int gr
     switch (mp_for(p.m)) {
         case 16: return launch_mp<16, F>(single, p, grid, s, pdl, cooperative);
         case 32: return launch_mp<32, F>(single, p, grid, s, pdl, cooperative);
-        default: return launch_mp<64, F>(single, p, grid, s, pdl, cooperative);
+        case 64: return launch_mp<64, F>(single, p, grid, s, pdl, cooperative);
+        default: return launch_mp<128, F>(single, p, grid, s, pdl, cooperative);
     }
 }
 

@@ -52,7 +52,7 @@ struct LaunchParams {
     int* err;                // sticky error word (mapped host memory)
     int64_t units;           // units of all matrices of the launch
     int32_t count;           // matrices in this launch
-    int32_t m;               // rows of this launch (1..16 mma.sync, 1..64 tcgen05)
+    int32_t m;               // rows of this launch (1..16 mma.sync, 1..128 tcgen05)
     int32_t ws_cols;         // floats per consumer thread in a partial slot
     int32_t pad;
     // Row-wise argmax instead of y (single-matrix launches only; null otherwise): the
@@ -104,10 +104,10 @@ constexpr int kRows = 128;
 constexpr int kUnitBytes = kRows * 144;  // Q4_K
 // bytes of one unit (128 rows x 256 weights) of a format
 __host__ __device__ constexpr int unit_bytes(int format) { return kRows * block_bytes(format) * (256 / block_weights(format)); }
-constexpr int kMaxM = 64;   // rows per launch
-int mp_for(int64_t m);      // tokens per launch tile: 16, 32 or 64
+constexpr int kMaxM = 128;  // rows per launch
+int mp_for(int64_t m);      // tokens per launch tile: 16, 32, 64 or 128
 cudaError_t repack(const uint8_t* src_dev, uint8_t* dst_dev, const Decomp& d, int format, cudaStream_t s);
-// Fill a matrix descriptor for a run of m rows (1..64) of x against the handle's weights.
+// Fill a matrix descriptor for a run of m rows (1..128) of x against the handle's weights.
 cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, int* tickets, int64_t units,
                      int64_t n, int32_t kb, int32_t m);
 // Launch over `p.count` matrices of one format (`single` when count == 1); p.ws_cols = mp_for(p.m).
@@ -153,6 +153,6 @@ struct qmm_handle_s {
     int* err_dev = nullptr;       // device view of the same word
     void* x_stage = nullptr;      // host_io staging
     float* y_stage = nullptr;
-    unsigned long long* amax_keys = nullptr;  // qmm_run_argmax: [64] keys, then the counter
+    unsigned long long* amax_keys = nullptr;  // qmm_run_argmax: [128] keys, then the counter
     int* amax_count = nullptr;
 };

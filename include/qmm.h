@@ -61,7 +61,7 @@ enum {
                                  m_max <= 8 -> MMA_SYNC (one n8 fragment per MMA, the
                                  faster stream there), else TCGEN05 */
     QMM_BACKEND_MMA_SYNC = 1, /* warp-level mma.sync m16n8k16, 16 rows per launch */
-    QMM_BACKEND_TCGEN05 = 2   /* tcgen05.mma with TMEM accumulators, 64 rows per launch */
+    QMM_BACKEND_TCGEN05 = 2   /* tcgen05.mma with TMEM accumulators, 128 rows per launch */
 };
 
 /*
