@@ -51,6 +51,7 @@ void free_handle(qmm_handle h) {
     cudaFree(h->x_stage);
     cudaFree(h->y_stage);
     cudaFree(h->amax_keys);
+    cudaFree(h->xsum);
     h->magic = 0;
     delete h;
 }
@@ -73,9 +74,11 @@ qmm_status launch_run(qmm_handle h, const void* x, int64_t m, float* y, cudaStre
         const __half* xc = reinterpret_cast<const __half*>(x) + r0 * K;
         float* yc = idx ? nullptr : y + r0 * N;
         const bool tc = h->backend == QMM_BACKEND_TCGEN05;
+        const bool pre = tc && qmm::b2::presum_for(mc, h->format);
         qmm::MatDesc mat;
         cudaError_t e = tc ? qmm::b2::make_mat(&mat, h->wq, xc, yc, h->tickets, h->d.units, N,
-                                               static_cast<int32_t>(h->d.kb), static_cast<int32_t>(mc))
+                                               static_cast<int32_t>(h->d.kb), static_cast<int32_t>(mc),
+                                               pre ? h->xsum : nullptr)
                            : qmm::b1::make_mat(&mat, h->wq, xc, yc, h->tickets, h->d.units, N,
                                                static_cast<int32_t>(h->d.kb), static_cast<int32_t>(mc));
         if (e == cudaSuccess) {
@@ -94,8 +97,12 @@ qmm_status launch_run(qmm_handle h, const void* x, int64_t m, float* y, cudaStre
                 p.amax_idx = idx + r0;
                 p.amax_val = val + r0;
             }
-            e = tc ? qmm::b2::launch(mat, p, h->d.grid, s, pdl, false, h->format)
-                   : qmm::b1::launch(mat, p, h->d.grid, s, pdl, false);
+            // the activation sums first, as a plain launch: that also keeps them from
+            // overwriting the sums the handle's previous launch may still be reading
+            if (pre) e = qmm::b2::presum(mat, p, static_cast<int32_t>(h->d.kb), s);
+            if (e == cudaSuccess)
+                e = tc ? qmm::b2::launch(mat, p, h->d.grid, s, pdl, false, h->format)
+                       : qmm::b1::launch(mat, p, h->d.grid, s, pdl, false);
         }
         if (e != cudaSuccess) return QMM_ERR_CUDA;
     }
@@ -213,6 +220,10 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
     if (cudaMalloc(&h->amax_keys, kAmaxBytes) != cudaSuccess) return fail(QMM_ERR_OOM);
     h->amax_count = reinterpret_cast<int*>(h->amax_keys + kKeys);
     if (cudaMemsetAsync(h->amax_keys, 0, kAmaxBytes, s) != cudaSuccess) return fail(QMM_ERR_CUDA);
+    // activation sums of launches of more than 64 rows (tcgen05 Q4_K)
+    if (tc && qmm::b2::presum_for(opt.m_max, opt.format) &&
+        cudaMalloc(&h->xsum, qmm::b2::presum_bytes(qmm::b2::kMaxM, d.kb)) != cudaSuccess)
+        return fail(QMM_ERR_OOM);
     if (cudaHostAlloc(&h->err_host, sizeof(int), cudaHostAllocMapped) != cudaSuccess) return fail(QMM_ERR_OOM);
     *h->err_host = 0;
     if (cudaHostGetDevicePointer(&h->err_dev, h->err_host, 0) != cudaSuccess) return fail(QMM_ERR_CUDA);
@@ -333,6 +344,9 @@ struct qmm_step_s {
     int32_t* first_mat = nullptr; // device, [grid]
     float* ws = nullptr;          // split-K partial slots, one per CTA
     bool tcgen05 = false;         // the backend of every handle of a persistent step
+    bool presum = false;          // ... whose activation sums come from a pre-pass
+    int32_t max_kb = 0;
+    __half* xsum = nullptr;       // device, the sums of every matrix
     int32_t format = QMM_FORMAT_Q4_K;  // ... and their block format
     int* err_host = nullptr;
     int* err_dev = nullptr;
@@ -347,6 +361,7 @@ static void free_step(qmm_step st) {
     cudaFree(st->mats);
     cudaFree(st->first_mat);
     cudaFree(st->ws);
+    cudaFree(st->xsum);
     if (st->err_host) cudaFreeHost(st->err_host);
     delete st;
 }
@@ -391,11 +406,23 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
         // boundary is split between two CTAs.
         std::vector<qmm::MatDesc> host(count);
         int64_t total = 0;
+        // activation sums of every matrix (launches of more than 64 rows), one pre-pass per launch
+        const bool pre = tc && qmm::b2::presum_for(m, handles[0]->format);
+        int64_t sum_bytes = 0;
+        int32_t max_kb = 0;
+        for (int32_t i = 0; i < count; ++i) {
+            sum_bytes += qmm::b2::presum_bytes(m, handles[i]->d.kb);
+            max_kb = handles[i]->d.kb > max_kb ? static_cast<int32_t>(handles[i]->d.kb) : max_kb;
+        }
+        if (pre && cudaMalloc(&st->xsum, sum_bytes) != cudaSuccess) rc = QMM_ERR_OOM;
+        int64_t sum_off = 0;
         for (int32_t i = 0; i < count && rc == QMM_OK; ++i) {
             const qmm_handle h = handles[i];
+            __half* xsi = pre ? st->xsum + sum_off / 2 : nullptr;
+            sum_off += qmm::b2::presum_bytes(m, h->d.kb);
             const cudaError_t me =
                 tc ? qmm::b2::make_mat(&host[i], h->wq, xs[i], ys[i], h->tickets, h->d.units, h->d.n,
-                                       static_cast<int32_t>(h->d.kb), static_cast<int32_t>(m))
+                                       static_cast<int32_t>(h->d.kb), static_cast<int32_t>(m), xsi)
                    : qmm::b1::make_mat(&host[i], h->wq, xs[i], ys[i], h->tickets, h->d.units, h->d.n,
                                        static_cast<int32_t>(h->d.kb), static_cast<int32_t>(m));
             if (me != cudaSuccess) rc = QMM_ERR_CUDA;
@@ -430,6 +457,8 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
         }
         if (rc == QMM_OK) {
             st->tcgen05 = tc;
+            st->presum = pre;
+            st->max_kb = max_kb;
             st->format = handles[0]->format;
             st->grid = grid;
             st->params.mats = st->mats;
@@ -479,8 +508,10 @@ qmm_status qmm_step_launch(qmm_step s, void* stream) {
     if (s->mats) {
         if (*reinterpret_cast<volatile int*>(s->err_host)) return QMM_ERR_DEVICE_TIMEOUT;
         const qmm::MatDesc unused = {};
-        const cudaError_t e = s->tcgen05 ? qmm::b2::launch(unused, s->params, s->grid, cs, true, true, s->format)
-                                         : qmm::b1::launch(unused, s->params, s->grid, cs, true, true);
+        cudaError_t e = s->presum ? qmm::b2::presum(unused, s->params, s->max_kb, cs) : cudaSuccess;
+        if (e == cudaSuccess)
+            e = s->tcgen05 ? qmm::b2::launch(unused, s->params, s->grid, cs, true, true, s->format)
+                           : qmm::b1::launch(unused, s->params, s->grid, cs, true, true);
         return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
     }
     return cudaGraphLaunch(s->exec, cs) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;

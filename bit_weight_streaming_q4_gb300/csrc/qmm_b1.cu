@@ -753,6 +753,8 @@ cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, i
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
+    out->xsrc = nullptr;
+    out->xs = nullptr;
     out->wq = wq;
     out->y = y;
     out->tickets = tickets;

@@ -95,6 +95,11 @@ template <int MP, int F>
 struct Cfg {
     static constexpr int kUnitBytes = unit_bytes(F);
     static constexpr bool kMin = F == QMM_FORMAT_Q4_K;  // the format has a min term (the -B_l step)
+    // MP = 128: shared memory holds two x tiles only, so the MMA issuers wait for a unit's x
+    // tile themselves and the dequantisation groups never touch x; the activation sums of the
+    // -B_l step come from the pre-pass (presum_for) with the tile
+    static constexpr bool kIssuerWaitsX = MP == 128;
+    static constexpr bool kPre = kMin && kIssuerWaitsX;
     static constexpr int kWRing = w_ring(F, MP);
     static constexpr int kXRing = x_ring(F, MP);
     static constexpr int kXBox = MP * 128;    // one 64-wide k box of x
@@ -432,6 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int64_t issued = 0;
             int cur = -1, kbn = 1, kb = 0;
             const void* xmap = nullptr;
+            const void* smap = nullptr;
             bool ok = true;
             griddep_wait();  // activations may be written by the previous kernel
             while (xc.i < count) {
@@ -444,13 +450,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const MatDesc& M = mat(xc.i);
                     cur = xc.i;
                     xmap = &M.xmap;
+                    smap = &M.smap;
                     kbn = M.kb;
                     kb = static_cast<int>(xc.j % kbn);
                 }
-                mbar_arrive_expect_tx(&xfull[xs], C::kXSlot);
+                mbar_arrive_expect_tx(&xfull[xs], C::kXSlot + (C::kPre ? MP * 16 : 0));
 #pragma unroll
                 for (int b = 0; b < 4; ++b)
                     tma_load_2d(xring + xs * C::kXSlot + b * C::kXBox, xmap, kb * 256 + 64 * b, 0, &xfull[xs]);
+                // the unit's activation sums, tokens 0 .. MP-1 of column kb (zero past m)
+                if constexpr (C::kPre) tma_load_3d(xsum + xs * C::kXsBytes, smap, 0, 0, kb, &xfull[xs]);
                 kb = (kb + 1 == kbn) ? 0 : kb + 1;
                 ++issued;
                 next(xc);
@@ -505,6 +514,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int a = static_cast<int>(j % C::kNA);
                     const int tb = static_cast<int>(j % kTB);
                     if (!warp_wait(&tfull[tb], (j / kTB) & 1, flags)) {
+                        live = false;
+                        break;
+                    }
+                    if (C::kIssuerWaitsX && !warp_wait(&xfull[xs], (j / kXRing) & 1, flags)) {
                         live = false;
                         break;
                     }
@@ -765,13 +778,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // activations of token t in sub-block s (fp16, clamped); MP * 8 of them, shared
                 // out over the group's 128 threads.  Formed before the wait for the A buffer: the
                 // sums' slot was last read by the MMAs of unit j - kXRing, which finished before
-                // the slot was refilled.
+                // the slot was refilled.  At MP = 128 they come from the pre-pass with the x tile
+                // (the same fp16 additions in the same order, so a row's bits do not depend on
+                // MP), and the group does not wait for the tile at all.
                 const int xs = static_cast<int>(j % kXRing);
-                if (!warp_wait(&xfull[xs], (j / kXRing) & 1, flags)) break;
+                if (!C::kIssuerWaitsX && !warp_wait(&xfull[xs], (j / kXRing) & 1, flags)) break;
                 const uint8_t* xt = xring + xs * C::kXSlot;
                 uint8_t* xst = xsum + xs * C::kXsBytes;
     #pragma unroll
-                for (int pi = row; pi < MP * 8; pi += kRows) {
+                for (int pi = row; pi < (C::kPre ? 0 : MP * 8); pi += kRows) {
                     const int t = pi % MP, sb = pi / MP;
                     const uint8_t* rowp = xt + (sb >> 1) * C::kXBox + t * 128;
                     __half2 acc2 = __float2half2_rn(0.f);
@@ -811,9 +826,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     make_uint4(ps[0].nbl, ps[1].nbl, ps[2].nbl, ps[3].nbl);
             } else {
                 // no sums to form: the wait on the activation tile keeps the MMAs of this unit
-                // after its arrival, as the Q4_K path's sums do
+                // after its arrival, as the Q4_K path's sums do (at MP = 128 the issuers wait)
                 const int xs = static_cast<int>(j % kXRing);
-                if (!warp_wait(&xfull[xs], (j / kXRing) & 1, flags)) break;
+                if (!C::kIssuerWaitsX && !warp_wait(&xfull[xs], (j / kXRing) & 1, flags)) break;
                 if (j >= C::kNA && !warp_wait(&tempty[(j - C::kNA) % kTB], ((j - C::kNA) / kTB) & 1, flags)) break;
                 tc_fence_after();
                 const uint32_t tcol = tlane + a * kACols;
@@ -1029,7 +1044,7 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 int mp_for(int64_t m) { return m <= 16 ? 16 : m <= 32 ? 32 : m <= 64 ? 64 : 128; }
 
 cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, int* tickets, int64_t units,
-                     int64_t n, int32_t kb, int32_t m) {
+                     int64_t n, int32_t kb, int32_t m, __half* xs) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     const int64_t k = static_cast<int64_t>(kb) * 256;
@@ -1041,6 +1056,21 @@ cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, i
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
+    out->xsrc = static_cast<const __half*>(x);
+    out->xs = xs;
+    if (xs) {
+        // the activation sums [kb][m][8 sub-blocks] fp16: box 8 x MP x 1, rows past m read as zero
+        const cuuint64_t sdim[3] = {8, static_cast<cuuint64_t>(m), static_cast<cuuint64_t>(kb)};
+        const cuuint64_t sstride[2] = {16, static_cast<cuuint64_t>(m) * 16};
+        const cuuint32_t sbox[3] = {8, static_cast<cuuint32_t>(mp_for(m)), 1};
+        const cuuint32_t sestr[3] = {1, 1, 1};
+        if (enc(&out->smap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, xs, sdim, sstride, sbox, sestr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    } else {
+        memset(&out->smap, 0, sizeof(out->smap));
+    }
     out->wq = wq;
     out->y = y;
     out->tickets = tickets;
@@ -1050,6 +1080,40 @@ cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, i
     out->kb = kb;
     out->pad = 0;
     return cudaSuccess;
+}
+
+// One thread per (super-block column kb, token t) of a matrix (blockIdx.y): the eight sums of
+// 32 activations of x[t][256 kb ..], with exactly the fp16 additions, in the same order, that
+// the kernel's dequantisation warps make from the x tile at MP <= 64.
+__global__ void __launch_bounds__(256) presum_kernel(const __grid_constant__ MatDesc single, const LaunchParams p) {
+    const MatDesc& M = p.count == 1 ? single : p.mats[blockIdx.y];
+    const int m = p.m;
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= static_cast<int64_t>(M.kb) * m) return;
+    const int kb = static_cast<int>(idx / m), t = static_cast<int>(idx % m);
+    const uint4* src = reinterpret_cast<const uint4*>(M.xsrc + (static_cast<int64_t>(t) * M.kb + kb) * 256);
+    __half sums[8];
+#pragma unroll
+    for (int sb = 0; sb < 8; ++sb) {
+        __half2 acc2 = __float2half2_rn(0.f);
+#pragma unroll
+        for (int cc4 = 0; cc4 < 4; ++cc4) {
+            const uint4 v = src[sb * 4 + cc4];  // activations 32 sb + 8 cc4 .. + 7
+            acc2 = __hadd2(acc2, __hadd2(__hadd2(as_h2(v.x), as_h2(v.y)), __hadd2(as_h2(v.z), as_h2(v.w))));
+        }
+        const __half sum = __hadd(__low2half(acc2), __high2half(acc2));
+        sums[sb] = __hmin(__hmax(sum, __ushort_as_half(0xFBFFu)), __ushort_as_half(0x7BFFu));
+    }
+    *reinterpret_cast<uint4*>(M.xs + (static_cast<int64_t>(kb) * m + t) * 8) =
+        make_uint4(as_u32(__halves2half2(sums[0], sums[1])), as_u32(__halves2half2(sums[2], sums[3])),
+                   as_u32(__halves2half2(sums[4], sums[5])), as_u32(__halves2half2(sums[6], sums[7])));
+}
+
+cudaError_t presum(const MatDesc& single, const LaunchParams& p, int32_t max_kb, cudaStream_t s) {
+    const int64_t n = static_cast<int64_t>(max_kb) * p.m;
+    const dim3 grid(static_cast<unsigned>((n + 255) / 256), static_cast<unsigned>(p.count));
+    presum_kernel<<<grid, 256, 0, s>>>(single, p);
+    return cudaGetLastError();
 }
 
 template <int MP, int F>

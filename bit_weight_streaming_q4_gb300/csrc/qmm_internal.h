@@ -35,6 +35,9 @@ inline int64_t piece_of(int64_t u, int64_t units, int64_t grid) {
 // them in device memory (the tensor map needs 64-byte alignment).
 struct alignas(128) MatDesc {
     CUtensorMap xmap;      // activations [m, k] fp16, 128-byte swizzle: box 64 x 8 (mma.sync) or 64 x MP (tcgen05)
+    CUtensorMap smap;      // tcgen05 Q4_K launches of MP = 128: the activation sums [kb][m][8] fp16, box 8 x 128 x 1
+    const __half* xsrc;    // ... the activations they are formed from ([m, k], row stride k)
+    __half* xs;            // ... and where the pre-pass writes them
     const uint8_t* wq;     // repacked units
     float* y;              // [m, n] fp32
     int* tickets;          // [tiles]: partials published for the tile; zero between runs
@@ -107,13 +110,27 @@ __host__ __device__ constexpr int unit_bytes(int format) { return kRows * block_
 constexpr int kMaxM = 128;  // rows per launch
 int mp_for(int64_t m);      // tokens per launch tile: 16, 32, 64 or 128
 cudaError_t repack(const uint8_t* src_dev, uint8_t* dst_dev, const Decomp& d, int format, cudaStream_t s);
-// Fill a matrix descriptor for a run of m rows (1..128) of x against the handle's weights.
+// Launches whose activation sums (the per-sub-block sums of x that the -B_l step needs) come
+// from a pre-pass kernel instead of being formed by the dequantisation warps from each unit's
+// x tile: Q4_K at more than 64 rows (MP = 128).  At that width shared memory holds only two
+// x tiles, and a tile's L2 round trip would otherwise sit between one unit's MMAs and the
+// dequantisation of the unit two places on.
+inline bool presum_for(int64_t m, int format) { return format == QMM_FORMAT_Q4_K && m > 64; }
+// Bytes of the activation sums of a launch of m rows of a matrix of kb super-block columns.
+inline int64_t presum_bytes(int64_t m, int64_t kb) { return kb * m * 16; }
+// Fill a matrix descriptor for a run of m rows (1..128) of x against the handle's weights;
+// xs (presum_bytes(m, kb) bytes, 16-byte aligned) receives the activation sums of launches
+// with presum_for(m, format), and is null otherwise.
 cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, int* tickets, int64_t units,
-                     int64_t n, int32_t kb, int32_t m);
+                     int64_t n, int32_t kb, int32_t m, __half* xs);
 // Launch over `p.count` matrices of one format (`single` when count == 1); p.ws_cols = mp_for(p.m).
 cudaError_t launch(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl, bool cooperative,
                    int format);
 cudaError_t configure();
+// The pre-pass of a launch with presum_for(p.m, format): the activation sums of every matrix
+// of the launch (`single` when p.count == 1, p.mats otherwise; max_kb the largest kb), issued
+// in stream order before the launch as a plain (not programmatic) launch.
+cudaError_t presum(const MatDesc& single, const LaunchParams& p, int32_t max_kb, cudaStream_t s);
 }  // namespace b2
 
 // Backend 1: warp-level mma.sync streaming kernel.
@@ -154,5 +171,6 @@ struct qmm_handle_s {
     void* x_stage = nullptr;      // host_io staging
     float* y_stage = nullptr;
     unsigned long long* amax_keys = nullptr;  // qmm_run_argmax: [128] keys, then the counter
+    __half* xsum = nullptr;       // activation sums of one launch of up to 128 rows (tcgen05 Q4_K, m_max > 64)
     int* amax_count = nullptr;
 };
