@@ -321,7 +321,7 @@ def attention_line(torch, stream, hbm, parity, reps=50):
     out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
     s = stream.cuda_stream
     dims = AttnDims(w.heads, w.kv_heads, table.shape[0], table.shape[1], total)
-    ws = torch.empty(attn_workspace_bytes(dims), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(attn_workspace_bytes(dims, len(ra)), dtype=torch.uint8, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     for _ in range(3):
         attn_decode(pool_d, table_d, ar_d, rl_d, q_d, out, w.kv_heads, s, ws, err)

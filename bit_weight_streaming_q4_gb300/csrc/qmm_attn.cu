@@ -47,7 +47,7 @@ constexpr int kMaxQ = 32;   // queries per item: rows of the agent x heads of th
 constexpr int kSlotCap = 1024;  // upper bound on the resident CTAs a launch is planned for
 constexpr int kStages = 4;  // pages in flight per CTA
 constexpr int kThreads = 128;
-constexpr int kPart = kD + 2;  // floats per query of an item's partial: o[128], m, l
+constexpr int kPart = kD + 4;  // floats per query of an item's partial: o[128], m, l, 2 unused (16-byte rows)
 constexpr float kNegBig = -1e30f;
 constexpr int kPS = kPT + 4;  // halves per row of the probability tile (136 bytes: conflict-free 8-byte reads)
 
@@ -68,7 +68,8 @@ struct Params {
     int32_t heads, kv_heads, group;
     int32_t agents;
     int32_t runs, chunk;        // runs of pages per (agent, KV head), pages per run
-    float* ws;                  // [agent][kv head][run][kMaxQ][kPart]
+    int32_t max_qt;             // query tiles of kMaxQ per (agent, KV head) the workspace holds
+    float* ws;                  // [agent][kv head][run][query tile][kMaxQ][kPart]
     int* err;                   // sticky error word
     float* out;                 // [rows][heads][128]
     int64_t rows;
@@ -80,7 +81,7 @@ __device__ __forceinline__ int agent_runs(const Params& p, int a, int& r0, int& 
     r0 = p.agent_rows[a];
     nr = p.agent_rows[a + 1] - r0;
     if (nr <= 0) return 0;
-    if (r0 < 0 || r0 + nr > p.rows || nr * p.group > kMaxQ) return -1;
+    if (r0 < 0 || r0 + nr > p.rows || nr * p.group > p.max_qt * kMaxQ) return -1;
     int maxlen = 0;
     for (int r = r0; r < r0 + nr; ++r) {
         const int len = p.row_len[r];
@@ -148,7 +149,10 @@ __global__ void __launch_bounds__(kThreads, 3) attn_partial(const Params p) {
         it.page0 = run * p.chunk;
         it.npages = pages - it.page0 < p.chunk ? pages - it.page0 : p.chunk;
     }
-    const int nq = it.nr * p.group;
+    // this CTA's query tile: the item's queries q0 .. q0 + nq - 1 (blockIdx.y = tile)
+    const int q0 = static_cast<int>(blockIdx.y) * kMaxQ;
+    const int nq = it.nr * p.group - q0 < kMaxQ ? it.nr * p.group - q0 : kMaxQ;
+    if (nq <= 0) return;
     const int nnt = (nq + 7) >> 3;  // n8 tiles of queries (1 .. 4)
     const float c2 = 1.4426950408889634f * 0.08838834764831845f;  // log2(e) / sqrt(128)
 
@@ -157,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 3) attn_partial(const Params p) {
         flags[0] = 0;
         fence_mbar_init();
     }
-    if (tid < kMaxQ) qlen_sm[tid] = tid < nq ? p.row_len[it.r0 + tid / p.group] : 0;
+    if (tid < kMaxQ) qlen_sm[tid] = tid < nq ? p.row_len[it.r0 + (q0 + tid) / p.group] : 0;
     __syncthreads();
 
     // the record of logical page i of the item, or null (and the error word) if the page
@@ -185,8 +189,9 @@ __global__ void __launch_bounds__(kThreads, 3) attn_partial(const Params p) {
         for (int i = 0; i < kStages - 1 && i < it.npages; ++i) issue(i);
 
     // Both products run with tokens or dims as the MMA's M and the item's queries as N (n8
-    // tiles nt: queries 8 nt .. 8 nt + 7; query qi is head g * group + qi % group of row
-    // r0 + qi / group, and queries past nq are zero).
+    // tiles nt: queries 8 nt .. 8 nt + 7 of the CTA's tile; its query qi is the item's query
+    // qa = q0 + qi, head g * group + qa % group of row r0 + qa / group, and queries past nq
+    // are zero).
     //
     // S^T = K . Q^T: warp w takes tokens 16w .. 16w + 15 of the page.  The dims of k-step
     // ks = 2 blk + k2 are assigned so that every thread's eight dims of a 32-dim block are
@@ -197,8 +202,10 @@ __global__ void __launch_bounds__(kThreads, 3) attn_partial(const Params p) {
     for (int nt = 0; nt < 4; ++nt) {
         const int qi = 8 * nt + g8;
         const __half* qrow = nullptr;
-        if (qi < nq)
-            qrow = p.q + (static_cast<int64_t>(it.r0 + qi / p.group) * p.heads + it.g * p.group + qi % p.group) * kD;
+        if (qi < nq) {
+            const int qa = q0 + qi;  // the item's query
+            qrow = p.q + (static_cast<int64_t>(it.r0 + qa / p.group) * p.heads + it.g * p.group + qa % p.group) * kD;
+        }
 #pragma unroll
         for (int blk = 0; blk < 4; ++blk) {
             const uint4 v = qrow ? *reinterpret_cast<const uint4*>(qrow + 32 * blk + 8 * t4) : make_uint4(0u, 0u, 0u, 0u);
@@ -418,7 +425,8 @@ __global__ void __launch_bounds__(kThreads, 3) attn_partial(const Params p) {
             }
         }
     __syncthreads();
-    float* part = p.ws + static_cast<int64_t>(blockIdx.x) * kMaxQ * kPart;  // slot (agent, g, run)
+    // slot (agent, g, run, tile)
+    float* part = p.ws + (static_cast<int64_t>(blockIdx.x) * p.max_qt + blockIdx.y) * kMaxQ * kPart;
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
@@ -440,13 +448,15 @@ __global__ void __launch_bounds__(kThreads, 3) attn_partial(const Params p) {
         }
 }
 
-// One thread per output element: the items of (agent, KV head) combined in item order.
+// One warp per (row, head): the partials of its (agent, KV head, query tile) merged in run
+// order; lane l writes dims 4l .. 4l + 3.
 __global__ void attn_combine(const Params p) {
-    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (idx >= p.rows * p.heads * kD) return;
-    const int d = static_cast<int>(idx % kD);
-    const int h = static_cast<int>((idx / kD) % p.heads);
-    const int64_t r = idx / (static_cast<int64_t>(kD) * p.heads);
+    const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (w >= p.rows * p.heads) return;
+    const int h = static_cast<int>(w % p.heads);
+    const int64_t r = w / p.heads;
+    float4* outp = reinterpret_cast<float4*>(p.out + w * kD);
     // the agent holding row r (agent_rows is non-decreasing)
     int lo = 0, hi = p.agents;
     while (hi - lo > 1) {
@@ -458,26 +468,48 @@ __global__ void attn_combine(const Params p) {
     int r0, nr;
     const int n = agent_runs(p, a, r0, nr);
     if (n <= 0 || r < r0 || r >= r0 + nr) {  // a row of no agent, or an agent the kernels refused
-        if (d == 0 && h == 0) atomicOr(p.err, 4);
-        p.out[idx] = 0.f;
+        if (lane == 0 && h == 0) atomicOr(p.err, 4);
+        outp[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
         return;
     }
     const int g = h / p.group;
-    const int qi = static_cast<int>(r - r0) * p.group + h % p.group;
+    const int qa = static_cast<int>(r - r0) * p.group + h % p.group;  // the item's query
+    const int qt = qa / kMaxQ, qi = qa % kMaxQ;                           // its tile, its slot there
     const int64_t first = (static_cast<int64_t>(a) * p.kv_heads + g) * p.runs;
     const float c2 = 1.4426950408889634f * 0.08838834764831845f;
+    auto slot = [&](int c) { return p.ws + (((first + c) * p.max_qt + qt) * kMaxQ + qi) * kPart; };
     float m = kNegBig;
-    for (int c = 0; c < n; ++c) m = fmaxf(m, p.ws[((first + c) * kMaxQ + qi) * kPart + kD]);
-    float l = 0.f, o = 0.f;
-    for (int c = 0; c < n; ++c) {
-        const float* pq = p.ws + ((first + c) * kMaxQ + qi) * kPart;
-        const float mc = pq[kD];
-        if (mc == kNegBig) continue;  // no attended token in this item
-        const float w = exp2f((mc - m) * c2);
-        l += pq[kD + 1] * w;
-        o += pq[d] * w;
+    for (int c = lane; c < n; c += 32) m = fmaxf(m, slot(c)[kD]);
+#pragma unroll
+    for (int k = 16; k >= 1; k >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, k));
+    // runs in groups of 32: lane j weighs run c0 + j (0 for a run without attended tokens),
+    // then the warp adds the group's runs in order, with independent loads of their o rows
+    float l = 0.f;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < n; c0 += 32) {
+        const int c = c0 + lane;
+        float wt = 0.f, lw = 0.f;
+        if (c < n) {
+            const float* pq = slot(c);
+            const float mc = pq[kD];
+            if (mc != kNegBig) {
+                wt = exp2f((mc - m) * c2);
+                lw = pq[kD + 1] * wt;
+            }
+        }
+        const int cn = n - c0 < 32 ? n - c0 : 32;
+#pragma unroll 4
+        for (int j = 0; j < cn; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, wt, j);
+            l += __shfl_sync(0xffffffffu, lw, j);
+            const float4 v = reinterpret_cast<const float4*>(slot(c0 + j))[lane];
+            o.x = fmaf(v.x, wj, o.x);
+            o.y = fmaf(v.y, wj, o.y);
+            o.z = fmaf(v.z, wj, o.z);
+            o.w = fmaf(v.w, wj, o.w);
+        }
     }
-    p.out[idx] = o / l;
+    outp[lane] = make_float4(o.x / l, o.y / l, o.z / l, o.w / l);
 }
 
 constexpr int kSmem = kStages * kRec + kMaxQ * kPS * 2 + 2 * 4 * kMaxQ * 4 + kStages * 8 + 16 + kMaxQ * 4;
@@ -502,31 +534,37 @@ int64_t max_runs(const qmm_attn_dims* dims) {
     return runs;
 }
 
+// Query tiles of kMaxQ an agent of a call with `rows` rows can need: all rows in one agent.
+int32_t max_tiles(const qmm_attn_dims* dims, int64_t rows) {
+    const int64_t q = rows * (dims->heads / dims->kv_heads);
+    return static_cast<int32_t>((q + kMaxQ - 1) / kMaxQ);
+}
+
 }  // namespace attn
 }  // namespace qmm
 
 extern "C" {
 
-qmm_status qmm_attn_workspace_bytes(const qmm_attn_dims* dims, int64_t* bytes) {
+qmm_status qmm_attn_workspace_bytes(const qmm_attn_dims* dims, int64_t rows, int64_t* bytes) {
     if (!dims || !bytes) return QMM_ERR_INVALID_ARG;
     if (dims->heads < 1 || dims->kv_heads < 1 || dims->heads % dims->kv_heads != 0 || dims->agents < 1 ||
-        dims->max_pages < 1 || dims->pool_pages < 1)
+        dims->max_pages < 1 || dims->pool_pages < 1 || rows < 1 || rows > (int64_t{1} << 24))
         return QMM_ERR_INVALID_ARG;
-    *bytes = static_cast<int64_t>(dims->agents) * dims->kv_heads * qmm::attn::max_runs(dims) * qmm::attn::kMaxQ *
-             qmm::attn::kPart * 4;
+    *bytes = static_cast<int64_t>(dims->agents) * dims->kv_heads * qmm::attn::max_runs(dims) *
+             qmm::attn::max_tiles(dims, rows) * qmm::attn::kMaxQ * qmm::attn::kPart * 4;
     return QMM_OK;
 }
 
 qmm_status qmm_attn_decode(const qmm_attn_dims* dims, const void* pool, const int32_t* page_table,
                            const int32_t* agent_rows, const int32_t* row_len, const void* q, int64_t rows, float* out,
                            void* workspace, int64_t workspace_bytes, int* err_word, void* stream) {
-    int64_t need = 0;
-    qmm_status st = qmm_attn_workspace_bytes(dims, &need);
-    if (st != QMM_OK) return st;
     if (!pool || !page_table || !agent_rows || !row_len || !q || !out || !workspace || !err_word || rows < 1)
         return QMM_ERR_INVALID_ARG;
+    int64_t need = 0;
+    qmm_status st = qmm_attn_workspace_bytes(dims, rows, &need);
+    if (st != QMM_OK) return st;
     if ((reinterpret_cast<uintptr_t>(pool) & 15) || (reinterpret_cast<uintptr_t>(q) & 15) ||
-        (reinterpret_cast<uintptr_t>(workspace) & 15))
+        (reinterpret_cast<uintptr_t>(out) & 15) || (reinterpret_cast<uintptr_t>(workspace) & 15))
         return QMM_ERR_MISALIGNED;
     if (workspace_bytes < need) return QMM_ERR_SCRATCH_TOO_SMALL;
     // resident CTAs of the partial kernel on the current device (queried once per device)
@@ -560,14 +598,17 @@ qmm_status qmm_attn_decode(const qmm_attn_dims* dims, const void* pool, const in
     p.group = dims->heads / dims->kv_heads;
     p.agents = dims->agents;
     qmm::attn::plan_runs(dims, slots, &p.runs, &p.chunk);
+    p.max_qt = qmm::attn::max_tiles(dims, rows);
     p.ws = static_cast<float*>(workspace);
     p.err = err_word;
     p.out = out;
     p.rows = rows;
-    const int64_t grid = static_cast<int64_t>(p.agents) * p.kv_heads * p.runs;
-    qmm::attn::attn_partial<<<static_cast<unsigned>(grid), qmm::attn::kThreads, qmm::attn::kSmem, s>>>(p);
+    // CTAs (agent, KV head, run) x query tile; the tiles past an agent's queries return at once
+    const dim3 grid(static_cast<unsigned>(static_cast<int64_t>(p.agents) * p.kv_heads * p.runs),
+                    static_cast<unsigned>(p.max_qt));
+    qmm::attn::attn_partial<<<grid, qmm::attn::kThreads, qmm::attn::kSmem, s>>>(p);
     if (cudaGetLastError() != cudaSuccess) return QMM_ERR_CUDA;
-    const int64_t n = rows * dims->heads * qmm::attn::kD;
+    const int64_t n = rows * dims->heads * 32;  // one warp per (row, head)
     qmm::attn::attn_combine<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(p);
     if (cudaGetLastError() != cudaSuccess) return QMM_ERR_CUDA;
     return QMM_OK;

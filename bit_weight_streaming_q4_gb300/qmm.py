@@ -87,7 +87,7 @@ def load(path: str = LIB_PATH):
         "qmm_step_launch": (ctypes.c_int, [vp, vp]),
         "qmm_step_destroy": (ctypes.c_int, [vp]),
         "qmm_run_noalloc": (ctypes.c_int, [vp, i64, i64, vp, i64, vp, vp]),
-        "qmm_attn_workspace_bytes": (ctypes.c_int, [ctypes.POINTER(AttnDims), ctypes.POINTER(i64)]),
+        "qmm_attn_workspace_bytes": (ctypes.c_int, [ctypes.POINTER(AttnDims), i64, ctypes.POINTER(i64)]),
         "qmm_attn_decode": (ctypes.c_int, [ctypes.POINTER(AttnDims), vp, vp, vp, vp, vp, i64, vp, vp, i64,
                                            vp, vp]),
     }
@@ -238,9 +238,10 @@ class Step:
 ATTN_RECORD_BYTES = 17408
 
 
-def attn_workspace_bytes(dims: AttnDims) -> int:
+def attn_workspace_bytes(dims: AttnDims, rows: int) -> int:
     n = ctypes.c_int64()
-    _check(load().qmm_attn_workspace_bytes(ctypes.byref(dims), ctypes.byref(n)), "qmm_attn_workspace_bytes")
+    _check(load().qmm_attn_workspace_bytes(ctypes.byref(dims), int(rows), ctypes.byref(n)),
+           "qmm_attn_workspace_bytes")
     return n.value
 
 
@@ -257,7 +258,7 @@ def attn_decode(pool, page_table, agent_rows, row_len, q, out, kv_heads: int, st
     lib = load()
     dims = AttnDims(int(q.shape[1]), int(kv_heads), int(page_table.shape[0]), int(page_table.shape[1]),
                     int(pool.numel() // (kv_heads * ATTN_RECORD_BYTES)))
-    nbytes = attn_workspace_bytes(dims)
+    nbytes = attn_workspace_bytes(dims, int(q.shape[0]))
     if workspace is None or workspace.numel() < nbytes:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     if err is None:

@@ -172,11 +172,13 @@ qmm_status qmm_run_argmax(qmm_handle h, const void* x, int64_t m, int32_t* idx, 
  *  agent_rows: int32 [agents + 1], non-decreasing: agent a's rows are agent_rows[a] ..
  *              agent_rows[a + 1] - 1 (an agent may have none).
  *  row_len:    int32 [rows]: 1 <= row_len[r] <= max_pages * 64.
- *  q:          fp16 [rows][heads][128], 16-byte aligned; out: fp32 [rows][heads][128].
- *  An agent with more than 32 queries per KV head (its rows x heads / kv_heads), or a row
- *  length out of range, sets *err_word |= 4 and its rows' outputs are zero.
- *  workspace:  16-byte aligned, at least qmm_attn_workspace_bytes(dims) bytes (fixed by dims);
- *              used by this call until its kernels finish.
+ *  q:          fp16 [rows][heads][128], 16-byte aligned; out: fp32 [rows][heads][128], 16-byte
+ *              aligned.
+ *  An agent's queries per KV head (its rows x heads / kv_heads) are taken 32 at a time, each
+ *  group of 32 a pass over the agent's pages.  A row length out of range sets
+ *  *err_word |= 4, and the agent's rows' outputs are zero.
+ *  workspace:  16-byte aligned, at least qmm_attn_workspace_bytes(dims, rows) bytes (fixed by
+ *              dims and rows); used by this call until its kernels finish.
  *  err_word:   device-visible int, or-ed with 1 if a device-side wait ran out, 2 or 4 as
  *              above; the caller zeroes it and reads it after synchronising.
  * Errors: INVALID_ARG, MISALIGNED, SCRATCH_TOO_SMALL, CUDA.
@@ -189,7 +191,9 @@ typedef struct {
     int64_t pool_pages;  /* pages in the pool */
 } qmm_attn_dims;
 
-qmm_status qmm_attn_workspace_bytes(const qmm_attn_dims* dims, int64_t* bytes);
+/* Workspace bytes of qmm_attn_decode for these dims and at most `rows` rows (1 .. 2^24):
+ * errors INVALID_ARG. */
+qmm_status qmm_attn_workspace_bytes(const qmm_attn_dims* dims, int64_t rows, int64_t* bytes);
 
 qmm_status qmm_attn_decode(const qmm_attn_dims* dims, const void* pool, const int32_t* page_table,
                            const int32_t* agent_rows, const int32_t* row_len, const void* q, int64_t rows,

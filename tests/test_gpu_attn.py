@@ -95,17 +95,26 @@ def test_attention_rows_do_not_depend_on_the_batch():
     assert np.array_equal(part.view(np.uint32), full[sel].view(np.uint32))
 
 
-def test_attention_refuses_too_many_queries():
-    """Six rows of one agent at 6 query heads per KV head make 36 queries for a KV head, more
-    than a work item holds: the error word gets 4 and the rows' outputs are zero; the other
-    agent is unaffected."""
-    pool, table, q, ra, rl, kvh = case((300, 100), 6, 48, 8, seed=6)
-    keep = np.r_[np.where(ra == 0)[0], np.where(ra == 1)[0][:3]]
-    got, err = run_attn(pool, table, q[keep], ra[keep], rl[keep], kvh)
-    assert err & 4
-    assert np.all(got[:6] == 0)
-    ref, s = oracle.attn(pool, table, q[keep[6:]], ra[keep[6:]], rl[keep[6:]], kvh)
-    assert np.all(np.abs(got[6:] - ref) <= 2e-3 * s + 1e-6)
+@pytest.mark.parametrize("rows,heads,kvh", [(6, 48, 8), (8, 48, 8), (11, 48, 8), (40, 8, 8)],
+                         ids=["36q", "48q-verify", "66q", "40q-mha"])
+def test_attention_wide_agents_in_query_tiles(rows, heads, kvh):
+    """More than 32 queries per (agent, KV head) run as tiles of 32, each a pass over the
+    agent's pages: 6, 8 (the wide-verify step's 1 + 7 drafts) and 11 rows at 6 queries per row
+    and KV head, and 40 rows of plain multi-head attention."""
+    check(*case((300, 1500), rows, heads, kvh, seed=6), what=f"{rows} rows")
+
+
+def test_attention_query_tiles_match_narrow_batches():
+    """A row computed in the second query tile of a wide agent has the bits it has when its
+    agent's batch holds only that row's tile (tiles never mix)."""
+    pool, table, q, ra, rl, kvh = case((900,), 8, 48, 8, seed=7)
+    full, _ = run_attn(pool, table, q, ra, rl, kvh)
+    # 8 rows x 6 heads per KV head = 48 queries: tile 0 holds queries 0..31, tile 1 holds
+    # 32..47 (the last four of row 5, then rows 6 and 7); alone, rows 6 and 7 make one tile
+    sel = np.arange(6, 8)
+    sub = np.ascontiguousarray(q[sel])
+    part, _ = run_attn(pool, table, sub, ra[sel], rl[sel], kvh)
+    assert np.array_equal(part.view(np.uint32), full[sel].view(np.uint32))
 
 
 def test_attention_bad_page_is_reported():
