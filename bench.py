@@ -302,13 +302,12 @@ def format_line(torch, fmt, code, m, stream, parity, reps=50):
     return line
 
 
-def attention_line(torch, stream, hbm, parity, reps=50):
-    """Stacked-row decode attention of one layer at the pages' decode step (4 agents with
-    23,000 cached tokens, 1 token + 2 drafts each, 48 query heads over 8 KV heads, q8_0 KV in
-    a shared paged pool): time per call, KV GB/s (every page read once per call) and a
-    sampled oracle check of two rows."""
+def attention_line(torch, stream, hbm, parity, reps=50, w=synth.ATTN_DECODE, name=None):
+    """Stacked-row decode attention of one layer (48 query heads over 8 KV heads, q8_0 KV in a
+    shared paged pool): time per call, KV GB/s (every page read once per query tile of an
+    agent) and a sampled oracle check of two rows.  The default workload is the pages' decode
+    step (4 agents with 23,000 cached tokens, 1 token + 2 drafts each)."""
     from bit_weight_streaming_q4_gb300.qmm import AttnDims, attn_decode, attn_workspace_bytes
-    w = synth.ATTN_DECODE
     table, total, ra, rl = w.build(seed=0)
     pool = synth.kv_pool(total, w.kv_heads, seed=0, tensor_id=60)
     q = synth.attn_q(len(ra), w.heads, seed=0, tensor_id=61)
@@ -334,9 +333,14 @@ def attention_line(torch, stream, hbm, parity, reps=50):
     e1.record(stream)
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / reps
-    kv_bytes = sum(w.pages_of()) * w.kv_heads * synth.KV_RECORD_BYTES
-    line = {"workload": "4 agents x 23,000 cached tokens, 3 rows each (1 token + 2 drafts), 48 query heads "
-                        "over 8 KV heads of 128, q8_0 KV pool in 64-token pages; one layer",
+    group = w.heads // w.kv_heads
+    tiles = -(-w.rows_per_agent * group // 32)  # query tiles per agent: each reads the agent's pages
+    kv_bytes = sum(w.pages_of()) * w.kv_heads * synth.KV_RECORD_BYTES * tiles
+    agents = len(w.cache)
+    line = {"workload": name or (f"{agents} agents x {w.cache[0]:,} cached tokens, {w.rows_per_agent} rows each "
+                                 f"(1 token + {w.rows_per_agent - 1} drafts), {w.heads} query heads over "
+                                 f"{w.kv_heads} KV heads of 128, q8_0 KV pool in 64-token pages; one layer"),
+            "query_tiles_per_agent": tiles,
             "kv_bytes": kv_bytes, "us_per_call": us, "kv_gbs": kv_bytes / us / 1e3,
             "frac_of_hbm_measured": kv_bytes / us / 1e3 / hbm, "error_word": int(err.item()),
             "kernels_per_call": 2}
@@ -831,13 +835,14 @@ def run_ours(args, rank, world, local_rank):
     verify = None
     formats = None
     attention = None
-    single = sweep = prefill = None
+    single = sweep = prefill = attention_verify = None
     if not args.no_extra:
         verify = {str(m): lm_head_verify(stack, m, stream) for m in sorted({*EXTRA_M, HEADLINE_M})}
         # the other block formats of a mixed-quant file, on the lm_head shape at M = 12
         formats = {name: format_line(torch, f, code, HEADLINE_M, stream, not args.no_parity)
                    for name, f, code in (("Q6_K", synth.Q6_K, 1), ("Q8_0", synth.Q8_0, 2))}
         attention = attention_line(torch, stream, hbm, not args.no_parity)
+        attention_verify = attention_line(torch, stream, hbm, not args.no_parity, w=synth.ATTN_VERIFY)
         single = single_projection_line(torch, stream, hbm, not args.no_parity)
         sweep = m_sweep_line(torch, stream, hbm)
         prefill = prefill_line(torch, stream, peaks, not args.no_parity, layers=args.layers)
@@ -865,6 +870,7 @@ def run_ours(args, rank, world, local_rank):
         "lm_head_verify": verify,
         "formats": formats,
         "attention": attention,
+        "attention_verify": attention_verify,
         "single_projection": single,
         "m_sweep": sweep,
         "chunked_prefill": prefill,
@@ -891,12 +897,13 @@ def run_single(args):
     import torch
     from bit_weight_streaming_q4_gb300 import Qmm
     torch.cuda.set_device(0)
-    if args.single == "attention":
+    if args.single in ("attention", "attention_verify"):
         peaks, _ = measured_peaks()
         stream = torch.cuda.Stream()
+        w = synth.ATTN_DECODE if args.single == "attention" else synth.ATTN_VERIFY
         line = attention_line(torch, stream, float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS)), not args.no_parity,
-                              reps=max(args.steps, 1))
-        print(json.dumps({"single": "attention", **line}), flush=True)
+                              reps=max(args.steps, 1), w=w)
+        print(json.dumps({"single": args.single, **line}), flush=True)
         return
     shapes = {"proj4096": synth.SINGLE_PROJECTION, "lm_head": synth.LM_HEAD}
     shapes.update({m.name.split(".")[1]: m for m in synth.layer_matrices(0)})

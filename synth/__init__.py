@@ -241,6 +241,9 @@ class AttnWorkload:
 
 # The decode step of the pages: 4 agents with 23K-token contexts, 1 token + 2 drafts each.
 ATTN_DECODE = AttnWorkload(cache=(23000, 23000, 23000, 23000), rows_per_agent=3)
+# The wide speculative verify step: 8 streams x (1 token + 7 block drafts); 8 x 16,000 cached
+# tokens fill most of the pages' shared 132K-token pool.
+ATTN_VERIFY = AttnWorkload(cache=(16000,) * 8, rows_per_agent=8)
 
 
 def attn_q(rows: int, heads: int, seed: int, tensor_id: int) -> np.ndarray:
