@@ -390,6 +390,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async_smem();
     __syncthreads();
     griddep_launch_dependents();
+    // Q6_K: the dequantisation warpgroups (warps 0-7), whose unit needs the most registers,
+    // take 176 per thread and the other two (producer, activations, issuers, epilogue) give
+    // theirs down to 80: 2 x 128 x 176 + 2 x 128 x 80 = 65,536 = the launch's 512 threads x
+    // 128.  Every warp runs its instruction here, before any role can return.  (Measured: Q6_K
+    // streams 8 % faster; Q4_K, whose epilogue and issuers then spill, 7 % slower.)
+    static_assert(kDqWarps == 8 && kThreads == 512, "register split by warpgroup");
+    if constexpr (F == QMM_FORMAT_Q6_K) {
+        if (warp < kDqWarps) setmaxnreg_inc<176>();
+        else setmaxnreg_dec<80>();
+    }
 
     // ------------------------------------------------------------------ weight producer
     if (warp == kProducerWarp) {
@@ -1007,7 +1017,13 @@ cudaError_t repack(const uint8_t* src_dev, uint8_t* dst_dev, const Decomp& d, in
 
 template <int MP, int F>
 static cudaError_t set_attr() {
-    return cudaFuncSetAttribute(tc_kernel<MP, F>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<MP, F>::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(tc_kernel<MP, F>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<MP, F>::kSmem);
+    if (e != cudaSuccess || F != QMM_FORMAT_Q6_K) return e;
+    // the Q6_K register split (setmaxnreg) is sized for launches of exactly 128 registers per
+    // thread: anything else and an increase could wait forever, so the library refuses to run
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, tc_kernel<MP, F>)) != cudaSuccess) return e;
+    return fa.numRegs == 128 ? cudaSuccess : cudaErrorInvalidKernelImage;
 }
 
 template <int F>

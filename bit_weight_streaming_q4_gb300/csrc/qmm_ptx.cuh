@@ -203,6 +203,17 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, in
         : "memory");
 }
 
+// Register rebalancing between warpgroups (every warp of a warpgroup executes the same one;
+// the increases of a CTA must fit in what its decreases and its launch allocation free).
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
