@@ -100,6 +100,8 @@ struct Cfg {
     // -B_l step come from the pre-pass (presum_for) with the tile
     static constexpr bool kIssuerWaitsX = MP == 128;
     static constexpr bool kPre = kMin && kIssuerWaitsX;
+    // registers per dequantisation thread after the warpgroup split (0: no split, 128 for all)
+    static constexpr int kRegSplit = F == QMM_FORMAT_Q6_K ? 176 : (F == QMM_FORMAT_Q4_K && MP >= 64) ? 152 : 0;
     static constexpr int kWRing = w_ring(F, MP);
     static constexpr int kXRing = x_ring(F, MP);
     static constexpr int kXBox = MP * 128;    // one 64-wide k box of x
@@ -390,15 +392,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async_smem();
     __syncthreads();
     griddep_launch_dependents();
-    // Q6_K: the dequantisation warpgroups (warps 0-7), whose unit needs the most registers,
-    // take 176 per thread and the other two (producer, activations, issuers, epilogue) give
-    // theirs down to 80: 2 x 128 x 176 + 2 x 128 x 80 = 65,536 = the launch's 512 threads x
-    // 128.  Every warp runs its instruction here, before any role can return.  (Measured: Q6_K
-    // streams 8 % faster; Q4_K, whose epilogue and issuers then spill, 7 % slower.)
+    // Registers moved to the dequantisation warpgroups (warps 0-7) from the other two
+    // (producer, activations, issuers, epilogue), where measured faster: Q6_K 176 / 80 (+8 %),
+    // Q4_K at MP >= 64 152 / 104 (+2-4 %; at MP <= 32 it lost 2 %, and 176 / 80 lost 7 %).
+    // 2 x 128 x 176 + 2 x 128 x 80 = 2 x 128 x 152 + 2 x 128 x 104 = 65,536 = the launch's
+    // 512 threads x 128 (checked on the host).  Every warp runs its instruction here, before
+    // any role can return.
     static_assert(kDqWarps == 8 && kThreads == 512, "register split by warpgroup");
-    if constexpr (F == QMM_FORMAT_Q6_K) {
+    if constexpr (C::kRegSplit == 176) {
         if (warp < kDqWarps) setmaxnreg_inc<176>();
         else setmaxnreg_dec<80>();
+    } else if constexpr (C::kRegSplit == 152) {
+        if (warp < kDqWarps) setmaxnreg_inc<152>();
+        else setmaxnreg_dec<104>();
     }
 
     // ------------------------------------------------------------------ weight producer
@@ -1018,9 +1024,9 @@ cudaError_t repack(const uint8_t* src_dev, uint8_t* dst_dev, const Decomp& d, in
 template <int MP, int F>
 static cudaError_t set_attr() {
     cudaError_t e = cudaFuncSetAttribute(tc_kernel<MP, F>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<MP, F>::kSmem);
-    if (e != cudaSuccess || F != QMM_FORMAT_Q6_K) return e;
-    // the Q6_K register split (setmaxnreg) is sized for launches of exactly 128 registers per
-    // thread: anything else and an increase could wait forever, so the library refuses to run
+    if (e != cudaSuccess || Cfg<MP, F>::kRegSplit == 0) return e;
+    // a register split (setmaxnreg) is sized for launches of exactly 128 registers per thread:
+    // anything else and an increase could wait forever, so the library refuses to run
     cudaFuncAttributes fa;
     if ((e = cudaFuncGetAttributes(&fa, tc_kernel<MP, F>)) != cudaSuccess) return e;
     return fa.numRegs == 128 ? cudaSuccess : cudaErrorInvalidKernelImage;
