@@ -307,7 +307,7 @@ def attention_line(torch, stream, hbm, parity, reps=50, w=synth.ATTN_DECODE, nam
     shared paged pool): time per call, KV GB/s (every page read once per query tile of an
     agent) and a sampled oracle check of two rows.  The default workload is the pages' decode
     step (4 agents with 23,000 cached tokens, 1 token + 2 drafts each)."""
-    from bit_weight_streaming_q4_gb300.qmm import AttnDims, attn_decode, attn_workspace_bytes
+    from bit_weight_streaming_q4_gb300.qmm import ATTN_QUERY_TILE, AttnDims, attn_decode, attn_workspace_bytes
     table, total, ra, rl = w.build(seed=0)
     pool = synth.kv_pool(total, w.kv_heads, seed=0, tensor_id=60)
     q = synth.attn_q(len(ra), w.heads, seed=0, tensor_id=61)
@@ -334,7 +334,7 @@ def attention_line(torch, stream, hbm, parity, reps=50, w=synth.ATTN_DECODE, nam
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / reps
     group = w.heads // w.kv_heads
-    tiles = -(-w.rows_per_agent * group // 32)  # query tiles per agent: each reads the agent's pages
+    tiles = -(-w.rows_per_agent * group // ATTN_QUERY_TILE)  # query tiles per agent: each reads its pages
     kv_bytes = sum(w.pages_of()) * w.kv_heads * synth.KV_RECORD_BYTES * tiles
     agents = len(w.cache)
     line = {"workload": name or (f"{agents} agents x {w.cache[0]:,} cached tokens, {w.rows_per_agent} rows each "

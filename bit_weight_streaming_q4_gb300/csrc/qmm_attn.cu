@@ -43,9 +43,10 @@ namespace qmm {
 namespace attn {
 
 constexpr int kD = 128, kPT = 64, kRec = 17408;
-constexpr int kMaxQ = 32;   // queries per item: rows of the agent x heads of the group
+constexpr int kMaxQ = 24;   // queries per tile (an agent's rows x the group's heads, 24 at a time)
+constexpr int kNT = kMaxQ / 8;  // n8 tiles of queries per tile
 constexpr int kSlotCap = 1024;  // upper bound on the resident CTAs a launch is planned for
-constexpr int kStages = 4;  // pages in flight per CTA
+constexpr int kStages = 3;  // pages in flight per CTA (4 CTAs per SM keep 8 in flight)
 constexpr int kThreads = 128;
 constexpr int kPart = kD + 4;  // floats per query of an item's partial: o[128], m, l, 2 unused (16-byte rows)
 constexpr float kNegBig = -1e30f;
@@ -114,7 +115,7 @@ __device__ __forceinline__ void mma_m16n8k16_z(float (&d)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
 
-__global__ void __launch_bounds__(kThreads, 3) attn_partial(const Params p) {
+__global__ void __launch_bounds__(kThreads, 4) attn_partial(const Params p) {
     extern __shared__ __align__(128) uint8_t sm[];
     // ring slot i % kStages holds page i
     __half* P = reinterpret_cast<__half*>(sm + kStages * kRec);       // [kMaxQ][kPS] probabilities
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 3) attn_partial(const Params p) {
     const int q0 = static_cast<int>(blockIdx.y) * kMaxQ;
     const int nq = it.nr * p.group - q0 < kMaxQ ? it.nr * p.group - q0 : kMaxQ;
     if (nq <= 0) return;
-    const int nnt = (nq + 7) >> 3;  // n8 tiles of queries (1 .. 4)
+    const int nnt = (nq + 7) >> 3;  // n8 tiles of queries (1 .. kNT)
     const float c2 = 1.4426950408889634f * 0.08838834764831845f;  // log2(e) / sqrt(128)
 
     if (tid == 0) {
@@ -197,9 +198,9 @@ __global__ void __launch_bounds__(kThreads, 3) attn_partial(const Params p) {
     // ks = 2 blk + k2 are assigned so that every thread's eight dims of a 32-dim block are
     // contiguous: k-slots (2t, 2t+1) are dims 32 blk + 8t + 4 k2 + {0, 1}, slots (2t+8, 2t+9)
     // dims 32 blk + 8t + 4 k2 + {2, 3}.  qb holds Q^T's B fragments for all k-steps.
-    uint32_t qb[4][8][2];
+    uint32_t qb[kNT][8][2];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
+    for (int nt = 0; nt < kNT; ++nt) {
         const int qi = 8 * nt + g8;
         const __half* qrow = nullptr;
         if (qi < nq) {
@@ -220,10 +221,10 @@ __global__ void __launch_bounds__(kThreads, 3) attn_partial(const Params p) {
     // sum of probabilities, and O^T (dims 32w + 16 mt + {g8, g8 + 8}).  Probabilities carry a
     // factor 2^8 (kept in the sum too) so that P times a V scale stays clear of the fp16
     // subnormal range.
-    float m_run[4][2], l_part[4][2];
-    float o[2][4][4];  // [m16 tile of dims][n8 tile of queries][accumulator]
+    float m_run[kNT][2], l_part[kNT][2];
+    float o[2][kNT][4];  // [m16 tile of dims][n8 tile of queries][accumulator]
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
+    for (int nt = 0; nt < kNT; ++nt) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             m_run[nt][e] = kNegBig;
@@ -245,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 3) attn_partial(const Params p) {
         const int tbase = (it.page0 + i) * kPT;  // logical index of the page's first token
 
         // ---- scores s[nt][c]: c0 (token t0, query 8nt + 2t4), c1 (t0, +1), c2 (t0 + 8, ..), c3
-        float s[4][4];
+        float s[kNT][4];
         {
             const uint2 sca = *reinterpret_cast<const uint2*>(rec + 8192 + t0 * 8);
             const uint2 scb = *reinterpret_cast<const uint2*>(rec + 8192 + (t0 + 8) * 8);
@@ -265,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 3) attn_partial(const Params p) {
                 const float sa = __half2float((blk & 1) ? __high2half(as_h2(wa)) : __low2half(as_h2(wa)));
                 const float sb = __half2float((blk & 1) ? __high2half(as_h2(wb)) : __low2half(as_h2(wb)));
 #pragma unroll
-                for (int nt = 0; nt < 4; ++nt) {
+                for (int nt = 0; nt < kNT; ++nt) {
                     if (nt < nnt) {
                         float tmp[4];
                         mma_m16n8k16_z(tmp, a00, a01, a02, a03, qb[nt][2 * blk][0], qb[nt][2 * blk][1]);
@@ -288,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 3) attn_partial(const Params p) {
         // ---- masks (only on pages reaching past the shortest row) and the warp's maxima
         if (tbase + kPT > minlen) {
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
+            for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     if (nt < nnt) {
@@ -299,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 3) attn_partial(const Params p) {
                 }
         }
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 if (nt < nnt) {
@@ -322,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 3) attn_partial(const Params p) {
 
         // ---- new maxima, rescaling, probabilities (x 2^8, fp16) to shared memory
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
+        for (int nt = 0; nt < kNT; ++nt) {
             if (nt < nnt) {
                 float pr[4];
 #pragma unroll
@@ -381,9 +382,9 @@ __global__ void __launch_bounds__(kThreads, 3) attn_partial(const Params p) {
             for (int ks = 0; ks < 4; ++ks) {
                 // V scales of tokens 16 t4 + 4 ks .. + 3 (this warp's block)
                 const uint2 dv = *reinterpret_cast<const uint2*>(rec + 16896 + (warp * kPT + 16 * t4 + 4 * ks) * 2);
-                uint32_t pb[4][2];  // B fragments: (P x V scale) of query 8 nt + g8, the k-step's tokens
+                uint32_t pb[kNT][2];  // B fragments: (P x V scale) of query 8 nt + g8, the k-step's tokens
 #pragma unroll
-                for (int nt = 0; nt < 4; ++nt) {
+                for (int nt = 0; nt < kNT; ++nt) {
                     if (nt < nnt) {
                         const uint2 pw = *reinterpret_cast<const uint2*>(P + (8 * nt + g8) * kPS + 16 * t4 + 4 * ks);
                         pb[nt][0] = as_u32(__hmul2(as_h2(pw.x), as_h2(dv.x)));
@@ -395,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 3) attn_partial(const Params p) {
                     const uint32_t a0 = i8pair_to_h2(wv[mt][0][ks], 0x4140u), a2 = i8pair_to_h2(wv[mt][0][ks], 0x4342u);
                     const uint32_t a1 = i8pair_to_h2(wv[mt][1][ks], 0x4140u), a3 = i8pair_to_h2(wv[mt][1][ks], 0x4342u);
 #pragma unroll
-                    for (int nt = 0; nt < 4; ++nt)
+                    for (int nt = 0; nt < kNT; ++nt)
                         if (nt < nnt) mma_m16n8k16(o[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
                 }
             }
@@ -413,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 3) attn_partial(const Params p) {
 
     // ---- the item's partial: o, m and l per query
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             if (nt < nnt) {
@@ -428,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 3) attn_partial(const Params p) {
     // slot (agent, g, run, tile)
     float* part = p.ws + (static_cast<int64_t>(blockIdx.x) * p.max_qt + blockIdx.y) * kMaxQ * kPart;
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < kNT; ++nt)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const int qi = 8 * nt + 2 * t4 + e;

@@ -236,6 +236,7 @@ class Step:
 
 
 ATTN_RECORD_BYTES = 17408
+ATTN_QUERY_TILE = 24  # queries per (agent, KV head) that one pass over the agent's pages serves
 
 
 def attn_workspace_bytes(dims: AttnDims, rows: int) -> int:

@@ -174,7 +174,7 @@ qmm_status qmm_run_argmax(qmm_handle h, const void* x, int64_t m, int32_t* idx, 
  *  row_len:    int32 [rows]: 1 <= row_len[r] <= max_pages * 64.
  *  q:          fp16 [rows][heads][128], 16-byte aligned; out: fp32 [rows][heads][128], 16-byte
  *              aligned.
- *  An agent's queries per KV head (its rows x heads / kv_heads) are taken 32 at a time, each
+ *  An agent's queries per KV head (its rows x heads / kv_heads) are taken 24 at a time, each
  *  group of 32 a pass over the agent's pages.  A row length out of range sets
  *  *err_word |= 4, and the agent's rows' outputs are zero.
  *  workspace:  16-byte aligned, at least qmm_attn_workspace_bytes(dims, rows) bytes (fixed by

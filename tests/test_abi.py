@@ -119,19 +119,19 @@ def test_attention_arguments_without_device(lib):
     the argument errors it reports before any launch."""
     dims = Q.AttnDims(48, 8, 4, 400, 1600)
     nbytes = ctypes.c_int64()
-    # agents x KV heads x runs x query tiles x 32 queries x (128 + 4) floats.  Runs are planned
+    # agents x KV heads x runs x query tiles x 24 queries x (128 + 4) floats.  Runs are planned
     # for at most 1024 resident CTAs: at most 1024 // 32 = 32 runs, so runs of
     # ceil(400 / 32) = 13 pages, of which 400 pages make 31.  Query tiles: all rows in one agent,
-    # 6 queries per row and KV head, 32 per tile.
-    for rows, tiles in ((1, 1), (5, 1), (6, 2), (12, 3), (64, 12)):
+    # 6 queries per row and KV head, 24 per tile.
+    for rows, tiles in ((1, 1), (4, 1), (5, 2), (8, 2), (12, 3), (64, 16)):
         assert lib.qmm_attn_workspace_bytes(ctypes.byref(dims), rows, ctypes.byref(nbytes)) == 0
-        assert nbytes.value == 4 * 8 * 31 * tiles * 32 * 132 * 4, rows
+        assert nbytes.value == 4 * 8 * 31 * tiles * 24 * 132 * 4, rows
     wide = Q.AttnDims(48, 8, 128, 20, 1600)  # 1024 (agent, KV head) pairs: one run each
     assert lib.qmm_attn_workspace_bytes(ctypes.byref(wide), 3, ctypes.byref(nbytes)) == 0
-    assert nbytes.value == 128 * 8 * 1 * 1 * 32 * 132 * 4
+    assert nbytes.value == 128 * 8 * 1 * 1 * 24 * 132 * 4
     short = Q.AttnDims(48, 8, 1, 5, 1600)  # at most one run per page
     assert lib.qmm_attn_workspace_bytes(ctypes.byref(short), 3, ctypes.byref(nbytes)) == 0
-    assert nbytes.value == 1 * 8 * 5 * 1 * 32 * 132 * 4
+    assert nbytes.value == 1 * 8 * 5 * 1 * 24 * 132 * 4
     for bad in (Q.AttnDims(48, 7, 4, 400, 1600), Q.AttnDims(0, 8, 4, 400, 1600), Q.AttnDims(48, 8, 0, 400, 1600),
                 Q.AttnDims(48, 8, 4, 0, 1600), Q.AttnDims(48, 8, 4, 400, 0)):
         assert lib.qmm_attn_workspace_bytes(ctypes.byref(bad), 3, ctypes.byref(nbytes)) == 1

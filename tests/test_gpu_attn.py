@@ -98,7 +98,7 @@ def test_attention_rows_do_not_depend_on_the_batch():
 @pytest.mark.parametrize("rows,heads,kvh", [(6, 48, 8), (8, 48, 8), (11, 48, 8), (40, 8, 8)],
                          ids=["36q", "48q-verify", "66q", "40q-mha"])
 def test_attention_wide_agents_in_query_tiles(rows, heads, kvh):
-    """More than 32 queries per (agent, KV head) run as tiles of 32, each a pass over the
+    """More than 24 queries per (agent, KV head) run as tiles of 24, each a pass over the
     agent's pages: 6, 8 (the wide-verify step's 1 + 7 drafts) and 11 rows at 6 queries per row
     and KV head, and 40 rows of plain multi-head attention."""
     check(*case((300, 1500), rows, heads, kvh, seed=6), what=f"{rows} rows")
@@ -109,8 +109,9 @@ def test_attention_query_tiles_match_narrow_batches():
     agent's batch holds only that row's tile (tiles never mix)."""
     pool, table, q, ra, rl, kvh = case((900,), 8, 48, 8, seed=7)
     full, _ = run_attn(pool, table, q, ra, rl, kvh)
-    # 8 rows x 6 heads per KV head = 48 queries: tile 0 holds queries 0..31, tile 1 holds
-    # 32..47 (the last four of row 5, then rows 6 and 7); alone, rows 6 and 7 make one tile
+    # 8 rows x 6 heads per KV head = 48 queries: tile 0 holds queries 0..23 (rows 0-3), tile 1
+    # holds 24..47 (rows 4-7, rows 6 and 7 at positions 12..23); alone, rows 6 and 7 make one
+    # tile, at positions 0..11
     sel = np.arange(6, 8)
     sub = np.ascontiguousarray(q[sel])
     part, _ = run_attn(pool, table, sub, ra[sel], rl[sel], kvh)
