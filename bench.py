@@ -42,8 +42,8 @@ TRAFFIC_PER_UNIT = {
         "sha256": "43d77ce69d57d591d1ae8852fdc3a0d12692e52edc2c34708f401cbef0162db2",
         "bytes": 37194.0},
     2: {"source": "bit_weight_streaming_q4_gb300/csrc/qmm_b2.cu",
-        "sha256": "76d56ffdbde34756aec0b112c19a91a39597102df4db42ddda76730d56590f4a",
-        "bytes": 18584.8},
+        "sha256": "9d85db3f16d473e7c7f934b4bc7aeac168090d8330a7a06fc39e50c4a501260e",
+        "bytes": 18585.1},
 }
 KERNEL_NAME = {1: "qmm::b1::stream_kernel<2>", 2: "qmm::b2::tc_kernel<16>"}
 HEADLINE_M = 12
