@@ -319,17 +319,17 @@ def attention_line(torch, stream, hbm, parity, reps=50, w=synth.ATTN_DECODE, nam
     q_d = torch.from_numpy(q.view(np.int16)).cuda().view(torch.float16)
     out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
     s = stream.cuda_stream
-    dims = AttnDims(w.heads, w.kv_heads, table.shape[0], table.shape[1], total)
+    dims = AttnDims(w.heads, w.kv_heads, table.shape[0], table.shape[1], total, w.rows_per_agent)
     ws = torch.empty(attn_workspace_bytes(dims, len(ra)), dtype=torch.uint8, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     for _ in range(3):
-        attn_decode(pool_d, table_d, ar_d, rl_d, q_d, out, w.kv_heads, s, ws, err)
+        attn_decode(pool_d, table_d, ar_d, rl_d, q_d, out, w.kv_heads, s, ws, err, max_agent_rows=w.rows_per_agent)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(reps):
-        attn_decode(pool_d, table_d, ar_d, rl_d, q_d, out, w.kv_heads, s, ws, err)
+        attn_decode(pool_d, table_d, ar_d, rl_d, q_d, out, w.kv_heads, s, ws, err, max_agent_rows=w.rows_per_agent)
     e1.record(stream)
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / reps

@@ -535,9 +535,11 @@ int64_t max_runs(const qmm_attn_dims* dims) {
     return runs;
 }
 
-// Query tiles of kMaxQ an agent of a call with `rows` rows can need: all rows in one agent.
+// Query tiles of kMaxQ an agent of a call with `rows` rows can need: all of them, or at most
+// dims->max_agent_rows rows in one agent when that bound is given.
 int32_t max_tiles(const qmm_attn_dims* dims, int64_t rows) {
-    const int64_t q = rows * (dims->heads / dims->kv_heads);
+    const int64_t r = dims->max_agent_rows > 0 && dims->max_agent_rows < rows ? dims->max_agent_rows : rows;
+    const int64_t q = r * (dims->heads / dims->kv_heads);
     return static_cast<int32_t>((q + kMaxQ - 1) / kMaxQ);
 }
 
@@ -549,7 +551,8 @@ extern "C" {
 qmm_status qmm_attn_workspace_bytes(const qmm_attn_dims* dims, int64_t rows, int64_t* bytes) {
     if (!dims || !bytes) return QMM_ERR_INVALID_ARG;
     if (dims->heads < 1 || dims->kv_heads < 1 || dims->heads % dims->kv_heads != 0 || dims->agents < 1 ||
-        dims->max_pages < 1 || dims->pool_pages < 1 || rows < 1 || rows > (int64_t{1} << 24))
+        dims->max_pages < 1 || dims->pool_pages < 1 || rows < 1 || rows > (int64_t{1} << 24) ||
+        dims->max_agent_rows < 0 || dims->reserved != 0)
         return QMM_ERR_INVALID_ARG;
     *bytes = static_cast<int64_t>(dims->agents) * dims->kv_heads * qmm::attn::max_runs(dims) *
              qmm::attn::max_tiles(dims, rows) * qmm::attn::kMaxQ * qmm::attn::kPart * 4;

@@ -47,7 +47,8 @@ class Info(ctypes.Structure):
 
 class AttnDims(ctypes.Structure):
     _fields_ = [("heads", ctypes.c_int32), ("kv_heads", ctypes.c_int32), ("agents", ctypes.c_int32),
-                ("max_pages", ctypes.c_int32), ("pool_pages", ctypes.c_int64)]
+                ("max_pages", ctypes.c_int32), ("pool_pages", ctypes.c_int64), ("max_agent_rows", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 _lib = None
@@ -247,18 +248,20 @@ def attn_workspace_bytes(dims: AttnDims, rows: int) -> int:
 
 
 def attn_decode(pool, page_table, agent_rows, row_len, q, out, kv_heads: int, stream: int | None = None,
-                workspace=None, err=None):
+                workspace=None, err=None, max_agent_rows: int = 0):
     """Stacked-row decode attention over a paged q8_0 KV pool (qmm_attn_decode in qmm.h).
 
     pool: uint8 CUDA tensor of 17,408-byte records; page_table: int32 CUDA tensor [agents,
     max_pages]; agent_rows: int32 CUDA tensor [agents + 1]; row_len: int32 CUDA tensor [rows];
     q: fp16 CUDA tensor [rows, heads, 128]; out: fp32 CUDA tensor [rows, heads, 128].  The
     workspace and the error word are allocated unless given; returns the error word (a CUDA
-    int32 tensor of one element, nonzero after the launch if the device reported a failure)."""
+    int32 tensor of one element, nonzero after the launch if the device reported a failure).
+    max_agent_rows: an upper bound on any agent's rows (0: the call's rows), which sizes the
+    workspace and the grid."""
     import torch
     lib = load()
     dims = AttnDims(int(q.shape[1]), int(kv_heads), int(page_table.shape[0]), int(page_table.shape[1]),
-                    int(pool.numel() // (kv_heads * ATTN_RECORD_BYTES)))
+                    int(pool.numel() // (kv_heads * ATTN_RECORD_BYTES)), int(max_agent_rows))
     nbytes = attn_workspace_bytes(dims, int(q.shape[0]))
     if workspace is None or workspace.numel() < nbytes:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)

@@ -189,10 +189,14 @@ typedef struct {
     int32_t agents;      /* rows of page_table */
     int32_t max_pages;   /* columns of page_table */
     int64_t pool_pages;  /* pages in the pool */
+    int32_t max_agent_rows;  /* upper bound on any agent's rows in a call, or 0 (= the call's
+                                rows): sizes the workspace and the grid; an agent above it
+                                sets *err_word |= 4 */
+    int32_t reserved;        /* zero */
 } qmm_attn_dims;
 
-/* Workspace bytes of qmm_attn_decode for these dims and at most `rows` rows (1 .. 2^24):
- * errors INVALID_ARG. */
+/* Workspace bytes of qmm_attn_decode for these dims and at most `rows` rows (1 .. 2^24),
+ * with at most min(rows, dims->max_agent_rows if > 0) rows in one agent: errors INVALID_ARG. */
 qmm_status qmm_attn_workspace_bytes(const qmm_attn_dims* dims, int64_t rows, int64_t* bytes);
 
 qmm_status qmm_attn_decode(const qmm_attn_dims* dims, const void* pool, const int32_t* page_table,

@@ -137,6 +137,15 @@ def test_attention_arguments_without_device(lib):
         assert lib.qmm_attn_workspace_bytes(ctypes.byref(bad), 3, ctypes.byref(nbytes)) == 1
     for rows in (0, -1, (1 << 24) + 1):
         assert lib.qmm_attn_workspace_bytes(ctypes.byref(dims), rows, ctypes.byref(nbytes)) == 1
+    # a bound on any agent's rows sizes the query tiles: 12 rows, at most 3 per agent -> 1 tile
+    hinted = Q.AttnDims(48, 8, 4, 400, 1600, 3)
+    assert lib.qmm_attn_workspace_bytes(ctypes.byref(hinted), 12, ctypes.byref(nbytes)) == 0
+    assert nbytes.value == 4 * 8 * 31 * 1 * 24 * 132 * 4
+    hinted = Q.AttnDims(48, 8, 4, 400, 1600, 50)  # a bound above the rows changes nothing
+    assert lib.qmm_attn_workspace_bytes(ctypes.byref(hinted), 12, ctypes.byref(nbytes)) == 0
+    assert nbytes.value == 4 * 8 * 31 * 3 * 24 * 132 * 4
+    for bad in (Q.AttnDims(48, 8, 4, 400, 1600, -1), Q.AttnDims(48, 8, 4, 400, 1600, 0, 1)):
+        assert lib.qmm_attn_workspace_bytes(ctypes.byref(bad), 12, ctypes.byref(nbytes)) == 1
     buf = (ctypes.c_uint8 * 64)()
     assert lib.qmm_attn_decode(ctypes.byref(dims), None, buf, buf, buf, buf, 1, buf, buf, 10**9, buf, None) == 1
     assert lib.qmm_attn_decode(ctypes.byref(dims), buf, buf, buf, buf, buf, 0, buf, buf, 10**9, buf, None) == 1

@@ -17,7 +17,7 @@ def agent_rows_of(ra, agents):
     return np.concatenate([[0], np.cumsum(np.bincount(np.asarray(ra), minlength=agents))]).astype(np.int32)
 
 
-def run_attn(pool, table, q, ra, rl, kvh, agent_rows=None):
+def run_attn(pool, table, q, ra, rl, kvh, agent_rows=None, max_agent_rows=0):
     from bit_weight_streaming_q4_gb300.qmm import attn_decode
     torch = torch_cuda()
     table = np.ascontiguousarray(table, dtype=np.int32)
@@ -29,7 +29,7 @@ def run_attn(pool, table, q, ra, rl, kvh, agent_rows=None):
     rl_d = torch.from_numpy(np.ascontiguousarray(rl, dtype=np.int32)).cuda()
     q_d = torch.from_numpy(np.ascontiguousarray(q).view(np.int16)).cuda().view(torch.float16)
     out = torch.full(q.shape, float("nan"), dtype=torch.float32, device="cuda")
-    err = attn_decode(pool_d, table_d, ar_d, rl_d, q_d, out, kvh)
+    err = attn_decode(pool_d, table_d, ar_d, rl_d, q_d, out, kvh, max_agent_rows=max_agent_rows)
     torch.cuda.synchronize()
     return out.cpu().numpy(), int(err.item())
 
@@ -116,6 +116,24 @@ def test_attention_query_tiles_match_narrow_batches():
     sub = np.ascontiguousarray(q[sel])
     part, _ = run_attn(pool, table, sub, ra[sel], rl[sel], kvh)
     assert np.array_equal(part.view(np.uint32), full[sel].view(np.uint32))
+
+
+def test_attention_agent_row_bound():
+    """With a bound on any agent's rows the workspace and grid hold fewer query tiles; results
+    are the same bits, and an agent above the bound is reported (4) with zero outputs while
+    the others are computed."""
+    pool, table, q, ra, rl, kvh = case((700, 130, 2500), 3, 48, 8, seed=8)
+    full, _ = run_attn(pool, table, q, ra, rl, kvh)
+    hinted, err = run_attn(pool, table, q, ra, rl, kvh, max_agent_rows=3)
+    assert err == 0
+    assert np.array_equal(hinted.view(np.uint32), full.view(np.uint32))
+    pool, table, q, ra, rl, kvh = case((700, 130), 6, 48, 8, seed=9)
+    keep = np.r_[np.where(ra == 0)[0], np.where(ra == 1)[0][:3]]  # 6 rows of agent 0, 3 of agent 1
+    got, err = run_attn(pool, table, q[keep], ra[keep], rl[keep], kvh, max_agent_rows=4)
+    assert err & 4
+    assert np.all(got[:6] == 0)
+    ref, s = oracle.attn(pool, table, q[keep[6:]], ra[keep[6:]], rl[keep[6:]], kvh)
+    assert np.all(np.abs(got[6:] - ref) <= 2e-3 * s + 1e-6)
 
 
 def test_attention_bad_page_is_reported():
