@@ -117,6 +117,9 @@ __device__ __forceinline__ void mma_m16n8k16_z(float (&d)[4], uint32_t a0, uint3
 
 __global__ void __launch_bounds__(kThreads, 4) attn_partial(const Params p) {
     extern __shared__ __align__(128) uint8_t sm[];
+    // the combine kernel may be scheduled as soon as every CTA of this grid has started; it
+    // waits for the whole grid (and its writes) before reading the workspace
+    griddep_launch_dependents();
     // ring slot i % kStages holds page i
     __half* P = reinterpret_cast<__half*>(sm + kStages * kRec);       // [kMaxQ][kPS] probabilities
     float* red_max = reinterpret_cast<float*>(P + kMaxQ * kPS);       // [kMaxQ][4 warps]
@@ -452,6 +455,7 @@ __global__ void __launch_bounds__(kThreads, 4) attn_partial(const Params p) {
 // One warp per (row, head): the partials of its (agent, KV head, query tile) merged in run
 // order; lane l writes dims 4l .. 4l + 3.
 __global__ void attn_combine(const Params p) {
+    griddep_wait();  // the partial kernel has finished and its partials are visible
     const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (w >= p.rows * p.heads) return;
@@ -612,9 +616,18 @@ qmm_status qmm_attn_decode(const qmm_attn_dims* dims, const void* pool, const in
                     static_cast<unsigned>(p.max_qt));
     qmm::attn::attn_partial<<<grid, qmm::attn::kThreads, qmm::attn::kSmem, s>>>(p);
     if (cudaGetLastError() != cudaSuccess) return QMM_ERR_CUDA;
-    const int64_t n = rows * dims->heads * 32;  // one warp per (row, head)
-    qmm::attn::attn_combine<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return QMM_ERR_CUDA;
+    // one warp per (row, head), launched as a programmatic dependent of the partial kernel
+    const int64_t n = rows * dims->heads * 32;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((n + 255) / 256));
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, qmm::attn::attn_combine, p) != cudaSuccess) return QMM_ERR_CUDA;
     return QMM_OK;
 }
 
