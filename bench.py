@@ -695,10 +695,38 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------------------- replicas
+# With N GPUs the step runs as N independent replicas (one process per GPU, nothing of the
+# data path crosses ranks): the timed region is bracketed by a barrier on every rank, the
+# time is the maximum over ranks, and the job's figure counts the work of all ranks.
+def ranks_barrier(world: int, cuda: bool) -> None:
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    if cuda:
+        torch.cuda.synchronize()
+
+
+def ranks_max(t: float, world: int, device: str) -> float:
+    """The largest of the ranks' values of t (every rank gets it)."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        tt = torch.tensor([t], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t = float(tt.item())
+    return t
+
+
+def job_gbs(weight_bytes_per_step: int, steps: int, world: int, seconds: float) -> float:
+    """Weight GB/s of the whole job: every rank streams the step's weights once per step."""
+    return weight_bytes_per_step * steps * world / seconds / 1e9
+
+
 # ------------------------------------------------------------------------------- our arm
 def run_ours(args, rank, world, local_rank):
     import torch
-    import torch.distributed as dist
     from bit_weight_streaming_q4_gb300 import Step
     from bit_weight_streaming_q4_gb300.qmm import STEP_INDEPENDENT
 
@@ -714,16 +742,10 @@ def run_ours(args, rank, world, local_rank):
     n_mats = len(stack.mats)
 
     def barrier():
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
+        ranks_barrier(world, cuda=True)
 
     def max_over_ranks(t):
-        if world > 1:
-            tt = torch.tensor([t], device="cuda")
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            t = float(tt.item())
-        return t
+        return ranks_max(t, world, "cuda")
 
     def make_step(m, flags, xs=None, ys=None):
         with torch.cuda.stream(stream):
@@ -757,7 +779,7 @@ def run_ours(args, rank, world, local_rank):
     clocks = clk.summary()
     wb, xb, yb = stack.bytes_for(HEADLINE_M)
     step_s = t / args.steps
-    value = wb * args.steps * world / t / 1e9
+    value = job_gbs(wb, args.steps, world, t)
     alg_bytes = wb + xb + yb
     achieved = alg_bytes / step_s / 1e9
     parity = None
