@@ -48,3 +48,23 @@ def test_repeat_determinism(backend):
     ref = bits(run(q, x))
     for _ in range(100):
         assert np.array_equal(bits(run(q, x)), ref)
+
+
+@pytest.mark.parametrize("mat", [synth.Matrix("wide_a", 1000, 2560, 78), synth.SWEEP_MATRICES[1]],
+                         ids=lambda m: m.name)
+def test_wide_launches_match_narrow_ones(mat):
+    """tcgen05 handles of 200 rows: a 200-row run is one 128-row launch (whose activation sums
+    come from the pre-pass, and whose dequantisation warps get more registers) and one of 72
+    rows; every row equals, bit for bit, the same row run in 1-, 16-, 32- and 64-row batches
+    (whose sums the dequantisation warps form themselves)."""
+    blocks = synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id)
+    x = synth.x_f16(200, mat.k, seed=0, tensor_id=synth.X_ID_OFFSET + mat.tensor_id)
+    q = make(blocks, m_max=200, backend=2)
+    full = bits(run(q, x))
+    for m in (1, 16, 32, 64, 65, 100, 127, 128, 129):
+        assert np.array_equal(bits(run(q, x[:m])), full[:m]), m
+    for parts in ([1] * 8, [16, 32, 64, 88], [129, 71], [7, 121, 72]):
+        r0 = 0
+        for p in parts:
+            assert np.array_equal(bits(run(q, x[r0:r0 + p])), full[r0:r0 + p]), (parts, r0)
+            r0 += p

@@ -38,9 +38,11 @@ def test_m_sweep_full_matrices(mat, backend):
 @pytest.mark.parametrize("n,k,m", [
     (1, 256, 1), (33, 256, 3), (40, 512, 5), (100, 768, 9), (257, 1024, 16), (31, 2560, 12),
     (5, 256, 17), (64, 4096, 8), (96, 256, 2), (500, 1280, 13), (1000, 512, 16), (77, 7680, 7),
+    (300, 768, 65), (129, 512, 128), (700, 1024, 129), (33, 2304, 200),
 ])
 def test_ragged_shapes(n, k, m, backend):
-    """Several tiles, ragged row tails, tiles split between CTAs, M chunked past 16."""
+    """Several tiles, ragged row tails, tiles split between CTAs, M chunked past 16 (mma.sync)
+    and past 128 (tcgen05), and the 64- and 128-row launch widths."""
     blocks = synth.q4k_matrix(n, k, seed=1, tensor_id=n * 7 + k)
     x = synth.x_f16(m, k, seed=1, tensor_id=n + k + m)
     y_ref, s_ref = oracle.qmm(blocks, x)
