@@ -35,12 +35,12 @@ import synth  # noqa: E402
 
 METRIC = "Q4K x M-row decode GEMM: weight GB/s (% of HBM peak) and step tok/s at M=1/12/64"
 # DRAM bytes per work unit of each backend's persistent step launch, measured by ncu
-# (profiles/stream_kernel_step_m12.md, profiles/tc_kernel_step_m12.md); each is valid only for
+# (profiles/stream_kernel_lm_head_m1.md, profiles/tc_kernel_step_m12.md); each is valid only for
 # the kernel source it was taken from
 TRAFFIC_PER_UNIT = {
     1: {"source": "bit_weight_streaming_q4_gb300/csrc/qmm_b1.cu",
-        "sha256": "43d77ce69d57d591d1ae8852fdc3a0d12692e52edc2c34708f401cbef0162db2",
-        "bytes": 37194.0},
+        "sha256": "8d28a050a994dd9106b4b8910343f214052ff97fd60f0c2f856f2a85a98513a5",
+        "bytes": 37208.9},
     2: {"source": "bit_weight_streaming_q4_gb300/csrc/qmm_b2.cu",
         "sha256": "9d85db3f16d473e7c7f934b4bc7aeac168090d8330a7a06fc39e50c4a501260e",
         "bytes": 18585.1},
