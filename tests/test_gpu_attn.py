@@ -143,3 +143,41 @@ def test_attention_bad_page_is_reported():
     table[0, 1] = 10**6
     _, err = run_attn(pool, table, q, ra, rl, kvh)
     assert err & 2
+
+
+def _set_scales(pool, kvh, which, values):
+    """Overwrite the K (which = 0) or V (which = 1) block scales of every record."""
+    recs = pool.reshape(-1, synth.KV_RECORD_BYTES)
+    off = 8192 if which == 0 else 16896
+    recs[:, off:off + 512] = values.astype(np.float16).view(np.uint8).reshape(len(recs), 512)
+
+
+def test_attention_peaked_softmax():
+    """Queries scaled by 24 make the softmax nearly one-hot (score gaps of tens), the case where
+    the running maximum moves most between pages."""
+    pool, table, q, ra, rl, kvh = case((900, 3000), 3, 48, 8, seed=10)
+    q = (q.astype(np.float32) * 24).astype(np.float16)
+    check(pool, table, q, ra, rl, kvh, what="peaked")
+
+
+def test_attention_v_scales_near_the_bound():
+    """V block scales up to 250 (the documented bound is 255: probabilities carry 2^8) and K
+    scales spread over four decades."""
+    pool, table, q, ra, rl, kvh = case((700, 1500), 3, 48, 8, seed=11)
+    n = pool.size // synth.KV_RECORD_BYTES
+    rng = np.random.default_rng(11)
+    _set_scales(pool, kvh, 1, rng.uniform(100.0, 250.0, size=(n, 256)))
+    _set_scales(pool, kvh, 0, 10.0 ** rng.uniform(-4.0, 0.0, size=(n, 256)))
+    check(pool, table, q, ra, rl, kvh, what="large V scales")
+
+
+def test_attention_misaligned_output_is_refused():
+    from bit_weight_streaming_q4_gb300.qmm import attn_decode
+    torch = torch_cuda()
+    pool, table, q, ra, rl, kvh = case((100,), 2, 16, 8, seed=12)
+    buf = torch.zeros(q.size + 1, dtype=torch.float32, device="cuda")
+    out = buf[1:].view(q.shape)  # 4 bytes past a 16-byte boundary
+    with pytest.raises(RuntimeError):
+        attn_decode(torch.from_numpy(pool).cuda(), torch.from_numpy(np.ascontiguousarray(table)).cuda(),
+                    torch.from_numpy(agent_rows_of(ra, table.shape[0])).cuda(), torch.from_numpy(rl).cuda(),
+                    torch.from_numpy(q.view(np.int16)).cuda().view(torch.float16), out, kvh)
