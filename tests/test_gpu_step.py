@@ -78,9 +78,12 @@ def test_independent_step_parity_and_repeatability(backend, m):
     step.close()
 
 
-@pytest.mark.parametrize("backend_ms", [(1, (16, 9, 3)), (2, (64, 40, 17, 5))], ids=["mma_sync", "tcgen05"])
+@pytest.mark.parametrize("backend_ms", [(1, (16, 9, 3)), (2, (64, 40, 17, 5)), (2, (128, 100, 65, 64, 17))],
+                         ids=["mma_sync", "tcgen05", "tcgen05-wide"])
 def test_independent_step_rows_do_not_depend_on_m(backend_ms):
-    """The persistent step's rows are bit-identical whatever the number of rows of the step."""
+    """The persistent step's rows are bit-identical whatever the number of rows of the step,
+    including steps of more than 64 rows, whose activation sums come from a pre-pass over all
+    the step's matrices."""
     from bit_weight_streaming_q4_gb300 import Step
     torch = torch_cuda()
     be, ms = backend_ms
@@ -101,8 +104,8 @@ def test_independent_step_rows_do_not_depend_on_m(backend_ms):
             assert np.array_equal(a[:m].view(np.uint32), b.view(np.uint32))
 
 
-@pytest.mark.parametrize("be_m", [(1, 1), (1, 8), (1, 16), (2, 24), (2, 64)],
-                         ids=["mma_sync-1", "mma_sync-8", "mma_sync-16", "tcgen05-24", "tcgen05-64"])
+@pytest.mark.parametrize("be_m", [(1, 1), (1, 8), (1, 16), (2, 24), (2, 64), (2, 100)],
+                         ids=["mma_sync-1", "mma_sync-8", "mma_sync-16", "tcgen05-24", "tcgen05-64", "tcgen05-100"])
 def test_persistent_step_many_small_matrices(be_m):
     """Forty matrices, most smaller than one unit per CTA, in one persistent launch: pieces of
     one or two units, row tiles that only one of the tensor-core issuers touches."""
