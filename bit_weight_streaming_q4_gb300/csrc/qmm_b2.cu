@@ -33,7 +33,9 @@
 //               one per issuing warp, double-buffered per row tile.  A single thread
 //               cannot keep the tensor core busy: after a burst of MMAs its next
 //               shared-memory access (the mbarrier wait for the next unit) stalls until the
-//               burst has drained, so two issuers take turns;
+//               burst has drained, so two issuers take turns.  At MP = 64 (Q4_K) a group
+//               hands each unit over in two halves: the issuer starts the MMAs of
+//               sub-blocks 0-3 while the group still dequantises sub-blocks 4-7;
 //   warps 11-14 epilogue: the sum of the two accumulators -> y, a split-K partial, or the
 //               reduction of a split row tile; warp 11 also publishes the CTA's partial and
 //               resets the ticket of the tile it reduced.
@@ -122,7 +124,13 @@ struct Cfg {
     static constexpr int kXsOff = kWOff + kWRing * kUnitBytes;
     static constexpr int kBlOff = kXsOff + kXRing * kXsBytes;
     static constexpr int kBarOff = kBlOff + (kMin ? kNA * kBlBytes : 0);
-    static constexpr int kNumBars = 2 * kWRing + 2 * kXRing + 2 * kTB + 4 + 2 + 2 + 1;
+    // Half-unit hand-off: the group signals sub-blocks 0-3 of a unit (tfull_lo) before it
+    // writes 4-7, and the issuer runs their 8 MMAs meanwhile.  Measured on this GB300 with
+    // identical outputs: +4-5 % at MP = 64, but -9 % at MP = 16, -3 % at MP = 32 and MP = 128,
+    // where the issuer's extra wait right after a burst of MMAs costs more than it saves.
+    static constexpr bool kSplit = F == QMM_FORMAT_Q4_K && MP == 64;
+    static_assert(!kSplit || !kIssuerWaitsX, "the first half's MMAs rely on the group's wait for the x tile");
+    static constexpr int kNumBars = 2 * kWRing + 2 * kXRing + 2 * kTB + 4 + 2 + 2 + 1 + (kSplit ? kTB : 0);
     // argmax launches: the epilogue warps' best keys, [warp 4][token MP]
     static constexpr int kAmaxOff = kBarOff + kNumBars * 8 + 16;
     static constexpr int kSmem = kAmaxOff + 4 * MP * 8 + 1024;  // + alignment slack
@@ -319,7 +327,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* evred = evpart + 1;       // ... have read the partials of the tile they reduced
     uint64_t* mmadone = evred + 1;      // [2]: every MMA of issuer e has finished
     uint64_t* evamax = mmadone + 2;     // argmax launches: the four epilogue warps' keys are in
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(evamax + 1);
+    // [kTB], kSplit only: sub-blocks 0-3 of the unit's A buffer are written (the other widths
+    // keep the shared-memory layout without them)
+    uint64_t* tfull_lo = evamax + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull_lo + (C::kSplit ? kTB : 0));
     unsigned long long* amax_sm = reinterpret_cast<unsigned long long*>(smem + C::kAmaxOff);
     volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] abort
 
@@ -364,6 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < kTB; ++i) {
             mbar_init(&tfull[i], 4);
+            if (C::kSplit) mbar_init(&tfull_lo[i], 4);
             mbar_init(&tempty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -529,6 +541,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int xs = static_cast<int>(j % kXRing);
                     const int a = static_cast<int>(j % C::kNA);
                     const int tb = static_cast<int>(j % kTB);
+                    const uint32_t xaddr = smem_u32(xring + xs * C::kXSlot);
+                    if constexpr (C::kSplit) {
+                        // sub-blocks 0-3 (k-steps 0-7) as soon as they are written; the x tile
+                        // is in, since the group waited for it before forming the sums
+                        if (!warp_wait(&tfull_lo[tb], (j / kTB) & 1, flags)) {
+                            live = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (lane == 0) {
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint64_t bdesc = smem_desc_sw128(xaddr + (kk >> 2) * C::kXBox + (kk & 3) * 32);
+                                tc_mma_f16_ts(d_tmem, tbase + a * kACols + 8 * kk, bdesc, kIdesc, (!fresh || kk > 0) ? 1u : 0u);
+                            }
+                        }
+                        __syncwarp();
+                    }
                     if (!warp_wait(&tfull[tb], (j / kTB) & 1, flags)) {
                         live = false;
                         break;
@@ -539,9 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     if (lane == 0) {
-                        const uint32_t xaddr = smem_u32(xring + xs * C::kXSlot);
 #pragma unroll
-                        for (int kk = 0; kk < 16; ++kk) {
+                        for (int kk = C::kSplit ? 8 : 0; kk < 16; ++kk) {
                             const uint64_t bdesc = smem_desc_sw128(xaddr + (kk >> 2) * C::kXBox + (kk & 3) * 32);
                             tc_mma_f16_ts(d_tmem, tbase + a * kACols + 8 * kk, bdesc, kIdesc, (!fresh || kk > 0) ? 1u : 0u);
                         }
@@ -836,6 +865,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dq_word(qv[sb].z, s1, n1, s16, n16, d2, nbh, out + 8);
                     dq_word(qv[sb].w, s1, n1, s16, n16, d2, nbh, out + 12);
                     tmem_st16(tcol + 16 * sb, out);
+                    if (C::kSplit && sb == 3) {
+                        tc_wait_st();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&tfull_lo[j % kTB]);
+                    }
                 }
                 // the -B_l step's A row: k slots 0..7 = sub-blocks 0..7 (slots 8..15 stay zero)
                 *reinterpret_cast<uint4*>(blt + a * kBlBytes + (row >> 3) * 256 + (row & 7) * 16) =
