@@ -42,8 +42,8 @@ TRAFFIC_PER_UNIT = {
         "sha256": "8d28a050a994dd9106b4b8910343f214052ff97fd60f0c2f856f2a85a98513a5",
         "bytes": 37208.9},
     2: {"source": "bit_weight_streaming_q4_gb300/csrc/qmm_b2.cu",
-        "sha256": "e8c448810dafe330afe5e0f23f1384ea5e55c979a80dc7ceba3db2697284d7e2",
-        "bytes": 18581.6},
+        "sha256": "3f984e5678a61fc87b0b638fe98485b979dda78a02ab8d90c2d0f8d9ff4f03ed",
+        "bytes": 18581.7},
 }
 KERNEL_NAME = {1: "qmm::b1::stream_kernel<2>", 2: "qmm::b2::tc_kernel<16>"}
 HEADLINE_M = 12

@@ -542,6 +542,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int a = static_cast<int>(j % C::kNA);
                     const int tb = static_cast<int>(j % kTB);
                     const uint32_t xaddr = smem_u32(xring + xs * C::kXSlot);
+                    // the start-address field is bits 0-13 (address / 16); shared-memory
+                    // addresses stay below 256 KB, so the constant offsets never carry out of it
+                    const uint64_t bdesc0 = smem_desc_sw128(xaddr);
+                    const uint32_t abase = tbase + a * kACols;
                     if constexpr (C::kSplit) {
                         // sub-blocks 0-3 (k-steps 0-7) as soon as they are written; the x tile
                         // is in, since the group waited for it before forming the sums
@@ -553,8 +557,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (lane == 0) {
 #pragma unroll
                             for (int kk = 0; kk < 8; ++kk) {
-                                const uint64_t bdesc = smem_desc_sw128(xaddr + (kk >> 2) * C::kXBox + (kk & 3) * 32);
-                                tc_mma_f16_ts(d_tmem, tbase + a * kACols + 8 * kk, bdesc, kIdesc, (!fresh || kk > 0) ? 1u : 0u);
+                                const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(((kk >> 2) * C::kXBox + (kk & 3) * 32) >> 4);
+                                tc_mma_f16_ts(d_tmem, abase + 8 * kk, bdesc, kIdesc, (!fresh || kk > 0) ? 1u : 0u);
                             }
                         }
                         __syncwarp();
@@ -571,8 +575,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) {
 #pragma unroll
                         for (int kk = C::kSplit ? 8 : 0; kk < 16; ++kk) {
-                            const uint64_t bdesc = smem_desc_sw128(xaddr + (kk >> 2) * C::kXBox + (kk & 3) * 32);
-                            tc_mma_f16_ts(d_tmem, tbase + a * kACols + 8 * kk, bdesc, kIdesc, (!fresh || kk > 0) ? 1u : 0u);
+                            const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(((kk >> 2) * C::kXBox + (kk & 3) * 32) >> 4);
+                            tc_mma_f16_ts(d_tmem, abase + 8 * kk, bdesc, kIdesc, (!fresh || kk > 0) ? 1u : 0u);
                         }
                         if constexpr (C::kMin)
                             tc_mma_f16_ss(d_tmem, smem_desc_k16(smem_u32(blt + a * kBlBytes), 128, 256),
