@@ -89,6 +89,7 @@ qmm_status launch_run(qmm_handle h, const void* x, int64_t m, float* y, cudaStre
             p.err = h->err_dev;
             p.units = h->d.units;
             p.count = 1;
+            p.wait_ns = h->wait_ns;
             p.m = static_cast<int32_t>(mc);
             p.ws_cols = tc ? qmm::b2::mp_for(mc) : h->ws_cols;
             if (idx) {
@@ -100,9 +101,12 @@ qmm_status launch_run(qmm_handle h, const void* x, int64_t m, float* y, cudaStre
             // the activation sums first, as a plain launch: that also keeps them from
             // overwriting the sums the handle's previous launch may still be reading
             if (pre) e = qmm::b2::presum(mat, p, static_cast<int32_t>(h->d.kb), s);
+            // the mma.sync kernel's split-K reducer waits for the partials of CTAs after it, so
+            // its CTAs must be co-resident: a cooperative launch (the tcgen05 kernel's last-
+            // arriver reduction waits for no other CTA)
             if (e == cudaSuccess)
-                e = tc ? qmm::b2::launch(mat, p, h->d.grid, s, pdl, false, h->format)
-                       : qmm::b1::launch(mat, p, h->d.grid, s, pdl, false);
+                e = tc ? qmm::b2::launch(mat, p, h->d.grid, s, pdl, h->format)
+                       : qmm::b1::launch(mat, p, h->d.grid, s, pdl, true);
         }
         if (e != cudaSuccess) return QMM_ERR_CUDA;
     }
@@ -120,6 +124,7 @@ void qmm_default_options(qmm_options* opt) {
     opt->ctas_per_sm = 0;
     opt->host_io = 0;
     opt->format = QMM_FORMAT_Q4_K;
+    opt->wait_limit_us = 0;
 }
 
 const char* qmm_status_str(qmm_status s) {
@@ -145,7 +150,7 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
     qmm_options opt;
     qmm_default_options(&opt);
     if (opt_in) opt = *opt_in;
-    if (opt.m_max < 1 || opt.ctas_per_sm < 0 || opt.ctas_per_sm > 4 || opt.backend < 0 ||
+    if (opt.m_max < 1 || opt.ctas_per_sm < 0 || opt.ctas_per_sm > 4 || opt.backend < 0 || opt.wait_limit_us < 0 ||
         opt.backend > QMM_BACKEND_TCGEN05 || opt.format < QMM_FORMAT_Q4_K || opt.format > QMM_FORMAT_Q8_0)
         return QMM_ERR_INVALID_ARG;
     // the mma.sync backend streams Q4_K only
@@ -179,6 +184,7 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
         h->backend = opt.backend;
     const bool tc = h->backend == QMM_BACKEND_TCGEN05;
     h->m_max = opt.m_max;
+    h->wait_ns = opt.wait_limit_us ? static_cast<uint64_t>(opt.wait_limit_us) * 1000u : qmm::kDefaultWaitNs;
     qmm::Decomp& d = h->d;
     d.n = n;
     d.k = k;
@@ -207,10 +213,11 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
         return code;
     };
     if (cudaMalloc(&h->wq, h->wq_bytes) != cudaSuccess) return fail(QMM_ERR_OOM);
-    // split-K partial slots, one per CTA: 128 rows x up to 128 columns (tcgen05), or the
-    // accumulators of the 128 consumer threads (mma.sync)
-    const size_t ws_bytes = static_cast<size_t>(d.grid) * (tc ? qmm::b2::kRows : qmm::b1::kConsumerThreads) *
-                            h->ws_cols * sizeof(float);
+    // split-K partial slots: two per CTA of 128 rows x up to 128 columns (tcgen05), or one per
+    // CTA holding the accumulators of the 128 consumer threads (mma.sync)
+    const size_t ws_bytes =
+        (tc ? static_cast<size_t>(qmm::b2::ws_floats(d.grid, h->ws_cols))
+            : static_cast<size_t>(d.grid) * qmm::b1::kConsumerThreads * h->ws_cols) * sizeof(float);
     if (cudaMalloc(&h->ws, ws_bytes) != cudaSuccess) return fail(QMM_ERR_OOM);
     if (cudaMalloc(&h->tickets, d.tiles * sizeof(int)) != cudaSuccess) return fail(QMM_ERR_OOM);
     if (cudaMemsetAsync(h->tickets, 0, d.tiles * sizeof(int), s) != cudaSuccess) return fail(QMM_ERR_CUDA);
@@ -313,9 +320,9 @@ qmm_status qmm_get_info(qmm_handle h, qmm_info* info) {
     info->rows_per_unit = h->d.rows;
     info->weight_bytes = h->d.n * (h->d.k / qmm::block_weights(h->format)) * qmm::block_bytes(h->format);
     info->packed_bytes = h->wq_bytes;
-    info->workspace_bytes = static_cast<int64_t>(h->d.grid) *
-                                (h->backend == QMM_BACKEND_TCGEN05 ? qmm::b2::kRows : qmm::b1::kConsumerThreads) *
-                                h->ws_cols * 4 +
+    info->workspace_bytes = (h->backend == QMM_BACKEND_TCGEN05
+                                 ? qmm::b2::ws_floats(h->d.grid, h->ws_cols)
+                                 : static_cast<int64_t>(h->d.grid) * qmm::b1::kConsumerThreads * h->ws_cols) * 4 +
                             h->d.tiles * 4;
     info->m_per_launch = per_launch(h);
     info->format = h->format;
@@ -339,9 +346,9 @@ qmm_status qmm_destroy(qmm_handle h) {
 struct qmm_step_s {
     cudaGraph_t graph = nullptr;  // launch-per-run path (tcgen05 handles, or more than 16 rows)
     cudaGraphExec_t exec = nullptr;
-    // persistent path: every matrix in one cooperative launch of the mma.sync kernel
+    // persistent path: every matrix in one launch (cooperative for the mma.sync kernel)
     qmm::MatDesc* mats = nullptr;   // device
-    int32_t* first_mat = nullptr; // device, [grid]
+    int32_t* first_mat = nullptr; // device, [grid]: the matrix of each CTA's first unit
     float* ws = nullptr;          // split-K partial slots, one per CTA
     bool tcgen05 = false;         // the backend of every handle of a persistent step
     bool presum = false;          // ... whose activation sums come from a pre-pass
@@ -381,9 +388,9 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
     }
     qmm_step st = new (std::nothrow) qmm_step_s();
     if (!st) return QMM_ERR_OOM;
-    // One persistent kernel for the whole step when the runs are independent, every handle is
-    // an mma.sync handle and M fits one launch (unless QMM_STEP_GRAPH asks for the graph); a
-    // CUDA graph of runs otherwise.
+    // One persistent kernel for the whole step when the runs are independent, every handle has
+    // the same backend and block format and M fits one launch (16 rows mma.sync, 128 tcgen05),
+    // unless QMM_STEP_GRAPH asks for the graph; a CUDA graph of runs otherwise.
     const int32_t be = handles[0]->backend;
     const bool tc = be == QMM_BACKEND_TCGEN05;
     bool persistent = m <= (tc ? qmm::b2::kMaxM : qmm::b1::kMaxM) && !(flags & QMM_STEP_GRAPH) &&
@@ -440,8 +447,9 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
             firsts[c] = i;
         }
         const int32_t ws_cols = tc ? qmm::b2::mp_for(m) : qmm::b1::ws_floats(m);
-        const size_t ws_bytes = static_cast<size_t>(grid) * (tc ? qmm::b2::kRows : qmm::b1::kConsumerThreads) *
-                                ws_cols * sizeof(float);
+        const size_t ws_bytes =
+            (tc ? static_cast<size_t>(qmm::b2::ws_floats(grid, ws_cols))
+                : static_cast<size_t>(grid) * qmm::b1::kConsumerThreads * ws_cols) * sizeof(float);
         if (rc == QMM_OK && cudaMalloc(&st->mats, sizeof(qmm::MatDesc) * count) != cudaSuccess) rc = QMM_ERR_OOM;
         if (rc == QMM_OK && cudaMalloc(&st->first_mat, sizeof(int32_t) * firsts.size()) != cudaSuccess) rc = QMM_ERR_OOM;
         if (rc == QMM_OK && cudaMalloc(&st->ws, ws_bytes) != cudaSuccess) rc = QMM_ERR_OOM;
@@ -467,6 +475,7 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
             st->params.err = st->err_dev;
             st->params.units = total;
             st->params.count = count;
+            st->params.wait_ns = handles[0]->wait_ns;
             st->params.m = static_cast<int32_t>(m);
             st->params.ws_cols = ws_cols;
         }
@@ -510,7 +519,7 @@ qmm_status qmm_step_launch(qmm_step s, void* stream) {
         const qmm::MatDesc unused = {};
         cudaError_t e = s->presum ? qmm::b2::presum(unused, s->params, s->max_kb, cs) : cudaSuccess;
         if (e == cudaSuccess)
-            e = s->tcgen05 ? qmm::b2::launch(unused, s->params, s->grid, cs, true, true, s->format)
+            e = s->tcgen05 ? qmm::b2::launch(unused, s->params, s->grid, cs, true, s->format)
                            : qmm::b1::launch(unused, s->params, s->grid, cs, true, true);
         return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
     }

@@ -143,19 +143,19 @@ struct Cursor {
 };
 
 // Bounded spin until *p >= target (acquire).  False on timeout or when the CTA aborts.
-__device__ __forceinline__ bool wait_count(const int* p, int target, volatile int* flags) {
+__device__ __forceinline__ bool wait_count(const int* p, int target, volatile int* flags, uint64_t lim) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 0;; ++it) {
         if (ld_acquire_gpu(p) >= target) return true;
         if (flags[0]) return false;
-        if ((it & 63u) == 63u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if ((it & 7u) == 7u && globaltimer_ns() - t0 > lim) return false;
         __nanosleep(64);
     }
 }
 
 // mbarrier wait whose outcome the whole warp agrees on (all lanes call it).
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* flags) {
-    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, flags));
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* flags, uint64_t lim) {
+    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, flags, lim));
 }
 
 template <int NT>
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             const uint8_t* src = nullptr;  // the current matrix's next unit
             while (w.i < count) {
                 const int s = static_cast<int>(wseq % kWRing);
-                if (wseq >= kWRing && !mbar_wait_bounded(&wempty[s], ((wseq / kWRing) - 1) & 1, flags)) {
+                if (wseq >= kWRing && !mbar_wait_bounded(&wempty[s], ((wseq / kWRing) - 1) & 1, flags, p.wait_ns)) {
                     ok = false;
                     break;
                 }
@@ -313,8 +313,8 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         for (int64_t j = 0; cc.i < count; ++j, next(cc)) {
             const int xs = static_cast<int>(j % kXRing);
             const int fs = static_cast<int>(j % kFRing);
-            bool ok = j < kFRing || warp_wait(&fempty[fs], ((j / kFRing) - 1) & 1, flags);
-            ok = ok && warp_wait(&myfull[xs], (j / kXRing) & 1, flags);
+            bool ok = j < kFRing || warp_wait(&fempty[fs], ((j / kFRing) - 1) & 1, flags, p.wait_ns);
+            ok = ok && warp_wait(&myfull[xs], (j / kXRing) & 1, flags, p.wait_ns);
             if (!ok) {
                 if (lane == 0) fail(p.err, flags);
                 break;
@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         if (lane == 0) {
             int64_t ev = 0;
             bool ok = true;
-            auto take = [&]() -> bool { return mbar_wait_bounded(&evfull[ev % kEv], (ev / kEv) & 1, flags); };
+            auto take = [&]() -> bool { return mbar_wait_bounded(&evfull[ev % kEv], (ev / kEv) & 1, flags, p.wait_ns); };
             auto give = [&]() {
                 mbar_arrive(&evempty[ev % kEv]);
                 ++ev;
@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     auto post = [&]() -> bool {  // hand an event to the helper (after this warp's writes)
         const int e = static_cast<int>(ev % kEv);
         __syncwarp();
-        if (ev >= kEv && !warp_wait(&evempty[e], ((ev / kEv) - 1) & 1, flags)) {
+        if (ev >= kEv && !warp_wait(&evempty[e], ((ev / kEv) - 1) & 1, flags, p.wait_ns)) {
             if (lane == 0) fail(p.err, flags);
             return false;
         }
@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             for (int64_t j = ja; j < jb; ++j, ++gseq) {
                 const int s = static_cast<int>(gseq % kWRing);
                 const int fs = static_cast<int>(gseq % kFRing);
-                if (!warp_wait(&wfull[s], (gseq / kWRing) & 1, flags)) {
+                if (!warp_wait(&wfull[s], (gseq / kWRing) & 1, flags, p.wait_ns)) {
                     if (lane == 0) fail(p.err, flags);
                     live = false;
                     break;
@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                     for (int h = 0; h < 2; ++h)
                         qv[r][h] = lds128(myq + (((r * 2 + h) * 2 + 0) * 32 + lane) * 16);
 
-                if (!warp_wait(&ffull[fs], (gseq / kFRing) & 1, flags)) {
+                if (!warp_wait(&ffull[fs], (gseq / kFRing) & 1, flags, p.wait_ns)) {
                     if (lane == 0) fail(p.err, flags);
                     live = false;
                     break;
@@ -574,7 +574,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                 // wait for the partials of pieces pa+1..pb, then add them in that order
                 const int64_t pb = dev_piece_of(base + (tile + 1) * KB - 1, U, P);
                 bool got = true;
-                if (lane == 0) got = wait_count(M.tickets + tile, static_cast<int>(pb - pa), flags);
+                if (lane == 0) got = wait_count(M.tickets + tile, static_cast<int>(pb - pa), flags, p.wait_ns);
                 if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
                     if (lane == 0) fail(p.err, flags);
                     live = false;

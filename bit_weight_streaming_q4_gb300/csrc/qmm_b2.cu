@@ -39,9 +39,11 @@
 //   warps 11-14 epilogue: the sum of the two accumulators -> y, a split-K partial, or the
 //               reduction of a split row tile; warp 11 also publishes the CTA's partial and
 //               resets the ticket of the tile it reduced.
-// Decomposition as in the mma.sync backend: a launch concatenates its matrices' unit
-// sequences, CTA c takes [c*U/P, (c+1)*U/P), and a row tile cut between CTAs pa..pb is
-// reduced by pa in piece order.  Nothing in any output's arithmetic depends on M.
+// Decomposition: a launch concatenates its matrices' unit sequences and CTA c takes
+// [c*U/P, (c+1)*U/P), so only CTA boundaries split a row tile.  A split tile's pieces each
+// write a partial and take a ticket; the last to arrive adds the partials in piece order
+// (fixed, whatever the arrival order) and writes y.  No CTA ever waits for another CTA, so a
+// launch needs no co-residency guarantee.  Nothing in any output's arithmetic depends on M.
 //
 // Dequantisation, exact to ~1 ulp of fp16 for every input: with code c = 1024 + q (or
 // 1024 + 16q), P = sc*q is exact from one fp16 FMA; B = dmin*m splits error-free into
@@ -78,7 +80,7 @@ constexpr int kACols = 128;  // one unit of fp16 weights: 128 rows x 256 k
 constexpr int kTB = 6;
 constexpr int kBlBytes = kRows * 32;  // A tile of the -B_l step: [128 rows][16 k] fp16
 // named barriers
-constexpr int kBarTmem = 1, kBarTeardown = 2;
+constexpr int kBarTmem = 1, kBarTeardown = 2, kBarEpi = 3;
 constexpr int kTmemUsers = (kDqWarps + 2 + 4) * 32;  // dequant + MMA + epilogue warps
 
 // Ring depths (weight slots, activation slots) per block format and tile width, as deep as
@@ -130,7 +132,8 @@ struct Cfg {
     // where the issuer's extra wait right after a burst of MMAs costs more than it saves.
     static constexpr bool kSplit = F == QMM_FORMAT_Q4_K && MP == 64;
     static_assert(!kSplit || !kIssuerWaitsX, "the first half's MMAs rely on the group's wait for the x tile");
-    static constexpr int kNumBars = 2 * kWRing + 2 * kXRing + 2 * kTB + 4 + 2 + 2 + 1 + (kSplit ? kTB : 0);
+    // wfull, wempty, xfull, xempty, tfull, tempty, accfull[2], accempty[2], mmadone[2], tfull_lo
+    static constexpr int kNumBars = 2 * kWRing + 2 * kXRing + 2 * kTB + 6 + (kSplit ? kTB : 0);
     // argmax launches: the epilogue warps' best keys, [warp 4][token MP]
     static constexpr int kAmaxOff = kBarOff + kNumBars * 8 + 16;
     static constexpr int kSmem = kAmaxOff + 4 * MP * 8 + 1024;  // + alignment slack
@@ -141,6 +144,11 @@ __device__ __forceinline__ int64_t dev_piece_of(int64_t u, int64_t units, int64_
     return ((u + 1) * grid + units - 1) / units - 1;
 }
 
+// First unit of piece c of `units` cut into `grid` pieces.
+__device__ __forceinline__ int64_t dev_piece_start(int64_t c, int64_t units, int64_t grid) {
+    return c * units / grid;
+}
+
 __device__ __forceinline__ void fail(int* err, volatile int* flags) {
     if (!flags[0]) {
         flags[0] = 1;
@@ -148,18 +156,8 @@ __device__ __forceinline__ void fail(int* err, volatile int* flags) {
     }
 }
 
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* flags) {
-    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, flags));
-}
-
-__device__ __forceinline__ bool wait_count(const int* p, int target, volatile int* flags) {
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 0;; ++it) {
-        if (ld_acquire_gpu(p) >= target) return true;
-        if (flags[0]) return false;
-        if ((it & 63u) == 63u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
-        __nanosleep(64);
-    }
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* flags, uint64_t lim) {
+    return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, flags, lim));
 }
 
 struct Cursor {
@@ -323,13 +321,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* tempty = tfull + kTB;
     uint64_t* accfull = tempty + kTB;   // [2]: both issuers' accumulators of buffer b are final
     uint64_t* accempty = accfull + 2;   // [2]: the epilogue has read buffer b
-    uint64_t* evpart = accempty + 2;    // the four epilogue warps have written the partial
-    uint64_t* evred = evpart + 1;       // ... have read the partials of the tile they reduced
-    uint64_t* mmadone = evred + 1;      // [2]: every MMA of issuer e has finished
-    uint64_t* evamax = mmadone + 2;     // argmax launches: the four epilogue warps' keys are in
+    uint64_t* mmadone = accempty + 2;   // [2]: every MMA of issuer e has finished
     // [kTB], kSplit only: sub-blocks 0-3 of the unit's A buffer are written (the other widths
     // keep the shared-memory layout without them)
-    uint64_t* tfull_lo = evamax + 1;
+    uint64_t* tfull_lo = mmadone + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull_lo + (C::kSplit ? kTB : 0));
     unsigned long long* amax_sm = reinterpret_cast<unsigned long long*>(smem + C::kAmaxOff);
     volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] abort
@@ -341,7 +336,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int count = p.count;
     const int64_t U = p.units;
     const int64_t P = gridDim.x;
-    const int64_t g0 = c * U / P, g1 = (c + 1) * U / P;
+    const int64_t g0 = dev_piece_start(c, U, P), g1 = dev_piece_start(c + 1, U, P);
+    const uint64_t lim = p.wait_ns;
     auto mat = [&](int i) -> const MatDesc& { return count == 1 ? single : p.mats[i]; };
     auto enter = [&](Cursor& k, int i) {
         for (; i < count; ++i) {
@@ -383,9 +379,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&accempty[i], 4);
             mbar_init(&mmadone[i], 1);
         }
-        mbar_init(evpart, 4);
-        mbar_init(evred, 4);
-        mbar_init(evamax, 4);
         flags[0] = 0;
         fence_mbar_init();
     }
@@ -431,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint8_t* src = nullptr;
             while (w.i < count) {
                 const int s = static_cast<int>(wseq % kWRing);
-                if (wseq >= kWRing && !mbar_wait_bounded(&wempty[s], ((wseq / kWRing) - 1) & 1, flags)) {
+                if (wseq >= kWRing && !mbar_wait_bounded(&wempty[s], ((wseq / kWRing) - 1) & 1, flags, lim)) {
                     ok = false;
                     break;
                 }
@@ -449,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (flags[0]) {
                 volatile int no_abort = 0;
                 for (int64_t j = wseq > kWRing ? wseq - kWRing : 0; j < wseq; ++j)
-                    mbar_wait_bounded(&wfull[j % kWRing], (j / kWRing) & 1, &no_abort);
+                    mbar_wait_bounded(&wfull[j % kWRing], (j / kWRing) & 1, &no_abort, kDrainLimitNs);
             }
         }
         return;
@@ -470,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             griddep_wait();  // activations may be written by the previous kernel
             while (xc.i < count) {
                 const int xs = static_cast<int>(issued % kXRing);
-                if (issued >= kXRing && !mbar_wait_bounded(&xempty[xs], ((issued / kXRing) - 1) & 1, flags)) {
+                if (issued >= kXRing && !mbar_wait_bounded(&xempty[xs], ((issued / kXRing) - 1) & 1, flags, lim)) {
                     ok = false;
                     break;
                 }
@@ -496,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (flags[0]) {
                 volatile int no_abort = 0;
                 for (int64_t j = issued > kXRing ? issued - kXRing : 0; j < issued; ++j)
-                    mbar_wait_bounded(&xfull[j % kXRing], (j / kXRing) & 1, &no_abort);
+                    mbar_wait_bounded(&xfull[j % kXRing], (j / kXRing) & 1, &no_abort, kDrainLimitNs);
             }
         }
         return;
@@ -529,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t ja = tile * KB > u0 ? tile * KB : u0;
                 const int64_t jb = (tile + 1) * KB < u1 ? (tile + 1) * KB : u1;
                 const int b = static_cast<int>(seg % C::kAccBufs);
-                if (seg >= C::kAccBufs && !warp_wait(&accempty[b], ((seg / C::kAccBufs) - 1) & 1, flags)) {
+                if (seg >= C::kAccBufs && !warp_wait(&accempty[b], ((seg / C::kAccBufs) - 1) & 1, flags, lim)) {
                     live = false;
                     break;
                 }
@@ -549,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if constexpr (C::kSplit) {
                         // sub-blocks 0-3 (k-steps 0-7) as soon as they are written; the x tile
                         // is in, since the group waited for it before forming the sums
-                        if (!warp_wait(&tfull_lo[tb], (j / kTB) & 1, flags)) {
+                        if (!warp_wait(&tfull_lo[tb], (j / kTB) & 1, flags, lim)) {
                             live = false;
                             break;
                         }
@@ -563,11 +556,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         __syncwarp();
                     }
-                    if (!warp_wait(&tfull[tb], (j / kTB) & 1, flags)) {
+                    if (!warp_wait(&tfull[tb], (j / kTB) & 1, flags, lim)) {
                         live = false;
                         break;
                     }
-                    if (C::kIssuerWaitsX && !warp_wait(&xfull[xs], (j / kXRing) & 1, flags)) {
+                    if (C::kIssuerWaitsX && !warp_wait(&xfull[xs], (j / kXRing) & 1, flags, lim)) {
                         live = false;
                         break;
                     }
@@ -598,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             tc_commit(&mmadone[e]);
             volatile int no_abort = 0;
-            mbar_wait_bounded(&mmadone[e], 0, &no_abort);
+            mbar_wait_bounded(&mmadone[e], 0, &no_abort, kDrainLimitNs);
         }
         __syncwarp();
         tc_fence_before();
@@ -609,6 +602,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------------------------------------ epilogue
+    // Every decision that ends or skips work is taken by the four warps together (a vote on
+    // named barrier kBarEpi), so that they always meet at the same barriers.
     if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
         const int q = warp & 3;  // tensor-memory lane quarter
         const int row = 32 * q + lane;
@@ -625,21 +620,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         unsigned long long best[(MP + 31) / 32];
 #pragma unroll
         for (int i = 0; i < (MP + 31) / 32; ++i) best[i] = 0ull;
-        // All four warps arrive on `ev` (each at most once per launch); lane 0 of warp
-        // kEpiWarp0 then waits for the other three.  False if that wait gave up.
-        auto gather = [&](uint64_t* ev) -> bool {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(ev);
-            return !(warp == kEpiWarp0 && lane == 0) || mbar_wait_bounded(ev, 0, flags);
-        };
         Cursor mk;
         first(mk);
         while (live && mk.i < count) {
             const MatDesc& M = mat(mk.i);
             const int64_t KB = M.kb;
             const int64_t u0 = mk.j, u1 = mk.e;
-            const int64_t base = M.base;
-            for (int64_t tile = u0 / KB; live && tile <= (u1 - 1) / KB; ++tile, ++seg) {
+            for (int64_t tile = u0 / KB; tile <= (u1 - 1) / KB; ++tile, ++seg) {
                 const int64_t ja = tile * KB > u0 ? tile * KB : u0;
                 const int64_t jb = (tile + 1) * KB < u1 ? (tile + 1) * KB : u1;
                 const int b = static_cast<int>(seg % C::kAccBufs);
@@ -647,7 +634,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool has0 = jb - ja >= 2 || (jl & 1) == 0;
                 const bool has1 = jb - ja >= 2 || (jl & 1) == 1;
                 jl += jb - ja;
-                if (!warp_wait(&accfull[b], (seg / C::kAccBufs) & 1, flags)) {
+                const bool got = warp_wait(&accfull[b], (seg / C::kAccBufs) & 1, flags, lim);
+                if (!bar_and(kBarEpi, kEpiThreads, got)) {
                     live = false;
                     break;
                 }
@@ -667,59 +655,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int i = 0; i < 16; ++i) acc[i] += __uint_as_float(v[i]);
                     }
                 };
-                const bool whole = (ja == tile * KB) && (jb == (tile + 1) * KB);
-                const int64_t pa = whole ? c : dev_piece_of(base + tile * KB, U, P);
-                const int64_t n = tile * kRows + row;
-                if (pa != c) {
-                    // a partial for the tile's reducer: [float4 f][128 rows] in this CTA's slot
-                    float4* part = reinterpret_cast<float4*>(p.ws + c * static_cast<int64_t>(kRows) * p.ws_cols);
-#pragma unroll 1
-                    for (int c0 = 0; c0 < MP; c0 += 16) {
-                        float acc[16];
-                        load_acc(c0, acc);
-#pragma unroll
-                        for (int f = 0; f < 4; ++f)
-                            part[(c0 / 4 + f) * kEpiThreads + etid] =
-                                make_float4(acc[4 * f], acc[4 * f + 1], acc[4 * f + 2], acc[4 * f + 3]);
-                    }
+                // the accumulators of buffer b are read: the issuers may overwrite them
+                auto release = [&]() {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&accempty[b]);
-                    // publish: one release increment of the tile's ticket after all four warps' writes
-                    const bool ok = gather(evpart);
-                    if (ok && warp == kEpiWarp0 && lane == 0) red_add_release_gpu(M.tickets + tile, 1);
-                    live = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                    continue;
-                }
-                int64_t pb = pa;
-                if (!whole) {
-                    pb = dev_piece_of(base + (tile + 1) * KB - 1, U, P);
-                    bool got = true;
-                    if (lane == 0) got = wait_count(M.tickets + tile, static_cast<int>(pb - pa), flags);
-                    if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
-                        live = false;
-                        break;
-                    }
-                    __syncwarp();  // the other lanes' loads come after lane 0's acquire
-                }
-#pragma unroll 1
-                for (int c0 = 0; c0 < MP; c0 += 16) {
-                    float acc[16];
-                    load_acc(c0, acc);
-#pragma unroll 1
-                    for (int64_t pc = pa + 1; pc <= pb; ++pc) {
-                        const float4* src = reinterpret_cast<const float4*>(p.ws + pc * static_cast<int64_t>(kRows) * p.ws_cols);
-                        float4 pv[4];
-#pragma unroll
-                        for (int f = 0; f < 4; ++f) pv[f] = __ldcg(src + (c0 / 4 + f) * kEpiThreads + etid);
-#pragma unroll
-                        for (int f = 0; f < 4; ++f) {
-                            acc[4 * f] += pv[f].x;
-                            acc[4 * f + 1] += pv[f].y;
-                            acc[4 * f + 2] += pv[f].z;
-                            acc[4 * f + 3] += pv[f].w;
-                        }
-                    }
+                };
+                const int64_t n = tile * kRows + row;
+                const int64_t tstart = M.base + tile * KB;  // the tile's first unit in the launch
+                // final values of columns c0 .. c0 + 15: y, or the argmax fold
+                auto emit = [&](int c0, const float (&acc)[16]) {
                     if (amax) {
                         // per token: the warp's largest value (one redux over order-mapped
                         // bits, 0 for rows past N; -0 counts as +0) and its lowest row
@@ -731,9 +676,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint32_t u = __float_as_uint(acc[i] + 0.0f);  // -0 -> +0
                             const uint32_t o = n < M.n ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
                             const uint32_t mx = __reduce_max_sync(0xffffffffu, o);
-                            const int first = __ffs(__ballot_sync(0xffffffffu, o == mx)) - 1;
+                            const int firstl = __ffs(__ballot_sync(0xffffffffu, o == mx)) - 1;
                             if ((m & 31) == lane && mx != 0u) {
-                                const uint32_t nf = static_cast<uint32_t>(n - lane + first);
+                                const uint32_t nf = static_cast<uint32_t>(n - lane + firstl);
                                 const unsigned long long key =
                                     (static_cast<unsigned long long>(mx) << 32) | (0xFFFFFFFFu - nf);
 #pragma unroll
@@ -748,16 +693,77 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (m < p.m && n < M.n) M.y[static_cast<int64_t>(m) * M.n + n] = acc[i];
                         }
                     }
+                };
+                if (ja == tile * KB && jb == (tile + 1) * KB) {
+                    // the whole tile is in this CTA's piece
+#pragma unroll 1
+                    for (int c0 = 0; c0 < MP; c0 += 16) {
+                        float acc[16];
+                        load_acc(c0, acc);
+                        emit(c0, acc);
+                    }
+                    release();
+                    continue;
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&accempty[b]);
-                // the partials are read: the tile's ticket is ready for the next run
-                if (!whole) {
-                    const bool ok = gather(evred);
-                    if (ok && warp == kEpiWarp0 && lane == 0) M.tickets[tile] = 0;
-                    live = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                // A tile split between pieces pa..pb: each writes its partial into one of its
+                // CTA's two slots (0: its piece's first tile, 1: its last) and takes a ticket;
+                // the last to arrive adds the partials in piece order and writes the result.
+                {
+                    const int slot = g0 >= tstart ? 0 : 1;
+                    float4* part = reinterpret_cast<float4*>(p.ws + (c * 2 + slot) * kRows * p.ws_cols);
+#pragma unroll 1
+                    for (int c0 = 0; c0 < MP; c0 += 16) {
+                        float acc[16];
+                        load_acc(c0, acc);
+#pragma unroll
+                        for (int f = 0; f < 4; ++f)
+                            part[(c0 / 4 + f) * kEpiThreads + etid] =
+                                make_float4(acc[4 * f], acc[4 * f + 1], acc[4 * f + 2], acc[4 * f + 3]);
+                    }
                 }
+                release();
+                __threadfence();  // this thread's partial before the ticket
+                named_bar_sync(kBarEpi, kEpiThreads);
+                const int64_t pa = dev_piece_of(tstart, U, P), pb = dev_piece_of(tstart + KB - 1, U, P);
+                bool last = false;
+                if (warp == kEpiWarp0 && lane == 0)
+                    last = atom_add_acq_rel_gpu(M.tickets + tile, 1) == static_cast<int>(pb - pa);
+                if (!bar_or(kBarEpi, kEpiThreads, last)) continue;
+                // the last piece: every partial of the tile is written (the loads are ordered
+                // after the ticket's acquire by the barrier)
+#pragma unroll 1
+                for (int c0 = 0; c0 < MP; c0 += 16) {
+                    float acc[16];
+#pragma unroll 1
+                    for (int64_t pc = pa; pc <= pb; ++pc) {
+                        const int sl = dev_piece_start(pc, U, P) >= tstart ? 0 : 1;
+                        const float4* src = reinterpret_cast<const float4*>(p.ws + (pc * 2 + sl) * kRows * p.ws_cols);
+                        float4 pv[4];
+#pragma unroll
+                        for (int f = 0; f < 4; ++f) pv[f] = __ldcg(src + (c0 / 4 + f) * kEpiThreads + etid);
+                        if (pc == pa) {
+#pragma unroll
+                            for (int f = 0; f < 4; ++f) {
+                                acc[4 * f] = pv[f].x;
+                                acc[4 * f + 1] = pv[f].y;
+                                acc[4 * f + 2] = pv[f].z;
+                                acc[4 * f + 3] = pv[f].w;
+                            }
+                        } else {
+#pragma unroll
+                            for (int f = 0; f < 4; ++f) {
+                                acc[4 * f] += pv[f].x;
+                                acc[4 * f + 1] += pv[f].y;
+                                acc[4 * f + 2] += pv[f].z;
+                                acc[4 * f + 3] += pv[f].w;
+                            }
+                        }
+                    }
+                    emit(c0, acc);
+                }
+                // every partial is read: the ticket is ready for the next launch
+                named_bar_sync(kBarEpi, kEpiThreads);
+                if (warp == kEpiWarp0 && lane == 0) M.tickets[tile] = 0;
             }
             enter(mk, mk.i + 1);
         }
@@ -766,20 +772,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int bi = 0; bi < (MP + 31) / 32; ++bi)
                 if (32 * bi + lane < MP) amax_sm[q * MP + 32 * bi + lane] = best[bi];
-            const bool ok = gather(evamax);
+            named_bar_sync(kBarEpi, kEpiThreads);
             if (warp == kEpiWarp0) {
-                if (__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
-                    __syncwarp();  // the other lanes read after lane 0's wait
-                    for (int m = lane; m < p.m; m += 32) {
-                        unsigned long long k = amax_sm[m];
+                for (int m = lane; m < p.m; m += 32) {
+                    unsigned long long k = amax_sm[m];
 #pragma unroll
-                        for (int w = 1; w < 4; ++w) k = amax_sm[w * MP + m] > k ? amax_sm[w * MP + m] : k;
-                        atomicMax(p.amax_keys + m, k);
-                    }
-                    amax_finish_warp(p, static_cast<int>(gridDim.x), lane);
-                } else {
-                    live = false;
+                    for (int w = 1; w < 4; ++w) k = amax_sm[w * MP + m] > k ? amax_sm[w * MP + m] : k;
+                    atomicMax(p.amax_keys + m, k);
                 }
+                amax_finish_warp(p, static_cast<int>(gridDim.x), lane);
             }
         }
         if (!live && lane == 0) fail(p.err, flags);
@@ -796,10 +797,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t tlane = *tmem_slot + (static_cast<uint32_t>(32 * q) << 16);
         const int64_t nunits = g1 - g0;
-        for (int64_t j = g; j < nunits; j += kGroups) {
+        int64_t j = g;
+        for (; j < nunits; j += kGroups) {
             const int s = static_cast<int>(j % kWRing);
             const int a = static_cast<int>(j % C::kNA);
-            if (!warp_wait(&wfull[s], (j / kWRing) & 1, flags)) break;
+            if (!warp_wait(&wfull[s], (j / kWRing) & 1, flags, lim)) break;
             const uint8_t* u = wring + s * kUnitBytes;
             if constexpr (F == QMM_FORMAT_Q4_K) {
                 uint4 qv[8];
@@ -831,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // (the same fp16 additions in the same order, so a row's bits do not depend on
                 // MP), and the group does not wait for the tile at all.
                 const int xs = static_cast<int>(j % kXRing);
-                if (!C::kIssuerWaitsX && !warp_wait(&xfull[xs], (j / kXRing) & 1, flags)) break;
+                if (!C::kIssuerWaitsX && !warp_wait(&xfull[xs], (j / kXRing) & 1, flags, lim)) break;
                 const uint8_t* xt = xring + xs * C::kXSlot;
                 uint8_t* xst = xsum + xs * C::kXsBytes;
     #pragma unroll
@@ -851,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
 
                 // the A buffer was last read by the MMAs of unit j - kNA
-                if (j >= C::kNA && !warp_wait(&tempty[(j - C::kNA) % kTB], ((j - C::kNA) / kTB) & 1, flags)) break;
+                if (j >= C::kNA && !warp_wait(&tempty[(j - C::kNA) % kTB], ((j - C::kNA) / kTB) & 1, flags, lim)) break;
                 tc_fence_after();
                 const uint32_t tcol = tlane + a * kACols;
     #pragma unroll
@@ -883,8 +885,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // no sums to form: the wait on the activation tile keeps the MMAs of this unit
                 // after its arrival, as the Q4_K path's sums do (at MP = 128 the issuers wait)
                 const int xs = static_cast<int>(j % kXRing);
-                if (!C::kIssuerWaitsX && !warp_wait(&xfull[xs], (j / kXRing) & 1, flags)) break;
-                if (j >= C::kNA && !warp_wait(&tempty[(j - C::kNA) % kTB], ((j - C::kNA) / kTB) & 1, flags)) break;
+                if (!C::kIssuerWaitsX && !warp_wait(&xfull[xs], (j / kXRing) & 1, flags, lim)) break;
+                if (j >= C::kNA && !warp_wait(&tempty[(j - C::kNA) % kTB], ((j - C::kNA) / kTB) & 1, flags, lim)) break;
                 tc_fence_after();
                 const uint32_t tcol = tlane + a * kACols;
                 if constexpr (F == QMM_FORMAT_Q8_0)
@@ -900,7 +902,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&tfull[j % kTB]);
         }
-        if (flags[0] && lane == 0) fail(p.err, flags);
+        tc_wait_st();
+        // a wait gave up (its own limit, or another warp's failure): report it
+        if (j < nunits && lane == 0) fail(p.err, flags);
         named_bar_sync(kBarTeardown, kTmemUsers);
     }
 }
@@ -1178,40 +1182,35 @@ cudaError_t presum(const MatDesc& single, const LaunchParams& p, int32_t max_kb,
 }
 
 template <int MP, int F>
-static cudaError_t launch_mp(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl,
-                             bool cooperative) {
+static cudaError_t launch_mp(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = Cfg<MP, F>::kSmem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
-    attr[1].id = cudaLaunchAttributeCooperative;
-    attr[1].val.cooperative = cooperative ? 1 : 0;
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, tc_kernel<MP, F>, single, p);
 }
 
 template <int F>
-static cudaError_t launch_f(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl,
-                            bool cooperative) {
+static cudaError_t launch_f(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl) {
     switch (mp_for(p.m)) {
-        case 16: return launch_mp<16, F>(single, p, grid, s, pdl, cooperative);
-        case 32: return launch_mp<32, F>(single, p, grid, s, pdl, cooperative);
-        case 64: return launch_mp<64, F>(single, p, grid, s, pdl, cooperative);
-        default: return launch_mp<128, F>(single, p, grid, s, pdl, cooperative);
+        case 16: return launch_mp<16, F>(single, p, grid, s, pdl);
+        case 32: return launch_mp<32, F>(single, p, grid, s, pdl);
+        case 64: return launch_mp<64, F>(single, p, grid, s, pdl);
+        default: return launch_mp<128, F>(single, p, grid, s, pdl);
     }
 }
 
-cudaError_t launch(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl, bool cooperative,
-                   int format) {
+cudaError_t launch(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl, int format) {
     switch (format) {
-        case QMM_FORMAT_Q6_K: return launch_f<QMM_FORMAT_Q6_K>(single, p, grid, s, pdl, cooperative);
-        case QMM_FORMAT_Q8_0: return launch_f<QMM_FORMAT_Q8_0>(single, p, grid, s, pdl, cooperative);
-        default: return launch_f<QMM_FORMAT_Q4_K>(single, p, grid, s, pdl, cooperative);
+        case QMM_FORMAT_Q6_K: return launch_f<QMM_FORMAT_Q6_K>(single, p, grid, s, pdl);
+        case QMM_FORMAT_Q8_0: return launch_f<QMM_FORMAT_Q8_0>(single, p, grid, s, pdl);
+        default: return launch_f<QMM_FORMAT_Q4_K>(single, p, grid, s, pdl);
     }
 }
 

@@ -12,6 +12,11 @@
 // the tile tickets and the error word, and runs; the array keeps the last call's contents.  All
 // calls share it, so calls that overlap on the GPU (different streams, or different host
 // threads) race and give wrong results: serialise them.
+//
+// A device-side wait that gives up cannot be reported through the return value (the call
+// returns before the kernel runs, and reading the error word back would synchronise).  So a
+// last small kernel of each call reads the call's error word and, if it is set, fills the
+// call's y with NaN: a failed call never leaves plausible numbers behind.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -28,9 +33,18 @@ __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
-unsigned char* g_scratch_dev[kMaxDevices] = {};  // device address of g_scratch, per device
+bool g_configured[kMaxDevices] = {};  // kernel attributes set, per device
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// y[0 .. count) = NaN if the call's error word is set; nothing otherwise.
+__global__ void poison_on_error(const int* __restrict__ err, float* __restrict__ y, int64_t count) {
+    if (*reinterpret_cast<const volatile int*>(err) == 0) return;
+    const float nan = __int_as_float(0x7FC00000);
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        y[i] = nan;
+}
 
 }  // namespace
 
@@ -62,19 +76,20 @@ extern "C" qmm_status qmm_run_noalloc(const void* blocks, int64_t n, int64_t k, 
     if (need > kScratchBytes) return QMM_ERR_SCRATCH_TOO_SMALL;
     if (m == 0) return QMM_OK;
 
-    // Set-up, once per device and with that device current: the host-side name g_scratch is
-    // only a stand-in, so look up the array's device address.  The first call on each device
-    // does this and must therefore come before any stream capture.
+    // The host-side name g_scratch is only a stand-in: every call looks up the array's device
+    // address on the current device (cheap, and never stale, e.g. after a device reset).  The
+    // first call on each device also sets the kernel's attributes, so it must come before any
+    // stream capture.
     unsigned char* base = nullptr;
     {
         std::lock_guard<std::mutex> lk(g_setup_mu);
-        if (!g_scratch_dev[dev]) {
-            void* p = nullptr;
-            if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return QMM_ERR_CUDA;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) return QMM_ERR_CUDA;
+        if (!g_configured[dev]) {
             if (qmm::b1::configure() != cudaSuccess) return QMM_ERR_CUDA;
-            g_scratch_dev[dev] = static_cast<unsigned char*>(p);
+            g_configured[dev] = true;
         }
-        base = g_scratch_dev[dev];
+        base = static_cast<unsigned char*>(p);
     }
     uint8_t* wq = base;
     float* wsp = reinterpret_cast<float*>(base + packed);
@@ -107,7 +122,14 @@ extern "C" qmm_status qmm_run_noalloc(const void* blocks, int64_t n, int64_t k, 
         p.count = 1;
         p.m = static_cast<int32_t>(mc);
         p.ws_cols = cols;
-        if (qmm::b1::launch(mat, p, static_cast<int>(grid), s, false, false) != cudaSuccess) return QMM_ERR_CUDA;
+        p.wait_ns = qmm::kDefaultWaitNs;
+        // cooperative, as qmm_run's launches of this kernel: its split-K reducer waits for the
+        // partials of CTAs after it
+        if (qmm::b1::launch(mat, p, static_cast<int>(grid), s, false, true) != cudaSuccess) return QMM_ERR_CUDA;
     }
+    const int64_t count = m * n;
+    const int64_t nblk = (count + 255) / 256 < 1024 ? (count + 255) / 256 : 1024;
+    poison_on_error<<<static_cast<unsigned>(nblk), 256, 0, s>>>(err, y, count);
+    if (cudaGetLastError() != cudaSuccess) return QMM_ERR_CUDA;
     return QMM_OK;
 }

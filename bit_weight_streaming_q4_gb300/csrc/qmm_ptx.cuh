@@ -55,17 +55,45 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
 
 // Wait for phase `parity` of `bar` to complete.  Gives up (returns false) when the
-// shared abort flag is raised by another thread or after kWaitLimitNs; never spins
-// forever.
+// shared abort flag is raised by another thread or after `limit_ns`; never spins forever.
+// Each failed try_wait has already suspended the thread for a while, so the clock is read
+// after every one of them.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  volatile int* abort_flag) {
+                                                  volatile int* abort_flag, uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 1;; ++i) {
+    for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
+}
+
+// ---------------------------------------------------------------- named-barrier votes
+// All `nthreads` threads of barrier `id` take part; returns the AND (OR) of their votes.
+__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t nthreads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ bool bar_or(uint32_t id, uint32_t nthreads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
 }
 
 // ---------------------------------------------------------------- bulk copies (TMA, 1-D)

@@ -33,7 +33,7 @@ class QmmError(RuntimeError):
 class Options(ctypes.Structure):
     _fields_ = [("m_max", ctypes.c_int32), ("backend", ctypes.c_int32),
                 ("ctas_per_sm", ctypes.c_int32), ("host_io", ctypes.c_int32),
-                ("format", ctypes.c_int32)]
+                ("format", ctypes.c_int32), ("wait_limit_us", ctypes.c_int32)]
 
 
 class Info(ctypes.Structure):
@@ -122,11 +122,11 @@ def current_stream() -> int:
 
 
 def default_options(m_max: int = 16, backend: int = BACKEND_AUTO, ctas_per_sm: int = 0,
-                    host_io: bool = False, format: int = FORMAT_Q4_K) -> Options:
+                    host_io: bool = False, format: int = FORMAT_Q4_K, wait_limit_us: int = 0) -> Options:
     o = Options()
     load().qmm_default_options(ctypes.byref(o))
     o.m_max, o.backend, o.ctas_per_sm, o.host_io = m_max, backend, ctas_per_sm, int(host_io)
-    o.format = format
+    o.format, o.wait_limit_us = format, wait_limit_us
     return o
 
 
@@ -139,11 +139,11 @@ class Qmm:
 
     def __init__(self, blocks, n: int, k: int, m_max: int = 16, backend: int = BACKEND_AUTO,
                  ctas_per_sm: int = 0, host_io: bool = False, stream: int | None = None,
-                 format: int = FORMAT_Q4_K):
+                 format: int = FORMAT_Q4_K, wait_limit_us: int = 0):
         lib = load()
         on_dev = bool(getattr(blocks, "is_cuda", False))
         self._h = ctypes.c_void_p()
-        opt = default_options(m_max, backend, ctas_per_sm, host_io, format)
+        opt = default_options(m_max, backend, ctas_per_sm, host_io, format, wait_limit_us)
         st = current_stream() if stream is None else stream
         _check(lib.qmm_create(ctypes.byref(self._h), _ptr(blocks), n, k, int(on_dev),
                               ctypes.byref(opt), st), "qmm_create")

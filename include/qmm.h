@@ -87,6 +87,11 @@ typedef struct {
     int32_t ctas_per_sm;  /* 0 = default; persistent CTAs per SM (part of the reduction order) */
     int32_t host_io;      /* nonzero: also allocate staging buffers for qmm_run_host */
     int32_t format;       /* QMM_FORMAT_* of the blocks passed to qmm_create */
+    int32_t wait_limit_us;/* 0 = default (4 s); otherwise the longest time, in microseconds, any
+                             device-side wait of the handle's launches between the kernel's own
+                             warps and CTAs may take before the launch gives up with
+                             QMM_ERR_DEVICE_TIMEOUT.  Exists so that the timeout path can be
+                             exercised; a limit far below a launch's duration fails every run. */
 } qmm_options;
 
 typedef struct {
@@ -103,7 +108,8 @@ typedef struct {
     int32_t format;           /* QMM_FORMAT_* of the handle */
 } qmm_info;
 
-/* Fill `opt` with defaults: m_max 16, backend auto, ctas_per_sm 0, host_io 0, format Q4_K. */
+/* Fill `opt` with defaults: m_max 16, backend auto, ctas_per_sm 0, host_io 0, format Q4_K,
+ * wait_limit_us 0. */
 void qmm_default_options(qmm_options* opt);
 
 /*
@@ -236,11 +242,12 @@ const char* qmm_status_str(qmm_status s);
  *                                (the weights of run i stream in while run i-1 ends); results
  *                                are bit-identical to the same runs issued one by one.
  *  flags = QMM_STEP_INDEPENDENT: the caller guarantees that no x_i is written by a run of
- *                                the step.  When every handle is an mma.sync handle and
- *                                M <= 16, one cooperative persistent kernel streams all the
- *                                matrices: their unit sequences are concatenated and cut into
- *                                one piece per CTA, so only CTA boundaries split a row tile.
- *                                Each handle may then appear at most once.  The split-K order
+ *                                the step.  When every handle has the same backend and block
+ *                                format and M fits one launch (M <= 16 for MMA_SYNC handles,
+ *                                M <= 128 for TCGEN05 handles), one persistent kernel streams
+ *                                all the matrices: their unit sequences are concatenated and
+ *                                cut into one piece per CTA, so only CTA boundaries split a
+ *                                row tile.  Each handle may then appear at most once.  The split-K order
  *                                differs from that of single runs, so results agree with them
  *                                within rounding (not bit for bit); a row's result still does
  *                                not depend on M.
@@ -276,10 +283,11 @@ qmm_status qmm_step_destroy(qmm_step s);
  *          process exits); the packed weights plus the workspace must fit, which allows Q4_K
  *          matrices up to about 40 MiB -- larger shapes return QMM_ERR_SCRATCH_TOO_SMALL.
  *          M may be any size (16 rows per launch).
- *  The first call on each device looks up the scratch array's device address, so it must
- *  come before any stream capture.  Calls share the array and keep its last contents (each
- *  call clears what must start at zero): calls that overlap on the GPU race -- serialise them.
- *  Device-side wait failures of this entry point are not reported.
+ *  The first call on each device sets up the kernel (function attributes), so it must come
+ *  before any stream capture.  Calls share the array and keep its last contents (each call
+ *  clears what must start at zero): calls that overlap on the GPU race -- serialise them.
+ *  A device-side wait that gives up (see QMM_ERR_DEVICE_TIMEOUT) cannot be returned by the
+ *  call, which returns before its kernels run: instead such a call leaves its whole y NaN.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, NO_DEVICE, SCRATCH_TOO_SMALL, CUDA.
  */
 qmm_status qmm_run_noalloc(const void* blocks, int64_t n, int64_t k, const void* x, int64_t m, float* y,
