@@ -355,6 +355,9 @@ struct qmm_step_s {
     int32_t max_kb = 0;
     __half* xsum = nullptr;       // device, the sums of every matrix
     int32_t format = QMM_FORMAT_Q4_K;  // ... and their block format
+    int* done = nullptr;          // device, dependent persistent steps: [count + 1] completion counters
+    int32_t* cta_units = nullptr; // device, dependent persistent steps: [grid] units of each CTA
+    qmm::MatDesc single = {};     // the descriptor a one-matrix launch takes by value
     int* err_host = nullptr;
     int* err_dev = nullptr;
     qmm::LaunchParams params = {};
@@ -369,6 +372,8 @@ static void free_step(qmm_step st) {
     cudaFree(st->first_mat);
     cudaFree(st->ws);
     cudaFree(st->xsum);
+    cudaFree(st->done);
+    cudaFree(st->cta_units);
     if (st->err_host) cudaFreeHost(st->err_host);
     delete st;
 }
@@ -378,7 +383,8 @@ extern "C" {
 qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handles,
                            const void* const* xs, float* const* ys, int64_t m, uint32_t flags, void* stream) {
     if (!out || count <= 0 || !handles || !xs || !ys || m < 1) return QMM_ERR_INVALID_ARG;
-    if (flags & ~static_cast<uint32_t>(QMM_STEP_INDEPENDENT | QMM_STEP_GRAPH)) return QMM_ERR_INVALID_ARG;
+    if (flags & ~static_cast<uint32_t>(QMM_STEP_INDEPENDENT | QMM_STEP_GRAPH | QMM_STEP_PERSISTENT))
+        return QMM_ERR_INVALID_ARG;
     *out = nullptr;
     for (int32_t i = 0; i < count; ++i) {
         if (!live_handle(handles[i])) return QMM_ERR_BAD_HANDLE;
@@ -388,18 +394,28 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
     }
     qmm_step st = new (std::nothrow) qmm_step_s();
     if (!st) return QMM_ERR_OOM;
-    // One persistent kernel for the whole step when the runs are independent, every handle has
-    // the same backend and block format and M fits one launch (16 rows mma.sync, 128 tcgen05),
-    // unless QMM_STEP_GRAPH asks for the graph; a CUDA graph of runs otherwise.
+    // One persistent kernel for the whole step, unless QMM_STEP_GRAPH asks for the graph, when
+    // every handle has the same backend and block format and M fits one launch (16 rows
+    // mma.sync, 128 tcgen05):
+    //  - independent runs: the matrices' unit sequences are concatenated and cut into one
+    //    piece per CTA (each handle at most once: its tickets serve one matrix of a launch);
+    //  - dependent runs, when QMM_STEP_PERSISTENT asks for it (tcgen05 handles, M <= 64): the
+    //    matrices are taken in order, each cut into its own pieces as a single run of its
+    //    handle would be, and a CTA loads matrix i's activations only once every output of
+    //    matrix i - 1 is written.
+    // A CUDA graph of runs otherwise.
     const int32_t be = handles[0]->backend;
     const bool tc = be == QMM_BACKEND_TCGEN05;
-    bool persistent = m <= (tc ? qmm::b2::kMaxM : qmm::b1::kMaxM) && !(flags & QMM_STEP_GRAPH) &&
-                      (flags & QMM_STEP_INDEPENDENT);
+    const bool indep = (flags & QMM_STEP_INDEPENDENT) != 0;
+    bool persistent = m <= (tc ? qmm::b2::kMaxM : qmm::b1::kMaxM) && !(flags & QMM_STEP_GRAPH);
     // one persistent launch runs one kernel: one backend and one block format
     for (int32_t i = 0; i < count; ++i)
         persistent = persistent && handles[i]->backend == be && handles[i]->format == handles[0]->format;
-    if (persistent) {
-        // a handle's tickets and partial slots serve one matrix of a launch at a time
+    // a dependent step reads activations written during the launch, so they cannot come from a
+    // pre-pass: the tensor-core kernel at up to 64 rows
+    const bool dep = persistent && !indep;
+    if (dep) persistent = (flags & QMM_STEP_PERSISTENT) && tc && !qmm::b2::presum_for(m, handles[0]->format);
+    if (persistent && indep) {
         std::set<qmm_handle> seen(handles, handles + count);
         if (static_cast<int32_t>(seen.size()) != count) {
             delete st;
@@ -408,9 +424,6 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
     }
     qmm_status rc = QMM_OK;
     if (persistent) {
-        // One persistent kernel: the matrices' unit sequences are concatenated and cut into one
-        // piece per CTA (stream-K over the whole step), so at most one row tile per CTA
-        // boundary is split between two CTAs.
         std::vector<qmm::MatDesc> host(count);
         int64_t total = 0;
         // activation sums of every matrix (launches of more than 64 rows), one pre-pass per launch
@@ -433,18 +446,31 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
                    : qmm::b1::make_mat(&host[i], h->wq, xs[i], ys[i], h->tickets, h->d.units, h->d.n,
                                        static_cast<int32_t>(h->d.kb), static_cast<int32_t>(m));
             if (me != cudaSuccess) rc = QMM_ERR_CUDA;
-            host[i].base = total;
+            host[i].base = dep ? 0 : total;
+            host[i].pieces = dep ? h->d.grid : 0;
             total += h->d.units;
         }
         int sms = 0;
         if (rc == QMM_OK && cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, handles[0]->device) != cudaSuccess)
             rc = QMM_ERR_CUDA;
-        const int grid = static_cast<int>(total < sms ? total : sms);
+        int grid = static_cast<int>(total < sms ? total : sms);
         std::vector<int32_t> firsts(grid > 0 ? grid : 1);
-        for (int c = 0, i = 0; c < grid; ++c) {
-            const int64_t g0 = c * total / grid;
-            while (host[i].base + host[i].units <= g0) ++i;
-            firsts[c] = i;
+        std::vector<int32_t> cta_units;
+        if (dep) {
+            // as many CTAs as the widest matrix has pieces; CTA c takes piece c of each matrix
+            grid = 0;
+            for (int32_t i = 0; i < count; ++i) grid = host[i].pieces > grid ? host[i].pieces : grid;
+            cta_units.assign(grid, 0);
+            for (int32_t i = 0; i < count; ++i)
+                for (int c = 0; c < host[i].pieces; ++c)
+                    cta_units[c] += static_cast<int32_t>((c + 1) * host[i].units / host[i].pieces -
+                                                         c * host[i].units / host[i].pieces);
+        } else {
+            for (int c = 0, i = 0; c < grid; ++c) {
+                const int64_t g0 = c * total / grid;
+                while (host[i].base + host[i].units <= g0) ++i;
+                firsts[c] = i;
+            }
         }
         const int32_t ws_cols = tc ? qmm::b2::mp_for(m) : qmm::b1::ws_floats(m);
         const size_t ws_bytes =
@@ -453,6 +479,15 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
         if (rc == QMM_OK && cudaMalloc(&st->mats, sizeof(qmm::MatDesc) * count) != cudaSuccess) rc = QMM_ERR_OOM;
         if (rc == QMM_OK && cudaMalloc(&st->first_mat, sizeof(int32_t) * firsts.size()) != cudaSuccess) rc = QMM_ERR_OOM;
         if (rc == QMM_OK && cudaMalloc(&st->ws, ws_bytes) != cudaSuccess) rc = QMM_ERR_OOM;
+        if (rc == QMM_OK && dep &&
+            (cudaMalloc(&st->done, sizeof(int) * (count + 1)) != cudaSuccess ||
+             cudaMalloc(&st->cta_units, sizeof(int32_t) * cta_units.size()) != cudaSuccess))
+            rc = QMM_ERR_OOM;
+        if (rc == QMM_OK && dep &&
+            (cudaMemset(st->done, 0, sizeof(int) * (count + 1)) != cudaSuccess ||
+             cudaMemcpy(st->cta_units, cta_units.data(), sizeof(int32_t) * cta_units.size(), cudaMemcpyHostToDevice) !=
+                 cudaSuccess))
+            rc = QMM_ERR_CUDA;
         if (rc == QMM_OK && cudaHostAlloc(&st->err_host, sizeof(int), cudaHostAllocMapped) != cudaSuccess)
             rc = QMM_ERR_OOM;
         if (rc == QMM_OK) {
@@ -478,6 +513,9 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
             st->params.wait_ns = handles[0]->wait_ns;
             st->params.m = static_cast<int32_t>(m);
             st->params.ws_cols = ws_cols;
+            st->params.done = st->done;
+            st->params.cta_units = st->cta_units;
+            st->single = host[0];
         }
     } else {
         cudaStream_t cap = nullptr;
@@ -516,11 +554,11 @@ qmm_status qmm_step_launch(qmm_step s, void* stream) {
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     if (s->mats) {
         if (*reinterpret_cast<volatile int*>(s->err_host)) return QMM_ERR_DEVICE_TIMEOUT;
-        const qmm::MatDesc unused = {};
-        cudaError_t e = s->presum ? qmm::b2::presum(unused, s->params, s->max_kb, cs) : cudaSuccess;
+        // (a one-matrix step's kernel takes the descriptor by value)
+        cudaError_t e = s->presum ? qmm::b2::presum(s->single, s->params, s->max_kb, cs) : cudaSuccess;
         if (e == cudaSuccess)
-            e = s->tcgen05 ? qmm::b2::launch(unused, s->params, s->grid, cs, true, s->format)
-                           : qmm::b1::launch(unused, s->params, s->grid, cs, true, true);
+            e = s->tcgen05 ? qmm::b2::launch(s->single, s->params, s->grid, cs, true, s->format)
+                           : qmm::b1::launch(s->single, s->params, s->grid, cs, true, true);
         return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
     }
     return cudaGraphLaunch(s->exec, cs) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;

@@ -762,7 +762,7 @@ cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, i
     out->units = units;
     out->n = n;
     out->kb = kb;
-    out->pad = 0;
+    out->pieces = 0;
     return cudaSuccess;
 }
 

@@ -160,6 +160,17 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, flags, lim));
 }
 
+// Bounded spin until *p >= target (acquire, device scope).  False on timeout or abort.
+__device__ __forceinline__ bool wait_count(const int* p, int target, volatile int* flags, uint64_t lim) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (ld_acquire_gpu(p) >= target) return true;
+        if (flags[0]) return false;
+        if ((it & 7u) == 7u && globaltimer_ns() - t0 > lim) return false;
+        __nanosleep(32);
+    }
+}
+
 struct Cursor {
     int i;
     int64_t j, e;
@@ -338,13 +349,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t P = gridDim.x;
     const int64_t g0 = dev_piece_start(c, U, P), g1 = dev_piece_start(c + 1, U, P);
     const uint64_t lim = p.wait_ns;
+    const bool dep = p.done != nullptr;  // a dependent step: each matrix cut into its own pieces
     auto mat = [&](int i) -> const MatDesc& { return count == 1 ? single : p.mats[i]; };
+    // where this CTA's piece of a matrix starts (in the units the split-K bookkeeping counts:
+    // the matrix's own in a dependent step, the launch's concatenated sequence otherwise), and
+    // how many units and pieces that sequence has
+    auto piece_lo = [&](const MatDesc& M) -> int64_t {
+        return dep ? (c < M.pieces ? c * M.units / M.pieces : M.units) : g0;
+    };
+    auto seq_units = [&](const MatDesc& M) -> int64_t { return dep ? M.units : U; };
+    auto seq_pieces = [&](const MatDesc& M) -> int64_t { return dep ? M.pieces : P; };
     auto enter = [&](Cursor& k, int i) {
         for (; i < count; ++i) {
             const MatDesc& M = mat(i);
-            if (M.base >= g1) break;
-            const int64_t lo = g0 > M.base ? g0 - M.base : 0;
-            const int64_t hi = g1 - M.base < M.units ? g1 - M.base : M.units;
+            int64_t lo, hi;
+            if (dep) {
+                lo = piece_lo(M);
+                hi = c < M.pieces ? (c + 1) * M.units / M.pieces : M.units;
+            } else {
+                if (M.base >= g1) break;
+                lo = g0 > M.base ? g0 - M.base : 0;
+                hi = g1 - M.base < M.units ? g1 - M.base : M.units;
+            }
             if (lo < hi) {
                 k.i = i;
                 k.j = lo;
@@ -355,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         k.i = count;
         k.j = k.e = 0;
     };
-    auto first = [&](Cursor& k) { enter(k, count == 1 ? 0 : p.first_mat[c]); };
+    auto first = [&](Cursor& k) { enter(k, (count == 1 || dep) ? 0 : p.first_mat[c]); };
     auto next = [&](Cursor& k) {
         if (++k.j >= k.e) enter(k, k.i + 1);
     };
@@ -474,6 +500,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     smap = &M.smap;
                     kbn = M.kb;
                     kb = static_cast<int>(xc.j % kbn);
+                    if (dep && xc.i > 0) {
+                        // a dependent step: matrix i's activations may be matrix i - 1's output;
+                        // load them only once every CTA has written its part of it, and order
+                        // those (generic-proxy) writes before this thread's bulk tensor loads
+                        if (!wait_count(p.done + (xc.i - 1), static_cast<int>(gridDim.x), flags, lim)) {
+                            ok = false;
+                            break;
+                        }
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                    }
                 }
                 mbar_arrive_expect_tx(&xfull[xs], C::kXSlot + (C::kPre ? MP * 16 : 0));
 #pragma unroll
@@ -620,9 +656,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         unsigned long long best[(MP + 31) / 32];
 #pragma unroll
         for (int i = 0; i < (MP + 31) / 32; ++i) best[i] = 0ull;
+        // dependent steps: count this CTA done with matrices arrived .. upto - 1 (its outputs of
+        // them are written, or it had none), one release add each after every warp's stores
+        int arrived = 0;
+        auto arrive_upto = [&](int upto) {
+            if (!dep || arrived >= upto) return;
+            __threadfence();
+            named_bar_sync(kBarEpi, kEpiThreads);
+            if (warp == kEpiWarp0 && lane == 0)
+                for (int t = arrived; t < upto; ++t) red_add_release_gpu(p.done + t, 1);
+            arrived = upto;
+        };
         Cursor mk;
         first(mk);
         while (live && mk.i < count) {
+            arrive_upto(mk.i);
             const MatDesc& M = mat(mk.i);
             const int64_t KB = M.kb;
             const int64_t u0 = mk.j, u1 = mk.e;
@@ -694,6 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 };
+                const int64_t SU = seq_units(M), SP = seq_pieces(M);
                 if (ja == tile * KB && jb == (tile + 1) * KB) {
                     // the whole tile is in this CTA's piece
 #pragma unroll 1
@@ -709,7 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // CTA's two slots (0: its piece's first tile, 1: its last) and takes a ticket;
                 // the last to arrive adds the partials in piece order and writes the result.
                 {
-                    const int slot = g0 >= tstart ? 0 : 1;
+                    const int slot = piece_lo(M) >= tstart ? 0 : 1;
                     float4* part = reinterpret_cast<float4*>(p.ws + (c * 2 + slot) * kRows * p.ws_cols);
 #pragma unroll 1
                     for (int c0 = 0; c0 < MP; c0 += 16) {
@@ -724,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 release();
                 __threadfence();  // this thread's partial before the ticket
                 named_bar_sync(kBarEpi, kEpiThreads);
-                const int64_t pa = dev_piece_of(tstart, U, P), pb = dev_piece_of(tstart + KB - 1, U, P);
+                const int64_t pa = dev_piece_of(tstart, SU, SP), pb = dev_piece_of(tstart + KB - 1, SU, SP);
                 bool last = false;
                 if (warp == kEpiWarp0 && lane == 0)
                     last = atom_add_acq_rel_gpu(M.tickets + tile, 1) == static_cast<int>(pb - pa);
@@ -736,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float acc[16];
 #pragma unroll 1
                     for (int64_t pc = pa; pc <= pb; ++pc) {
-                        const int sl = dev_piece_start(pc, U, P) >= tstart ? 0 : 1;
+                        const int sl = dev_piece_start(pc, SU, SP) >= tstart ? 0 : 1;
                         const float4* src = reinterpret_cast<const float4*>(p.ws + (pc * 2 + sl) * kRows * p.ws_cols);
                         float4 pv[4];
 #pragma unroll
@@ -783,6 +832,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 amax_finish_warp(p, static_cast<int>(gridDim.x), lane);
             }
         }
+        if (dep && live) {
+            arrive_upto(count);
+            // the last CTA to finish zeroes the counters for the next launch (every CTA has
+            // passed its last wait on them by then)
+            if (warp == kEpiWarp0 && lane == 0 &&
+                atom_add_acq_rel_gpu(p.done + count, 1) == static_cast<int>(gridDim.x) - 1)
+                for (int t = 0; t <= count; ++t) p.done[t] = 0;
+        }
         if (!live && lane == 0) fail(p.err, flags);
         named_bar_sync(kBarTeardown, kTmemUsers);
         return;
@@ -796,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(kBarTmem, kTmemUsers);
         tc_fence_after();
         const uint32_t tlane = *tmem_slot + (static_cast<uint32_t>(32 * q) << 16);
-        const int64_t nunits = g1 - g0;
+        const int64_t nunits = dep ? p.cta_units[c] : g1 - g0;
         int64_t j = g;
         for (; j < nunits; j += kGroups) {
             const int s = static_cast<int>(j % kWRing);
@@ -1143,7 +1200,7 @@ cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, i
     out->units = units;
     out->n = n;
     out->kb = kb;
-    out->pad = 0;
+    out->pieces = 0;
     return cudaSuccess;
 }
 

@@ -41,11 +41,11 @@ struct alignas(128) MatDesc {
     const uint8_t* wq;     // repacked units
     float* y;              // [m, n] fp32
     int* tickets;          // [tiles]: partials published for the tile; zero between runs
-    int64_t base;          // first unit of this matrix in the launch's sequence
+    int64_t base;          // first unit of this matrix in the launch's sequence (0 in dependent steps)
     int64_t units;
     int64_t n;
     int32_t kb;
-    int32_t pad;
+    int32_t pieces;        // dependent steps: pieces the matrix is cut into (its handle's grid)
 };
 
 struct LaunchParams {
@@ -70,6 +70,15 @@ struct LaunchParams {
     // before the launch gives up and reports QMM_ERR_DEVICE_TIMEOUT; the waits that let copies
     // in flight land before a CTA exits always use kDrainLimitNs.
     uint64_t wait_ns;
+    // Dependent steps (tcgen05 backend; null otherwise): matrix i is cut into its own
+    // mats[i].pieces pieces, exactly as a single run of its handle (CTA c takes piece c, CTAs
+    // past the last piece none), the matrices are taken in order, and a CTA loads matrix i's
+    // activations only once done[i - 1] counts every CTA of the launch, i.e. once every output
+    // of matrix i - 1 is written.  done[count] counts the CTAs that have finished; the last of
+    // them zeroes all count + 1 counters for the next launch.  cta_units[c] = CTA c's units
+    // over all matrices.
+    int* done;
+    const int32_t* cta_units;
 };
 
 // Default wait limit of a launch, and the limit of the drains on a failure path.

@@ -203,6 +203,7 @@ def run_noalloc(blocks, n: int, k: int, x, y, m: int | None = None, stream: int 
 
 STEP_INDEPENDENT = 1   # no x of the step is written by one of its runs: runs may overlap
 STEP_GRAPH = 2         # force the CUDA-graph implementation
+STEP_PERSISTENT = 4    # dependent runs as one persistent kernel (tcgen05 handles, M <= 64)
 
 
 class Step:

@@ -237,10 +237,21 @@ const char* qmm_status_str(qmm_status s);
  * (handle i: x_i -> y_i, all with the same M), set up once and replayed with one call.
  *  flags = 0:                    dependent runs: run i reads x_i only after run i-1 has
  *                                finished (as a layer waits for the one before), so x_i may be
- *                                run i-1's output.  The runs are recorded into a CUDA graph,
+ *                                run i-1's output.  Results are bit-identical to the same runs
+ *                                issued one by one.  The runs are recorded into a CUDA graph,
  *                                consecutive kernels linked by programmatic dependent launch
- *                                (the weights of run i stream in while run i-1 ends); results
- *                                are bit-identical to the same runs issued one by one.
+ *                                (the weights of run i stream in while run i-1 ends).
+ *  flags = QMM_STEP_PERSISTENT:  dependent runs as one persistent kernel ("How parallel
+ *                                decoding works": one persistent kernel, no per-layer
+ *                                launches), when every handle is a TCGEN05 handle of one block
+ *                                format and M <= 64 (the graph otherwise): each matrix is cut
+ *                                into the pieces a single run of its handle would use (so the
+ *                                results are again bit-identical to single runs), the weights
+ *                                stream in continuously across matrix boundaries, and a CTA
+ *                                loads x_i only once every CTA has written its part of run
+ *                                i-1's output (device-scope counters, bounded waits).  A handle
+ *                                may appear more than once.  On this GB300 it is slower than
+ *                                the graph (see the design notes), so it is not the default.
  *  flags = QMM_STEP_INDEPENDENT: the caller guarantees that no x_i is written by a run of
  *                                the step.  When every handle has the same backend and block
  *                                format and M fits one launch (M <= 16 for MMA_SYNC handles,
@@ -251,7 +262,8 @@ const char* qmm_status_str(qmm_status s);
  *                                differs from that of single runs, so results agree with them
  *                                within rounding (not bit for bit); a row's result still does
  *                                not depend on M.
- *  QMM_STEP_GRAPH:               use the CUDA graph even for an independent step.
+ *  QMM_STEP_GRAPH:               use the CUDA graph even for an independent step (it takes
+ *                                precedence over the other flags).
  *  qmm_step_create: builds the step (synchronous; `stream` is not used).
  *  qmm_step_launch: replays it on `stream` (asynchronous, no allocation).
  * The x_i/y_i pointers are baked in; the handles must outlive the step, and a step must not
@@ -262,7 +274,8 @@ const char* qmm_status_str(qmm_status s);
  */
 enum {
     QMM_STEP_INDEPENDENT = 1u,
-    QMM_STEP_GRAPH = 2u
+    QMM_STEP_GRAPH = 2u,
+    QMM_STEP_PERSISTENT = 4u
 };
 typedef struct qmm_step_s* qmm_step;
 qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handles,

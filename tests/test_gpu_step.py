@@ -30,7 +30,7 @@ def _setup(backend, m, mats, m_max=None):
     return qs, xs, ys, refs
 
 
-@pytest.mark.parametrize("flags", [0, 2, 3], ids=["dependent", "graph", "graph_independent"])
+@pytest.mark.parametrize("flags", [0, 2, 3, 4], ids=["dependent", "graph", "graph_independent", "persistent_dependent"])
 def test_graph_step_matches_individual_runs(backend, flags):
     from bit_weight_streaming_q4_gb300 import Step
     torch = torch_cuda()
@@ -200,3 +200,101 @@ def test_tcgen05_step_sustained_launches(m):
         blocks = synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id, rows=rows)
         y_ref, s_ref = oracle.qmm(blocks, x)
         assert_parity(a[:, rows], y_ref, s_ref, mat.name)
+
+
+@pytest.mark.parametrize("m", [8, 64])
+def test_tcgen05_dependent_step_reads_previous_output(m):
+    """The persistent dependent step of the tensor-core backend really waits for run 1's
+    output before run 2 loads it: run 2's activations alias run 1's output buffer, which run 1
+    overwrites with exact zeros (over fp16 ones left there before every launch)."""
+    from bit_weight_streaming_q4_gb300 import Step
+    from bit_weight_streaming_q4_gb300.qmm import STEP_PERSISTENT
+    torch = torch_cuda()
+    n1, k1 = 2560, 4096
+    k2, n2 = 2 * n1, 1024                     # x2 [m, 2 n1] fp16 is the bytes of y1 [m, n1] fp32
+    b1 = synth.q4k_matrix(n1, k1, seed=1, tensor_id=52)
+    b2 = synth.q4k_matrix(n2, k2, seed=1, tensor_id=53)
+    q1, q2 = make(b1, m_max=m, backend=2), make(b2, m_max=m, backend=2)
+    x1 = torch.zeros((m, k1), dtype=torch.float16, device="cuda")      # y1 = 0 exactly
+    y1 = torch.empty((m, n1), dtype=torch.float32, device="cuda")
+    x2 = y1.view(torch.float16)                                         # [m, 2 n1]
+    y2 = torch.empty((m, n2), dtype=torch.float32, device="cuda")
+    ones = np.full((m, 2 * n1), 1.0, dtype=np.float16).view(np.float32)
+    step = Step([q1, q2], [x1, x2], [y1, y2], m, flags=STEP_PERSISTENT)
+    for _ in range(5):
+        y1.copy_(torch.from_numpy(ones))
+        y2.fill_(float("nan"))
+        torch.cuda.synchronize()
+        step.launch()
+        torch.cuda.synchronize()
+        assert np.all(y1.cpu().numpy() == 0.0)
+        assert np.all(y2.cpu().numpy() == 0.0)
+    assert q1.error() == 0 and q2.error() == 0
+    step.close()
+
+
+def test_tcgen05_dependent_chain_with_repeated_handle():
+    """A chain a -> b -> a -> b in one dependent step (a handle may appear more than once):
+    each run reads the previous run's output buffer as its activations, so the step must
+    match the same runs issued one by one, bit for bit, launch after launch."""
+    from bit_weight_streaming_q4_gb300 import Step
+    from bit_weight_streaming_q4_gb300.qmm import STEP_PERSISTENT
+    torch = torch_cuda()
+    m, n, k = 12, 2048, 4096
+    ba = synth.q4k_matrix(n, k, seed=4, tensor_id=54)
+    bb = synth.q4k_matrix(n, k, seed=4, tensor_id=55)
+    qa, qb = make(ba, m_max=m, backend=2), make(bb, m_max=m, backend=2)
+    # run i + 1's activations are the bytes of run i's output: y_i fp32 [m, n] is x fp16 [m, k]
+    bufs = [torch.zeros((m, n), dtype=torch.float32, device="cuda") for _ in range(4)]
+    x0 = torch.from_numpy(synth.x_f16(m, k, seed=4, tensor_id=1054).view(np.int16)).cuda().view(torch.float16)
+    xs = [x0] + [bufs[i].view(torch.float16) for i in range(3)]
+    qs = [qa, qb, qa, qb]
+    # the same runs one by one (each after the previous one has finished)
+    for q, x, y in zip(qs, xs, bufs):
+        q.run(x, y, m)
+        torch.cuda.synchronize()
+    alone = [y.cpu().numpy().copy() for y in bufs]
+    step = Step(qs, [x.data_ptr() for x in xs], bufs, m, flags=STEP_PERSISTENT)
+    for _ in range(3):
+        for y in bufs:
+            y.fill_(float("nan"))
+        torch.cuda.synchronize()
+        step.launch()
+        torch.cuda.synchronize()
+        for a, y in zip(alone, bufs):
+            assert np.array_equal(a.view(np.uint32), y.cpu().numpy().view(np.uint32))
+    assert qa.error() == 0 and qb.error() == 0
+    step.close()
+
+
+@pytest.mark.parametrize("m", [12, 64])
+def test_tcgen05_dependent_step_sustained_launches(m):
+    """Forty back-to-back launches of a dependent persistent step over two layers of the 27B
+    shapes and the lm_head: the completion counters are back at zero for every launch (each
+    launch gives the bits of the same runs issued one by one) and no wait runs out."""
+    from bit_weight_streaming_q4_gb300 import Step
+    from bit_weight_streaming_q4_gb300.qmm import STEP_PERSISTENT
+    torch = torch_cuda()
+    mats = synth.stack(2)
+    qs, xs, ys = [], [], []
+    for mat in mats:
+        blocks = synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id)
+        qs.append(make(blocks, m_max=m, backend=2))
+        del blocks
+        x = synth.x_f16(m, mat.k, seed=0, tensor_id=synth.X_ID_OFFSET + mat.tensor_id)
+        xs.append(torch.from_numpy(x.view(np.int16)).cuda().view(torch.float16))
+        ys.append(torch.zeros((m, mat.n), dtype=torch.float32, device="cuda"))
+    alone = []
+    for q, x, y in zip(qs, xs, ys):
+        q.run(x, y, m)
+        torch.cuda.synchronize()
+        alone.append(y.cpu().numpy().copy())
+    step = Step(qs, xs, ys, m, flags=STEP_PERSISTENT)
+    for rep in range(4):
+        for _ in range(10):
+            step.launch()
+        torch.cuda.synchronize()
+        for a, y, mat in zip(alone, ys, mats):
+            assert np.array_equal(a.view(np.uint32), y.cpu().numpy().view(np.uint32)), (rep, mat.name)
+    assert all(q.error() == 0 for q in qs)
+    step.close()
