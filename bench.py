@@ -223,9 +223,10 @@ def measured_traffic(handles):
 
 
 def lm_head_verify(stack, m, stream, reps=50):
-    """Per-launch time of the lm_head run that writes y[m, 151936] and of the fused argmax
-    (qmm_run_argmax) on the same handle and activations; the argmax is checked against the
-    plain run's y (exact: same arithmetic)."""
+    """Per-launch time of the lm_head run that writes y[m, 151936], of the fused argmax
+    (qmm_run_argmax) on the same handle and activations, and of the split alternative (the
+    run that writes y followed by a separate reduction of y); the fused argmax is checked
+    against the plain run's y (exact: same arithmetic)."""
     torch = stack.torch
     i = len(stack.mats) - 1
     q = stack.handles(m)[i]
@@ -256,8 +257,20 @@ def lm_head_verify(stack, m, stream, reps=50):
     ref = np.argmax(yh, axis=1)
     ok = bool(np.array_equal(ih, ref) and
               np.array_equal(vh.view(np.uint32), yh[np.arange(m), ref].view(np.uint32)))
+    # the alternative to the fused call: write y, then reduce it in a separate pass (a library
+    # reduction over the [m, 151936] fp32 logits, on the same stream), for comparison only
+    ym = y[:m * mat.n].view(m, mat.n)
+
+    def split():
+        q.run(x, y.data_ptr(), m, s)
+        with torch.cuda.stream(stream):
+            torch.max(ym, dim=1)
+
+    us_split = timed(split)
     wb = mat.weight_bytes
     return {"backend": int(q.info().backend), "us_write_y": us_y, "us_argmax": us_a,
+            "us_write_y_then_separate_argmax": us_split,
+            "fused_faster_than_split": us_a < us_split,
             "weight_gbs_write_y": wb / us_y / 1e3, "weight_gbs_argmax": wb / us_a / 1e3,
             "y_bytes_not_written": 4 * m * mat.n, "argmax_matches_y": ok}
 
@@ -688,6 +701,8 @@ def run_reference(args, rank, world):
         "data": "synthetic",
         "config": workload_config(args.layers, HEADLINE_M, full_bytes),
         "tok_s": HEADLINE_M / step_s,
+        "ms_per_step_extrapolated": "ms_per_step is the full step's weight bytes at the oracle's "
+                                    "rate on the sampled matrices (no full step was run)",
         "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": walk.cores(), "kind": "oracle",
                          "sample": walk.describe(w, t)},
         "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -728,7 +743,7 @@ def job_gbs(weight_bytes_per_step: int, steps: int, world: int, seconds: float) 
 def run_ours(args, rank, world, local_rank):
     import torch
     from bit_weight_streaming_q4_gb300 import Step
-    from bit_weight_streaming_q4_gb300.qmm import STEP_INDEPENDENT
+    from bit_weight_streaming_q4_gb300.qmm import STEP_INDEPENDENT, STEP_PERSISTENT
 
     torch.cuda.set_device(local_rank)
     peaks, peak_kind = measured_peaks()
@@ -798,6 +813,8 @@ def run_ours(args, rank, world, local_rank):
     x_dense = np.concatenate([stack.x_host[o:o + HEADLINE_M * mat.k]
                               for mat, o in zip(stack.mats, stack.x_off)])
     x_pin = torch.from_numpy(x_dense.view(np.int16)).view(torch.float16).pin_memory()
+    e2e_steps = max(3, min(args.steps, 50))
+    # (1) serialised: each step's copies and launch one after the other on one stream
     y_pin = torch.empty(offy, dtype=torch.float32).pin_memory()
     xd = torch.empty(offx, dtype=torch.float16, device="cuda")
     yd = torch.empty(offy, dtype=torch.float32, device="cuda")
@@ -810,7 +827,6 @@ def run_ours(args, rank, world, local_rank):
             e2e_step.launch(stream.cuda_stream)
             y_pin.copy_(yd, non_blocking=True)
 
-    e2e_steps = max(3, min(args.steps, 50))
     for _ in range(3):
         e2e_once()
     barrier()
@@ -821,13 +837,59 @@ def run_ours(args, rank, world, local_rank):
         e2e_once()
     a1.record(stream)
     torch.cuda.synchronize()
-    te = max_over_ranks(a0.elapsed_time(a1) / 1e3)
+    te_serial = max_over_ranks(a0.elapsed_time(a1) / 1e3)
     e2e_step.close()
     ydev = stack.y.cpu().numpy()
-    yh = y_pin.numpy()
-    e2e_ok = all(np.array_equal(yh[a:a + HEADLINE_M * mat.n].view(np.uint32),
-                                ydev[b:b + HEADLINE_M * mat.n].view(np.uint32))
-                 for mat, a, b in zip(stack.mats, yo, stack.y_off))
+
+    def matches(yh):
+        return all(np.array_equal(yh[a:a + HEADLINE_M * mat.n].view(np.uint32),
+                                  ydev[b:b + HEADLINE_M * mat.n].view(np.uint32))
+                   for mat, a, b in zip(stack.mats, yo, stack.y_off))
+
+    e2e_ok = matches(y_pin.numpy())
+    # (2) pipelined, as a server streams steps: two sets of device buffers; step i's inputs are
+    # copied in (copy stream) while step i - 1 runs, and its outputs copied out (a second copy
+    # stream) while step i + 1 runs.  Timed from the first input copy to the last output copy.
+    xds = [xd, torch.empty(offx, dtype=torch.float16, device="cuda")]
+    yds = [yd, torch.empty(offy, dtype=torch.float32, device="cuda")]
+    ypins = [y_pin, torch.empty(offy, dtype=torch.float32).pin_memory()]
+    steps2 = [make_step(HEADLINE_M, STEP_INDEPENDENT, [xds[b][o:].data_ptr() for o in xo],
+                        [yds[b][o:].data_ptr() for o in yo]) for b in (0, 1)]
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {k: [torch.cuda.Event() for _ in (0, 1)] for k in ("in", "run", "out")}
+
+    def pipelined(n):
+        for i in range(n):
+            b = i % 2
+            if i >= 2:
+                h2d.wait_event(ev["run"][b])   # step i - 2 has read xds[b]
+            with torch.cuda.stream(h2d):
+                xds[b].copy_(x_pin, non_blocking=True)
+                ev["in"][b].record(h2d)
+            stream.wait_event(ev["in"][b])
+            if i >= 2:
+                stream.wait_event(ev["out"][b])  # step i - 2's outputs have left yds[b]
+            steps2[b].launch(stream.cuda_stream)
+            ev["run"][b].record(stream)
+            d2h.wait_event(ev["run"][b])
+            with torch.cuda.stream(d2h):
+                ypins[b].copy_(yds[b], non_blocking=True)
+                ev["out"][b].record(d2h)
+
+    pipelined(3)
+    torch.cuda.synchronize()
+    barrier()
+    p0 = torch.cuda.Event(enable_timing=True)
+    p1 = torch.cuda.Event(enable_timing=True)
+    p0.record(h2d)
+    pipelined(e2e_steps)
+    d2h.wait_stream(stream)
+    p1.record(d2h)
+    torch.cuda.synchronize()
+    te = max_over_ranks(p0.elapsed_time(p1) / 1e3)
+    e2e_ok = e2e_ok and matches(ypins[(e2e_steps - 1) % 2].numpy())
+    for st2 in steps2:
+        st2.close()
 
     head_backend = int(stack.handles(HEADLINE_M)[0].info().backend)
     by_m = {str(HEADLINE_M): {"weight_gbs": value / world, "tok_s": HEADLINE_M / step_s,
@@ -838,6 +900,10 @@ def run_ours(args, rank, world, local_rank):
     td = measure(HEADLINE_M, 0, steps_dep, 3) / steps_dep
     dependent = {"weight_gbs": wb / td / 1e9, "tok_s": HEADLINE_M / td, "ms_per_step": td * 1e3,
                  "runs": "dependent (CUDA graph)"}
+    # the same dependent step as one persistent launch (opt-in: slower than the graph here)
+    tdp = measure(HEADLINE_M, STEP_PERSISTENT, steps_dep, 3) / steps_dep
+    dependent["persistent"] = {"weight_gbs": wb / tdp / 1e9, "ms_per_step": tdp * 1e3,
+                               "runs": "dependent, one persistent launch (QMM_STEP_PERSISTENT)"}
     if not args.no_extra:
         for m in EXTRA_M:
             steps_m = max(20, args.steps // (4 if m > 16 else 1))
@@ -905,7 +971,13 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": wb * e2e_steps / te / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": xb, "d2h_bytes_per_step": yb,
                 "ms_per_step": te / e2e_steps * 1e3, "outputs_match_device_run": e2e_ok,
-                "steps": e2e_steps},
+                "steps": e2e_steps,
+                "how": "public API (Step.launch) with every step's activations copied in from pinned "
+                       "host memory and its outputs copied back, inside the timed region; copies of "
+                       "adjacent steps overlap the running step (two device buffer sets, two copy streams)",
+                "serialised": {"value": wb * e2e_steps / te_serial / 1e9,
+                               "ms_per_step": te_serial / e2e_steps * 1e3,
+                               "how": "copy in, launch, copy out, one after the other on one stream"}},
         "gpu_launches": args.steps,
         "clocks": clocks,
         "parity": parity,
