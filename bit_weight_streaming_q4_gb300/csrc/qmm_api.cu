@@ -355,6 +355,7 @@ struct qmm_step_s {
     int32_t max_kb = 0;
     __half* xsum = nullptr;       // device, the sums of every matrix
     int32_t format = QMM_FORMAT_Q4_K;  // ... and their block format
+    uint8_t* frag = nullptr;      // device, mma.sync persistent steps: every matrix's fragment records
     int* done = nullptr;          // device, dependent persistent steps: [count + 1] completion counters
     int32_t* cta_units = nullptr; // device, dependent persistent steps: [grid] units of each CTA
     qmm::MatDesc single = {};     // the descriptor a one-matrix launch takes by value
@@ -374,6 +375,7 @@ static void free_step(qmm_step st) {
     cudaFree(st->xsum);
     cudaFree(st->done);
     cudaFree(st->cta_units);
+    cudaFree(st->frag);
     if (st->err_host) cudaFreeHost(st->err_host);
     delete st;
 }
@@ -435,6 +437,13 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
             max_kb = handles[i]->d.kb > max_kb ? static_cast<int32_t>(handles[i]->d.kb) : max_kb;
         }
         if (pre && cudaMalloc(&st->xsum, sum_bytes) != cudaSuccess) rc = QMM_ERR_OOM;
+        // mma.sync: the MMA B fragments of every matrix's activations, formed once per launch by
+        // a pre-pass (one record per super-block column) instead of once per unit in the kernel
+        const int64_t frag_rec = tc ? 0 : qmm::b1::frag_record_bytes(m);
+        int64_t frag_bytes = 0;
+        for (int32_t i = 0; i < count && !tc; ++i) frag_bytes += handles[i]->d.kb * frag_rec;
+        if (!tc && rc == QMM_OK && cudaMalloc(&st->frag, frag_bytes) != cudaSuccess) rc = QMM_ERR_OOM;
+        int64_t frag_off = 0;
         int64_t sum_off = 0;
         for (int32_t i = 0; i < count && rc == QMM_OK; ++i) {
             const qmm_handle h = handles[i];
@@ -446,6 +455,10 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
                    : qmm::b1::make_mat(&host[i], h->wq, xs[i], ys[i], h->tickets, h->d.units, h->d.n,
                                        static_cast<int32_t>(h->d.kb), static_cast<int32_t>(m));
             if (me != cudaSuccess) rc = QMM_ERR_CUDA;
+            if (!tc) {
+                host[i].frag = st->frag + frag_off;
+                frag_off += h->d.kb * frag_rec;
+            }
             host[i].base = dep ? 0 : total;
             host[i].pieces = dep ? h->d.grid : 0;
             total += h->d.units;
@@ -515,6 +528,7 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
             st->params.ws_cols = ws_cols;
             st->params.done = st->done;
             st->params.cta_units = st->cta_units;
+            st->params.b1_frags = tc ? 0 : 1;
             st->single = host[0];
         }
     } else {
@@ -555,7 +569,9 @@ qmm_status qmm_step_launch(qmm_step s, void* stream) {
     if (s->mats) {
         if (*reinterpret_cast<volatile int*>(s->err_host)) return QMM_ERR_DEVICE_TIMEOUT;
         // (a one-matrix step's kernel takes the descriptor by value)
-        cudaError_t e = s->presum ? qmm::b2::presum(s->single, s->params, s->max_kb, cs) : cudaSuccess;
+        cudaError_t e = s->presum ? qmm::b2::presum(s->single, s->params, s->max_kb, cs)
+                        : s->frag ? qmm::b1::prefrag(s->single, s->params, s->max_kb, cs)
+                                  : cudaSuccess;
         if (e == cudaSuccess)
             e = s->tcgen05 ? qmm::b2::launch(s->single, s->params, s->grid, cs, true, s->format)
                            : qmm::b1::launch(s->single, s->params, s->grid, cs, true, true);

@@ -216,7 +216,8 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
         }
         for (int i = 0; i < NT * kXRing; ++i) mbar_init(&xfull[i], 1);
         for (int i = 0; i < kFRing; ++i) {
-            mbar_init(&ffull[i], NT);
+            // fragments formed by the NT fragment warps, or one bulk copy of a precomputed record
+            mbar_init(&ffull[i], p.b1_frags ? 1 : NT);
             mbar_init(&fempty[i], kWarps);
         }
         for (int i = 0; i < kEv; ++i) {
@@ -274,6 +275,48 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     // fragments (lane (g, t) of word step i: the 4+4 activations at k = 64t + 4i' and
     // 64t + 32 + 4i', i' = (i + 2t) % 8, in k order) and into the min-term fragments (fp32
     // sums of sub-blocks 2t and 2t+1, split into fp16 hi + lo).
+    if (warp >= C::kFragWarp0 && warp < C::kHelperWarp && p.b1_frags) {
+        // Precomputed fragments (persistent steps): a pre-pass formed each matrix's records,
+        // one per super-block column, and each unit's record is one bulk copy into its slot.
+        if (warp == C::kFragWarp0 && lane == 0) {
+            Cursor fc;
+            first(fc);
+            int64_t j = 0;
+            bool ok = true;
+            int cur = -1, kbn = 1, kb = 0;
+            const uint8_t* rec = nullptr;
+            griddep_wait();  // the records are written by the pre-pass launched just before
+            while (fc.i < count) {
+                const int fs = static_cast<int>(j % kFRing);
+                if (j >= kFRing && !mbar_wait_bounded(&fempty[fs], ((j / kFRing) - 1) & 1, flags, p.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                if (fc.i != cur) {
+                    const MatDesc& M = mat(fc.i);
+                    cur = fc.i;
+                    rec = M.frag;
+                    kbn = M.kb;
+                    kb = static_cast<int>(fc.j % kbn);
+                }
+                uint8_t* fst = fring + fs * C::kFSlot;
+                const uint8_t* src = rec + static_cast<int64_t>(kb) * C::kFSlot;
+                mbar_arrive_expect_tx(&ffull[fs], C::kFSlot);
+                bulk_g2s_nohint(fst, src, C::kFSlot, &ffull[fs]);
+                kb = (kb + 1 == kbn) ? 0 : kb + 1;
+                ++j;
+                next(fc);
+            }
+            if (!ok) fail(p.err, flags);
+            if (flags[0]) {
+                // failure path: let every record copy already issued land before exiting
+                volatile int no_abort = 0;
+                for (int64_t jj = j > kFRing ? j - kFRing : 0; jj < j; ++jj)
+                    mbar_wait_bounded(&ffull[jj % kFRing], (jj / kFRing) & 1, &no_abort);
+            }
+        }
+        return;
+    }
     if (warp >= C::kFragWarp0 && warp < C::kHelperWarp) {
         const int g = lane >> 2, t = lane & 3;
         const int nt = warp - C::kFragWarp0;
@@ -753,8 +796,9 @@ cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, i
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    out->xsrc = nullptr;
+    out->xsrc = static_cast<const __half*>(x);
     out->xs = nullptr;
+    out->frag = nullptr;
     out->wq = wq;
     out->y = y;
     out->tickets = tickets;
@@ -764,6 +808,57 @@ cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, i
     out->kb = kb;
     out->pieces = 0;
     return cudaSuccess;
+}
+
+// One warp per 8 tokens, one block per (super-block column, matrix): the record of column kb
+// of a matrix, exactly what the fragment warps form from the unit's activation tile (same
+// loads, same fp32 additions in the same order), rows past m as zeros.
+template <int NT>
+__global__ void __launch_bounds__(32 * NT) frag_kernel(const __grid_constant__ MatDesc single, const LaunchParams p) {
+    using C = Cfg<NT>;
+    const MatDesc& M = p.count == 1 ? single : p.mats[blockIdx.y];
+    const int kb = blockIdx.x;
+    if (kb >= M.kb) return;
+    const int nt = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int m = 8 * nt + g;
+    const int64_t k = static_cast<int64_t>(M.kb) * 256;
+    const __half* xr = M.xsrc + static_cast<int64_t>(m) * k + kb * 256 + 64 * t;
+    uint8_t* fst = M.frag + static_cast<int64_t>(kb) * C::kFSlot;
+    float sl[8], sh[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int ir = (i + 2 * t) & 7;
+        uint2 vl = make_uint2(0u, 0u), vh = make_uint2(0u, 0u);
+        if (m < p.m) {
+            vl = *reinterpret_cast<const uint2*>(xr + 8 * (ir >> 1) + 4 * (ir & 1));
+            vh = *reinterpret_cast<const uint2*>(xr + 32 + 8 * (ir >> 1) + 4 * (ir & 1));
+        }
+        *reinterpret_cast<uint4*>(fst + ((nt * 8 + i) * 32 + lane) * 16) = make_uint4(vl.x, vl.y, vh.x, vh.y);
+        const float2 a0 = __half22float2(as_h2(vl.x)), a1 = __half22float2(as_h2(vl.y));
+        const float2 b0 = __half22float2(as_h2(vh.x)), b1 = __half22float2(as_h2(vh.y));
+        sl[i] = (a0.x + a0.y) + (a1.x + a1.y);
+        sh[i] = (b0.x + b0.y) + (b1.x + b1.y);
+    }
+    const float x_lo = ((sl[0] + sl[1]) + (sl[2] + sl[3])) + ((sl[4] + sl[5]) + (sl[6] + sl[7]));
+    const float x_hi = ((sh[0] + sh[1]) + (sh[2] + sh[3])) + ((sh[4] + sh[5]) + (sh[6] + sh[7]));
+    const float lim = 65504.f;
+    const float cl = fminf(fmaxf(x_lo, -lim), lim), ch = fminf(fmaxf(x_hi, -lim), lim);
+    const __half l_hi = __float2half_rn(cl), h_hi = __float2half_rn(ch);
+    uint2 mt;
+    mt.x = as_u32(__halves2half2(l_hi, __float2half_rn(cl - __half2float(l_hi))));
+    mt.y = as_u32(__halves2half2(h_hi, __float2half_rn(ch - __half2float(h_hi))));
+    *reinterpret_cast<uint2*>(fst + C::kFragBytes + (nt * 32 + lane) * 8) = mt;
+}
+
+int64_t frag_record_bytes(int64_t m) { return m <= 8 ? Cfg<1>::kFSlot : Cfg<2>::kFSlot; }
+
+cudaError_t prefrag(const MatDesc& single, const LaunchParams& p, int32_t max_kb, cudaStream_t s) {
+    const dim3 grid(static_cast<unsigned>(max_kb), static_cast<unsigned>(p.count));
+    if (p.m <= 8)
+        frag_kernel<1><<<grid, 32, 0, s>>>(single, p);
+    else
+        frag_kernel<2><<<grid, 64, 0, s>>>(single, p);
+    return cudaGetLastError();
 }
 
 cudaError_t launch(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl, bool cooperative) {

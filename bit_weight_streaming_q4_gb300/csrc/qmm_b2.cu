@@ -1180,6 +1180,7 @@ cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, i
         return cudaErrorInvalidValue;
     out->xsrc = static_cast<const __half*>(x);
     out->xs = xs;
+    out->frag = nullptr;
     if (xs) {
         // the activation sums [kb][m][8 sub-blocks] fp16: box 8 x MP x 1, rows past m read as zero
         const cuuint64_t sdim[3] = {8, static_cast<cuuint64_t>(m), static_cast<cuuint64_t>(kb)};

@@ -38,6 +38,8 @@ struct alignas(128) MatDesc {
     CUtensorMap smap;      // tcgen05 Q4_K launches of MP = 128: the activation sums [kb][m][8] fp16, box 8 x 128 x 1
     const __half* xsrc;    // ... the activations they are formed from ([m, k], row stride k)
     __half* xs;            // ... and where the pre-pass writes them
+    uint8_t* frag;         // mma.sync steps: the matrix's MMA B fragments, one record per super-block
+                           // column, formed from xsrc by a pre-pass (null otherwise)
     const uint8_t* wq;     // repacked units
     float* y;              // [m, n] fp32
     int* tickets;          // [tiles]: partials published for the tile; zero between runs
@@ -57,7 +59,7 @@ struct LaunchParams {
     int32_t count;           // matrices in this launch
     int32_t m;               // rows of this launch (1..16 mma.sync, 1..128 tcgen05)
     int32_t ws_cols;         // floats per consumer thread in a partial slot
-    int32_t pad;
+    int32_t b1_frags;        // mma.sync: the matrices' fragments come from their frag records
     // Row-wise argmax instead of y (single-matrix launches only; null otherwise): the
     // launch folds (value, column) keys into amax_keys[m] (zero before and after a launch),
     // and the last of its writer warps, counted in amax_count (zero before and after),
@@ -167,6 +169,12 @@ cudaError_t repack(const uint8_t* src_dev, uint8_t* dst_dev, const Decomp& d, cu
 // Fill a matrix descriptor for a run of m rows (1..16) of x against the handle's weights.
 cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, int* tickets, int64_t units,
                      int64_t n, int32_t kb, int32_t m);
+// Bytes of one fragment record (one super-block column of x: the MMA B fragments of the
+// launch's rows and their sub-block sums) for launches of m rows.
+int64_t frag_record_bytes(int64_t m);
+// The pre-pass of a launch with p.b1_frags: writes every matrix's fragment records (MatDesc::frag,
+// kb records each) from its activations, as a plain launch in stream order before the main one.
+cudaError_t prefrag(const MatDesc& single, const LaunchParams& p, int32_t max_kb, cudaStream_t s);
 // Launch over `p.count` matrices (`single` when count == 1) on `grid` persistent CTAs.
 cudaError_t launch(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl, bool cooperative);
 cudaError_t configure();  // one-time function attributes

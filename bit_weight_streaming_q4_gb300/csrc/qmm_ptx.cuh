@@ -114,6 +114,15 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint3
         : "memory");
 }
 
+// The same without a cache hint (data that other CTAs read again).
+__device__ __forceinline__ void bulk_g2s_nohint(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 // Shared-memory loads that stay where they are written: the scheduler may not hoist them
 // (and stretch their registers' live ranges) across the other pinned loads and mbarrier ops.
