@@ -35,13 +35,16 @@
 // slots is a pair of adjacent activations.  The min-term step uses slots
 // (2t, 2t+1) for (hi, lo) of sub-block 2t and (2t+8, 2t+9) for sub-block 2t+1.
 //
-// Warp roles (one persistent CTA per SM; 7 or 8 warps, so up to 255 registers per thread):
-//   warps 0-3   consumers, 64 rows each (4 m16 row tiles): dequantise into MMA A fragments,
-//               mma.sync, per-unit scaling, the row tile's result or split-K partial;
-//   warp 4      weight producer: 1-D bulk copies of whole units into a 4-slot ring, streaming
+// Warp roles (one persistent CTA per SM; 11 or 12 warps, up to 168 registers per thread):
+//   warps 0-7   consumers, 32 rows each (2 m16 row tiles), two per SM sub-partition:
+//               dequantise into MMA A fragments, mma.sync, per-unit scaling, the row tile's
+//               result or split-K partial;
+//   warp 8      weight producer: 1-D bulk copies of whole units into a 4-slot ring, streaming
 //               across matrix boundaries without waiting on anything but the ring;
-//   warps 5..   one fragment warp per 8 tokens: 2-D TMA (128-byte swizzle) of its 8 activation
-//               rows of each unit, turned into MMA B fragments and sub-block sums;
+//   warps 9..   one fragment warp per 8 tokens: 2-D TMA (128-byte swizzle) of its 8 activation
+//               rows of each unit, turned into MMA B fragments and sub-block sums (in a
+//               persistent step a pre-pass forms each super-block column's fragments once,
+//               and the first fragment warp only copies each unit's record);
 //   last warp   helper: publishes the CTA's split-K partial with a device-scope release add
 //               and resets the ticket of the tile the CTA reduced, so that no consumer waits
 //               on a device-wide write.
@@ -62,8 +65,8 @@
 namespace qmm {
 namespace b1 {
 
-constexpr int kWarps = 4;                       // consumer warps, 64 rows each
-constexpr int kRT = 4;                          // m16 row tiles per consumer warp
+constexpr int kWarps = 8;                       // consumer warps, 32 rows each (two per sub-partition)
+constexpr int kRT = 2;                          // m16 row tiles per consumer warp
 constexpr int kProducerWarp = kWarps;           // weight units
 static_assert(kConsumerThreads == kWarps * 32 && kWarps * kRT * 16 == kRows, "row split");
 constexpr int kQBytes = kRows * 128;            // 32768
@@ -85,9 +88,9 @@ struct Cfg {
     static constexpr int kFOff = kXOff + NT * kXRing * kXSlot;
     static constexpr int kBarOff = kFOff + kFRing * kFSlot;
     static constexpr int kNumBars = 2 * kWRing + NT * kXRing + 2 * kFRing + 2 * kEv;
-    // argmax launches: each consumer warp's best key per token, [warp 4][token 16]
+    // argmax launches: each consumer warp's best key per token, [consumer warp][token 16]
     static constexpr int kBestOff = kBarOff + kNumBars * 8 + 16;
-    static constexpr int kSmem = kBestOff + 4 * 16 * 8 + 1024;
+    static constexpr int kSmem = kBestOff + kWarps * 16 * 8 + 1024;
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -504,7 +507,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                 for (int r = 0; r < kRT; ++r)
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
-                        rk[r][h] = row_consts(lds128(wring + s * kUnitBytes + kQBytes + (64 * warp + 16 * r + 8 * h + g) * 16), t);
+                        rk[r][h] = row_consts(lds128(wring + s * kUnitBytes + kQBytes + (16 * kRT * warp + 16 * r + 8 * h + g) * 16), t);
                 uint4 qv[kRT][2];  // words of the current half (i4) of the unit
 #pragma unroll
                 for (int r = 0; r < kRT; ++r)
@@ -664,7 +667,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                         for (int r = 0; r < kRT; ++r)
 #pragma unroll
                             for (int h = 0; h < 2; ++h) {
-                                const int64_t n = tile * kRows + 64 * warp + 16 * r + g + 8 * h;
+                                const int64_t n = tile * kRows + 16 * kRT * warp + 16 * r + g + 8 * h;
                                 if (n < M.n) {
                                     const unsigned long long k = amax_key(acc[r][nt][2 * h + par], n);
                                     key = k > key ? k : key;
@@ -685,7 +688,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int row = 64 * warp + 16 * r + g + 8 * (e >> 1);
+                            const int row = 16 * kRT * warp + 16 * r + g + 8 * (e >> 1);
                             const int m = nt * 8 + 2 * t + (e & 1);
                             const int64_t n = tile * kRows + row;
                             if (m < p.m && n < M.n) M.y[static_cast<int64_t>(m) * M.n + n] = acc[r][nt][e];
@@ -698,7 +701,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     if (amax && live) {
         __syncwarp();
         if (lane < p.m) atomicMax(p.amax_keys + lane, best[lane]);
-        amax_finish_warp(p, 4 * static_cast<int>(gridDim.x), lane);
+        amax_finish_warp(p, kWarps * static_cast<int>(gridDim.x), lane);
     }
 }
 

@@ -160,10 +160,10 @@ namespace b1 {
 constexpr int kRows = 256;
 constexpr int kUnitBytes = kRows * 144;
 constexpr int kMaxM = 16;  // rows per launch
-constexpr int kConsumerThreads = 128;  // 4 consumer warps, 64 rows each
+constexpr int kConsumerThreads = 256;  // 8 consumer warps, 32 rows each
 // floats of a split-K partial per consumer thread for runs of up to m rows; a handle keeps
 // one slot of kConsumerThreads x ws_floats per CTA
-constexpr int32_t ws_floats(int64_t m) { return m > 8 ? 32 : 16; }
+constexpr int32_t ws_floats(int64_t m) { return m > 8 ? 16 : 8; }
 int smem_bytes(int nt);
 cudaError_t repack(const uint8_t* src_dev, uint8_t* dst_dev, const Decomp& d, cudaStream_t s);
 // Fill a matrix descriptor for a run of m rows (1..16) of x against the handle's weights.
