@@ -748,11 +748,10 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     peaks, peak_kind = measured_peaks()
     hbm = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
-    # decode handles: up to 16 rows (tcgen05) for M = 12, up to 8 rows (mma.sync) for M = 1,
-    # up to 64 rows (tcgen05) for M = 64
+    # decode handles: up to 16 rows (the automatic backend: mma.sync) for M = 12 and M = 1, up to
+    # 64 rows (tcgen05) for M = 64
     wide = 0 if args.no_extra else max(m for m in EXTRA_M)
-    narrow = 0 if args.no_extra or min(EXTRA_M) > 8 else 8
-    stack = Stack(args.layers, 16, torch, wide_m=wide if wide > 16 else 0, narrow_m=narrow)
+    stack = Stack(args.layers, 16, torch, wide_m=wide if wide > 16 else 0)
     stream = torch.cuda.Stream()
     n_mats = len(stack.mats)
 

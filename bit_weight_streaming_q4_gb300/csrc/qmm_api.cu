@@ -60,8 +60,9 @@ int32_t per_launch(const qmm_handle h) {
     return h->backend == QMM_BACKEND_TCGEN05 ? qmm::b2::kMaxM : qmm::b1::kMaxM;
 }
 
-// Largest m_max for which QMM_BACKEND_AUTO picks the mma.sync backend.
-constexpr int64_t kAutoMmaSyncMaxM = 8;
+// Largest m_max for which QMM_BACKEND_AUTO picks the mma.sync backend (all it supports: one
+// launch of up to 16 rows streams faster there than the tcgen05 kernel's, measured on GB300).
+constexpr int64_t kAutoMmaSyncMaxM = 16;
 
 // One run in launches of at most per_launch(h) rows.  With idx and val given, each launch
 // writes its rows' argmax column and value there instead of y (y is not touched).
@@ -173,10 +174,10 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
     if (!h) return QMM_ERR_OOM;
     h->magic = kMagic;
     h->device = dev;
-    // Auto: the register-fed mma.sync stream for handles that never see more than 8 rows (one
-    // n8 fragment per MMA), tcgen05 otherwise (from 9 rows on it streams faster than two
-    // mma.sync fragments).  Fixed per handle (never per run), so that a row's result does not
-    // depend on how many rows it is batched with.
+    // Auto: the register-fed mma.sync stream for handles that never see more than 16 rows (one
+    // launch, one or two n8 fragments per MMA), tcgen05 for wider handles.  Fixed per handle
+    // (never per run), so that a row's result does not depend on how many rows it is batched
+    // with.
     if (opt.backend == QMM_BACKEND_AUTO)
         h->backend = opt.m_max <= kAutoMmaSyncMaxM && opt.format == QMM_FORMAT_Q4_K ? QMM_BACKEND_MMA_SYNC
                                                                                     : QMM_BACKEND_TCGEN05;

@@ -35,13 +35,13 @@
 // slots is a pair of adjacent activations.  The min-term step uses slots
 // (2t, 2t+1) for (hi, lo) of sub-block 2t and (2t+8, 2t+9) for sub-block 2t+1.
 //
-// Warp roles (one persistent CTA per SM; 11 or 12 warps, up to 168 registers per thread):
-//   warps 0-7   consumers, 32 rows each (2 m16 row tiles), two per SM sub-partition:
-//               dequantise into MMA A fragments, mma.sync, per-unit scaling, the row tile's
-//               result or split-K partial;
-//   warp 8      weight producer: 1-D bulk copies of whole units into a 4-slot ring, streaming
+// Warp roles (one persistent CTA per SM; 11 warps of up to 168 registers, or 20 of up to 96):
+//   warps 0..W-1 consumers, two or four per SM sub-partition (W = 8 of 32 rows for launches
+//               of up to 8 rows, 16 of 16 rows for 9-16): dequantise into MMA A fragments,
+//               mma.sync, per-unit scaling, the row tile's result or split-K partial;
+//   warp W      weight producer: 1-D bulk copies of whole units into a 4-slot ring, streaming
 //               across matrix boundaries without waiting on anything but the ring;
-//   warps 9..   one fragment warp per 8 tokens: 2-D TMA (128-byte swizzle) of its 8 activation
+//   warps W+1.. one fragment warp per 8 tokens: 2-D TMA (128-byte swizzle) of its 8 activation
 //               rows of each unit, turned into MMA B fragments and sub-block sums (in a
 //               persistent step a pre-pass forms each super-block column's fragments once,
 //               and the first fragment warp only copies each unit's record);
@@ -65,10 +65,6 @@
 namespace qmm {
 namespace b1 {
 
-constexpr int kWarps = 8;                       // consumer warps, 32 rows each (two per sub-partition)
-constexpr int kRT = 2;                          // m16 row tiles per consumer warp
-constexpr int kProducerWarp = kWarps;           // weight units
-static_assert(kConsumerThreads == kWarps * 32 && kWarps * kRT * 16 == kRows, "row split");
 constexpr int kQBytes = kRows * 128;            // 32768
 constexpr int kWRing = 4;                       // weight slots
 constexpr int kXRing = 5;                       // activation slots per 8-token group
@@ -79,6 +75,14 @@ constexpr int kXSlot = 4 * kXBox;               // 8 tokens x 256 k
 
 template <int NT>
 struct Cfg {
+    // Consumer warps: 8 of 32 rows (2 m16 row tiles) for one n8 fragment; 16 of 16 rows for
+    // two, where the second fragment doubles the MMAs and four warps per sub-partition hide
+    // their latency better (measured on GB300: +4.5 % at 12 rows, -3.6 % at 1 row).
+    static constexpr int kWarps = NT == 1 ? 8 : 16;
+    static constexpr int kRT = kRows / 16 / kWarps;            // m16 row tiles per consumer warp
+    static constexpr int kConsumers = kWarps * 32;
+    static_assert(kConsumers <= kConsumerThreads && kWarps * kRT * 16 == kRows, "row split");
+    static constexpr int kProducerWarp = kWarps;               // weight units
     static constexpr int kFragWarp0 = kProducerWarp + 1;      // NT fragment warps (one per 8 tokens)
     static constexpr int kHelperWarp = kFragWarp0 + NT;       // publishes partials, resets tickets
     static constexpr int kThreads = (kHelperWarp + 1) * 32;   // 7 or 8 warps: up to 255 registers
@@ -165,6 +169,7 @@ template <int NT>
 __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     stream_kernel(const __grid_constant__ MatDesc single, const LaunchParams p) {
     using C = Cfg<NT>;
+    constexpr int kWarps = C::kWarps, kRT = C::kRT, kProducerWarp = C::kProducerWarp;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* wring = smem;
@@ -611,7 +616,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                 for (int r = 0; r < kRT; ++r)
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
-                        part[(r * NT + nt) * kConsumerThreads + tid] =
+                        part[(r * NT + nt) * C::kConsumers + tid] =
                             make_float4(acc[r][nt][0], acc[r][nt][1], acc[r][nt][2], acc[r][nt][3]);
                 live = post();
                 continue;
@@ -637,7 +642,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                         const float4* src = reinterpret_cast<const float4*>(
                             p.ws + pq * static_cast<int64_t>(kConsumerThreads) * p.ws_cols);
 #pragma unroll
-                        for (int f = 0; f < kRT * NT; ++f) v[q][f] = __ldcg(src + f * kConsumerThreads + tid);
+                        for (int f = 0; f < kRT * NT; ++f) v[q][f] = __ldcg(src + f * C::kConsumers + tid);
                     }
 #pragma unroll
                     for (int q = 0; q < kB; ++q) {

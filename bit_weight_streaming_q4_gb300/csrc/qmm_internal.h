@@ -160,10 +160,10 @@ namespace b1 {
 constexpr int kRows = 256;
 constexpr int kUnitBytes = kRows * 144;
 constexpr int kMaxM = 16;  // rows per launch
-constexpr int kConsumerThreads = 256;  // 8 consumer warps, 32 rows each
+constexpr int kConsumerThreads = 512;  // most consumer threads of a launch (16 warps at 9-16 rows)
 // floats of a split-K partial per consumer thread for runs of up to m rows; a handle keeps
 // one slot of kConsumerThreads x ws_floats per CTA
-constexpr int32_t ws_floats(int64_t m) { return m > 8 ? 16 : 8; }
+constexpr int32_t ws_floats(int64_t) { return 8; }  // 8 warps x 2 row tiles x 1 fragment, or 16 x 1 x 2
 int smem_bytes(int nt);
 cudaError_t repack(const uint8_t* src_dev, uint8_t* dst_dev, const Decomp& d, cudaStream_t s);
 // Fill a matrix descriptor for a run of m rows (1..16) of x against the handle's weights.

@@ -58,7 +58,7 @@ typedef enum {
 
 enum {
     QMM_BACKEND_AUTO = 0,     /* chosen from m_max only (never from a run's M):
-                                 m_max <= 8 -> MMA_SYNC (one n8 fragment per MMA, the
+                                 m_max <= 16 -> MMA_SYNC (one launch of up to 16 rows, the
                                  faster stream there), else TCGEN05 */
     QMM_BACKEND_MMA_SYNC = 1, /* warp-level mma.sync m16n8k16, 16 rows per launch */
     QMM_BACKEND_TCGEN05 = 2   /* tcgen05.mma with TMEM accumulators, 128 rows per launch */
