@@ -102,11 +102,10 @@ qmm_status launch_run(qmm_handle h, const void* x, int64_t m, float* y, cudaStre
             // the activation sums first, as a plain launch: that also keeps them from
             // overwriting the sums the handle's previous launch may still be reading
             if (pre) e = qmm::b2::presum(mat, p, static_cast<int32_t>(h->d.kb), s);
-            // the mma.sync kernel's split-K reducer waits for the partials of CTAs after it, so
-            // its CTAs must be co-resident: a cooperative launch (the tcgen05 kernel's last-
-            // arriver reduction waits for no other CTA)
+            // both kernels' split-K reducers wait for the partials of CTAs after them, so their
+            // CTAs must be co-resident: cooperative launches
             if (e == cudaSuccess)
-                e = tc ? qmm::b2::launch(mat, p, h->d.grid, s, pdl, h->format)
+                e = tc ? qmm::b2::launch(mat, p, h->d.grid, s, pdl, true, h->format)
                        : qmm::b1::launch(mat, p, h->d.grid, s, pdl, true);
         }
         if (e != cudaSuccess) return QMM_ERR_CUDA;
@@ -214,8 +213,8 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
         return code;
     };
     if (cudaMalloc(&h->wq, h->wq_bytes) != cudaSuccess) return fail(QMM_ERR_OOM);
-    // split-K partial slots: two per CTA of 128 rows x up to 128 columns (tcgen05), or one per
-    // CTA holding the accumulators of the 128 consumer threads (mma.sync)
+    // split-K partial slots, one per CTA: 128 rows x up to 128 columns (tcgen05), or the
+    // accumulators of the consumer threads (mma.sync)
     const size_t ws_bytes =
         (tc ? static_cast<size_t>(qmm::b2::ws_floats(d.grid, h->ws_cols))
             : static_cast<size_t>(d.grid) * qmm::b1::kConsumerThreads * h->ws_cols) * sizeof(float);
@@ -574,7 +573,7 @@ qmm_status qmm_step_launch(qmm_step s, void* stream) {
                         : s->frag ? qmm::b1::prefrag(s->single, s->params, s->max_kb, cs)
                                   : cudaSuccess;
         if (e == cudaSuccess)
-            e = s->tcgen05 ? qmm::b2::launch(s->single, s->params, s->grid, cs, true, s->format)
+            e = s->tcgen05 ? qmm::b2::launch(s->single, s->params, s->grid, cs, true, true, s->format)
                            : qmm::b1::launch(s->single, s->params, s->grid, cs, true, true);
         return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
     }

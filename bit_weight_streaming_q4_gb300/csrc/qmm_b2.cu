@@ -40,10 +40,11 @@
 //               reduction of a split row tile; warp 11 also publishes the CTA's partial and
 //               resets the ticket of the tile it reduced.
 // Decomposition: a launch concatenates its matrices' unit sequences and CTA c takes
-// [c*U/P, (c+1)*U/P), so only CTA boundaries split a row tile.  A split tile's pieces each
-// write a partial and take a ticket; the last to arrive adds the partials in piece order
-// (fixed, whatever the arrival order) and writes y.  No CTA ever waits for another CTA, so a
-// launch needs no co-residency guarantee.  Nothing in any output's arithmetic depends on M.
+// [c*U/P, (c+1)*U/P), so only CTA boundaries split a row tile.  A tile split between CTAs
+// pa..pb is reduced by pa (it reaches the tile last, at the end of its piece): pa+1..pb write
+// fp32 partials and publish them with one release add on the tile's ticket; pa waits for the
+// ticket and adds the partials to its own in piece order.  Launches are cooperative, so the
+// CTAs a reducer waits for are resident.  Nothing in any output's arithmetic depends on M.
 //
 // Dequantisation, exact to ~1 ulp of fp16 for every input: with code c = 1024 + q (or
 // 1024 + 16q), P = sc*q is exact from one fp16 FMA; B = dmin*m splits error-free into
@@ -661,8 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int arrived = 0;
         auto arrive_upto = [&](int upto) {
             if (!dep || arrived >= upto) return;
-            __threadfence();
-            named_bar_sync(kBarEpi, kEpiThreads);
+            named_bar_sync(kBarEpi, kEpiThreads);  // every warp's outputs are written
             if (warp == kEpiWarp0 && lane == 0)
                 for (int t = arrived; t < upto; ++t) red_add_release_gpu(p.done + t, 1);
             arrived = upto;
@@ -754,12 +754,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     release();
                     continue;
                 }
-                // A tile split between pieces pa..pb: each writes its partial into one of its
-                // CTA's two slots (0: its piece's first tile, 1: its last) and takes a ticket;
-                // the last to arrive adds the partials in piece order and writes the result.
-                {
-                    const int slot = piece_lo(M) >= tstart ? 0 : 1;
-                    float4* part = reinterpret_cast<float4*>(p.ws + (c * 2 + slot) * kRows * p.ws_cols);
+                // A tile split between pieces pa..pb is reduced by pa, the piece holding its first
+                // units, which reaches them last (at the end of its piece): the others write their
+                // partials and move on (only a piece's first tile can be shared without being
+                // owned, so one partial slot per CTA); pa waits for the ticket to count them and
+                // adds them to its own in piece order.  The launch is cooperative, so every piece
+                // the reducer waits for is running.
+                const int64_t pa = dev_piece_of(tstart, SU, SP);
+                if (pa != c) {
+                    float4* part = reinterpret_cast<float4*>(p.ws + c * static_cast<int64_t>(kRows) * p.ws_cols);
 #pragma unroll 1
                     for (int c0 = 0; c0 < MP; c0 += 16) {
                         float acc[16];
@@ -769,47 +772,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                             part[(c0 / 4 + f) * kEpiThreads + etid] =
                                 make_float4(acc[4 * f], acc[4 * f + 1], acc[4 * f + 2], acc[4 * f + 3]);
                     }
+                    release();
+                    // every warp's partial is written (the barrier); one release add publishes them
+                    named_bar_sync(kBarEpi, kEpiThreads);
+                    if (warp == kEpiWarp0 && lane == 0) red_add_release_gpu(M.tickets + tile, 1);
+                    continue;
                 }
-                release();
-                __threadfence();  // this thread's partial before the ticket
-                named_bar_sync(kBarEpi, kEpiThreads);
-                const int64_t pa = dev_piece_of(tstart, SU, SP), pb = dev_piece_of(tstart + KB - 1, SU, SP);
-                bool last = false;
-                if (warp == kEpiWarp0 && lane == 0)
-                    last = atom_add_acq_rel_gpu(M.tickets + tile, 1) == static_cast<int>(pb - pa);
-                if (!bar_or(kBarEpi, kEpiThreads, last)) continue;
-                // the last piece: every partial of the tile is written (the loads are ordered
-                // after the ticket's acquire by the barrier)
+                const int64_t pb = dev_piece_of(tstart + KB - 1, SU, SP);
+                bool counted = true;
+                if (warp == kEpiWarp0 && lane == 0) counted = wait_count(M.tickets + tile, static_cast<int>(pb - pa), flags, lim);
+                // (the vote is also the barrier that orders every warp's loads after the acquire)
+                if (!bar_and(kBarEpi, kEpiThreads, counted)) {
+                    live = false;
+                    break;
+                }
 #pragma unroll 1
                 for (int c0 = 0; c0 < MP; c0 += 16) {
                     float acc[16];
+                    load_acc(c0, acc);
 #pragma unroll 1
-                    for (int64_t pc = pa; pc <= pb; ++pc) {
-                        const int sl = dev_piece_start(pc, SU, SP) >= tstart ? 0 : 1;
-                        const float4* src = reinterpret_cast<const float4*>(p.ws + (pc * 2 + sl) * kRows * p.ws_cols);
+                    for (int64_t pc = pa + 1; pc <= pb; ++pc) {
+                        const float4* src = reinterpret_cast<const float4*>(p.ws + pc * static_cast<int64_t>(kRows) * p.ws_cols);
                         float4 pv[4];
 #pragma unroll
                         for (int f = 0; f < 4; ++f) pv[f] = __ldcg(src + (c0 / 4 + f) * kEpiThreads + etid);
-                        if (pc == pa) {
 #pragma unroll
-                            for (int f = 0; f < 4; ++f) {
-                                acc[4 * f] = pv[f].x;
-                                acc[4 * f + 1] = pv[f].y;
-                                acc[4 * f + 2] = pv[f].z;
-                                acc[4 * f + 3] = pv[f].w;
-                            }
-                        } else {
-#pragma unroll
-                            for (int f = 0; f < 4; ++f) {
-                                acc[4 * f] += pv[f].x;
-                                acc[4 * f + 1] += pv[f].y;
-                                acc[4 * f + 2] += pv[f].z;
-                                acc[4 * f + 3] += pv[f].w;
-                            }
+                        for (int f = 0; f < 4; ++f) {
+                            acc[4 * f] += pv[f].x;
+                            acc[4 * f + 1] += pv[f].y;
+                            acc[4 * f + 2] += pv[f].z;
+                            acc[4 * f + 3] += pv[f].w;
                         }
                     }
                     emit(c0, acc);
                 }
+                release();
                 // every partial is read: the ticket is ready for the next launch
                 named_bar_sync(kBarEpi, kEpiThreads);
                 if (warp == kEpiWarp0 && lane == 0) M.tickets[tile] = 0;
@@ -1240,35 +1237,40 @@ cudaError_t presum(const MatDesc& single, const LaunchParams& p, int32_t max_kb,
 }
 
 template <int MP, int F>
-static cudaError_t launch_mp(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl) {
+static cudaError_t launch_mp(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl,
+                             bool cooperative) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = Cfg<MP, F>::kSmem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = cooperative ? 1 : 0;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, tc_kernel<MP, F>, single, p);
 }
 
 template <int F>
-static cudaError_t launch_f(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl) {
+static cudaError_t launch_f(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl,
+                            bool cooperative) {
     switch (mp_for(p.m)) {
-        case 16: return launch_mp<16, F>(single, p, grid, s, pdl);
-        case 32: return launch_mp<32, F>(single, p, grid, s, pdl);
-        case 64: return launch_mp<64, F>(single, p, grid, s, pdl);
-        default: return launch_mp<128, F>(single, p, grid, s, pdl);
+        case 16: return launch_mp<16, F>(single, p, grid, s, pdl, cooperative);
+        case 32: return launch_mp<32, F>(single, p, grid, s, pdl, cooperative);
+        case 64: return launch_mp<64, F>(single, p, grid, s, pdl, cooperative);
+        default: return launch_mp<128, F>(single, p, grid, s, pdl, cooperative);
     }
 }
 
-cudaError_t launch(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl, int format) {
+cudaError_t launch(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl, bool cooperative,
+                   int format) {
     switch (format) {
-        case QMM_FORMAT_Q6_K: return launch_f<QMM_FORMAT_Q6_K>(single, p, grid, s, pdl);
-        case QMM_FORMAT_Q8_0: return launch_f<QMM_FORMAT_Q8_0>(single, p, grid, s, pdl);
-        default: return launch_f<QMM_FORMAT_Q4_K>(single, p, grid, s, pdl);
+        case QMM_FORMAT_Q6_K: return launch_f<QMM_FORMAT_Q6_K>(single, p, grid, s, pdl, cooperative);
+        case QMM_FORMAT_Q8_0: return launch_f<QMM_FORMAT_Q8_0>(single, p, grid, s, pdl, cooperative);
+        default: return launch_f<QMM_FORMAT_Q4_K>(single, p, grid, s, pdl, cooperative);
     }
 }
 

@@ -137,17 +137,19 @@ cudaError_t repack(const uint8_t* src_dev, uint8_t* dst_dev, const Decomp& d, in
 inline bool presum_for(int64_t m, int format) { return format == QMM_FORMAT_Q4_K && m > 64; }
 // Bytes of the activation sums of a launch of m rows of a matrix of kb super-block columns.
 inline int64_t presum_bytes(int64_t m, int64_t kb) { return kb * m * 16; }
-// Floats of the split-K partial slots of a launch of `grid` CTAs at tile width mp: two slots
-// per CTA (its piece's first and last row tile), 128 rows x mp columns each.
-inline int64_t ws_floats(int64_t grid, int32_t mp) { return grid * 2 * kRows * mp; }
+// Floats of the split-K partial slots of a launch of `grid` CTAs at tile width mp: one slot
+// per CTA (the partial of its piece's first row tile), 128 rows x mp columns.
+inline int64_t ws_floats(int64_t grid, int32_t mp) { return grid * kRows * mp; }
 // Fill a matrix descriptor for a run of m rows (1..128) of x against the handle's weights;
 // xs (presum_bytes(m, kb) bytes, 16-byte aligned) receives the activation sums of launches
 // with presum_for(m, format), and is null otherwise.
 cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, int* tickets, int64_t units,
                      int64_t n, int32_t kb, int32_t m, __half* xs);
 // Launch over `p.count` matrices of one format (`single` when count == 1) on `grid` CTAs;
-// p.ws_cols = mp_for(p.m).  No CTA waits for another, so the grid needs no co-residency.
-cudaError_t launch(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl, int format);
+// p.ws_cols = mp_for(p.m).  A split tile's reducer waits for the partials of later CTAs, so
+// launches must be cooperative (all CTAs resident) whenever another kernel may hold SMs.
+cudaError_t launch(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl, bool cooperative,
+                   int format);
 cudaError_t configure();
 // The pre-pass of a launch with presum_for(p.m, format): the activation sums of every matrix
 // of the launch (`single` when p.count == 1, p.mats otherwise; max_kb the largest kb), issued

@@ -107,29 +107,30 @@ def test_pieces_partition_units(units, grid):
 @pytest.mark.parametrize("mats,grid", [([(40, 20)], 152), ([(40, 68)], 152), ([(1187, 20)], 152),
                                        ([(64, 20), (40, 24), (272, 20), (40, 68)] * 3 + [(1187, 20)], 152),
                                        ([(2, 1), (1, 3), (5, 2)], 4), ([(3, 256)], 7)])
-def test_split_tile_slots(mats, grid):
-    """The tensor-core kernel's split-K bookkeeping, restated on the host: a launch of
-    matrices (tiles, kb) cut into `grid` pieces; a tile shared by pieces pa..pb gets one
-    partial from each, piece c writing it into slot 0 of its pair of slots if the tile holds
-    c's first unit (c's piece starts inside the tile) and slot 1 otherwise.  Every piece must
-    need at most its two slots, never the same slot for two tiles, and the reducer's formula
-    (slot 0 iff the piece starts at or after the tile's first unit) must find each one."""
+def test_split_tile_bookkeeping(mats, grid):
+    """Both kernels' split-K bookkeeping, restated on the host: a launch of matrices (tiles, kb)
+    cut into `grid` pieces.  A tile shared by pieces pa..pb is reduced by pa; each other piece
+    writes one partial into its CTA's single slot.  That slot suffices because a piece can
+    share, without reducing, only its first tile; the reducer pa reaches the tile at the end of
+    its piece (the tile is pa's last tile), after the pieces it waits for have started."""
     units = sum(t * kb for t, kb in mats)
     grid = min(grid, units)
     start = [c * units // grid for c in range(grid + 1)]
-    used = {}
+    partials = {}
     base = 0
     for tiles, kb in mats:
         for tile in range(tiles):
             t0, t1 = base + tile * kb, base + (tile + 1) * kb
             pa, pb = _piece_of(t0, units, grid), _piece_of(t1 - 1, units, grid)
-            assert start[pa] <= t0 < start[pa + 1] and start[pb] < t1 <= start[pb + 1]
-            for c in range(pa, pb + 1) if pb > pa else ():
-                slot = 0 if start[c] >= t0 else 1
-                assert (c, slot) not in used, (c, slot, used.get((c, slot)), (base, tile))
-                used[(c, slot)] = (base, tile)
-                # writer's test (its piece starts inside this tile) = reader's test
-                assert (slot == 0) == (t0 <= start[c] < t1)
+            if pa == pb:
+                continue
+            # the reducer's piece ends inside the tile: it is pa's last tile
+            assert t0 < start[pa + 1] <= t1
+            for c in range(pa + 1, pb + 1):
+                # each writer starts inside the tile: it is that piece's first tile
+                assert t0 < start[c] < t1
+                assert c not in partials, (c, partials[c], (base, tile))
+                partials[c] = (base, tile)
         base += tiles * kb
 
 
