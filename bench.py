@@ -964,8 +964,9 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": measured_traffic(stack.handles(HEADLINE_M)),
                      "kernel": f"{KERNEL_NAME[head_backend]} (one persistent launch per step)",
-                     "note": f"algorithmic bytes per launch (weights + x + y of the 257 matrices) "
-                             f"/ launch time; peak is the {peak_kind} copy bandwidth"},
+                     "note": f"algorithmic bytes per step (weights + x + y of the 257 matrices) "
+                             f"/ step time (the stream kernel plus, for mma.sync, its fragment "
+                             f"pre-pass); peak is the {peak_kind} copy bandwidth"},
         "cpu_baseline": cpu,
         "e2e": {"value": wb * e2e_steps / te / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": xb, "d2h_bytes_per_step": yb,
@@ -977,7 +978,9 @@ def run_ours(args, rank, world, local_rank):
                 "serialised": {"value": wb * e2e_steps / te_serial / 1e9,
                                "ms_per_step": te_serial / e2e_steps * 1e3,
                                "how": "copy in, launch, copy out, one after the other on one stream"}},
-        "gpu_launches": args.steps,
+        # a persistent mma.sync step is two launches (the activation-fragment pre-pass, then the
+        # stream); a tcgen05 step at M <= 64 is one
+        "gpu_launches": args.steps * (2 if head_backend == 1 else 1),
         "clocks": clocks,
         "parity": parity,
     }
