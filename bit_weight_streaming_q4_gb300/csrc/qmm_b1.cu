@@ -23,7 +23,12 @@
 //                        bytes are the lane's words i = 4 i4 .. 4 i4 + 3; lane (g = lane/4,
 //                        t = lane%4) word i of row 32w + 16r + 8h + g is bytes qs[32t + 4i' .. +3]
 //                        with i' = (i + 2t) % 8.
-//   bytes [32768, 36864) the 16-byte block headers (d, dmin, scales) of the 256 rows.
+//   bytes [32768, 36864) the 16-byte headers of the 256 rows: d and dmin as in the block, then
+//                        the same 96 bits of 6-bit scales and mins re-laid as three words Y, Z,
+//                        W whose byte t serves quad lane t (sub-blocks j0 = 2t, j1 = 2t+1):
+//                        Y_t = sc_j0 << 2 | m_j0 >> 4, Z_t = sc_j1 << 2 | m_j1 >> 4,
+//                        W_t = (m_j0 & 15) << 4 | (m_j1 & 15).  Two byte permutes and a few
+//                        masks then give every lane its values without branching on t.
 // Lane t of a quad reads qs[32t .. 32t+31] of its rows: the low nibbles are weights 64t..64t+31
 // (sub-block 2t), the high nibbles weights 64t+32..64t+63 (sub-block 2t+1).  Its eight words
 // are visited rotated by 2t, so that at any step the four lanes of a quad use four different
@@ -32,8 +37,9 @@
 // MMA k-order.  For step s = 0..15 (i = s % 8, i' = (i + 2t) % 8, high = s >= 8) lane t fills
 // the MMA k slots {2t, 2t+1, 2t+8, 2t+9} with weight offsets 64t + 32*high + 4i' + {0, 1, 2, 3}
 // (repack swaps the middle bytes of each quant word to get this order), so that each pair of
-// slots is a pair of adjacent activations.  The min-term step uses slots
-// (2t, 2t+1) for (hi, lo) of sub-block 2t and (2t+8, 2t+9) for sub-block 2t+1.
+// slots is a pair of adjacent activations.  The min-term step uses slots (2t, 2t+1) for the
+// fp16 high parts of the sums of sub-blocks 2t and 2t+1 and (2t+8, 2t+9) for their low parts,
+// so that its A fragment is the lane's pair (m_2t, m_2t+1) in every register.
 //
 // Warp roles (one persistent CTA per SM; 11 warps of up to 168 registers, or 20 of up to 96):
 //   warps 0..W-1 consumers, two or four per SM sub-partition (W = 8 of 32 rows for launches
@@ -121,23 +127,25 @@ struct RowK {
     uint32_t dd;   // {d, dmin} as fp16
 };
 
-__device__ __forceinline__ RowK row_consts(uint4 hd, int t) {
-    uint32_t SC, MN;
-    if (t >= 2) {  // sub-blocks 4..7: low 4 bits from s[8..11], top 2 bits from s[0..7]
-        SC = (hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u);
-        MN = ((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u);
-    } else {       // sub-blocks 0..3: low 6 bits of s[0..3] and s[4..7]
-        SC = hd.y & 0x3F3F3F3Fu;
-        MN = hd.z & 0x3F3F3F3Fu;
-    }
-    const uint32_t b0 = 2u * (t & 1);
-    const uint32_t sel = b0 | ((b0 + 1) << 8);  // bytes b0, b0+1 -> 16-bit lanes
-    const __half2 k1024 = as_h2(0x64006400u);
-    const __half2 sc = __hsub2(as_h2(and_or(prmt(SC, 0, sel), 0x00FF00FFu, 0x64006400u)), k1024);
-    const __half2 mn = __hsub2(as_h2(and_or(prmt(MN, 0, sel), 0x00FF00FFu, 0x64006400u)), k1024);
+// Byte-permute selectors of quad lane t for row_consts: {Y_t, Y_t, Z_t, Z_t}, and then
+// {W_t, Y_t, W_t, Z_t} from (W, the first result).
+__device__ __forceinline__ uint32_t sel_sc(int t) { return t | (t << 4) | ((4 + t) << 8) | ((4 + t) << 12); }
+__device__ __forceinline__ uint32_t sel_mn(int t) { return t | (4 << 4) | (t << 8) | (6 << 12); }
+
+// The row's constants from its re-laid header (the unit layout above).  Every step is exact:
+// the 6-bit values go into the mantissa of 1024 (at a power-of-two offset) and one fp16 FMA
+// takes the offset and the scaling out.
+__device__ __forceinline__ RowK row_consts(uint4 hd, uint32_t selsc, uint32_t selmn) {
+    const uint32_t r1 = prmt(hd.y, hd.z, selsc);                  // {Y_t, Y_t, Z_t, Z_t}
+    const uint32_t csc = and_or(r1, 0x00FC00FCu, 0x64006400u);    // {1024 + 4 sc0, 1024 + 4 sc1}
+    const __half2 sc = __hfma2(as_h2(csc), as_h2(0x24003400u), as_h2(0xCC00DC00u));  // * {1/4, 1/64} - {256, 16}
+    const uint32_t r2 = prmt(hd.w, r1, selmn);                   // {W_t, Y_t, W_t, Z_t}
+    // {16 m0 at bits 4..9 | m1 low nibble at bits 16..19} | m1 high bits moved to 20..21
+    const uint32_t cmn = and_or(r2, 0x000F03F0u, 0x64006400u) | ((r2 >> 4) & 0x00300000u);
+    const __half2 mn = __hfma2(as_h2(cmn), as_h2(0x3C002C00u), as_h2(0xE400D400u));  // * {1/16, 1} - {64, 1024}
     RowK r;
-    r.s = as_u32(__hmul2(sc, as_h2(0x2C003C00u)));  // * {1, 1/16}
-    r.n = as_u32(__hmul2(sc, as_h2(0xD400E400u)));  // * {-1024, -64}
+    r.s = as_u32(sc);
+    r.n = as_u32(__hmul2(sc, as_h2(0xE400E400u)));  // * -1024
     r.m = as_u32(mn);
     r.dd = hd.x;
     return r;
@@ -392,8 +400,9 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             const float cl = fminf(fmaxf(x_lo, -lim), lim), ch = fminf(fmaxf(x_hi, -lim), lim);
             const __half l_hi = __float2half_rn(cl), h_hi = __float2half_rn(ch);
             uint2 mt;
-            mt.x = as_u32(__halves2half2(l_hi, __float2half_rn(cl - __half2float(l_hi))));  // slots 2t, 2t+1
-            mt.y = as_u32(__halves2half2(h_hi, __float2half_rn(ch - __half2float(h_hi))));  // slots 2t+8, 2t+9
+            mt.x = as_u32(__halves2half2(l_hi, h_hi));  // slots 2t, 2t+1: high parts
+            mt.y = as_u32(__halves2half2(__float2half_rn(cl - __half2float(l_hi)),
+                                         __float2half_rn(ch - __half2float(h_hi))));  // slots 2t+8, 2t+9: low parts
             *reinterpret_cast<uint2*>(fst + C::kFragBytes + (nt * 32 + lane) * 8) = mt;
             __syncwarp();
             if (lane == 0) {
@@ -457,6 +466,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     // ------------------------------------------------------------------ consumers
     const int g = lane >> 2;
     const int t = lane & 3;
+    const uint32_t selsc = sel_sc(t), selmn = sel_mn(t);
     // argmax launches: the best key of each token over this warp's final rows (one lane
     // owns each entry)
     const bool amax = p.amax_keys != nullptr;
@@ -464,7 +474,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
     if (lane < 16) best[lane] = 0ull;
     __syncwarp();
     griddep_wait();  // y, the partial slots and the tickets may still be in use by the previous kernel
-    int64_t gseq = 0;  // position in the CTA's unit sequence (ring slots and phases)
+    uint32_t gseq = 0;  // position in the CTA's unit sequence (ring slots and phases)
     int64_t ev = 0;    // events handed to the helper
     bool live = true;
     auto post = [&]() -> bool {  // hand an event to the helper (after this warp's writes)
@@ -497,7 +507,8 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) acc[r][nt][e] = 0.f;
 
-            for (int64_t j = ja; j < jb; ++j, ++gseq) {
+            const uint32_t nj = static_cast<uint32_t>(jb - ja);  // (a piece has < 2^31 units)
+            for (uint32_t jj = 0; jj < nj; ++jj, ++gseq) {
                 const int s = static_cast<int>(gseq % kWRing);
                 const int fs = static_cast<int>(gseq % kFRing);
                 if (!warp_wait(&wfull[s], (gseq / kWRing) & 1, flags, p.wait_ns)) {
@@ -512,7 +523,7 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                 for (int r = 0; r < kRT; ++r)
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
-                        rk[r][h] = row_consts(lds128(wring + s * kUnitBytes + kQBytes + (16 * kRT * warp + 16 * r + 8 * h + g) * 16), t);
+                        rk[r][h] = row_consts(lds128(wring + s * kUnitBytes + kQBytes + (16 * kRT * warp + 16 * r + 8 * h + g) * 16), selsc, selmn);
                 uint4 qv[kRT][2];  // words of the current half (i4) of the unit
 #pragma unroll
                 for (int r = 0; r < kRT; ++r)
@@ -582,14 +593,13 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                 if (lane == 0) mbar_arrive(&fempty[fs]);
 #pragma unroll
                 for (int r = 0; r < kRT; ++r) {
-                    const __half2 m0 = as_h2(rk[r][0].m), m1 = as_h2(rk[r][1].m);
-                    const uint32_t a0 = as_u32(__low2half2(m0)), a2 = as_u32(__high2half2(m0));   // row g
-                    const uint32_t a1 = as_u32(__low2half2(m1)), a3 = as_u32(__high2half2(m1));   // row g+8
+                    // A: (m_2t, m_2t+1) of row g (registers 0, 2) and row g+8 (1, 3)
+                    const uint32_t a0 = rk[r][0].m, a1 = rk[r][1].m;
                     const float2 dd0 = __half22float2(as_h2(rk[r][0].dd)), dd1 = __half22float2(as_h2(rk[r][1].dd));
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         float dm[4] = {0.f, 0.f, 0.f, 0.f};
-                        mma_m16n8k16(dm, a0, a1, a2, a3, xb[nt].x, xb[nt].y);
+                        mma_m16n8k16(dm, a0, a1, a0, a1, xb[nt].x, xb[nt].y);
                         acc[r][nt][0] = fmaf(dd0.x, dp[r][nt][0], acc[r][nt][0]);
                         acc[r][nt][1] = fmaf(dd0.x, dp[r][nt][1], acc[r][nt][1]);
                         acc[r][nt][2] = fmaf(dd1.x, dp[r][nt][2], acc[r][nt][2]);
@@ -736,9 +746,31 @@ __global__ void repack_kernel(const uint8_t* __restrict__ src, uint8_t* __restri
             v = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
     } else {
+        // the row's header: d and dmin unchanged, the twelve scale bytes re-laid so that lane t
+        // of a quad finds (sc, m) of its sub-blocks 2t, 2t+1 in byte t of words 1..3
         const int row = seg - kQBytes / 16;
         const int64_t nrow = tile * kRows + row;
-        if (nrow < n) v = *reinterpret_cast<const uint4*>(src + (nrow * kb + b) * 144);
+        if (nrow < n) {
+            const uint8_t* hb = src + (nrow * kb + b) * 144;
+            uint32_t y = 0, z = 0, w = 0;
+            for (int t = 0; t < 4; ++t) {
+                int sc[2], mn[2];
+                for (int e = 0; e < 2; ++e) {
+                    const int j = 2 * t + e;  // GGUF 6-bit (scale, min) packing of sub-block j
+                    if (j < 4) {
+                        sc[e] = hb[4 + j] & 63;
+                        mn[e] = hb[8 + j] & 63;
+                    } else {
+                        sc[e] = (hb[8 + j] & 0x0F) | ((hb[j] >> 6) << 4);
+                        mn[e] = (hb[8 + j] >> 4) | ((hb[4 + j] >> 6) << 4);
+                    }
+                }
+                y |= static_cast<uint32_t>((sc[0] << 2) | (mn[0] >> 4)) << (8 * t);
+                z |= static_cast<uint32_t>((sc[1] << 2) | (mn[1] >> 4)) << (8 * t);
+                w |= static_cast<uint32_t>(((mn[0] & 15) << 4) | (mn[1] & 15)) << (8 * t);
+            }
+            v = make_uint4(*reinterpret_cast<const uint32_t*>(hb), y, z, w);
+        }
     }
     *reinterpret_cast<uint4*>(dst + u * kUnitBytes + static_cast<int64_t>(seg) * 16) = v;
 }
@@ -853,8 +885,8 @@ __global__ void __launch_bounds__(32 * NT) frag_kernel(const __grid_constant__ M
     const float cl = fminf(fmaxf(x_lo, -lim), lim), ch = fminf(fmaxf(x_hi, -lim), lim);
     const __half l_hi = __float2half_rn(cl), h_hi = __float2half_rn(ch);
     uint2 mt;
-    mt.x = as_u32(__halves2half2(l_hi, __float2half_rn(cl - __half2float(l_hi))));
-    mt.y = as_u32(__halves2half2(h_hi, __float2half_rn(ch - __half2float(h_hi))));
+    mt.x = as_u32(__halves2half2(l_hi, h_hi));
+    mt.y = as_u32(__halves2half2(__float2half_rn(cl - __half2float(l_hi)), __float2half_rn(ch - __half2float(h_hi))));
     *reinterpret_cast<uint2*>(fst + C::kFragBytes + (nt * 32 + lane) * 8) = mt;
 }
 

@@ -41,10 +41,12 @@
 //               resets the ticket of the tile it reduced.
 // Decomposition: a launch concatenates its matrices' unit sequences and CTA c takes
 // [c*U/P, (c+1)*U/P), so only CTA boundaries split a row tile.  A tile split between CTAs
-// pa..pb is reduced by pa (it reaches the tile last, at the end of its piece): pa+1..pb write
-// fp32 partials and publish them with one release add on the tile's ticket; pa waits for the
-// ticket and adds the partials to its own in piece order.  Launches are cooperative, so the
-// CTAs a reducer waits for are resident.  Nothing in any output's arithmetic depends on M.
+// pa..pb is normally reduced by pa (it reaches the tile last, at the end of its piece):
+// pa+1..pb write fp32 partials and publish them with one add on the tile's ticket; pa reads
+// the ticket once and adds the partials to its own in piece order.  If they are not all in
+// (a late CTA), pa parks its partial as well and the last CTA to arrive adds them up in the
+// same order, so no CTA ever waits for another and launches need not be co-resident.
+// Nothing in any output's arithmetic depends on M.
 //
 // Dequantisation, exact to ~1 ulp of fp16 for every input: with code c = 1024 + q (or
 // 1024 + 16q), P = sc*q is exact from one fp16 FMA; B = dmin*m splits error-free into
@@ -754,45 +756,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     release();
                     continue;
                 }
-                // A tile split between pieces pa..pb is reduced by pa, the piece holding its first
-                // units, which reaches them last (at the end of its piece): the others write their
-                // partials and move on (only a piece's first tile can be shared without being
-                // owned, so one partial slot per CTA); pa waits for the ticket to count them and
-                // adds them to its own in piece order.  The launch is cooperative, so every piece
-                // the reducer waits for is running.
+                // A tile split between pieces pa..pb: pa, the piece holding its first units,
+                // reaches it last (at the end of its piece) and normally finds the partials of
+                // pa+1..pb published on the tile's ticket; it then adds them to its own in piece
+                // order.  Nobody waits for another CTA: a piece that finds the tile incomplete
+                // parks its partial too, and whichever piece arrives last (the ticket's
+                // acquire-release add returns pb - pa) sums the parked partials in the same
+                // order.  Each CTA has two slots: its first tile (shared with earlier pieces)
+                // and its last tile (reduced or parked).
                 const int64_t pa = dev_piece_of(tstart, SU, SP);
-                if (pa != c) {
-                    float4* part = reinterpret_cast<float4*>(p.ws + c * static_cast<int64_t>(kRows) * p.ws_cols);
-#pragma unroll 1
-                    for (int c0 = 0; c0 < MP; c0 += 16) {
-                        float acc[16];
-                        load_acc(c0, acc);
-#pragma unroll
-                        for (int f = 0; f < 4; ++f)
-                            part[(c0 / 4 + f) * kEpiThreads + etid] =
-                                make_float4(acc[4 * f], acc[4 * f + 1], acc[4 * f + 2], acc[4 * f + 3]);
-                    }
-                    release();
-                    // every warp's partial is written (the barrier); one release add publishes them
-                    named_bar_sync(kBarEpi, kEpiThreads);
-                    if (warp == kEpiWarp0 && lane == 0) red_add_release_gpu(M.tickets + tile, 1);
-                    continue;
-                }
                 const int64_t pb = dev_piece_of(tstart + KB - 1, SU, SP);
-                bool counted = true;
-                if (warp == kEpiWarp0 && lane == 0) counted = wait_count(M.tickets + tile, static_cast<int>(pb - pa), flags, lim);
-                // (the vote is also the barrier that orders every warp's loads after the acquire)
-                if (!bar_and(kBarEpi, kEpiThreads, counted)) {
-                    live = false;
-                    break;
-                }
-#pragma unroll 1
-                for (int c0 = 0; c0 < MP; c0 += 16) {
-                    float acc[16];
-                    load_acc(c0, acc);
+                const int need = static_cast<int>(pb - pa);
+                auto slot = [&](int64_t piece, int role) {
+                    return reinterpret_cast<float4*>(p.ws + (2 * piece + role) * static_cast<int64_t>(kRows) * p.ws_cols);
+                };
+                // the partials of pa+1..pb added, in piece order, to acc (columns c0 .. c0 + 15)
+                auto add_partials = [&](int c0, float (&acc)[16]) {
 #pragma unroll 1
                     for (int64_t pc = pa + 1; pc <= pb; ++pc) {
-                        const float4* src = reinterpret_cast<const float4*>(p.ws + pc * static_cast<int64_t>(kRows) * p.ws_cols);
+                        const float4* src = slot(pc, 0);
                         float4 pv[4];
 #pragma unroll
                         for (int f = 0; f < 4; ++f) pv[f] = __ldcg(src + (c0 / 4 + f) * kEpiThreads + etid);
@@ -804,10 +786,72 @@ __global__ void __launch_bounds__(kThreads, 1)
                             acc[4 * f + 3] += pv[f].w;
                         }
                     }
-                    emit(c0, acc);
+                };
+                bool direct = false;
+                if (pa == c) {
+                    // a short bounded poll (the other pieces normally published long ago; a
+                    // piece that is not running yet must not be waited for); the vote is also
+                    // the barrier that orders every warp's loads after the acquire
+                    bool all = false;
+                    if (warp == kEpiWarp0 && lane == 0 && !p.park_all) {
+                        const uint64_t t0 = globaltimer_ns();
+                        for (;;) {
+                            if (ld_acquire_gpu(M.tickets + tile) == need) {
+                                all = true;
+                                break;
+                            }
+                            if (globaltimer_ns() - t0 > kParkAfterNs) break;
+                            __nanosleep(64);
+                        }
+                    }
+                    direct = bar_or(kBarEpi, kEpiThreads, all);
+                }
+                if (direct) {
+#pragma unroll 1
+                    for (int c0 = 0; c0 < MP; c0 += 16) {
+                        float acc[16];
+                        load_acc(c0, acc);
+                        add_partials(c0, acc);
+                        emit(c0, acc);
+                    }
+                    release();
+                    // every partial is read: the ticket is ready for the next launch
+                    named_bar_sync(kBarEpi, kEpiThreads);
+                    if (warp == kEpiWarp0 && lane == 0) M.tickets[tile] = 0;
+                    continue;
+                }
+                float4* own = slot(c, pa == c ? 1 : 0);
+#pragma unroll 1
+                for (int c0 = 0; c0 < MP; c0 += 16) {
+                    float acc[16];
+                    load_acc(c0, acc);
+#pragma unroll
+                    for (int f = 0; f < 4; ++f)
+                        own[(c0 / 4 + f) * kEpiThreads + etid] =
+                            make_float4(acc[4 * f], acc[4 * f + 1], acc[4 * f + 2], acc[4 * f + 3]);
                 }
                 release();
-                // every partial is read: the ticket is ready for the next launch
+                // every warp's partial is written (the barrier); one acquire-release add
+                // publishes it and tells whether this CTA is the last to arrive
+                named_bar_sync(kBarEpi, kEpiThreads);
+                bool last = false;
+                if (warp == kEpiWarp0 && lane == 0) last = atom_add_acq_rel_gpu(M.tickets + tile, 1) == need;
+                if (!bar_or(kBarEpi, kEpiThreads, last)) continue;
+                const float4* first_part = slot(pa, 1);
+#pragma unroll 1
+                for (int c0 = 0; c0 < MP; c0 += 16) {
+                    float acc[16];
+#pragma unroll
+                    for (int f = 0; f < 4; ++f) {
+                        const float4 v = __ldcg(first_part + (c0 / 4 + f) * kEpiThreads + etid);
+                        acc[4 * f] = v.x;
+                        acc[4 * f + 1] = v.y;
+                        acc[4 * f + 2] = v.z;
+                        acc[4 * f + 3] = v.w;
+                    }
+                    add_partials(c0, acc);
+                    emit(c0, acc);
+                }
                 named_bar_sync(kBarEpi, kEpiThreads);
                 if (warp == kEpiWarp0 && lane == 0) M.tickets[tile] = 0;
             }

@@ -53,13 +53,16 @@ struct alignas(128) MatDesc {
 struct LaunchParams {
     const MatDesc* mats;       // device array of `count` matrices (count > 1 only)
     const int32_t* first_mat;// [grid]: matrix holding each piece's first unit (count > 1 only)
-    float* ws;               // split-K partials, one slot per CTA of 128 threads x ws_cols floats
+    float* ws;               // split-K partials: per CTA one (mma.sync) or two (tcgen05) slots of
+                             // 128 threads x ws_cols floats
     int* err;                // sticky error word (mapped host memory)
     int64_t units;           // units of all matrices of the launch
     int32_t count;           // matrices in this launch
     int32_t m;               // rows of this launch (1..16 mma.sync, 1..128 tcgen05)
     int32_t ws_cols;         // floats per consumer thread in a partial slot
     int32_t b1_frags;        // mma.sync: the matrices' fragments come from their frag records
+    int32_t park_all;        // tcgen05, testing: every split tile's reducer parks its partial
+                             // (the rare path of the split-K sum; same results)
     // Row-wise argmax instead of y (single-matrix launches only; null otherwise): the
     // launch folds (value, column) keys into amax_keys[m] (zero before and after a launch),
     // and the last of its writer warps, counted in amax_count (zero before and after),
@@ -86,6 +89,10 @@ struct LaunchParams {
 // Default wait limit of a launch, and the limit of the drains on a failure path.
 constexpr uint64_t kDefaultWaitNs = 4000000000ull;  // 4 s
 constexpr uint64_t kDrainLimitNs = 10000000000ull;  // 10 s
+// How long the tcgen05 kernel's split-tile reducer polls for the other pieces' partials before
+// it parks its own and leaves the sum to the last piece to arrive (a piece that has not
+// started cannot be waited for).
+constexpr uint64_t kParkAfterNs = 3000;  // 3 us
 
 // Argmax keys: the value's bits mapped to an unsigned order (larger value, larger key; -0
 // counts as +0) in the high half, the complement of the column in the low half, so that the
@@ -137,17 +144,19 @@ cudaError_t repack(const uint8_t* src_dev, uint8_t* dst_dev, const Decomp& d, in
 inline bool presum_for(int64_t m, int format) { return format == QMM_FORMAT_Q4_K && m > 64; }
 // Bytes of the activation sums of a launch of m rows of a matrix of kb super-block columns.
 inline int64_t presum_bytes(int64_t m, int64_t kb) { return kb * m * 16; }
-// Floats of the split-K partial slots of a launch of `grid` CTAs at tile width mp: one slot
-// per CTA (the partial of its piece's first row tile), 128 rows x mp columns.
-inline int64_t ws_floats(int64_t grid, int32_t mp) { return grid * kRows * mp; }
+// Floats of the split-K partial slots of a launch of `grid` CTAs at tile width mp: two slots
+// per CTA of 128 rows x mp columns (the partial of its piece's first row tile, and its last
+// row tile's partial when it must leave that tile's reduction to a later CTA).
+inline int64_t ws_floats(int64_t grid, int32_t mp) { return 2 * grid * kRows * mp; }
 // Fill a matrix descriptor for a run of m rows (1..128) of x against the handle's weights;
 // xs (presum_bytes(m, kb) bytes, 16-byte aligned) receives the activation sums of launches
 // with presum_for(m, format), and is null otherwise.
 cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, int* tickets, int64_t units,
                      int64_t n, int32_t kb, int32_t m, __half* xs);
 // Launch over `p.count` matrices of one format (`single` when count == 1) on `grid` CTAs;
-// p.ws_cols = mp_for(p.m).  A split tile's reducer waits for the partials of later CTAs, so
-// launches must be cooperative (all CTAs resident) whenever another kernel may hold SMs.
+// p.ws_cols = mp_for(p.m).  No CTA waits for another in the split-K reduction, so a launch
+// needs to be cooperative only where it waits across CTAs for another reason (the dependent
+// persistent step's completion counters).
 cudaError_t launch(const MatDesc& single, const LaunchParams& p, int grid, cudaStream_t s, bool pdl, bool cooperative,
                    int format);
 cudaError_t configure();
@@ -196,6 +205,7 @@ struct qmm_handle_s {
     float* ws = nullptr;          // split-K partials
     int32_t ws_cols = 0;
     int* tickets = nullptr;
+    int32_t park = 0;             // QMM_SPLITK_PARK set at create: launches set park_all
     int* err_host = nullptr;      // mapped pinned word: host view
     int* err_dev = nullptr;       // device view of the same word
     void* x_stage = nullptr;      // host_io staging

@@ -123,6 +123,11 @@ void qmm_default_options(qmm_options* opt);
  *          is an INVALID_ARG.
  *  opt:    NULL for defaults.
  *  stream: the repack is ordered on it; qmm_create synchronises it before returning.
+ * Testing: with QMM_SPLITK_PARK=1 in the environment at create, every run and step of the
+ * handle takes the rare path of the tcgen05 kernel's split-K sum on each row tile cut
+ * between CTAs (the tile's first CTA parks its partial and the last CTA to arrive adds them
+ * up), which otherwise happens only when a CTA starts late.  Results are the same bit for
+ * bit; launches are slower.  No effect on mma.sync handles.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, OOM, CUDA, NO_DEVICE.
  */
 qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
@@ -133,6 +138,10 @@ qmm_status qmm_create(qmm_handle* out, const void* blocks, int64_t n, int64_t k,
  * 16-byte aligned) times W^T.  M = 0 is a no-op returning QMM_OK.  1 <= M <= m_max.
  * Asynchronous: errors found on the device (a bounded wait timing out) are reported by a
  * later qmm_run or by qmm_get_error.
+ * Calls on one handle must be ordered (same stream, or synchronised): they share its split-K
+ * workspace.  Runs of different handles may overlap on the GPU (other streams, other
+ * kernels): a run never waits for a CTA that might not be resident (mma.sync launches are
+ * cooperative; in the tcgen05 kernel no CTA waits for another).
  * Errors: BAD_HANDLE, INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA, DEVICE_TIMEOUT.
  */
 qmm_status qmm_run(qmm_handle h, const void* x, int64_t m, float* y, void* stream);

@@ -110,13 +110,15 @@ def test_pieces_partition_units(units, grid):
 def test_split_tile_bookkeeping(mats, grid):
     """Both kernels' split-K bookkeeping, restated on the host: a launch of matrices (tiles, kb)
     cut into `grid` pieces.  A tile shared by pieces pa..pb is reduced by pa; each other piece
-    writes one partial into its CTA's single slot.  That slot suffices because a piece can
-    share, without reducing, only its first tile; the reducer pa reaches the tile at the end of
-    its piece (the tile is pa's last tile), after the pieces it waits for have started."""
+    writes one partial into its CTA's writer slot.  That slot suffices because a piece can
+    share, without reducing, only its first tile.  The reducer pa reaches the tile at the end
+    of its piece (the tile is pa's last tile), so each piece is pa for at most one shared tile
+    and one more slot holds a partial that pa parks when it must leave the sum to the last
+    CTA to arrive (tcgen05 kernel)."""
     units = sum(t * kb for t, kb in mats)
     grid = min(grid, units)
     start = [c * units // grid for c in range(grid + 1)]
-    partials = {}
+    partials, parked = {}, {}
     base = 0
     for tiles, kb in mats:
         for tile in range(tiles):
@@ -126,6 +128,8 @@ def test_split_tile_bookkeeping(mats, grid):
                 continue
             # the reducer's piece ends inside the tile: it is pa's last tile
             assert t0 < start[pa + 1] <= t1
+            assert pa not in parked, (pa, parked[pa], (base, tile))
+            parked[pa] = (base, tile)
             for c in range(pa + 1, pb + 1):
                 # each writer starts inside the tile: it is that piece's first tile
                 assert t0 < start[c] < t1

@@ -1,7 +1,8 @@
 """Runs of two different handles in flight at once on two streams (the way a server overlaps
-independent work).  No launch may wait for a CTA that cannot become resident: the tcgen05
-kernel's split-K reduction is taken by whichever piece of a row tile finishes last (no CTA
-waits for another), and the mma.sync kernel, whose reducer does wait for the other pieces,
+independent work).  No launch may wait for a CTA that cannot become resident: in the tcgen05
+kernel's split-K reduction no CTA waits for another (a row tile's first piece adds the other
+pieces' partials if they are all in, else the last piece to arrive does), and the mma.sync
+kernel, whose reducer does wait for the other pieces,
 is launched cooperatively (all its CTAs resident at once).  Twenty overlapped rounds must give
 no device-side timeout, results bit-identical to the same runs issued alone, and parity with
 the oracle."""
