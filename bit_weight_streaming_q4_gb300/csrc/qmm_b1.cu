@@ -37,9 +37,11 @@
 // MMA k-order.  For step s = 0..15 (i = s % 8, i' = (i + 2t) % 8, high = s >= 8) lane t fills
 // the MMA k slots {2t, 2t+1, 2t+8, 2t+9} with weight offsets 64t + 32*high + 4i' + {0, 1, 2, 3}
 // (repack swaps the middle bytes of each quant word to get this order), so that each pair of
-// slots is a pair of adjacent activations.  The min-term step uses slots (2t, 2t+1) for the
-// fp16 high parts of the sums of sub-blocks 2t and 2t+1 and (2t+8, 2t+9) for their low parts,
-// so that its A fragment is the lane's pair (m_2t, m_2t+1) in every register.
+// slots is a pair of adjacent activations.  The min-term step uses, with one n8 fragment,
+// slots (2t, 2t+1) for the fp16 high parts of the sums of sub-blocks 2t and 2t+1 and
+// (2t+8, 2t+9) for their low parts, so that its A fragment is the lane's pair
+// (m_2t, m_2t+1) in every register; with two, (2t, 2t+1) for the high and low part of
+// sub-block 2t and (2t+8, 2t+9) for those of 2t+1 (Cfg::kMinPairs).
 //
 // Warp roles (one persistent CTA per SM; 11 warps of up to 168 registers, or 20 of up to 96):
 //   warps 0..W-1 consumers, two or four per SM sub-partition (W = 8 of 32 rows for launches
@@ -87,6 +89,13 @@ struct Cfg {
     static constexpr int kWarps = NT == 1 ? 8 : 16;
     static constexpr int kRT = kRows / 16 / kWarps;            // m16 row tiles per consumer warp
     static constexpr int kConsumers = kWarps * 32;
+    // Min-term operands: with one n8 fragment the A fragment is the lane's scale-min pair
+    // (m_2t, m_2t+1) in every register, against B = the fp16 high parts of sub-blocks 2t, 2t+1,
+    // then their low parts; with two, A holds m_2t twice, then m_2t+1 twice, against B =
+    // (high, low) of sub-block 2t, then of 2t+1.  Same sums; each was measured the faster one
+    // for its width on GB300 (by 4 % at 1-8 rows and 2-3 % at 9-16; the difference is in
+    // the compiled schedule of 96-register consumer warps).
+    static constexpr bool kMinPairs = NT == 1;
     static_assert(kConsumers <= kConsumerThreads && kWarps * kRT * 16 == kRows, "row split");
     static constexpr int kProducerWarp = kWarps;               // weight units
     static constexpr int kFragWarp0 = kProducerWarp + 1;      // NT fragment warps (one per 8 tokens)
@@ -399,10 +408,15 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
             const float lim = 65504.f;
             const float cl = fminf(fmaxf(x_lo, -lim), lim), ch = fminf(fmaxf(x_hi, -lim), lim);
             const __half l_hi = __float2half_rn(cl), h_hi = __float2half_rn(ch);
+            const __half l_lo = __float2half_rn(cl - __half2float(l_hi)), h_lo = __float2half_rn(ch - __half2float(h_hi));
             uint2 mt;
-            mt.x = as_u32(__halves2half2(l_hi, h_hi));  // slots 2t, 2t+1: high parts
-            mt.y = as_u32(__halves2half2(__float2half_rn(cl - __half2float(l_hi)),
-                                         __float2half_rn(ch - __half2float(h_hi))));  // slots 2t+8, 2t+9: low parts
+            if constexpr (C::kMinPairs) {
+                mt.x = as_u32(__halves2half2(l_hi, h_hi));  // slots 2t, 2t+1: high parts
+                mt.y = as_u32(__halves2half2(l_lo, h_lo));  // slots 2t+8, 2t+9: low parts
+            } else {
+                mt.x = as_u32(__halves2half2(l_hi, l_lo));  // slots 2t, 2t+1: sub-block 2t
+                mt.y = as_u32(__halves2half2(h_hi, h_lo));  // slots 2t+8, 2t+9: sub-block 2t+1
+            }
             *reinterpret_cast<uint2*>(fst + C::kFragBytes + (nt * 32 + lane) * 8) = mt;
             __syncwarp();
             if (lane == 0) {
@@ -593,13 +607,19 @@ __global__ void __launch_bounds__(Cfg<NT>::kThreads, 1)
                 if (lane == 0) mbar_arrive(&fempty[fs]);
 #pragma unroll
                 for (int r = 0; r < kRT; ++r) {
-                    // A: (m_2t, m_2t+1) of row g (registers 0, 2) and row g+8 (1, 3)
-                    const uint32_t a0 = rk[r][0].m, a1 = rk[r][1].m;
+                    // A (rows g and g+8): the pairs (m_2t, m_2t+1) as they are, or each m twice
+                    uint32_t a0 = rk[r][0].m, a1 = rk[r][1].m, a2 = a0, a3 = a1;
+                    if constexpr (!C::kMinPairs) {
+                        a0 = as_u32(__low2half2(as_h2(rk[r][0].m)));
+                        a2 = as_u32(__high2half2(as_h2(rk[r][0].m)));
+                        a1 = as_u32(__low2half2(as_h2(rk[r][1].m)));
+                        a3 = as_u32(__high2half2(as_h2(rk[r][1].m)));
+                    }
                     const float2 dd0 = __half22float2(as_h2(rk[r][0].dd)), dd1 = __half22float2(as_h2(rk[r][1].dd));
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         float dm[4] = {0.f, 0.f, 0.f, 0.f};
-                        mma_m16n8k16(dm, a0, a1, a0, a1, xb[nt].x, xb[nt].y);
+                        mma_m16n8k16(dm, a0, a1, a2, a3, xb[nt].x, xb[nt].y);
                         acc[r][nt][0] = fmaf(dd0.x, dp[r][nt][0], acc[r][nt][0]);
                         acc[r][nt][1] = fmaf(dd0.x, dp[r][nt][1], acc[r][nt][1]);
                         acc[r][nt][2] = fmaf(dd1.x, dp[r][nt][2], acc[r][nt][2]);
@@ -884,9 +904,15 @@ __global__ void __launch_bounds__(32 * NT) frag_kernel(const __grid_constant__ M
     const float lim = 65504.f;
     const float cl = fminf(fmaxf(x_lo, -lim), lim), ch = fminf(fmaxf(x_hi, -lim), lim);
     const __half l_hi = __float2half_rn(cl), h_hi = __float2half_rn(ch);
+    const __half l_lo = __float2half_rn(cl - __half2float(l_hi)), h_lo = __float2half_rn(ch - __half2float(h_hi));
     uint2 mt;
-    mt.x = as_u32(__halves2half2(l_hi, h_hi));
-    mt.y = as_u32(__halves2half2(__float2half_rn(cl - __half2float(l_hi)), __float2half_rn(ch - __half2float(h_hi))));
+    if constexpr (C::kMinPairs) {
+        mt.x = as_u32(__halves2half2(l_hi, h_hi));
+        mt.y = as_u32(__halves2half2(l_lo, h_lo));
+    } else {
+        mt.x = as_u32(__halves2half2(l_hi, l_lo));
+        mt.y = as_u32(__halves2half2(h_hi, h_lo));
+    }
     *reinterpret_cast<uint2*>(fst + C::kFragBytes + (nt * 32 + lane) * 8) = mt;
 }
 
