@@ -34,16 +34,17 @@ if ROOT not in sys.path:
 import synth  # noqa: E402
 
 METRIC = "Q4K x M-row decode GEMM: weight GB/s (% of HBM peak) and step tok/s at M=1/12/64"
-# DRAM bytes per work unit of each backend's persistent step launch, measured by ncu
-# (profiles/stream_kernel_lm_head_m1.md, profiles/tc_kernel_step_m12.md); each is valid only for
-# the kernel source it was taken from
+# DRAM bytes per work unit of each backend's launch, measured by ncu
+# (profiles/stream_kernel_step_m12.md: the persistent mma.sync step at M = 12;
+# profiles/tc_kernel_lm_head_m64.md: a tcgen05 launch at M = 64); each is valid only for the
+# kernel source it was taken from
 TRAFFIC_PER_UNIT = {
     1: {"source": "bit_weight_streaming_q4_gb300/csrc/qmm_b1.cu",
-        "sha256": "8d28a050a994dd9106b4b8910343f214052ff97fd60f0c2f856f2a85a98513a5",
-        "bytes": 37208.9},
+        "sha256": "bae3eeda86c6491280b68b62aa4330743b6a37c5b6bf453dbf937272692a680a",
+        "bytes": 37278.3},
     2: {"source": "bit_weight_streaming_q4_gb300/csrc/qmm_b2.cu",
-        "sha256": "3f984e5678a61fc87b0b638fe98485b979dda78a02ab8d90c2d0f8d9ff4f03ed",
-        "bytes": 18581.7},
+        "sha256": "948e2d0dd60561a6cf1ca57ebac24742023dd41a99c0f8fd3ef2f4d4abee206f",
+        "bytes": 18799.3},
 }
 KERNEL_NAME = {1: "qmm::b1::stream_kernel<2>", 2: "qmm::b2::tc_kernel<16>"}
 HEADLINE_M = 12
@@ -761,13 +762,13 @@ def run_ours(args, rank, world, local_rank):
     def max_over_ranks(t):
         return ranks_max(t, world, "cuda")
 
-    def make_step(m, flags, xs=None, ys=None):
+    def make_step(m, flags, xs=None, ys=None, qs=None):
         with torch.cuda.stream(stream):
-            return Step(stack.handles(m), stack.x_ptrs() if xs is None else xs,
+            return Step(stack.handles(m) if qs is None else qs, stack.x_ptrs() if xs is None else xs,
                         stack.y_ptrs() if ys is None else ys, m, stream=stream.cuda_stream, flags=flags)
 
-    def measure(m, flags, steps, warmup):
-        step = make_step(m, flags)
+    def measure(m, flags, steps, warmup, qs=None):
+        step = make_step(m, flags, qs=qs)
         barrier()
         t = time_graph(torch, step, steps, warmup, stream)
         step.close()
@@ -898,11 +899,17 @@ def run_ours(args, rank, world, local_rank):
     steps_dep = max(20, args.steps // 2)
     td = measure(HEADLINE_M, 0, steps_dep, 3) / steps_dep
     dependent = {"weight_gbs": wb / td / 1e9, "tok_s": HEADLINE_M / td, "ms_per_step": td * 1e3,
-                 "runs": "dependent (CUDA graph)"}
-    # the same dependent step as one persistent launch (opt-in: slower than the graph here)
-    tdp = measure(HEADLINE_M, STEP_PERSISTENT, steps_dep, 3) / steps_dep
-    dependent["persistent"] = {"weight_gbs": wb / tdp / 1e9, "ms_per_step": tdp * 1e3,
-                               "runs": "dependent, one persistent launch (QMM_STEP_PERSISTENT)"}
+                 "runs": "dependent (CUDA graph)", "backend": head_backend}
+    if stack.qs_wide and int(stack.qs_wide[0].info().backend) == 2:
+        # the dependent step on tcgen05 handles (the wide set) at M = 12: as a graph, and as one
+        # persistent launch (QMM_STEP_PERSISTENT, which only the tcgen05 kernel supports)
+        tdg = measure(HEADLINE_M, 0, steps_dep, 3, qs=stack.qs_wide) / steps_dep
+        tdp = measure(HEADLINE_M, STEP_PERSISTENT, steps_dep, 3, qs=stack.qs_wide) / steps_dep
+        dependent["tcgen05"] = {
+            "graph": {"weight_gbs": wb / tdg / 1e9, "ms_per_step": tdg * 1e3},
+            "persistent": {"weight_gbs": wb / tdp / 1e9, "ms_per_step": tdp * 1e3,
+                           "runs": "dependent, one persistent launch (QMM_STEP_PERSISTENT)"},
+            "handles": f"m_max {max(EXTRA_M)} (tcgen05)"}
     if not args.no_extra:
         for m in EXTRA_M:
             steps_m = max(20, args.steps // (4 if m > 16 else 1))

@@ -66,12 +66,8 @@ constexpr int64_t kAutoMmaSyncMaxM = 16;
 
 // One run in launches of at most per_launch(h) rows.  With idx and val given, each launch
 // writes its rows' argmax column and value there instead of y (y is not touched).
-// tc_coop: launch the tcgen05 kernel cooperatively.  Its split-K sum never waits for another
-// CTA, so it needs no co-residency; but in a graph of runs linked by programmatic dependent
-// launch, cooperative launches (no overlap with the previous run) measured faster at 64 and
-// 128 rows on GB300 (4-5 %), while direct runs gain ~2 us each without the attribute.
 qmm_status launch_run(qmm_handle h, const void* x, int64_t m, float* y, cudaStream_t s, bool pdl,
-                      int32_t* idx = nullptr, float* val = nullptr, bool tc_coop = false) {
+                      int32_t* idx = nullptr, float* val = nullptr) {
     const int64_t K = h->d.k, N = h->d.n;
     const int64_t step = per_launch(h);
     for (int64_t r0 = 0; r0 < m; r0 += step) {
@@ -109,9 +105,10 @@ qmm_status launch_run(qmm_handle h, const void* x, int64_t m, float* y, cudaStre
             if (pre) e = qmm::b2::presum(mat, p, static_cast<int32_t>(h->d.kb), s);
             // the mma.sync kernel's split-K reducer waits for the partials of the CTAs after it,
             // so its CTAs must be co-resident (a cooperative launch); in the tcgen05 kernel no
-            // CTA waits for another
+            // CTA waits for another, and without the attribute a run overlaps the one before
+            // it (about 2 us per launch on GB300)
             if (e == cudaSuccess)
-                e = tc ? qmm::b2::launch(mat, p, h->d.grid, s, pdl, tc_coop, h->format)
+                e = tc ? qmm::b2::launch(mat, p, h->d.grid, s, pdl, false, h->format)
                        : qmm::b1::launch(mat, p, h->d.grid, s, pdl, true);
         }
         if (e != cudaSuccess) return QMM_ERR_CUDA;
@@ -549,7 +546,7 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
         if (rc == QMM_OK && cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
             rc = QMM_ERR_CUDA;
         for (int32_t i = 0; rc == QMM_OK && i < count; ++i)
-            rc = launch_run(handles[i], xs[i], m, ys[i], cap, /*pdl=*/i > 0, nullptr, nullptr, /*tc_coop=*/true);
+            rc = launch_run(handles[i], xs[i], m, ys[i], cap, /*pdl=*/i > 0);
         if (cap) {
             cudaGraph_t g = nullptr;
             cudaError_t ec = cudaStreamEndCapture(cap, &g);
