@@ -139,7 +139,18 @@ struct Cfg {
     static constexpr int kNumBars = 2 * kWRing + 2 * kXRing + 2 * kTB + 6 + (kSplit ? kTB : 0);
     // argmax launches: the epilogue warps' best keys, [warp 4][token MP]
     static constexpr int kAmaxOff = kBarOff + kNumBars * 8 + 16;
-    static constexpr int kSmem = kAmaxOff + 4 * MP * 8 + 1024;  // + alignment slack
+    // ... which y launches use instead, where shared memory has the room, as the epilogue
+    // warps' staging tiles, [warp 4][token 16][row 32] fp32: a warp writes 16 tokens of its 32
+    // rows there and stores them to y as 16-byte pieces of 4 rows, a quarter of the store
+    // instructions of one value per thread (those took ≈ 19 K clocks for a 128 x 128 tile
+    // while the weight stream ran, measured on GB300)
+    static constexpr int kStageBytes = 4 * 16 * 32 * 4;
+    static constexpr int kAmaxBytes = 4 * MP * 8;
+    static constexpr int kSmemPlain = kAmaxOff + kAmaxBytes + 1024;  // + alignment slack
+    static constexpr int kSmemStaged = kAmaxOff + (kAmaxBytes > kStageBytes ? kAmaxBytes : kStageBytes) + 1024;
+    // (not for Q6_K, whose epilogue warps run at 80 registers and would spill)
+    static constexpr bool kStage = kSmemStaged <= 232448 && F != QMM_FORMAT_Q6_K;
+    static constexpr int kSmem = kStage ? kSmemStaged : kSmemPlain;
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -341,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* tfull_lo = mmadone + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tfull_lo + (C::kSplit ? kTB : 0));
     unsigned long long* amax_sm = reinterpret_cast<unsigned long long*>(smem + C::kAmaxOff);
+    float* stage_sm = reinterpret_cast<float*>(smem + C::kAmaxOff);  // y launches only
     volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 1);  // [0] abort
 
     const int tid = threadIdx.x;
@@ -736,6 +748,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     if (bi == (m >> 5)) best[bi] = key > best[bi] ? key : best[bi];
                             }
                         }
+                    } else if (C::kStage && (M.n & 3) == 0) {
+                        // through the warp's staging tile: rows n0 + 4j .. + 3 of token c0 + t
+                        // (t = 4k + lane / 8, j = lane % 8) as one 16-byte store
+                        float* st = stage_sm + q * (16 * 32);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) st[i * 32 + lane] = acc[i];
+                        __syncwarp();
+                        const int j4 = 4 * (lane & 7);
+                        const int64_t n4 = tile * kRows + 32 * q + j4;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int t = 4 * k + (lane >> 3);
+                            const float4 v = *reinterpret_cast<const float4*>(st + t * 32 + j4);
+                            const int m = c0 + t;
+                            // N % 4 == 0: the 4 rows are all inside or all past N
+                            if (m < p.m && n4 < M.n)
+                                *reinterpret_cast<float4*>(M.y + static_cast<int64_t>(m) * M.n + n4) = v;
+                        }
+                        __syncwarp();  // the tile is read before the next chunk overwrites it
                     } else {
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
