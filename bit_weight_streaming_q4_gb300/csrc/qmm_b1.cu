@@ -859,6 +859,8 @@ cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, i
     out->xsrc = static_cast<const __half*>(x);
     out->xs = nullptr;
     out->frag = nullptr;
+    memset(&out->ymap, 0, sizeof(out->ymap));
+    out->ytma = 0;
     out->wq = wq;
     out->y = y;
     out->tickets = tickets;

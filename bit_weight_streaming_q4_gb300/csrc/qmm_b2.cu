@@ -138,12 +138,12 @@ struct Cfg {
     // wfull, wempty, xfull, xempty, tfull, tempty, accfull[2], accempty[2], mmadone[2], tfull_lo
     static constexpr int kNumBars = 2 * kWRing + 2 * kXRing + 2 * kTB + 6 + (kSplit ? kTB : 0);
     // argmax launches: the epilogue warps' best keys, [warp 4][token MP]
-    static constexpr int kAmaxOff = kBarOff + kNumBars * 8 + 16;
-    // ... which y launches use instead, where shared memory has the room, as the epilogue
-    // warps' staging tiles, [warp 4][token 16][row 32] fp32: a warp writes 16 tokens of its 32
-    // rows there and stores them to y as 16-byte pieces of 4 rows, a quarter of the store
-    // instructions of one value per thread (those took ≈ 19 K clocks for a 128 x 128 tile
-    // while the weight stream ran, measured on GB300)
+    static constexpr int kAmaxOff = (kBarOff + kNumBars * 8 + 16 + 127) / 128 * 128;  // 128-byte aligned (bulk stores)
+    // ... which y launches use instead, where shared memory has the room, as the epilogue's
+    // staging tile, [token 16][row 128] fp32: the four warps write 16 tokens of their rows
+    // there and one thread stores the tile to y with a bulk tensor store (one value per thread
+    // and store instruction took ≈ 19 K clocks for a 128 x 128 tile while the weight stream
+    // ran, measured on GB300)
     static constexpr int kStageBytes = 4 * 16 * 32 * 4;
     static constexpr int kAmaxBytes = 4 * MP * 8;
     static constexpr int kSmemPlain = kAmaxOff + kAmaxBytes + 1024;  // + alignment slack
@@ -677,8 +677,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto arrive_upto = [&](int upto) {
             if (!dep || arrived >= upto) return;
             named_bar_sync(kBarEpi, kEpiThreads);  // every warp's outputs are written
-            if (warp == kEpiWarp0 && lane == 0)
+            if (warp == kEpiWarp0 && lane == 0) {
+                // ... including the bulk tensor stores, which go through the async proxy
+                bulk_wait_all();
+                asm volatile("fence.proxy.async.global;" ::: "memory");
                 for (int t = arrived; t < upto; ++t) red_add_release_gpu(p.done + t, 1);
+            }
             arrived = upto;
         };
         Cursor mk;
@@ -748,25 +752,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     if (bi == (m >> 5)) best[bi] = key > best[bi] ? key : best[bi];
                             }
                         }
-                    } else if (C::kStage && (M.n & 3) == 0) {
-                        // through the warp's staging tile: rows n0 + 4j .. + 3 of token c0 + t
-                        // (t = 4k + lane / 8, j = lane % 8) as one 16-byte store
-                        float* st = stage_sm + q * (16 * 32);
+                    } else if (C::kStage && M.ytma) {
+                        // the chunk goes through the staging tile [token 16][row 128] to one
+                        // bulk tensor store (the tensor map clips rows past N and tokens past M)
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) st[i * 32 + lane] = acc[i];
-                        __syncwarp();
-                        const int j4 = 4 * (lane & 7);
-                        const int64_t n4 = tile * kRows + 32 * q + j4;
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const int t = 4 * k + (lane >> 3);
-                            const float4 v = *reinterpret_cast<const float4*>(st + t * 32 + j4);
-                            const int m = c0 + t;
-                            // N % 4 == 0: the 4 rows are all inside or all past N
-                            if (m < p.m && n4 < M.n)
-                                *reinterpret_cast<float4*>(M.y + static_cast<int64_t>(m) * M.n + n4) = v;
+                        for (int i = 0; i < 16; ++i) stage_sm[i * kRows + row] = acc[i];
+                        fence_proxy_async_smem();  // the tile's generic writes, before the bulk read
+                        named_bar_sync(kBarEpi, kEpiThreads);
+                        if (warp == kEpiWarp0 && lane == 0) {
+                            tma_store_2d(&M.ymap, stage_sm, static_cast<int32_t>(tile * kRows), c0);
+                            bulk_commit_group();
+                            bulk_wait_read_all();  // the tile may be written again
                         }
-                        __syncwarp();  // the tile is read before the next chunk overwrites it
+                        named_bar_sync(kBarEpi, kEpiThreads);
                     } else {
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
@@ -913,6 +911,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int t = 0; t <= count; ++t) p.done[t] = 0;
         }
         if (!live && lane == 0) fail(p.err, flags);
+        if (warp == kEpiWarp0 && lane == 0) bulk_wait_all();  // y's bulk stores have completed
         named_bar_sync(kBarTeardown, kTmemUsers);
         return;
     }
@@ -1265,6 +1264,22 @@ cudaError_t make_mat(MatDesc* out, const uint8_t* wq, const void* x, float* y, i
             return cudaErrorInvalidValue;
     } else {
         memset(&out->smap, 0, sizeof(out->smap));
+    }
+    // y [m, n] fp32 for the epilogue's bulk stores: 16 tokens x 128 rows per store (rows
+    // past n and tokens past m are not written); the row stride must be a multiple of 16
+    // bytes
+    memset(&out->ymap, 0, sizeof(out->ymap));
+    out->ytma = 0;
+    if (y && (n & 3) == 0 && (reinterpret_cast<uintptr_t>(y) & 15) == 0) {
+        const cuuint64_t ydim[2] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(m)};
+        const cuuint64_t ystride[1] = {static_cast<cuuint64_t>(n) * 4};
+        const cuuint32_t ybox[2] = {static_cast<cuuint32_t>(kRows), 16};
+        const cuuint32_t yestr[2] = {1, 1};
+        if (enc(&out->ymap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, y, ydim, ystride, ybox, yestr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        out->ytma = 1;
     }
     out->wq = wq;
     out->y = y;

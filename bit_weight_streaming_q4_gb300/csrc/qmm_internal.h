@@ -36,6 +36,7 @@ inline int64_t piece_of(int64_t u, int64_t units, int64_t grid) {
 struct alignas(128) MatDesc {
     CUtensorMap xmap;      // activations [m, k] fp16, 128-byte swizzle: box 64 x 8 (mma.sync) or 64 x MP (tcgen05)
     CUtensorMap smap;      // tcgen05 Q4_K launches of MP = 128: the activation sums [kb][m][8] fp16, box 8 x 128 x 1
+    CUtensorMap ymap;      // tcgen05 y launches with N % 4 == 0: y [m, n] fp32, box 128 x 16 (bulk stores)
     const __half* xsrc;    // ... the activations they are formed from ([m, k], row stride k)
     __half* xs;            // ... and where the pre-pass writes them
     uint8_t* frag;         // mma.sync steps: the matrix's MMA B fragments, one record per super-block
@@ -48,6 +49,8 @@ struct alignas(128) MatDesc {
     int64_t n;
     int32_t kb;
     int32_t pieces;        // dependent steps: pieces the matrix is cut into (its handle's grid)
+    int32_t ytma;          // ymap is set: the epilogue may write y with bulk tensor stores
+    int32_t pad[3];
 };
 
 struct LaunchParams {
