@@ -43,8 +43,8 @@ TRAFFIC_PER_UNIT = {
         "sha256": "bae3eeda86c6491280b68b62aa4330743b6a37c5b6bf453dbf937272692a680a",
         "bytes": 37278.3},
     2: {"source": "bit_weight_streaming_q4_gb300/csrc/qmm_b2.cu",
-        "sha256": "948e2d0dd60561a6cf1ca57ebac24742023dd41a99c0f8fd3ef2f4d4abee206f",
-        "bytes": 18799.3},
+        "sha256": "eca0d17beb65bd96ad19829f1275703a238bed26ed1df6a8e83e5d1e83c7852c",
+        "bytes": 18801.5},
 }
 KERNEL_NAME = {1: "qmm::b1::stream_kernel<2>", 2: "qmm::b2::tc_kernel<16>"}
 HEADLINE_M = 12
