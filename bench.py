@@ -40,8 +40,8 @@ METRIC = "Q4K x M-row decode GEMM: weight GB/s (% of HBM peak) and step tok/s at
 # kernel source it was taken from
 TRAFFIC_PER_UNIT = {
     1: {"source": "bit_weight_streaming_q4_gb300/csrc/qmm_b1.cu",
-        "sha256": "bae3eeda86c6491280b68b62aa4330743b6a37c5b6bf453dbf937272692a680a",
-        "bytes": 37278.3},
+        "sha256": "a44227027e9ff57bf6103abe0de8b75fe722a45bb0c243cfd7e945ad0f9933f5",
+        "bytes": 37262.0},
     2: {"source": "bit_weight_streaming_q4_gb300/csrc/qmm_b2.cu",
         "sha256": "eca0d17beb65bd96ad19829f1275703a238bed26ed1df6a8e83e5d1e83c7852c",
         "bytes": 18801.5},
