@@ -186,6 +186,9 @@ __global__ void __launch_bounds__(kThreads, 4) attn_partial(const Params p) {
             mbar_arrive(b);  // completes the phase without data; the abort flag stops its use
             return;
         }
+        // (a refill: every warp's generic reads of the slot, ordered by the CTA barrier before
+        // this, precede the bulk write)
+        if (i >= kStages) fence_proxy_async_smem();
         mbar_arrive_expect_tx(b, kRec);
         bulk_g2s(sm + (i % kStages) * kRec, src, kRec, b, l2_policy_evict_first());
     };

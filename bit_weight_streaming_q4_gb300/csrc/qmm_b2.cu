@@ -474,6 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
+                // the dequantisation warps' generic reads of the slot, before this bulk write
+                if (wseq >= kWRing) fence_proxy_async_smem();
                 if (w.i != cur) {
                     cur = w.i;
                     src = mat(w.i).wq + w.j * kUnitBytes;
@@ -513,6 +515,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
+                // the dequantisation warps' generic reads of the slot (the activation sums at
+                // MP <= 64), before this bulk write
+                if (issued >= kXRing) fence_proxy_async_smem();
                 if (xc.i != cur) {
                     const MatDesc& M = mat(xc.i);
                     cur = xc.i;
