@@ -43,8 +43,8 @@ TRAFFIC_PER_UNIT = {
         "sha256": "a44227027e9ff57bf6103abe0de8b75fe722a45bb0c243cfd7e945ad0f9933f5",
         "bytes": 37262.0},
     2: {"source": "bit_weight_streaming_q4_gb300/csrc/qmm_b2.cu",
-        "sha256": "eca0d17beb65bd96ad19829f1275703a238bed26ed1df6a8e83e5d1e83c7852c",
-        "bytes": 18801.5},
+        "sha256": "8293ef0cab229e6bb6adca8f48745f550dd78e9897daa68e8b1cb56de9e94397",
+        "bytes": 18799.1},
 }
 KERNEL_NAME = {1: "qmm::b1::stream_kernel<2>", 2: "qmm::b2::tc_kernel<16>"}
 HEADLINE_M = 12
