@@ -822,10 +822,8 @@ def run_ours(args, rank, world, local_rank):
                          [yd[o:].data_ptr() for o in yo])
 
     def e2e_once():
-        with torch.cuda.stream(stream):
-            xd.copy_(x_pin, non_blocking=True)
-            e2e_step.launch(stream.cuda_stream)
-            y_pin.copy_(yd, non_blocking=True)
+        # the C-ABI host-buffer call: copy in, run, copy out, all on one stream
+        e2e_step.launch_host(x_pin, y_pin, stream.cuda_stream)
 
     for _ in range(3):
         e2e_once()
@@ -847,34 +845,21 @@ def run_ours(args, rank, world, local_rank):
                    for mat, a, b in zip(stack.mats, yo, stack.y_off))
 
     e2e_ok = matches(y_pin.numpy())
-    # (2) pipelined, as a server streams steps: two sets of device buffers; step i's inputs are
-    # copied in (copy stream) while step i - 1 runs, and its outputs copied out (a second copy
-    # stream) while step i + 1 runs.  Timed from the first input copy to the last output copy.
+    # (2) pipelined, as a server streams steps: two sets of device buffers (two steps), called
+    # alternately through the same C-ABI call on one stream, with the copies in and out on
+    # two more streams: step i's inputs are copied in while step i - 1 runs, and its outputs
+    # copied out while step i + 1 runs.  Timed from the first input copy to the last output copy.
     xds = [xd, torch.empty(offx, dtype=torch.float16, device="cuda")]
     yds = [yd, torch.empty(offy, dtype=torch.float32, device="cuda")]
     ypins = [y_pin, torch.empty(offy, dtype=torch.float32).pin_memory()]
     steps2 = [make_step(HEADLINE_M, STEP_INDEPENDENT, [xds[b][o:].data_ptr() for o in xo],
                         [yds[b][o:].data_ptr() for o in yo]) for b in (0, 1)]
     h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
-    ev = {k: [torch.cuda.Event() for _ in (0, 1)] for k in ("in", "run", "out")}
 
     def pipelined(n):
         for i in range(n):
             b = i % 2
-            if i >= 2:
-                h2d.wait_event(ev["run"][b])   # step i - 2 has read xds[b]
-            with torch.cuda.stream(h2d):
-                xds[b].copy_(x_pin, non_blocking=True)
-                ev["in"][b].record(h2d)
-            stream.wait_event(ev["in"][b])
-            if i >= 2:
-                stream.wait_event(ev["out"][b])  # step i - 2's outputs have left yds[b]
-            steps2[b].launch(stream.cuda_stream)
-            ev["run"][b].record(stream)
-            d2h.wait_event(ev["run"][b])
-            with torch.cuda.stream(d2h):
-                ypins[b].copy_(yds[b], non_blocking=True)
-                ev["out"][b].record(d2h)
+            steps2[b].launch_host(x_pin, ypins[b], stream.cuda_stream, h2d.cuda_stream, d2h.cuda_stream)
 
     pipelined(3)
     torch.cuda.synchronize()
@@ -979,12 +964,13 @@ def run_ours(args, rank, world, local_rank):
                 "h2d_bytes_per_step": xb, "d2h_bytes_per_step": yb,
                 "ms_per_step": te / e2e_steps * 1e3, "outputs_match_device_run": e2e_ok,
                 "steps": e2e_steps,
-                "how": "public API (Step.launch) with every step's activations copied in from pinned "
-                       "host memory and its outputs copied back, inside the timed region; copies of "
-                       "adjacent steps overlap the running step (two device buffer sets, two copy streams)",
+                "how": "C-ABI host-buffer call qmm_step_launch_host: every step's activations copied in "
+                       "from pinned host memory and its outputs copied back, inside the timed region; "
+                       "two steps over two device buffer sets called alternately, with the copies on two "
+                       "more streams, so the copies of adjacent steps overlap the running step",
                 "serialised": {"value": wb * e2e_steps / te_serial / 1e9,
                                "ms_per_step": te_serial / e2e_steps * 1e3,
-                               "how": "copy in, launch, copy out, one after the other on one stream"}},
+                               "how": "qmm_step_launch_host with copy in, launch and copy out on one stream"}},
         # a persistent mma.sync step is two launches (the activation-fragment pre-pass, then the
         # stream); a tcgen05 step at M <= 64 is one
         "gpu_launches": args.steps * (2 if head_backend == 1 else 1),

@@ -351,7 +351,34 @@ qmm_status qmm_destroy(qmm_handle h) {
 }  // extern "C"
 
 // ------------------------------------------------------------------------- decode step
+// One host<->device copy of a step's host-buffer launch: `bytes` at device address `dev` and
+// at byte offset `off` of the caller's host slab.
+struct HostSeg {
+    uint8_t* dev;
+    size_t off;
+    size_t bytes;
+};
+
+// Appends [dev, dev + bytes) at host offset off, merged into the previous copy when both
+// ranges continue it.
+static void add_seg(std::vector<HostSeg>& v, const void* dev, size_t off, size_t bytes) {
+    uint8_t* d = static_cast<uint8_t*>(const_cast<void*>(dev));
+    if (!v.empty() && v.back().dev + v.back().bytes == d && v.back().off + v.back().bytes == off)
+        v.back().bytes += bytes;
+    else
+        v.push_back({d, off, bytes});
+}
+
 struct qmm_step_s {
+    // qmm_step_launch_host: the copies in (x_i) and out (y_i), in matrix order, and the slabs' sizes
+    std::vector<HostSeg> xin, yout;
+    size_t x_bytes = 0, y_bytes = 0;
+    // ... and, for copies on the caller's other streams: the last kernel's completion (which a
+    // copy-out waits for, and the next copy-in, since it rewrites the x_i), the copy-in's (which
+    // the kernel waits for) and the copy-out's (which the step's next kernel waits for, since it
+    // rewrites the y_i)
+    cudaEvent_t kernel_done = nullptr, in_done = nullptr, out_done = nullptr;
+    bool out_pending = false;
     cudaGraph_t graph = nullptr;  // launch-per-run path (tcgen05 handles, or more than 16 rows)
     cudaGraphExec_t exec = nullptr;
     // persistent path: every matrix in one launch (cooperative for the mma.sync kernel)
@@ -385,6 +412,9 @@ static void free_step(qmm_step st) {
     cudaFree(st->cta_units);
     cudaFree(st->frag);
     if (st->err_host) cudaFreeHost(st->err_host);
+    if (st->kernel_done) cudaEventDestroy(st->kernel_done);
+    if (st->in_done) cudaEventDestroy(st->in_done);
+    if (st->out_done) cudaEventDestroy(st->out_done);
     delete st;
 }
 
@@ -561,6 +591,20 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
         return rc;
     }
     (void)stream;
+    if (cudaEventCreateWithFlags(&st->kernel_done, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&st->in_done, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&st->out_done, cudaEventDisableTiming) != cudaSuccess) {
+        free_step(st);
+        return QMM_ERR_CUDA;
+    }
+    for (int32_t i = 0; i < count; ++i) {
+        const size_t xb = static_cast<size_t>(m) * handles[i]->d.k * 2;
+        const size_t yb = static_cast<size_t>(m) * handles[i]->d.n * 4;
+        add_seg(st->xin, xs[i], st->x_bytes, xb);
+        add_seg(st->yout, ys[i], st->y_bytes, yb);
+        st->x_bytes += xb;
+        st->y_bytes += yb;
+    }
     {
         std::lock_guard<std::mutex> lk(g_mu);
         g_steps.insert(st);
@@ -569,12 +613,10 @@ qmm_status qmm_step_create(qmm_step* out, int32_t count, const qmm_handle* handl
     return QMM_OK;
 }
 
-qmm_status qmm_step_launch(qmm_step s, void* stream) {
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        if (!s || !g_steps.count(s)) return QMM_ERR_BAD_HANDLE;
-    }
+static qmm_status step_launch(qmm_step s, void* stream) {
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    // a host-buffer launch may still be copying the y_i out on another stream
+    if (s->out_pending && cudaStreamWaitEvent(cs, s->out_done, 0) != cudaSuccess) return QMM_ERR_CUDA;
     if (s->mats) {
         if (*reinterpret_cast<volatile int*>(s->err_host)) return QMM_ERR_DEVICE_TIMEOUT;
         // (a one-matrix step's kernel takes the descriptor by value)
@@ -587,6 +629,52 @@ qmm_status qmm_step_launch(qmm_step s, void* stream) {
         return e == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
     }
     return cudaGraphLaunch(s->exec, cs) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
+}
+
+qmm_status qmm_step_launch(qmm_step s, void* stream) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!s || !g_steps.count(s)) return QMM_ERR_BAD_HANDLE;
+    }
+    const qmm_status st = step_launch(s, stream);
+    if (st != QMM_OK) return st;
+    // a later host-buffer launch may copy its x_i in on another stream: after this kernel
+    return cudaEventRecord(s->kernel_done, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? QMM_OK
+                                                                                               : QMM_ERR_CUDA;
+}
+
+qmm_status qmm_step_launch_host(qmm_step s, const void* x_host, float* y_host, void* stream,
+                                void* in_stream, void* out_stream) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (!s || !g_steps.count(s)) return QMM_ERR_BAD_HANDLE;
+    }
+    if (!x_host || !y_host) return QMM_ERR_INVALID_ARG;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    cudaStream_t is = reinterpret_cast<cudaStream_t>(in_stream);
+    cudaStream_t os = reinterpret_cast<cudaStream_t>(out_stream);
+    const bool split_in = in_stream != nullptr && is != cs;
+    const bool split_out = out_stream != nullptr && os != cs;
+    const uint8_t* xh = static_cast<const uint8_t*>(x_host);
+    uint8_t* yh = reinterpret_cast<uint8_t*>(y_host);
+    // copy-in: on in_stream once the step's last kernel has read the x_i, then the kernel waits
+    if (split_in && cudaStreamWaitEvent(is, s->kernel_done, 0) != cudaSuccess) return QMM_ERR_CUDA;
+    for (const HostSeg& g : s->xin)
+        if (cudaMemcpyAsync(g.dev, xh + g.off, g.bytes, cudaMemcpyHostToDevice, split_in ? is : cs) != cudaSuccess)
+            return QMM_ERR_CUDA;
+    if (split_in && (cudaEventRecord(s->in_done, is) != cudaSuccess || cudaStreamWaitEvent(cs, s->in_done, 0) != cudaSuccess))
+        return QMM_ERR_CUDA;
+    const qmm_status st = step_launch(s, stream);
+    if (st != QMM_OK) return st;
+    if (cudaEventRecord(s->kernel_done, cs) != cudaSuccess) return QMM_ERR_CUDA;
+    // copy-out: on out_stream after the kernel; the step's next kernel waits for it
+    if (split_out && cudaStreamWaitEvent(os, s->kernel_done, 0) != cudaSuccess) return QMM_ERR_CUDA;
+    for (const HostSeg& g : s->yout)
+        if (cudaMemcpyAsync(yh + g.off, g.dev, g.bytes, cudaMemcpyDeviceToHost, split_out ? os : cs) != cudaSuccess)
+            return QMM_ERR_CUDA;
+    if (split_out && cudaEventRecord(s->out_done, os) != cudaSuccess) return QMM_ERR_CUDA;
+    s->out_pending = split_out;
+    return QMM_OK;
 }
 
 qmm_status qmm_step_destroy(qmm_step s) {

@@ -86,6 +86,7 @@ def load(path: str = LIB_PATH):
         "qmm_step_create": (ctypes.c_int, [ctypes.POINTER(vp), i32, ctypes.POINTER(vp),
                                            ctypes.POINTER(vp), ctypes.POINTER(vp), i64, ctypes.c_uint32, vp]),
         "qmm_step_launch": (ctypes.c_int, [vp, vp]),
+        "qmm_step_launch_host": (ctypes.c_int, [vp, vp, vp, vp, vp, vp]),
         "qmm_step_destroy": (ctypes.c_int, [vp]),
         "qmm_run_noalloc": (ctypes.c_int, [vp, i64, i64, vp, i64, vp, vp]),
         "qmm_attn_workspace_bytes": (ctypes.c_int, [ctypes.POINTER(AttnDims), i64, ctypes.POINTER(i64)]),
@@ -224,6 +225,15 @@ class Step:
     def launch(self, stream: int | None = None) -> None:
         st = current_stream() if stream is None else stream
         _check(load().qmm_step_launch(self._s, st), "qmm_step_launch")
+
+    def launch_host(self, x_host, y_host, stream: int | None = None, in_stream: int | None = None,
+                    out_stream: int | None = None) -> None:
+        """Copy every x_i in from x_host (one slab, step order), run, copy every y_i out to
+        y_host (qmm_step_launch_host): y_host is complete once `out_stream` (if given, else
+        `stream`) is synchronised."""
+        st = current_stream() if stream is None else stream
+        _check(load().qmm_step_launch_host(self._s, _ptr(x_host), _ptr(y_host), st, in_stream or 0,
+                                           out_stream or 0), "qmm_step_launch_host")
 
     def close(self) -> None:
         if self._s and self._s.value:

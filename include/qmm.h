@@ -302,6 +302,38 @@ qmm_status qmm_step_launch(qmm_step s, void* stream);
 qmm_status qmm_step_destroy(qmm_step s);
 
 /*
+ * A step with its activations and outputs in host memory (the end-to-end form of "How
+ * parallel decoding works": one step's rows in, every matrix's products out).
+ *  x_host: every matrix's activations, matrix after matrix in the step's order, each
+ *          x_i [M, K_i] fp16 row-major (sum over i of M*K_i*2 bytes), read only.
+ *  y_host: receives every output, y_i [M, N_i] fp32 row-major in the same order (sum of
+ *          M*N_i*4 bytes).
+ * Copies x_host into the step's device x_i, replays the step on `stream`, and copies the y_i
+ * back to y_host.
+ *  in_stream:  NULL (or `stream`): the copy-in is ordered on `stream` before the kernel.
+ *              Otherwise it runs on in_stream once the step's last kernel has finished
+ *              reading the x_i, and the kernel waits for it (the call orders both with
+ *              events).
+ *  out_stream: NULL (or `stream`): the copy-out is ordered on `stream` after the kernel, and
+ *              y_host is complete once `stream` has been synchronised.  Otherwise it runs on
+ *              out_stream after the kernel, y_host is complete once out_stream has been
+ *              synchronised, and the step's next launch (host-buffer or not) waits for it
+ *              before it rewrites the y_i.
+ * So two steps over two sets of device buffers, called alternately on one `stream` with
+ * their copies on two other streams, overlap one step's copies with the other's kernel.
+ * Calls on one step must be ordered on `stream`.  Device ranges that continue one another
+ * (buffers laid out as one slab in step order) move as one copy.  The host buffers should be
+ * page-locked (cudaHostAlloc / cudaHostRegister), or the copies are not asynchronous.
+ * Where an x_i is also written by a run of the step (a dependent step whose x_i aliases an
+ * earlier y_j), it receives the copied bytes first and that run's output after, as in
+ * qmm_step_launch.  Ownership: the caller keeps the host buffers and the streams; nothing is
+ * allocated.
+ * Errors: BAD_HANDLE, INVALID_ARG (a null buffer), CUDA, and those of qmm_step_launch.
+ */
+qmm_status qmm_step_launch_host(qmm_step s, const void* x_host, float* y_host, void* stream,
+                                void* in_stream, void* out_stream);
+
+/*
  * A run that allocates nothing (no counterpart on the pages: it exists for callers that
  * cannot call cudaMalloc where they need the matmul -- a framework whose memory pool owns the
  * device, code that must not synchronise the device, a plugin with a fixed memory budget).

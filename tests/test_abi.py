@@ -21,7 +21,7 @@ def test_header_declares_expected_api():
     names = Q.header_functions()
     assert names == sorted(["qmm_default_options", "qmm_create", "qmm_run", "qmm_run_host",
                             "qmm_get_error", "qmm_get_info", "qmm_destroy", "qmm_status_str",
-                            "qmm_step_create", "qmm_step_launch", "qmm_step_destroy",
+                            "qmm_step_create", "qmm_step_launch", "qmm_step_launch_host", "qmm_step_destroy",
                             "qmm_run_noalloc", "qmm_run_argmax", "qmm_attn_workspace_bytes",
                             "qmm_attn_decode"])
 

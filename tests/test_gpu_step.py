@@ -298,3 +298,101 @@ def test_tcgen05_dependent_step_sustained_launches(m):
             assert np.array_equal(a.view(np.uint32), y.cpu().numpy().view(np.uint32)), (rep, mat.name)
     assert all(q.error() == 0 for q in qs)
     step.close()
+
+
+@pytest.mark.parametrize("layout", ["slab", "separate"])
+@pytest.mark.parametrize("flags", [1, 0], ids=["independent", "dependent"])
+def test_step_launch_host_matches_device_launch(backend, flags, layout):
+    """qmm_step_launch_host: the activations from one host slab in step order, the outputs
+    back to one host slab; bit-identical to the device launch with the caller's own copies,
+    whether the device buffers form one slab (one copy each way) or are separate."""
+    from bit_weight_streaming_q4_gb300 import Step
+    torch = torch_cuda()
+    m = 12
+    blocks = [synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id) for mat in MATS]
+    xh = [synth.x_f16(m, mat.k, seed=0, tensor_id=1000 + mat.tensor_id) for mat in MATS]
+    qs = [make(b, m_max=m, backend=backend) for b in blocks]
+    xsz = [m * mat.k for mat in MATS]
+    ysz = [m * mat.n for mat in MATS]
+    if layout == "slab":
+        xd = torch.empty(sum(xsz), dtype=torch.float16, device="cuda")
+        yd = torch.empty(sum(ysz), dtype=torch.float32, device="cuda")
+        xs = [xd[a:a + n] for a, n in zip(np.cumsum([0] + xsz[:-1]), xsz)]
+        ys = [yd[a:a + n] for a, n in zip(np.cumsum([0] + ysz[:-1]), ysz)]
+    else:
+        xs = [torch.empty(n, dtype=torch.float16, device="cuda") for n in xsz]
+        ys = [torch.empty(n, dtype=torch.float32, device="cuda") for n in ysz]
+    x_pin = torch.from_numpy(np.concatenate([x.reshape(-1) for x in xh]).view(np.int16)).view(torch.float16).pin_memory()
+    y_pin = torch.full((sum(ysz),), float("nan"), dtype=torch.float32).pin_memory()
+    step = Step(qs, xs, ys, m, flags=flags)
+    # the device form: the caller's copies, then the launch
+    for x, a in zip(xs, xh):
+        x.copy_(torch.from_numpy(a.reshape(-1).view(np.int16)).view(torch.float16))
+    step.launch()
+    torch.cuda.synchronize()
+    want = [y.cpu().numpy().copy() for y in ys]
+    for y in ys:
+        y.fill_(float("nan"))
+    for x in xs:
+        x.zero_()
+    torch.cuda.synchronize()
+    cin, out = torch.cuda.Stream(), torch.cuda.Stream()
+    for split in (False, True, True, False):
+        y_pin.fill_(float("nan"))
+        step.launch_host(x_pin, y_pin, in_stream=cin.cuda_stream if split else None,
+                         out_stream=out.cuda_stream if split else None)
+        (out if split else torch.cuda.current_stream()).synchronize()
+        got = y_pin.numpy()
+        off = 0
+        for w, n in zip(want, ysz):
+            assert np.array_equal(got[off:off + n].view(np.uint32), w.view(np.uint32))
+            off += n
+    torch.cuda.synchronize()
+    off = 0
+    for b, x, mat, n in zip(blocks, xh, MATS, ysz):
+        y_ref, s_ref = oracle.qmm(b, x)
+        assert_parity(y_pin.numpy()[off:off + n].reshape(m, mat.n), y_ref, s_ref, mat.name)
+        off += n
+    step.close()
+
+
+def test_two_host_steps_overlap_copies_and_stay_exact():
+    """Two steps over two sets of device buffers, launched alternately on one stream with
+    their copies in and out on two others: every call's host outputs equal the device
+    launch's, bit for bit (a step's copy-in waits for its last kernel, and its next kernel
+    for its last copy-out)."""
+    from bit_weight_streaming_q4_gb300 import Step
+    torch = torch_cuda()
+    m = 12
+    blocks = [synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id) for mat in MATS]
+    qs = [make(b, m_max=m, backend=1) for b in blocks]
+    xsz = [m * mat.k for mat in MATS]
+    ysz = [m * mat.n for mat in MATS]
+    xs2 = [[torch.empty(n, dtype=torch.float16, device="cuda") for n in xsz] for _ in range(2)]
+    ys2 = [[torch.empty(n, dtype=torch.float32, device="cuda") for n in ysz] for _ in range(2)]
+    steps = [Step(qs, xs2[b], ys2[b], m, flags=1) for b in range(2)]
+    inputs = []
+    for it in range(4):   # a different x slab per call, so that a stale copy would show
+        xh = [synth.x_f16(m, mat.k, seed=it, tensor_id=1000 + mat.tensor_id) for mat in MATS]
+        inputs.append(torch.from_numpy(np.concatenate([x.reshape(-1) for x in xh]).view(np.int16))
+                      .view(torch.float16).pin_memory())
+    # expected: each input through the device launch of step 0
+    want = []
+    for xp in inputs:
+        off = 0
+        for x, n in zip(xs2[0], xsz):
+            x.copy_(xp[off:off + n])
+            off += n
+        steps[0].launch()
+        torch.cuda.synchronize()
+        want.append(np.concatenate([y.cpu().numpy() for y in ys2[0]]))
+    outs = [torch.full((sum(ysz),), float("nan"), dtype=torch.float32).pin_memory() for _ in inputs]
+    cin, out = torch.cuda.Stream(), torch.cuda.Stream()
+    for it, (xp, yp) in enumerate(zip(inputs, outs)):
+        steps[it % 2].launch_host(xp, yp, in_stream=cin.cuda_stream, out_stream=out.cuda_stream)
+    out.synchronize()
+    torch.cuda.synchronize()
+    for w, yp in zip(want, outs):
+        assert np.array_equal(yp.numpy().view(np.uint32), w.view(np.uint32))
+    for st in steps:
+        st.close()
