@@ -71,6 +71,8 @@ def test_argument_errors_need_no_device(lib):
     assert lib.qmm_destroy(ctypes.c_void_p(0x1000)) == 7
     assert lib.qmm_get_error(None) == 7
     assert lib.qmm_step_launch(None, None) == 7
+    assert lib.qmm_step_launch_host(None, buf, buf, None, None, None) == 7
+    assert lib.qmm_step_launch_host(ctypes.c_void_p(0x1000), buf, buf, None, None, None) == 7
     assert lib.qmm_run_argmax(None, buf, 1, buf, buf, None) == 7
     assert lib.qmm_run_argmax(ctypes.c_void_p(0x1000), buf, 1, buf, buf, None) == 7
     assert lib.qmm_step_destroy(None) == 7
