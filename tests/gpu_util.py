@@ -48,6 +48,14 @@ def assert_parity(y: np.ndarray, y_ref: np.ndarray, s_ref: np.ndarray, what: str
     bad = err > bound
     if bad.any():
         i = np.unravel_index(np.argmax(err / bound), err.shape)
+        where = ""
+        if bad.ndim == 2:
+            # which activation rows (tokens) and output columns, to tell a row tile, a lane
+            # group or a chunk of tokens apart
+            toks = np.where(bad.any(axis=1))[0]
+            cols = np.where(bad.any(axis=0))[0]
+            where = (f"; tokens {toks.min()}..{toks.max()} ({toks.size}), output columns "
+                     f"{cols.min()}..{cols.max()} ({cols.size}): {cols[:48].tolist()}")
         raise AssertionError(f"{what}: {bad.sum()} of {bad.size} elements out of tolerance; "
-                             f"worst at {i}: got {y[i]!r}, want {y_ref[i]!r}, bound {bound[i]!r}")
+                             f"worst at {i}: got {y[i]!r}, want {y_ref[i]!r}, bound {bound[i]!r}{where}")
     return float((err / bound).max()) if err.size else 0.0
