@@ -639,8 +639,13 @@ qmm_status qmm_step_launch(qmm_step s, void* stream) {
     const qmm_status st = step_launch(s, stream);
     if (st != QMM_OK) return st;
     // a later host-buffer launch may copy its x_i in on another stream: after this kernel
-    return cudaEventRecord(s->kernel_done, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? QMM_OK
-                                                                                               : QMM_ERR_CUDA;
+    // (not while the stream is being captured into a graph, where the event would belong to
+    // the capture; the caller then orders the graph's launches with the copies)
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(cs, &cap) != cudaSuccess) return QMM_ERR_CUDA;
+    if (cap != cudaStreamCaptureStatusNone) return QMM_OK;
+    return cudaEventRecord(s->kernel_done, cs) == cudaSuccess ? QMM_OK : QMM_ERR_CUDA;
 }
 
 qmm_status qmm_step_launch_host(qmm_step s, const void* x_host, float* y_host, void* stream,

@@ -313,7 +313,8 @@ qmm_status qmm_step_destroy(qmm_step s);
  *  in_stream:  NULL (or `stream`): the copy-in is ordered on `stream` before the kernel.
  *              Otherwise it runs on in_stream once the step's last kernel has finished
  *              reading the x_i, and the kernel waits for it (the call orders both with
- *              events).
+ *              events; a launch of the step captured into a CUDA graph is not tracked, so
+ *              order that graph's launches with the copy-in yourself).
  *  out_stream: NULL (or `stream`): the copy-out is ordered on `stream` after the kernel, and
  *              y_host is complete once `stream` has been synchronised.  Otherwise it runs on
  *              out_stream after the kernel, y_host is complete once out_stream has been
