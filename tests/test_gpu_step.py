@@ -396,3 +396,30 @@ def test_two_host_steps_overlap_copies_and_stay_exact():
         assert np.array_equal(yp.numpy().view(np.uint32), w.view(np.uint32))
     for st in steps:
         st.close()
+
+
+def test_host_step_with_aliased_activations_reads_the_run_output():
+    """A dependent step whose x_2 is the bytes of y_1, launched from host buffers: x_2's copied
+    bytes (fp16 ones) are replaced by run 1's output (exact zeros) before run 2 reads them, as
+    the host-buffer call documents, so y_2 = 0."""
+    from bit_weight_streaming_q4_gb300 import Step
+    torch = torch_cuda()
+    m, n1, k1 = 8, 2560, 4096
+    k2, n2 = 2 * n1, 1024
+    b1 = synth.q4k_matrix(n1, k1, seed=1, tensor_id=50)
+    b2 = synth.q4k_matrix(n2, k2, seed=1, tensor_id=51)
+    q1, q2 = make(b1, m_max=m, backend=1), make(b2, m_max=m, backend=1)
+    x1 = torch.empty((m, k1), dtype=torch.float16, device="cuda")
+    y1 = torch.empty((m, n1), dtype=torch.float32, device="cuda")
+    x2 = y1.view(torch.float16)
+    y2 = torch.empty((m, n2), dtype=torch.float32, device="cuda")
+    step = Step([q1, q2], [x1, x2], [y1, y2], m)
+    x_host = torch.cat([torch.zeros(m * k1, dtype=torch.float16),
+                        torch.ones(m * k2, dtype=torch.float16)]).pin_memory()
+    y_host = torch.full((m * (n1 + n2),), float("nan"), dtype=torch.float32).pin_memory()
+    for _ in range(3):
+        step.launch_host(x_host, y_host)
+        torch.cuda.synchronize()
+        assert np.all(y_host.numpy() == 0.0)
+        y_host.fill_(float("nan"))
+    step.close()
