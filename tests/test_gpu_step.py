@@ -300,15 +300,17 @@ def test_tcgen05_dependent_step_sustained_launches(m):
     step.close()
 
 
+@pytest.mark.parametrize("m", [12, 64])
 @pytest.mark.parametrize("layout", ["slab", "separate"])
 @pytest.mark.parametrize("flags", [1, 0], ids=["independent", "dependent"])
-def test_step_launch_host_matches_device_launch(backend, flags, layout):
+def test_step_launch_host_matches_device_launch(backend, flags, layout, m):
     """qmm_step_launch_host: the activations from one host slab in step order, the outputs
     back to one host slab; bit-identical to the device launch with the caller's own copies,
     whether the device buffers form one slab (one copy each way) or are separate."""
     from bit_weight_streaming_q4_gb300 import Step
     torch = torch_cuda()
-    m = 12
+    if backend == 1 and m > 16:
+        pytest.skip("mma.sync handles take at most 16 rows")
     blocks = [synth.q4k_matrix(mat.n, mat.k, seed=0, tensor_id=mat.tensor_id) for mat in MATS]
     xh = [synth.x_f16(m, mat.k, seed=0, tensor_id=1000 + mat.tensor_id) for mat in MATS]
     qs = [make(b, m_max=m, backend=backend) for b in blocks]
