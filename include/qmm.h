@@ -267,9 +267,9 @@ const char* qmm_status_str(qmm_status s);
  *                                full 64-layer stack at M = 12 it is the fastest dependent
  *                                step (5.07-5.10 ms, against 5.30-5.32 for the graph of the
  *                                same handles and 5.37-5.40 for a graph of MMA_SYNC runs); at
- *                                M = 64 it
- *                                is about even with the graph.  It is opt-in because the
- *                                launch is cooperative and holds every SM for the whole step.
+ *                                M = 64 it is about even with the graph.  It is opt-in
+ *                                because the launch is cooperative and holds every SM for the
+ *                                whole step.
  *  flags = QMM_STEP_INDEPENDENT: the caller guarantees that no x_i is written by a run of
  *                                the step.  When every handle has the same backend and block
  *                                format and M fits one launch (M <= 16 for MMA_SYNC handles,
